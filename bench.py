@@ -1,0 +1,317 @@
+"""Benchmark of the PagedAttention hot path on one GB300 (or N replicas).
+
+One step = one pass of the whole path over the Llama-3-70B-shaped decode
+batch (256 sequences, 64 query / 8 KV heads, head_dim 128, 32-token blocks,
+bf16, log-normal context lengths, split-KV partitions of 512 tokens):
+write the 256 new tokens' K/V into their slots (pa_reshape_and_cache), then
+paged decode over every sequence (pa_decode).  The metric is decode KV
+bandwidth: algorithmic K+V bytes read per step / step time, plus decode
+tokens/s per layer.
+
+Prints one JSON line.  ``--impl reference`` times the fp64 CPU oracle instead
+(bounded samples of the same workload on the host cores).
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "paged-attn decode KV GB/s and tokens/s/layer on 1 GB300; % of HBM roofline"
+UNIT = "GB/s"
+WORKLOAD = "Llama-3-70B-shaped decode layer"
+
+
+def _peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    return 6800.0, "fallback"
+
+
+def _config(b, extra=None):
+    cfg = {"workload": WORKLOAD, "num_seqs": b.num_seqs, "num_q_heads": b.num_q_heads,
+           "num_kv_heads": b.num_kv_heads, "head_dim": b.head_dim, "block_size": b.block_size,
+           "kv_dtype": b.kv_dtype, "partition_size": b.partition_size or 512,
+           "context_tokens": int(b.seq_lens.astype(np.int64).sum()), "max_seq_len": b.max_seq_len,
+           "lengths": "log-normal, median 1000, sigma 1.0, cap 8192 (seeded)",
+           "l2": "inputs larger than L2 (KV read per step >> 129 MB L2)"}
+    if extra:
+        cfg.update(extra)
+    return cfg
+
+
+class ClockSampler:
+    """nvidia-smi samples of SM clock and throttle reasons during the timed region."""
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+        self.lines = []
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.index), "--query-gpu=" + self.Q,
+                                          "--format=csv,noheader,nounits", "-lms", "200"],
+                                         stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.thread = threading.Thread(target=self._read, daemon=True)
+            self.thread.start()
+        except OSError:
+            self.proc = None
+        time.sleep(0.3)
+        return self
+
+    def _read(self):
+        for ln in self.proc.stdout:
+            self.lines.append(ln.strip())
+
+    def __exit__(self, *a):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self):
+        sm, mx, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            f = [x.strip() for x in ln.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                mx = float(f[2])
+            except ValueError:
+                continue
+            for n, v in zip(names, f[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": mx,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def _dist():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+def _time_oracle(b, kp, vp, ids) -> float:
+    import oracle
+    t0 = time.perf_counter()
+    oracle.decode_batch(b, kp, vp, seq_ids=ids)
+    return time.perf_counter() - t0
+
+
+def _sample_ids(b, budget_bytes, rng):
+    """Random sequences whose KV bytes add up to about ``budget_bytes``."""
+    per = b.seq_lens.astype(np.int64) * 2 * b.num_kv_heads * b.head_dim * b.kv_elem_bytes
+    ids, tot = [], 0
+    for i in rng.permutation(b.num_seqs):
+        ids.append(int(i))
+        tot += int(per[i])
+        if tot >= budget_bytes:
+            break
+    return np.array(sorted(ids), dtype=np.int32), tot
+
+
+def cpu_oracle_rate(b, seconds: float = 15.0):
+    """The oracle as it stands, on the host cores, over a bounded sample."""
+    import oracle
+    import workloads as W
+    kp, vp = W.empty_pools(b)
+    oracle.populate(b, kp, vp)
+    rng = np.random.default_rng(0)
+    ids, nbytes = _sample_ids(b, 8 << 20, rng)          # calibrate on ~8 MB of KV
+    t = _time_oracle(b, kp, vp, ids)
+    target = max(1 << 20, int(nbytes * seconds / max(t, 1e-3)))
+    ids, nbytes = _sample_ids(b, target, rng)
+    t = _time_oracle(b, kp, vp, ids)
+    return {"value": nbytes / t / 1e9, "unit": UNIT, "cores": oracle.max_threads(), "kind": "oracle",
+            "sample": f"{len(ids)} of {b.num_seqs} sequences ({nbytes / 1e6:.0f} MB of KV), fp64 C, OpenMP, "
+                      f"{t:.1f} s"}
+
+
+def run_reference(args):
+    """--impl reference: the oracle timed per step on bounded samples."""
+    import oracle
+    import workloads as W
+    ws, rank, _ = _dist()
+    if rank != 0:
+        return
+    b = W.cfg_llama70b()
+    kp, vp = W.empty_pools(b)
+    oracle.populate(b, kp, vp)
+    rng = np.random.default_rng(1)
+    budget = 6 << 20
+    for _ in range(args.warmup):
+        ids, _ = _sample_ids(b, budget, rng)
+        _time_oracle(b, kp, vp, ids)
+    tot_b, tot_t, tot_seq = 0, 0.0, 0
+    for _ in range(args.steps):
+        ids, nb = _sample_ids(b, budget, rng)
+        tot_t += _time_oracle(b, kp, vp, ids)
+        tot_b += nb
+        tot_seq += len(ids)
+    value = tot_b / tot_t / 1e9
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": tot_t / args.steps * 1e3,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic (seeded N(0,1) K/V/q, seeded block tables)",
+            "config": _config(b, {"sample_per_step": f"~{budget >> 20} MB of KV (random sequences)"}),
+            "cpu_baseline": {"value": value, "unit": UNIT, "cores": oracle.max_threads(), "kind": "oracle",
+                             "sample": f"{tot_seq} sequences over {args.steps} steps, ~{budget >> 20} MB KV each"},
+            "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line))
+
+
+def run_ours(args):
+    import torch
+    import workloads as W
+    from paged_kv_cache_writes_gb300 import build_lib
+    build_lib.build()
+    import paged_kv_cache_writes_gb300 as pa
+    from paged_kv_cache_writes_gb300.staging import DeviceBatch
+
+    ws, rank, local = _dist()
+    if ws > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl" if torch.cuda.is_available() else "gloo")
+    torch.cuda.set_device(local)
+    dev_name = f"cuda:{local}"
+
+    b = W.cfg_llama70b()
+    db = DeviceBatch(b, dev_name)
+    db.run_setup()
+    torch.cuda.synchronize()
+    stream = torch.cuda.current_stream()
+
+    kv_bytes = b.decode_kv_bytes()
+    # algorithmic bytes of one pa_decode launch: K+V once per KV head, q in, out, tables, lengths
+    eb_q = 2
+    dec_bytes = (kv_bytes + 2 * b.num_seqs * b.num_q_heads * b.head_dim * eb_q +
+                 int(np.ceil(b.seq_lens / b.block_size).sum()) * 4 + b.num_seqs * 4)
+
+    for _ in range(args.warmup):
+        db.step_all()
+    torch.cuda.synchronize()
+
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    if ws > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    with ClockSampler(local) as clocks:
+        start.record(stream)
+        for i in range(args.steps):
+            db.write_step()
+            ev[i][0].record(stream)
+            db.decode()
+            ev[i][1].record(stream)
+        end.record(stream)
+        torch.cuda.synchronize()
+    if ws > 1:
+        torch.distributed.barrier()
+    ms = start.elapsed_time(end) / args.steps
+    dec_ms = statistics.mean(a.elapsed_time(z) for a, z in ev)
+    assert pa.pa_get_device_error() == 0
+    if ws > 1:
+        t = torch.tensor([ms], device=dev_name)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        ms = float(t.item())
+
+    # end to end through the public API with host buffers (pinned), copies inside the timed region
+    host = {k: v.cpu().pin_memory() for k, v in (("q", db.q), ("bt", db.block_tables), ("sl", db.seq_lens),
+                                                 ("k", db.step[0]), ("v", db.step[1]), ("s", db.step[2]))}
+    out_h = torch.empty(db.out.shape, dtype=db.out.dtype, pin_memory=True)
+    h2d = sum(t.numel() * t.element_size() for t in host.values())
+    d2h = out_h.numel() * out_h.element_size()
+
+    def e2e_step():
+        db.q.copy_(host["q"], non_blocking=True)
+        db.block_tables.copy_(host["bt"], non_blocking=True)
+        db.seq_lens.copy_(host["sl"], non_blocking=True)
+        db.step[0].copy_(host["k"], non_blocking=True)
+        db.step[1].copy_(host["v"], non_blocking=True)
+        db.step[2].copy_(host["s"], non_blocking=True)
+        db.step_all()
+        out_h.copy_(db.out, non_blocking=True)
+
+    for _ in range(args.warmup):
+        e2e_step()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(args.steps):
+        e2e_step()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = e0.elapsed_time(e1) / args.steps
+    if ws > 1:
+        t = torch.tensor([e2e_ms], device=dev_name)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        e2e_ms = float(t.item())
+
+    if rank != 0:
+        if ws > 1:
+            torch.distributed.destroy_process_group()
+        return
+    peak, peak_kind = _peaks()
+    achieved = dec_bytes / (dec_ms * 1e-3) / 1e9
+    value = kv_bytes * ws / (ms * 1e-3) / 1e9
+    line = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": ws, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": ms, "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic (seeded N(0,1) K/V/q rounded to bf16, seeded shuffled block tables)",
+        "config": _config(b, {"parallelism": f"replicas x{ws}" if ws > 1 else "single GPU"}),
+        "tokens_per_s_per_layer": b.num_seqs * ws / (ms * 1e-3),
+        "decode_ms": dec_ms,
+        "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
+                     "traffic": None, "kernel": "paged_attention_kernel (pa_decode)",
+                     "peak_source": f"{peak_kind} hbm_gbs"},
+        "e2e": {"value": kv_bytes * ws / (e2e_ms * 1e-3) / 1e9, "unit": UNIT, "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms},
+        "gpu_launches": 2 * args.steps,
+        "clocks": clocks.summary(),
+    }
+    if not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_oracle_rate(b, args.cpu_seconds)
+    print(json.dumps(line))
+    if ws > 1:
+        torch.distributed.destroy_process_group()
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=15.0)
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+    (run_reference if args.impl == "reference" else run_ours)(args)
+
+
+if __name__ == "__main__":
+    main()

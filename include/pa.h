@@ -1,0 +1,226 @@
+/*
+ * pa.h -- C ABI of libpa, a PagedAttention hot path for NVIDIA GB300 (sm_103a).
+ *
+ * The operations follow the problem statement of these pages:
+ *   [V07]  "Inside vLLM v0.7: How PagedAttention & Chunked Prefill Scaled 10x
+ *          Token Serving" (bicarait.com)
+ *   [ARCH] "Inside vLLM Architecture: How PagedAttention and Continuous
+ *          Batching Solved the KV Cache Crisis" (codebumble.net)
+ *   [HT]   "High-Throughput LLM Serving with vLLM & PagedAttention: Production
+ *          Architecture & Optimization" (infoisland)
+ *
+ * Data model.  The KV cache of one attention layer is two pools, K and V, each
+ * laid out [num_blocks][num_kv_heads][block_size][head_dim] in the element
+ * type of the cache.  A sequence's token at position p lives in physical block
+ * block_table[p / block_size] at offset p % block_size ([V07] "Architectural
+ * Blueprint 2: How PagedAttention Actually Works"; [ARCH] "The Block Table
+ * Mapping Subsystem").  Each (block, head) row group is one contiguous run of
+ * block_size * head_dim elements.  A "slot" is block * block_size + offset.
+ *
+ * Conventions for every call:
+ *  - Every pointer argument is DEVICE memory owned by the caller, except the
+ *    pa_kv_cache descriptor, which is read on the host during the call.  The
+ *    library allocates no memory and keeps no state between calls other than a
+ *    per-device error word (see pa_get_device_error).
+ *  - Calls are asynchronous: they validate arguments on the host, enqueue
+ *    kernels on `stream` and return.  No call synchronises, except
+ *    pa_get_device_error.  NULL stream = the legacy default stream.
+ *  - Device pointers must be 16-byte aligned; q, out and the K/V inputs are
+ *    contiguous [tokens or sequences][heads][head_dim] unless a stride is given.
+ *  - Supported: head_dim 64 or 128; block_size 16 or 32; cache dtype f16,
+ *    bf16 or fp8-e4m3; query dtype f16 or bf16 (equal to the cache dtype
+ *    unless the cache is fp8).  Other combinations return PA_ERR_UNSUPPORTED.
+ *  - Zero work (num_tokens, num_seqs, num_chunks or num_pairs == 0) returns
+ *    PA_OK without launching anything.
+ *  - Device-resident metadata (block ids, slots, sequence lengths) is the
+ *    caller's contract.  The kernels check it as they read it: an out-of-range
+ *    value is recorded in the device error word and the offending work is
+ *    skipped; nothing traps.
+ *  - A failed launch returns PA_ERR_CUDA.
+ */
+#ifndef PA_H
+#define PA_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Entry points stay visible when the library is built with hidden visibility. */
+#if defined(__GNUC__)
+#define PA_API __attribute__((visibility("default")))
+#else
+#define PA_API
+#endif
+
+/* Same type as the CUDA runtime's cudaStream_t, declared without CUDA headers. */
+struct CUstream_st;
+typedef struct CUstream_st *pa_stream_t;
+
+typedef enum {
+    PA_OK = 0,
+    PA_ERR_INVALID_ARG = 1,  /* null/misaligned pointer, negative count, bad shape */
+    PA_ERR_UNSUPPORTED = 2,  /* head_dim / block_size / dtype combination not built */
+    PA_ERR_CUDA = 3,         /* a CUDA runtime call or kernel launch failed */
+    PA_ERR_DEVICE_CHECK = 4, /* a kernel found out-of-range device metadata */
+    PA_ERR_TIMEOUT = 5       /* a kernel's bounded wait on an async copy expired */
+} pa_status;
+
+typedef enum { PA_F16 = 0, PA_BF16 = 1, PA_FP8_E4M3 = 2 } pa_dtype;
+
+/* Shape and element type of one layer's K and V pools. */
+typedef struct {
+    int64_t num_blocks;   /* physical blocks in each pool */
+    int32_t block_size;   /* tokens per block: 16 or 32 */
+    int32_t num_kv_heads;
+    int32_t head_dim;     /* 64 or 128 */
+    pa_dtype kv_dtype;    /* PA_F16, PA_BF16 or PA_FP8_E4M3 */
+    /* fp8 only: one fp32 scale per pool; a stored code c means c * scale.
+     * Ignored for f16/bf16 pools.  Must be finite and > 0 for fp8. */
+    float k_scale;
+    float v_scale;
+} pa_kv_cache;
+
+/*
+ * pa_reshape_and_cache -- scatter new tokens' K and V into their cache slots.
+ *
+ * Defined by the slot arithmetic of PagedKVCacheManager.allocate_slot ([ARCH]
+ * "The Block Table Mapping Subsystem"): for every token t with
+ * s = slot_mapping[t] >= 0 and every KV head h,
+ *     k_cache[s / block_size][h][s % block_size][:] = k[t][h][:]   (same for v).
+ * A negative slot marks a padding token and is skipped.
+ *
+ *   k, v          device, dtype in_dtype (PA_F16 or PA_BF16); token t, head h,
+ *                 element e at index t * token_stride + h * head_dim + e
+ *   token_stride  elements between consecutive tokens (>= num_kv_heads*head_dim,
+ *                 a multiple of 8), so k and v may be views into a fused QKV
+ *   slot_mapping  device int64 [num_tokens]
+ *   k_cache, v_cache  device pools described by *cache
+ * An f16/bf16 pool must have kv_dtype == in_dtype and receives the bits
+ * unchanged.  An fp8 pool receives e4m3(fp32(x) / scale): IEEE fp32 division,
+ * then round to nearest even with saturation to +-448 ([HT] "4. Production
+ * vLLM Docker Deployment with FP8 Quantization", --kv-cache-dtype fp8; the
+ * format and the per-tensor scale are this library's reading).
+ * Slots >= num_blocks * block_size set PA_ERR_DEVICE_CHECK in the error word.
+ * Two tokens mapping to the same slot race (the result is one of them).
+ */
+PA_API pa_status pa_reshape_and_cache(const void *k, const void *v, pa_dtype in_dtype,
+                               int32_t num_tokens, int64_t token_stride,
+                               const int64_t *slot_mapping, void *k_cache,
+                               void *v_cache, const pa_kv_cache *cache,
+                               pa_stream_t stream);
+
+/*
+ * pa_copy_blocks -- copy-on-write of shared blocks ([HT] "2. Virtual Memory
+ * Paging Applied to GPUs: PagedAttention": when branches that share prompt
+ * blocks diverge, a new block is allocated for the writer).
+ *
+ * For each pair i, the whole physical block src = pairs[2i] (every head, slot
+ * and element) of both pools is copied bit for bit to dst = pairs[2i+1].
+ *   src_dst_pairs  device int32 [num_pairs][2]
+ * Destinations must be distinct and must not appear as a source in the same
+ * call (pairs run in parallel).  Ids outside [0, num_blocks) set
+ * PA_ERR_DEVICE_CHECK and that pair is skipped.
+ */
+PA_API pa_status pa_copy_blocks(void *k_cache, void *v_cache, const pa_kv_cache *cache,
+                         const int32_t *src_dst_pairs, int32_t num_pairs,
+                         pa_stream_t stream);
+
+/*
+ * pa_decode_workspace_bytes -- device workspace pa_decode needs for split-KV.
+ *
+ * partition_size 0 selects the library default (512 tokens).  Returns 0 when
+ * no sequence can span more than one partition (max_seq_len <= partition
+ * size); then pa_decode accepts a NULL workspace.  Returns 0 as well for
+ * invalid arguments, which pa_decode then reports.
+ */
+PA_API size_t pa_decode_workspace_bytes(int32_t num_seqs, int32_t num_q_heads,
+                                 int32_t num_kv_heads, int32_t head_dim,
+                                 int32_t max_seq_len, int32_t partition_size);
+
+/*
+ * pa_decode -- paged attention for one query token per sequence (the decode
+ * step; [V07] "Architectural Blueprint 3: Chunked Prefill", decode phase;
+ * [ARCH] "Architectural Anatomy" pipeline: the kernel gathers the
+ * non-contiguous K/V blocks while computing Q K^T).
+ *
+ * For sequence i with L = seq_lens[i] tokens (including the token being
+ * decoded, whose K/V must already be in the cache) and query head h, reading
+ * KV head g = h / (num_q_heads / num_kv_heads):
+ *     out[i][h] = sum_p softmax_p(scale * q[i][h] . K_i[p][g]) * V_i[p][g]
+ * over p = 0 .. L-1, where K_i[p] is the row at slot p % block_size of block
+ * block_tables[i][p / block_size].  Exact attention ([ARCH] "Semantic FAQ
+ * Section": paging does not change the result); fp32 accumulation.  L == 0
+ * yields a zero row.  For an fp8 cache, K and V elements are code * scale.
+ *
+ *   q              device [num_seqs][num_q_heads][head_dim], dtype q_dtype
+ *   block_tables   device int32 [num_seqs][max_blocks_per_seq]
+ *   seq_lens       device int32 [num_seqs], each <= max_seq_len and
+ *                  <= max_blocks_per_seq * block_size
+ *   max_seq_len    host upper bound of seq_lens; sizes the grid
+ *   partition_size 0 = default (512); else a multiple of 32 tokens.  A
+ *                  sequence longer than one partition is split across CTAs
+ *                  and the pieces are merged with a log-sum-exp combine.
+ *   workspace      device, >= pa_decode_workspace_bytes(...) bytes, 256-byte
+ *                  aligned, ZERO-FILLED before its first use; every call that
+ *                  completes leaves it zero-filled again, so it can be reused
+ *                  by later calls on the same stream (concurrent calls need
+ *                  separate workspaces).
+ *   out            device [num_seqs][num_q_heads][head_dim], dtype q_dtype
+ */
+PA_API pa_status pa_decode(const void *q, pa_dtype q_dtype, int32_t num_seqs,
+                    int32_t num_q_heads, const void *k_cache,
+                    const void *v_cache, const pa_kv_cache *cache,
+                    const int32_t *block_tables, int32_t max_blocks_per_seq,
+                    const int32_t *seq_lens, int32_t max_seq_len, float scale,
+                    int32_t partition_size, void *workspace,
+                    size_t workspace_bytes, void *out, pa_stream_t stream);
+
+/*
+ * pa_prefill_chunk -- causal attention of prompt chunks over paged context
+ * ([V07] "Architectural Blueprint 3: Chunked Prefill"; [HT] "5. Chunked
+ * Prefill & Latency SLA Management": a long prompt is processed in chunks,
+ * e.g. 512 tokens, batched with decodes).
+ *
+ * Chunk c owns query rows cu_q_lens[c] .. cu_q_lens[c+1]-1.  Row r of chunk c
+ * sits at absolute position q_start[c] + r of sequence c and attends to
+ * positions 0 .. q_start[c] + r inclusive, read through block_tables[c]:
+ *     out[row][h] = sum_p softmax_p(scale * q[row][h] . K_c[p][g]) * V_c[p][g].
+ * The chunk's own K/V must already be in the cache (pa_reshape_and_cache), so
+ * seq_lens[c] must equal q_start[c] + (cu_q_lens[c+1] - cu_q_lens[c]).
+ *
+ *   q_chunk    device [total_q][num_q_heads][head_dim], total_q = cu_q_lens[num_chunks]
+ *   cu_q_lens  device int32 [num_chunks + 1], non-decreasing, cu_q_lens[0] = 0
+ *   q_start    device int32 [num_chunks]
+ *   max_q_len  host upper bound of any chunk length; sizes the grid
+ *   max_seq_len host upper bound of seq_lens
+ *   out        device [total_q][num_q_heads][head_dim], dtype q_dtype
+ */
+PA_API pa_status pa_prefill_chunk(const void *q_chunk, pa_dtype q_dtype,
+                           const int32_t *cu_q_lens, const int32_t *q_start,
+                           int32_t num_chunks, int32_t max_q_len,
+                           int32_t num_q_heads, const void *k_cache,
+                           const void *v_cache, const pa_kv_cache *cache,
+                           const int32_t *block_tables,
+                           int32_t max_blocks_per_seq, const int32_t *seq_lens,
+                           int32_t max_seq_len, float scale, void *out,
+                           pa_stream_t stream);
+
+/*
+ * pa_get_device_error -- read and clear the current device's error word.
+ * Synchronises `stream`, then stores into *code the first device-side status
+ * recorded since the last clear (PA_OK if none): PA_ERR_DEVICE_CHECK for
+ * out-of-range metadata, PA_ERR_TIMEOUT for an expired wait.
+ */
+PA_API pa_status pa_get_device_error(pa_stream_t stream, int32_t *code);
+
+/* Static, human-readable name of a status code. */
+PA_API const char *pa_status_string(pa_status status);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* PA_H */

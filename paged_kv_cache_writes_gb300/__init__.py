@@ -1,0 +1,178 @@
+"""Python binding of libpa, a PagedAttention hot path for GB300 (sm_103a).
+
+Thin marshalling over the C ABI declared in ``include/pa.h``: every function
+here has the name of its C entry point, takes PyTorch CUDA tensors (used only
+as device memory), passes their data pointers and the current CUDA stream, and
+raises ``PaError`` on a non-OK status.  All arithmetic runs in the library's
+CUDA kernels.  There is no CPU fallback: if ``libpa.so`` has not been built,
+importing the binding works but every call raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+import torch
+
+__all__ = [
+    "PA_F16", "PA_BF16", "PA_FP8_E4M3", "PaError", "PaKvCache", "lib", "kv_cache_desc",
+    "pa_reshape_and_cache", "pa_copy_blocks", "pa_decode_workspace_bytes", "pa_decode",
+    "pa_prefill_chunk", "pa_get_device_error", "pa_status_string",
+]
+
+PA_F16, PA_BF16, PA_FP8_E4M3 = 0, 1, 2
+STATUS_NAMES = {0: "PA_OK", 1: "PA_ERR_INVALID_ARG", 2: "PA_ERR_UNSUPPORTED", 3: "PA_ERR_CUDA",
+                4: "PA_ERR_DEVICE_CHECK", 5: "PA_ERR_TIMEOUT"}
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libpa.so")
+
+
+class PaError(RuntimeError):
+    def __init__(self, status: int, where: str):
+        self.status = status
+        super().__init__(f"{where}: {STATUS_NAMES.get(status, status)}")
+
+
+class PaKvCache(ctypes.Structure):
+    """Mirror of ``pa_kv_cache``."""
+    _fields_ = [("num_blocks", ctypes.c_int64), ("block_size", ctypes.c_int32),
+                ("num_kv_heads", ctypes.c_int32), ("head_dim", ctypes.c_int32),
+                ("kv_dtype", ctypes.c_int), ("k_scale", ctypes.c_float), ("v_scale", ctypes.c_float)]
+
+
+_lib = None
+
+
+def lib() -> ctypes.CDLL:
+    """Load libpa.so (built by ``build_lib.build()``); raise if it is missing."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(LIB_PATH):
+            raise RuntimeError(f"libpa.so not built at {LIB_PATH}; run build_lib.build() first")
+        L = ctypes.CDLL(LIB_PATH)
+        P, I32, I64, F, SZ = ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64, ctypes.c_float, ctypes.c_size_t
+        L.pa_reshape_and_cache.argtypes = [P, P, ctypes.c_int, I32, I64, P, P, P, ctypes.POINTER(PaKvCache), P]
+        L.pa_copy_blocks.argtypes = [P, P, ctypes.POINTER(PaKvCache), P, I32, P]
+        L.pa_decode_workspace_bytes.argtypes = [I32, I32, I32, I32, I32, I32]
+        L.pa_decode_workspace_bytes.restype = SZ
+        L.pa_decode.argtypes = [P, ctypes.c_int, I32, I32, P, P, ctypes.POINTER(PaKvCache), P, I32, P, I32, F,
+                                I32, P, SZ, P, P]
+        L.pa_prefill_chunk.argtypes = [P, ctypes.c_int, P, P, I32, I32, I32, P, P, ctypes.POINTER(PaKvCache), P,
+                                       I32, P, I32, F, P, P]
+        L.pa_get_device_error.argtypes = [P, ctypes.POINTER(I32)]
+        L.pa_status_string.argtypes = [ctypes.c_int]
+        L.pa_status_string.restype = ctypes.c_char_p
+        for name in ("pa_reshape_and_cache", "pa_copy_blocks", "pa_decode", "pa_prefill_chunk",
+                     "pa_get_device_error"):
+            getattr(L, name).restype = ctypes.c_int
+        _lib = L
+    return _lib
+
+
+def _dtype_code(t: torch.dtype) -> int:
+    if t == torch.float16:
+        return PA_F16
+    if t == torch.bfloat16:
+        return PA_BF16
+    if t in (torch.uint8, torch.float8_e4m3fn):
+        return PA_FP8_E4M3
+    raise TypeError(f"unsupported dtype {t}")
+
+
+def _stream(stream) -> int:
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream)
+
+
+def _dev(t: torch.Tensor | None, name: str) -> int | None:
+    if t is None:
+        return None
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    return t.data_ptr()
+
+
+def _ok(status: int, where: str) -> None:
+    if status != 0:
+        raise PaError(status, where)
+
+
+def kv_cache_desc(k_cache: torch.Tensor, k_scale: float = 1.0, v_scale: float = 1.0) -> PaKvCache:
+    """Descriptor of a pool tensor shaped [num_blocks, num_kv_heads, block_size, head_dim]."""
+    nb, hkv, bs, d = k_cache.shape
+    return PaKvCache(nb, bs, hkv, d, _dtype_code(k_cache.dtype), float(k_scale), float(v_scale))
+
+
+def pa_reshape_and_cache(k: torch.Tensor, v: torch.Tensor, slot_mapping: torch.Tensor, k_cache: torch.Tensor,
+                         v_cache: torch.Tensor, cache: PaKvCache, stream=None) -> None:
+    """k, v: [T, Hkv, D] (f16/bf16, token stride may exceed Hkv*D); slot_mapping int64 [T]."""
+    T = k.shape[0]
+    stride = k.stride(0)
+    if k.stride()[1:] != (k.shape[2], 1) or v.stride() != k.stride():
+        raise ValueError("k and v must be [T, Hkv, D] with unit inner strides and equal strides")
+    if slot_mapping.dtype != torch.int64:
+        raise TypeError("slot_mapping must be int64")
+    _ok(lib().pa_reshape_and_cache(k.data_ptr(), v.data_ptr(), _dtype_code(k.dtype), T, stride,
+                                   _dev(slot_mapping, "slot_mapping"), _dev(k_cache, "k_cache"),
+                                   _dev(v_cache, "v_cache"), ctypes.byref(cache), _stream(stream)),
+        "pa_reshape_and_cache")
+
+
+def pa_copy_blocks(k_cache: torch.Tensor, v_cache: torch.Tensor, cache: PaKvCache, src_dst_pairs: torch.Tensor,
+                   stream=None) -> None:
+    """src_dst_pairs: int32 [n, 2] of (src, dst) physical block ids."""
+    if src_dst_pairs.dtype != torch.int32:
+        raise TypeError("src_dst_pairs must be int32")
+    _ok(lib().pa_copy_blocks(_dev(k_cache, "k_cache"), _dev(v_cache, "v_cache"), ctypes.byref(cache),
+                             _dev(src_dst_pairs, "src_dst_pairs"), src_dst_pairs.shape[0], _stream(stream)),
+        "pa_copy_blocks")
+
+
+def pa_decode_workspace_bytes(num_seqs: int, num_q_heads: int, num_kv_heads: int, head_dim: int,
+                              max_seq_len: int, partition_size: int = 0) -> int:
+    return int(lib().pa_decode_workspace_bytes(num_seqs, num_q_heads, num_kv_heads, head_dim, max_seq_len,
+                                               partition_size))
+
+
+def pa_decode(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor, cache: PaKvCache,
+              block_tables: torch.Tensor, seq_lens: torch.Tensor, max_seq_len: int, scale: float,
+              out: torch.Tensor, workspace: torch.Tensor | None = None, partition_size: int = 0,
+              stream=None) -> None:
+    """q, out: [B, Hq, D]; block_tables int32 [B, max_blocks]; seq_lens int32 [B].
+    ``workspace``: uint8 tensor of >= pa_decode_workspace_bytes(...) bytes,
+    zero-filled before its first use (None when that size is 0)."""
+    B, hq, _ = q.shape
+    ws_ptr = _dev(workspace, "workspace")
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    _ok(lib().pa_decode(_dev(q, "q"), _dtype_code(q.dtype), B, hq, _dev(k_cache, "k_cache"), _dev(v_cache, "v_cache"),
+                        ctypes.byref(cache), _dev(block_tables, "block_tables"), block_tables.shape[1],
+                        _dev(seq_lens, "seq_lens"), int(max_seq_len), float(scale), int(partition_size), ws_ptr,
+                        ws_bytes, _dev(out, "out"), _stream(stream)), "pa_decode")
+
+
+def pa_prefill_chunk(q_chunk: torch.Tensor, cu_q_lens: torch.Tensor, q_start: torch.Tensor, max_q_len: int,
+                     k_cache: torch.Tensor, v_cache: torch.Tensor, cache: PaKvCache, block_tables: torch.Tensor,
+                     seq_lens: torch.Tensor, max_seq_len: int, scale: float, out: torch.Tensor,
+                     stream=None) -> None:
+    """q_chunk, out: [total_q, Hq, D]; cu_q_lens int32 [n+1]; q_start, seq_lens int32 [n]."""
+    _ok(lib().pa_prefill_chunk(_dev(q_chunk, "q_chunk"), _dtype_code(q_chunk.dtype), _dev(cu_q_lens, "cu_q_lens"),
+                               _dev(q_start, "q_start"), q_start.shape[0], int(max_q_len), q_chunk.shape[1],
+                               _dev(k_cache, "k_cache"), _dev(v_cache, "v_cache"), ctypes.byref(cache),
+                               _dev(block_tables, "block_tables"), block_tables.shape[1], _dev(seq_lens, "seq_lens"),
+                               int(max_seq_len), float(scale), _dev(out, "out"), _stream(stream)),
+        "pa_prefill_chunk")
+
+
+def pa_get_device_error(stream=None) -> int:
+    """Synchronise the stream, then read and clear the device error word."""
+    code = ctypes.c_int32(0)
+    _ok(lib().pa_get_device_error(_stream(stream), ctypes.byref(code)), "pa_get_device_error")
+    return code.value
+
+
+def pa_status_string(status: int) -> str:
+    return lib().pa_status_string(int(status)).decode()

@@ -1,0 +1,313 @@
+// pa_api.cu -- the extern "C" entry points of libpa declared in include/pa.h.
+//
+// Host side only: validate arguments, build the TMA tensor maps of the two
+// pools, lay out the split-KV workspace, pick the kernel instantiation and
+// enqueue it on the caller's stream.  No call allocates memory or
+// synchronises (except pa_get_device_error).
+#include <cudaTypedefs.h>
+
+#include <cmath>
+#include <mutex>
+
+#include "pa_common.cuh"
+#include "pa_internal.h"
+
+namespace pa {
+
+__device__ int32_t g_device_error = 0;
+
+namespace {
+
+bool aligned(const void *p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; }
+
+// Address of the current device's error word (a host-side name is not a
+// device address; the runtime resolves it per device).
+int32_t *device_error_word() {
+  void *ptr = nullptr;
+  return cudaGetSymbolAddress(&ptr, g_device_error) == cudaSuccess ? static_cast<int32_t *>(ptr)
+                                                                   : nullptr;
+}
+size_t round256(size_t x) { return (x + 255) & ~size_t(255); }
+
+pa_status check_cache(const pa_kv_cache *c) {
+  if (c == nullptr || c->num_blocks <= 0 || c->num_kv_heads <= 0) return PA_ERR_INVALID_ARG;
+  if (c->block_size != 16 && c->block_size != 32) return PA_ERR_UNSUPPORTED;
+  if (c->head_dim != 64 && c->head_dim != 128) return PA_ERR_UNSUPPORTED;
+  if (c->kv_dtype != PA_F16 && c->kv_dtype != PA_BF16 && c->kv_dtype != PA_FP8_E4M3)
+    return PA_ERR_UNSUPPORTED;
+  if (c->kv_dtype == PA_FP8_E4M3 &&
+      !(std::isfinite(c->k_scale) && c->k_scale > 0.f && std::isfinite(c->v_scale) &&
+        c->v_scale > 0.f))
+    return PA_ERR_INVALID_ARG;
+  // tile rows of the 2D pool view are addressed with int32 TMA coordinates
+  if ((double)c->num_blocks * c->num_kv_heads * c->block_size >= 2147483648.0)
+    return PA_ERR_UNSUPPORTED;
+  return PA_OK;
+}
+
+pa_status check_pools(const void *k_cache, const void *v_cache) {
+  if (!k_cache || !v_cache || !aligned(k_cache, 16) || !aligned(v_cache, 16))
+    return PA_ERR_INVALID_ARG;
+  return PA_OK;
+}
+
+// q dtype must equal the cache dtype, except that an fp8 cache takes f16/bf16 queries.
+pa_status check_q_dtype(pa_dtype q, const pa_kv_cache &c) {
+  if (q != PA_F16 && q != PA_BF16) return PA_ERR_UNSUPPORTED;
+  if (c.kv_dtype != PA_FP8_E4M3 && q != c.kv_dtype) return PA_ERR_UNSUPPORTED;
+  return PA_OK;
+}
+
+int heads_per_cta(int gqa) { return gqa % 8 == 0 ? 8 : gqa % 4 == 0 ? 4 : 1; }
+
+PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void *ptr = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(ptr);
+  });
+  return fn;
+}
+
+// One pool as a 2D tensor [num_blocks*Hkv*bs rows][head_dim]; box = 16 rows x
+// one 128-byte (or 64-byte) panel, swizzled to match the kernels' reads.
+bool encode_pool_map(CUtensorMap *map, const void *base, const pa_kv_cache &c) {
+  auto enc = tensor_map_encoder();
+  if (!enc) return false;
+  const int eb = dtype_bytes(c.kv_dtype);
+  const int row_bytes = c.head_dim * eb;
+  const int panel_bytes = row_bytes < 128 ? row_bytes : 128;
+  const cuuint64_t dims[2] = {(cuuint64_t)c.head_dim,
+                              (cuuint64_t)c.num_blocks * c.num_kv_heads * c.block_size};
+  const cuuint64_t strides[1] = {(cuuint64_t)row_bytes};
+  const cuuint32_t box[2] = {(cuuint32_t)(panel_bytes / eb), 16u};
+  const cuuint32_t estr[2] = {1u, 1u};
+  const CUtensorMapDataType dt = c.kv_dtype == PA_FP8_E4M3 ? CU_TENSOR_MAP_DATA_TYPE_UINT8
+                                 : c.kv_dtype == PA_BF16   ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16
+                                                           : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
+  const CUtensorMapSwizzle sw =
+      panel_bytes == 128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B;
+  return enc(map, dt, 2, const_cast<void *>(base), dims, strides, box, estr,
+             CU_TENSOR_MAP_INTERLEAVE_NONE, sw, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+cudaError_t dispatch_attention(pa_dtype q_dtype, const pa_kv_cache &c, const AttnParams &p,
+                               const PoolMaps &m, int rows, cudaStream_t s) {
+  if (c.kv_dtype == PA_BF16) return launch_attention_bf16(p, m, c.head_dim, rows, s);
+  if (c.kv_dtype == PA_F16) return launch_attention_f16(p, m, c.head_dim, rows, s);
+  if (q_dtype == PA_BF16) return launch_attention_fp8_bf16q(p, m, c.head_dim, rows, s);
+  return launch_attention_fp8_f16q(p, m, c.head_dim, rows, s);
+}
+
+}  // namespace
+
+WorkspaceLayout decode_workspace_layout(int64_t rows, int64_t num_q_heads, int64_t head_dim,
+                                        int64_t max_partitions) {
+  WorkspaceLayout w;
+  w.acc_off = 0;
+  w.ml_off = round256((size_t)(rows * num_q_heads * max_partitions * head_dim * 4));
+  w.cnt_off = w.ml_off + round256((size_t)(rows * num_q_heads * max_partitions * 8));
+  w.total = w.cnt_off + round256((size_t)(rows * num_q_heads * 4));
+  return w;
+}
+
+}  // namespace pa
+
+using namespace pa;
+
+extern "C" {
+
+pa_status pa_reshape_and_cache(const void *k, const void *v, pa_dtype in_dtype, int32_t num_tokens,
+                               int64_t token_stride, const int64_t *slot_mapping, void *k_cache,
+                               void *v_cache, const pa_kv_cache *cache, pa_stream_t stream) {
+  pa_status st = check_cache(cache);
+  if (st != PA_OK) return st;
+  if (num_tokens < 0) return PA_ERR_INVALID_ARG;
+  if (in_dtype != PA_F16 && in_dtype != PA_BF16) return PA_ERR_UNSUPPORTED;
+  if (cache->kv_dtype != PA_FP8_E4M3 && cache->kv_dtype != in_dtype) return PA_ERR_UNSUPPORTED;
+  if (token_stride < (int64_t)cache->num_kv_heads * cache->head_dim || token_stride % 8)
+    return PA_ERR_INVALID_ARG;
+  if (num_tokens == 0) return PA_OK;
+  if (!k || !v || !slot_mapping || !aligned(k, 16) || !aligned(v, 16) || !aligned(slot_mapping, 8))
+    return PA_ERR_INVALID_ARG;
+  if ((st = check_pools(k_cache, v_cache)) != PA_OK) return st;
+  int32_t *err = device_error_word();
+  if (!err) return PA_ERR_CUDA;
+  return launch_reshape_and_cache(k, v, in_dtype, num_tokens, token_stride, slot_mapping, k_cache,
+                                  v_cache, *cache, err, reinterpret_cast<cudaStream_t>(stream)) ==
+                 cudaSuccess
+             ? PA_OK
+             : PA_ERR_CUDA;
+}
+
+pa_status pa_copy_blocks(void *k_cache, void *v_cache, const pa_kv_cache *cache,
+                         const int32_t *src_dst_pairs, int32_t num_pairs, pa_stream_t stream) {
+  pa_status st = check_cache(cache);
+  if (st != PA_OK) return st;
+  if (num_pairs < 0) return PA_ERR_INVALID_ARG;
+  if (num_pairs == 0) return PA_OK;
+  if (!src_dst_pairs || !aligned(src_dst_pairs, 8)) return PA_ERR_INVALID_ARG;
+  if ((st = check_pools(k_cache, v_cache)) != PA_OK) return st;
+  int32_t *err = device_error_word();
+  if (!err) return PA_ERR_CUDA;
+  return launch_copy_blocks(k_cache, v_cache, *cache, src_dst_pairs, num_pairs, err,
+                            reinterpret_cast<cudaStream_t>(stream)) == cudaSuccess
+             ? PA_OK
+             : PA_ERR_CUDA;
+}
+
+size_t pa_decode_workspace_bytes(int32_t num_seqs, int32_t num_q_heads, int32_t num_kv_heads,
+                                 int32_t head_dim, int32_t max_seq_len, int32_t partition_size) {
+  if (num_seqs < 0 || num_q_heads <= 0 || num_kv_heads <= 0 || head_dim <= 0 || max_seq_len < 0 ||
+      partition_size < 0 || num_q_heads % num_kv_heads)
+    return 0;
+  const int ps = partition_size ? partition_size : kDefaultPartition;
+  if (ps % 32) return 0;
+  const int64_t parts = ((int64_t)max_seq_len + ps - 1) / ps;
+  if (parts <= 1 || parts > kMaxPartitions) return 0;
+  return decode_workspace_layout(num_seqs, num_q_heads, head_dim, parts).total;
+}
+
+pa_status pa_decode(const void *q, pa_dtype q_dtype, int32_t num_seqs, int32_t num_q_heads,
+                    const void *k_cache, const void *v_cache, const pa_kv_cache *cache,
+                    const int32_t *block_tables, int32_t max_blocks_per_seq,
+                    const int32_t *seq_lens, int32_t max_seq_len, float scale,
+                    int32_t partition_size, void *workspace, size_t workspace_bytes, void *out,
+                    pa_stream_t stream) {
+  pa_status st = check_cache(cache);
+  if (st != PA_OK) return st;
+  const pa_kv_cache &c = *cache;
+  if (num_seqs < 0 || num_q_heads <= 0 || num_q_heads % c.num_kv_heads || max_seq_len < 0 ||
+      max_blocks_per_seq <= 0 || partition_size < 0 || partition_size % 32 || !std::isfinite(scale))
+    return PA_ERR_INVALID_ARG;
+  if ((st = check_q_dtype(q_dtype, c)) != PA_OK) return st;
+  if (num_seqs == 0) return PA_OK;
+  if (!q || !out || !block_tables || !seq_lens || !aligned(q, 16) || !aligned(out, 16) ||
+      !aligned(block_tables, 4) || !aligned(seq_lens, 4))
+    return PA_ERR_INVALID_ARG;
+  if ((st = check_pools(k_cache, v_cache)) != PA_OK) return st;
+  if (num_q_heads > 65535) return PA_ERR_UNSUPPORTED;
+
+  const int ps = partition_size ? partition_size : kDefaultPartition;
+  const int64_t parts64 = std::max<int64_t>(1, ((int64_t)max_seq_len + ps - 1) / ps);
+  if (parts64 > kMaxPartitions) return PA_ERR_UNSUPPORTED;
+  const int parts = (int)parts64;
+
+  AttnParams p{};
+  p.q = q;
+  p.out = out;
+  p.block_tables = block_tables;
+  p.max_blocks_per_seq = max_blocks_per_seq;
+  p.seq_lens = seq_lens;
+  p.num_q_heads = num_q_heads;
+  p.num_kv_heads = c.num_kv_heads;
+  p.heads_per_cta = heads_per_cta(num_q_heads / c.num_kv_heads);
+  p.block_size = c.block_size;
+  p.num_blocks = c.num_blocks;
+  p.partition_size = ps;
+  p.max_partitions = parts;
+  const bool fp8 = c.kv_dtype == PA_FP8_E4M3;
+  p.q_mult = scale * 1.4426950408889634f * (fp8 ? c.k_scale : 1.f);
+  p.out_mult = fp8 ? c.v_scale : 1.f;
+  if (parts > 1) {
+    const WorkspaceLayout w = decode_workspace_layout(num_seqs, num_q_heads, c.head_dim, parts);
+    if (!workspace || !aligned(workspace, 256) || workspace_bytes < w.total)
+      return PA_ERR_INVALID_ARG;
+    char *ws = static_cast<char *>(workspace);
+    p.ws_acc = reinterpret_cast<float *>(ws + w.acc_off);
+    p.ws_ml = reinterpret_cast<float2 *>(ws + w.ml_off);
+    p.ws_count = reinterpret_cast<int32_t *>(ws + w.cnt_off);
+  }
+  p.err = device_error_word();
+  PoolMaps maps;
+  if (!p.err || !encode_pool_map(&maps.k, k_cache, c) || !encode_pool_map(&maps.v, v_cache, c))
+    return PA_ERR_CUDA;
+  return dispatch_attention(q_dtype, c, p, maps, num_seqs, reinterpret_cast<cudaStream_t>(stream)) ==
+                 cudaSuccess
+             ? PA_OK
+             : PA_ERR_CUDA;
+}
+
+pa_status pa_prefill_chunk(const void *q_chunk, pa_dtype q_dtype, const int32_t *cu_q_lens,
+                           const int32_t *q_start, int32_t num_chunks, int32_t max_q_len,
+                           int32_t num_q_heads, const void *k_cache, const void *v_cache,
+                           const pa_kv_cache *cache, const int32_t *block_tables,
+                           int32_t max_blocks_per_seq, const int32_t *seq_lens,
+                           int32_t max_seq_len, float scale, void *out, pa_stream_t stream) {
+  pa_status st = check_cache(cache);
+  if (st != PA_OK) return st;
+  const pa_kv_cache &c = *cache;
+  if (num_chunks < 0 || max_q_len < 0 || num_q_heads <= 0 || num_q_heads % c.num_kv_heads ||
+      max_seq_len < 0 || max_blocks_per_seq <= 0 || !std::isfinite(scale))
+    return PA_ERR_INVALID_ARG;
+  if ((st = check_q_dtype(q_dtype, c)) != PA_OK) return st;
+  if (num_chunks == 0 || max_q_len == 0) return PA_OK;
+  if (!q_chunk || !out || !cu_q_lens || !q_start || !block_tables || !seq_lens ||
+      !aligned(q_chunk, 16) || !aligned(out, 16) || !aligned(cu_q_lens, 4) ||
+      !aligned(q_start, 4) || !aligned(block_tables, 4) || !aligned(seq_lens, 4))
+    return PA_ERR_INVALID_ARG;
+  if ((st = check_pools(k_cache, v_cache)) != PA_OK) return st;
+  const int64_t rows = (int64_t)num_chunks * max_q_len;
+  if (rows > 2147483647ll || num_q_heads > 65535) return PA_ERR_UNSUPPORTED;
+
+  AttnParams p{};
+  p.q = q_chunk;
+  p.out = out;
+  p.block_tables = block_tables;
+  p.max_blocks_per_seq = max_blocks_per_seq;
+  p.seq_lens = seq_lens;
+  p.cu_q_lens = cu_q_lens;
+  p.q_start = q_start;
+  p.max_q_len = max_q_len;
+  p.num_q_heads = num_q_heads;
+  p.num_kv_heads = c.num_kv_heads;
+  p.heads_per_cta = heads_per_cta(num_q_heads / c.num_kv_heads);
+  p.block_size = c.block_size;
+  p.num_blocks = c.num_blocks;
+  p.partition_size = std::max(32, (max_seq_len + 31) / 32 * 32);  // one partition per row
+  p.max_partitions = 1;
+  const bool fp8 = c.kv_dtype == PA_FP8_E4M3;
+  p.q_mult = scale * 1.4426950408889634f * (fp8 ? c.k_scale : 1.f);
+  p.out_mult = fp8 ? c.v_scale : 1.f;
+  p.err = device_error_word();
+  PoolMaps maps;
+  if (!p.err || !encode_pool_map(&maps.k, k_cache, c) || !encode_pool_map(&maps.v, v_cache, c))
+    return PA_ERR_CUDA;
+  return dispatch_attention(q_dtype, c, p, maps, (int)rows, reinterpret_cast<cudaStream_t>(stream)) ==
+                 cudaSuccess
+             ? PA_OK
+             : PA_ERR_CUDA;
+}
+
+pa_status pa_get_device_error(pa_stream_t stream, int32_t *code) {
+  if (!code) return PA_ERR_INVALID_ARG;
+  if (cudaStreamSynchronize(reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess)
+    return PA_ERR_CUDA;
+  int32_t v = 0;
+  const int32_t zero = 0;
+  if (cudaMemcpyFromSymbol(&v, g_device_error, sizeof v) != cudaSuccess ||
+      cudaMemcpyToSymbol(g_device_error, &zero, sizeof zero) != cudaSuccess)
+    return PA_ERR_CUDA;
+  *code = v;
+  return PA_OK;
+}
+
+const char *pa_status_string(pa_status status) {
+  switch (status) {
+    case PA_OK: return "PA_OK";
+    case PA_ERR_INVALID_ARG: return "PA_ERR_INVALID_ARG";
+    case PA_ERR_UNSUPPORTED: return "PA_ERR_UNSUPPORTED";
+    case PA_ERR_CUDA: return "PA_ERR_CUDA";
+    case PA_ERR_DEVICE_CHECK: return "PA_ERR_DEVICE_CHECK";
+    case PA_ERR_TIMEOUT: return "PA_ERR_TIMEOUT";
+  }
+  return "PA_ERR_UNKNOWN";
+}
+
+}  // extern "C"

@@ -1,0 +1,10 @@
+// pa_attn_fp8_f16q.cu -- paged attention instantiations for a fp8-e4m3 cache, f16 queries.
+// One translation unit per dtype pair so the library compiles in parallel.
+#include "pa_attention.cuh"
+
+namespace pa {
+cudaError_t launch_attention_fp8_f16q(const AttnParams &p, const PoolMaps &m, int head_dim, int rows,
+                                     cudaStream_t s) {
+  return launch_attention<uint8_t, __half>(p, m, head_dim, rows, s);
+}
+}  // namespace pa

@@ -1,0 +1,76 @@
+// pa_internal.h -- host-side interface between the C ABI (pa_api.cu) and the
+// kernel launchers.  Not installed; not part of the public header.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "../../include/pa.h"
+
+namespace pa {
+
+inline int dtype_bytes(pa_dtype t) { return t == PA_FP8_E4M3 ? 1 : 2; }
+
+constexpr int kDefaultPartition = 512;   // split-KV partition, tokens
+constexpr int kMaxPartitions = 4096;     // per sequence (limits the combine's smem)
+
+// Decode / CUDA-core prefill parameters shared by every instantiation.
+struct AttnParams {
+  const void *q;              // [rows][Hq][D]
+  void *out;                  // [rows][Hq][D]
+  const int32_t *block_tables;
+  int32_t max_blocks_per_seq;
+  // decode: one row per sequence, row i has seq_lens[i] tokens
+  const int32_t *seq_lens;
+  // prefill (cu_q_lens != nullptr): row (c, r) has q_start[c] + r + 1 tokens
+  const int32_t *cu_q_lens;
+  const int32_t *q_start;
+  int32_t max_q_len;
+  int32_t num_q_heads;
+  int32_t num_kv_heads;
+  int32_t heads_per_cta;      // query heads one CTA serves (share one KV read)
+  int32_t block_size;
+  int64_t num_blocks;
+  int32_t partition_size;     // tokens per split-KV partition (multiple of 32)
+  int32_t max_partitions;     // grid.z
+  float q_mult;               // softmax scale * log2(e) (* k_scale for fp8)
+  float out_mult;             // v_scale for fp8, else 1
+  // split-KV workspace (null when max_partitions == 1)
+  float *ws_acc;              // [rows][Hq][max_partitions][D]
+  float2 *ws_ml;              // [rows][Hq][max_partitions] (max, sum) in log2 units
+  int32_t *ws_count;          // [rows][Hq] arrival counters (self-resetting)
+  int32_t *err;               // device error word
+};
+
+struct WorkspaceLayout {
+  size_t acc_off, ml_off, cnt_off, total;
+};
+WorkspaceLayout decode_workspace_layout(int64_t rows, int64_t num_q_heads, int64_t head_dim,
+                                        int64_t max_partitions);
+
+cudaError_t launch_reshape_and_cache(const void *k, const void *v, pa_dtype in_dtype,
+                                     int64_t num_tokens, int64_t token_stride,
+                                     const int64_t *slot_mapping, void *k_cache, void *v_cache,
+                                     const pa_kv_cache &c, int32_t *err, cudaStream_t stream);
+
+cudaError_t launch_copy_blocks(void *k_cache, void *v_cache, const pa_kv_cache &c,
+                               const int32_t *pairs, int32_t num_pairs, int32_t *err,
+                               cudaStream_t stream);
+
+// Tensor maps over one pool viewed as a 2D array [num_blocks*Hkv*bs rows][D].
+struct PoolMaps {
+  CUtensorMap k, v;
+};
+
+// Launch the paged decode / CUDA-core prefill kernel for one (kv dtype, q dtype).
+cudaError_t launch_attention_bf16(const AttnParams &p, const PoolMaps &m, int head_dim, int rows,
+                                  cudaStream_t s);
+cudaError_t launch_attention_f16(const AttnParams &p, const PoolMaps &m, int head_dim, int rows,
+                                 cudaStream_t s);
+cudaError_t launch_attention_fp8_bf16q(const AttnParams &p, const PoolMaps &m, int head_dim,
+                                       int rows, cudaStream_t s);
+cudaError_t launch_attention_fp8_f16q(const AttnParams &p, const PoolMaps &m, int head_dim,
+                                      int rows, cudaStream_t s);
+
+}  // namespace pa

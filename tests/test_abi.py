@@ -1,0 +1,143 @@
+"""C-ABI checks that need no GPU: the library builds for sm_103a, loads,
+exports every entry point the header declares, and rejects bad arguments on
+the host before touching the device."""
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "pa.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from paged_kv_cache_writes_gb300 import build_lib
+    build_lib.build()
+    import paged_kv_cache_writes_gb300 as pa
+    return pa.lib()
+
+
+def declared_functions():
+    src = open(HEADER).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"^\s*(?:PA_API\s+)?(?:const\s+)?[A-Za-z_][A-Za-z0-9_]*\s*\*?\s*(pa_[a-z0-9_]+)\s*\(", src, re.M)))
+
+
+def test_header_declares_the_boundary():
+    names = declared_functions()
+    for want in ("pa_reshape_and_cache", "pa_decode", "pa_prefill_chunk", "pa_copy_blocks",
+                 "pa_decode_workspace_bytes", "pa_get_device_error", "pa_status_string"):
+        assert want in names
+
+
+def test_every_declared_symbol_is_exported(lib):
+    for name in declared_functions():
+        assert hasattr(lib, name), name
+
+
+def test_only_the_c_abi_is_exported(lib):
+    """Hidden visibility: the shared object exports the pa_* C symbols and no C++ internals."""
+    import subprocess
+    from paged_kv_cache_writes_gb300 import LIB_PATH
+    out = subprocess.run(["nm", "-D", "--defined-only", LIB_PATH], capture_output=True, text=True).stdout
+    syms = [ln.split()[-1] for ln in out.splitlines() if " T " in ln]
+    pa_syms = [s for s in syms if s.startswith("pa_")]
+    assert sorted(pa_syms) == declared_functions()
+    assert not [s for s in syms if s.startswith("_ZN2pa")]
+
+
+def test_status_strings(lib):
+    import paged_kv_cache_writes_gb300 as pa
+    assert [pa.pa_status_string(i) for i in range(6)] == [pa.STATUS_NAMES[i] for i in range(6)]
+    assert pa.pa_status_string(99) == "PA_ERR_UNKNOWN"
+
+
+def _desc(**kw):
+    import paged_kv_cache_writes_gb300 as pa
+    d = dict(num_blocks=64, block_size=16, num_kv_heads=8, head_dim=128, kv_dtype=pa.PA_BF16, k_scale=1.0,
+             v_scale=1.0)
+    d.update(kw)
+    return pa.PaKvCache(**d)
+
+
+FAKE = 0x10000  # a 16-byte aligned non-null address; never dereferenced on these paths
+
+
+def _decode(lib, desc, **kw):
+    a = dict(q=FAKE, q_dtype=1, num_seqs=4, num_q_heads=32, k=FAKE, v=FAKE, bt=FAKE, mb=8, sl=FAKE, msl=100,
+             scale=0.1, ps=0, ws=None, wsb=0, out=FAKE)
+    a.update(kw)
+    return lib.pa_decode(a["q"], a["q_dtype"], a["num_seqs"], a["num_q_heads"], a["k"], a["v"], ctypes.byref(desc),
+                         a["bt"], a["mb"], a["sl"], a["msl"], a["scale"], a["ps"], a["ws"], a["wsb"], a["out"], None)
+
+
+@pytest.mark.parametrize("kw,desc_kw,want", [
+    (dict(num_seqs=0), {}, 0),                                  # zero work: OK, nothing launched
+    (dict(num_seqs=-1), {}, 1),
+    (dict(num_q_heads=30), {}, 1),                              # Hq % Hkv != 0
+    (dict(q=FAKE + 4), {}, 1),                                  # misaligned
+    (dict(q=None), {}, 1),
+    (dict(out=None), {}, 1),
+    (dict(ps=48), {}, 1),                                       # partition not a multiple of 32
+    (dict(scale=float("nan")), {}, 1),
+    (dict(msl=2000, ws=None), {}, 1),                           # split-KV needs a workspace
+    (dict(q_dtype=0), {}, 2),                                   # f16 q with a bf16 cache
+    ({}, dict(head_dim=96), 2),
+    ({}, dict(block_size=8), 2),
+    ({}, dict(kv_dtype=7), 2),
+    ({}, dict(kv_dtype=2, k_scale=0.0), 1),                     # fp8 needs a positive scale
+    ({}, dict(num_blocks=0), 1),
+    ({}, dict(num_blocks=1 << 30), 2),                          # rows beyond int32 TMA coordinates
+])
+def test_decode_host_validation(lib, kw, desc_kw, want):
+    assert _decode(lib, _desc(**desc_kw), **kw) == want
+
+
+def test_reshape_and_cache_validation(lib):
+    d = _desc()
+    f = lib.pa_reshape_and_cache
+    assert f(FAKE, FAKE, 1, 0, 1024, FAKE, FAKE, FAKE, ctypes.byref(d), None) == 0
+    assert f(FAKE, FAKE, 1, -1, 1024, FAKE, FAKE, FAKE, ctypes.byref(d), None) == 1
+    assert f(FAKE, FAKE, 1, 4, 1000, FAKE, FAKE, FAKE, ctypes.byref(d), None) == 1      # stride < Hkv*D
+    assert f(FAKE, FAKE, 1, 4, 1028, FAKE, FAKE, FAKE, ctypes.byref(d), None) == 1      # stride % 8
+    assert f(FAKE, FAKE, 0, 4, 1024, FAKE, FAKE, FAKE, ctypes.byref(d), None) == 2      # f16 into bf16 cache
+    assert f(FAKE, FAKE, 2, 4, 1024, FAKE, FAKE, FAKE, ctypes.byref(d), None) == 2      # fp8 input
+    assert f(FAKE, FAKE, 1, 4, 1024, FAKE + 4, FAKE, FAKE, ctypes.byref(d), None) == 1  # slots misaligned
+    assert f(FAKE, FAKE, 1, 4, 1024, FAKE, None, FAKE, ctypes.byref(d), None) == 1
+    assert f(FAKE, FAKE, 1, 4, 1024, FAKE, FAKE, FAKE, None, None) == 1
+
+
+def test_copy_blocks_validation(lib):
+    d = _desc()
+    f = lib.pa_copy_blocks
+    assert f(FAKE, FAKE, ctypes.byref(d), FAKE, 0, None) == 0
+    assert f(FAKE, FAKE, ctypes.byref(d), FAKE, -2, None) == 1
+    assert f(FAKE, FAKE, ctypes.byref(d), None, 3, None) == 1
+    assert f(None, FAKE, ctypes.byref(d), FAKE, 3, None) == 1
+
+
+def test_prefill_validation(lib):
+    d = _desc()
+    f = lib.pa_prefill_chunk
+    ok = (FAKE, 1, FAKE, FAKE, 1, 64, 32, FAKE, FAKE, ctypes.byref(d), FAKE, 8, FAKE, 128, 0.1, FAKE, None)
+    assert f(*ok[:4], 0, *ok[5:]) == 0                      # no chunks
+    assert f(*ok[:5], 0, *ok[6:]) == 0                      # empty chunks
+    assert f(*ok[:4], -1, *ok[5:]) == 1
+    assert f(*ok[:6], 31, *ok[7:]) == 1                     # Hq % Hkv
+    assert f(ok[0], 0, *ok[2:]) == 2                        # f16 q, bf16 cache
+    assert f(*ok[:2], None, *ok[3:]) == 1
+
+
+def test_workspace_size(lib):
+    import paged_kv_cache_writes_gb300 as pa
+    assert pa.pa_decode_workspace_bytes(256, 64, 8, 128, 512, 0) == 0        # one partition: none needed
+    n = pa.pa_decode_workspace_bytes(256, 64, 8, 128, 8192, 512)
+    parts = 16
+    acc = 256 * 64 * parts * 128 * 4
+    ml = 256 * 64 * parts * 8
+    cnt = 256 * 64 * 4
+    assert n == acc + ml + cnt                                                 # all multiples of 256
+    assert pa.pa_decode_workspace_bytes(4, 30, 8, 128, 8192, 0) == 0         # invalid -> 0
+    assert pa.pa_decode_workspace_bytes(4, 32, 8, 128, 8192, 48) == 0

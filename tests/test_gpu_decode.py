@@ -1,0 +1,123 @@
+"""GPU parity of paged decode against the fp64 oracle, element by element.
+
+Tolerance (max abs error): 2e-3 for f16/bf16 caches, 2e-2 for an fp8-e4m3
+cache (the oracle dequantises the same codes with the same scales).  Shapes
+span several tiles and partitions with ragged tails; the named workloads run
+at full size, compared on all sequences or on a sample the oracle computes
+one by one, plus size-independent properties on the rest."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import workloads as W
+from _gpu import TOL, max_err, oracle_pools, run_gpu
+
+pytestmark = pytest.mark.gpu
+
+EDGE_LENS = [1, 15, 16, 17, 31, 32, 33, 511, 512, 513, 1000, 1537]
+
+
+def _check(b, seq_ids=None):
+    dev = run_gpu(b)
+    kp, vp = oracle_pools(b)
+    ref = oracle.decode_batch(b, kp, vp, seq_ids=seq_ids)
+    got = dev.out if seq_ids is None else dev.out[torch.as_tensor(seq_ids, device=dev.out.device).long()]
+    ref = ref if seq_ids is None else ref[np.asarray(seq_ids)]
+    err = max_err(got, ref)
+    assert err <= TOL[b.kv_dtype], err
+    return dev, err
+
+
+def test_tiny_config():
+    _check(W.cfg_tiny())
+
+
+@pytest.mark.parametrize("hq,hkv", [(4, 4), (8, 2), (16, 2), (32, 8), (64, 8), (12, 4), (6, 2), (5, 5)])
+@pytest.mark.parametrize("d,bs", [(128, 16), (64, 32), (128, 32), (64, 16)])
+def test_shapes_bf16(hq, hkv, d, bs):
+    _check(W.decode_batch("s", EDGE_LENS, hq, hkv, d, bs, "bf16", seed=hq * 7 + d + bs, partition_size=512))
+
+
+@pytest.mark.parametrize("kv,src", [("f16", "f16"), ("fp8", "bf16"), ("fp8", "f16")])
+@pytest.mark.parametrize("hq,hkv,d,bs", [(32, 8, 128, 16), (64, 8, 128, 32), (8, 8, 64, 16), (16, 4, 64, 32)])
+def test_shapes_other_dtypes(kv, src, hq, hkv, d, bs):
+    _check(W.decode_batch("s", EDGE_LENS, hq, hkv, d, bs, src, kv_dtype=kv, seed=hq + d + bs, partition_size=512))
+
+
+@pytest.mark.parametrize("ps", [0, 32, 96, 512, 2048])
+def test_partition_sizes_agree(ps):
+    b = W.decode_batch("p", [1, 40, 700, 2049, 3000], 16, 2, 128, 16, "bf16", seed=31, partition_size=ps)
+    _check(b)
+
+
+def test_single_token_context_returns_v_exactly():
+    b = W.decode_batch("one", [1] * 9, 16, 4, 128, 32, "bf16", seed=32)
+    dev = run_gpu(b)
+    v = torch.from_numpy(b.step_write.v.view(np.int16)).cuda().view(torch.bfloat16)   # [B, Hkv, D]
+    want = v.repeat_interleave(4, dim=1)
+    assert torch.equal(dev.out.view(torch.int16), want.contiguous().view(torch.int16))
+
+
+def test_zero_length_sequences():
+    b = W.decode_batch("z", [0, 5, 0, 600], 8, 2, 64, 16, "bf16", seed=33, partition_size=256)
+    dev, _ = _check(b)
+    assert dev.out[0].abs().max().item() == 0 and dev.out[2].abs().max().item() == 0
+
+
+def test_workspace_left_zeroed_and_reusable():
+    b = W.decode_batch("r", [3000, 100, 2500], 16, 2, 128, 16, "bf16", seed=34, partition_size=256)
+    dev = run_gpu(b)
+    first = dev.out.clone()
+    assert dev.workspace is not None
+    from paged_kv_cache_writes_gb300 import _HERE  # noqa: F401  (package import check)
+    ws = dev.workspace
+    # the arrival counters live at the end of the workspace and must be zero again
+    hq, parts = b.num_q_heads, -(-3000 // 256)
+    cnt_off = (-(-(b.num_seqs * hq * parts * b.head_dim * 4) // 256) * 256 +
+               -(-(b.num_seqs * hq * parts * 8) // 256) * 256)
+    assert int(ws[cnt_off:].view(torch.int32).abs().sum().item()) == 0
+    for _ in range(3):
+        dev.decode()
+    torch.cuda.synchronize()
+    assert torch.equal(dev.out.view(torch.int16), first.view(torch.int16))
+
+
+def test_llama8b_full():
+    _check(W.cfg_llama8b())
+
+
+def test_llama70b_sampled():
+    b = W.cfg_llama70b()
+    order = np.argsort(b.seq_lens)
+    sample = np.unique(np.concatenate([order[:6], order[-10:], order[::32]]))
+    dev, _ = _check(b, seq_ids=sample)
+    out = dev.out.float()
+    assert torch.isfinite(out).all()
+    # every output row is a convex combination of V rows: bounded by max |V|
+    assert out.abs().max().item() <= 7.0
+
+
+def test_shared_prefix_full():
+    b = W.cfg_shared_prefix()
+    _check(b)
+
+
+def test_mixed_fp8_decode_part_sampled():
+    b = W.cfg_mixed_fp8()
+    _check(b, seq_ids=np.arange(0, b.num_seqs, 8))
+
+
+def test_bad_block_id_sets_error_without_fault():
+    import paged_kv_cache_writes_gb300 as pa
+    b = W.decode_batch("bad", [40, 70], 8, 2, 128, 16, "bf16", seed=35)
+    from paged_kv_cache_writes_gb300.staging import DeviceBatch
+    dev = DeviceBatch(b, "cuda")
+    dev.run_setup()
+    dev.write_step()
+    dev.block_tables[1, 2] = b.num_blocks + 5        # out of range
+    dev.decode()
+    assert pa.pa_get_device_error() == 4
+    dev.block_tables[1, 2] = -3
+    dev.decode()
+    assert pa.pa_get_device_error() == 4

@@ -1,0 +1,57 @@
+"""GPU parity of chunked-prefill attention against the fp64 oracle.
+
+Row r of a chunk at absolute position q_start + r attends causally to
+positions 0 .. q_start + r of its sequence.  Small batches are compared on
+every row; the 512-row chunk of the mixed fp8 workload is compared on sampled
+rows, each of which the oracle computes as a decode with seq_len =
+q_start + r + 1 (the pinned identity "last row of a chunk = decode")."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import workloads as W
+from _gpu import TOL, max_err, oracle_pools, run_gpu
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.mark.parametrize("src,kv", [("bf16", "bf16"), ("f16", "f16"), ("bf16", "fp8")])
+@pytest.mark.parametrize("hq,hkv,d,bs", [(32, 8, 128, 16), (8, 8, 64, 32), (16, 2, 128, 32)])
+def test_prefill_small(src, kv, hq, hkv, d, bs):
+    chunks = [(0, 37), (100, 64), (17, 1), (512, 130), (31, 33)]
+    b = W.prefill_batch("p", chunks, hq, hkv, d, bs, src, kv_dtype=kv, seed=hq + d + bs)
+    dev = run_gpu(b)
+    kp, vp = oracle_pools(b)
+    ref = oracle.prefill_batch(b, kp, vp)
+    assert max_err(dev.prefill["out"], ref) <= TOL[kv]
+
+
+def test_mixed_fp8_prefill_sampled_rows():
+    b = W.cfg_mixed_fp8()
+    dev = run_gpu(b)
+    kp, vp = oracle_pools(b)
+    p = b.prefill
+    rows = np.unique(np.concatenate([np.arange(0, 512, 37), [0, 1, 255, 510, 511]]))
+    qs = int(p.q_start[0])
+    ref = oracle.decode(p.q[rows], oracle.BF16, kp, vp, oracle.FP8_E4M3,
+                        np.repeat(p.block_tables, len(rows), axis=0), (qs + rows + 1).astype(np.int32),
+                        b.scale, b.k_scale, b.v_scale)
+    got = dev.prefill["out"][torch.as_tensor(rows, device="cuda")]
+    assert max_err(got, ref) <= TOL["fp8"]
+    # decode part of the same step
+    sample = np.arange(0, b.num_seqs, 16)
+    dref = oracle.decode_batch(b, kp, vp, seq_ids=sample)[sample]
+    assert max_err(dev.out[torch.as_tensor(sample, device="cuda")], dref) <= TOL["fp8"]
+
+
+def test_prefill_seq_len_mismatch_sets_error():
+    import paged_kv_cache_writes_gb300 as pa
+    from paged_kv_cache_writes_gb300.staging import DeviceBatch
+    b = W.prefill_batch("p", [(20, 10)], 8, 8, 64, 16, "bf16", seed=5)
+    dev = DeviceBatch(b, "cuda")
+    dev.run_setup()
+    dev.write_step()
+    dev.prefill["seq_lens"][0] += 1
+    dev.prefill_chunk()
+    assert pa.pa_get_device_error() == 4

@@ -29,6 +29,8 @@ sampling, chunked prefill with an fp8 KV cache); see ``CONFIGS``.
 """
 from __future__ import annotations
 
+import os
+from concurrent.futures import ThreadPoolExecutor
 from dataclasses import dataclass, field
 
 import numpy as np
@@ -42,9 +44,13 @@ def round_to_bits(x: np.ndarray, dtype: str) -> np.ndarray:
     if dtype == "f16":
         return x.astype(np.float16).view(np.uint16)
     if dtype == "bf16":
-        u = x.view(np.uint32).astype(np.uint64)
-        u = (u + 0x7FFF + ((u >> 16) & 1)) >> 16
-        return u.astype(np.uint16)
+        u = x.view(np.uint32)
+        r = u >> 16
+        r &= 1
+        r += 0x7FFF
+        r += u            # finite inputs only: no carry out of 32 bits below NaN
+        r >>= 16
+        return r.astype(np.uint16)
     raise ValueError(dtype)
 
 
@@ -57,13 +63,29 @@ def bits_to_f32(bits: np.ndarray, dtype: str) -> np.ndarray:
     raise ValueError(dtype)
 
 
-def _normal_bits(rng: np.random.Generator, shape, dtype: str, chunk: int = 1 << 26) -> np.ndarray:
-    """N(0,1) samples rounded to ``dtype`` bits, generated in chunks to bound memory."""
+_CHUNK = 1 << 22
+
+
+def _normal_bits(rng: np.random.Generator, shape, dtype: str) -> np.ndarray:
+    """N(0,1) samples rounded to ``dtype`` bits.  One 64-bit key is drawn from
+    ``rng``; chunk c of the output comes from default_rng([key, c]), so the
+    result does not depend on how many threads fill the chunks."""
     n = int(np.prod(shape))
     out = np.empty(n, dtype=np.uint16)
-    for s in range(0, n, chunk):
-        e = min(n, s + chunk)
-        out[s:e] = round_to_bits(rng.standard_normal(e - s, dtype=np.float32), dtype)
+    key = int(rng.integers(0, 2**63))
+
+    def fill(c):
+        s, e = c * _CHUNK, min(n, (c + 1) * _CHUNK)
+        g = np.random.default_rng([key, c])
+        out[s:e] = round_to_bits(g.standard_normal(e - s, dtype=np.float32), dtype)
+
+    nchunks = -(-n // _CHUNK)
+    if nchunks <= 1:
+        for c in range(nchunks):
+            fill(c)
+    else:
+        with ThreadPoolExecutor(min(nchunks, os.cpu_count() or 1)) as ex:
+            list(ex.map(fill, range(nchunks)))
     return out.reshape(shape)
 
 
@@ -209,7 +231,7 @@ def decode_batch(name: str, lens, num_q_heads: int, num_kv_heads: int, head_dim:
     is_new[(starts + lens - 1)[lens > 0]] = True
     ctx = WriteOp(k_all[~is_new], v_all[~is_new], slots[~is_new])
     new = WriteOp(k_all[is_new], v_all[is_new], slots[is_new])
-    ks, vs = _fp8_scales(k_all, v_all, src_dtype) if kv_dtype == "fp8" else (1.0, 1.0)
+    ks, vs = _fp8_scales([k_all], [v_all], src_dtype) if kv_dtype == "fp8" else (1.0, 1.0)
     return PagedBatch(name=name, num_q_heads=num_q_heads, num_kv_heads=num_kv_heads, head_dim=head_dim,
                       block_size=bs, src_dtype=src_dtype, kv_dtype=kv_dtype, num_blocks=nb, pad_block=pool.pad,
                       block_tables=bt, seq_lens=lens.astype(np.int32), q=q,
@@ -218,15 +240,23 @@ def decode_batch(name: str, lens, num_q_heads: int, num_kv_heads: int, head_dim:
                       blocks_unshared=needed)
 
 
-def _fp8_scales(k_bits: np.ndarray, v_bits: np.ndarray, src_dtype: str):
-    """Per-tensor scales amax(|x|) / 448 in fp32 (448 = largest E4M3 magnitude)."""
-    def one(bits):
-        amax = np.float32(0.0)
-        flat = bits.reshape(-1)
-        for s in range(0, flat.size, 1 << 26):
-            amax = max(amax, np.abs(bits_to_f32(flat[s:s + (1 << 26)], src_dtype)).max(initial=0.0))
+def _amax(bits: np.ndarray, src_dtype: str) -> np.float32:
+    """max |x| of finite 16-bit floats: the magnitude bits order like the values."""
+    m = np.uint16(0)
+    flat = bits.reshape(-1)
+    for s in range(0, flat.size, 1 << 26):
+        part = flat[s:s + (1 << 26)] & np.uint16(0x7FFF)
+        m = max(m, part.max(initial=0))
+    return bits_to_f32(np.array([m], np.uint16), src_dtype)[0]
+
+
+def _fp8_scales(k_parts, v_parts, src_dtype: str):
+    """Per-tensor scales amax(|x|) / 448 in fp32 (448 = largest E4M3 magnitude),
+    the amax taken over every token of the tensor (given as a list of parts)."""
+    def one(parts):
+        amax = max(_amax(p, src_dtype) for p in parts)
         return float(np.float32(amax) / np.float32(448.0)) if amax > 0 else 1.0
-    return one(k_bits), one(v_bits)
+    return one(k_parts), one(v_parts)
 
 
 def shared_prefix_batch(name: str = "shared-prefix sampling", num_prompts: int = 32, branches: int = 4,
@@ -333,7 +363,7 @@ def mixed_prefill_batch(name: str = "chunked-prefill mixed batch, fp8 KV", chunk
     step = WriteOp(np.concatenate([pk[q_start:], dk[is_new]]), np.concatenate([pv[q_start:], dv[is_new]]),
                    np.concatenate([pslots[q_start:], dslots[is_new]]))
     if kv_dtype == "fp8":
-        ks, vs = _fp8_scales(np.concatenate([dk, pk]), np.concatenate([dv, pv]), src_dtype)
+        ks, vs = _fp8_scales([dk, pk], [dv, pv], src_dtype)
     else:
         ks, vs = 1.0, 1.0
     pre = PrefillPart(q=q_chk, cu_q_lens=np.array([0, chunk], dtype=np.int32),
@@ -373,7 +403,7 @@ def prefill_batch(name: str, chunks, num_q_heads: int, num_kv_heads: int, head_d
     ctx = WriteOp(np.concatenate(ks), np.concatenate(vs), np.concatenate(sc))
     new = WriteOp(np.concatenate(kn), np.concatenate(vn), np.concatenate(sn))
     if kv_dtype == "fp8":
-        k_scale, v_scale = _fp8_scales(np.concatenate([ctx.k, new.k]), np.concatenate([ctx.v, new.v]), src_dtype)
+        k_scale, v_scale = _fp8_scales([ctx.k, new.k], [ctx.v, new.v], src_dtype)
     else:
         k_scale, v_scale = 1.0, 1.0
     cu = np.concatenate([[0], np.cumsum([c for _, c in chunks])]).astype(np.int32)
