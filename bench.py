@@ -42,7 +42,8 @@ def _peaks():
 
 
 def _config(b, extra=None):
-    cfg = {"workload": WORKLOAD, "num_seqs": b.num_seqs, "num_q_heads": b.num_q_heads,
+    name = WORKLOAD if b.num_seqs == 256 else f"{WORKLOAD} (reduced to {b.num_seqs} sequences)"
+    cfg = {"workload": name, "num_seqs": b.num_seqs, "num_q_heads": b.num_q_heads,
            "num_kv_heads": b.num_kv_heads, "head_dim": b.head_dim, "block_size": b.block_size,
            "kv_dtype": b.kv_dtype, "partition_size": b.partition_size or 512,
            "context_tokens": int(b.seq_lens.astype(np.int64).sum()), "max_seq_len": b.max_seq_len,
@@ -198,7 +199,7 @@ def run_ours(args):
     torch.cuda.set_device(local)
     dev_name = f"cuda:{local}"
 
-    b = W.cfg_llama70b()
+    b = W.cfg_llama70b(batch=args.batch)
     db = DeviceBatch(b, dev_name)
     db.run_setup()
     torch.cuda.synchronize()
@@ -307,6 +308,8 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
+    ap.add_argument("--batch", type=int, default=256,
+                    help="sequences in the decode batch (256 = the named workload; smaller only for profiling)")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")

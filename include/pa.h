@@ -68,7 +68,8 @@ typedef enum {
     PA_ERR_TIMEOUT = 5       /* a kernel's bounded wait on an async copy expired */
 } pa_status;
 
-typedef enum { PA_F16 = 0, PA_BF16 = 1, PA_FP8_E4M3 = 2 } pa_dtype;
+/* PA_F32 is accepted only as the dtype of an attention output. */
+typedef enum { PA_F16 = 0, PA_BF16 = 1, PA_FP8_E4M3 = 2, PA_F32 = 3 } pa_dtype;
 
 /* Shape and element type of one layer's K and V pools. */
 typedef struct {
@@ -168,7 +169,9 @@ PA_API size_t pa_decode_workspace_bytes(int32_t num_seqs, int32_t num_q_heads,
  *                  completes leaves it zero-filled again, so it can be reused
  *                  by later calls on the same stream (concurrent calls need
  *                  separate workspaces).
- *   out            device [num_seqs][num_q_heads][head_dim], dtype q_dtype
+ *   out            device [num_seqs][num_q_heads][head_dim]
+ *   out_dtype      q_dtype (rounded to nearest even from the fp32 result) or
+ *                  PA_F32 (the fp32 result itself)
  */
 PA_API pa_status pa_decode(const void *q, pa_dtype q_dtype, int32_t num_seqs,
                     int32_t num_q_heads, const void *k_cache,
@@ -176,7 +179,8 @@ PA_API pa_status pa_decode(const void *q, pa_dtype q_dtype, int32_t num_seqs,
                     const int32_t *block_tables, int32_t max_blocks_per_seq,
                     const int32_t *seq_lens, int32_t max_seq_len, float scale,
                     int32_t partition_size, void *workspace,
-                    size_t workspace_bytes, void *out, pa_stream_t stream);
+                    size_t workspace_bytes, void *out, pa_dtype out_dtype,
+                    pa_stream_t stream);
 
 /*
  * pa_prefill_chunk -- causal attention of prompt chunks over paged context
@@ -196,7 +200,8 @@ PA_API pa_status pa_decode(const void *q, pa_dtype q_dtype, int32_t num_seqs,
  *   q_start    device int32 [num_chunks]
  *   max_q_len  host upper bound of any chunk length; sizes the grid
  *   max_seq_len host upper bound of seq_lens
- *   out        device [total_q][num_q_heads][head_dim], dtype q_dtype
+ *   out        device [total_q][num_q_heads][head_dim], dtype out_dtype
+ *              (q_dtype or PA_F32, as for pa_decode)
  */
 PA_API pa_status pa_prefill_chunk(const void *q_chunk, pa_dtype q_dtype,
                            const int32_t *cu_q_lens, const int32_t *q_start,
@@ -206,7 +211,7 @@ PA_API pa_status pa_prefill_chunk(const void *q_chunk, pa_dtype q_dtype,
                            const int32_t *block_tables,
                            int32_t max_blocks_per_seq, const int32_t *seq_lens,
                            int32_t max_seq_len, float scale, void *out,
-                           pa_stream_t stream);
+                           pa_dtype out_dtype, pa_stream_t stream);
 
 /*
  * pa_get_device_error -- read and clear the current device's error word.

@@ -15,12 +15,12 @@ import os
 import torch
 
 __all__ = [
-    "PA_F16", "PA_BF16", "PA_FP8_E4M3", "PaError", "PaKvCache", "lib", "kv_cache_desc",
+    "PA_F16", "PA_BF16", "PA_FP8_E4M3", "PA_F32", "PaError", "PaKvCache", "lib", "kv_cache_desc",
     "pa_reshape_and_cache", "pa_copy_blocks", "pa_decode_workspace_bytes", "pa_decode",
     "pa_prefill_chunk", "pa_get_device_error", "pa_status_string",
 ]
 
-PA_F16, PA_BF16, PA_FP8_E4M3 = 0, 1, 2
+PA_F16, PA_BF16, PA_FP8_E4M3, PA_F32 = 0, 1, 2, 3
 STATUS_NAMES = {0: "PA_OK", 1: "PA_ERR_INVALID_ARG", 2: "PA_ERR_UNSUPPORTED", 3: "PA_ERR_CUDA",
                 4: "PA_ERR_DEVICE_CHECK", 5: "PA_ERR_TIMEOUT"}
 
@@ -57,9 +57,9 @@ def lib() -> ctypes.CDLL:
         L.pa_decode_workspace_bytes.argtypes = [I32, I32, I32, I32, I32, I32]
         L.pa_decode_workspace_bytes.restype = SZ
         L.pa_decode.argtypes = [P, ctypes.c_int, I32, I32, P, P, ctypes.POINTER(PaKvCache), P, I32, P, I32, F,
-                                I32, P, SZ, P, P]
+                                I32, P, SZ, P, ctypes.c_int, P]
         L.pa_prefill_chunk.argtypes = [P, ctypes.c_int, P, P, I32, I32, I32, P, P, ctypes.POINTER(PaKvCache), P,
-                                       I32, P, I32, F, P, P]
+                                       I32, P, I32, F, P, ctypes.c_int, P]
         L.pa_get_device_error.argtypes = [P, ctypes.POINTER(I32)]
         L.pa_status_string.argtypes = [ctypes.c_int]
         L.pa_status_string.restype = ctypes.c_char_p
@@ -77,6 +77,8 @@ def _dtype_code(t: torch.dtype) -> int:
         return PA_BF16
     if t in (torch.uint8, torch.float8_e4m3fn):
         return PA_FP8_E4M3
+    if t == torch.float32:
+        return PA_F32
     raise TypeError(f"unsupported dtype {t}")
 
 
@@ -142,7 +144,7 @@ def pa_decode(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor, cac
               block_tables: torch.Tensor, seq_lens: torch.Tensor, max_seq_len: int, scale: float,
               out: torch.Tensor, workspace: torch.Tensor | None = None, partition_size: int = 0,
               stream=None) -> None:
-    """q, out: [B, Hq, D]; block_tables int32 [B, max_blocks]; seq_lens int32 [B].
+    """q, out: [B, Hq, D] (out: q's dtype or float32); block_tables int32 [B, max_blocks]; seq_lens int32 [B].
     ``workspace``: uint8 tensor of >= pa_decode_workspace_bytes(...) bytes,
     zero-filled before its first use (None when that size is 0)."""
     B, hq, _ = q.shape
@@ -151,19 +153,20 @@ def pa_decode(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor, cac
     _ok(lib().pa_decode(_dev(q, "q"), _dtype_code(q.dtype), B, hq, _dev(k_cache, "k_cache"), _dev(v_cache, "v_cache"),
                         ctypes.byref(cache), _dev(block_tables, "block_tables"), block_tables.shape[1],
                         _dev(seq_lens, "seq_lens"), int(max_seq_len), float(scale), int(partition_size), ws_ptr,
-                        ws_bytes, _dev(out, "out"), _stream(stream)), "pa_decode")
+                        ws_bytes, _dev(out, "out"), _dtype_code(out.dtype), _stream(stream)), "pa_decode")
 
 
 def pa_prefill_chunk(q_chunk: torch.Tensor, cu_q_lens: torch.Tensor, q_start: torch.Tensor, max_q_len: int,
                      k_cache: torch.Tensor, v_cache: torch.Tensor, cache: PaKvCache, block_tables: torch.Tensor,
                      seq_lens: torch.Tensor, max_seq_len: int, scale: float, out: torch.Tensor,
                      stream=None) -> None:
-    """q_chunk, out: [total_q, Hq, D]; cu_q_lens int32 [n+1]; q_start, seq_lens int32 [n]."""
+    """q_chunk, out: [total_q, Hq, D] (out: q's dtype or float32); cu_q_lens int32 [n+1]; q_start, seq_lens int32 [n]."""
     _ok(lib().pa_prefill_chunk(_dev(q_chunk, "q_chunk"), _dtype_code(q_chunk.dtype), _dev(cu_q_lens, "cu_q_lens"),
                                _dev(q_start, "q_start"), q_start.shape[0], int(max_q_len), q_chunk.shape[1],
                                _dev(k_cache, "k_cache"), _dev(v_cache, "v_cache"), ctypes.byref(cache),
                                _dev(block_tables, "block_tables"), block_tables.shape[1], _dev(seq_lens, "seq_lens"),
-                               int(max_seq_len), float(scale), _dev(out, "out"), _stream(stream)),
+                               int(max_seq_len), float(scale), _dev(out, "out"), _dtype_code(out.dtype),
+                               _stream(stream)),
         "pa_prefill_chunk")
 
 

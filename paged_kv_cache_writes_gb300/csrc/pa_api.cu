@@ -179,7 +179,7 @@ pa_status pa_decode(const void *q, pa_dtype q_dtype, int32_t num_seqs, int32_t n
                     const int32_t *block_tables, int32_t max_blocks_per_seq,
                     const int32_t *seq_lens, int32_t max_seq_len, float scale,
                     int32_t partition_size, void *workspace, size_t workspace_bytes, void *out,
-                    pa_stream_t stream) {
+                    pa_dtype out_dtype, pa_stream_t stream) {
   pa_status st = check_cache(cache);
   if (st != PA_OK) return st;
   const pa_kv_cache &c = *cache;
@@ -187,6 +187,7 @@ pa_status pa_decode(const void *q, pa_dtype q_dtype, int32_t num_seqs, int32_t n
       max_blocks_per_seq <= 0 || partition_size < 0 || partition_size % 32 || !std::isfinite(scale))
     return PA_ERR_INVALID_ARG;
   if ((st = check_q_dtype(q_dtype, c)) != PA_OK) return st;
+  if (out_dtype != q_dtype && out_dtype != PA_F32) return PA_ERR_UNSUPPORTED;
   if (num_seqs == 0) return PA_OK;
   if (!q || !out || !block_tables || !seq_lens || !aligned(q, 16) || !aligned(out, 16) ||
       !aligned(block_tables, 4) || !aligned(seq_lens, 4))
@@ -215,6 +216,7 @@ pa_status pa_decode(const void *q, pa_dtype q_dtype, int32_t num_seqs, int32_t n
   const bool fp8 = c.kv_dtype == PA_FP8_E4M3;
   p.q_mult = scale * 1.4426950408889634f * (fp8 ? c.k_scale : 1.f);
   p.out_mult = fp8 ? c.v_scale : 1.f;
+  p.out_f32 = out_dtype == PA_F32;
   if (parts > 1) {
     const WorkspaceLayout w = decode_workspace_layout(num_seqs, num_q_heads, c.head_dim, parts);
     if (!workspace || !aligned(workspace, 256) || workspace_bytes < w.total)
@@ -239,7 +241,8 @@ pa_status pa_prefill_chunk(const void *q_chunk, pa_dtype q_dtype, const int32_t 
                            int32_t num_q_heads, const void *k_cache, const void *v_cache,
                            const pa_kv_cache *cache, const int32_t *block_tables,
                            int32_t max_blocks_per_seq, const int32_t *seq_lens,
-                           int32_t max_seq_len, float scale, void *out, pa_stream_t stream) {
+                           int32_t max_seq_len, float scale, void *out, pa_dtype out_dtype,
+                           pa_stream_t stream) {
   pa_status st = check_cache(cache);
   if (st != PA_OK) return st;
   const pa_kv_cache &c = *cache;
@@ -247,6 +250,7 @@ pa_status pa_prefill_chunk(const void *q_chunk, pa_dtype q_dtype, const int32_t 
       max_seq_len < 0 || max_blocks_per_seq <= 0 || !std::isfinite(scale))
     return PA_ERR_INVALID_ARG;
   if ((st = check_q_dtype(q_dtype, c)) != PA_OK) return st;
+  if (out_dtype != q_dtype && out_dtype != PA_F32) return PA_ERR_UNSUPPORTED;
   if (num_chunks == 0 || max_q_len == 0) return PA_OK;
   if (!q_chunk || !out || !cu_q_lens || !q_start || !block_tables || !seq_lens ||
       !aligned(q_chunk, 16) || !aligned(out, 16) || !aligned(cu_q_lens, 4) ||
@@ -275,6 +279,7 @@ pa_status pa_prefill_chunk(const void *q_chunk, pa_dtype q_dtype, const int32_t 
   const bool fp8 = c.kv_dtype == PA_FP8_E4M3;
   p.q_mult = scale * 1.4426950408889634f * (fp8 ? c.k_scale : 1.f);
   p.out_mult = fp8 ? c.v_scale : 1.f;
+  p.out_f32 = out_dtype == PA_F32;
   p.err = device_error_word();
   PoolMaps maps;
   if (!p.err || !encode_pool_map(&maps.k, k_cache, c) || !encode_pool_map(&maps.v, v_cache, c))

@@ -104,9 +104,11 @@ __device__ __forceinline__ void load8(const uint8_t *tile, int t, int c, float2 
   }
 }
 
+// Output element: fp32 as computed, or rounded to the query dtype.
 template <typename QT>
-__device__ __forceinline__ void store_out(QT *dst, float x) {
-  *dst = Elem<QT>::from_f32(x);
+__device__ __forceinline__ void store_out(void *out, int64_t idx, bool f32, float x) {
+  if (f32) static_cast<float *>(out)[idx] = x;
+  else static_cast<QT *>(out)[idx] = Elem<QT>::from_f32(x);
 }
 
 template <typename KV, typename QT, int D, int HPC>
@@ -160,10 +162,11 @@ __global__ void __launch_bounds__(Geo<KV, D>::kThreads)
     L = L < 0 ? 0 : (int)cap;
   }
   const int nparts = (L + p.partition_size - 1) / p.partition_size;
-  QT *out_row = static_cast<QT *>(p.out) + ((int64_t)row * p.num_q_heads + h0) * D;
+  const int64_t out_row = ((int64_t)row * p.num_q_heads + h0) * D;  // element index
+  const bool out_f32 = p.out_f32 != 0;
   if (L == 0) {
     if (part == 0)
-      for (int e = tid; e < HPC * D; e += blockDim.x) store_out(out_row + e, 0.f);
+      for (int e = tid; e < HPC * D; e += blockDim.x) store_out<QT>(p.out, out_row + e, out_f32, 0.f);
     return;
   }
   if (part >= nparts) return;
@@ -425,7 +428,7 @@ __global__ void __launch_bounds__(Geo<KV, D>::kThreads)
       l += wt * mg_l[w * HPC + h];
     }
     if (!split) {
-      store_out(out_row + e, l > 0.f ? a / l * p.out_mult : 0.f);
+      store_out<QT>(p.out, out_row + e, out_f32, l > 0.f ? a / l * p.out_mult : 0.f);
     } else {
       const int64_t slot = (ws_head + h) * p.max_partitions + part;
       p.ws_acc[slot * D + d] = a;
@@ -458,7 +461,7 @@ __global__ void __launch_bounds__(Geo<KV, D>::kThreads)
       a += wt * __ldcg(&p.ws_acc[(base + q) * D + d]);
       l += wt * ml.y;
     }
-    store_out(out_row + e, l > 0.f ? a / l * p.out_mult : 0.f);
+    store_out<QT>(p.out, out_row + e, out_f32, l > 0.f ? a / l * p.out_mult : 0.f);
   }
 }
 

@@ -34,9 +34,10 @@ def to_bits(t: torch.Tensor) -> np.ndarray:
 
 
 class DeviceBatch:
-    """A ``workloads.PagedBatch`` resident on one GPU."""
+    """A ``workloads.PagedBatch`` resident on one GPU.  ``out_dtype`` "f32"
+    keeps the attention outputs in fp32; "q" stores them in the query dtype."""
 
-    def __init__(self, b, device: str | torch.device = "cuda"):
+    def __init__(self, b, device: str | torch.device = "cuda", out_dtype: str = "f32"):
         self.b = b
         self.device = torch.device(device)
         dev = self.device
@@ -58,7 +59,8 @@ class DeviceBatch:
         self.q = to_device(b.q, b.src_dtype, dev)
         self.block_tables = torch.from_numpy(np.ascontiguousarray(b.block_tables)).to(dev)
         self.seq_lens = torch.from_numpy(np.ascontiguousarray(b.seq_lens)).to(dev)
-        self.out = torch.empty_like(self.q)
+        odt = torch.float32 if out_dtype == "f32" else self.q.dtype
+        self.out = torch.empty(self.q.shape, dtype=odt, device=dev)
         ws = pa_decode_workspace_bytes(b.num_seqs, b.num_q_heads, b.num_kv_heads, b.head_dim,
                                        int(b.seq_lens.max()) if b.num_seqs else 0, b.partition_size)
         self.workspace = torch.zeros(ws, dtype=torch.uint8, device=dev) if ws else None
@@ -74,7 +76,7 @@ class DeviceBatch:
                 max_q_len=int(np.diff(p.cu_q_lens).max()) if len(p.q_start) else 0,
                 max_seq_len=int(p.seq_lens.max()) if len(p.seq_lens) else 0,
             )
-            self.prefill["out"] = torch.empty_like(self.prefill["q"])
+            self.prefill["out"] = torch.empty(self.prefill["q"].shape, dtype=odt, device=dev)
 
     def _write_tensors(self, op):
         return (to_device(op.k, self.b.src_dtype, self.device), to_device(op.v, self.b.src_dtype, self.device),

@@ -67,10 +67,11 @@ FAKE = 0x10000  # a 16-byte aligned non-null address; never dereferenced on thes
 
 def _decode(lib, desc, **kw):
     a = dict(q=FAKE, q_dtype=1, num_seqs=4, num_q_heads=32, k=FAKE, v=FAKE, bt=FAKE, mb=8, sl=FAKE, msl=100,
-             scale=0.1, ps=0, ws=None, wsb=0, out=FAKE)
+             scale=0.1, ps=0, ws=None, wsb=0, out=FAKE, odt=1)
     a.update(kw)
     return lib.pa_decode(a["q"], a["q_dtype"], a["num_seqs"], a["num_q_heads"], a["k"], a["v"], ctypes.byref(desc),
-                         a["bt"], a["mb"], a["sl"], a["msl"], a["scale"], a["ps"], a["ws"], a["wsb"], a["out"], None)
+                         a["bt"], a["mb"], a["sl"], a["msl"], a["scale"], a["ps"], a["ws"], a["wsb"], a["out"], a["odt"],
+                         None)
 
 
 @pytest.mark.parametrize("kw,desc_kw,want", [
@@ -84,6 +85,9 @@ def _decode(lib, desc, **kw):
     (dict(scale=float("nan")), {}, 1),
     (dict(msl=2000, ws=None), {}, 1),                           # split-KV needs a workspace
     (dict(q_dtype=0), {}, 2),                                   # f16 q with a bf16 cache
+    (dict(odt=0), {}, 2),                                       # out must be q dtype or f32
+    (dict(odt=2), {}, 2),
+    (dict(odt=3, num_seqs=0), {}, 0),                           # f32 out accepted
     ({}, dict(head_dim=96), 2),
     ({}, dict(block_size=8), 2),
     ({}, dict(kv_dtype=7), 2),
@@ -121,13 +125,14 @@ def test_copy_blocks_validation(lib):
 def test_prefill_validation(lib):
     d = _desc()
     f = lib.pa_prefill_chunk
-    ok = (FAKE, 1, FAKE, FAKE, 1, 64, 32, FAKE, FAKE, ctypes.byref(d), FAKE, 8, FAKE, 128, 0.1, FAKE, None)
+    ok = (FAKE, 1, FAKE, FAKE, 1, 64, 32, FAKE, FAKE, ctypes.byref(d), FAKE, 8, FAKE, 128, 0.1, FAKE, 3, None)
     assert f(*ok[:4], 0, *ok[5:]) == 0                      # no chunks
     assert f(*ok[:5], 0, *ok[6:]) == 0                      # empty chunks
     assert f(*ok[:4], -1, *ok[5:]) == 1
     assert f(*ok[:6], 31, *ok[7:]) == 1                     # Hq % Hkv
     assert f(ok[0], 0, *ok[2:]) == 2                        # f16 q, bf16 cache
     assert f(*ok[:2], None, *ok[3:]) == 1
+    assert f(*ok[:16], 2, None) == 2                        # fp8 output
 
 
 def test_workspace_size(lib):

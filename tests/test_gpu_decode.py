@@ -11,7 +11,7 @@ import torch
 
 import oracle
 import workloads as W
-from _gpu import TOL, max_err, oracle_pools, run_gpu
+from _gpu import TOL, max_err, oracle_pools, rounded_excess, run_gpu
 
 pytestmark = pytest.mark.gpu
 
@@ -53,10 +53,22 @@ def test_partition_sizes_agree(ps):
 
 def test_single_token_context_returns_v_exactly():
     b = W.decode_batch("one", [1] * 9, 16, 4, 128, 32, "bf16", seed=32)
-    dev = run_gpu(b)
+    dev = run_gpu(b, out_dtype="q")
     v = torch.from_numpy(b.step_write.v.view(np.int16)).cuda().view(torch.bfloat16)   # [B, Hkv, D]
     want = v.repeat_interleave(4, dim=1)
     assert torch.equal(dev.out.view(torch.int16), want.contiguous().view(torch.int16))
+
+
+@pytest.mark.parametrize("src,kv", [("bf16", "bf16"), ("f16", "f16"), ("bf16", "fp8")])
+def test_query_dtype_outputs(src, kv):
+    """Outputs stored in the query dtype: within the tolerance plus half an
+    ulp of the stored value (the round-to-nearest-even storage step)."""
+    b = W.decode_batch("q", EDGE_LENS, 32, 8, 128, 16, src, kv_dtype=kv, seed=36, partition_size=512)
+    dev = run_gpu(b, out_dtype="q")
+    assert dev.out.dtype != torch.float32
+    kp, vp = oracle_pools(b)
+    ref = oracle.decode_batch(b, kp, vp)
+    assert rounded_excess(dev.out, ref, src, TOL[kv]) <= 0
 
 
 def test_zero_length_sequences():

@@ -11,7 +11,7 @@ import torch
 
 import oracle
 import workloads as W
-from _gpu import TOL, max_err, oracle_pools, run_gpu
+from _gpu import TOL, max_err, oracle_pools, rounded_excess, run_gpu
 
 pytestmark = pytest.mark.gpu
 
@@ -25,6 +25,14 @@ def test_prefill_small(src, kv, hq, hkv, d, bs):
     kp, vp = oracle_pools(b)
     ref = oracle.prefill_batch(b, kp, vp)
     assert max_err(dev.prefill["out"], ref) <= TOL[kv]
+
+
+def test_prefill_query_dtype_output():
+    b = W.prefill_batch("p", [(0, 37), (100, 64)], 32, 8, 128, 16, "bf16", seed=9)
+    dev = run_gpu(b, out_dtype="q")
+    kp, vp = oracle_pools(b)
+    ref = oracle.prefill_batch(b, kp, vp)
+    assert rounded_excess(dev.prefill["out"], ref, "bf16", TOL["bf16"]) <= 0
 
 
 def test_mixed_fp8_prefill_sampled_rows():
