@@ -130,12 +130,13 @@ PA_API pa_status pa_copy_blocks(void *k_cache, void *v_cache, const pa_kv_cache 
                          pa_stream_t stream);
 
 /*
- * pa_decode_workspace_bytes -- device workspace pa_decode needs for split-KV.
+ * pa_decode_workspace_bytes -- device workspace pa_decode needs: a work list
+ * of (sequence, partition) items built on the device each call, and, when a
+ * sequence can span several partitions, the split-KV partial results.
  *
- * partition_size 0 selects the library default (512 tokens).  Returns 0 when
- * no sequence can span more than one partition (max_seq_len <= partition
- * size); then pa_decode accepts a NULL workspace.  Returns 0 as well for
- * invalid arguments, which pa_decode then reports.
+ * partition_size 0 selects the library default (512 tokens); larger values
+ * are treated as 512.  Returns 0 for invalid arguments (which pa_decode then
+ * reports).
  */
 PA_API size_t pa_decode_workspace_bytes(int32_t num_seqs, int32_t num_q_heads,
                                  int32_t num_kv_heads, int32_t head_dim,
@@ -161,14 +162,14 @@ PA_API size_t pa_decode_workspace_bytes(int32_t num_seqs, int32_t num_q_heads,
  *   seq_lens       device int32 [num_seqs], each <= max_seq_len and
  *                  <= max_blocks_per_seq * block_size
  *   max_seq_len    host upper bound of seq_lens; sizes the grid
- *   partition_size 0 = default (512); else a multiple of 32 tokens.  A
- *                  sequence longer than one partition is split across CTAs
- *                  and the pieces are merged with a log-sum-exp combine.
+ *   partition_size 0 = default (512); else a multiple of 32 tokens (values
+ *                  above 512 act as 512).  A sequence longer than one
+ *                  partition is split across workers and the pieces are
+ *                  merged with a log-sum-exp combine.
  *   workspace      device, >= pa_decode_workspace_bytes(...) bytes, 256-byte
- *                  aligned, ZERO-FILLED before its first use; every call that
- *                  completes leaves it zero-filled again, so it can be reused
- *                  by later calls on the same stream (concurrent calls need
- *                  separate workspaces).
+ *                  aligned.  Its contents on entry are ignored (each call
+ *                  rebuilds them), so one workspace serves every call on a
+ *                  stream; calls that may overlap need separate workspaces.
  *   out            device [num_seqs][num_q_heads][head_dim]
  *   out_dtype      q_dtype (rounded to nearest even from the fp32 result) or
  *                  PA_F32 (the fp32 result itself)

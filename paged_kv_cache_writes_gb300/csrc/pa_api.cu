@@ -10,6 +10,7 @@
 #include <mutex>
 
 #include "pa_common.cuh"
+#include "pa_decode.cuh"
 #include "pa_internal.h"
 
 namespace pa {
@@ -110,12 +111,22 @@ cudaError_t dispatch_attention(pa_dtype q_dtype, const pa_kv_cache &c, const Att
 WorkspaceLayout decode_workspace_layout(int64_t rows, int64_t num_q_heads, int64_t head_dim,
                                         int64_t max_partitions) {
   WorkspaceLayout w;
-  w.acc_off = 0;
-  w.ml_off = round256((size_t)(rows * num_q_heads * max_partitions * head_dim * 4));
-  w.cnt_off = w.ml_off + round256((size_t)(rows * num_q_heads * max_partitions * 8));
+  w.hdr_off = 0;
+  w.items_off = round256(sizeof(DecodeHeader));
+  w.acc_off = w.items_off + round256((size_t)(rows * max_partitions * 4));
+  const int64_t partials = max_partitions > 1 ? rows * num_q_heads * max_partitions : 0;
+  w.ml_off = w.acc_off + round256((size_t)(partials * head_dim * 4));
+  w.cnt_off = w.ml_off + round256((size_t)(partials * 8));
   w.total = w.cnt_off + round256((size_t)(rows * num_q_heads * 4));
   return w;
 }
+
+namespace {
+int effective_partition(int32_t requested) {
+  const int ps = requested ? requested : kDefaultPartition;
+  return ps < kDefaultPartition ? ps : kDefaultPartition;  // a unit spans at most 32 blocks
+}
+}  // namespace
 
 }  // namespace pa
 
@@ -167,10 +178,10 @@ size_t pa_decode_workspace_bytes(int32_t num_seqs, int32_t num_q_heads, int32_t 
   if (num_seqs < 0 || num_q_heads <= 0 || num_kv_heads <= 0 || head_dim <= 0 || max_seq_len < 0 ||
       partition_size < 0 || num_q_heads % num_kv_heads)
     return 0;
-  const int ps = partition_size ? partition_size : kDefaultPartition;
-  if (ps % 32) return 0;
-  const int64_t parts = ((int64_t)max_seq_len + ps - 1) / ps;
-  if (parts <= 1 || parts > kMaxPartitions) return 0;
+  if (partition_size % 32 || num_seqs > kMaxDecodeRows) return 0;
+  const int ps = effective_partition(partition_size);
+  const int64_t parts = std::max<int64_t>(1, ((int64_t)max_seq_len + ps - 1) / ps);
+  if (parts > kMaxPartitions) return 0;
   return decode_workspace_layout(num_seqs, num_q_heads, head_dim, parts).total;
 }
 
@@ -193,22 +204,28 @@ pa_status pa_decode(const void *q, pa_dtype q_dtype, int32_t num_seqs, int32_t n
       !aligned(block_tables, 4) || !aligned(seq_lens, 4))
     return PA_ERR_INVALID_ARG;
   if ((st = check_pools(k_cache, v_cache)) != PA_OK) return st;
-  if (num_q_heads > 65535) return PA_ERR_UNSUPPORTED;
+  if (num_seqs > kMaxDecodeRows) return PA_ERR_UNSUPPORTED;
 
-  const int ps = partition_size ? partition_size : kDefaultPartition;
+  const int ps = effective_partition(partition_size);
   const int64_t parts64 = std::max<int64_t>(1, ((int64_t)max_seq_len + ps - 1) / ps);
   if (parts64 > kMaxPartitions) return PA_ERR_UNSUPPORTED;
   const int parts = (int)parts64;
+  const int hpc = heads_per_cta(num_q_heads / c.num_kv_heads);
+  if ((double)num_seqs * parts * num_q_heads / hpc >= 2147483647.0) return PA_ERR_UNSUPPORTED;
+  const WorkspaceLayout w = decode_workspace_layout(num_seqs, num_q_heads, c.head_dim, parts);
+  if (!workspace || !aligned(workspace, 256) || workspace_bytes < w.total) return PA_ERR_INVALID_ARG;
 
-  AttnParams p{};
+  DecodeParams p{};
   p.q = q;
   p.out = out;
+  p.out_f32 = out_dtype == PA_F32;
   p.block_tables = block_tables;
   p.max_blocks_per_seq = max_blocks_per_seq;
   p.seq_lens = seq_lens;
+  p.num_seqs = num_seqs;
   p.num_q_heads = num_q_heads;
   p.num_kv_heads = c.num_kv_heads;
-  p.heads_per_cta = heads_per_cta(num_q_heads / c.num_kv_heads);
+  p.groups = (num_q_heads / c.num_kv_heads) / hpc;
   p.block_size = c.block_size;
   p.num_blocks = c.num_blocks;
   p.partition_size = ps;
@@ -216,24 +233,23 @@ pa_status pa_decode(const void *q, pa_dtype q_dtype, int32_t num_seqs, int32_t n
   const bool fp8 = c.kv_dtype == PA_FP8_E4M3;
   p.q_mult = scale * 1.4426950408889634f * (fp8 ? c.k_scale : 1.f);
   p.out_mult = fp8 ? c.v_scale : 1.f;
-  p.out_f32 = out_dtype == PA_F32;
-  if (parts > 1) {
-    const WorkspaceLayout w = decode_workspace_layout(num_seqs, num_q_heads, c.head_dim, parts);
-    if (!workspace || !aligned(workspace, 256) || workspace_bytes < w.total)
-      return PA_ERR_INVALID_ARG;
-    char *ws = static_cast<char *>(workspace);
-    p.ws_acc = reinterpret_cast<float *>(ws + w.acc_off);
-    p.ws_ml = reinterpret_cast<float2 *>(ws + w.ml_off);
-    p.ws_count = reinterpret_cast<int32_t *>(ws + w.cnt_off);
-  }
+  char *ws = static_cast<char *>(workspace);
+  p.hdr = reinterpret_cast<DecodeHeader *>(ws + w.hdr_off);
+  p.items = reinterpret_cast<int32_t *>(ws + w.items_off);
+  p.ws_acc = reinterpret_cast<float *>(ws + w.acc_off);
+  p.ws_ml = reinterpret_cast<float2 *>(ws + w.ml_off);
+  p.ws_count = reinterpret_cast<int32_t *>(ws + w.cnt_off);
   p.err = device_error_word();
   PoolMaps maps;
   if (!p.err || !encode_pool_map(&maps.k, k_cache, c) || !encode_pool_map(&maps.v, v_cache, c))
     return PA_ERR_CUDA;
-  return dispatch_attention(q_dtype, c, p, maps, num_seqs, reinterpret_cast<cudaStream_t>(stream)) ==
-                 cudaSuccess
-             ? PA_OK
-             : PA_ERR_CUDA;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  cudaError_t e;
+  if (c.kv_dtype == PA_BF16) e = launch_decode_bf16(p, hpc, maps, c.head_dim, s);
+  else if (c.kv_dtype == PA_F16) e = launch_decode_f16(p, hpc, maps, c.head_dim, s);
+  else if (q_dtype == PA_BF16) e = launch_decode_fp8_bf16q(p, hpc, maps, c.head_dim, s);
+  else e = launch_decode_fp8_f16q(p, hpc, maps, c.head_dim, s);
+  return e == cudaSuccess ? PA_OK : PA_ERR_CUDA;
 }
 
 pa_status pa_prefill_chunk(const void *q_chunk, pa_dtype q_dtype, const int32_t *cu_q_lens,

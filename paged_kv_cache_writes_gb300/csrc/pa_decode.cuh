@@ -1,0 +1,610 @@
+// pa_decode.cuh -- paged decode on CUDA cores, persistent and warp-granular.
+//
+// What it computes: for each sequence (row) and query head h,
+//   out[row][h] = sum_p softmax_p(scale * q[row][h] . K[p][g]) V[p][g],
+// g = h / (Hq / Hkv), K/V gathered through the block table ("Inside vLLM
+// Architecture", sections "Architectural Anatomy: PagedAttention Virtual
+// Memory Paging" and "CUDA Shared Memory Optimization in PagedAttention";
+// exact attention per its "Semantic FAQ Section").
+//
+// Work decomposition.  A row of L tokens is cut into partitions of PS tokens
+// (split-KV).  A *unit* is (row, partition, KV head, group of HPC query
+// heads); the HPC heads share every K/V byte read.  A one-CTA plan kernel
+// lists the non-empty (row, partition) items -- full partitions first, then
+// the ragged last partitions -- so no work slot is wasted on the tail of a
+// short row.  The decode kernel is persistent (one CTA per SM); each of its
+// warps is an independent worker that claims units from an atomic cursor.
+//
+// Inside a warp:
+//  * lane 0 keeps a ring of kSlots 16-token K/V tiles in flight with 2D
+//    bulk-tensor (TMA) copies (128-byte swizzle), running ahead across the
+//    boundary into the next claimed unit; the unit's block ids sit one per
+//    lane in a register (one coalesced load per unit);
+//  * q for the next unit arrives by a 1D bulk copy while the current unit
+//    computes, and is widened to fp32, pre-scaled by scale*log2(e);
+//  * Q.K^T: lane = (token t of the tile, half of the heads), the whole head
+//    dim in registers, q broadcast from shared memory, packed fp32x2 FMAs;
+//  * online softmax in the log2 domain with a lazy reference maximum: the
+//    accumulators are rescaled only when a tile's maximum exceeds the
+//    reference by more than kRescaleLog2 (2^8 headroom in fp32), which
+//    leaves the result exact and skips nearly every rescale;
+//  * P.V: lane = (token sub-step, 8 output elements), all HPC heads;
+//  * a unit of a split row writes (acc, max, sum) to the workspace; the last
+//    unit of the row to arrive (atomic counter, reset after use) combines
+//    the partitions, sum_p 2^(m_p-M) acc_p / sum_p 2^(m_p-M) l_p.
+#pragma once
+
+#include "pa_attention.cuh"
+
+namespace pa {
+
+constexpr float kRescaleLog2 = 8.f;
+
+// Workspace header (first 256 bytes), written by the plan kernel.
+struct DecodeHeader {
+  int32_t next_unit;   // dynamic scheduling cursor
+  int32_t num_items;   // (row, partition) items listed
+  int32_t pad[62];
+};
+
+template <typename KV, int D, int HPC>
+struct DecGeo {
+  using G = Geo<KV, D>;
+  static constexpr int kStageTok = 16;
+  static constexpr int kStageBytes = G::kStageBytes;
+  static constexpr int kSlots = kStageBytes >= 8192 ? 3 : kStageBytes >= 4096 ? 6 : 8;
+  static constexpr int kQsOff = kSlots * kStageBytes;               // fp32 [D/2][HPC][2]
+  static constexpr int kQrawOff = kQsOff + D * HPC * 4;             // raw q, HPC x D
+  static constexpr int kPOff = kQrawOff + HPC * D * 2;              // float2 [16][HPC]
+  static constexpr int kBarOff = kPOff + kStageTok * HPC * 8;       // full[kSlots], qbar
+  static constexpr int kWarpBytes = (kBarOff + (kSlots + 1) * 8 + 1023) / 1024 * 1024;
+  static constexpr int kNW0 = (226 * 1024) / kWarpBytes;
+  static constexpr int kNW = kNW0 > 8 ? 8 : kNW0;                   // warps (workers) per CTA
+  static constexpr int kSmem = kNW * kWarpBytes + 1024;
+  static_assert(kNW >= 1, "per-warp shared memory too large");
+};
+
+struct DecodeParams {
+  const void *q;
+  void *out;
+  int32_t out_f32;
+  const int32_t *block_tables;
+  int32_t max_blocks_per_seq;
+  const int32_t *seq_lens;
+  int32_t num_seqs;
+  int32_t num_q_heads;
+  int32_t num_kv_heads;
+  int32_t groups;            // query-head groups per KV head (G / HPC)
+  int32_t block_size;
+  int64_t num_blocks;
+  int32_t partition_size;    // <= 32 * block_size, multiple of 32
+  int32_t max_partitions;
+  float q_mult;
+  float out_mult;
+  DecodeHeader *hdr;
+  int32_t *items;            // (row << 12) | partition
+  float *ws_acc;             // [rows][Hq][max_partitions][D]
+  float2 *ws_ml;             // [rows][Hq][max_partitions]
+  int32_t *ws_count;         // [rows][Hq]
+  int32_t *err;
+};
+
+// Clamp a row's length to what its block table and the partition count can
+// address, recording the violation.
+__device__ __forceinline__ int checked_len(const DecodeParams &p, int row, bool report) {
+  int L = __ldg(p.seq_lens + row);
+  const int64_t cap = min((int64_t)p.max_blocks_per_seq * p.block_size,
+                          (int64_t)p.max_partitions * p.partition_size);
+  if (L < 0 || L > cap) {
+    if (report) record_error(p.err, PA_ERR_DEVICE_CHECK);
+    L = L < 0 ? 0 : (int)cap;
+  }
+  return L;
+}
+
+// One CTA: list (row, partition) items -- every full partition first, then
+// each row's ragged last partition (an empty row lists one item of zero
+// tokens, whose unit writes a zero output) -- and reset the scheduling
+// cursor and the split-KV arrival counters.
+template <int kUnused>
+__global__ void __launch_bounds__(1024) decode_plan_kernel(DecodeParams p) {
+  __shared__ int s_full[1024];
+  __shared__ int s_part[1024];
+  const int tid = threadIdx.x;
+  for (int64_t i = tid; i < (int64_t)p.num_seqs * p.num_q_heads; i += blockDim.x) p.ws_count[i] = 0;
+  // pass 0: total number of full partitions (the ragged ones are listed after them)
+  int tot_full = 0;
+  for (int r0 = 0; r0 < p.num_seqs; r0 += 1024) {
+    const int r = r0 + tid;
+    s_full[tid] = r < p.num_seqs ? checked_len(p, r, true) / p.partition_size : 0;
+    __syncthreads();
+    for (int off = 512; off > 0; off >>= 1) {
+      if (tid < off) s_full[tid] += s_full[tid + off];
+      __syncthreads();
+    }
+    tot_full += s_full[0];
+    __syncthreads();
+  }
+  int base_full = 0, base_part = tot_full;
+  for (int r0 = 0; r0 < p.num_seqs; r0 += 1024) {
+    const int r = r0 + tid;
+    const int L = r < p.num_seqs ? checked_len(p, r, false) : 0;
+    const int nfull = r < p.num_seqs ? L / p.partition_size : 0;
+    const int npart = r < p.num_seqs && (L % p.partition_size != 0 || L == 0) ? 1 : 0;
+    s_full[tid] = nfull;
+    s_part[tid] = npart;
+    __syncthreads();
+    for (int off = 1; off < 1024; off <<= 1) {  // inclusive scans
+      const int af = tid >= off ? s_full[tid - off] : 0;
+      const int ap = tid >= off ? s_part[tid - off] : 0;
+      __syncthreads();
+      s_full[tid] += af;
+      s_part[tid] += ap;
+      __syncthreads();
+    }
+    const int ex_full = s_full[tid] - nfull, ex_part = s_part[tid] - npart;
+    for (int q = 0; q < nfull; ++q) p.items[base_full + ex_full + q] = (r << 12) | q;
+    if (npart) p.items[base_part + ex_part] = (r << 12) | nfull;
+    const int add_full = s_full[1023], add_part = s_part[1023];
+    __syncthreads();
+    base_full += add_full;
+    base_part += add_part;
+  }
+  if (tid == 0) {
+    p.hdr->num_items = base_part;
+    p.hdr->next_unit = 0;
+  }
+}
+
+// A claimed unit, replicated in every lane (blk: this lane's block id).
+struct Unit {
+  int valid, row, kvh, h0, part, tok_begin, tok_end, nst, nparts;
+  int32_t blk;
+};
+
+template <typename KV, int D, int HPC>
+__device__ __forceinline__ Unit claim_unit(const DecodeParams &p, int total_units, int lane) {
+  Unit u;
+  int id = 0;
+  if (lane == 0) id = atomicAdd(&p.hdr->next_unit, 1);
+  id = __shfl_sync(0xffffffffu, id, 0);
+  u.valid = id < total_units;
+  u.blk = -1;
+  if (!u.valid) return u;
+  const int hgt = p.num_kv_heads * p.groups;
+  const int item = __ldg(p.items + id / hgt);
+  const int hs = id % hgt;
+  u.row = item >> 12;
+  u.part = item & 4095;
+  u.kvh = hs / p.groups;
+  u.h0 = u.kvh * (p.num_q_heads / p.num_kv_heads) + (hs % p.groups) * HPC;
+  const int L = checked_len(p, u.row, false);
+  u.nparts = max(1, (L + p.partition_size - 1) / p.partition_size);  // an empty row: one empty unit
+  u.tok_begin = u.part * p.partition_size;
+  u.tok_end = min(L, u.tok_begin + p.partition_size);
+  u.nst = (u.tok_end - u.tok_begin + 15) >> 4;
+  const int nblk = (u.tok_end - u.tok_begin + p.block_size - 1) / p.block_size;
+  const int lb = u.tok_begin / p.block_size + lane;
+  if (lane < nblk && lb < p.max_blocks_per_seq)
+    u.blk = __ldg(p.block_tables + (int64_t)u.row * p.max_blocks_per_seq + lb);
+  return u;
+}
+
+__device__ __forceinline__ void fence_proxy_async_smem() {
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+__device__ __forceinline__ void bulk_load_1d(void *smem_dst, const void *gsrc, uint32_t bytes,
+                                             uint64_t *bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cta.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+          smem_u32(smem_dst)),
+      "l"(reinterpret_cast<uint64_t>(gsrc)), "r"(bytes), "r"(smem_u32(bar))
+      : "memory");
+}
+
+template <typename KV, typename QT, int D, int HPC>
+__global__ void __launch_bounds__(DecGeo<KV, D, HPC>::kNW * 32, 1)
+    paged_decode_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap tmap_k,
+                        const __grid_constant__ CUtensorMap tmap_v) {
+  using G = Geo<KV, D>;
+  using DG = DecGeo<KV, D, HPC>;
+  constexpr int S = DG::kSlots;
+  constexpr int HH = HPC >= 2 ? HPC / 2 : 1;
+  const float kNegInf = -__int_as_float(0x7f800000);
+
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                              ~uintptr_t(1023));
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  uint8_t *wbase = smem + warp * DG::kWarpBytes;
+  float *q_s = reinterpret_cast<float *>(wbase + DG::kQsOff);
+  QT *q_raw = reinterpret_cast<QT *>(wbase + DG::kQrawOff);
+  float2 *p_s = reinterpret_cast<float2 *>(wbase + DG::kPOff);
+  uint64_t *full = reinterpret_cast<uint64_t *>(wbase + DG::kBarOff);
+  uint64_t *qbar = full + S;
+
+  if (lane == 0) {
+    for (int s = 0; s < S; ++s) mbar_init(&full[s], 1);
+    mbar_init(qbar, 1);
+    fence_mbar_init();
+    if (warp == 0) {
+      prefetch_tensor_map(&tmap_k);
+      prefetch_tensor_map(&tmap_v);
+    }
+  }
+  __syncwarp();
+
+  const int total_units = __ldcg(&p.hdr->num_items) * p.num_kv_heads * p.groups;
+  const int bs = p.block_size;
+
+  // --------------------------------------------------------------- producer side
+  auto issue_q = [&](const Unit &u) {
+    if (lane == 0) {
+      fence_proxy_async_smem();
+      constexpr uint32_t bytes = HPC * D * sizeof(QT);
+      mbar_arrive_expect_tx(qbar, bytes);
+      bulk_load_1d(q_raw, static_cast<const QT *>(p.q) + ((int64_t)u.row * p.num_q_heads + u.h0) * D,
+                   bytes, qbar);
+    }
+  };
+  auto issue_stage = [&](const Unit &u, int st, uint32_t g) {
+    const int slot = g % S;
+    const int tok = u.tok_begin + st * 16;
+    const int32_t blk = __shfl_sync(0xffffffffu, u.blk, (tok - u.tok_begin) / bs);
+    if (lane == 0) {
+      fence_proxy_async_smem();
+      if (blk < 0 || blk >= p.num_blocks) {
+        record_error(p.err, PA_ERR_DEVICE_CHECK);
+        mbar_arrive(&full[slot]);
+      } else {
+        mbar_arrive_expect_tx(&full[slot], G::kStageBytes);
+        const int32_t y = (blk * p.num_kv_heads + u.kvh) * bs + (tok % bs);
+        uint8_t *st_base = wbase + slot * G::kStageBytes;
+#pragma unroll
+        for (int pn = 0; pn < G::kPanels; ++pn) {
+          tma_load_2d(st_base + pn * G::kPanelTileBytes, &tmap_k, &full[slot], pn * G::kPanelElems, y);
+          tma_load_2d(st_base + G::kTileBytes + pn * G::kPanelTileBytes, &tmap_v, &full[slot],
+                      pn * G::kPanelElems, y);
+        }
+      }
+    }
+  };
+
+  Unit U0 = claim_unit<KV, D, HPC>(p, total_units, lane);
+  Unit U1;
+  U1.valid = 0;
+  U1.blk = -1;
+  uint32_t g_issue = 0, g_comp = 0, qphase = 0;
+  int cur_u = 0, cur_s = 0;  // issue cursor: unit (0 = U0, 1 = U1), stage within it
+  auto fill = [&]() {
+    while (g_issue - g_comp < (uint32_t)S) {
+      const Unit &u = cur_u == 0 ? U0 : U1;
+      if (!u.valid) break;
+      if (cur_s < u.nst) {
+        issue_stage(u, cur_s, g_issue);
+        ++cur_s;
+        ++g_issue;
+      } else if (cur_u == 0) {
+        cur_u = 1;
+        cur_s = 0;
+      } else {
+        break;
+      }
+    }
+  };
+  if (U0.valid) issue_q(U0);
+  fill();
+
+  bool ok = true;
+  while (U0.valid && ok) {
+    U1 = claim_unit<KV, D, HPC>(p, total_units, lane);
+    // q of this unit: widen, pre-scale, lay out [D/2][HPC][2]
+    ok = __all_sync(0xffffffffu, mbar_wait(qbar, qphase, p.err));
+    if (!ok) break;
+    qphase ^= 1;
+    for (int e = lane; e < HPC * D; e += 32) {
+      const int h = e / D, d = e % D;
+      q_s[((d >> 1) * HPC + h) * 2 + (d & 1)] = Elem<QT>::to_f32(q_raw[e]) * p.q_mult;
+    }
+    __syncwarp();
+    if (U1.valid) issue_q(U1);
+    fill();
+
+    float2 acc[HPC][4];
+    float m_ref[HPC];
+    float l_part[HH];
+#pragma unroll
+    for (int h = 0; h < HPC; ++h) {
+      m_ref[h] = kNegInf;
+#pragma unroll
+      for (int i = 0; i < 4; ++i) acc[h][i] = make_float2(0.f, 0.f);
+    }
+#pragma unroll
+    for (int j = 0; j < HH; ++j) l_part[j] = 0.f;
+    const int t = lane & 15, hh = lane >> 4;
+
+    for (int cs = 0; cs < U0.nst; ++cs) {
+      const int slot = g_comp % S;
+      ok = __all_sync(0xffffffffu, mbar_wait(&full[slot], (g_comp / S) & 1, p.err));
+      if (!ok) break;
+      const uint8_t *kt = wbase + slot * G::kStageBytes;
+      const uint8_t *vt = kt + G::kTileBytes;
+      const int nvalid = min(16, U0.tok_end - (U0.tok_begin + cs * 16));
+
+      // ---------------- scores (log2 units)
+      float s[HH];
+      if constexpr (HPC >= 2) {
+        float2 sacc[HH];
+#pragma unroll
+        for (int jh = 0; jh < HH; ++jh) sacc[jh] = make_float2(0.f, 0.f);
+#pragma unroll 4
+        for (int c = 0; c < D / 8; ++c) {
+          float2 kf[4];
+          load8<KV, D>(kt, t, c, kf);
+#pragma unroll
+          for (int dp = 0; dp < 4; ++dp) {
+            const float4 *qp = reinterpret_cast<const float4 *>(q_s + ((c * 4 + dp) * HPC + hh * HH) * 2);
+#pragma unroll
+            for (int j2 = 0; j2 < HH / 2; ++j2) {
+              const float4 qv = qp[j2];
+              sacc[2 * j2] = ffma2(kf[dp], make_float2(qv.x, qv.y), sacc[2 * j2]);
+              sacc[2 * j2 + 1] = ffma2(kf[dp], make_float2(qv.z, qv.w), sacc[2 * j2 + 1]);
+            }
+          }
+        }
+#pragma unroll
+        for (int jh = 0; jh < HH; ++jh) s[jh] = t < nvalid ? sacc[jh].x + sacc[jh].y : kNegInf;
+      } else {
+        float2 sacc = make_float2(0.f, 0.f);
+#pragma unroll 4
+        for (int cc = 0; cc < D / 16; ++cc) {
+          const int c = hh * (D / 16) + cc;
+          float2 kf[4];
+          load8<KV, D>(kt, t, c, kf);
+          const float4 *qp = reinterpret_cast<const float4 *>(q_s + c * 8);
+          const float4 qa = qp[0], qb = qp[1];
+          sacc = ffma2(kf[0], make_float2(qa.x, qa.y), sacc);
+          sacc = ffma2(kf[1], make_float2(qa.z, qa.w), sacc);
+          sacc = ffma2(kf[2], make_float2(qb.x, qb.y), sacc);
+          sacc = ffma2(kf[3], make_float2(qb.z, qb.w), sacc);
+        }
+        float x = sacc.x + sacc.y;
+        x += __shfl_xor_sync(0xffffffffu, x, 16);
+        s[0] = t < nvalid ? x : kNegInf;
+      }
+
+      // ---------------- tile maxima, lazy rescale
+      float ms[HPC];
+      {
+        float mx[HH];
+#pragma unroll
+        for (int jh = 0; jh < HH; ++jh) {
+          mx[jh] = s[jh];
+#pragma unroll
+          for (int off = 1; off < 16; off <<= 1)
+            mx[jh] = fmaxf(mx[jh], __shfl_xor_sync(0xffffffffu, mx[jh], off));
+        }
+        if constexpr (HPC >= 2) {
+#pragma unroll
+          for (int jh = 0; jh < HH; ++jh) {
+            const float other = __shfl_xor_sync(0xffffffffu, mx[jh], 16);
+            ms[jh] = hh ? other : mx[jh];
+            ms[HH + jh] = hh ? mx[jh] : other;
+          }
+        } else {
+          ms[0] = mx[0];
+        }
+      }
+      bool grow = false;
+#pragma unroll
+      for (int h = 0; h < HPC; ++h) grow |= ms[h] > m_ref[h] + kRescaleLog2;
+      if (grow) {  // warp-uniform
+        float alpha[HPC];
+#pragma unroll
+        for (int h = 0; h < HPC; ++h) {
+          const float mn = fmaxf(m_ref[h], ms[h]);
+          alpha[h] = fast_exp2(m_ref[h] - mn);
+          m_ref[h] = mn;
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            acc[h][i].x *= alpha[h];
+            acc[h][i].y *= alpha[h];
+          }
+        }
+#pragma unroll
+        for (int jh = 0; jh < HH; ++jh)
+          l_part[jh] *= (HPC >= 2 && hh) ? alpha[(HH + jh) % HPC] : alpha[jh];
+      }
+      {
+        float pv[HH];
+#pragma unroll
+        for (int jh = 0; jh < HH; ++jh) {
+          const float mh = (HPC >= 2 && hh) ? m_ref[(HH + jh) % HPC] : m_ref[jh];
+          pv[jh] = t < nvalid ? fast_exp2(s[jh] - mh) : 0.f;
+        }
+        if constexpr (HPC >= 2) {
+          float4 *pw = reinterpret_cast<float4 *>(p_s + t * HPC + hh * HH);
+#pragma unroll
+          for (int j2 = 0; j2 < HH / 2; ++j2) {
+            pw[j2] = make_float4(pv[2 * j2], pv[2 * j2], pv[2 * j2 + 1], pv[2 * j2 + 1]);
+            l_part[2 * j2] += pv[2 * j2];
+            l_part[2 * j2 + 1] += pv[2 * j2 + 1];
+          }
+        } else if (hh == 0) {
+          p_s[t] = make_float2(pv[0], pv[0]);
+          l_part[0] += pv[0];
+        }
+      }
+      __syncwarp();
+
+      // ---------------- P.V
+      {
+        const int ts = lane / G::kLPT, dc = lane % G::kLPT;
+#pragma unroll
+        for (int k = 0; k < 16 / G::kTPS; ++k) {
+          const int t2 = k * G::kTPS + ts;
+          if (t2 < nvalid) {
+            float2 vf[4];
+            load8<KV, D>(vt, t2, dc, vf);
+            if constexpr (HPC >= 2) {
+              const float4 *pp = reinterpret_cast<const float4 *>(p_s + t2 * HPC);
+#pragma unroll
+              for (int h2 = 0; h2 < HPC / 2; ++h2) {
+                const float4 pq = pp[h2];
+                const float2 pa = make_float2(pq.x, pq.y), pb = make_float2(pq.z, pq.w);
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                  acc[2 * h2][i] = ffma2(pa, vf[i], acc[2 * h2][i]);
+                  acc[2 * h2 + 1][i] = ffma2(pb, vf[i], acc[2 * h2 + 1][i]);
+                }
+              }
+            } else {
+              const float2 pa = p_s[t2];
+#pragma unroll
+              for (int i = 0; i < 4; ++i) acc[0][i] = ffma2(pa, vf[i], acc[0][i]);
+            }
+          }
+        }
+      }
+      __syncwarp();  // this warp is done with the slot and with p_s
+      ++g_comp;
+      fill();
+    }
+    if (!ok) break;
+
+    // ---------------- finish the unit
+#pragma unroll
+    for (int jh = 0; jh < HH; ++jh)
+#pragma unroll
+      for (int off = 1; off < 16; off <<= 1) l_part[jh] += __shfl_xor_sync(0xffffffffu, l_part[jh], off);
+    float l_all[HPC];
+    if constexpr (HPC >= 2) {
+#pragma unroll
+      for (int jh = 0; jh < HH; ++jh) {
+        l_all[jh] = __shfl_sync(0xffffffffu, l_part[jh], 0);
+        l_all[HH + jh] = __shfl_sync(0xffffffffu, l_part[jh], 16);
+      }
+    } else {
+      l_all[0] = __shfl_sync(0xffffffffu, l_part[0], 0);
+    }
+#pragma unroll
+    for (int off = G::kLPT; off < 32; off <<= 1)
+#pragma unroll
+      for (int h = 0; h < HPC; ++h)
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          acc[h][i].x += __shfl_xor_sync(0xffffffffu, acc[h][i].x, off);
+          acc[h][i].y += __shfl_xor_sync(0xffffffffu, acc[h][i].y, off);
+        }
+    const int ts = lane / G::kLPT, dc = lane % G::kLPT;
+    const int64_t head0 = (int64_t)U0.row * p.num_q_heads + U0.h0;
+    if (U0.nparts == 1) {
+      if (ts == 0) {
+#pragma unroll
+        for (int h = 0; h < HPC; ++h) {
+          const float inv = l_all[h] > 0.f ? p.out_mult / l_all[h] : 0.f;
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            const int64_t idx = (head0 + h) * D + dc * 8 + 2 * i;
+            store_out<QT>(p.out, idx, p.out_f32 != 0, acc[h][i].x * inv);
+            store_out<QT>(p.out, idx + 1, p.out_f32 != 0, acc[h][i].y * inv);
+          }
+        }
+      }
+    } else {
+      if (ts == 0) {
+#pragma unroll
+        for (int h = 0; h < HPC; ++h) {
+          float4 *dst = reinterpret_cast<float4 *>(
+              p.ws_acc + ((head0 + h) * p.max_partitions + U0.part) * D + dc * 8);
+          dst[0] = make_float4(acc[h][0].x, acc[h][0].y, acc[h][1].x, acc[h][1].y);
+          dst[1] = make_float4(acc[h][2].x, acc[h][2].y, acc[h][3].x, acc[h][3].y);
+        }
+      }
+      if (lane < HPC) {
+        float mv = m_ref[0], lv = l_all[0];
+#pragma unroll
+        for (int h = 1; h < HPC; ++h)
+          if (lane == h) {
+            mv = m_ref[h];
+            lv = l_all[h];
+          }
+        p.ws_ml[(head0 + lane) * p.max_partitions + U0.part] = make_float2(mv, lv);
+      }
+      __threadfence();
+      __syncwarp();
+      int last = 0;
+      if (lane == 0) {
+        last = atomicAdd(p.ws_count + head0, 1) == U0.nparts - 1;
+        if (last) p.ws_count[head0] = 0;  // ready for the next call
+      }
+      last = __shfl_sync(0xffffffffu, last, 0);
+      if (last) {
+        __threadfence();
+        for (int h = 0; h < HPC; ++h) {
+          const int64_t base = (head0 + h) * p.max_partitions;
+          float M = kNegInf;
+          for (int q = 0; q < U0.nparts; ++q) M = fmaxf(M, __ldcg(&p.ws_ml[base + q].x));
+          for (int d = lane; d < D; d += 32) {
+            float a = 0.f, l = 0.f;
+            for (int q = 0; q < U0.nparts; ++q) {
+              const float2 ml = __ldcg(&p.ws_ml[base + q]);
+              const float wt = fast_exp2(ml.x - M);
+              a += wt * __ldcg(&p.ws_acc[(base + q) * D + d]);
+              l += wt * ml.y;
+            }
+            store_out<QT>(p.out, (head0 + h) * D + d, p.out_f32 != 0, l > 0.f ? a / l * p.out_mult : 0.f);
+          }
+        }
+      }
+    }
+
+    // advance: U1 becomes current; the issue cursor follows it
+    U0 = U1;
+    U1.valid = 0;
+    if (cur_u == 1) {
+      cur_u = 0;
+    } else {
+      cur_s = 0;
+    }
+    fill();
+  }
+  // a warp that gave up on a timed-out wait still has copies in flight: let
+  // them land (bounded) before the CTA's shared memory is released
+  if (!ok) {
+    for (uint32_t g = g_comp; g < g_issue; ++g) (void)mbar_wait(&full[g % S], (g / S) & 1, p.err);
+  }
+}
+
+// Host launcher: plan kernel, then one persistent CTA per SM.
+template <typename KV, typename QT, int D, int HPC>
+cudaError_t launch_decode_one(const DecodeParams &p, const PoolMaps &m, cudaStream_t s) {
+  using DG = DecGeo<KV, D, HPC>;
+  decode_plan_kernel<0><<<1, 1024, 0, s>>>(p);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  auto kern = paged_decode_kernel<KV, QT, D, HPC>;
+  e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, DG::kSmem);
+  if (e != cudaSuccess) return e;
+  int dev = 0, sms = 0;
+  if ((e = cudaGetDevice(&dev)) != cudaSuccess) return e;
+  if ((e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess) return e;
+  kern<<<sms, DG::kNW * 32, DG::kSmem, s>>>(p, m.k, m.v);
+  return cudaGetLastError();
+}
+
+template <typename KV, typename QT>
+cudaError_t launch_decode(const DecodeParams &p, int hpc, const PoolMaps &m, int head_dim,
+                          cudaStream_t s) {
+  if (head_dim == 128) {
+    if (hpc == 8) return launch_decode_one<KV, QT, 128, 8>(p, m, s);
+    if (hpc == 4) return launch_decode_one<KV, QT, 128, 4>(p, m, s);
+    return launch_decode_one<KV, QT, 128, 1>(p, m, s);
+  }
+  if (hpc == 8) return launch_decode_one<KV, QT, 64, 8>(p, m, s);
+  if (hpc == 4) return launch_decode_one<KV, QT, 64, 4>(p, m, s);
+  return launch_decode_one<KV, QT, 64, 1>(p, m, s);
+}
+
+}  // namespace pa

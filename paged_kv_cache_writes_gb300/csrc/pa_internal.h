@@ -12,8 +12,9 @@ namespace pa {
 
 inline int dtype_bytes(pa_dtype t) { return t == PA_FP8_E4M3 ? 1 : 2; }
 
-constexpr int kDefaultPartition = 512;   // split-KV partition, tokens
-constexpr int kMaxPartitions = 4096;     // per sequence (limits the combine's smem)
+constexpr int kDefaultPartition = 512;   // split-KV partition, tokens (also the largest used)
+constexpr int kMaxPartitions = 4096;     // per sequence (item encoding: 12 bits)
+constexpr int kMaxDecodeRows = 1 << 19;  // sequences per call (item encoding: row << 12)
 
 // Decode / CUDA-core prefill parameters shared by every instantiation.
 struct AttnParams {
@@ -44,8 +45,9 @@ struct AttnParams {
   int32_t *err;               // device error word
 };
 
+// Decode workspace: header | item list | split-KV partials (acc, max/sum) | counters.
 struct WorkspaceLayout {
-  size_t acc_off, ml_off, cnt_off, total;
+  size_t hdr_off, items_off, acc_off, ml_off, cnt_off, total;
 };
 WorkspaceLayout decode_workspace_layout(int64_t rows, int64_t num_q_heads, int64_t head_dim,
                                         int64_t max_partitions);
@@ -64,7 +66,9 @@ struct PoolMaps {
   CUtensorMap k, v;
 };
 
-// Launch the paged decode / CUDA-core prefill kernel for one (kv dtype, q dtype).
+struct DecodeParams;  // pa_decode.cuh
+
+// Launch the CUDA-core prefill-row kernel / the persistent decode for one (kv dtype, q dtype).
 cudaError_t launch_attention_bf16(const AttnParams &p, const PoolMaps &m, int head_dim, int rows,
                                   cudaStream_t s);
 cudaError_t launch_attention_f16(const AttnParams &p, const PoolMaps &m, int head_dim, int rows,
@@ -73,5 +77,13 @@ cudaError_t launch_attention_fp8_bf16q(const AttnParams &p, const PoolMaps &m, i
                                        int rows, cudaStream_t s);
 cudaError_t launch_attention_fp8_f16q(const AttnParams &p, const PoolMaps &m, int head_dim,
                                       int rows, cudaStream_t s);
+cudaError_t launch_decode_bf16(const DecodeParams &p, int hpc, const PoolMaps &m, int head_dim,
+                               cudaStream_t s);
+cudaError_t launch_decode_f16(const DecodeParams &p, int hpc, const PoolMaps &m, int head_dim,
+                              cudaStream_t s);
+cudaError_t launch_decode_fp8_bf16q(const DecodeParams &p, int hpc, const PoolMaps &m, int head_dim,
+                                    cudaStream_t s);
+cudaError_t launch_decode_fp8_f16q(const DecodeParams &p, int hpc, const PoolMaps &m, int head_dim,
+                                   cudaStream_t s);
 
 }  // namespace pa

@@ -137,12 +137,15 @@ def test_prefill_validation(lib):
 
 def test_workspace_size(lib):
     import paged_kv_cache_writes_gb300 as pa
-    assert pa.pa_decode_workspace_bytes(256, 64, 8, 128, 512, 0) == 0        # one partition: none needed
+    hdr, cnt = 256, 256 * 64 * 4
+    # one partition: header, item list and counters only
+    assert pa.pa_decode_workspace_bytes(256, 64, 8, 128, 512, 0) == hdr + 256 * 4 + cnt
     n = pa.pa_decode_workspace_bytes(256, 64, 8, 128, 8192, 512)
     parts = 16
+    items = 256 * parts * 4
     acc = 256 * 64 * parts * 128 * 4
     ml = 256 * 64 * parts * 8
-    cnt = 256 * 64 * 4
-    assert n == acc + ml + cnt                                                 # all multiples of 256
+    assert n == hdr + items + acc + ml + cnt                                  # all multiples of 256
+    assert pa.pa_decode_workspace_bytes(256, 64, 8, 128, 8192, 2048) == n     # partitions above 512 act as 512
     assert pa.pa_decode_workspace_bytes(4, 30, 8, 128, 8192, 0) == 0         # invalid -> 0
     assert pa.pa_decode_workspace_bytes(4, 32, 8, 128, 8192, 48) == 0

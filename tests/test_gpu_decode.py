@@ -77,22 +77,17 @@ def test_zero_length_sequences():
     assert dev.out[0].abs().max().item() == 0 and dev.out[2].abs().max().item() == 0
 
 
-def test_workspace_left_zeroed_and_reusable():
-    b = W.decode_batch("r", [3000, 100, 2500], 16, 2, 128, 16, "bf16", seed=34, partition_size=256)
+def test_workspace_contents_ignored_and_reusable():
+    """Each call rebuilds its workspace: garbage left in it changes nothing,
+    and repeated calls give bit-identical outputs."""
+    b = W.decode_batch("r", [3000, 100, 2500, 0, 17], 16, 2, 128, 16, "bf16", seed=34, partition_size=256)
     dev = run_gpu(b)
     first = dev.out.clone()
-    assert dev.workspace is not None
-    from paged_kv_cache_writes_gb300 import _HERE  # noqa: F401  (package import check)
-    ws = dev.workspace
-    # the arrival counters live at the end of the workspace and must be zero again
-    hq, parts = b.num_q_heads, -(-3000 // 256)
-    cnt_off = (-(-(b.num_seqs * hq * parts * b.head_dim * 4) // 256) * 256 +
-               -(-(b.num_seqs * hq * parts * 8) // 256) * 256)
-    assert int(ws[cnt_off:].view(torch.int32).abs().sum().item()) == 0
-    for _ in range(3):
+    for fill in (0xFF, 0x00, 0x5A):
+        dev.workspace.fill_(fill)
         dev.decode()
-    torch.cuda.synchronize()
-    assert torch.equal(dev.out.view(torch.int16), first.view(torch.int16))
+        torch.cuda.synchronize()
+        assert torch.equal(dev.out.view(torch.int32), first.view(torch.int32))
 
 
 def test_llama8b_full():
