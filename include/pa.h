@@ -184,6 +184,41 @@ PA_API pa_status pa_decode(const void *q, pa_dtype q_dtype, int32_t num_seqs,
                     pa_stream_t stream);
 
 /*
+ * pa_decode_noalloc -- pa_decode for callers that cannot allocate device
+ * memory.  The pages have no counterpart to this call; it exists for the
+ * library's users.
+ *
+ * Some callers cannot call cudaMalloc (or any allocator) at the point where
+ * they decode: code that runs while allocation is forbidden or unsafe, such
+ * as a host thread driving a memory pool that is fully carved up in advance,
+ * or a runtime whose device memory is owned by another framework.  This entry
+ * point takes the same arguments as pa_decode minus the workspace and uses a
+ * fixed scratch area that lives inside the library: a static device array of
+ * PA_NOALLOC_SCRATCH_BYTES (64 MiB).  Every GPU that loads the library holds
+ * that array until the process exits.
+ *
+ *  - The first call on a device, with that device current, looks up the
+ *    array's device address (cudaGetSymbolAddress); make that first call
+ *    before any stream capture on that device.
+ *  - A problem whose workspace (pa_decode_workspace_bytes) exceeds the array
+ *    returns PA_ERR_UNSUPPORTED before anything is launched.
+ *  - Every call on a device shares the one array.  Its contents are rebuilt
+ *    by each call (the work list and counters are reset on the device before
+ *    use), but two calls that overlap on the GPU (different streams without
+ *    ordering) race on it and give undefined results.
+ *  - No allocation of any kind is made; results equal pa_decode's.
+ */
+#define PA_NOALLOC_SCRATCH_BYTES ((size_t)64 << 20)
+PA_API pa_status pa_decode_noalloc(const void *q, pa_dtype q_dtype, int32_t num_seqs,
+                            int32_t num_q_heads, const void *k_cache,
+                            const void *v_cache, const pa_kv_cache *cache,
+                            const int32_t *block_tables,
+                            int32_t max_blocks_per_seq, const int32_t *seq_lens,
+                            int32_t max_seq_len, float scale,
+                            int32_t partition_size, void *out,
+                            pa_dtype out_dtype, pa_stream_t stream);
+
+/*
  * pa_prefill_chunk -- causal attention of prompt chunks over paged context
  * ([V07] "Architectural Blueprint 3: Chunked Prefill"; [HT] "5. Chunked
  * Prefill & Latency SLA Management": a long prompt is processed in chunks,
