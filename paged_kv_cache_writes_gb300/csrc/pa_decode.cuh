@@ -16,6 +16,9 @@
 // warps is an independent worker that claims units from an atomic cursor.
 //
 // Inside a warp:
+//  * the next unit is claimed while the current one computes: the cursor
+//    bump and the two dependent reads behind it (item, then the row's length
+//    and block ids) are issued one per tile, so their latency is hidden;
 //  * lane 0 keeps a ring of kSlots 16-token K/V tiles in flight with 2D
 //    bulk-tensor (TMA) copies (128-byte swizzle), running ahead across the
 //    boundary into the next claimed unit; the unit's block ids sit one per
@@ -162,32 +165,66 @@ struct Unit {
   int32_t blk;
 };
 
-template <typename KV, int D, int HPC>
-__device__ __forceinline__ Unit claim_unit(const DecodeParams &p, int total_units, int lane) {
-  Unit u;
-  int id = 0;
-  if (lane == 0) id = atomicAdd(&p.hdr->next_unit, 1);
-  id = __shfl_sync(0xffffffffu, id, 0);
-  u.valid = id < total_units;
-  u.blk = -1;
-  if (!u.valid) return u;
+// A claim in flight.  Its three dependent global reads (cursor -> item ->
+// length and block ids) are issued one step at a time between K/V tiles, so
+// their latency hides behind the current unit's compute.
+struct PendingClaim {
+  int phase;  // 0: cursor bumped, 1: item requested, 2: row data requested, 3: resolved
+  int id, item, L;
+  int32_t blk;
+};
+
+__device__ __forceinline__ void claim_start(PendingClaim &c, const DecodeParams &p, int lane) {
+  c.id = 0;
+  if (lane == 0) c.id = atomicAdd(&p.hdr->next_unit, 1);
+  c.phase = 0;
+}
+
+// Advance a pending claim by one step (warp-uniform); true once `u` is filled.
+template <int HPC>
+__device__ __forceinline__ bool claim_step(PendingClaim &c, Unit &u, const DecodeParams &p, int total_units,
+                                           int lane) {
   const int hgt = p.num_kv_heads * p.groups;
-  const int item = __ldg(p.items + id / hgt);
-  const int hs = id % hgt;
-  u.row = item >> 12;
-  u.part = item & 4095;
-  u.kvh = hs / p.groups;
-  u.h0 = u.kvh * (p.num_q_heads / p.num_kv_heads) + (hs % p.groups) * HPC;
-  const int L = checked_len(p, u.row, false);
-  u.nparts = max(1, (L + p.partition_size - 1) / p.partition_size);  // an empty row: one empty unit
-  u.tok_begin = u.part * p.partition_size;
-  u.tok_end = min(L, u.tok_begin + p.partition_size);
-  u.nst = (u.tok_end - u.tok_begin + 15) >> 4;
-  const int nblk = (u.tok_end - u.tok_begin + p.block_size - 1) / p.block_size;
-  const int lb = u.tok_begin / p.block_size + lane;
-  if (lane < nblk && lb < p.max_blocks_per_seq)
-    u.blk = __ldg(p.block_tables + (int64_t)u.row * p.max_blocks_per_seq + lb);
-  return u;
+  if (c.phase == 0) {
+    c.id = __shfl_sync(0xffffffffu, c.id, 0);
+    if (c.id < total_units) c.item = __ldg(p.items + c.id / hgt);
+    c.phase = 1;
+    return false;
+  }
+  if (c.phase == 1) {
+    c.blk = -1;
+    if (c.id < total_units) {
+      const int row = c.item >> 12, part = c.item & 4095;
+      c.L = __ldg(p.seq_lens + row);
+      const int lb = part * p.partition_size / p.block_size + lane;
+      if (lb < p.max_blocks_per_seq) c.blk = __ldg(p.block_tables + (int64_t)row * p.max_blocks_per_seq + lb);
+    }
+    c.phase = 2;
+    return false;
+  }
+  if (c.phase == 2) {
+    u.valid = c.id < total_units;
+    u.blk = -1;
+    if (u.valid) {
+      const int hs = c.id % hgt;
+      u.row = c.item >> 12;
+      u.part = c.item & 4095;
+      u.kvh = hs / p.groups;
+      u.h0 = u.kvh * (p.num_q_heads / p.num_kv_heads) + (hs % p.groups) * HPC;
+      int L = c.L;
+      const int64_t cap = min((int64_t)p.max_blocks_per_seq * p.block_size,
+                              (int64_t)p.max_partitions * p.partition_size);
+      if (L < 0 || L > cap) L = L < 0 ? 0 : (int)cap;  // reported by the plan kernel
+      u.nparts = max(1, (L + p.partition_size - 1) / p.partition_size);
+      u.tok_begin = u.part * p.partition_size;
+      u.tok_end = min(L, u.tok_begin + p.partition_size);
+      u.nst = (u.tok_end - u.tok_begin + 15) >> 4;
+      const int nblk = (u.tok_end - u.tok_begin + p.block_size - 1) / p.block_size;
+      u.blk = lane < nblk ? c.blk : -1;
+    }
+    c.phase = 3;
+  }
+  return true;
 }
 
 __device__ __forceinline__ void fence_proxy_async_smem() {
@@ -271,7 +308,13 @@ __global__ void __launch_bounds__(DecGeo<KV, D, HPC>::kNW * 32, 1)
     }
   };
 
-  Unit U0 = claim_unit<KV, D, HPC>(p, total_units, lane);
+  Unit U0;
+  {
+    PendingClaim c0;
+    claim_start(c0, p, lane);
+    while (!claim_step<HPC>(c0, U0, p, total_units, lane)) {
+    }
+  }
   Unit U1;
   U1.valid = 0;
   U1.blk = -1;
@@ -298,7 +341,9 @@ __global__ void __launch_bounds__(DecGeo<KV, D, HPC>::kNW * 32, 1)
 
   bool ok = true;
   while (U0.valid && ok) {
-    U1 = claim_unit<KV, D, HPC>(p, total_units, lane);
+    PendingClaim pc;
+    claim_start(pc, p, lane);
+    bool have_next = false;
     // q of this unit: widen, pre-scale, lay out [D/2][HPC][2]
     ok = __all_sync(0xffffffffu, mbar_wait(qbar, qphase, p.err));
     if (!ok) break;
@@ -308,7 +353,6 @@ __global__ void __launch_bounds__(DecGeo<KV, D, HPC>::kNW * 32, 1)
       q_s[((d >> 1) * HPC + h) * 2 + (d & 1)] = Elem<QT>::to_f32(q_raw[e]) * p.q_mult;
     }
     __syncwarp();
-    if (U1.valid) issue_q(U1);
     fill();
 
     float2 acc[HPC][4];
@@ -335,9 +379,9 @@ __global__ void __launch_bounds__(DecGeo<KV, D, HPC>::kNW * 32, 1)
       // ---------------- scores (log2 units)
       float s[HH];
       if constexpr (HPC >= 2) {
-        float2 sacc[HH];
+        float2 sacc[2][HH];  // two chains per head (even / odd element pairs) for ILP
 #pragma unroll
-        for (int jh = 0; jh < HH; ++jh) sacc[jh] = make_float2(0.f, 0.f);
+        for (int jh = 0; jh < HH; ++jh) sacc[0][jh] = sacc[1][jh] = make_float2(0.f, 0.f);
 #pragma unroll 4
         for (int c = 0; c < D / 8; ++c) {
           float2 kf[4];
@@ -348,13 +392,14 @@ __global__ void __launch_bounds__(DecGeo<KV, D, HPC>::kNW * 32, 1)
 #pragma unroll
             for (int j2 = 0; j2 < HH / 2; ++j2) {
               const float4 qv = qp[j2];
-              sacc[2 * j2] = ffma2(kf[dp], make_float2(qv.x, qv.y), sacc[2 * j2]);
-              sacc[2 * j2 + 1] = ffma2(kf[dp], make_float2(qv.z, qv.w), sacc[2 * j2 + 1]);
+              sacc[dp & 1][2 * j2] = ffma2(kf[dp], make_float2(qv.x, qv.y), sacc[dp & 1][2 * j2]);
+              sacc[dp & 1][2 * j2 + 1] = ffma2(kf[dp], make_float2(qv.z, qv.w), sacc[dp & 1][2 * j2 + 1]);
             }
           }
         }
 #pragma unroll
-        for (int jh = 0; jh < HH; ++jh) s[jh] = t < nvalid ? sacc[jh].x + sacc[jh].y : kNegInf;
+        for (int jh = 0; jh < HH; ++jh)
+          s[jh] = t < nvalid ? (sacc[0][jh].x + sacc[0][jh].y) + (sacc[1][jh].x + sacc[1][jh].y) : kNegInf;
       } else {
         float2 sacc = make_float2(0.f, 0.f);
 #pragma unroll 4
@@ -469,9 +514,17 @@ __global__ void __launch_bounds__(DecGeo<KV, D, HPC>::kNW * 32, 1)
       }
       __syncwarp();  // this warp is done with the slot and with p_s
       ++g_comp;
+      if (!have_next) {
+        have_next = claim_step<HPC>(pc, U1, p, total_units, lane);
+        if (have_next && U1.valid) issue_q(U1);
+      }
       fill();
     }
     if (!ok) break;
+    while (!have_next) {
+      have_next = claim_step<HPC>(pc, U1, p, total_units, lane);
+      if (have_next && U1.valid) issue_q(U1);
+    }
 
     // ---------------- finish the unit
 #pragma unroll
