@@ -240,6 +240,21 @@ __device__ __forceinline__ void bulk_load_1d(void *smem_dst, const void *gsrc, u
       : "memory");
 }
 
+// Position of q[h][d] (fp32, pre-scaled) in a warp's q buffer.  HPC >= 4:
+// d-pair dp = d/2 lies in quarter dq = dp / (D/8) at local index dpl; the 16
+// bytes holding heads (2k, 2k+1) of that d-pair for the four quarters are
+// adjacent, so the four quarter lanes of a Q.K^T step read one 64-byte run.
+// HPC == 1: plain [D] order.
+template <int D, int HPC>
+__device__ __forceinline__ int q_index(int d, int h) {
+  if constexpr (HPC >= 4) {
+    const int dp = d >> 1, dq = dp / (D / 8), dpl = dp % (D / 8), k = h >> 1;
+    return (((dpl * (HPC / 2) + k) * 4 + dq) * 4) + (h & 1) * 2 + (d & 1);
+  } else {
+    return d;
+  }
+}
+
 template <typename KV, typename QT, int D, int HPC>
 __global__ void __launch_bounds__(DecGeo<KV, D, HPC>::kNW * 32, 1)
     paged_decode_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap tmap_k,
@@ -247,7 +262,6 @@ __global__ void __launch_bounds__(DecGeo<KV, D, HPC>::kNW * 32, 1)
   using G = Geo<KV, D>;
   using DG = DecGeo<KV, D, HPC>;
   constexpr int S = DG::kSlots;
-  constexpr int HH = HPC >= 2 ? HPC / 2 : 1;
   const float kNegInf = -__int_as_float(0x7f800000);
 
   extern __shared__ uint8_t smem_raw[];
@@ -344,20 +358,33 @@ __global__ void __launch_bounds__(DecGeo<KV, D, HPC>::kNW * 32, 1)
     PendingClaim pc;
     claim_start(pc, p, lane);
     bool have_next = false;
-    // q of this unit: widen, pre-scale, lay out [D/2][HPC][2]
+    // q of this unit: widen and pre-scale into q_s (layout: see q_index)
     ok = __all_sync(0xffffffffu, mbar_wait(qbar, qphase, p.err));
     if (!ok) break;
     qphase ^= 1;
     for (int e = lane; e < HPC * D; e += 32) {
       const int h = e / D, d = e % D;
-      q_s[((d >> 1) * HPC + h) * 2 + (d & 1)] = Elem<QT>::to_f32(q_raw[e]) * p.q_mult;
+      q_s[q_index<D, HPC>(d, h)] = Elem<QT>::to_f32(q_raw[e]) * p.q_mult;
     }
     __syncwarp();
     fill();
 
+    // Q.K^T lane mapping (HPC >= 4): lane = dq * 8 + t8 covers tokens t8 and
+    // t8 + 8 of the tile, every head of the group, and the dq-th quarter of
+    // head_dim.  Each K element is widened once per lane that uses it; each
+    // 16-byte q load feeds 2 tokens x 2 heads of FMA pairs, and the 4 quarters
+    // read 64 contiguous bytes per wavefront.  A two-level shuffle reduction
+    // over dq leaves lane (dq, t8) with token t8 + 8*(dq & 1) and heads
+    // (dq >> 1) * HPC/2 + j.  One head (HPC == 1): lane = (d half, token).
+    constexpr int HS = HPC >= 4 ? HPC / 2 : 1;  // scores held per lane after the reduction
+    const int dq = lane >> 3, t8 = lane & 7;
+    const int my_t = HPC >= 4 ? t8 + 8 * (dq & 1) : (lane & 15);
+    const int my_h0 = HPC >= 4 ? (dq >> 1) * HS : 0;
+    const int hh = lane >> 4;  // HPC == 1: which half of head_dim
+
     float2 acc[HPC][4];
     float m_ref[HPC];
-    float l_part[HH];
+    float l_part[HS];
 #pragma unroll
     for (int h = 0; h < HPC; ++h) {
       m_ref[h] = kNegInf;
@@ -365,8 +392,7 @@ __global__ void __launch_bounds__(DecGeo<KV, D, HPC>::kNW * 32, 1)
       for (int i = 0; i < 4; ++i) acc[h][i] = make_float2(0.f, 0.f);
     }
 #pragma unroll
-    for (int j = 0; j < HH; ++j) l_part[j] = 0.f;
-    const int t = lane & 15, hh = lane >> 4;
+    for (int j = 0; j < HS; ++j) l_part[j] = 0.f;
 
     for (int cs = 0; cs < U0.nst; ++cs) {
       const int slot = g_comp % S;
@@ -377,36 +403,56 @@ __global__ void __launch_bounds__(DecGeo<KV, D, HPC>::kNW * 32, 1)
       const int nvalid = min(16, U0.tok_end - (U0.tok_begin + cs * 16));
 
       // ---------------- scores (log2 units)
-      float s[HH];
-      if constexpr (HPC >= 2) {
-        float2 sacc[2][HH];  // two chains per head (even / odd element pairs) for ILP
+      float s[HS];
+      if constexpr (HPC >= 4) {
+        float2 sacc[2][HPC];
 #pragma unroll
-        for (int jh = 0; jh < HH; ++jh) sacc[0][jh] = sacc[1][jh] = make_float2(0.f, 0.f);
-#pragma unroll 4
-        for (int c = 0; c < D / 8; ++c) {
-          float2 kf[4];
-          load8<KV, D>(kt, t, c, kf);
+        for (int i = 0; i < 2; ++i)
 #pragma unroll
-          for (int dp = 0; dp < 4; ++dp) {
-            const float4 *qp = reinterpret_cast<const float4 *>(q_s + ((c * 4 + dp) * HPC + hh * HH) * 2);
+          for (int h = 0; h < HPC; ++h) sacc[i][h] = make_float2(0.f, 0.f);
+        constexpr int CPQ = D / 32;  // 8-element chunks per quarter of head_dim
 #pragma unroll
-            for (int j2 = 0; j2 < HH / 2; ++j2) {
-              const float4 qv = qp[j2];
-              sacc[dp & 1][2 * j2] = ffma2(kf[dp], make_float2(qv.x, qv.y), sacc[dp & 1][2 * j2]);
-              sacc[dp & 1][2 * j2 + 1] = ffma2(kf[dp], make_float2(qv.z, qv.w), sacc[dp & 1][2 * j2 + 1]);
+        for (int cl = 0; cl < CPQ; ++cl) {
+          float2 kf[2][4];
+          load8<KV, D>(kt, t8, dq * CPQ + cl, kf[0]);
+          load8<KV, D>(kt, t8 + 8, dq * CPQ + cl, kf[1]);
+#pragma unroll
+          for (int dpi = 0; dpi < 4; ++dpi) {
+            const float4 *qp = reinterpret_cast<const float4 *>(q_s) + ((cl * 4 + dpi) * (HPC / 2)) * 4 + dq;
+#pragma unroll
+            for (int k = 0; k < HPC / 2; ++k) {
+              const float4 qv = qp[k * 4];
+              const float2 qa = make_float2(qv.x, qv.y), qb = make_float2(qv.z, qv.w);
+#pragma unroll
+              for (int i = 0; i < 2; ++i) {
+                sacc[i][2 * k] = ffma2(kf[i][dpi], qa, sacc[i][2 * k]);
+                sacc[i][2 * k + 1] = ffma2(kf[i][dpi], qb, sacc[i][2 * k + 1]);
+              }
             }
           }
         }
+        // reduce over the four quarters of head_dim
+        float w[HPC];
+        const bool odd_tok = dq & 1, hi_heads = dq >> 1;
 #pragma unroll
-        for (int jh = 0; jh < HH; ++jh)
-          s[jh] = t < nvalid ? (sacc[0][jh].x + sacc[0][jh].y) + (sacc[1][jh].x + sacc[1][jh].y) : kNegInf;
+        for (int h = 0; h < HPC; ++h) {
+          const float v0 = sacc[0][h].x + sacc[0][h].y, v1 = sacc[1][h].x + sacc[1][h].y;
+          const float keep = odd_tok ? v1 : v0, send = odd_tok ? v0 : v1;
+          w[h] = keep + __shfl_xor_sync(0xffffffffu, send, 8);
+        }
+#pragma unroll
+        for (int j = 0; j < HS; ++j) {
+          const float keep = hi_heads ? w[HS + j] : w[j], send = hi_heads ? w[j] : w[HS + j];
+          s[j] = keep + __shfl_xor_sync(0xffffffffu, send, 16);
+          s[j] = my_t < nvalid ? s[j] : kNegInf;
+        }
       } else {
         float2 sacc = make_float2(0.f, 0.f);
 #pragma unroll 4
         for (int cc = 0; cc < D / 16; ++cc) {
           const int c = hh * (D / 16) + cc;
           float2 kf[4];
-          load8<KV, D>(kt, t, c, kf);
+          load8<KV, D>(kt, my_t, c, kf);
           const float4 *qp = reinterpret_cast<const float4 *>(q_s + c * 8);
           const float4 qa = qp[0], qb = qp[1];
           sacc = ffma2(kf[0], make_float2(qa.x, qa.y), sacc);
@@ -416,35 +462,33 @@ __global__ void __launch_bounds__(DecGeo<KV, D, HPC>::kNW * 32, 1)
         }
         float x = sacc.x + sacc.y;
         x += __shfl_xor_sync(0xffffffffu, x, 16);
-        s[0] = t < nvalid ? x : kNegInf;
+        s[0] = my_t < nvalid ? x : kNegInf;
       }
 
-      // ---------------- tile maxima, lazy rescale
-      float ms[HPC];
-      {
-        float mx[HH];
+      // ---------------- lazy online softmax: shuffles only when a score
+      // exceeds the reference maximum by more than kRescaleLog2
+      float mh[HS];
 #pragma unroll
-        for (int jh = 0; jh < HH; ++jh) {
-          mx[jh] = s[jh];
+      for (int j = 0; j < HS; ++j) mh[j] = HPC >= 4 && (dq >> 1) ? m_ref[(HS + j) % HPC] : m_ref[j];
+      bool over = false;
 #pragma unroll
-          for (int off = 1; off < 16; off <<= 1)
-            mx[jh] = fmaxf(mx[jh], __shfl_xor_sync(0xffffffffu, mx[jh], off));
-        }
-        if constexpr (HPC >= 2) {
+      for (int j = 0; j < HS; ++j) over |= s[j] > mh[j] + kRescaleLog2;
+      if (__any_sync(0xffffffffu, over)) {
+        float mx[HS], ms[HPC];
 #pragma unroll
-          for (int jh = 0; jh < HH; ++jh) {
-            const float other = __shfl_xor_sync(0xffffffffu, mx[jh], 16);
-            ms[jh] = hh ? other : mx[jh];
-            ms[HH + jh] = hh ? mx[jh] : other;
+        for (int j = 0; j < HS; ++j) {
+          mx[j] = s[j];
+          if constexpr (HPC >= 4) {  // tokens live on t8 (lane bits 0-2) and dq bit 0 (lane bit 3)
+#pragma unroll
+            for (int off = 1; off < 16; off <<= 1) mx[j] = fmaxf(mx[j], __shfl_xor_sync(0xffffffffu, mx[j], off));
+            ms[j] = __shfl_sync(0xffffffffu, mx[j], 0);
+            ms[HS + j] = __shfl_sync(0xffffffffu, mx[j], 16);
+          } else {
+#pragma unroll
+            for (int off = 1; off < 16; off <<= 1) mx[j] = fmaxf(mx[j], __shfl_xor_sync(0xffffffffu, mx[j], off));
+            ms[0] = __shfl_sync(0xffffffffu, mx[0], 0);
           }
-        } else {
-          ms[0] = mx[0];
         }
-      }
-      bool grow = false;
-#pragma unroll
-      for (int h = 0; h < HPC; ++h) grow |= ms[h] > m_ref[h] + kRescaleLog2;
-      if (grow) {  // warp-uniform
         float alpha[HPC];
 #pragma unroll
         for (int h = 0; h < HPC; ++h) {
@@ -458,27 +502,26 @@ __global__ void __launch_bounds__(DecGeo<KV, D, HPC>::kNW * 32, 1)
           }
         }
 #pragma unroll
-        for (int jh = 0; jh < HH; ++jh)
-          l_part[jh] *= (HPC >= 2 && hh) ? alpha[(HH + jh) % HPC] : alpha[jh];
+        for (int j = 0; j < HS; ++j) {
+          const bool hi = HPC >= 4 && (dq >> 1);
+          l_part[j] *= hi ? alpha[(HS + j) % HPC] : alpha[j];
+          mh[j] = hi ? m_ref[(HS + j) % HPC] : m_ref[j];
+        }
       }
       {
-        float pv[HH];
+        float pv[HS];
 #pragma unroll
-        for (int jh = 0; jh < HH; ++jh) {
-          const float mh = (HPC >= 2 && hh) ? m_ref[(HH + jh) % HPC] : m_ref[jh];
-          pv[jh] = t < nvalid ? fast_exp2(s[jh] - mh) : 0.f;
+        for (int j = 0; j < HS; ++j) {
+          pv[j] = my_t < nvalid ? fast_exp2(s[j] - mh[j]) : 0.f;
+          l_part[j] += (HPC >= 4 || hh == 0) ? pv[j] : 0.f;
         }
-        if constexpr (HPC >= 2) {
-          float4 *pw = reinterpret_cast<float4 *>(p_s + t * HPC + hh * HH);
+        if constexpr (HPC >= 4) {
+          float4 *pw = reinterpret_cast<float4 *>(p_s + my_t * HPC + my_h0);
 #pragma unroll
-          for (int j2 = 0; j2 < HH / 2; ++j2) {
+          for (int j2 = 0; j2 < HS / 2; ++j2)
             pw[j2] = make_float4(pv[2 * j2], pv[2 * j2], pv[2 * j2 + 1], pv[2 * j2 + 1]);
-            l_part[2 * j2] += pv[2 * j2];
-            l_part[2 * j2 + 1] += pv[2 * j2 + 1];
-          }
         } else if (hh == 0) {
-          p_s[t] = make_float2(pv[0], pv[0]);
-          l_part[0] += pv[0];
+          p_s[my_t] = make_float2(pv[0], pv[0]);
         }
       }
       __syncwarp();
@@ -528,18 +571,14 @@ __global__ void __launch_bounds__(DecGeo<KV, D, HPC>::kNW * 32, 1)
 
     // ---------------- finish the unit
 #pragma unroll
-    for (int jh = 0; jh < HH; ++jh)
+    for (int j = 0; j < HS; ++j)
 #pragma unroll
-      for (int off = 1; off < 16; off <<= 1) l_part[jh] += __shfl_xor_sync(0xffffffffu, l_part[jh], off);
+      for (int off = 1; off < 16; off <<= 1) l_part[j] += __shfl_xor_sync(0xffffffffu, l_part[j], off);
     float l_all[HPC];
-    if constexpr (HPC >= 2) {
 #pragma unroll
-      for (int jh = 0; jh < HH; ++jh) {
-        l_all[jh] = __shfl_sync(0xffffffffu, l_part[jh], 0);
-        l_all[HH + jh] = __shfl_sync(0xffffffffu, l_part[jh], 16);
-      }
-    } else {
-      l_all[0] = __shfl_sync(0xffffffffu, l_part[0], 0);
+    for (int j = 0; j < HS; ++j) {
+      l_all[j] = __shfl_sync(0xffffffffu, l_part[j], 0);
+      if constexpr (HPC >= 4) l_all[HS + j] = __shfl_sync(0xffffffffu, l_part[j], 16);
     }
 #pragma unroll
     for (int off = G::kLPT; off < 32; off <<= 1)
