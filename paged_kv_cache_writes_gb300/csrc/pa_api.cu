@@ -76,8 +76,11 @@ PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
 }
 
 // One pool as a 2D tensor [num_blocks*Hkv*bs rows][head_dim]; box = 16 rows x
-// one 128-byte (or 64-byte) panel, swizzled to match the kernels' reads.
-bool encode_pool_map(CUtensorMap *map, const void *base, const pa_kv_cache &c) {
+// one 128-byte (or 64-byte) panel, swizzled to match the kernels' reads.  With
+// `panels3d` and 256-byte rows the pool is viewed as [2 panels][rows][64] and
+// one box covers 16 rows of both panels (same shared-memory layout as two
+// 2D boxes).
+bool encode_pool_map(CUtensorMap *map, const void *base, const pa_kv_cache &c, bool panels3d = false) {
   auto enc = tensor_map_encoder();
   if (!enc) return false;
   const int eb = dtype_bytes(c.kv_dtype);
@@ -93,6 +96,15 @@ bool encode_pool_map(CUtensorMap *map, const void *base, const pa_kv_cache &c) {
                                                            : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
   const CUtensorMapSwizzle sw =
       panel_bytes == 128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B;
+  if (panels3d && row_bytes == 2 * panel_bytes) {
+    const cuuint64_t dims3[3] = {(cuuint64_t)(panel_bytes / eb), dims[1], 2};
+    const cuuint64_t strides3[2] = {(cuuint64_t)row_bytes, (cuuint64_t)panel_bytes};
+    const cuuint32_t box3[3] = {(cuuint32_t)(panel_bytes / eb), 16u, 2u};
+    const cuuint32_t estr3[3] = {1u, 1u, 1u};
+    return enc(map, dt, 3, const_cast<void *>(base), dims3, strides3, box3, estr3,
+               CU_TENSOR_MAP_INTERLEAVE_NONE, sw, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+  }
   return enc(map, dt, 2, const_cast<void *>(base), dims, strides, box, estr,
              CU_TENSOR_MAP_INTERLEAVE_NONE, sw, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
@@ -239,9 +251,11 @@ pa_status pa_decode(const void *q, pa_dtype q_dtype, int32_t num_seqs, int32_t n
   p.ws_acc = reinterpret_cast<float *>(ws + w.acc_off);
   p.ws_ml = reinterpret_cast<float2 *>(ws + w.ml_off);
   p.ws_count = reinterpret_cast<int32_t *>(ws + w.cnt_off);
+  p.tile_shift = c.block_size == 32 ? 1 : 0;
+  p.kv_rows = c.num_kv_heads * c.block_size;
   p.err = device_error_word();
   PoolMaps maps;
-  if (!p.err || !encode_pool_map(&maps.k, k_cache, c) || !encode_pool_map(&maps.v, v_cache, c))
+  if (!p.err || !encode_pool_map(&maps.k, k_cache, c, true) || !encode_pool_map(&maps.v, v_cache, c, true))
     return PA_ERR_CUDA;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   cudaError_t e;

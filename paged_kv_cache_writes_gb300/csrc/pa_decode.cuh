@@ -55,7 +55,9 @@ struct DecGeo {
   using G = Geo<KV, D>;
   static constexpr int kStageTok = 16;
   static constexpr int kStageBytes = G::kStageBytes;
-  static constexpr int kSlots = kStageBytes >= 8192 ? 3 : kStageBytes >= 4096 ? 6 : 8;
+  // ~16 KB of tiles per warp: one being computed, the rest in flight.  More
+  // warps per SM (9 for bf16 with head_dim 128) beat deeper per-warp rings.
+  static constexpr int kSlots = kStageBytes >= 8192 ? 2 : kStageBytes >= 4096 ? 4 : 8;
   static constexpr int kQsOff = kSlots * kStageBytes;               // fp32 [D/2][HPC][2]
   static constexpr int kQrawOff = kQsOff + D * HPC * 4;             // raw q, HPC x D
   static constexpr int kPOff = kQrawOff + HPC * D * 2;              // float2 [16][HPC]
@@ -82,6 +84,8 @@ struct DecodeParams {
   int64_t num_blocks;
   int32_t partition_size;    // <= 32 * block_size, multiple of 32
   int32_t max_partitions;
+  int32_t tile_shift;        // log2(block_size / 16): 16-token tiles per block
+  int32_t kv_rows;           // num_kv_heads * block_size: rows of one block in the 2D pool view
   float q_mult;
   float out_mult;
   DecodeHeader *hdr;
@@ -227,10 +231,6 @@ __device__ __forceinline__ bool claim_step(PendingClaim &c, Unit &u, const Decod
   return true;
 }
 
-__device__ __forceinline__ void fence_proxy_async_smem() {
-  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-}
-
 __device__ __forceinline__ void bulk_load_1d(void *smem_dst, const void *gsrc, uint32_t bytes,
                                              uint64_t *bar) {
   asm volatile(
@@ -291,37 +291,13 @@ __global__ void __launch_bounds__(DecGeo<KV, D, HPC>::kNW * 32, 1)
 
   // --------------------------------------------------------------- producer side
   auto issue_q = [&](const Unit &u) {
-    if (lane == 0) {
-      fence_proxy_async_smem();
+    if (lane == 0) {  // every lane's reads of q_raw completed before this point
       constexpr uint32_t bytes = HPC * D * sizeof(QT);
-      mbar_arrive_expect_tx(qbar, bytes);
+      mbar_arrive_expect_tx_relaxed(qbar, bytes);
       bulk_load_1d(q_raw, static_cast<const QT *>(p.q) + ((int64_t)u.row * p.num_q_heads + u.h0) * D,
                    bytes, qbar);
     }
   };
-  auto issue_stage = [&](const Unit &u, int st, uint32_t g) {
-    const int slot = g % S;
-    const int tok = u.tok_begin + st * 16;
-    const int32_t blk = __shfl_sync(0xffffffffu, u.blk, (tok - u.tok_begin) / bs);
-    if (lane == 0) {
-      fence_proxy_async_smem();
-      if (blk < 0 || blk >= p.num_blocks) {
-        record_error(p.err, PA_ERR_DEVICE_CHECK);
-        mbar_arrive(&full[slot]);
-      } else {
-        mbar_arrive_expect_tx(&full[slot], G::kStageBytes);
-        const int32_t y = (blk * p.num_kv_heads + u.kvh) * bs + (tok % bs);
-        uint8_t *st_base = wbase + slot * G::kStageBytes;
-#pragma unroll
-        for (int pn = 0; pn < G::kPanels; ++pn) {
-          tma_load_2d(st_base + pn * G::kPanelTileBytes, &tmap_k, &full[slot], pn * G::kPanelElems, y);
-          tma_load_2d(st_base + G::kTileBytes + pn * G::kPanelTileBytes, &tmap_v, &full[slot],
-                      pn * G::kPanelElems, y);
-        }
-      }
-    }
-  };
-
   Unit U0;
   {
     PendingClaim c0;
@@ -333,23 +309,55 @@ __global__ void __launch_bounds__(DecGeo<KV, D, HPC>::kNW * 32, 1)
   U1.valid = 0;
   U1.blk = -1;
   uint32_t g_issue = 0, g_comp = 0, qphase = 0;
-  int cur_u = 0, cur_s = 0;  // issue cursor: unit (0 = U0, 1 = U1), stage within it
+
+  // Issue target: the unit whose next tile is loaded next (U0, then U1),
+  // kept in its own registers with the per-unit address terms precomputed.
+  int it_valid = 0, it_nst = 0, it_st = 0, it_row = 0, it_which = 0;
+  int32_t it_blk = -1;
+  auto set_target = [&](const Unit &u, int which) {
+    it_valid = u.valid;
+    it_nst = u.valid ? u.nst : 0;
+    it_st = 0;
+    it_row = u.valid ? u.kvh * bs : 0;
+    it_blk = u.blk;
+    it_which = which;
+  };
+  // Tile it_st of the target into slot g_issue % S: one box for K, one for V.
+  auto issue_tile = [&]() {
+    const int slot = g_issue % S;
+    const int32_t blk = __shfl_sync(0xffffffffu, it_blk, it_st >> p.tile_shift);
+    if (lane == 0) {  // the slot's previous tile was fully read (its values were consumed)
+      if (blk < 0 || blk >= p.num_blocks) {
+        record_error(p.err, PA_ERR_DEVICE_CHECK);
+        mbar_arrive(&full[slot]);
+      } else {
+        mbar_arrive_expect_tx_relaxed(&full[slot], G::kStageBytes);
+        const int32_t y = blk * p.kv_rows + it_row + ((it_st & ((1 << p.tile_shift) - 1)) << 4);
+        uint8_t *st_base = wbase + slot * G::kStageBytes;
+        if constexpr (G::kPanels == 2) {  // both 128-byte panels of the rows in one 3D box
+          tma_load_3d(st_base, &tmap_k, &full[slot], 0, y, 0);
+          tma_load_3d(st_base + G::kTileBytes, &tmap_v, &full[slot], 0, y, 0);
+        } else {
+          tma_load_2d(st_base, &tmap_k, &full[slot], 0, y);
+          tma_load_2d(st_base + G::kTileBytes, &tmap_v, &full[slot], 0, y);
+        }
+      }
+    }
+    ++it_st;
+    ++g_issue;
+  };
   auto fill = [&]() {
-    while (g_issue - g_comp < (uint32_t)S) {
-      const Unit &u = cur_u == 0 ? U0 : U1;
-      if (!u.valid) break;
-      if (cur_s < u.nst) {
-        issue_stage(u, cur_s, g_issue);
-        ++cur_s;
-        ++g_issue;
-      } else if (cur_u == 0) {
-        cur_u = 1;
-        cur_s = 0;
+    while (g_issue - g_comp < (uint32_t)S && it_valid) {
+      if (it_st < it_nst) {
+        issue_tile();
+      } else if (it_which == 0 && U1.valid) {
+        set_target(U1, 1);
       } else {
         break;
       }
     }
   };
+  set_target(U0, 0);
   if (U0.valid) issue_q(U0);
   fill();
 
@@ -362,9 +370,16 @@ __global__ void __launch_bounds__(DecGeo<KV, D, HPC>::kNW * 32, 1)
     ok = __all_sync(0xffffffffu, mbar_wait(qbar, qphase, p.err));
     if (!ok) break;
     qphase ^= 1;
-    for (int e = lane; e < HPC * D; e += 32) {
-      const int h = e / D, d = e % D;
-      q_s[q_index<D, HPC>(d, h)] = Elem<QT>::to_f32(q_raw[e]) * p.q_mult;
+    for (int e8 = lane * 8; e8 < HPC * D; e8 += 256) {
+      const uint4 w = *reinterpret_cast<const uint4 *>(q_raw + e8);
+      const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
+      const int h = e8 / D, d0 = e8 % D;
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const float2 f = unpack2(ws[i], QT{});
+        *reinterpret_cast<float2 *>(q_s + q_index<D, HPC>(d0 + 2 * i, h)) =
+            make_float2(f.x * p.q_mult, f.y * p.q_mult);
+      }
     }
     __syncwarp();
     fill();
@@ -529,30 +544,34 @@ __global__ void __launch_bounds__(DecGeo<KV, D, HPC>::kNW * 32, 1)
       // ---------------- P.V
       {
         const int ts = lane / G::kLPT, dc = lane % G::kLPT;
+        auto pv_step = [&](int t2) {
+          float2 vf[4];
+          load8<KV, D>(vt, t2, dc, vf);
+          if constexpr (HPC >= 2) {
+            const float4 *pp = reinterpret_cast<const float4 *>(p_s + t2 * HPC);
 #pragma unroll
-        for (int k = 0; k < 16 / G::kTPS; ++k) {
-          const int t2 = k * G::kTPS + ts;
-          if (t2 < nvalid) {
-            float2 vf[4];
-            load8<KV, D>(vt, t2, dc, vf);
-            if constexpr (HPC >= 2) {
-              const float4 *pp = reinterpret_cast<const float4 *>(p_s + t2 * HPC);
+            for (int h2 = 0; h2 < HPC / 2; ++h2) {
+              const float4 pq = pp[h2];
+              const float2 pa = make_float2(pq.x, pq.y), pb = make_float2(pq.z, pq.w);
 #pragma unroll
-              for (int h2 = 0; h2 < HPC / 2; ++h2) {
-                const float4 pq = pp[h2];
-                const float2 pa = make_float2(pq.x, pq.y), pb = make_float2(pq.z, pq.w);
-#pragma unroll
-                for (int i = 0; i < 4; ++i) {
-                  acc[2 * h2][i] = ffma2(pa, vf[i], acc[2 * h2][i]);
-                  acc[2 * h2 + 1][i] = ffma2(pb, vf[i], acc[2 * h2 + 1][i]);
-                }
+              for (int i = 0; i < 4; ++i) {
+                acc[2 * h2][i] = ffma2(pa, vf[i], acc[2 * h2][i]);
+                acc[2 * h2 + 1][i] = ffma2(pb, vf[i], acc[2 * h2 + 1][i]);
               }
-            } else {
-              const float2 pa = p_s[t2];
-#pragma unroll
-              for (int i = 0; i < 4; ++i) acc[0][i] = ffma2(pa, vf[i], acc[0][i]);
             }
+          } else {
+            const float2 pa = p_s[t2];
+#pragma unroll
+            for (int i = 0; i < 4; ++i) acc[0][i] = ffma2(pa, vf[i], acc[0][i]);
           }
+        };
+        if (nvalid == 16) {  // full tile: straight-line, loads can be hoisted
+#pragma unroll
+          for (int k = 0; k < 16 / G::kTPS; ++k) pv_step(k * G::kTPS + ts);
+        } else {  // ragged last tile: rows past the sequence end are never read
+#pragma unroll
+          for (int k = 0; k < 16 / G::kTPS; ++k)
+            if (k * G::kTPS + ts < nvalid) pv_step(k * G::kTPS + ts);
         }
       }
       __syncwarp();  // this warp is done with the slot and with p_s
@@ -634,32 +653,56 @@ __global__ void __launch_bounds__(DecGeo<KV, D, HPC>::kNW * 32, 1)
       last = __shfl_sync(0xffffffffu, last, 0);
       if (last) {
         __threadfence();
+        // lane q holds partition q's (max, sum); the warp reduces the weights,
+        // then every lane combines D/32 output elements with independent loads
+        constexpr int EPL = D / 32;  // output elements per lane
         for (int h = 0; h < HPC; ++h) {
           const int64_t base = (head0 + h) * p.max_partitions;
           float M = kNegInf;
-          for (int q = 0; q < U0.nparts; ++q) M = fmaxf(M, __ldcg(&p.ws_ml[base + q].x));
-          for (int d = lane; d < D; d += 32) {
-            float a = 0.f, l = 0.f;
-            for (int q = 0; q < U0.nparts; ++q) {
-              const float2 ml = __ldcg(&p.ws_ml[base + q]);
-              const float wt = fast_exp2(ml.x - M);
-              a += wt * __ldcg(&p.ws_acc[(base + q) * D + d]);
-              l += wt * ml.y;
-            }
-            store_out<QT>(p.out, (head0 + h) * D + d, p.out_f32 != 0, l > 0.f ? a / l * p.out_mult : 0.f);
+          for (int q0 = 0; q0 < U0.nparts; q0 += 32) {
+            const float mq = q0 + lane < U0.nparts ? __ldcg(&p.ws_ml[base + q0 + lane].x) : kNegInf;
+            M = fmaxf(M, mq);
           }
+#pragma unroll
+          for (int off = 16; off > 0; off >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
+          float a[EPL], l = 0.f;
+#pragma unroll
+          for (int e = 0; e < EPL; ++e) a[e] = 0.f;
+          for (int q0 = 0; q0 < U0.nparts; q0 += 32) {
+            float wq = 0.f;
+            if (q0 + lane < U0.nparts) {
+              const float2 ml = __ldcg(&p.ws_ml[base + q0 + lane]);
+              wq = fast_exp2(ml.x - M);
+              l += wq * ml.y;
+            }
+            const int nq = min(32, U0.nparts - q0);
+            for (int q = 0; q < nq; ++q) {
+              const float w = __shfl_sync(0xffffffffu, wq, q);
+              const float *src = p.ws_acc + (base + q0 + q) * D + lane * EPL;
+              if constexpr (EPL == 4) {
+                const float4 v = __ldcg(reinterpret_cast<const float4 *>(src));
+                a[0] += w * v.x; a[1] += w * v.y; a[2] += w * v.z; a[3] += w * v.w;
+              } else {
+                const float2 v = __ldcg(reinterpret_cast<const float2 *>(src));
+                a[0] += w * v.x; a[1] += w * v.y;
+              }
+            }
+          }
+#pragma unroll
+          for (int off = 16; off > 0; off >>= 1) l += __shfl_xor_sync(0xffffffffu, l, off);
+          const float inv = l > 0.f ? p.out_mult / l : 0.f;
+#pragma unroll
+          for (int e = 0; e < EPL; ++e)
+            store_out<QT>(p.out, (head0 + h) * D + lane * EPL + e, p.out_f32 != 0, a[e] * inv);
         }
       }
     }
 
-    // advance: U1 becomes current; the issue cursor follows it
+    // advance: U1 becomes current; the issue target follows it
     U0 = U1;
     U1.valid = 0;
-    if (cur_u == 1) {
-      cur_u = 0;
-    } else {
-      cur_s = 0;
-    }
+    if (it_which == 1) it_which = 0;
+    else set_target(U0, 0);
     fill();
   }
   // a warp that gave up on a timed-out wait still has copies in flight: let

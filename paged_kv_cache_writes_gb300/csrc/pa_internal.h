@@ -65,6 +65,7 @@ cudaError_t launch_copy_blocks(void *k_cache, void *v_cache, const pa_kv_cache &
 struct PoolMaps {
   CUtensorMap k, v;
 };
+// The decode kernel reads 256-byte rows as one 3D box of two 128-byte panels.
 
 struct DecodeParams;  // pa_decode.cuh
 
