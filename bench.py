@@ -41,6 +41,28 @@ def _peaks():
     return 6800.0, "fallback"
 
 
+def _profiled_traffic(kv_bytes: int):
+    """DRAM bytes per decode launch, scaled from the committed ncu capture of the
+    decode kernel -- or None if the decode sources changed since that capture."""
+    import hashlib
+    import re
+    path = os.path.join(ROOT, "profiles", "paged_decode_kernel__llama70b_decode.md")
+    if not os.path.exists(path):
+        return None
+    text = open(path).read()
+    m1 = re.search(r"traffic_per_kv_byte:\s*([0-9.]+)", text)
+    m2 = re.search(r"source_sha256_16:\s*([0-9a-f]{16})", text)
+    if not (m1 and m2):
+        return None
+    h = hashlib.sha256()
+    for f in ("pa_decode.cuh", "pa_attention.cuh", "pa_common.cuh"):
+        with open(os.path.join(ROOT, "paged_kv_cache_writes_gb300", "csrc", f), "rb") as fh:
+            h.update(fh.read())
+    if h.hexdigest()[:16] != m2.group(1):
+        return None
+    return float(m1.group(1)) * kv_bytes
+
+
 def _config(b, extra=None):
     name = WORKLOAD if b.num_seqs == 256 else f"{WORKLOAD} (reduced to {b.num_seqs} sequences)"
     cfg = {"workload": name, "num_seqs": b.num_seqs, "num_q_heads": b.num_q_heads,
@@ -286,11 +308,12 @@ def run_ours(args):
         "tokens_per_s_per_layer": b.num_seqs * ws / (ms * 1e-3),
         "decode_ms": dec_ms,
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
-                     "traffic": None, "kernel": "paged_attention_kernel (pa_decode)",
+                     "traffic": _profiled_traffic(kv_bytes),
+                     "kernel": "paged_decode_kernel (pa_decode: plan + decode launches, timed together)",
                      "peak_source": f"{peak_kind} hbm_gbs"},
         "e2e": {"value": kv_bytes * ws / (e2e_ms * 1e-3) / 1e9, "unit": UNIT, "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms},
-        "gpu_launches": 2 * args.steps,
+        "gpu_launches": 3 * args.steps,  # per step: cache write, decode plan, decode
         "clocks": clocks.summary(),
     }
     if not args.no_cpu_baseline:
