@@ -12,6 +12,7 @@
 #include "pa_common.cuh"
 #include "pa_decode.cuh"
 #include "pa_internal.h"
+#include "pa_prefill_tc.cuh"
 
 namespace pa {
 
@@ -289,7 +290,41 @@ pa_status pa_prefill_chunk(const void *q_chunk, pa_dtype q_dtype, const int32_t 
   if ((st = check_pools(k_cache, v_cache)) != PA_OK) return st;
   const int64_t rows = (int64_t)num_chunks * max_q_len;
   if (rows > 2147483647ll || num_q_heads > 65535) return PA_ERR_UNSUPPORTED;
+  const bool fp8 = c.kv_dtype == PA_FP8_E4M3;
+  const int gqa = num_q_heads / c.num_kv_heads;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
 
+  if (prefill_tc_supported(c.head_dim, gqa)) {
+    // tensor-core tiles: 128 GQA-packed rows x 64-key tiles (pa_prefill_tc.cuh)
+    PrefillTcParams t{};
+    t.q = q_chunk;
+    t.out = out;
+    t.out_f32 = out_dtype == PA_F32;
+    t.cu_q_lens = cu_q_lens;
+    t.q_start = q_start;
+    t.seq_lens = seq_lens;
+    t.block_tables = block_tables;
+    t.max_blocks_per_seq = max_blocks_per_seq;
+    t.max_q_len = max_q_len;
+    t.num_q_heads = num_q_heads;
+    t.num_kv_heads = c.num_kv_heads;
+    t.block_size = c.block_size;
+    t.num_blocks = c.num_blocks;
+    t.s_mult = scale * 1.4426950408889634f * (fp8 ? c.k_scale : 1.f);
+    t.out_mult = fp8 ? c.v_scale : 1.f;
+    t.err = device_error_word();
+    PoolMaps maps;
+    if (!t.err || !encode_pool_map(&maps.k, k_cache, c) || !encode_pool_map(&maps.v, v_cache, c))
+      return PA_ERR_CUDA;
+    cudaError_t e;
+    if (c.kv_dtype == PA_BF16) e = launch_prefill_tc_bf16(t, maps, gqa, num_chunks, s);
+    else if (c.kv_dtype == PA_F16) e = launch_prefill_tc_f16(t, maps, gqa, num_chunks, s);
+    else if (q_dtype == PA_BF16) e = launch_prefill_tc_fp8_bf16q(t, maps, gqa, num_chunks, s);
+    else e = launch_prefill_tc_fp8_f16q(t, maps, gqa, num_chunks, s);
+    return e == cudaSuccess ? PA_OK : PA_ERR_CUDA;
+  }
+
+  // head_dim 64 or an uneven GQA group: one CTA per query row on the CUDA cores
   AttnParams p{};
   p.q = q_chunk;
   p.out = out;
@@ -306,7 +341,6 @@ pa_status pa_prefill_chunk(const void *q_chunk, pa_dtype q_dtype, const int32_t 
   p.num_blocks = c.num_blocks;
   p.partition_size = std::max(32, (max_seq_len + 31) / 32 * 32);  // one partition per row
   p.max_partitions = 1;
-  const bool fp8 = c.kv_dtype == PA_FP8_E4M3;
   p.q_mult = scale * 1.4426950408889634f * (fp8 ? c.k_scale : 1.f);
   p.out_mult = fp8 ? c.v_scale : 1.f;
   p.out_f32 = out_dtype == PA_F32;
@@ -314,8 +348,7 @@ pa_status pa_prefill_chunk(const void *q_chunk, pa_dtype q_dtype, const int32_t 
   PoolMaps maps;
   if (!p.err || !encode_pool_map(&maps.k, k_cache, c) || !encode_pool_map(&maps.v, v_cache, c))
     return PA_ERR_CUDA;
-  return dispatch_attention(q_dtype, c, p, maps, (int)rows, reinterpret_cast<cudaStream_t>(stream)) ==
-                 cudaSuccess
+  return dispatch_attention(q_dtype, c, p, maps, (int)rows, s) == cudaSuccess
              ? PA_OK
              : PA_ERR_CUDA;
 }

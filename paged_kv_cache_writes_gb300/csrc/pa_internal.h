@@ -67,7 +67,8 @@ struct PoolMaps {
 };
 // The decode kernel reads 256-byte rows as one 3D box of two 128-byte panels.
 
-struct DecodeParams;  // pa_decode.cuh
+struct DecodeParams;     // pa_decode.cuh
+struct PrefillTcParams;  // pa_prefill_tc.cuh
 
 // Launch the CUDA-core prefill-row kernel / the persistent decode for one (kv dtype, q dtype).
 cudaError_t launch_attention_bf16(const AttnParams &p, const PoolMaps &m, int head_dim, int rows,
@@ -86,5 +87,18 @@ cudaError_t launch_decode_fp8_bf16q(const DecodeParams &p, int hpc, const PoolMa
                                     cudaStream_t s);
 cudaError_t launch_decode_fp8_f16q(const DecodeParams &p, int hpc, const PoolMaps &m, int head_dim,
                                    cudaStream_t s);
+
+// Tensor-core chunked prefill (head_dim 128; gqa = Hq / Hkv in {1, 2, 4, 8, 16}).
+constexpr bool prefill_tc_supported(int head_dim, int gqa) {
+  return head_dim == 128 && (gqa == 1 || gqa == 2 || gqa == 4 || gqa == 8 || gqa == 16);
+}
+cudaError_t launch_prefill_tc_bf16(const PrefillTcParams &p, const PoolMaps &m, int gqa, int num_chunks,
+                                   cudaStream_t s);
+cudaError_t launch_prefill_tc_f16(const PrefillTcParams &p, const PoolMaps &m, int gqa, int num_chunks,
+                                  cudaStream_t s);
+cudaError_t launch_prefill_tc_fp8_bf16q(const PrefillTcParams &p, const PoolMaps &m, int gqa, int num_chunks,
+                                        cudaStream_t s);
+cudaError_t launch_prefill_tc_fp8_f16q(const PrefillTcParams &p, const PoolMaps &m, int gqa, int num_chunks,
+                                       cudaStream_t s);
 
 }  // namespace pa

@@ -2,9 +2,13 @@
 
 Row r of a chunk at absolute position q_start + r attends causally to
 positions 0 .. q_start + r of its sequence.  Small batches are compared on
-every row; the 512-row chunk of the mixed fp8 workload is compared on sampled
-rows, each of which the oracle computes as a decode with seq_len =
-q_start + r + 1 (the pinned identity "last row of a chunk = decode")."""
+every row; the 512-row chunks (mixed fp8 workload, long bf16/f16 chunks) are
+compared on sampled rows, each of which the oracle computes as a decode with
+seq_len = q_start + r + 1 (the pinned identity "last row of a chunk = decode").
+
+head_dim 128 with a GQA group of 1, 2, 4, 8 or 16 runs on the tensor-core
+kernel (128 GQA-packed rows per CTA, 64-key tiles); head_dim 64 and other
+groups run on the CUDA-core row kernel.  Both are covered here."""
 import numpy as np
 import pytest
 import torch
@@ -61,5 +65,77 @@ def test_prefill_seq_len_mismatch_sets_error():
     dev.run_setup()
     dev.write_step()
     dev.prefill["seq_lens"][0] += 1
+    dev.prefill_chunk()
+    assert pa.pa_get_device_error() == 4
+
+
+# chunks that cross the 128-packed-row CTA boundary for every group size, a
+# chunk of one row at position 0, an empty chunk, and contexts that end
+# inside a 64-key tile and inside a block
+RAGGED_CHUNKS = [(0, 1), (0, 77), (45, 0), (300, 129), (1000, 8), (63, 65)]
+
+
+@pytest.mark.parametrize("src,kv", [("bf16", "bf16"), ("f16", "f16"), ("bf16", "fp8"), ("f16", "fp8")])
+@pytest.mark.parametrize("hq,hkv,bs", [(8, 8, 16), (16, 8, 32), (64, 8, 16), (32, 2, 16)])
+def test_prefill_tensor_core_groups(src, kv, hq, hkv, bs):
+    b = W.prefill_batch("p", RAGGED_CHUNKS, hq, hkv, 128, bs, src, kv_dtype=kv, seed=hq * 3 + hkv + bs)
+    dev = run_gpu(b)
+    kp, vp = oracle_pools(b)
+    ref = oracle.prefill_batch(b, kp, vp)
+    assert max_err(dev.prefill["out"], ref) <= TOL[kv]
+
+
+def test_prefill_uneven_group_uses_row_kernel():
+    # GQA group 3 at head_dim 128: the CUDA-core path
+    b = W.prefill_batch("p", [(0, 20), (90, 33)], 24, 8, 128, 16, "bf16", seed=77)
+    dev = run_gpu(b)
+    kp, vp = oracle_pools(b)
+    assert max_err(dev.prefill["out"], oracle.prefill_batch(b, kp, vp)) <= TOL["bf16"]
+
+
+@pytest.mark.parametrize("src,kv", [("f16", "f16"), ("bf16", "fp8"), ("f16", "fp8")])
+def test_prefill_tensor_core_query_dtype_output(src, kv):
+    b = W.prefill_batch("p", [(0, 37), (200, 100)], 32, 8, 128, 16, src, kv_dtype=kv, seed=19)
+    dev = run_gpu(b, out_dtype="q")
+    kp, vp = oracle_pools(b)
+    ref = oracle.prefill_batch(b, kp, vp)
+    assert rounded_excess(dev.prefill["out"], ref, src, TOL[kv]) <= 0
+
+
+@pytest.mark.parametrize("src,hq", [("bf16", 64), ("f16", 32)])
+def test_prefill_long_chunk_sampled_rows(src, hq):
+    # a 512-row chunk over 4096 tokens of context, Llama-shaped GQA (8 KV heads)
+    b = W.prefill_batch("p", [(4096, 512)], hq, 8, 128, 16, src, seed=23)
+    dev = run_gpu(b)
+    kp, vp = oracle_pools(b)
+    p = b.prefill
+    rows = np.unique(np.concatenate([np.arange(0, 512, 29), [0, 1, 127, 128, 511]]))
+    qs = int(p.q_start[0])
+    ref = oracle.decode(p.q[rows], {"bf16": oracle.BF16, "f16": oracle.F16}[src], kp, vp,
+                        {"bf16": oracle.BF16, "f16": oracle.F16}[src],
+                        np.repeat(p.block_tables, len(rows), axis=0), (qs + rows + 1).astype(np.int32),
+                        b.scale, 1.0, 1.0)
+    got = dev.prefill["out"][torch.as_tensor(rows, device="cuda")]
+    assert max_err(got, ref) <= TOL[src]
+
+
+@pytest.mark.parametrize("kv", ["bf16", "fp8"])
+def test_prefill_tensor_core_metadata_errors(kv):
+    import paged_kv_cache_writes_gb300 as pa
+    from paged_kv_cache_writes_gb300.staging import DeviceBatch
+    b = W.prefill_batch("p", [(40, 70), (10, 5)], 32, 8, 128, 16, "bf16", kv_dtype=kv, seed=31)
+    dev = DeviceBatch(b, "cuda")
+    dev.run_setup()
+    dev.write_step()
+    dev.prefill_chunk()
+    assert pa.pa_get_device_error() == 0
+    dev.prefill["seq_lens"][1] += 1                     # seq_len != q_start + chunk length
+    dev.prefill_chunk()
+    assert pa.pa_get_device_error() == 4
+    dev.prefill["seq_lens"][1] -= 1
+    dev.prefill["block_tables"][0, 3] = b.num_blocks + 5  # out-of-range block id
+    dev.prefill_chunk()
+    assert pa.pa_get_device_error() == 4
+    dev.prefill["block_tables"][0, 3] = -2
     dev.prefill_chunk()
     assert pa.pa_get_device_error() == 4
