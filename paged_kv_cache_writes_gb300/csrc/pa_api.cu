@@ -298,6 +298,8 @@ pa_status pa_prefill_chunk(const void *q_chunk, pa_dtype q_dtype, const int32_t 
     // tensor-core tiles: 128 GQA-packed rows x 64-key tiles (pa_prefill_tc.cuh)
     PrefillTcParams t{};
     t.q = q_chunk;
+    t.k_cache = k_cache;
+    t.v_cache = v_cache;
     t.out = out;
     t.out_f32 = out_dtype == PA_F32;
     t.cu_q_lens = cu_q_lens;
@@ -313,14 +315,12 @@ pa_status pa_prefill_chunk(const void *q_chunk, pa_dtype q_dtype, const int32_t 
     t.s_mult = scale * 1.4426950408889634f * (fp8 ? c.k_scale : 1.f);
     t.out_mult = fp8 ? c.v_scale : 1.f;
     t.err = device_error_word();
-    PoolMaps maps;
-    if (!t.err || !encode_pool_map(&maps.k, k_cache, c) || !encode_pool_map(&maps.v, v_cache, c))
-      return PA_ERR_CUDA;
+    if (!t.err) return PA_ERR_CUDA;
     cudaError_t e;
-    if (c.kv_dtype == PA_BF16) e = launch_prefill_tc_bf16(t, maps, gqa, num_chunks, s);
-    else if (c.kv_dtype == PA_F16) e = launch_prefill_tc_f16(t, maps, gqa, num_chunks, s);
-    else if (q_dtype == PA_BF16) e = launch_prefill_tc_fp8_bf16q(t, maps, gqa, num_chunks, s);
-    else e = launch_prefill_tc_fp8_f16q(t, maps, gqa, num_chunks, s);
+    if (c.kv_dtype == PA_BF16) e = launch_prefill_tc_bf16(t, gqa, num_chunks, s);
+    else if (c.kv_dtype == PA_F16) e = launch_prefill_tc_f16(t, gqa, num_chunks, s);
+    else if (q_dtype == PA_BF16) e = launch_prefill_tc_fp8_bf16q(t, gqa, num_chunks, s);
+    else e = launch_prefill_tc_fp8_f16q(t, gqa, num_chunks, s);
     return e == cudaSuccess ? PA_OK : PA_ERR_CUDA;
   }
 

@@ -11,36 +11,42 @@
 // KV Cache Bottleneck in LLM Serving"), so Q.K^T and P.V run as dense tiles on
 // the tensor pipe; the softmax stays in fp32 on the CUDA cores.
 //
-// Tiling.  One CTA = 128 GQA-packed query rows (128/G token rows x the G query
-// heads of one KV head; packed row m = token m / G, head m % G) x every key
-// tile of 64 keys up to its causal limit, so each K/V byte a CTA reads feeds
-// all G heads.
+// Tiling.  One CTA = two Q tiles of 128 GQA-packed query rows (256/G token
+// rows x the G query heads of one KV head; packed row m = token m / G, head
+// m % G; tile m / 128) x every key tile of 64 keys up to its causal limit.
+// Each K/V tile feeds both Q tiles and all G heads.
 //
-// Roles (288 threads):
-//  * warps 0-3, softmax: thread m owns packed row m = tensor-memory lane m.  It
-//    reads its 64 scores of a tile with tcgen05.ld, scales and masks them,
-//    keeps a lazy reference maximum (its O row in tensor memory is rescaled
-//    only when a tile maximum exceeds the reference by more than 2^8), and
-//    writes its row of P (16-bit, 128-byte-swizzled, K-major) for the P.V MMA.
-//  * warp 4, loads: TMA boxes of 16 keys (one block-table entry) x one
-//    128-byte panel into a ring of kStages K and V tiles.
-//  * warps 5-7, tile preparation: fp8 tiles are widened (exactly) to the
-//    query's 16-bit type; V rows past the end of the sequence are zeroed so a
-//    zero probability never meets a stale (possibly NaN) value in the MMA.
-//  * warp 8, MMA (one thread): S_j = Q K_j^T into one of two tensor-memory
-//    score buffers, then O += P_{j-1} V_{j-1} one tile behind, so the tensor
-//    pipe computes a score tile while the softmax warps work on the previous.
+// Roles (416 threads):
+//  * warps 0-3 / 4-7, softmax of Q tile 0 / 1: thread m owns packed row m
+//    (tensor-memory lane m % 128).  It reads its 64 scores with tcgen05.ld,
+//    masks and scales them, keeps a lazy reference maximum (its O row in
+//    tensor memory is rescaled only when a tile maximum exceeds the reference
+//    by more than 2^8), and writes its row of P (16-bit pairs) back over the
+//    scores with tcgen05.st: the P.V MMA reads P straight from tensor memory.
+//  * warps 8-11, loads: each warp gathers 16 rows (keys inside one block of
+//    the block table) of every K and V tile into a ring of kStages tiles,
+//    512 contiguous bytes per warp instruction.  16-bit caches: 16-byte
+//    cp.async straight into the 128-byte-swizzled MMA layout; fp8 caches:
+//    register loads one tile ahead, widened exactly to the query's 16-bit
+//    type on the way to shared memory.  Rows past the end of the sequence are
+//    zero-filled so a zero probability never meets a stale (possibly NaN)
+//    value in the MMA.
+//  * warp 12, MMA (one elected lane issues): per key tile j, S_t(j) = Q_t K_j^T
+//    for both Q tiles into one of each tile's two score buffers, then
+//    O_t += P_t(j-1) V_{j-1}; the tensor pipe computes the next scores while
+//    the softmax warps work on the current ones, and the two Q tiles' softmax
+//    phases overlap each other.
 //
 // Precision.  Q, K and V are exact in the MMA (fp8 codes widen exactly to
 // bf16/f16); accumulation is fp32.  P is rounded to the 16-bit type; with a
 // bf16 cache P is split into hi + lo bf16 parts (two P.V MMAs) so its
-// rounding stays near 2^-16 relative, and with f16 or fp8 caches the softmax
+// rounding stays below 2^-16 relative, and with f16 or fp8 caches the softmax
 // denominator sums the rounded P, so the output remains a convex combination
 // of V rows.
 //
 // Every mbarrier wait is bounded (PA_ERR_TIMEOUT, then the CTA abandons its
 // work); before tensor memory is freed the CTA waits for its outstanding MMAs
-// and TMA copies.
+// and copies.
 #pragma once
 
 #include <type_traits>
@@ -52,6 +58,8 @@ namespace pa {
 
 struct PrefillTcParams {
   const void *q;               // [total_q][Hq][128]
+  const void *k_cache;         // [num_blocks][Hkv][block_size][128]
+  const void *v_cache;
   void *out;                   // [total_q][Hq][128]
   int32_t out_f32;
   const int32_t *cu_q_lens;
@@ -65,7 +73,7 @@ struct PrefillTcParams {
   int32_t num_kv_heads;
   int32_t block_size;
   int64_t num_blocks;
-  float s_mult;                // scale * log2(e) (* k_scale for fp8)
+  float s_mult;                // scale * log2(e) (* k_scale for fp8); a negative value flips q's sign
   float out_mult;              // v_scale for fp8, else 1
   int32_t *err;
 };
@@ -73,30 +81,34 @@ struct PrefillTcParams {
 namespace tc {
 
 constexpr int kD = 128;         // head_dim
-constexpr int kM = 128;         // packed query rows per CTA (MMA M, tensor-memory lanes)
+constexpr int kM = 128;         // packed query rows per Q tile (MMA M, tensor-memory lanes)
 constexpr int kN = 64;          // keys per tile
 constexpr int kStages = 3;      // K/V tiles in flight
-constexpr int kThreads = 288;
+
+// Warp roles and tensor-memory size for a CTA of QT Q tiles (1 or 2).
+template <int QT>
+struct Roles {
+  static constexpr int kSoftmax = QT * 128;           // softmax threads (warps 0 .. 4*QT-1)
+  static constexpr int kLoadWarp0 = kSoftmax / 32;    // the next 4 warps load
+  static constexpr int kMmaWarp = kLoadWarp0 + 4;     // the last warp issues the MMAs
+  static constexpr int kThreads = (kMmaWarp + 1) * 32;
+  static constexpr int kTmemCols = QT * 256;          // per Q tile: 2 score/P buffers of 64 columns; then the O tiles
+};
 constexpr float kRescaleLog2 = 8.f;
 
-constexpr int kQBytes = kM * kD * 2;        // 2 panels x [128 rows x 128 B]
+constexpr int kQBytes = kM * kD * 2;        // one Q tile: 2 panels x [128 rows x 128 B]
 constexpr int kTileBytes = kN * kD * 2;     // 2 panels x [64 rows x 128 B]
 constexpr int kTilePanel = kN * 128;        // 8 KB
-constexpr int kPPanel = kM * kN * 2;        // [128 rows x 128 B] = 16 KB
-constexpr int kRawBytes = kN * kD;          // fp8 tile: [64 rows x 128 B]
-constexpr int kNumBars = 8 * kStages + 10;
+constexpr int kLoaders = 128;               // threads of the load warps
+constexpr int kNumBars = 4 * kStages + 3 * 2 * 2 + 2;
 
 // Shared-memory map, bytes from a 1024-aligned base (128-byte swizzle atoms).
-template <bool kFp8, bool kSplit>
+template <int QT>
 struct Layout {
-  static constexpr int kPBuf = (kSplit ? 2 : 1) * kPPanel;  // one P buffer (hi [+ lo] panel)
   static constexpr int kOffQ = 0;
-  static constexpr int kOffK = kOffQ + kQBytes;
+  static constexpr int kOffK = kOffQ + QT * kQBytes;
   static constexpr int kOffV = kOffK + kStages * kTileBytes;
-  static constexpr int kOffP = kOffV + kStages * kTileBytes;
-  static constexpr int kOffRawK = kOffP + 2 * kPBuf;
-  static constexpr int kOffRawV = kOffRawK + (kFp8 ? kStages * kRawBytes : 0);
-  static constexpr int kOffBar = kOffRawV + (kFp8 ? kStages * kRawBytes : 0);
+  static constexpr int kOffBar = kOffV + kStages * kTileBytes;
   static constexpr int kOffMisc = kOffBar + kNumBars * 8;
   static constexpr int kSmemBytes = kOffMisc + 64 + 1024;  // + alignment slack
   static_assert(kSmemBytes <= 227 * 1024, "shared memory");
@@ -153,6 +165,26 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, float (&v)[32]) {
   for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
 }
 
+// 16 consecutive 32-bit columns of this thread's tensor-memory lane (warp-collective).
+__device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&v)[16]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16};" ::"r"(
+          taddr),
+      "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7]), "r"(v[8]), "r"(v[9]),
+      "r"(v[10]), "r"(v[11]), "r"(v[12]), "r"(v[13]), "r"(v[14]), "r"(v[15])
+      : "memory");
+}
+__device__ __forceinline__ void tmem_wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
+
+// A operand in tensor memory (P): O[tmem_d] (+)= A[tmem_a] * B[desc].
+__device__ __forceinline__ void umma_ts(uint32_t tmem_d, uint32_t tmem_a, uint64_t b, uint32_t idesc, uint32_t acc) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(tmem_d),
+      "r"(tmem_a), "l"(b), "r"(idesc), "r"(acc)
+      : "memory");
+}
+
 __device__ __forceinline__ void tmem_st32(uint32_t taddr, const float (&v)[32]) {
   asm volatile(
       "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,"
@@ -182,6 +214,22 @@ __device__ __forceinline__ uint32_t pack2(float a, float b, __half) {
   return *reinterpret_cast<uint32_t *>(&h);
 }
 
+// True in exactly one lane of the (fully active) warp, the same lane every time.
+__device__ __forceinline__ bool elect_one() {
+  uint32_t pred;
+  asm volatile("{\n\t.reg .pred P;\n\telect.sync _|P, 0xffffffff;\n\tselp.u32 %0, 1, 0, P;\n\t}" : "=r"(pred));
+  return pred != 0;
+}
+
+// bf16 bits of a non-negative-or-any finite fp32 value rounded to 8 significant
+// bits (ties away from zero), kept in the upper half of the fp32 bit pattern
+// so that the result is also the rounded value as an fp32.
+__device__ __forceinline__ uint32_t bf16_round_bits(float x) {
+  return (__float_as_uint(x) + 0x8000u) & 0xffff0000u;
+}
+// Pack the upper halves of two fp32 bit patterns into one bf16x2 word (a low, b high).
+__device__ __forceinline__ uint32_t pack_hi_halves(uint32_t a, uint32_t b) { return __byte_perm(a, b, 0x7632); }
+
 // Bounded wait that also gives up once another role of the CTA has given up.
 __device__ __forceinline__ bool wait_or_abort(uint64_t *bar, uint32_t parity, int32_t *err,
                                               volatile int *abort_flag) {
@@ -191,39 +239,60 @@ __device__ __forceinline__ bool wait_or_abort(uint64_t *bar, uint32_t parity, in
   return false;
 }
 
-// Widen 16 e4m3 codes (swizzled 16-byte chunk `ch` of raw row r) into 16
-// elements of row r of the 16-bit tile (two 16-byte chunks of panel ch / 4).
+// 16-byte global -> shared copy that bypasses L1; src_bytes 0 writes zeros
+// (and reads nothing).
+__device__ __forceinline__ void cp_async16(void *dst, const void *src, uint32_t src_bytes) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(smem_u32(dst)), "l"(src), "r"(src_bytes)
+               : "memory");
+}
+// One arrival on `bar` once every cp.async this thread issued so far has landed
+// (the arrival is counted in the barrier's initial count).
+__device__ __forceinline__ void cp_async_arrive_noinc(uint64_t *bar) {
+  asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(smem_u32(bar)) : "memory");
+}
+__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;" ::: "memory"); }
+
+__device__ __forceinline__ uint4 ld_nc16(const void *p) {
+  uint4 v;
+  asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0, %1, %2, %3}, [%4];"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+               : "l"(p));
+  return v;
+}
+
+// 16 e4m3 codes (one 16-byte word) -> 16 elements of the query's 16-bit type,
+// exactly (e4m3 -> f16 is exact, and every e4m3 value is a bf16 value).
 template <typename QT>
-__device__ __forceinline__ void widen_chunk(const uint8_t *raw_row, uint8_t *tile, int r, int ch, bool zero) {
-  uint32_t o[8] = {0, 0, 0, 0, 0, 0, 0, 0};
-  if (!zero) {
-    const uint4 w = *reinterpret_cast<const uint4 *>(raw_row + ((ch ^ (r & 7)) << 4));
-    const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
+__device__ __forceinline__ void widen16(uint4 w, uint32_t (&o)[8]) {
+  const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
 #pragma unroll
-    for (int i = 0; i < 4; ++i) {
+  for (int i = 0; i < 4; ++i) {
+    if constexpr (std::is_same<QT, __half>::value) {
+      const __half2_raw lo = __nv_cvt_fp8x2_to_halfraw2(static_cast<__nv_fp8x2_storage_t>(ws[i] & 0xffffu), __NV_E4M3);
+      const __half2_raw hi = __nv_cvt_fp8x2_to_halfraw2(static_cast<__nv_fp8x2_storage_t>(ws[i] >> 16), __NV_E4M3);
+      o[2 * i] = *reinterpret_cast<const uint32_t *>(&lo);
+      o[2 * i + 1] = *reinterpret_cast<const uint32_t *>(&hi);
+    } else {
       const float2 lo = unpack2_e4m3(ws[i]), hi = unpack2_e4m3(ws[i] >> 16);
       o[2 * i] = pack2(lo.x, lo.y, QT{});
       o[2 * i + 1] = pack2(hi.x, hi.y, QT{});
     }
   }
-  const int c0 = (2 * ch) & 7;
-  uint8_t *row = tile + (ch >> 2) * kTilePanel + r * 128;
-  *reinterpret_cast<uint4 *>(row + ((c0 ^ (r & 7)) << 4)) = make_uint4(o[0], o[1], o[2], o[3]);
-  *reinterpret_cast<uint4 *>(row + (((c0 + 1) ^ (r & 7)) << 4)) = make_uint4(o[4], o[5], o[6], o[7]);
 }
 
 }  // namespace tc
 
-template <typename KV, typename QT, int G>
-__global__ void __launch_bounds__(tc::kThreads, 1)
-    prefill_tc_kernel(const PrefillTcParams p, const __grid_constant__ CUtensorMap tmap_k,
-                      const __grid_constant__ CUtensorMap tmap_v) {
+template <typename KV, typename QT, int G, int kQTiles>
+__global__ void __launch_bounds__(tc::Roles<kQTiles>::kThreads, 1) prefill_tc_kernel(const PrefillTcParams p) {
   using namespace tc;
+  using L = Layout<kQTiles>;
+  using R = Roles<kQTiles>;
+  constexpr int kSoftmax = R::kSoftmax, kLoadWarp0 = R::kLoadWarp0, kMmaWarp = R::kMmaWarp;
+  constexpr int kTmemCols = R::kTmemCols;
   constexpr bool kFp8 = std::is_same<KV, uint8_t>::value;
   constexpr bool kBf16 = std::is_same<QT, __nv_bfloat16>::value;
   constexpr bool kSplit = kBf16 && !kFp8;   // bf16 cache: P as hi + lo
-  using L = Layout<kFp8, kSplit>;
-  constexpr int BR = kM / G;                // token rows per CTA
+  constexpr int BR = kQTiles * kM / G;      // token rows per CTA
   constexpr uint32_t kAB = kBf16 ? 1u : 0u;
   const float kNegInf = -__int_as_float(0x7f800000);
 
@@ -231,20 +300,15 @@ __global__ void __launch_bounds__(tc::kThreads, 1)
   uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                               ~uintptr_t(1023));
   uint64_t *bars = reinterpret_cast<uint64_t *>(smem + L::kOffBar);
-  uint64_t *k_tma = bars;                      // [kStages] TMA bytes of a K tile landed
-  uint64_t *v_tma = k_tma + kStages;           // [kStages]
-  uint64_t *k_ready = v_tma + kStages;         // [kStages] fp8: widened K tile written (96)
-  uint64_t *v_ready = k_ready + kStages;       // [kStages] V tile ready for the MMA (96)
-  uint64_t *k_free = v_ready + kStages;        // [kStages] MMA finished reading the K tile
-  uint64_t *v_free = k_free + kStages;         // [kStages] MMA finished reading the V tile
-  uint64_t *raw_k_free = v_free + kStages;     // [kStages] fp8: raw K tile consumed (96)
-  uint64_t *raw_v_free = raw_k_free + kStages; // [kStages]
-  uint64_t *s_full = raw_v_free + kStages;     // [2] score tile in tensor memory
-  uint64_t *s_free = s_full + 2;               // [2] score tile read by the softmax warps (128)
-  uint64_t *p_full = s_free + 2;               // [2] P tile written (128)
-  uint64_t *o_done = p_full + 2;               // [2] P.V group i done -> o_done[i & 1]
-  uint64_t *q_ready = o_done + 2;              // Q staged (128)
-  uint64_t *fin = q_ready + 1;                 // every MMA of the CTA complete
+  uint64_t *k_full = bars;                       // [kStages] K tile in shared memory (128 loader arrivals)
+  uint64_t *v_full = k_full + kStages;           // [kStages] V tile (128)
+  uint64_t *k_free = v_full + kStages;           // [kStages] MMAs finished reading the K tile
+  uint64_t *v_free = k_free + kStages;           // [kStages] MMAs finished reading the V tile
+  uint64_t *s_full = v_free + kStages;           // [tile][buf] scores in tensor memory
+  uint64_t *p_full = s_full + 2 * kQTiles;       // [tile][buf] P written over them (128 arrivals)
+  uint64_t *o_done = p_full + 2 * kQTiles;       // [tile][buf] P.V group i of the tile done -> buf i & 1
+  uint64_t *q_ready = o_done + 2 * kQTiles;      // Q staged (every softmax thread)
+  uint64_t *fin = q_ready + 1;                   // every MMA of the CTA complete
   uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + L::kOffMisc);
   volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + L::kOffMisc + 8);
 
@@ -272,157 +336,170 @@ __global__ void __launch_bounds__(tc::kThreads, 1)
 
   if (tid == 0) {
     for (int s = 0; s < kStages; ++s) {
-      mbar_init(&k_tma[s], 1);
-      mbar_init(&v_tma[s], 1);
-      mbar_init(&k_ready[s], 96);
-      mbar_init(&v_ready[s], 96);
+      mbar_init(&k_full[s], kLoaders);
+      mbar_init(&v_full[s], kLoaders);
       mbar_init(&k_free[s], 1);
       mbar_init(&v_free[s], 1);
-      mbar_init(&raw_k_free[s], 96);
-      mbar_init(&raw_v_free[s], 96);
     }
-    for (int b = 0; b < 2; ++b) {
-      mbar_init(&s_full[b], 1);
-      mbar_init(&s_free[b], 128);
-      mbar_init(&p_full[b], 128);
-      mbar_init(&o_done[b], 1);
+    for (int i = 0; i < 2 * kQTiles; ++i) {
+      mbar_init(&s_full[i], 1);
+      mbar_init(&p_full[i], 128);
+      mbar_init(&o_done[i], 1);
     }
-    mbar_init(q_ready, 128);
+    mbar_init(q_ready, kSoftmax);
     mbar_init(fin, 1);
     *abort_flag = 0;
     fence_mbar_init();
   }
-  if (warp == 8) {  // tensor memory: S0 cols [0,64), S1 [64,128), O [128,256)
-    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], 256;" ::"r"(smem_u32(tmem_slot)));
+  if (warp == kMmaWarp) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(tmem_slot)),
+                 "n"(kTmemCols));
     asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;");
-  }
-  if (warp == 4 && lane == 0) {
-    prefetch_tensor_map(&tmap_k);
-    prefetch_tensor_map(&tmap_v);
   }
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
-  const uint32_t tmem_o = tmem + 2 * kN;
+  // columns: tile t's score/P buffer b at t*128 + b*64; tile t's O at QT*128 + t*128
+  auto sbuf = [&](int t, int b) { return tmem + (uint32_t)(t * 2 * kN + b * kN); };
+  auto obuf = [&](int t) { return tmem + (uint32_t)(kQTiles * 2 * kN + t * kD); };
 
-  if (warp < 4) {
-    // ===================================================== softmax warps
-    const int m = tid;                         // packed row = tensor-memory lane
+  if (warp < kLoadWarp0) {
+    // ===================================================== softmax warps (Q tile t = warp / 4)
+    const int m = tid;                         // packed row
+    const int t = m / kM;
     const int rl = m / G, hq = m % G;
     const bool row_ok = r0 + rl < nrows;
     const int head = g * G + hq;
     // keys this row attends to: positions < lim
     const int lim = row_ok ? min(seq_eff, max(0, qs + r0 + rl + 1)) : 0;
-    const uint32_t lane_base = (uint32_t)(warp * 32) << 16;
-    {  // stage row m of Q (16-bit, 128-byte-swizzled K-major, 2 panels)
+    const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
+    // scores are scaled by |s_mult| in the exponent; a negative scale flips q's sign instead
+    const float cmul = fabsf(p.s_mult);
+    const uint32_t qflip = p.s_mult < 0.f ? 0x80008000u : 0u;
+    {  // stage row m of Q (16-bit, 128-byte-swizzled K-major, 2 panels per tile)
       const QT *src = static_cast<const QT *>(p.q) + ((int64_t)(cu0 + r0 + rl) * p.num_q_heads + head) * kD;
+      const int mr = m % kM;
+      uint8_t *qt = smem + L::kOffQ + t * kQBytes;
 #pragma unroll
       for (int ch = 0; ch < 16; ++ch) {
-        const uint4 v = row_ok ? __ldg(reinterpret_cast<const uint4 *>(src) + ch) : make_uint4(0, 0, 0, 0);
-        *reinterpret_cast<uint4 *>(smem + L::kOffQ + (ch >> 3) * (kM * 128) + m * 128 +
-                                   (((ch & 7) ^ (m & 7)) << 4)) = v;
+        uint4 v = row_ok ? __ldg(reinterpret_cast<const uint4 *>(src) + ch) : make_uint4(0, 0, 0, 0);
+        v.x ^= qflip; v.y ^= qflip; v.z ^= qflip; v.w ^= qflip;
+        *reinterpret_cast<uint4 *>(qt + (ch >> 3) * (kM * 128) + mr * 128 + (((ch & 7) ^ (mr & 7)) << 4)) = v;
       }
     }
     fence_async_smem();
     mbar_arrive(q_ready);
 
-    float m_ref = kNegInf, l = 0.f;
-    int o_seen = 0;  // P.V groups this thread has seen complete
+    float m_ref = kNegInf;                     // reference maximum, log2 units
+    float2 lacc[4] = {{0.f, 0.f}, {0.f, 0.f}, {0.f, 0.f}, {0.f, 0.f}};   // partial row sums
+    const float2 ones = make_float2(1.f, 1.f);
     bool ok = true;
+    auto wait_all = [&](uint64_t *bar, uint32_t parity) {
+      return __all_sync(0xffffffffu, wait_or_abort(bar, parity, p.err, abort_flag));
+    };
     for (int j = 0; j < nkt; ++j) {
       const int b = j & 1;
-      ok = __all_sync(0xffffffffu, wait_or_abort(&s_full[b], (j >> 1) & 1, p.err, abort_flag));
+      ok = wait_all(&s_full[t * 2 + b], (j >> 1) & 1);
       if (!ok) break;
       tc_fence_after();
+      const uint32_t sb = sbuf(t, b) + lane_base;
       float s[kN];
       {
         float t0[32], t1[32];
-        tmem_ld32(tmem + lane_base + b * kN, t0);
-        tmem_ld32(tmem + lane_base + b * kN + 32, t1);
+        tmem_ld32(sb, t0);
+        tmem_ld32(sb + 32, t1);
 #pragma unroll
         for (int i = 0; i < 32; ++i) {
           s[i] = t0[i];
           s[32 + i] = t1[i];
         }
       }
-      tc_fence_before();
-      mbar_arrive(&s_free[b]);
-      // scale into log2 units; mask keys at or past this row's limit
+      // keys at or past this row's limit are masked, but only tiles that reach
+      // some row's limit (the causal diagonal, the sequence end) need the test
       const int nvis = lim - j * kN;
+      const bool full_tile = __all_sync(0xffffffffu, nvis >= kN);
+      if (!full_tile) {
+#pragma unroll
+        for (int i = 0; i < kN; ++i)
+          if (i >= nvis) s[i] = kNegInf;
+      }
       float mx[8];
 #pragma unroll
-      for (int i = 0; i < kN; ++i) {
-        s[i] = i < nvis ? s[i] * p.s_mult : kNegInf;
-        if (i < 8) mx[i] = s[i];
-        else mx[i & 7] = fmaxf(mx[i & 7], s[i]);
-      }
-      const float mt = fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])),
+      for (int i = 0; i < 8; ++i) mx[i] = fmaxf(s[i], s[i + 8]);
+#pragma unroll
+      for (int i = 16; i < kN; ++i) mx[i & 7] = fmaxf(mx[i & 7], s[i]);
+      const float mr = fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])),
                              fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7])));
+      const float mt = mr == kNegInf ? kNegInf : mr * cmul;   // tile maximum, log2 units
       const bool rescale = mt > m_ref + tc::kRescaleLog2;
-      const bool warp_rescale = __any_sync(0xffffffffu, rescale);
-      // P buffer b was last read by P.V group j-2; rescaling O needs group j-1 done
-      const int need = warp_rescale ? j - 1 : j - 2;
-      while (o_seen <= need) {
-        ok = __all_sync(0xffffffffu,
-                        wait_or_abort(&o_done[o_seen & 1], (o_seen >> 1) & 1, p.err, abort_flag));
-        if (!ok) break;
-        ++o_seen;
-      }
-      if (!ok) break;
-      if (warp_rescale) {
+      if (__any_sync(0xffffffffu, rescale)) {
         const float alpha = rescale ? fast_exp2(m_ref - mt) : 1.f;
-        if (j > 0) {  // O holds groups 0 .. j-1 (no group has run before tile 0)
+        if (j > 0) {
+          // O holds P.V groups 0 .. j-1: wait for the last of them, then rescale in place
+          ok = wait_all(&o_done[t * 2 + ((j - 1) & 1)], ((j - 1) >> 1) & 1);
+          if (!ok) break;
           tc_fence_after();
 #pragma unroll 1
           for (int c0 = 0; c0 < kD; c0 += 32) {
             float o[32];
-            tmem_ld32(tmem_o + lane_base + c0, o);
+            tmem_ld32(obuf(t) + lane_base + c0, o);
 #pragma unroll
             for (int i = 0; i < 32; ++i) o[i] *= alpha;
-            tmem_st32(tmem_o + lane_base + c0, o);
+            tmem_st32(obuf(t) + lane_base + c0, o);
           }
         }
         if (rescale) {
-          l *= alpha;
+#pragma unroll
+          for (int i = 0; i < 4; ++i) lacc[i] = make_float2(lacc[i].x * alpha, lacc[i].y * alpha);
           m_ref = mt;
         }
       }
-      // a row with nothing visible yet keeps m_ref = -inf and all s = -inf
+      // p = 2^(s * |s_mult| - m_ref); a row with nothing visible yet keeps m_ref = -inf
       const float msub = m_ref == kNegInf ? 0.f : m_ref;
-      uint8_t *prow = smem + L::kOffP + b * L::kPBuf + m * 128;
-      float lp[4] = {0.f, 0.f, 0.f, 0.f};
+      const float2 cc = make_float2(cmul, cmul), nm = make_float2(-msub, -msub);
+      // P over the scores: hi words in columns 0..31 of the buffer, lo words (bf16 cache) in 32..63
 #pragma unroll
-      for (int ch = 0; ch < 8; ++ch) {
-        float pv[8];
+      for (int hh = 0; hh < 2; ++hh) {   // keys 32*hh .. 32*hh+31
+        uint32_t w[16], wl[16];
 #pragma unroll
-        for (int i = 0; i < 8; ++i) pv[i] = fast_exp2(s[ch * 8 + i] - msub);  // masked: 2^-inf = 0
-        uint32_t w[4], wl[4];
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-          w[i] = pack2(pv[2 * i], pv[2 * i + 1], QT{});
-          const float2 hi = unpack2(w[i], QT{});
-          if constexpr (kSplit) {
-            wl[i] = pack2(pv[2 * i] - hi.x, pv[2 * i + 1] - hi.y, QT{});
-            lp[i] += pv[2 * i] + pv[2 * i + 1];
+        for (int k = 0; k < 16; ++k) {
+          const int i0 = 32 * hh + 2 * k;
+          const float2 a = ffma2(make_float2(s[i0], s[i0 + 1]), cc, nm);
+          float2 pk = make_float2(fast_exp2(a.x), fast_exp2(a.y));
+          if (!full_tile) {
+            if (i0 >= nvis) pk.x = 0.f;
+            if (i0 + 1 >= nvis) pk.y = 0.f;
+          }
+          if constexpr (kBf16) {
+            // integer rounding keeps the conversion off the transcendental pipe
+            const uint32_t h0 = bf16_round_bits(pk.x), h1 = bf16_round_bits(pk.y);
+            w[k] = pack_hi_halves(h0, h1);
+            const float2 hi = make_float2(__uint_as_float(h0), __uint_as_float(h1));
+            if constexpr (kSplit) {
+              // lo = p - hi is exact in fp32; truncating it to bf16 leaves < 2^-16 relative error in P
+              const float2 lo = ffma2(hi, make_float2(-1.f, -1.f), pk);
+              wl[k] = pack_hi_halves(__float_as_uint(lo.x), __float_as_uint(lo.y));
+              lacc[k & 3] = ffma2(pk, ones, lacc[k & 3]);
+            } else {
+              lacc[k & 3] = ffma2(hi, ones, lacc[k & 3]);   // the rounded P that the MMA will use
+            }
           } else {
-            lp[i] += hi.x + hi.y;   // the rounded P that the MMA will use
+            w[k] = pack2(pk.x, pk.y, QT{});
+            lacc[k & 3] = ffma2(unpack2(w[k], QT{}), ones, lacc[k & 3]);   // the rounded P the MMA uses
           }
         }
-        *reinterpret_cast<uint4 *>(prow + ((ch ^ (m & 7)) << 4)) = make_uint4(w[0], w[1], w[2], w[3]);
-        if constexpr (kSplit)
-          *reinterpret_cast<uint4 *>(prow + kPPanel + ((ch ^ (m & 7)) << 4)) = make_uint4(wl[0], wl[1], wl[2], wl[3]);
+        tmem_st16(sb + 16 * hh, w);
+        if constexpr (kSplit) tmem_st16(sb + 32 + 16 * hh, wl);
       }
-      l += (lp[0] + lp[1]) + (lp[2] + lp[3]);
-      fence_async_smem();
+      tmem_wait_st();
       tc_fence_before();
-      mbar_arrive(&p_full[b]);
+      mbar_arrive(&p_full[t * 2 + b]);
     }
-    // O is complete once every P.V group has finished
-    while (ok && o_seen < nkt) {
-      ok = __all_sync(0xffffffffu, wait_or_abort(&o_done[o_seen & 1], (o_seen >> 1) & 1, p.err, abort_flag));
-      ++o_seen;
-    }
+    const float l = ((lacc[0].x + lacc[0].y) + (lacc[1].x + lacc[1].y)) +
+                    ((lacc[2].x + lacc[2].y) + (lacc[3].x + lacc[3].y));
+    // O is complete once the tile's last P.V group has finished
+    if (ok && nkt > 0) ok = wait_all(&o_done[t * 2 + ((nkt - 1) & 1)], ((nkt - 1) >> 1) & 1);
     if (ok) {
       tc_fence_after();
       const float inv = l > 0.f ? p.out_mult / l : 0.f;
@@ -431,7 +508,7 @@ __global__ void __launch_bounds__(tc::kThreads, 1)
       for (int c0 = 0; c0 < kD; c0 += 32) {
         float o[32];
         if (nkt > 0) {
-          tmem_ld32(tmem_o + lane_base + c0, o);
+          tmem_ld32(obuf(t) + lane_base + c0, o);
         } else {
 #pragma unroll
           for (int i = 0; i < 32; ++i) o[i] = 0.f;
@@ -453,207 +530,244 @@ __global__ void __launch_bounds__(tc::kThreads, 1)
         }
       }
     }
-  } else if (warp == 4) {
-    // ===================================================== TMA loads (lane 0 issues)
-    constexpr int kSub = kN / 16;                          // 16-key boxes per tile
-    constexpr int kPanels = kFp8 ? 1 : 2;
-    constexpr uint32_t kBox = 16 * 128;                    // bytes per box
-    int k_issued = 0, v_issued = 0;                        // tiles whose copies were issued
-    bool ok = true;
-    for (int j = 0; j < nkt && ok; ++j) {
-      const int s = j % kStages;
-      const uint32_t ph_prev = ((j / kStages) - 1) & 1;
-      // lanes 0 .. kSub-1: block id of box `lane` (16 keys inside one block)
-      const int key = j * kN + lane * 16;
-      const bool has = lane < kSub && key < seq_eff;
-      const int32_t blk = has ? __ldg(table + key / p.block_size) : 0;
-      const bool bad = has && (blk < 0 || blk >= p.num_blocks);
-      const uint32_t load_mask = __ballot_sync(0xffffffffu, has && !bad);
-      const uint32_t bad_mask = __ballot_sync(0xffffffffu, bad);
-      if (lane == 0 && bad_mask != 0u) record_error(p.err, PA_ERR_DEVICE_CHECK);
-      const uint32_t tx = __popc(load_mask) * kPanels * kBox;
-      const int32_t y = (blk * p.num_kv_heads + g) * p.block_size + (key % p.block_size);
-      for (int which = 0; which < 2; ++which) {  // 0: K, 1: V
-        if (lane == 0) {
-          uint64_t *freed = which == 0 ? (kFp8 ? &raw_k_free[s] : &k_free[s])
-                                       : (kFp8 ? &raw_v_free[s] : &v_free[s]);
-          if (j >= kStages) ok = wait_or_abort(freed, ph_prev, p.err, abort_flag);
-          if (ok) mbar_arrive_expect_tx_relaxed(which == 0 ? &k_tma[s] : &v_tma[s], tx);
+  } else if (warp < kMmaWarp) {
+    // ===================================================== loaders (4 warps)
+    // Warp lw fills rows 16*lw .. 16*lw+15 of every K and V tile: 16 keys that
+    // lie inside one block of the block table (tiles start at multiples of 64,
+    // blocks hold 16 or 32 keys).
+    const int lw = warp - kLoadWarp0;
+    constexpr int kRowBytes = kFp8 ? kD : 2 * kD;
+    const char *kpool = static_cast<const char *>(p.k_cache);
+    const char *vpool = static_cast<const char *>(p.v_cache);
+    int32_t win = -1;                 // lane l: block id for tile win_base + l (-1: no data)
+    int win_base = -32;
+    // block id of this warp's rows in tile j (warp-uniform j); -1 past the sequence
+    auto block_of = [&](int j) -> int32_t {
+      if (j - win_base >= 32) {
+        win_base = j;
+        const int key = (j + lane) * kN + 16 * lw;
+        win = -1;
+        if (j + lane < nkt && key < seq_eff) {
+          const int32_t bi = __ldg(table + key / p.block_size);
+          if (bi < 0 || bi >= p.num_blocks) record_error(p.err, PA_ERR_DEVICE_CHECK);
+          else win = bi;
         }
-        ok = __shfl_sync(0xffffffffu, (int)ok, 0) != 0;
-        if (!ok) break;
-        if (which == 0) ++k_issued;
-        else ++v_issued;
+      }
+      return __shfl_sync(0xffffffffu, win, j - win_base);
+    };
+    // first cache row of this warp's 16 keys in tile j, and how many of them hold data
+    auto rows_of = [&](int j, int32_t blk, int64_t &row0) -> int {
+      const int key0 = j * kN + 16 * lw;
+      row0 = ((int64_t)max(blk, 0) * p.num_kv_heads + g) * p.block_size + (key0 % p.block_size);
+      return blk < 0 ? 0 : min(16, seq_eff - key0);
+    };
+    bool ok = true;
+    if constexpr (!kFp8) {
+      // 16-bit rows (256 B): per instruction 2 rows x 16 chunks of 16 B
+      const int q = lane & 15, pn = q >> 3, cq = q & 7;
+      for (int j = 0; j < nkt && ok; ++j) {
+        const int s = j % kStages;
+        const uint32_t ph_prev = ((j / kStages) - 1) & 1;
+        int64_t row0;
+        const int nval = rows_of(j, block_of(j), row0);
 #pragma unroll
-        for (int i = 0; i < kSub; ++i) {
-          const int32_t yi = __shfl_sync(0xffffffffu, y, i);
-          if (lane == 0 && ((load_mask >> i) & 1u)) {
-            const CUtensorMap *map = which == 0 ? &tmap_k : &tmap_v;
-            uint64_t *bar = which == 0 ? &k_tma[s] : &v_tma[s];
-            const int base = which == 0 ? (kFp8 ? L::kOffRawK : L::kOffK) : (kFp8 ? L::kOffRawV : L::kOffV);
-            const int stage_bytes = kFp8 ? kRawBytes : kTileBytes;
+        for (int which = 0; which < 2; ++which) {
+          if (j >= kStages)
+            ok = __all_sync(0xffffffffu, wait_or_abort(which ? &v_free[s] : &k_free[s], ph_prev, p.err, abort_flag));
+          if (!ok) break;
+          const char *pool = which ? vpool : kpool;
+          uint8_t *tile = smem + (which ? L::kOffV : L::kOffK) + s * kTileBytes + pn * kTilePanel;
 #pragma unroll
-            for (int pn = 0; pn < kPanels; ++pn)
-              tma_load_2d(smem + base + s * stage_bytes + pn * kTilePanel + i * kBox, map, bar, pn * 64, yi);
+          for (int i = 0; i < 8; ++i) {
+            const int r = 2 * i + (lane >> 4);          // row among the warp's 16
+            const int row = 16 * lw + r;                 // row of the tile
+            const bool v = r < nval;
+            const char *src = v ? pool + (row0 + r) * kRowBytes + q * 16 : pool;
+            cp_async16(tile + row * 128 + ((cq ^ (row & 7)) << 4), src, v ? 16u : 0u);
           }
+          cp_async_arrive_noinc(which ? &v_full[s] : &k_full[s]);
         }
       }
-    }
-    // before exit: every copy issued has landed (last phase of each stage)
-    if (lane == 0) {
-      for (int t = max(0, k_issued - kStages); t < k_issued; ++t) mbar_wait(&k_tma[t % kStages], (t / kStages) & 1, p.err);
-      for (int t = max(0, v_issued - kStages); t < v_issued; ++t) mbar_wait(&v_tma[t % kStages], (t / kStages) & 1, p.err);
-      // bf16/f16 tiles: the MMA's releases of the last tiles have arrived
-      if (!kFp8 && ok) {
-        for (int t = max(0, nkt - kStages); t < nkt; ++t) {
-          wait_or_abort(&k_free[t % kStages], (t / kStages) & 1, p.err, abort_flag);
-          wait_or_abort(&v_free[t % kStages], (t / kStages) & 1, p.err, abort_flag);
+    } else {
+      // fp8 rows (128 B): per instruction 4 rows x 8 words of 16 codes, loaded one tile ahead
+      const int q = lane & 7, pn = q >> 2, c0 = (2 * q) & 7;
+      uint4 rk[4], rv[4];
+      auto load = [&](int j, uint4 (&ok4)[4], uint4 (&ov4)[4]) {
+        int64_t row0;
+        const int nval = rows_of(j, block_of(j), row0);
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          const int r = 4 * i + (lane >> 3);
+          const bool v = r < nval;
+          ok4[i] = v ? ld_nc16(kpool + (row0 + r) * kRowBytes + q * 16) : make_uint4(0, 0, 0, 0);
+          ov4[i] = v ? ld_nc16(vpool + (row0 + r) * kRowBytes + q * 16) : make_uint4(0, 0, 0, 0);
         }
-      }
-    }
-    __syncwarp();
-  } else if (warp < 8) {
-    // ===================================================== tile preparation (96 threads)
-    const int t = tid - 160;
-    bool ok = true;
-    for (int j = 0; j < nkt && ok; ++j) {
-      const int s = j % kStages;
-      const uint32_t ph = (j / kStages) & 1, ph_prev = ((j / kStages) - 1) & 1;
-      const int valid_rows = min(kN, seq_eff - j * kN);   // V rows at or past this become zeros
-      if constexpr (kFp8) {
-        ok = wait_or_abort(&k_tma[s], ph, p.err, abort_flag);
-        if (ok && j >= kStages) ok = wait_or_abort(&k_free[s], ph_prev, p.err, abort_flag);
-        if (!ok) break;
-        for (int idx = t; idx < kN * 8; idx += 96) {     // 64 rows x 8 chunks of 16 codes
-          const int r = idx >> 3, ch = idx & 7;
-          widen_chunk<QT>(smem + L::kOffRawK + s * kRawBytes + r * 128, smem + L::kOffK + s * kTileBytes, r, ch,
-                          false);
-        }
-        fence_async_smem();
-        mbar_arrive(&raw_k_free[s]);
-        mbar_arrive(&k_ready[s]);
-        ok = wait_or_abort(&v_tma[s], ph, p.err, abort_flag);
-        if (ok && j >= kStages) ok = wait_or_abort(&v_free[s], ph_prev, p.err, abort_flag);
-        if (!ok) break;
-        for (int idx = t; idx < kN * 8; idx += 96) {
-          const int r = idx >> 3, ch = idx & 7;
-          widen_chunk<QT>(smem + L::kOffRawV + s * kRawBytes + r * 128, smem + L::kOffV + s * kTileBytes, r, ch,
-                          r >= valid_rows);
-        }
-        fence_async_smem();
-        mbar_arrive(&raw_v_free[s]);
-        mbar_arrive(&v_ready[s]);
-      } else {
-        // V landed in the MMA tile itself; zero its rows past the sequence end
-        ok = wait_or_abort(&v_tma[s], ph, p.err, abort_flag);
-        if (!ok) break;
-        if (valid_rows < kN) {
-          for (int idx = t; idx < (kN - valid_rows) * 16; idx += 96) {
-            const int r = valid_rows + (idx >> 4), ch = idx & 15;
-            *reinterpret_cast<uint4 *>(smem + L::kOffV + s * kTileBytes + (ch >> 3) * kTilePanel + r * 128 +
-                                       ((ch & 7) << 4)) = make_uint4(0, 0, 0, 0);
+      };
+      if (nkt > 0) load(0, rk, rv);
+      for (int j = 0; j < nkt && ok; ++j) {
+        const int s = j % kStages;
+        const uint32_t ph_prev = ((j / kStages) - 1) & 1;
+        uint4 nk[4], nv[4];
+        if (j + 1 < nkt) load(j + 1, nk, nv);
+#pragma unroll
+        for (int which = 0; which < 2; ++which) {
+          if (j >= kStages)
+            ok = __all_sync(0xffffffffu, wait_or_abort(which ? &v_free[s] : &k_free[s], ph_prev, p.err, abort_flag));
+          if (!ok) break;
+          uint8_t *tile = smem + (which ? L::kOffV : L::kOffK) + s * kTileBytes + pn * kTilePanel;
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            const int row = 16 * lw + 4 * i + (lane >> 3);
+            uint32_t o[8];
+            widen16<QT>(which ? rv[i] : rk[i], o);
+            uint8_t *dst = tile + row * 128;
+            *reinterpret_cast<uint4 *>(dst + ((c0 ^ (row & 7)) << 4)) = make_uint4(o[0], o[1], o[2], o[3]);
+            *reinterpret_cast<uint4 *>(dst + (((c0 + 1) ^ (row & 7)) << 4)) = make_uint4(o[4], o[5], o[6], o[7]);
           }
           fence_async_smem();
+          mbar_arrive(which ? &v_full[s] : &k_full[s]);
         }
-        mbar_arrive(&v_ready[s]);
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          rk[i] = nk[i];
+          rv[i] = nv[i];
+        }
       }
     }
-    // fp8: the MMA's releases of the last widened tiles have arrived
-    if (kFp8 && ok) {
+    // before exit: the MMAs' releases of the last tiles have arrived, and no copy is in flight
+    if (ok) {
       for (int tt = max(0, nkt - kStages); tt < nkt; ++tt) {
         wait_or_abort(&k_free[tt % kStages], (tt / kStages) & 1, p.err, abort_flag);
         wait_or_abort(&v_free[tt % kStages], (tt / kStages) & 1, p.err, abort_flag);
       }
     }
+    if constexpr (!kFp8) cp_async_wait_all();
   } else {
-    // ===================================================== MMA issue (warp 8, lane 0)
-    if (lane == 0) {
-      const uint32_t idesc_s = umma_idesc(kAB, kN, false);
-      const uint32_t idesc_o = umma_idesc(kAB, kD, true);
-      bool ok = nkt == 0 || wait_or_abort(q_ready, 0, p.err, abort_flag);
-      auto pv = [&](int i) {  // O += P_i V_i
-        const int s = i % kStages, b = i & 1;
-        ok = ok && wait_or_abort(&p_full[b], (i >> 1) & 1, p.err, abort_flag);
-        ok = ok && wait_or_abort(&v_ready[s], (i / kStages) & 1, p.err, abort_flag);
+    // ===================================================== MMA issue (last warp)
+    // The whole warp runs the schedule (so descriptors stay warp-uniform); one
+    // elected lane issues the MMAs and their commits.
+    const bool leader = elect_one();
+    const uint32_t idesc_s = umma_idesc(kAB, kN, false);
+    const uint32_t idesc_o = umma_idesc(kAB, kD, true);
+    const uint64_t qdesc = umma_desc(smem_u32(smem + L::kOffQ), 16);
+    const uint64_t kdesc0 = umma_desc(smem_u32(smem + L::kOffK), 16);
+    const uint64_t vdesc0 = umma_desc(smem_u32(smem + L::kOffV), kTilePanel);
+    auto wait_all = [&](uint64_t *bar, uint32_t parity) {
+      return __all_sync(0xffffffffu, wait_or_abort(bar, parity, p.err, abort_flag));
+    };
+    bool ok = nkt == 0 || wait_all(q_ready, 0);
+    bool issued = false;
+    auto pv = [&](int i) {  // O_t += P_t(i) V_i for both Q tiles
+      const int s = i % kStages, b = i & 1;
+      ok = ok && wait_all(&v_full[s], (i / kStages) & 1);
+      if (!ok) return;
+      fence_async_smem();   // tile written through the generic proxy (cp.async / st.shared)
+      const uint64_t vd = vdesc0 + ((s * kTileBytes) >> 4);
+#pragma unroll
+      for (int t = 0; t < kQTiles; ++t) {
+        ok = wait_all(&p_full[t * 2 + b], (i >> 1) & 1);
         if (!ok) return;
         tc_fence_after();
-        const uint32_t pbase = smem_u32(smem + L::kOffP + b * L::kPBuf);
-        const uint32_t vbase = smem_u32(smem + L::kOffV + s * kTileBytes);
+        if (leader) {
 #pragma unroll
-        for (int half = 0; half < (kSplit ? 2 : 1); ++half) {
+          for (int half = 0; half < (kSplit ? 2 : 1); ++half) {
 #pragma unroll
-          for (int kk = 0; kk < kN / 16; ++kk) {
-            const uint64_t ad = umma_desc(pbase + half * kPPanel + kk * 32, 16);
-            const uint64_t bd = umma_desc(vbase + kk * 16 * 128, kTilePanel);
-            umma(tmem_o, ad, bd, idesc_o, (i > 0 || half > 0 || kk > 0) ? 1u : 0u);
+            for (int kk = 0; kk < kN / 16; ++kk)
+              umma_ts(obuf(t), sbuf(t, b) + half * 32 + kk * 8, vd + ((kk * 16 * 128) >> 4), idesc_o,
+                      (i > 0 || half > 0 || kk > 0) ? 1u : 0u);
           }
+          umma_commit(&o_done[t * 2 + b]);
         }
-        umma_commit(&o_done[b]);
-        umma_commit(&v_free[s]);
-      };
-      if (ok) tc_fence_after();
-      const uint32_t qbase = smem_u32(smem + L::kOffQ);
-      for (int j = 0; j < nkt && ok; ++j) {
-        const int s = j % kStages, b = j & 1;
-        ok = kFp8 ? wait_or_abort(&k_ready[s], (j / kStages) & 1, p.err, abort_flag)
-                  : wait_or_abort(&k_tma[s], (j / kStages) & 1, p.err, abort_flag);
-        if (ok && j >= 2) ok = wait_or_abort(&s_free[b], ((j - 2) >> 1) & 1, p.err, abort_flag);
+        __syncwarp();
+      }
+      if (leader) umma_commit(&v_free[s]);
+      __syncwarp();
+    };
+    if (ok) tc_fence_after();
+    for (int j = 0; j < nkt && ok; ++j) {
+      const int s = j % kStages, b = j & 1;
+      ok = wait_all(&k_full[s], (j / kStages) & 1);
+      if (!ok) break;
+      fence_async_smem();
+      const uint64_t kd = kdesc0 + ((s * kTileBytes) >> 4);
+#pragma unroll
+      for (int t = 0; t < kQTiles; ++t) {
+        // score buffer b of tile t last held P_t(j-2): its P.V group must be done
+        if (j >= 2) ok = wait_all(&o_done[t * 2 + b], ((j - 2) >> 1) & 1);
         if (!ok) break;
         tc_fence_after();
-        const uint32_t kbase = smem_u32(smem + L::kOffK + s * kTileBytes);
+        const uint64_t qd = qdesc + ((t * kQBytes) >> 4);
+        if (leader) {
 #pragma unroll
-        for (int k = 0; k < kD / 16; ++k) {
-          const uint64_t ad = umma_desc(qbase + (k >> 2) * (kM * 128) + (k & 3) * 32, 16);
-          const uint64_t bd = umma_desc(kbase + (k >> 2) * kTilePanel + (k & 3) * 32, 16);
-          umma(tmem + b * kN, ad, bd, idesc_s, k > 0 ? 1u : 0u);
+          for (int k = 0; k < kD / 16; ++k)
+            umma(sbuf(t, b), qd + (((k >> 2) * (kM * 128) + (k & 3) * 32) >> 4),
+                 kd + (((k >> 2) * kTilePanel + (k & 3) * 32) >> 4), idesc_s, k > 0 ? 1u : 0u);
+          umma_commit(&s_full[t * 2 + b]);
         }
-        umma_commit(&s_full[b]);
-        umma_commit(&k_free[s]);
-        if (j >= 1) pv(j - 1);
+        __syncwarp();
+        issued = true;
       }
-      if (ok && nkt > 0) pv(nkt - 1);
-      // every MMA issued above is complete before tensor memory is freed
-      umma_commit(fin);
+      if (!ok) break;
+      if (leader) umma_commit(&k_free[s]);
+      __syncwarp();
+      if (j >= 1) pv(j - 1);
+    }
+    if (ok && nkt > 0) pv(nkt - 1);
+    // every MMA issued above is complete before tensor memory is freed
+    if (issued) {
+      if (leader) umma_commit(fin);
+      __syncwarp();
       mbar_wait(fin, 0, p.err);
     }
-    __syncwarp();
   }
 
   // ===================================================== teardown
   tc_fence_before();
   __syncthreads();
-  if (warp == 8) {
+  if (warp == kMmaWarp) {
     tc_fence_after();
-    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, 256;" ::"r"(tmem));
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "n"(kTmemCols));
   }
 }
 
-// Host launcher: grid (chunks x row blocks, KV heads), 288 threads, one CTA per SM.
-template <typename KV, typename QT, int G>
-cudaError_t launch_prefill_tc_one(const PrefillTcParams &p0, const PoolMaps &m, int num_chunks, cudaStream_t s) {
-  constexpr bool kFp8 = std::is_same<KV, uint8_t>::value;
-  constexpr bool kSplit = std::is_same<QT, __nv_bfloat16>::value && !kFp8;
-  constexpr int smem = tc::Layout<kFp8, kSplit>::kSmemBytes;
+// Host launcher: grid (chunks x row blocks, KV heads), one CTA per SM.  Two Q
+// tiles per CTA share every K/V tile, unless that leaves SMs idle (few rows):
+// then one Q tile per CTA doubles the grid.
+template <typename KV, typename QT, int G, int kQTiles>
+cudaError_t launch_prefill_tc_tiles(const PrefillTcParams &p0, int num_chunks, cudaStream_t s) {
+  constexpr int smem = tc::Layout<kQTiles>::kSmemBytes;
+  constexpr int BR = kQTiles * tc::kM / G;
   PrefillTcParams p = p0;
-  p.row_blocks = (p.max_q_len + (tc::kM / G) - 1) / (tc::kM / G);
-  auto kern = prefill_tc_kernel<KV, QT, G>;
+  p.row_blocks = (p.max_q_len + BR - 1) / BR;
+  auto kern = prefill_tc_kernel<KV, QT, G, kQTiles>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
   const int64_t gx = (int64_t)num_chunks * p.row_blocks;
   if (gx > 2147483647ll || p.num_kv_heads > 65535) return cudaErrorInvalidValue;
   dim3 grid((unsigned)gx, (unsigned)p.num_kv_heads);
-  kern<<<grid, tc::kThreads, smem, s>>>(p, m.k, m.v);
+  kern<<<grid, tc::Roles<kQTiles>::kThreads, smem, s>>>(p);
   return cudaGetLastError();
 }
 
+template <typename KV, typename QT, int G>
+cudaError_t launch_prefill_tc_one(const PrefillTcParams &p, int num_chunks, int num_sms, cudaStream_t s) {
+  const int64_t two = (int64_t)num_chunks * ((p.max_q_len + 2 * tc::kM / G - 1) / (2 * tc::kM / G)) * p.num_kv_heads;
+  if (two >= num_sms) return launch_prefill_tc_tiles<KV, QT, G, 2>(p, num_chunks, s);
+  return launch_prefill_tc_tiles<KV, QT, G, 1>(p, num_chunks, s);
+}
+
 template <typename KV, typename QT>
-cudaError_t launch_prefill_tc(const PrefillTcParams &p, const PoolMaps &m, int gqa, int num_chunks, cudaStream_t s) {
+cudaError_t launch_prefill_tc(const PrefillTcParams &p, int gqa, int num_chunks, cudaStream_t s) {
+  int dev = 0, num_sms = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&num_sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+    return cudaErrorUnknown;
   switch (gqa) {
-    case 1: return launch_prefill_tc_one<KV, QT, 1>(p, m, num_chunks, s);
-    case 2: return launch_prefill_tc_one<KV, QT, 2>(p, m, num_chunks, s);
-    case 4: return launch_prefill_tc_one<KV, QT, 4>(p, m, num_chunks, s);
-    case 8: return launch_prefill_tc_one<KV, QT, 8>(p, m, num_chunks, s);
-    case 16: return launch_prefill_tc_one<KV, QT, 16>(p, m, num_chunks, s);
+    case 1: return launch_prefill_tc_one<KV, QT, 1>(p, num_chunks, num_sms, s);
+    case 2: return launch_prefill_tc_one<KV, QT, 2>(p, num_chunks, num_sms, s);
+    case 4: return launch_prefill_tc_one<KV, QT, 4>(p, num_chunks, num_sms, s);
+    case 8: return launch_prefill_tc_one<KV, QT, 8>(p, num_chunks, num_sms, s);
+    case 16: return launch_prefill_tc_one<KV, QT, 16>(p, num_chunks, num_sms, s);
     default: return cudaErrorInvalidValue;
   }
 }

@@ -139,3 +139,23 @@ def test_prefill_tensor_core_metadata_errors(kv):
     dev.prefill["block_tables"][0, 3] = -2
     dev.prefill_chunk()
     assert pa.pa_get_device_error() == 4
+
+
+# Batches large enough that the tensor-core kernel puts two 128-row Q tiles in
+# each CTA (at least one CTA per SM); the cases above are small enough to use
+# one Q tile per CTA.
+@pytest.mark.parametrize("src,kv", [("bf16", "bf16"), ("f16", "f16"), ("bf16", "fp8")])
+@pytest.mark.parametrize("hq,hkv,chunks", [
+    (32, 8, [(100, 300), (7, 300), (640, 257), (0, 299)]),
+    (64, 8, [(int(s), 100) for s in range(0, 800, 100)]),
+    (8, 8, [(int(s), 256 - s % 7) for s in range(0, 2000, 100)]),
+])
+def test_prefill_two_q_tiles_per_cta(src, kv, hq, hkv, chunks):
+    g = hq // hkv
+    br = 256 // g
+    assert sum(-(-c // br) for _, c in chunks) * hkv >= 152
+    b = W.prefill_batch("p", chunks, hq, hkv, 128, 16, src, kv_dtype=kv, seed=hq + len(chunks))
+    dev = run_gpu(b)
+    kp, vp = oracle_pools(b)
+    ref = oracle.prefill_batch(b, kp, vp)
+    assert max_err(dev.prefill["out"], ref) <= TOL[kv]
