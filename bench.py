@@ -10,6 +10,13 @@ tokens/s per layer.
 
 Prints one JSON line.  ``--impl reference`` times the fp64 CPU oracle instead
 (bounded samples of the same workload on the host cores).
+
+The line also carries ``prefill``: the tensor-core chunked-prefill kernel
+timed on its own (CUDA events, inputs resident), as useful causal TFLOP/s
+(4 * head_dim * Hq * sum over query rows of the keys each row attends to)
+against the measured dense bf16 peak, for the 512-token chunk of the
+chunked-prefill mixed batch (fp8 KV) and for a batch that fills every SM.
+``--prefill-only`` prints just that measurement (used for profiling).
 """
 from __future__ import annotations
 
@@ -39,6 +46,71 @@ def _peaks():
             d = json.load(f)
         return float(d["hbm_gbs"]), "measured"
     return 6800.0, "fallback"
+
+
+def _tensor_peak():
+    """Dense bf16 TFLOP/s for a kernel timed on its own (burst figure)."""
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            return float(json.load(f)["bf16_tflops"]), "measured bf16_tflops (burst)"
+    return 1900.0, "fallback"
+
+
+def _causal_flops(b) -> float:
+    """Useful FLOPs of one pa_prefill_chunk call: Q.K^T and P.V over the keys each row sees."""
+    p = b.prefill
+    keys = 0
+    for c in range(len(p.q_start)):
+        n = int(p.cu_q_lens[c + 1] - p.cu_q_lens[c])
+        keys += n * int(p.q_start[c]) + n * (n + 1) // 2
+    return 4.0 * b.head_dim * b.num_q_heads * keys
+
+
+PREFILL_WORKLOADS = {
+    # the chunk of the chunked-prefill mixed batch (fp8 KV, bf16 q): one 512-row chunk over 4096 tokens
+    "mixed_fp8_chunk": ("chunked-prefill mixed batch, fp8 KV: 512-token chunk at position 4096, GQA 32/8, "
+                        "head_dim 128, block 16"),
+    # enough rows to give every SM a CTA: 8 chunks of 2048 tokens over 2048 tokens of context, bf16 KV
+    "bf16_8x2048": "8 chunks x 2048 tokens at position 2048, GQA 32/8, head_dim 128, block 16, bf16 KV",
+}
+
+
+def measure_prefill(dev_name: str, steps: int, warmup: int) -> dict:
+    import torch
+    import workloads as W
+    import paged_kv_cache_writes_gb300 as pa
+    from paged_kv_cache_writes_gb300.staging import DeviceBatch
+    peak, kind = _tensor_peak()
+    res = {}
+    for key, desc in PREFILL_WORKLOADS.items():
+        if key == "mixed_fp8_chunk":
+            b = W.cfg_mixed_fp8()
+        else:
+            b = W.prefill_batch("prefill 8x2048", [(2048, 2048)] * 8, 32, 8, 128, 16, "bf16", seed=3)
+        db = DeviceBatch(b, dev_name)
+        db.run_setup()
+        db.write_step()
+        for _ in range(warmup):
+            db.prefill_chunk()
+        torch.cuda.synchronize()
+        s = torch.cuda.current_stream()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(s)
+        for _ in range(steps):
+            db.prefill_chunk()
+        e1.record(s)
+        torch.cuda.synchronize()
+        assert pa.pa_get_device_error() == 0
+        ms = e0.elapsed_time(e1) / steps
+        tf = _causal_flops(b) / (ms * 1e-3) / 1e12
+        res[key] = {"workload": desc, "kv_dtype": b.kv_dtype, "ms": ms, "useful_tflop": _causal_flops(b) / 1e12,
+                    "roofline": {"bound": "tensor", "achieved": tf, "peak": peak, "unit": "TFLOP/s",
+                                 "frac": tf / peak, "peak_source": kind,
+                                 "kernel": "prefill_tc_kernel (pa_prefill_chunk)"}}
+        del db
+        torch.cuda.empty_cache()
+    return res
 
 
 def _profiled_traffic(kv_bytes: int):
@@ -316,6 +388,10 @@ def run_ours(args):
         "gpu_launches": 3 * args.steps,  # per step: cache write, decode plan, decode
         "clocks": clocks.summary(),
     }
+    if ws == 1:
+        del db
+        torch.cuda.empty_cache()
+        line["prefill"] = measure_prefill(dev_name, max(5, args.steps // 5), args.warmup)
     if not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_oracle_rate(b, args.cpu_seconds)
     print(json.dumps(line))
@@ -333,9 +409,19 @@ def main():
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     ap.add_argument("--batch", type=int, default=256,
                     help="sequences in the decode batch (256 = the named workload; smaller only for profiling)")
+    ap.add_argument("--prefill-only", action="store_true",
+                    help="time only the tensor-core prefill kernel (profiling)")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
+    if args.prefill_only:
+        import torch
+        from paged_kv_cache_writes_gb300 import build_lib
+        build_lib.build()
+        torch.cuda.set_device(0)
+        print(json.dumps({"metric": "prefill useful TFLOP/s", "prefill": measure_prefill("cuda:0", args.steps,
+                                                                                       args.warmup)}))
+        return
     (run_reference if args.impl == "reference" else run_ours)(args)
 
 
