@@ -11,7 +11,9 @@ tokens/s per layer.
 Prints one JSON line.  ``--impl reference`` times the fp64 CPU oracle instead
 (bounded samples of the same workload on the host cores).
 
-The line also carries ``prefill``: the tensor-core chunked-prefill kernel
+``other_decodes`` is pa_decode alone on the 8B-shaped, shared-prefix and
+mixed fp8 decode workloads (K+V bytes / time).  The line also carries
+``prefill``: the tensor-core chunked-prefill kernel
 timed on its own (CUDA events, inputs resident), as useful causal TFLOP/s
 (4 * head_dim * Hq * sum over query rows of the keys each row attends to)
 against the measured dense bf16 peak, for the 512-token chunk of the
@@ -74,6 +76,42 @@ PREFILL_WORKLOADS = {
     # enough rows to give every SM a CTA: 8 chunks of 2048 tokens over 2048 tokens of context, bf16 KV
     "bf16_8x2048": "8 chunks x 2048 tokens at position 2048, GQA 32/8, head_dim 128, block 16, bf16 KV",
 }
+
+
+def measure_other_decodes(dev_name: str, steps: int, warmup: int) -> dict:
+    """pa_decode alone on the other decode workloads: algorithmic K+V bytes / CUDA-event time."""
+    import torch
+    import workloads as W
+    import paged_kv_cache_writes_gb300 as pa
+    from paged_kv_cache_writes_gb300.staging import DeviceBatch
+    peak, kind = _peaks()
+    res = {}
+    for key, fn in (("llama8b", W.cfg_llama8b), ("shared_prefix", W.cfg_shared_prefix), ("mixed_fp8_decodes", W.cfg_mixed_fp8)):
+        b = fn()
+        db = DeviceBatch(b, dev_name)
+        db.run_setup()
+        db.write_step()
+        for _ in range(warmup):
+            db.decode()
+        torch.cuda.synchronize()
+        s = torch.cuda.current_stream()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(s)
+        for _ in range(steps):
+            db.decode()
+        e1.record(s)
+        torch.cuda.synchronize()
+        assert pa.pa_get_device_error() == 0
+        ms = e0.elapsed_time(e1) / steps
+        gbs = b.decode_kv_bytes() / (ms * 1e-3) / 1e9
+        res[key] = {"workload": b.name, "kv_dtype": b.kv_dtype, "num_seqs": b.num_seqs,
+                    "heads": f"{b.num_q_heads}/{b.num_kv_heads}", "kv_bytes": b.decode_kv_bytes(), "ms": ms,
+                    "GBps": gbs, "frac_of_hbm": gbs / peak, "peak_source": kind,
+                    "note": "shared prefix blocks are read once per branch (counted per branch)"
+                    if key == "shared_prefix" else None}
+        del db
+        torch.cuda.empty_cache()
+    return res
 
 
 def measure_prefill(dev_name: str, steps: int, warmup: int) -> dict:
@@ -392,6 +430,7 @@ def run_ours(args):
         del db
         torch.cuda.empty_cache()
         line["prefill"] = measure_prefill(dev_name, max(5, args.steps // 5), args.warmup)
+        line["other_decodes"] = measure_other_decodes(dev_name, max(5, args.steps // 5), args.warmup)
     if not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_oracle_rate(b, args.cpu_seconds)
     print(json.dumps(line))

@@ -257,6 +257,18 @@ PA_API pa_status pa_prefill_chunk(const void *q_chunk, pa_dtype q_dtype,
  */
 PA_API pa_status pa_get_device_error(pa_stream_t stream, int32_t *code);
 
+/*
+ * pa_selftest_wait_timeout -- check that the library's waits end.  The pages
+ * have no counterpart; this call exists for the library's users and tests.
+ *
+ * Launches one warp that waits, with the same bounded wait every kernel of the
+ * library uses, on an mbarrier that nothing completes.  The wait gives up
+ * after its limit (about one second of %globaltimer), records PA_ERR_TIMEOUT
+ * in the device error word (read it with pa_get_device_error) and the kernel
+ * returns; the context stays usable.  Returns PA_ERR_CUDA if the launch fails.
+ */
+PA_API pa_status pa_selftest_wait_timeout(pa_stream_t stream);
+
 /* Static, human-readable name of a status code. */
 PA_API const char *pa_status_string(pa_status status);
 

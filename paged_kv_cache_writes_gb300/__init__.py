@@ -61,10 +61,11 @@ def lib() -> ctypes.CDLL:
         L.pa_prefill_chunk.argtypes = [P, ctypes.c_int, P, P, I32, I32, I32, P, P, ctypes.POINTER(PaKvCache), P,
                                        I32, P, I32, F, P, ctypes.c_int, P]
         L.pa_get_device_error.argtypes = [P, ctypes.POINTER(I32)]
+        L.pa_selftest_wait_timeout.argtypes = [P]
         L.pa_status_string.argtypes = [ctypes.c_int]
         L.pa_status_string.restype = ctypes.c_char_p
         for name in ("pa_reshape_and_cache", "pa_copy_blocks", "pa_decode", "pa_prefill_chunk",
-                     "pa_get_device_error"):
+                     "pa_get_device_error", "pa_selftest_wait_timeout"):
             getattr(L, name).restype = ctypes.c_int
         _lib = L
     return _lib
@@ -175,6 +176,11 @@ def pa_get_device_error(stream=None) -> int:
     code = ctypes.c_int32(0)
     _ok(lib().pa_get_device_error(_stream(stream), ctypes.byref(code)), "pa_get_device_error")
     return code.value
+
+
+def pa_selftest_wait_timeout(stream=None) -> None:
+    """Enqueue one warp whose bounded wait expires (records PA_ERR_TIMEOUT, then returns)."""
+    _ok(lib().pa_selftest_wait_timeout(_stream(stream)), "pa_selftest_wait_timeout")
 
 
 def pa_status_string(status: int) -> str:

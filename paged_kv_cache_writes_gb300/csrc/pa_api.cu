@@ -18,6 +18,18 @@ namespace pa {
 
 __device__ int32_t g_device_error = 0;
 
+// One warp waits on an mbarrier nothing completes; the bounded wait records
+// PA_ERR_TIMEOUT and the kernel returns.
+__global__ void selftest_wait_kernel(int32_t *err) {
+  __shared__ uint64_t bar;
+  if (threadIdx.x == 0) {
+    mbar_init(&bar, 1);
+    fence_mbar_init();
+  }
+  __syncwarp();
+  (void)mbar_wait(&bar, 0, err);
+}
+
 namespace {
 
 bool aligned(const void *p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; }
@@ -351,6 +363,13 @@ pa_status pa_prefill_chunk(const void *q_chunk, pa_dtype q_dtype, const int32_t 
   return dispatch_attention(q_dtype, c, p, maps, (int)rows, s) == cudaSuccess
              ? PA_OK
              : PA_ERR_CUDA;
+}
+
+pa_status pa_selftest_wait_timeout(pa_stream_t stream) {
+  int32_t *err = device_error_word();
+  if (!err) return PA_ERR_CUDA;
+  selftest_wait_kernel<<<1, 32, 0, reinterpret_cast<cudaStream_t>(stream)>>>(err);
+  return cudaGetLastError() == cudaSuccess ? PA_OK : PA_ERR_CUDA;
 }
 
 pa_status pa_get_device_error(pa_stream_t stream, int32_t *code) {
