@@ -1,6 +1,10 @@
-// pa_attention.cuh -- paged attention on CUDA cores: decode (one query row
-// per sequence, GQA, split-KV with a log-sum-exp combine) and, with the same
-// kernel, causal prefill rows that each see their own context length.
+// pa_attention.cuh -- paged attention on CUDA cores, one CTA per query row:
+// the chunked-prefill path for shapes the tensor-core kernel does not take
+// (head_dim 64, GQA groups outside {1, 2, 4, 8, 16}); each prefill row sees
+// its own causal length.  The tile geometry (Geo), the swizzled tile reads
+// (load8) and the output store are shared with the persistent decode
+// (pa_decode.cuh).  With no cu_q_lens the kernel treats each row as a decode
+// row of length seq_lens[row].
 //
 // What it computes ("Inside vLLM Architecture", sections "Architectural
 // Anatomy: PagedAttention Virtual Memory Paging" and "CUDA Shared Memory

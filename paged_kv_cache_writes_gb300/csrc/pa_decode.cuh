@@ -19,14 +19,18 @@
 //  * the next unit is claimed while the current one computes: the cursor
 //    bump and the two dependent reads behind it (item, then the row's length
 //    and block ids) are issued one per tile, so their latency is hidden;
-//  * lane 0 keeps a ring of kSlots 16-token K/V tiles in flight with 2D
-//    bulk-tensor (TMA) copies (128-byte swizzle), running ahead across the
-//    boundary into the next claimed unit; the unit's block ids sit one per
-//    lane in a register (one coalesced load per unit);
+//  * lane 0 keeps a ring of kSlots 16-token K/V tiles in flight with bulk-
+//    tensor (TMA) copies, one box per K and per V tile (3D box over both
+//    128-byte panels of the 256-byte rows; 128-byte swizzle), running ahead
+//    across the boundary into the next claimed unit; the unit's block ids
+//    sit one per lane in a register (one coalesced load per unit);
 //  * q for the next unit arrives by a 1D bulk copy while the current unit
 //    computes, and is widened to fp32, pre-scaled by scale*log2(e);
-//  * Q.K^T: lane = (token t of the tile, half of the heads), the whole head
-//    dim in registers, q broadcast from shared memory, packed fp32x2 FMAs;
+//  * Q.K^T (HPC >= 4): lane = (quarter of head_dim, token pair), every head
+//    of the group; one 16-byte q load from shared memory feeds 2 tokens x 2
+//    heads of packed fp32x2 FMAs, and a two-level shuffle reduction over the
+//    quarters leaves each lane with its scores (HPC == 1: lane = (half of
+//    head_dim, token));
 //  * online softmax in the log2 domain with a lazy reference maximum: the
 //    accumulators are rescaled only when a tile's maximum exceeds the
 //    reference by more than kRescaleLog2 (2^8 headroom in fp32), which
