@@ -11,31 +11,33 @@
 // KV Cache Bottleneck in LLM Serving"), so Q.K^T and P.V run as dense tiles on
 // the tensor pipe; the softmax stays in fp32 on the CUDA cores.
 //
-// Tiling.  One CTA = two Q tiles of 128 GQA-packed query rows (256/G token
-// rows x the G query heads of one KV head; packed row m = token m / G, head
-// m % G; tile m / 128) x every key tile of 64 keys up to its causal limit.
-// Each K/V tile feeds both Q tiles and all G heads.
+// Tiling.  One CTA = one or two Q tiles of 128 GQA-packed query rows (128/G
+// token rows per tile x the G query heads of one KV head; packed row m =
+// token m / G, head m % G; tile m / 128) x every key tile of 128 keys up to
+// its causal limit.  Each K/V tile feeds every Q tile and all G heads.
 //
-// Roles (416 threads):
+// Roles (416 threads with two Q tiles, 288 with one):
 //  * warps 0-3 / 4-7, softmax of Q tile 0 / 1: thread m owns packed row m
-//    (tensor-memory lane m % 128).  It reads its 64 scores with tcgen05.ld,
-//    masks and scales them, keeps a lazy reference maximum (its O row in
-//    tensor memory is rescaled only when a tile maximum exceeds the reference
-//    by more than 2^8), and writes its row of P (16-bit pairs) back over the
-//    scores with tcgen05.st: the P.V MMA reads P straight from tensor memory.
-//  * warps 8-11, loads: each warp gathers 16 rows (keys inside one block of
-//    the block table) of every K and V tile into a ring of kStages tiles,
-//    512 contiguous bytes per warp instruction.  16-bit caches: 16-byte
-//    cp.async straight into the 128-byte-swizzled MMA layout; fp8 caches:
-//    register loads one tile ahead, widened exactly to the query's 16-bit
-//    type on the way to shared memory.  Rows past the end of the sequence are
+//    (tensor-memory lane m % 128).  It reads its 128 scores with tcgen05.ld
+//    twice (maximum, then probabilities), masks them on tiles that reach its
+//    causal limit, keeps a lazy reference maximum (its O row in tensor memory
+//    is rescaled only when a tile maximum exceeds the reference by more than
+//    2^8), and writes P (16-bit pairs) back over the scores with tcgen05.st,
+//    each 16 keys' P into those keys' own 16 columns (hi pairs, then lo
+//    pairs for a bf16 cache): the P.V MMA reads P straight from tensor
+//    memory.
+//  * the next 4 warps load: each warp gathers 32 rows (two runs of 16 keys,
+//    each inside one block of the block table) of every K and V tile into a
+//    ring of kStages tiles, 512 contiguous bytes per warp instruction.
+//    16-bit caches: 16-byte cp.async straight into the 128-byte-swizzled MMA
+//    layout; fp8 caches: register loads a quarter tile ahead, widened
+//    exactly to the query's 16-bit type on the way to shared memory.  Rows past the end of the sequence are
 //    zero-filled so a zero probability never meets a stale (possibly NaN)
 //    value in the MMA.
-//  * warp 12, MMA (one elected lane issues): per key tile j, S_t(j) = Q_t K_j^T
-//    for both Q tiles into one of each tile's two score buffers, then
-//    O_t += P_t(j-1) V_{j-1}; the tensor pipe computes the next scores while
-//    the softmax warps work on the current ones, and the two Q tiles' softmax
-//    phases overlap each other.
+//  * last warp, MMA (one elected lane issues): for each Q tile t in turn,
+//    O_t += P_t(j) V_j as soon as P_t(j) is written, then S_t(j+1) = Q_t
+//    K_{j+1}^T into the same buffer once that P.V has completed; with two Q
+//    tiles, one tile's MMAs run while the other tile's softmax works.
 //
 // Precision.  Q, K and V are exact in the MMA (fp8 codes widen exactly to
 // bf16/f16); accumulation is fp32.  P is rounded to the 16-bit type; with a
@@ -82,8 +84,8 @@ namespace tc {
 
 constexpr int kD = 128;         // head_dim
 constexpr int kM = 128;         // packed query rows per Q tile (MMA M, tensor-memory lanes)
-constexpr int kN = 64;          // keys per tile
-constexpr int kStages = 3;      // K/V tiles in flight
+constexpr int kN = 128;         // keys per tile
+constexpr int kStages = 2;      // K/V tiles in flight
 
 // Warp roles and tensor-memory size for a CTA of QT Q tiles (1 or 2).
 template <int QT>
@@ -92,15 +94,18 @@ struct Roles {
   static constexpr int kLoadWarp0 = kSoftmax / 32;    // the next 4 warps load
   static constexpr int kMmaWarp = kLoadWarp0 + 4;     // the last warp issues the MMAs
   static constexpr int kThreads = (kMmaWarp + 1) * 32;
-  static constexpr int kTmemCols = QT * 256;          // per Q tile: 2 score/P buffers of 64 columns; then the O tiles
+  // score/P buffers of 128 columns per Q tile: two with one Q tile (the next
+  // scores are computed while the softmax works), one with two Q tiles
+  static constexpr int kBufs = QT == 1 ? 2 : 1;
+  static constexpr int kTmemCols = 512;               // QT*kBufs*128 score/P columns, then QT*128 of O
 };
 constexpr float kRescaleLog2 = 8.f;
 
 constexpr int kQBytes = kM * kD * 2;        // one Q tile: 2 panels x [128 rows x 128 B]
-constexpr int kTileBytes = kN * kD * 2;     // 2 panels x [64 rows x 128 B]
-constexpr int kTilePanel = kN * 128;        // 8 KB
+constexpr int kTileBytes = kN * kD * 2;     // 2 panels x [128 rows x 128 B]
+constexpr int kTilePanel = kN * 128;        // 16 KB
 constexpr int kLoaders = 128;               // threads of the load warps
-constexpr int kNumBars = 4 * kStages + 3 * 2 * 2 + 2;
+constexpr int kNumBars = 4 * kStages + 3 * 4 + 2;
 
 // Shared-memory map, bytes from a 1024-aligned base (128-byte swizzle atoms).
 template <int QT>
@@ -163,6 +168,26 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, float (&v)[32]) {
   asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
 #pragma unroll
   for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
+}
+
+// 16 consecutive fp32 columns of this thread's tensor-memory lane (warp-collective).
+__device__ __forceinline__ void tmem_ld16(uint32_t taddr, float (&v)[16]) {
+  uint32_t r[16];
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+        "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
+      : "r"(taddr));
+  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+#pragma unroll
+  for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
+}
+
+// 8 consecutive 32-bit columns of this thread's tensor-memory lane (warp-collective).
+__device__ __forceinline__ void tmem_st8(uint32_t taddr, const uint32_t (&v)[8]) {
+  asm volatile("tcgen05.st.sync.aligned.32x32b.x8.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8};" ::"r"(taddr), "r"(v[0]),
+               "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7])
+               : "memory");
 }
 
 // 16 consecutive 32-bit columns of this thread's tensor-memory lane (warp-collective).
@@ -289,11 +314,13 @@ __global__ void __launch_bounds__(tc::Roles<kQTiles>::kThreads, 1) prefill_tc_ke
   using R = Roles<kQTiles>;
   constexpr int kSoftmax = R::kSoftmax, kLoadWarp0 = R::kLoadWarp0, kMmaWarp = R::kMmaWarp;
   constexpr int kTmemCols = R::kTmemCols;
+  constexpr int kBufs = R::kBufs;
   constexpr bool kFp8 = std::is_same<KV, uint8_t>::value;
   constexpr bool kBf16 = std::is_same<QT, __nv_bfloat16>::value;
   constexpr bool kSplit = kBf16 && !kFp8;   // bf16 cache: P as hi + lo
   constexpr int BR = kQTiles * kM / G;      // token rows per CTA
   constexpr uint32_t kAB = kBf16 ? 1u : 0u;
+  constexpr int kChunks = kN / 32;          // 32-key chunks of a score tile
   const float kNegInf = -__int_as_float(0x7f800000);
 
   extern __shared__ uint8_t smem_raw[];
@@ -304,10 +331,10 @@ __global__ void __launch_bounds__(tc::Roles<kQTiles>::kThreads, 1) prefill_tc_ke
   uint64_t *v_full = k_full + kStages;           // [kStages] V tile (128)
   uint64_t *k_free = v_full + kStages;           // [kStages] MMAs finished reading the K tile
   uint64_t *v_free = k_free + kStages;           // [kStages] MMAs finished reading the V tile
-  uint64_t *s_full = v_free + kStages;           // [tile][buf] scores in tensor memory
-  uint64_t *p_full = s_full + 2 * kQTiles;       // [tile][buf] P written over them (128 arrivals)
-  uint64_t *o_done = p_full + 2 * kQTiles;       // [tile][buf] P.V group i of the tile done -> buf i & 1
-  uint64_t *q_ready = o_done + 2 * kQTiles;      // Q staged (every softmax thread)
+  uint64_t *s_full = v_free + kStages;           // [tile][buf] scores of key tile j in buffer j % kBufs
+  uint64_t *p_full = s_full + 4;                 // [tile][buf] P of key tile j written over them (128 arrivals)
+  uint64_t *o_done = p_full + 4;                 // [tile] P.V of key tile j complete (phase j)
+  uint64_t *q_ready = o_done + 4;                // Q staged (every softmax thread)
   uint64_t *fin = q_ready + 1;                   // every MMA of the CTA complete
   uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + L::kOffMisc);
   volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + L::kOffMisc + 8);
@@ -341,7 +368,7 @@ __global__ void __launch_bounds__(tc::Roles<kQTiles>::kThreads, 1) prefill_tc_ke
       mbar_init(&k_free[s], 1);
       mbar_init(&v_free[s], 1);
     }
-    for (int i = 0; i < 2 * kQTiles; ++i) {
+    for (int i = 0; i < 4; ++i) {
       mbar_init(&s_full[i], 1);
       mbar_init(&p_full[i], 128);
       mbar_init(&o_done[i], 1);
@@ -360,9 +387,9 @@ __global__ void __launch_bounds__(tc::Roles<kQTiles>::kThreads, 1) prefill_tc_ke
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
-  // columns: tile t's score/P buffer b at t*128 + b*64; tile t's O at QT*128 + t*128
-  auto sbuf = [&](int t, int b) { return tmem + (uint32_t)(t * 2 * kN + b * kN); };
-  auto obuf = [&](int t) { return tmem + (uint32_t)(kQTiles * 2 * kN + t * kD); };
+  // columns: tile t's score/P buffer b at (t*kBufs + b)*128; tile t's O after all of them
+  auto sbuf = [&](int t, int b) { return tmem + (uint32_t)((t * kBufs + b) * kN); };
+  auto obuf = [&](int t) { return tmem + (uint32_t)(kQTiles * kBufs * kN + t * kD); };
 
   if (warp < kLoadWarp0) {
     // ===================================================== softmax warps (Q tile t = warp / 4)
@@ -399,36 +426,29 @@ __global__ void __launch_bounds__(tc::Roles<kQTiles>::kThreads, 1) prefill_tc_ke
       return __all_sync(0xffffffffu, wait_or_abort(bar, parity, p.err, abort_flag));
     };
     for (int j = 0; j < nkt; ++j) {
-      const int b = j & 1;
-      ok = wait_all(&s_full[t * 2 + b], (j >> 1) & 1);
+      const int b = j % kBufs;
+      ok = wait_all(&s_full[t * kBufs + b], (j / kBufs) & 1);
       if (!ok) break;
-      tc_fence_after();
       const uint32_t sb = sbuf(t, b) + lane_base;
-      float s[kN];
-      {
-        float t0[32], t1[32];
-        tmem_ld32(sb, t0);
-        tmem_ld32(sb + 32, t1);
-#pragma unroll
-        for (int i = 0; i < 32; ++i) {
-          s[i] = t0[i];
-          s[32 + i] = t1[i];
-        }
-      }
+      tc_fence_after();
       // keys at or past this row's limit are masked, but only tiles that reach
       // some row's limit (the causal diagonal, the sequence end) need the test
       const int nvis = lim - j * kN;
       const bool full_tile = __all_sync(0xffffffffu, nvis >= kN);
-      if (!full_tile) {
-#pragma unroll
-        for (int i = 0; i < kN; ++i)
-          if (i >= nvis) s[i] = kNegInf;
-      }
+      // pass 1: the tile maximum
       float mx[8];
 #pragma unroll
-      for (int i = 0; i < 8; ++i) mx[i] = fmaxf(s[i], s[i + 8]);
+      for (int i = 0; i < 8; ++i) mx[i] = kNegInf;
 #pragma unroll
-      for (int i = 16; i < kN; ++i) mx[i & 7] = fmaxf(mx[i & 7], s[i]);
+      for (int ck = 0; ck < kChunks; ++ck) {
+        float sv[32];
+        tmem_ld32(sb + 32 * ck, sv);
+#pragma unroll
+        for (int i = 0; i < 32; ++i) {
+          const float x = (full_tile || 32 * ck + i < nvis) ? sv[i] : kNegInf;
+          mx[i & 7] = fmaxf(mx[i & 7], x);
+        }
+      }
       const float mr = fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])),
                              fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7])));
       const float mt = mr == kNegInf ? kNegInf : mr * cmul;   // tile maximum, log2 units
@@ -436,8 +456,8 @@ __global__ void __launch_bounds__(tc::Roles<kQTiles>::kThreads, 1) prefill_tc_ke
       if (__any_sync(0xffffffffu, rescale)) {
         const float alpha = rescale ? fast_exp2(m_ref - mt) : 1.f;
         if (j > 0) {
-          // O holds P.V groups 0 .. j-1: wait for the last of them, then rescale in place
-          ok = wait_all(&o_done[t * 2 + ((j - 1) & 1)], ((j - 1) >> 1) & 1);
+          // O holds the P.V of tiles 0 .. j-1: wait for the last of them, then rescale in place
+          ok = wait_all(&o_done[t], (j - 1) & 1);
           if (!ok) break;
           tc_fence_after();
 #pragma unroll 1
@@ -455,51 +475,59 @@ __global__ void __launch_bounds__(tc::Roles<kQTiles>::kThreads, 1) prefill_tc_ke
           m_ref = mt;
         }
       }
-      // p = 2^(s * |s_mult| - m_ref); a row with nothing visible yet keeps m_ref = -inf
+      // pass 2: p = 2^(s * |s_mult| - m_ref), 16 keys at a time, written over
+      // those keys' own 16 score columns.  A row with nothing visible yet keeps
+      // m_ref = -inf.
       const float msub = m_ref == kNegInf ? 0.f : m_ref;
       const float2 cc = make_float2(cmul, cmul), nm = make_float2(-msub, -msub);
-      // P over the scores: hi words in columns 0..31 of the buffer, lo words (bf16 cache) in 32..63
+#pragma unroll 1
+      for (int ck = 0; ck < kChunks; ++ck) {
 #pragma unroll
-      for (int hh = 0; hh < 2; ++hh) {   // keys 32*hh .. 32*hh+31
-        uint32_t w[16], wl[16];
+        for (int hh = 0; hh < 2; ++hh) {   // keys 32ck + 16hh .. +15
+          float sv[16];
+          tmem_ld16(sb + 32 * ck + 16 * hh, sv);
+          uint32_t w[8], wl[8];
 #pragma unroll
-        for (int k = 0; k < 16; ++k) {
-          const int i0 = 32 * hh + 2 * k;
-          const float2 a = ffma2(make_float2(s[i0], s[i0 + 1]), cc, nm);
-          float2 pk = make_float2(fast_exp2(a.x), fast_exp2(a.y));
-          if (!full_tile) {
-            if (i0 >= nvis) pk.x = 0.f;
-            if (i0 + 1 >= nvis) pk.y = 0.f;
-          }
-          if constexpr (kBf16) {
-            // integer rounding keeps the conversion off the transcendental pipe
-            const uint32_t h0 = bf16_round_bits(pk.x), h1 = bf16_round_bits(pk.y);
-            w[k] = pack_hi_halves(h0, h1);
-            const float2 hi = make_float2(__uint_as_float(h0), __uint_as_float(h1));
-            if constexpr (kSplit) {
-              // lo = p - hi is exact in fp32; truncating it to bf16 leaves < 2^-16 relative error in P
-              const float2 lo = ffma2(hi, make_float2(-1.f, -1.f), pk);
-              wl[k] = pack_hi_halves(__float_as_uint(lo.x), __float_as_uint(lo.y));
-              lacc[k & 3] = ffma2(pk, ones, lacc[k & 3]);
-            } else {
-              lacc[k & 3] = ffma2(hi, ones, lacc[k & 3]);   // the rounded P that the MMA will use
+          for (int k = 0; k < 8; ++k) {
+            const int i0 = 32 * ck + 16 * hh + 2 * k;
+            const float2 a = ffma2(make_float2(sv[2 * k], sv[2 * k + 1]), cc, nm);
+            float2 pk = make_float2(fast_exp2(a.x), fast_exp2(a.y));
+            if (!full_tile) {
+              if (i0 >= nvis) pk.x = 0.f;
+              if (i0 + 1 >= nvis) pk.y = 0.f;
             }
-          } else {
-            w[k] = pack2(pk.x, pk.y, QT{});
-            lacc[k & 3] = ffma2(unpack2(w[k], QT{}), ones, lacc[k & 3]);   // the rounded P the MMA uses
+            if constexpr (kBf16) {
+              // integer rounding keeps the conversion off the transcendental pipe
+              const uint32_t h0 = bf16_round_bits(pk.x), h1 = bf16_round_bits(pk.y);
+              w[k] = pack_hi_halves(h0, h1);
+              const float2 hi = make_float2(__uint_as_float(h0), __uint_as_float(h1));
+              if constexpr (kSplit) {
+                // lo = p - hi is exact in fp32; truncating it to bf16 leaves < 2^-16 relative error in P
+                const float2 lo = ffma2(hi, make_float2(-1.f, -1.f), pk);
+                wl[k] = pack_hi_halves(__float_as_uint(lo.x), __float_as_uint(lo.y));
+                lacc[k & 3] = ffma2(pk, ones, lacc[k & 3]);
+              } else {
+                lacc[k & 3] = ffma2(hi, ones, lacc[k & 3]);   // the rounded P that the MMA will use
+              }
+            } else {
+              w[k] = pack2(pk.x, pk.y, QT{});
+              lacc[k & 3] = ffma2(unpack2(w[k], QT{}), ones, lacc[k & 3]);   // the rounded P the MMA uses
+            }
           }
+          // P of these 16 keys goes over their own 16 score columns (read just
+          // above): hi words in the first 8, lo words (bf16 cache) in the next 8
+          tmem_st8(sb + 32 * ck + 16 * hh, w);
+          if constexpr (kSplit) tmem_st8(sb + 32 * ck + 16 * hh + 8, wl);
         }
-        tmem_st16(sb + 16 * hh, w);
-        if constexpr (kSplit) tmem_st16(sb + 32 + 16 * hh, wl);
       }
       tmem_wait_st();
       tc_fence_before();
-      mbar_arrive(&p_full[t * 2 + b]);
+      mbar_arrive(&p_full[t * kBufs + b]);
     }
     const float l = ((lacc[0].x + lacc[0].y) + (lacc[1].x + lacc[1].y)) +
                     ((lacc[2].x + lacc[2].y) + (lacc[3].x + lacc[3].y));
-    // O is complete once the tile's last P.V group has finished
-    if (ok && nkt > 0) ok = wait_all(&o_done[t * 2 + ((nkt - 1) & 1)], ((nkt - 1) >> 1) & 1);
+    // O is complete once the tile's last P.V has finished
+    if (ok && nkt > 0) ok = wait_all(&o_done[t], (nkt - 1) & 1);
     if (ok) {
       tc_fence_after();
       const float inv = l > 0.f ? p.out_mult / l : 0.f;
@@ -532,105 +560,113 @@ __global__ void __launch_bounds__(tc::Roles<kQTiles>::kThreads, 1) prefill_tc_ke
     }
   } else if (warp < kMmaWarp) {
     // ===================================================== loaders (4 warps)
-    // Warp lw fills rows 16*lw .. 16*lw+15 of every K and V tile: 16 keys that
-    // lie inside one block of the block table (tiles start at multiples of 64,
-    // blocks hold 16 or 32 keys).
+    // Warp lw fills rows 32*lw .. 32*lw+31 of every K and V tile: two runs of
+    // 16 keys, each inside one block of the block table (tiles start at
+    // multiples of 128, blocks hold 16 or 32 keys).
     const int lw = warp - kLoadWarp0;
     constexpr int kRowBytes = kFp8 ? kD : 2 * kD;
     const char *kpool = static_cast<const char *>(p.k_cache);
     const char *vpool = static_cast<const char *>(p.v_cache);
-    int32_t win = -1;                 // lane l: block id for tile win_base + l (-1: no data)
-    int win_base = -32;
-    // block id of this warp's rows in tile j (warp-uniform j); -1 past the sequence
-    auto block_of = [&](int j) -> int32_t {
-      if (j - win_base >= 32) {
+    int32_t win = -1;                 // lane l: block id of run (l & 1) of tile win_base + (l >> 1)
+    int win_base = -16;
+    // block id of this warp's run r (0/1) of tile j (warp-uniform); -1 past the sequence
+    auto block_of = [&](int j, int r) -> int32_t {
+      if (j - win_base >= 16) {
         win_base = j;
-        const int key = (j + lane) * kN + 16 * lw;
+        const int jt = j + (lane >> 1);
+        const int key = jt * kN + 32 * lw + 16 * (lane & 1);
         win = -1;
-        if (j + lane < nkt && key < seq_eff) {
+        if (jt < nkt && key < seq_eff) {
           const int32_t bi = __ldg(table + key / p.block_size);
           if (bi < 0 || bi >= p.num_blocks) record_error(p.err, PA_ERR_DEVICE_CHECK);
           else win = bi;
         }
       }
-      return __shfl_sync(0xffffffffu, win, j - win_base);
+      return __shfl_sync(0xffffffffu, win, 2 * (j - win_base) + r);
     };
-    // first cache row of this warp's 16 keys in tile j, and how many of them hold data
-    auto rows_of = [&](int j, int32_t blk, int64_t &row0) -> int {
-      const int key0 = j * kN + 16 * lw;
+    // first cache row of run r's 16 keys in tile j, and how many of them hold data
+    auto rows_of = [&](int j, int r, int64_t &row0) -> int {
+      const int key0 = j * kN + 32 * lw + 16 * r;
+      const int32_t blk = block_of(j, r);
       row0 = ((int64_t)max(blk, 0) * p.num_kv_heads + g) * p.block_size + (key0 % p.block_size);
       return blk < 0 ? 0 : min(16, seq_eff - key0);
     };
     bool ok = true;
+    auto wait_slot = [&](uint64_t *bar, uint32_t parity) {
+      ok = __all_sync(0xffffffffu, wait_or_abort(bar, parity, p.err, abort_flag));
+      return ok;
+    };
     if constexpr (!kFp8) {
       // 16-bit rows (256 B): per instruction 2 rows x 16 chunks of 16 B
       const int q = lane & 15, pn = q >> 3, cq = q & 7;
       for (int j = 0; j < nkt && ok; ++j) {
         const int s = j % kStages;
         const uint32_t ph_prev = ((j / kStages) - 1) & 1;
-        int64_t row0;
-        const int nval = rows_of(j, block_of(j), row0);
+        int64_t row0[2];
+        int nval[2];
+#pragma unroll
+        for (int r = 0; r < 2; ++r) nval[r] = rows_of(j, r, row0[r]);
 #pragma unroll
         for (int which = 0; which < 2; ++which) {
-          if (j >= kStages)
-            ok = __all_sync(0xffffffffu, wait_or_abort(which ? &v_free[s] : &k_free[s], ph_prev, p.err, abort_flag));
-          if (!ok) break;
+          if (j >= kStages && !wait_slot(which ? &v_free[s] : &k_free[s], ph_prev)) break;
           const char *pool = which ? vpool : kpool;
           uint8_t *tile = smem + (which ? L::kOffV : L::kOffK) + s * kTileBytes + pn * kTilePanel;
 #pragma unroll
-          for (int i = 0; i < 8; ++i) {
-            const int r = 2 * i + (lane >> 4);          // row among the warp's 16
-            const int row = 16 * lw + r;                 // row of the tile
-            const bool v = r < nval;
-            const char *src = v ? pool + (row0 + r) * kRowBytes + q * 16 : pool;
-            cp_async16(tile + row * 128 + ((cq ^ (row & 7)) << 4), src, v ? 16u : 0u);
+          for (int r = 0; r < 2; ++r) {
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+              const int rr = 2 * i + (lane >> 4);             // row among the run's 16
+              const int row = 32 * lw + 16 * r + rr;           // row of the tile
+              const bool v = rr < nval[r];
+              const char *src = v ? pool + (row0[r] + rr) * kRowBytes + q * 16 : pool;
+              cp_async16(tile + row * 128 + ((cq ^ (row & 7)) << 4), src, v ? 16u : 0u);
+            }
           }
           cp_async_arrive_noinc(which ? &v_full[s] : &k_full[s]);
         }
       }
     } else {
-      // fp8 rows (128 B): per instruction 4 rows x 8 words of 16 codes, loaded one tile ahead
+      // fp8 rows (128 B): per instruction 4 rows x 8 words of 16 codes.  A tile
+      // is four quarters (K run 0, K run 1, V run 0, V run 1); the next quarter
+      // is in flight while the current one is widened into shared memory.
       const int q = lane & 7, pn = q >> 2, c0 = (2 * q) & 7;
-      uint4 rk[4], rv[4];
-      auto load = [&](int j, uint4 (&ok4)[4], uint4 (&ov4)[4]) {
+      auto load = [&](int j, int qi, uint4 (&w)[4]) {
         int64_t row0;
-        const int nval = rows_of(j, block_of(j), row0);
+        const int nval = rows_of(j, qi & 1, row0);
+        const char *pool = (qi >> 1) ? vpool : kpool;
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
-          const int r = 4 * i + (lane >> 3);
-          const bool v = r < nval;
-          ok4[i] = v ? ld_nc16(kpool + (row0 + r) * kRowBytes + q * 16) : make_uint4(0, 0, 0, 0);
-          ov4[i] = v ? ld_nc16(vpool + (row0 + r) * kRowBytes + q * 16) : make_uint4(0, 0, 0, 0);
+          const int rr = 4 * i + (lane >> 3);
+          w[i] = rr < nval ? ld_nc16(pool + (row0 + rr) * kRowBytes + q * 16) : make_uint4(0, 0, 0, 0);
         }
       };
-      if (nkt > 0) load(0, rk, rv);
+      uint4 cur[4], nxt[4];
+      if (nkt > 0) load(0, 0, cur);
       for (int j = 0; j < nkt && ok; ++j) {
         const int s = j % kStages;
         const uint32_t ph_prev = ((j / kStages) - 1) & 1;
-        uint4 nk[4], nv[4];
-        if (j + 1 < nkt) load(j + 1, nk, nv);
 #pragma unroll
-        for (int which = 0; which < 2; ++which) {
-          if (j >= kStages)
-            ok = __all_sync(0xffffffffu, wait_or_abort(which ? &v_free[s] : &k_free[s], ph_prev, p.err, abort_flag));
-          if (!ok) break;
+        for (int qi = 0; qi < 4; ++qi) {
+          const int which = qi >> 1, r = qi & 1;
+          if (qi < 3) load(j, qi + 1, nxt);
+          else if (j + 1 < nkt) load(j + 1, 0, nxt);
+          if (r == 0 && j >= kStages && !wait_slot(which ? &v_free[s] : &k_free[s], ph_prev)) break;
           uint8_t *tile = smem + (which ? L::kOffV : L::kOffK) + s * kTileBytes + pn * kTilePanel;
 #pragma unroll
           for (int i = 0; i < 4; ++i) {
-            const int row = 16 * lw + 4 * i + (lane >> 3);
+            const int row = 32 * lw + 16 * r + 4 * i + (lane >> 3);
             uint32_t o[8];
-            widen16<QT>(which ? rv[i] : rk[i], o);
+            widen16<QT>(cur[i], o);
             uint8_t *dst = tile + row * 128;
             *reinterpret_cast<uint4 *>(dst + ((c0 ^ (row & 7)) << 4)) = make_uint4(o[0], o[1], o[2], o[3]);
             *reinterpret_cast<uint4 *>(dst + (((c0 + 1) ^ (row & 7)) << 4)) = make_uint4(o[4], o[5], o[6], o[7]);
           }
-          fence_async_smem();
-          mbar_arrive(which ? &v_full[s] : &k_full[s]);
-        }
+          if (r == 1) {
+            fence_async_smem();
+            mbar_arrive(which ? &v_full[s] : &k_full[s]);
+          }
 #pragma unroll
-        for (int i = 0; i < 4; ++i) {
-          rk[i] = nk[i];
-          rv[i] = nv[i];
+          for (int i = 0; i < 4; ++i) cur[i] = nxt[i];
         }
       }
     }
@@ -645,7 +681,9 @@ __global__ void __launch_bounds__(tc::Roles<kQTiles>::kThreads, 1) prefill_tc_ke
   } else {
     // ===================================================== MMA issue (last warp)
     // The whole warp runs the schedule (so descriptors stay warp-uniform); one
-    // elected lane issues the MMAs and their commits.
+    // elected lane issues the MMAs and their commits.  Per key tile j and Q
+    // tile t: O_t += P_t(j) V_j, then -- once that P.V is complete, because
+    // the scores of tile j+1 go where P_t(j) is -- S_t(j+1) = Q_t K_{j+1}^T.
     const bool leader = elect_one();
     const uint32_t idesc_s = umma_idesc(kAB, kN, false);
     const uint32_t idesc_o = umma_idesc(kAB, kD, true);
@@ -657,62 +695,71 @@ __global__ void __launch_bounds__(tc::Roles<kQTiles>::kThreads, 1) prefill_tc_ke
     };
     bool ok = nkt == 0 || wait_all(q_ready, 0);
     bool issued = false;
-    auto pv = [&](int i) {  // O_t += P_t(i) V_i for both Q tiles
-      const int s = i % kStages, b = i & 1;
-      ok = ok && wait_all(&v_full[s], (i / kStages) & 1);
-      if (!ok) return;
-      fence_async_smem();   // tile written through the generic proxy (cp.async / st.shared)
-      const uint64_t vd = vdesc0 + ((s * kTileBytes) >> 4);
+    auto issue_s = [&](int t, int j) {  // S_t(j) = Q_t K_j^T into buffer j % kBufs (K tile j waited for)
+      const uint64_t kd = kdesc0 + (((j % kStages) * kTileBytes) >> 4);
+      const uint64_t qd = qdesc + ((t * kQBytes) >> 4);
+      const int bb = j % kBufs;
+      if (leader) {
 #pragma unroll
-      for (int t = 0; t < kQTiles; ++t) {
-        ok = wait_all(&p_full[t * 2 + b], (i >> 1) & 1);
-        if (!ok) return;
+        for (int k = 0; k < kD / 16; ++k)
+          umma(sbuf(t, bb), qd + (((k >> 2) * (kM * 128) + (k & 3) * 32) >> 4),
+               kd + (((k >> 2) * kTilePanel + (k & 3) * 32) >> 4), idesc_s, k > 0 ? 1u : 0u);
+        umma_commit(&s_full[t * kBufs + bb]);
+      }
+      __syncwarp();
+      issued = true;
+    };
+    // the first kBufs score tiles
+    for (int jj = 0; jj < kBufs && jj < nkt && ok; ++jj) {
+      ok = wait_all(&k_full[jj % kStages], (jj / kStages) & 1);
+      if (!ok) break;
+      fence_async_smem();
+      tc_fence_after();
+      for (int t = 0; t < kQTiles; ++t) issue_s(t, jj);
+      if (leader) umma_commit(&k_free[jj % kStages]);
+      __syncwarp();
+    }
+    for (int j = 0; j < nkt && ok; ++j) {
+      const int s = j % kStages, b = j % kBufs;
+      ok = wait_all(&v_full[s], (j / kStages) & 1);
+      if (!ok) break;
+      const int jn = j + kBufs;                 // the score tile that reuses buffer b
+      const bool more = jn < nkt;
+      const int sn = jn % kStages;
+      const uint64_t vd = vdesc0 + ((s * kTileBytes) >> 4);
+      for (int t = 0; t < kQTiles && ok; ++t) {
+        ok = wait_all(&p_full[t * kBufs + b], (j / kBufs) & 1);
+        if (!ok) break;
+        fence_async_smem();   // V tile written through the generic proxy (cp.async / st.shared)
         tc_fence_after();
         if (leader) {
 #pragma unroll
           for (int half = 0; half < (kSplit ? 2 : 1); ++half) {
 #pragma unroll
-            for (int kk = 0; kk < kN / 16; ++kk)
-              umma_ts(obuf(t), sbuf(t, b) + half * 32 + kk * 8, vd + ((kk * 16 * 128) >> 4), idesc_o,
-                      (i > 0 || half > 0 || kk > 0) ? 1u : 0u);
+            for (int kk = 0; kk < kN / 16; ++kk)   // keys 16kk..16kk+15: P hi at column 16kk, lo at 16kk+8
+              umma_ts(obuf(t), sbuf(t, b) + 16 * kk + 8 * half, vd + ((kk * 16 * 128) >> 4), idesc_o,
+                      (j > 0 || half > 0 || kk > 0) ? 1u : 0u);
           }
-          umma_commit(&o_done[t * 2 + b]);
+          umma_commit(&o_done[t]);
+          if (t == kQTiles - 1) umma_commit(&v_free[s]);
         }
         __syncwarp();
-      }
-      if (leader) umma_commit(&v_free[s]);
-      __syncwarp();
-    };
-    if (ok) tc_fence_after();
-    for (int j = 0; j < nkt && ok; ++j) {
-      const int s = j % kStages, b = j & 1;
-      ok = wait_all(&k_full[s], (j / kStages) & 1);
-      if (!ok) break;
-      fence_async_smem();
-      const uint64_t kd = kdesc0 + ((s * kTileBytes) >> 4);
-#pragma unroll
-      for (int t = 0; t < kQTiles; ++t) {
-        // score buffer b of tile t last held P_t(j-2): its P.V group must be done
-        if (j >= 2) ok = wait_all(&o_done[t * 2 + b], ((j - 2) >> 1) & 1);
-        if (!ok) break;
-        tc_fence_after();
-        const uint64_t qd = qdesc + ((t * kQBytes) >> 4);
-        if (leader) {
-#pragma unroll
-          for (int k = 0; k < kD / 16; ++k)
-            umma(sbuf(t, b), qd + (((k >> 2) * (kM * 128) + (k & 3) * 32) >> 4),
-                 kd + (((k >> 2) * kTilePanel + (k & 3) * 32) >> 4), idesc_s, k > 0 ? 1u : 0u);
-          umma_commit(&s_full[t * 2 + b]);
+        if (more) {
+          if (t == 0) {
+            ok = wait_all(&k_full[sn], (jn / kStages) & 1);
+            if (!ok) break;
+          }
+          // S_t(jn) overwrites P_t(j): wait for its P.V
+          ok = wait_all(&o_done[t], j & 1);
+          if (!ok) break;
+          fence_async_smem();
+          tc_fence_after();
+          issue_s(t, jn);
+          if (t == kQTiles - 1 && leader) umma_commit(&k_free[sn]);
+          __syncwarp();
         }
-        __syncwarp();
-        issued = true;
       }
-      if (!ok) break;
-      if (leader) umma_commit(&k_free[s]);
-      __syncwarp();
-      if (j >= 1) pv(j - 1);
     }
-    if (ok && nkt > 0) pv(nkt - 1);
     // every MMA issued above is complete before tensor memory is freed
     if (issued) {
       if (leader) umma_commit(fin);
