@@ -40,11 +40,11 @@
 //    tiles, one tile's MMAs run while the other tile's softmax works.
 //
 // Precision.  Q, K and V are exact in the MMA (fp8 codes widen exactly to
-// bf16/f16); accumulation is fp32.  P is rounded to the 16-bit type; with a
-// bf16 cache P is split into hi + lo bf16 parts (two P.V MMAs) so its
-// rounding stays below 2^-16 relative, and with f16 or fp8 caches the softmax
-// denominator sums the rounded P, so the output remains a convex combination
-// of V rows.
+// bf16/f16); accumulation is fp32.  P must be 16-bit in the MMA: with a bf16
+// cache P is split into hi + lo bf16 parts (two P.V MMAs) that sum to P
+// within 2^-15 relative; with f16 or fp8 caches P is rounded once and the
+// softmax denominator sums the rounded P, so the output remains a convex
+// combination of V rows.
 //
 // Every mbarrier wait is bounded (PA_ERR_TIMEOUT, then the CTA abandons its
 // work); before tensor memory is freed the CTA waits for its outstanding MMAs
@@ -255,6 +255,13 @@ __device__ __forceinline__ uint32_t bf16_round_bits(float x) {
 // Pack the upper halves of two fp32 bit patterns into one bf16x2 word (a low, b high).
 __device__ __forceinline__ uint32_t pack_hi_halves(uint32_t a, uint32_t b) { return __byte_perm(a, b, 0x7632); }
 
+// max(a, b, c) in one instruction.
+__device__ __forceinline__ float fmax3(float a, float b, float c) {
+  float d;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+  return d;
+}
+
 // Bounded wait that also gives up once another role of the CTA has given up.
 __device__ __forceinline__ bool wait_or_abort(uint64_t *bar, uint32_t parity, int32_t *err,
                                               volatile int *abort_flag) {
@@ -443,11 +450,13 @@ __global__ void __launch_bounds__(tc::Roles<kQTiles>::kThreads, 1) prefill_tc_ke
       for (int ck = 0; ck < kChunks; ++ck) {
         float sv[32];
         tmem_ld32(sb + 32 * ck, sv);
+        if (!full_tile) {
 #pragma unroll
-        for (int i = 0; i < 32; ++i) {
-          const float x = (full_tile || 32 * ck + i < nvis) ? sv[i] : kNegInf;
-          mx[i & 7] = fmaxf(mx[i & 7], x);
+          for (int i = 0; i < 32; ++i)
+            if (32 * ck + i >= nvis) sv[i] = kNegInf;
         }
+#pragma unroll
+        for (int i = 0; i < 16; ++i) mx[i & 7] = fmax3(mx[i & 7], sv[2 * i], sv[2 * i + 1]);
       }
       const float mr = fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])),
                              fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7])));
@@ -496,19 +505,21 @@ __global__ void __launch_bounds__(tc::Roles<kQTiles>::kThreads, 1) prefill_tc_ke
               if (i0 >= nvis) pk.x = 0.f;
               if (i0 + 1 >= nvis) pk.y = 0.f;
             }
-            if constexpr (kBf16) {
+            if constexpr (kSplit) {
+              // bf16 cache: hi = p truncated to bf16, lo = p - hi (exact in fp32) truncated to
+              // bf16; hi + lo is within 2^-15 of p, and the denominator sums p itself
+              const uint32_t h0 = __float_as_uint(pk.x) & 0xffff0000u, h1 = __float_as_uint(pk.y) & 0xffff0000u;
+              w[k] = pack_hi_halves(h0, h1);
+              const float2 lo = ffma2(make_float2(__uint_as_float(h0), __uint_as_float(h1)),
+                                      make_float2(-1.f, -1.f), pk);
+              wl[k] = pack_hi_halves(__float_as_uint(lo.x), __float_as_uint(lo.y));
+              lacc[k & 3] = ffma2(pk, ones, lacc[k & 3]);
+            } else if constexpr (kBf16) {
               // integer rounding keeps the conversion off the transcendental pipe
               const uint32_t h0 = bf16_round_bits(pk.x), h1 = bf16_round_bits(pk.y);
               w[k] = pack_hi_halves(h0, h1);
-              const float2 hi = make_float2(__uint_as_float(h0), __uint_as_float(h1));
-              if constexpr (kSplit) {
-                // lo = p - hi is exact in fp32; truncating it to bf16 leaves < 2^-16 relative error in P
-                const float2 lo = ffma2(hi, make_float2(-1.f, -1.f), pk);
-                wl[k] = pack_hi_halves(__float_as_uint(lo.x), __float_as_uint(lo.y));
-                lacc[k & 3] = ffma2(pk, ones, lacc[k & 3]);
-              } else {
-                lacc[k & 3] = ffma2(hi, ones, lacc[k & 3]);   // the rounded P that the MMA will use
-              }
+              lacc[k & 3] = ffma2(make_float2(__uint_as_float(h0), __uint_as_float(h1)), ones,
+                                  lacc[k & 3]);   // the rounded P that the MMA will use
             } else {
               w[k] = pack2(pk.x, pk.y, QT{});
               lacc[k & 3] = ffma2(unpack2(w[k], QT{}), ones, lacc[k & 3]);   // the rounded P the MMA uses
