@@ -305,9 +305,10 @@ __device__ __forceinline__ void widen16(uint4 w, uint32_t (&o)[8]) {
       o[2 * i] = *reinterpret_cast<const uint32_t *>(&lo);
       o[2 * i + 1] = *reinterpret_cast<const uint32_t *>(&hi);
     } else {
+      // every e4m3 value is a bf16 value: the upper halves of the fp32 patterns are exact
       const float2 lo = unpack2_e4m3(ws[i]), hi = unpack2_e4m3(ws[i] >> 16);
-      o[2 * i] = pack2(lo.x, lo.y, QT{});
-      o[2 * i + 1] = pack2(hi.x, hi.y, QT{});
+      o[2 * i] = __byte_perm(__float_as_uint(lo.x), __float_as_uint(lo.y), 0x7632);
+      o[2 * i + 1] = __byte_perm(__float_as_uint(hi.x), __float_as_uint(hi.y), 0x7632);
     }
   }
 }
