@@ -6,11 +6,49 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <atomic>
+
 #include "../../include/pa.h"
 
 namespace pa {
 
 inline int dtype_bytes(pa_dtype t) { return t == PA_FP8_E4M3 ? 1 : 2; }
+
+// Raise kernel Kern's dynamic shared-memory limit to `bytes`, once per device
+// (the attribute belongs to the function on the current device; setting it on
+// every launch would cost a driver call per launch).
+template <auto Kern>
+inline cudaError_t ensure_smem_limit(int bytes) {
+  static std::atomic<uint64_t> done{0};  // bit d: set on device d (devices 0..63; others every call)
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  const uint64_t bit = dev >= 0 && dev < 64 ? (uint64_t{1} << dev) : 0;
+  if (bit && (done.load(std::memory_order_acquire) & bit)) return cudaSuccess;
+  e = cudaFuncSetAttribute(Kern, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+  if (e == cudaSuccess && bit) done.fetch_or(bit, std::memory_order_acq_rel);
+  return e;
+}
+
+// Number of SMs of the current device (queried once per device).
+inline cudaError_t current_sm_count(int *sms) {
+  static std::atomic<int> cache[64];
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev >= 0 && dev < 64) {
+    const int v = cache[dev].load(std::memory_order_relaxed);
+    if (v > 0) {
+      *sms = v;
+      return cudaSuccess;
+    }
+  }
+  int v = 0;
+  if ((e = cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess) return e;
+  if (dev >= 0 && dev < 64) cache[dev].store(v, std::memory_order_relaxed);
+  *sms = v;
+  return cudaSuccess;
+}
 
 constexpr int kDefaultPartition = 512;   // split-KV partition, tokens (also the largest used)
 constexpr int kMaxPartitions = 4096;     // per sequence (item encoding: 12 bits)

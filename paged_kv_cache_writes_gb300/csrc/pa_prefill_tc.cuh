@@ -799,7 +799,7 @@ cudaError_t launch_prefill_tc_tiles(const PrefillTcParams &p0, int num_chunks, c
   PrefillTcParams p = p0;
   p.row_blocks = (p.max_q_len + BR - 1) / BR;
   auto kern = prefill_tc_kernel<KV, QT, G, kQTiles>;
-  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  cudaError_t e = ensure_smem_limit<prefill_tc_kernel<KV, QT, G, kQTiles>>(smem);
   if (e != cudaSuccess) return e;
   const int64_t gx = (int64_t)num_chunks * p.row_blocks;
   if (gx > 2147483647ll || p.num_kv_heads > 65535) return cudaErrorInvalidValue;
@@ -817,10 +817,8 @@ cudaError_t launch_prefill_tc_one(const PrefillTcParams &p, int num_chunks, int 
 
 template <typename KV, typename QT>
 cudaError_t launch_prefill_tc(const PrefillTcParams &p, int gqa, int num_chunks, cudaStream_t s) {
-  int dev = 0, num_sms = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess ||
-      cudaDeviceGetAttribute(&num_sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
-    return cudaErrorUnknown;
+  int num_sms = 0;
+  if (current_sm_count(&num_sms) != cudaSuccess) return cudaErrorUnknown;
   switch (gqa) {
     case 1: return launch_prefill_tc_one<KV, QT, 1>(p, num_chunks, num_sms, s);
     case 2: return launch_prefill_tc_one<KV, QT, 2>(p, num_chunks, num_sms, s);

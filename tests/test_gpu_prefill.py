@@ -150,11 +150,12 @@ def test_prefill_tensor_core_metadata_errors(kv):
     (64, 8, [(int(s), 100) for s in range(0, 800, 100)]),
     (8, 8, [(int(s), 256 - s % 7) for s in range(0, 2000, 100)]),
 ])
-def test_prefill_two_q_tiles_per_cta(src, kv, hq, hkv, chunks):
+@pytest.mark.parametrize("bs", [16, 32])
+def test_prefill_two_q_tiles_per_cta(src, kv, hq, hkv, chunks, bs):
     g = hq // hkv
     br = 256 // g
     assert sum(-(-c // br) for _, c in chunks) * hkv >= 152
-    b = W.prefill_batch("p", chunks, hq, hkv, 128, 16, src, kv_dtype=kv, seed=hq + len(chunks))
+    b = W.prefill_batch("p", chunks, hq, hkv, 128, bs, src, kv_dtype=kv, seed=hq + len(chunks) + bs)
     dev = run_gpu(b)
     kp, vp = oracle_pools(b)
     ref = oracle.prefill_batch(b, kp, vp)
