@@ -65,7 +65,8 @@ typedef enum {
     PA_ERR_UNSUPPORTED = 2,  /* head_dim / block_size / dtype combination not built */
     PA_ERR_CUDA = 3,         /* a CUDA runtime call or kernel launch failed */
     PA_ERR_DEVICE_CHECK = 4, /* a kernel found out-of-range device metadata */
-    PA_ERR_TIMEOUT = 5       /* a kernel's bounded wait on an async copy expired */
+    PA_ERR_TIMEOUT = 5,      /* a kernel's bounded wait on an async copy expired */
+    PA_ERR_NO_BLOCKS = 6     /* block manager: not enough free blocks for the request */
 } pa_status;
 
 /* PA_F32 is accepted only as the dtype of an attention output. */
@@ -268,6 +269,72 @@ PA_API pa_status pa_get_device_error(pa_stream_t stream, int32_t *code);
  * returns; the context stays usable.  Returns PA_ERR_CUDA if the launch fails.
  */
 PA_API pa_status pa_selftest_wait_timeout(pa_stream_t stream);
+
+/*
+ * Block manager -- host-side bookkeeping of the paged pool (no GPU work, no
+ * device memory): the block tables, slots and copy-on-write pairs that the
+ * calls above take.  ([ARCH] "The Block Table Mapping Subsystem"; [V07]
+ * "Architectural Blueprint 2: How PagedAttention Actually Works"; [HT] "2.
+ * Virtual Memory Paging Applied to GPUs": blocks on demand, sharing with
+ * reference counts, copy-on-write of a shared block on the first write.)
+ *
+ * A manager owns num_blocks physical blocks of block_size slots.  Sequences
+ * are small integer ids it hands out.  A token at position p of a sequence
+ * lives in slot table[p / block_size] * block_size + p % block_size.
+ *  - pa_bm_create: shuffle_seed 0 hands out blocks in increasing id order; any
+ *    other value hands them out in a seeded random order (a fragmented pool).
+ *    *bm receives the manager, released with pa_bm_destroy.
+ *  - pa_bm_new_sequence: an empty sequence.
+ *  - pa_bm_fork: a new sequence sharing every block of `parent` (its length
+ *    and table), e.g. one branch of parallel sampling.
+ *  - pa_bm_append: extend `seq` by num_tokens positions; slots[i] (host
+ *    int64, num_tokens entries) receives the slot of each new token, to pass
+ *    to pa_reshape_and_cache.  A block is taken when a sequence enters a new
+ *    logical block.  If the last block is shared (a fork) and partly filled,
+ *    it is first replaced by a fresh copy: the (src, dst) block pair goes to
+ *    cow_pairs (host int32, 2 per pair, cow_capacity pairs) and *num_cow
+ *    receives the count (at most 1); run pa_copy_blocks on them before the
+ *    cache write.  token_ids (host int32, num_tokens entries, or NULL) enables
+ *    prefix reuse: every block this call fills completely is remembered by a
+ *    hash of the token ids of the sequence up to and including it, and a later
+ *    append that fills a block with the same ids after the same prefix shares
+ *    that block instead of taking a new one; its slots are returned as -1,
+ *    which pa_reshape_and_cache skips.  PA_ERR_NO_BLOCKS if the free blocks
+ *    cannot cover the worst case (no reuse); PA_ERR_INVALID_ARG with *num_cow
+ *    = 1 if a copy is needed and cow_capacity is 0.  Nothing changes on error.
+ *  - pa_bm_free: release the sequence's blocks (a shared block returns to the
+ *    free list when its last sequence releases it).
+ *  - pa_bm_block_table: copy the sequence's table into `table` (host int32,
+ *    `capacity` entries); *num_blocks and *seq_len receive its size and length
+ *    (set even when capacity is too small, which returns PA_ERR_INVALID_ARG).
+ *  - pa_bm_get_stats: pool occupancy.
+ * Not thread-safe: one manager per thread, or external locking.
+ */
+typedef struct pa_block_manager pa_block_manager;
+typedef struct {
+    int32_t free_blocks;      /* blocks on the free list */
+    int32_t used_blocks;      /* blocks with at least one reference */
+    int32_t shared_blocks;    /* blocks referenced by more than one sequence */
+    int32_t cached_blocks;    /* full blocks remembered for prefix reuse */
+    int32_t live_sequences;
+    int64_t logical_tokens;   /* sum of live sequences' lengths */
+    int64_t logical_blocks;   /* sum of live sequences' table sizes */
+} pa_bm_stats;
+
+PA_API pa_status pa_bm_create(int32_t num_blocks, int32_t block_size,
+                              uint64_t shuffle_seed, pa_block_manager **bm);
+PA_API void pa_bm_destroy(pa_block_manager *bm);
+PA_API pa_status pa_bm_new_sequence(pa_block_manager *bm, int32_t *seq);
+PA_API pa_status pa_bm_fork(pa_block_manager *bm, int32_t parent, int32_t *child);
+PA_API pa_status pa_bm_append(pa_block_manager *bm, int32_t seq, int32_t num_tokens,
+                              const int32_t *token_ids, int64_t *slots,
+                              int32_t *cow_pairs, int32_t cow_capacity,
+                              int32_t *num_cow);
+PA_API pa_status pa_bm_free(pa_block_manager *bm, int32_t seq);
+PA_API pa_status pa_bm_block_table(const pa_block_manager *bm, int32_t seq,
+                                   int32_t *table, int32_t capacity,
+                                   int32_t *num_blocks, int32_t *seq_len);
+PA_API pa_status pa_bm_get_stats(const pa_block_manager *bm, pa_bm_stats *stats);
 
 /* Static, human-readable name of a status code. */
 PA_API const char *pa_status_string(pa_status status);

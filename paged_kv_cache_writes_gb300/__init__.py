@@ -17,12 +17,13 @@ import torch
 __all__ = [
     "PA_F16", "PA_BF16", "PA_FP8_E4M3", "PA_F32", "PaError", "PaKvCache", "lib", "kv_cache_desc",
     "pa_reshape_and_cache", "pa_copy_blocks", "pa_decode_workspace_bytes", "pa_decode",
-    "pa_prefill_chunk", "pa_get_device_error", "pa_status_string",
+    "pa_prefill_chunk", "pa_get_device_error", "pa_status_string", "pa_selftest_wait_timeout",
+    "BlockManager", "PaBmStats",
 ]
 
 PA_F16, PA_BF16, PA_FP8_E4M3, PA_F32 = 0, 1, 2, 3
 STATUS_NAMES = {0: "PA_OK", 1: "PA_ERR_INVALID_ARG", 2: "PA_ERR_UNSUPPORTED", 3: "PA_ERR_CUDA",
-                4: "PA_ERR_DEVICE_CHECK", 5: "PA_ERR_TIMEOUT"}
+                4: "PA_ERR_DEVICE_CHECK", 5: "PA_ERR_TIMEOUT", 6: "PA_ERR_NO_BLOCKS"}
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_HERE, "libpa.so")
@@ -39,6 +40,14 @@ class PaKvCache(ctypes.Structure):
     _fields_ = [("num_blocks", ctypes.c_int64), ("block_size", ctypes.c_int32),
                 ("num_kv_heads", ctypes.c_int32), ("head_dim", ctypes.c_int32),
                 ("kv_dtype", ctypes.c_int), ("k_scale", ctypes.c_float), ("v_scale", ctypes.c_float)]
+
+
+class PaBmStats(ctypes.Structure):
+    """Mirror of ``pa_bm_stats``."""
+    _fields_ = [("free_blocks", ctypes.c_int32), ("used_blocks", ctypes.c_int32),
+                ("shared_blocks", ctypes.c_int32), ("cached_blocks", ctypes.c_int32),
+                ("live_sequences", ctypes.c_int32), ("logical_tokens", ctypes.c_int64),
+                ("logical_blocks", ctypes.c_int64)]
 
 
 _lib = None
@@ -64,8 +73,19 @@ def lib() -> ctypes.CDLL:
         L.pa_selftest_wait_timeout.argtypes = [P]
         L.pa_status_string.argtypes = [ctypes.c_int]
         L.pa_status_string.restype = ctypes.c_char_p
+        VP = ctypes.c_void_p
+        L.pa_bm_create.argtypes = [I32, I32, ctypes.c_uint64, ctypes.POINTER(VP)]
+        L.pa_bm_destroy.argtypes = [VP]
+        L.pa_bm_destroy.restype = None
+        L.pa_bm_new_sequence.argtypes = [VP, ctypes.POINTER(I32)]
+        L.pa_bm_fork.argtypes = [VP, I32, ctypes.POINTER(I32)]
+        L.pa_bm_append.argtypes = [VP, I32, I32, P, P, P, I32, ctypes.POINTER(I32)]
+        L.pa_bm_free.argtypes = [VP, I32]
+        L.pa_bm_block_table.argtypes = [VP, I32, P, I32, ctypes.POINTER(I32), ctypes.POINTER(I32)]
+        L.pa_bm_get_stats.argtypes = [VP, ctypes.POINTER(PaBmStats)]
         for name in ("pa_reshape_and_cache", "pa_copy_blocks", "pa_decode", "pa_prefill_chunk",
-                     "pa_get_device_error", "pa_selftest_wait_timeout"):
+                     "pa_get_device_error", "pa_selftest_wait_timeout", "pa_bm_create", "pa_bm_new_sequence",
+                     "pa_bm_fork", "pa_bm_append", "pa_bm_free", "pa_bm_block_table", "pa_bm_get_stats"):
             getattr(L, name).restype = ctypes.c_int
         _lib = L
     return _lib
@@ -185,3 +205,73 @@ def pa_selftest_wait_timeout(stream=None) -> None:
 
 def pa_status_string(status: int) -> str:
     return lib().pa_status_string(int(status)).decode()
+
+
+class BlockManager:
+    """Host block manager of one paged pool (``pa_bm_*``): block tables, slots,
+    fork with shared blocks, copy-on-write pairs and prefix reuse.  Host only:
+    works without a GPU.  Arrays are numpy (int32 tables/ids/pairs, int64 slots)."""
+
+    def __init__(self, num_blocks: int, block_size: int, shuffle_seed: int = 0):
+        import numpy as np  # noqa: F401  (numpy arrays are the interface)
+        self._h = ctypes.c_void_p()
+        self.block_size = int(block_size)
+        _ok(lib().pa_bm_create(int(num_blocks), int(block_size), int(shuffle_seed), ctypes.byref(self._h)),
+            "pa_bm_create")
+
+    def close(self) -> None:
+        if self._h:
+            lib().pa_bm_destroy(self._h)
+            self._h = ctypes.c_void_p()
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+    def new_sequence(self) -> int:
+        s = ctypes.c_int32()
+        _ok(lib().pa_bm_new_sequence(self._h, ctypes.byref(s)), "pa_bm_new_sequence")
+        return s.value
+
+    def fork(self, parent: int) -> int:
+        c = ctypes.c_int32()
+        _ok(lib().pa_bm_fork(self._h, int(parent), ctypes.byref(c)), "pa_bm_fork")
+        return c.value
+
+    def append(self, seq: int, num_tokens: int, token_ids=None):
+        """Returns (slots int64[num_tokens], cow pairs int32[k, 2])."""
+        import numpy as np
+        slots = np.empty(int(num_tokens), dtype=np.int64)
+        pairs = np.empty((1, 2), dtype=np.int32)
+        ncow = ctypes.c_int32()
+        ids = None
+        if token_ids is not None:
+            ids = np.ascontiguousarray(token_ids, dtype=np.int32)
+            if ids.shape != (int(num_tokens),):
+                raise ValueError("token_ids must have num_tokens entries")
+        _ok(lib().pa_bm_append(self._h, int(seq), int(num_tokens),
+                               None if ids is None else ids.ctypes.data, slots.ctypes.data if num_tokens else None,
+                               pairs.ctypes.data, 1, ctypes.byref(ncow)), "pa_bm_append")
+        return slots, pairs[:ncow.value].copy()
+
+    def free(self, seq: int) -> None:
+        _ok(lib().pa_bm_free(self._h, int(seq)), "pa_bm_free")
+
+    def block_table(self, seq: int):
+        """Returns (table int32[num_blocks], seq_len)."""
+        import numpy as np
+        nb, L = ctypes.c_int32(), ctypes.c_int32()
+        st = lib().pa_bm_block_table(self._h, int(seq), None, 0, ctypes.byref(nb), ctypes.byref(L))
+        if st not in (0, 1):
+            _ok(st, "pa_bm_block_table")
+        table = np.empty(nb.value, dtype=np.int32)
+        _ok(lib().pa_bm_block_table(self._h, int(seq), table.ctypes.data if nb.value else None, nb.value,
+                                    ctypes.byref(nb), ctypes.byref(L)), "pa_bm_block_table")
+        return table, L.value
+
+    def stats(self) -> PaBmStats:
+        st = PaBmStats()
+        _ok(lib().pa_bm_get_stats(self._h, ctypes.byref(st)), "pa_bm_get_stats")
+        return st

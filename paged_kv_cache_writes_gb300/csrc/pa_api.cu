@@ -393,6 +393,7 @@ const char *pa_status_string(pa_status status) {
     case PA_ERR_CUDA: return "PA_ERR_CUDA";
     case PA_ERR_DEVICE_CHECK: return "PA_ERR_DEVICE_CHECK";
     case PA_ERR_TIMEOUT: return "PA_ERR_TIMEOUT";
+    case PA_ERR_NO_BLOCKS: return "PA_ERR_NO_BLOCKS";
   }
   return "PA_ERR_UNKNOWN";
 }
