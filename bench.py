@@ -75,6 +75,10 @@ PREFILL_WORKLOADS = {
                         "head_dim 128, block 16"),
     # enough rows to give every SM a CTA: 8 chunks of 2048 tokens over 2048 tokens of context, bf16 KV
     "bf16_8x2048": "8 chunks x 2048 tokens at position 2048, GQA 32/8, head_dim 128, block 16, bf16 KV",
+    # chunk-size and shape variants: one 2048-token chunk at position 4096 (GQA 32/8), and an MHA layer
+    # (32 KV heads) with 4 chunks of 1024 tokens at position 1024
+    "bf16_chunk2048": "one 2048-token chunk at position 4096, GQA 32/8, head_dim 128, block 16, bf16 KV",
+    "bf16_mha_4x1024": "4 chunks x 1024 tokens at position 1024, MHA 32/32, head_dim 128, block 16, bf16 KV",
 }
 
 
@@ -86,7 +90,11 @@ def measure_other_decodes(dev_name: str, steps: int, warmup: int) -> dict:
     from paged_kv_cache_writes_gb300.staging import DeviceBatch
     peak, kind = _peaks()
     res = {}
-    for key, fn in (("llama8b", W.cfg_llama8b), ("shared_prefix", W.cfg_shared_prefix), ("mixed_fp8_decodes", W.cfg_mixed_fp8)):
+    cases = (("llama8b", W.cfg_llama8b), ("shared_prefix", W.cfg_shared_prefix),
+             ("mixed_fp8_decodes", W.cfg_mixed_fp8),
+             ("llama8b_fp8_cache", lambda: W.cfg_llama8b(kv_dtype="fp8")),
+             ("llama70b_fp8_cache", lambda: W.cfg_llama70b(kv_dtype="fp8")))
+    for key, fn in cases:
         b = fn()
         db = DeviceBatch(b, dev_name)
         db.run_setup()
@@ -124,8 +132,12 @@ def measure_prefill(dev_name: str, steps: int, warmup: int) -> dict:
     for key, desc in PREFILL_WORKLOADS.items():
         if key == "mixed_fp8_chunk":
             b = W.cfg_mixed_fp8()
-        else:
+        elif key == "bf16_8x2048":
             b = W.prefill_batch("prefill 8x2048", [(2048, 2048)] * 8, 32, 8, 128, 16, "bf16", seed=3)
+        elif key == "bf16_chunk2048":
+            b = W.prefill_batch("prefill chunk 2048", [(4096, 2048)], 32, 8, 128, 16, "bf16", seed=5)
+        else:
+            b = W.prefill_batch("prefill MHA 4x1024", [(1024, 1024)] * 4, 32, 32, 128, 16, "bf16", seed=6)
         db = DeviceBatch(b, dev_name)
         db.run_setup()
         db.write_step()
@@ -278,9 +290,20 @@ def cpu_oracle_rate(b, seconds: float = 15.0):
     target = max(1 << 20, int(nbytes * seconds / max(t, 1e-3)))
     ids, nbytes = _sample_ids(b, target, rng)
     t = _time_oracle(b, kp, vp, ids)
-    return {"value": nbytes / t / 1e9, "unit": UNIT, "cores": oracle.max_threads(), "kind": "oracle",
-            "sample": f"{len(ids)} of {b.num_seqs} sequences ({nbytes / 1e6:.0f} MB of KV), fp64 C, OpenMP, "
-                      f"{t:.1f} s"}
+    res = {"value": nbytes / t / 1e9, "unit": UNIT, "cores": oracle.max_threads(), "kind": "oracle",
+           "sample": f"{len(ids)} of {b.num_seqs} sequences ({nbytes / 1e6:.0f} MB of KV), fp64 C, OpenMP, "
+                     f"{t:.1f} s"}
+    # the same oracle on one thread, over a smaller sample (reference point only)
+    cores = oracle.max_threads()
+    oracle.set_threads(1)
+    try:
+        ids1, nb1 = _sample_ids(b, max(1 << 20, target // max(1, cores) // 3), rng)
+        t1 = _time_oracle(b, kp, vp, ids1)
+    finally:
+        oracle.set_threads(cores)
+    res["one_thread"] = {"value": nb1 / t1 / 1e9, "unit": UNIT,
+                         "sample": f"{len(ids1)} sequences ({nb1 / 1e6:.0f} MB of KV), {t1:.1f} s"}
+    return res
 
 
 def run_reference(args):
@@ -348,6 +371,7 @@ def run_ours(args):
     torch.cuda.synchronize()
 
     ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    evw = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
     start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     if ws > 1:
         torch.distributed.barrier()
@@ -355,6 +379,7 @@ def run_ours(args):
     with ClockSampler(local) as clocks:
         start.record(stream)
         for i in range(args.steps):
+            evw[i].record(stream)
             db.write_step()
             ev[i][0].record(stream)
             db.decode()
@@ -364,7 +389,12 @@ def run_ours(args):
     if ws > 1:
         torch.distributed.barrier()
     ms = start.elapsed_time(end) / args.steps
-    dec_ms = statistics.mean(a.elapsed_time(z) for a, z in ev)
+    dec_all = sorted(a.elapsed_time(z) for a, z in ev)
+    dec_ms = statistics.mean(dec_all)
+    write_ms = statistics.mean(w.elapsed_time(a) for w, (a, _) in zip(evw, ev))
+
+    def pct(q):
+        return dec_all[min(len(dec_all) - 1, int(q * (len(dec_all) - 1) + 0.5))]
     assert pa.pa_get_device_error() == 0
     if ws > 1:
         t = torch.tensor([ms], device=dev_name)
@@ -417,6 +447,8 @@ def run_ours(args):
         "config": _config(b, {"parallelism": f"replicas x{ws}" if ws > 1 else "single GPU"}),
         "tokens_per_s_per_layer": b.num_seqs * ws / (ms * 1e-3),
         "decode_ms": dec_ms,
+        "decode_ms_p10_p50_p90": [pct(0.1), pct(0.5), pct(0.9)],
+        "write_ms": write_ms,
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
                      "traffic": _profiled_traffic(kv_bytes),
                      "kernel": "paged_decode_kernel (pa_decode: plan + decode launches, timed together)",

@@ -110,6 +110,16 @@ def test_shared_prefix_full():
     _check(b)
 
 
+@pytest.mark.parametrize("cfg", ["llama8b", "llama70b"])
+def test_decode_shapes_with_fp8_cache_sampled(cfg):
+    # the decode-only workloads with the cache stored as e4m3 (same values, per-tensor scales)
+    b = {"llama8b": W.cfg_llama8b, "llama70b": W.cfg_llama70b}[cfg](kv_dtype="fp8")
+    assert b.kv_dtype == "fp8"
+    order = np.argsort(b.seq_lens)
+    sample = np.unique(np.concatenate([order[:4], order[-6:], order[::16]]))
+    _check(b, seq_ids=sample)
+
+
 def test_mixed_fp8_decode_part_sampled():
     b = W.cfg_mixed_fp8()
     _check(b, seq_ids=np.arange(0, b.num_seqs, 8))

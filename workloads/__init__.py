@@ -434,20 +434,22 @@ def cfg_tiny(seed: int = 0) -> PagedBatch:
                         num_blocks=64, scale=float(np.float32(0.125)))
 
 
-def cfg_llama8b(seed: int = 1, batch: int = 64) -> PagedBatch:
+def cfg_llama8b(seed: int = 1, batch: int = 64, kv_dtype: str = "bf16") -> PagedBatch:
     """Llama-3-8B-shaped decode layer: 32/8 heads, head_dim 128, block 16,
-    bf16, lengths uniform 512..4096, 20k-block pool."""
+    bf16, lengths uniform 512..4096, 20k-block pool.  kv_dtype "fp8" stores
+    the same values as e4m3 codes with per-tensor scales."""
     lens = np.random.default_rng(seed + 100).integers(512, 4097, size=batch)
-    return decode_batch("Llama-3-8B-shaped decode layer", lens, 32, 8, 128, 16, "bf16", seed=seed,
-                        num_blocks=20000)
+    name = "Llama-3-8B-shaped decode layer" + (", fp8 KV" if kv_dtype == "fp8" else "")
+    return decode_batch(name, lens, 32, 8, 128, 16, "bf16", kv_dtype=kv_dtype, seed=seed, num_blocks=20000)
 
 
-def cfg_llama70b(seed: int = 2, batch: int = 256) -> PagedBatch:
+def cfg_llama70b(seed: int = 2, batch: int = 256, kv_dtype: str = "bf16") -> PagedBatch:
     """Llama-3-70B-shaped decode layer: 64/8 heads, head_dim 128, block 32,
-    bf16, log-normal lengths (median 1000, cap 8192), split-KV 512."""
+    bf16, log-normal lengths (median 1000, cap 8192), split-KV 512.  kv_dtype
+    "fp8" stores the same values as e4m3 codes with per-tensor scales."""
     lens = lognormal_lens(np.random.default_rng(seed + 100), batch)
-    return decode_batch("Llama-3-70B-shaped decode layer", lens, 64, 8, 128, 32, "bf16", seed=seed,
-                        partition_size=512)
+    name = "Llama-3-70B-shaped decode layer" + (", fp8 KV" if kv_dtype == "fp8" else "")
+    return decode_batch(name, lens, 64, 8, 128, 32, "bf16", kv_dtype=kv_dtype, seed=seed, partition_size=512)
 
 
 def cfg_shared_prefix(seed: int = 3, num_prompts: int = 32) -> PagedBatch:
