@@ -185,6 +185,25 @@ PA_API pa_status pa_decode(const void *q, pa_dtype q_dtype, int32_t num_seqs,
                     pa_stream_t stream);
 
 /*
+ * pa_set_decode_kernel -- choose which of the library's two decode kernels
+ * pa_decode and pa_decode_noalloc launch from now on (process-wide, any
+ * thread, effective from the next call).  The pages describe one decode
+ * kernel on CUDA cores; the choice is this library's own.  Both compute the
+ * result defined above, in fp32, within the decode tolerance of each other.
+ *   PA_DECODE_KERNEL_AUTO (default): the tensor-core kernel where it applies
+ *     (head_dim 128 with 4, 8 or 16 query heads per KV head: the Q.K^T and
+ *     P.V of a KV head's query group run as MMAs), the CUDA-core kernel
+ *     for every other shape;
+ *   PA_DECODE_KERNEL_CUDA_CORES: the CUDA-core kernel for every shape.
+ * Returns PA_ERR_INVALID_ARG for any other value (the setting is unchanged).
+ */
+typedef enum {
+  PA_DECODE_KERNEL_AUTO = 0,
+  PA_DECODE_KERNEL_CUDA_CORES = 1
+} pa_decode_kernel;
+PA_API pa_status pa_set_decode_kernel(int32_t kernel);
+
+/*
  * pa_decode_noalloc -- pa_decode for callers that cannot allocate device
  * memory.  The pages have no counterpart to this call; it exists for the
  * library's users.

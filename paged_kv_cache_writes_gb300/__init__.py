@@ -9,6 +9,7 @@ importing the binding works but every call raises.
 """
 from __future__ import annotations
 
+import contextlib
 import ctypes
 import os
 
@@ -18,7 +19,7 @@ __all__ = [
     "PA_F16", "PA_BF16", "PA_FP8_E4M3", "PA_F32", "PaError", "PaKvCache", "lib", "kv_cache_desc",
     "pa_reshape_and_cache", "pa_copy_blocks", "pa_decode_workspace_bytes", "pa_decode",
     "pa_prefill_chunk", "pa_get_device_error", "pa_status_string", "pa_selftest_wait_timeout",
-    "BlockManager", "PaBmStats",
+    "BlockManager", "PaBmStats", "pa_set_decode_kernel", "decode_kernel", "DECODE_KERNELS",
 ]
 
 PA_F16, PA_BF16, PA_FP8_E4M3, PA_F32 = 0, 1, 2, 3
@@ -70,6 +71,7 @@ def lib() -> ctypes.CDLL:
         L.pa_prefill_chunk.argtypes = [P, ctypes.c_int, P, P, I32, I32, I32, P, P, ctypes.POINTER(PaKvCache), P,
                                        I32, P, I32, F, P, ctypes.c_int, P]
         L.pa_get_device_error.argtypes = [P, ctypes.POINTER(I32)]
+        L.pa_set_decode_kernel.argtypes = [I32]
         L.pa_selftest_wait_timeout.argtypes = [P]
         L.pa_status_string.argtypes = [ctypes.c_int]
         L.pa_status_string.restype = ctypes.c_char_p
@@ -83,7 +85,7 @@ def lib() -> ctypes.CDLL:
         L.pa_bm_free.argtypes = [VP, I32]
         L.pa_bm_block_table.argtypes = [VP, I32, P, I32, ctypes.POINTER(I32), ctypes.POINTER(I32)]
         L.pa_bm_get_stats.argtypes = [VP, ctypes.POINTER(PaBmStats)]
-        for name in ("pa_reshape_and_cache", "pa_copy_blocks", "pa_decode", "pa_prefill_chunk",
+        for name in ("pa_reshape_and_cache", "pa_copy_blocks", "pa_decode", "pa_prefill_chunk", "pa_set_decode_kernel",
                      "pa_get_device_error", "pa_selftest_wait_timeout", "pa_bm_create", "pa_bm_new_sequence",
                      "pa_bm_fork", "pa_bm_append", "pa_bm_free", "pa_bm_block_table", "pa_bm_get_stats"):
             getattr(L, name).restype = ctypes.c_int
@@ -201,6 +203,25 @@ def pa_get_device_error(stream=None) -> int:
 def pa_selftest_wait_timeout(stream=None) -> None:
     """Enqueue one warp whose bounded wait expires (records PA_ERR_TIMEOUT, then returns)."""
     _ok(lib().pa_selftest_wait_timeout(_stream(stream)), "pa_selftest_wait_timeout")
+
+
+DECODE_KERNELS = {"auto": 0, "cuda_cores": 1}
+
+
+def pa_set_decode_kernel(kernel: str) -> None:
+    """Process-wide choice of decode kernel: "auto" (tensor cores where they
+    apply) or "cuda_cores"."""
+    _ok(lib().pa_set_decode_kernel(DECODE_KERNELS[kernel]), "pa_set_decode_kernel")
+
+
+@contextlib.contextmanager
+def decode_kernel(kernel: str):
+    """Use one decode kernel inside the block, then return to "auto"."""
+    pa_set_decode_kernel(kernel)
+    try:
+        yield
+    finally:
+        pa_set_decode_kernel("auto")
 
 
 def pa_status_string(status: int) -> str:

@@ -11,6 +11,7 @@
 
 #include "pa_common.cuh"
 #include "pa_decode.cuh"
+#include "pa_decode_tc.cuh"
 #include "pa_internal.h"
 #include "pa_prefill_tc.cuh"
 
@@ -91,9 +92,10 @@ PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
 // One pool as a 2D tensor [num_blocks*Hkv*bs rows][head_dim]; box = 16 rows x
 // one 128-byte (or 64-byte) panel, swizzled to match the kernels' reads.  With
 // `panels3d` and 256-byte rows the pool is viewed as [2 panels][rows][64] and
-// one box covers 16 rows of both panels (same shared-memory layout as two
-// 2D boxes).
-bool encode_pool_map(CUtensorMap *map, const void *base, const pa_kv_cache &c, bool panels3d = false) {
+// one box covers box_rows rows of both panels (same shared-memory layout as
+// two 2D boxes: the first panel's rows, then the second's).
+bool encode_pool_map(CUtensorMap *map, const void *base, const pa_kv_cache &c, bool panels3d = false,
+                     int box_rows = 16) {
   auto enc = tensor_map_encoder();
   if (!enc) return false;
   const int eb = dtype_bytes(c.kv_dtype);
@@ -112,7 +114,7 @@ bool encode_pool_map(CUtensorMap *map, const void *base, const pa_kv_cache &c, b
   if (panels3d && row_bytes == 2 * panel_bytes) {
     const cuuint64_t dims3[3] = {(cuuint64_t)(panel_bytes / eb), dims[1], 2};
     const cuuint64_t strides3[2] = {(cuuint64_t)row_bytes, (cuuint64_t)panel_bytes};
-    const cuuint32_t box3[3] = {(cuuint32_t)(panel_bytes / eb), 16u, 2u};
+    const cuuint32_t box3[3] = {(cuuint32_t)(panel_bytes / eb), (cuuint32_t)box_rows, 2u};
     const cuuint32_t estr3[3] = {1u, 1u, 1u};
     return enc(map, dt, 3, const_cast<void *>(base), dims3, strides3, box3, estr3,
                CU_TENSOR_MAP_INTERLEAVE_NONE, sw, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
@@ -147,6 +149,8 @@ WorkspaceLayout decode_workspace_layout(int64_t rows, int64_t num_q_heads, int64
 }
 
 namespace {
+std::atomic<int32_t> g_decode_kernel{PA_DECODE_KERNEL_AUTO};  // pa_set_decode_kernel
+
 int effective_partition(int32_t requested) {
   const int ps = requested ? requested : kDefaultPartition;
   return ps < kDefaultPartition ? ps : kDefaultPartition;  // a unit spans at most 32 blocks
@@ -210,6 +214,12 @@ size_t pa_decode_workspace_bytes(int32_t num_seqs, int32_t num_q_heads, int32_t 
   return decode_workspace_layout(num_seqs, num_q_heads, head_dim, parts).total;
 }
 
+pa_status pa_set_decode_kernel(int32_t kernel) {
+  if (kernel != PA_DECODE_KERNEL_AUTO && kernel != PA_DECODE_KERNEL_CUDA_CORES) return PA_ERR_INVALID_ARG;
+  g_decode_kernel.store(kernel, std::memory_order_relaxed);
+  return PA_OK;
+}
+
 pa_status pa_decode(const void *q, pa_dtype q_dtype, int32_t num_seqs, int32_t num_q_heads,
                     const void *k_cache, const void *v_cache, const pa_kv_cache *cache,
                     const int32_t *block_tables, int32_t max_blocks_per_seq,
@@ -235,7 +245,10 @@ pa_status pa_decode(const void *q, pa_dtype q_dtype, int32_t num_seqs, int32_t n
   const int64_t parts64 = std::max<int64_t>(1, ((int64_t)max_seq_len + ps - 1) / ps);
   if (parts64 > kMaxPartitions) return PA_ERR_UNSUPPORTED;
   const int parts = (int)parts64;
-  const int hpc = heads_per_cta(num_q_heads / c.num_kv_heads);
+  const int gqa = num_q_heads / c.num_kv_heads;
+  const bool use_tc = g_decode_kernel.load(std::memory_order_relaxed) == PA_DECODE_KERNEL_AUTO &&
+                      decode_tc_supported(c.head_dim, gqa);
+  const int hpc = use_tc ? gqa : heads_per_cta(gqa);   // query heads per work unit
   if ((double)num_seqs * parts * num_q_heads / hpc >= 2147483647.0) return PA_ERR_UNSUPPORTED;
   const WorkspaceLayout w = decode_workspace_layout(num_seqs, num_q_heads, c.head_dim, parts);
   if (!workspace || !aligned(workspace, 256) || workspace_bytes < w.total) return PA_ERR_INVALID_ARG;
@@ -250,7 +263,7 @@ pa_status pa_decode(const void *q, pa_dtype q_dtype, int32_t num_seqs, int32_t n
   p.num_seqs = num_seqs;
   p.num_q_heads = num_q_heads;
   p.num_kv_heads = c.num_kv_heads;
-  p.groups = (num_q_heads / c.num_kv_heads) / hpc;
+  p.groups = gqa / hpc;
   p.block_size = c.block_size;
   p.num_blocks = c.num_blocks;
   p.partition_size = ps;
@@ -267,11 +280,28 @@ pa_status pa_decode(const void *q, pa_dtype q_dtype, int32_t num_seqs, int32_t n
   p.tile_shift = c.block_size == 32 ? 1 : 0;
   p.kv_rows = c.num_kv_heads * c.block_size;
   p.err = device_error_word();
-  PoolMaps maps;
-  if (!p.err || !encode_pool_map(&maps.k, k_cache, c, true) || !encode_pool_map(&maps.v, v_cache, c, true))
-    return PA_ERR_CUDA;
+  if (!p.err) return PA_ERR_CUDA;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   cudaError_t e;
+  if (use_tc) {
+    DecodeTcParams tp{};
+    tp.d = p;
+    tp.k_cache = k_cache;
+    tp.v_cache = v_cache;
+    tp.s_mult = p.q_mult;
+    PoolMaps maps{};
+    if (c.kv_dtype != PA_FP8_E4M3 &&
+        (!encode_pool_map(&maps.k, k_cache, c, true, 8) || !encode_pool_map(&maps.v, v_cache, c, true, 8)))
+      return PA_ERR_CUDA;
+    if (c.kv_dtype == PA_BF16) e = launch_decode_tc_bf16(tp, gqa, maps, s);
+    else if (c.kv_dtype == PA_F16) e = launch_decode_tc_f16(tp, gqa, maps, s);
+    else if (q_dtype == PA_BF16) e = launch_decode_tc_fp8_bf16q(tp, gqa, maps, s);
+    else e = launch_decode_tc_fp8_f16q(tp, gqa, maps, s);
+    return e == cudaSuccess ? PA_OK : PA_ERR_CUDA;
+  }
+  PoolMaps maps;
+  if (!encode_pool_map(&maps.k, k_cache, c, true) || !encode_pool_map(&maps.v, v_cache, c, true))
+    return PA_ERR_CUDA;
   if (c.kv_dtype == PA_BF16) e = launch_decode_bf16(p, hpc, maps, c.head_dim, s);
   else if (c.kv_dtype == PA_F16) e = launch_decode_f16(p, hpc, maps, c.head_dim, s);
   else if (q_dtype == PA_BF16) e = launch_decode_fp8_bf16q(p, hpc, maps, c.head_dim, s);

@@ -1,0 +1,982 @@
+// pa_decode_tc.cuh -- paged decode for grouped-query attention on the
+// 5th-generation tensor cores (tcgen05.mma, accumulators in tensor memory),
+// head_dim 128, G = 4, 8 or 16 query heads per KV head.
+//
+// What it computes: the same as the CUDA-core decode (pa_decode.cuh).  For
+// each sequence and query head h,
+//   out[row][h] = sum_p softmax_p(scale * q[row][h] . K[p][g]) V[p][g],
+// g the KV head of h, K/V gathered through the block table ("Inside vLLM
+// Architecture", sections "Architectural Anatomy: PagedAttention Virtual
+// Memory Paging" and "CUDA Shared Memory Optimization in PagedAttention").
+// A row is cut into partitions of at most 512 tokens whose partial results
+// are merged by their log-sum-exp, as in the CUDA-core kernel, by a warp of
+// the CTA whose softmax warps wrote the row's last partition.  The merge and
+// the counting of finished partitions stay off the softmax warps' path: they
+// are one stage of the CTA's pipeline, and waiting there on dependent global
+// reads stalled every other stage (measured: merging inline took more than
+// half of their time).
+//
+// Why tensor cores.  The G query heads of a KV head all read every K and V
+// element: G multiply-adds per K element and G per V element.  With a bf16
+// cache and G = 8 that is 4 fp32 FMAs per byte of cache, about 27 T FMA/s at
+// the GPU's copy bandwidth, two thirds of the CUDA cores' fp32 rate before any
+// conversion or softmax work (measured: the CUDA-core kernel takes the same
+// time on an fp8 cache as on a bf16 one, so it is not bound by memory).  Per
+// (sequence, KV head) the work is a dense [G x 128] x [128 x keys] product
+// and its [G x keys] x [keys x 128] partner: the contraction of prefill with
+// G query rows.
+//
+// Transposed tiles.  With only G query rows the keys take the MMA's M side:
+//   S^T (128 keys x 16)  = K_tile (128 x 128, K-major) . Q^T (K-major: the q rows)
+//   O^T (128 d x N_O)   += V_tile^T (MN-major view of the tile as stored) . P^T
+// S^T lands in tensor memory with lane = key, column = head; O^T with lane =
+// head element d, column = head.  Q rows G..15 are zero.  P^T is staged in
+// shared memory (K-major, lane = key writes its column): columns 0..G-1 hold
+// p (its bf16 hi part for a bf16 cache) and, for a bf16 cache, columns
+// G..2G-1 hold the lo part p - hi, so one MMA per 16 keys accumulates both
+// and the epilogue adds the two halves of O^T.
+//
+// Softmax per unit (no online rescale): all tiles of a unit (<= 4 x 128
+// keys) are scored first, the exact maximum per head over the unit comes from
+// a warp reduction and one exchange between the four softmax warps (an
+// mbarrier, bounded), then p = 2^(t - max) for every key.  The exchange also
+// carries the previous unit's row sums, which its epilogue needs.
+//
+// Work: a unit is (row, partition, KV head), listed by a plan kernel (rows
+// with the most partitions first, each row's partitions together) and
+// claimed from an atomic cursor by a persistent CTA per SM.  Roles:
+//  * warps 0-3, softmax and epilogue: thread i owns tensor-memory lane i (key
+//    i of a score tile, element d = i of an output row);
+//  * loaders (one warp for a 16-bit cache, four for fp8): stage Q (cp.async)
+//    and stream the unit's K tiles,
+//    then the previous unit's V tiles, through a ring of 32 KB tiles in the
+//    MMA's 128-byte-swizzled layout (16-byte cp.async with zero fill past the
+//    sequence end for 16-bit caches; register loads widened exactly to the
+//    query's type for fp8);
+//  * MMA warp (one elected lane issues): S^T of unit u, then O^T of unit
+//    u-1, whose softmax ran while the scores of u were computed;
+//  * scheduler warp: claims units two at a time and publishes each, with
+//    the block ids of its tiles, in a ring of eight descriptors, so the chain
+//    of dependent reads behind a claim (cursor, work item, sequence length,
+//    block table) runs ahead of the loads instead of between them;
+//  * merge warp: merges split rows queued by the softmax warps.
+//
+// Every mbarrier wait is bounded (PA_ERR_TIMEOUT, after which the CTA
+// abandons its work); tensor memory is freed only after every issued MMA has
+// completed.
+#pragma once
+
+#include <type_traits>
+
+#include "pa_decode.cuh"
+#include "pa_internal.h"
+#include "pa_tcgen05.cuh"
+
+namespace pa {
+
+struct DecodeTcParams {
+  DecodeParams d;            // shapes, plan and workspace (d.groups = 1: a unit serves all G heads)
+  const void *k_cache;       // [num_blocks][Hkv][block_size][128]
+  const void *v_cache;
+  float s_mult;              // scale * log2(e) (* k_scale for an fp8 cache); any sign
+};
+
+namespace dtc {
+
+constexpr int kD = 128;                   // head_dim
+constexpr int kKeys = 128;                // keys per tile (MMA M, tensor-memory lanes)
+constexpr int kMaxTiles = 4;              // tiles per unit: partitions hold <= 512 tokens
+// A K or V tile in shared memory: 16 atoms of 8 keys, atom a at a * 2048,
+// its first 64 elements (128-byte rows, 128-byte swizzle) at +0 and the last
+// 64 at +1024 -- the layout of one 3D bulk-tensor box {64, 8 rows, 2 panels}.
+constexpr int kTileBytes = kKeys * kD * 2;
+constexpr int kNS = 16;                   // S^T columns per tile (MMA N; heads padded to 16)
+constexpr int kQBytes = 2 * kNS * 128;    // Q^T operand: 2 panels x 16 rows x 128 B
+constexpr int kInfo = 8;                  // unit descriptors in flight
+constexpr int kAtomBytes = 2048;          // 8 keys x 256 B: the two 128-byte panels of 8 rows
+
+// Warp roles: 0-3 softmax, then the loaders (one warp issuing bulk-tensor
+// copies for a 16-bit cache; four widening fp8 codes), the MMA warp, the
+// scheduler warp, the merge warp.
+template <bool kFp8>
+struct Roles {
+  static constexpr int kLoadWarps = kFp8 ? 4 : 1;
+  static constexpr int kLoadWarp0 = 4;
+  static constexpr int kMmaWarp = kLoadWarp0 + kLoadWarps;
+  static constexpr int kSchedWarp = kMmaWarp + 1;
+  static constexpr int kMergeWarp = kSchedWarp + 1;
+  static constexpr int kThreads = (kMergeWarp + 1) * 32;
+};
+constexpr int kJobs = 32;                 // merge jobs queued
+
+// A split row's (sequence, KV head) whose partitions are all written; row -1 ends the queue.
+struct MergeJob {
+  int32_t row, kvh, nparts, pad;
+};
+constexpr int kMaxSlots = 8;
+
+// A claimed unit as published by the scheduler warp: its place, and the
+// block id of each 16-key run of its tiles (run r of tile j at blk[8*j + r];
+// -1 past the end of the unit).
+struct TcUnit {
+  int32_t valid, row, kvh, part, tok_begin, ntok, nparts, pad;
+  int32_t blk[kMaxTiles * 8];
+};
+
+template <int G, bool kSplit>
+struct TcGeo {
+  static_assert(G == 4 || G == 8 || G == 16, "4, 8 or 16 query heads per KV head");
+  static constexpr int kPRows = kSplit ? 2 * G : G;         // P^T columns in use
+  static constexpr int kNO = kPRows <= 16 ? 16 : 32;        // O^T columns (MMA N)
+  static constexpr int kPBytes = 2 * kNO * 128;             // P^T of a tile: 2 panels (64 keys) x kNO rows
+  static constexpr int kColO = 2 * kMaxTiles * kNS;         // tensor-memory column of O^T, buffer 0
+  static constexpr int kTmemCols = 256;                     // 128 S^T + 2 * kNO O^T columns, rounded up
+  static constexpr int kNumBars = 2 * kMaxSlots + 8 * 2 + 2 * kInfo + kJobs + 1;
+  static constexpr int kOffQ = 0;                                        // [2] Q^T
+  static constexpr int kOffP = kOffQ + 2 * kQBytes;                      // [2][4] P^T
+  static constexpr int kOffRed = kOffP + 2 * kMaxTiles * kPBytes;        // float [2][4 warps][2][16]
+  static constexpr int kOffInfo = kOffRed + 2 * 4 * 2 * 16 * 4;          // TcUnit [kInfo] (16-byte aligned)
+  static constexpr int kOffJobs = kOffInfo + kInfo * (int)sizeof(TcUnit);   // MergeJob [kJobs]
+  static constexpr int kOffBar = kOffJobs + kJobs * (int)sizeof(MergeJob);
+  static constexpr int kOffMisc = kOffBar + kNumBars * 8;
+  static constexpr int kOffRing = (kOffMisc + 64 + 1023) / 1024 * 1024;  // [kSlots] K/V tiles
+  static constexpr int kSlots0 = (227 * 1024 - 1024 - kOffRing) / kTileBytes;
+  static constexpr int kSlots = kSlots0 > kMaxSlots ? kMaxSlots : kSlots0;
+  static constexpr int kSmemBytes = kOffRing + kSlots * kTileBytes + 1024;  // + alignment slack
+  static_assert(kSlots >= 2 && kSmemBytes <= 227 * 1024, "shared memory");
+};
+
+// N consecutive fp32 columns of this thread's tensor-memory lane (warp-collective).
+template <int N>
+__device__ __forceinline__ void tmem_ld_cols(uint32_t taddr, float (&v)[N]) {
+  if constexpr (N == 4) {
+    uint32_t r[4];
+    asm volatile("tcgen05.ld.sync.aligned.32x32b.x4.b32 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+                 : "r"(taddr));
+    asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+#pragma unroll
+    for (int i = 0; i < 4; ++i) v[i] = __uint_as_float(r[i]);
+  } else if constexpr (N == 8) {
+    uint32_t r[8];
+    asm volatile("tcgen05.ld.sync.aligned.32x32b.x8.b32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];"
+                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+                   "=r"(r[7])
+                 : "r"(taddr));
+    asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+#pragma unroll
+    for (int i = 0; i < 8; ++i) v[i] = __uint_as_float(r[i]);
+  } else if constexpr (N == 16) {
+    tc::tmem_ld16(taddr, v);
+  } else {
+    static_assert(N == 32, "4, 8, 16 or 32 columns");
+    tc::tmem_ld32(taddr, v);
+  }
+}
+
+// Reduce v[h] (h < G) over the 32 lanes of the warp by halving exchanges:
+// each level swaps half of the remaining heads with the partner lane.  The
+// lane ends with the reduction of head lane >> (5 - log2 G).
+template <int G, bool kMax>
+__device__ __forceinline__ float warp_reduce_heads(float (&v)[G], int lane) {
+  constexpr int kLog = G == 4 ? 2 : G == 8 ? 3 : 4;
+#pragma unroll
+  for (int lv = 0; lv < kLog; ++lv) {
+    const int n = G >> lv, mask = 16 >> lv;
+    const bool upper = (lane & mask) != 0;
+#pragma unroll
+    for (int k = 0; k < n / 2; ++k) {
+      const float send = upper ? v[k] : v[k + n / 2];
+      const float keep = upper ? v[k + n / 2] : v[k];
+      const float got = __shfl_xor_sync(0xffffffffu, send, mask);
+      v[k] = kMax ? fmaxf(keep, got) : keep + got;
+    }
+  }
+#pragma unroll
+  for (int mask = 16 >> kLog; mask > 0; mask >>= 1) {
+    const float got = __shfl_xor_sync(0xffffffffu, v[0], mask);
+    v[0] = kMax ? fmaxf(v[0], got) : v[0] + got;
+  }
+  return v[0];
+}
+
+// The descriptor's header, copied to registers (the block ids stay in shared memory).
+struct UnitHdr {
+  int32_t valid, row, kvh, part, tok_begin, ntok, nparts, pad;
+};
+__device__ __forceinline__ UnitHdr read_unit(const TcUnit *u) {
+  const volatile int32_t *s = reinterpret_cast<const volatile int32_t *>(u);
+  UnitHdr r;
+  r.valid = s[0];
+  r.row = s[1];
+  r.kvh = s[2];
+  r.part = s[3];
+  r.tok_begin = s[4];
+  r.ntok = s[5];
+  r.nparts = s[6];
+  r.pad = 0;
+  return r;
+}
+
+__device__ __forceinline__ int num_tiles(const UnitHdr &u) { return u.valid ? (u.ntok + kKeys - 1) / kKeys : 0; }
+
+}  // namespace dtc
+
+template <typename KV, typename QT, int G>
+__global__ void __launch_bounds__(dtc::Roles<std::is_same<KV, uint8_t>::value>::kThreads, 1)
+    decode_tc_kernel(const DecodeTcParams tp, const __grid_constant__ CUtensorMap tmap_k,
+                     const __grid_constant__ CUtensorMap tmap_v) {
+  using namespace tc;
+  using namespace dtc;
+  constexpr bool kFp8 = std::is_same<KV, uint8_t>::value;
+  using RO = Roles<kFp8>;
+  constexpr int kLoadWarp0 = RO::kLoadWarp0, kLoadWarps = RO::kLoadWarps, kMmaWarp = RO::kMmaWarp;
+  constexpr int kSchedWarp = RO::kSchedWarp, kMergeWarp = RO::kMergeWarp, kThreads = RO::kThreads;
+  constexpr int kLoaders = 32 * kLoadWarps;
+  constexpr bool kBf16 = std::is_same<QT, __nv_bfloat16>::value;
+  constexpr bool kSplit = kBf16 && !kFp8;   // bf16 cache: P as hi + lo
+  using GE = TcGeo<G, kSplit>;
+  constexpr int S = GE::kSlots, kNO = GE::kNO;
+  constexpr uint32_t kAB = kBf16 ? 1u : 0u;
+  const DecodeParams &p = tp.d;
+  const float kNegInf = -__int_as_float(0x7f800000);
+
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                              ~uintptr_t(1023));
+  uint64_t *bars = reinterpret_cast<uint64_t *>(smem + GE::kOffBar);
+  uint64_t *slot_full = bars;                 // [S] tile staged
+  uint64_t *slot_free = bars + kMaxSlots;     // [S] the MMAs reading the tile are complete
+  uint64_t *q_full = bars + 2 * kMaxSlots;    // [2] Q^T of unit buffer b staged (every loader thread)
+  uint64_t *q_free = q_full + 2;              // [2] its S^T MMAs are complete
+  uint64_t *s_full = q_free + 2;              // [2] S^T of every tile of the unit ready
+  uint64_t *s_free = s_full + 2;              // [2] read by every softmax thread (128)
+  uint64_t *p_full = s_free + 2;              // [2] P^T written (128)
+  uint64_t *o_full = p_full + 2;              // [2] O^T complete
+  uint64_t *o_free = o_full + 2;              // [2] O^T read by every softmax thread (128)
+  uint64_t *red_bar = o_free + 2;             // [2] per-warp maxima and sums exchanged (128)
+  uint64_t *info_full = red_bar + 2;          // [kInfo] unit descriptor published
+  uint64_t *info_free = info_full + kInfo;    // [kInfo] released by the MMA warp and the softmax warps
+  uint64_t *job_full = info_free + kInfo;     // [kJobs] merge job queued
+  uint64_t *fin = job_full + kJobs;           // every MMA of the CTA complete
+  MergeJob *jobs = reinterpret_cast<MergeJob *>(smem + GE::kOffJobs);
+  TcUnit *info = reinterpret_cast<TcUnit *>(smem + GE::kOffInfo);
+  float *red = reinterpret_cast<float *>(smem + GE::kOffRed);
+  uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + GE::kOffMisc);
+  volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + GE::kOffMisc + 8);
+  int *job_ticket = reinterpret_cast<int *>(smem + GE::kOffMisc + 16);      // next merge job's queue position
+  int *softmax_done = reinterpret_cast<int *>(smem + GE::kOffMisc + 20);    // softmax warps finished
+  volatile int *jobs_taken = reinterpret_cast<volatile int *>(smem + GE::kOffMisc + 24);  // read by the merge warp
+
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+
+  // Q^T and P^T buffers start zeroed: their padding rows are never written
+  for (int i = tid; i < (GE::kOffRed - GE::kOffQ) / 16; i += kThreads)
+    reinterpret_cast<uint4 *>(smem + GE::kOffQ)[i] = make_uint4(0, 0, 0, 0);
+  if (tid == 0) {
+    for (int s = 0; s < S; ++s) {
+      mbar_init(&slot_full[s], kFp8 ? kLoaders : 1);   // fp8: every loader thread; else one expect-tx arrival
+      mbar_init(&slot_free[s], 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(&q_full[b], kLoaders);
+      mbar_init(&q_free[b], 1);
+      mbar_init(&s_full[b], 1);
+      mbar_init(&s_free[b], 128);
+      mbar_init(&p_full[b], 128);
+      mbar_init(&o_full[b], 1);
+      mbar_init(&o_free[b], 128);
+      mbar_init(&red_bar[b], 128);
+    }
+    for (int i = 0; i < kInfo; ++i) {
+      mbar_init(&info_full[i], 1);
+      mbar_init(&info_free[i], 2);
+    }
+    for (int i = 0; i < kJobs; ++i) mbar_init(&job_full[i], 1);
+    mbar_init(fin, 1);
+    *abort_flag = 0;
+    *job_ticket = 0;
+    *softmax_done = 0;
+    *jobs_taken = 0;
+    fence_mbar_init();
+    if constexpr (!kFp8) {
+      prefetch_tensor_map(&tmap_k);
+      prefetch_tensor_map(&tmap_v);
+    }
+  }
+  if (warp == kMmaWarp) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(tmem_slot)),
+                 "n"(GE::kTmemCols));
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;");
+  }
+  fence_async_smem();   // the zeroed operand rows, for the MMAs' reads
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+  auto col_s = [&](int b, int j) { return tmem + (uint32_t)((b * kMaxTiles + j) * kNS); };
+  auto col_o = [&](int b) { return tmem + (uint32_t)(GE::kColO + b * kNO); };
+  auto wait_all = [&](uint64_t *bar, uint32_t parity) {
+    return __all_sync(0xffffffffu, wait_or_abort(bar, parity, p.err, abort_flag));
+  };
+
+  const int hkv = p.num_kv_heads;
+  const int hq = p.num_q_heads;
+
+  if (warp < kLoadWarp0) {
+    // ===================================================== softmax and epilogue (warps 0-3)
+    const uint32_t lane_base = (uint32_t)(warp * 32) << 16;
+    const float c = tp.s_mult;
+    constexpr int kLog = G == 4 ? 2 : G == 8 ? 3 : 4;
+    const int my_head = lane >> (5 - kLog);
+    const bool red_writer = (lane & ((1 << (5 - kLog)) - 1)) == 0;
+    float l_part[G], m_prev[G];
+#pragma unroll
+    for (int h = 0; h < G; ++h) {
+      l_part[h] = 0.f;
+      m_prev[h] = kNegInf;
+    }
+    UnitHdr prev;
+    prev.valid = 0;
+    bool ok = true;
+    // Completion of split units, per warp.  A unit's partial results are written
+    // in one epilogue (pending), reported in the next (fence, then one count per
+    // warp on the row's counter: by then the fence finds the writes done), and
+    // the count returned is checked in the one after (reported); the warp that
+    // brings a row's count to 4 * nparts queues the row for the merge warp.
+    int pend_row = -1, pend_kvh = 0, pend_np = 0;
+    int rep_row = -1, rep_kvh = 0, rep_np = 0, rep_old = 0;
+    // queue a merge job (one thread): its slot is free once the merge warp has
+    // read job t - kJobs (bounded wait)
+    auto queue_job = [&](int row, int kvh, int np) {
+      const int t = atomicAdd(job_ticket, 1);
+      if (*jobs_taken <= t - kJobs) {
+        const uint64_t t0 = global_timer_ns();
+        while (*jobs_taken <= t - kJobs) {
+          if (*abort_flag) return;
+          if (global_timer_ns() - t0 > kWaitLimitNs) {
+            record_error(p.err, PA_ERR_TIMEOUT);
+            *abort_flag = 1;
+            return;
+          }
+        }
+      }
+      MergeJob *j = &jobs[t % kJobs];
+      j->row = row;
+      j->kvh = kvh;
+      j->nparts = np;
+      mbar_arrive(&job_full[t % kJobs]);
+    };
+    auto check_reported = [&]() {
+      if (rep_row >= 0) {
+        const int last = __shfl_sync(0xffffffffu, rep_old, 0) == 4 * rep_np - 1;
+        if (last && lane == 0) {
+          __threadfence();   // the other partitions' results, observed through the counter
+          queue_job(rep_row, rep_kvh, rep_np);
+        }
+        rep_row = -1;
+      }
+    };
+    auto report_pending = [&]() {
+      if (pend_row >= 0) {
+        __threadfence();
+        __syncwarp();
+        if (lane == 0)
+          rep_old = atomicAdd(p.ws_count + (int64_t)pend_row * hq + (int64_t)pend_kvh * G, 1);
+        rep_row = pend_row;
+        rep_kvh = pend_kvh;
+        rep_np = pend_np;
+        pend_row = -1;
+      }
+    };
+    for (int u = 0; ok; ++u) {
+      const int ib = u % kInfo, b = u & 1;
+      ok = wait_all(&info_full[ib], (u / kInfo) & 1);
+      if (!ok) break;
+      const UnitHdr cur = read_unit(&info[ib]);
+      const int nt = num_tiles(cur);
+      // scores of this unit in log2 units, t = s * scale * log2(e); masked keys -inf
+      float t[kMaxTiles][G];
+      float mloc[G];
+#pragma unroll
+      for (int h = 0; h < G; ++h) mloc[h] = kNegInf;
+      if (cur.valid) {
+        ok = wait_all(&s_full[b], (u >> 1) & 1);
+        if (!ok) break;
+        tc_fence_after();
+#pragma unroll
+        for (int j = 0; j < kMaxTiles; ++j) {
+          if (j < nt) {
+            float raw[G];
+            tmem_ld_cols<G>(col_s(b, j) + lane_base, raw);
+            const bool kv = j * kKeys + tid < cur.ntok;
+#pragma unroll
+            for (int h = 0; h < G; ++h) {
+              t[j][h] = kv ? raw[h] * c : kNegInf;
+              mloc[h] = fmaxf(mloc[h], t[j][h]);
+            }
+          } else {
+#pragma unroll
+            for (int h = 0; h < G; ++h) t[j][h] = kNegInf;
+          }
+        }
+        tc_fence_before();
+        mbar_arrive(&s_free[b]);
+      }
+      // exchange: this unit's per-warp maxima and the previous unit's per-warp sums
+      {
+        const float wm = warp_reduce_heads<G, true>(mloc, lane);
+        const float ws = warp_reduce_heads<G, false>(l_part, lane);
+        float *rb = red + (b * 4 + warp) * 32;
+        if (red_writer) {
+          rb[my_head] = wm;
+          rb[16 + my_head] = ws;
+        }
+        mbar_arrive(&red_bar[b]);
+        ok = wait_all(&red_bar[b], (u >> 1) & 1);
+        if (!ok) break;
+      }
+      float m_cur[G], l_prev[G];
+#pragma unroll
+      for (int h = 0; h < G; ++h) {
+        const float *r0 = red + (b * 4) * 32;
+        m_cur[h] = fmaxf(fmaxf(r0[h], r0[32 + h]), fmaxf(r0[64 + h], r0[96 + h]));
+        l_prev[h] = (r0[16 + h] + r0[48 + h]) + (r0[80 + h] + r0[112 + h]);
+      }
+      // P^T of this unit (its buffer's previous reader, P.V of unit u-2, finished
+      // before the epilogue of u-2, which ran in the previous iteration)
+      if (cur.valid) {
+#pragma unroll
+        for (int h = 0; h < G; ++h) l_part[h] = 0.f;
+        uint8_t *pb = smem + GE::kOffP + b * kMaxTiles * GE::kPBytes + (tid >> 6) * (kNO * 128) + (tid & 7) * 2;
+        const int ck = (tid & 63) >> 3;
+#pragma unroll
+        for (int j = 0; j < kMaxTiles; ++j) {
+          if (j >= nt) break;
+          uint8_t *pt = pb + j * GE::kPBytes;
+#pragma unroll
+          for (int h = 0; h < G; ++h) {
+            const float msub = m_cur[h] == kNegInf ? 0.f : m_cur[h];
+            const float pv = fast_exp2(t[j][h] - msub);
+            if constexpr (kSplit) {
+              // hi = p truncated to bf16, lo = (p - hi) truncated; hi + lo is within 2^-15 of p
+              const uint32_t hi = __float_as_uint(pv) & 0xffff0000u;
+              const float lo = pv - __uint_as_float(hi);
+              *reinterpret_cast<uint16_t *>(pt + h * 128 + ((ck ^ (h & 7)) << 4)) = (uint16_t)(hi >> 16);
+              *reinterpret_cast<uint16_t *>(pt + (G + h) * 128 + ((ck ^ ((G + h) & 7)) << 4)) =
+                  (uint16_t)(__float_as_uint(lo) >> 16);
+              l_part[h] += pv;
+            } else if constexpr (kBf16) {
+              const uint32_t r = bf16_round_bits(pv);
+              *reinterpret_cast<uint16_t *>(pt + h * 128 + ((ck ^ (h & 7)) << 4)) = (uint16_t)(r >> 16);
+              l_part[h] += __uint_as_float(r);   // the rounded p the MMA uses
+            } else {
+              const __half hv = __float2half_rn(pv);
+              *reinterpret_cast<__half *>(pt + h * 128 + ((ck ^ (h & 7)) << 4)) = hv;
+              l_part[h] += __half2float(hv);
+            }
+          }
+        }
+        fence_async_smem();
+        mbar_arrive(&p_full[b]);
+      }
+      // epilogue of the previous unit
+      if (prev.valid) {
+        const int bp = (u - 1) & 1;
+        ok = wait_all(&o_full[bp], ((u - 1) >> 1) & 1);
+        if (!ok) break;
+        tc_fence_after();
+        float o[kNO];
+        if (num_tiles(prev) > 0) {
+          tmem_ld_cols<kNO>(col_o(bp) + lane_base, o);
+        } else {
+#pragma unroll
+          for (int i = 0; i < kNO; ++i) o[i] = 0.f;
+        }
+        tc_fence_before();
+        mbar_arrive(&o_free[bp]);
+        const int64_t head0 = (int64_t)prev.row * hq + (int64_t)prev.kvh * G;
+        const int d = tid;
+        if (prev.nparts == 1) {
+#pragma unroll
+          for (int h = 0; h < G; ++h) {
+            const float val = kSplit ? o[h] + o[G + h] : o[h];
+            const float inv = l_prev[h] > 0.f ? p.out_mult / l_prev[h] : 0.f;
+            store_out<QT>(p.out, (head0 + h) * kD + d, p.out_f32 != 0, val * inv);
+          }
+        } else {
+#pragma unroll
+          for (int h = 0; h < G; ++h)
+            p.ws_acc[((head0 + h) * p.max_partitions + prev.part) * kD + d] = kSplit ? o[h] + o[G + h] : o[h];
+          if (tid < G) {
+            float mv = m_prev[0], lv = l_prev[0];
+#pragma unroll
+            for (int h = 1; h < G; ++h)
+              if (tid == h) {
+                mv = m_prev[h];
+                lv = l_prev[h];
+              }
+            p.ws_ml[(head0 + tid) * p.max_partitions + prev.part] = make_float2(mv, lv);
+          }
+        }
+        check_reported();
+        report_pending();
+        if (prev.nparts > 1) {
+          pend_row = prev.row;
+          pend_kvh = prev.kvh;
+          pend_np = prev.nparts;
+        }
+        if (tid == 0) mbar_arrive(&info_free[(u - 1) % kInfo]);
+      }
+      if (!cur.valid) break;
+      prev = cur;
+#pragma unroll
+      for (int h = 0; h < G; ++h) m_prev[h] = m_cur[h];
+    }
+    if (ok) {
+      check_reported();
+      report_pending();
+      check_reported();
+      // the last softmax warp to finish ends the merge queue (after every job of every warp)
+      if (lane == 0 && atomicAdd(softmax_done, 1) == kLoadWarp0 - 1) queue_job(-1, 0, 0);
+    }
+  } else if (warp < kMmaWarp) {
+    // ===================================================== loaders
+    const int lt = tid - kLoadWarp0 * 32, lw = lt >> 5;
+    constexpr int kRowBytes = kFp8 ? kD : 2 * kD;
+    const char *kpool = static_cast<const char *>(tp.k_cache);
+    const char *vpool = static_cast<const char *>(tp.v_cache);
+    const int bs = p.block_size;
+    uint32_t g_load = 0;
+    bool ok = true;
+
+    // first cache row of run r (of this warp's two) of tile j of the unit in
+    // descriptor slot ib, and how many of its 16 rows hold keys of the unit
+    auto run_rows = [&](const UnitHdr &un, int ib, int j, int r, int64_t &row0) -> int {
+      const int32_t bi = reinterpret_cast<const volatile int32_t *>(info[ib].blk)[8 * j + 2 * lw + r];
+      const int key0 = un.tok_begin + j * kKeys + 32 * lw + 16 * r;
+      row0 = ((int64_t)max(bi, 0) * hkv + un.kvh) * bs + (key0 % bs);
+      return bi < 0 ? 0 : min(16, un.tok_begin + un.ntok - key0);
+    };
+    auto acquire_slot = [&]() -> int {
+      const int slot = (int)(g_load % S);
+      if (g_load >= (uint32_t)S) ok = wait_all(&slot_free[slot], ((g_load / S) - 1) & 1);
+      return slot;
+    };
+
+    UnitHdr prev;
+    prev.valid = 0;
+    for (int u = 0; ok; ++u) {
+      const int ib = u % kInfo, ibp = (u + kInfo - 1) % kInfo, b = u & 1;
+      ok = wait_all(&info_full[ib], (u / kInfo) & 1);
+      if (!ok) break;
+      const UnitHdr cur = read_unit(&info[ib]);
+      const int ntc = num_tiles(cur), ntp = num_tiles(prev);
+      if (cur.valid) {
+        // Q^T rows: the G query heads of the KV head, 256 B each
+        if (u >= 2) {
+          ok = wait_all(&q_free[b], ((u >> 1) - 1) & 1);
+          if (!ok) break;
+        }
+#pragma unroll
+        for (int e = lt; e < G * 16; e += kLoaders) {
+          const int h = e >> 4, c16 = e & 15;
+          const char *src = static_cast<const char *>(p.q) +
+                            (((int64_t)cur.row * hq + (int64_t)cur.kvh * G + h) * kD) * 2 + c16 * 16;
+          cp_async16(smem + GE::kOffQ + b * kQBytes + (c16 >> 3) * (kNS * 128) + h * 128 +
+                         (((c16 & 7) ^ (h & 7)) << 4),
+                     src, 16u);
+        }
+        cp_async_arrive_noinc(&q_full[b]);
+      }
+      // tiles in the MMA's order: K tiles of this unit, then V tiles of the previous one
+      if constexpr (!kFp8) {
+        // one bulk-tensor box per atom of 8 keys holding keys of the unit; lane a issues atom a
+        for (int i = 0; i < ntc + ntp && ok; ++i) {
+          const bool is_k = i < ntc;
+          const UnitHdr &un = is_k ? cur : prev;
+          const int j = is_k ? i : i - ntc;
+          const int slot = acquire_slot();
+          if (!ok) break;
+          const int nvalid = min(kKeys, un.ntok - j * kKeys);
+          bool issue = false;
+          int32_t row = 0;
+          if (lane < (nvalid + 7) >> 3) {
+            const int32_t bi =
+                reinterpret_cast<const volatile int32_t *>(info[is_k ? ib : ibp].blk)[8 * j + (lane >> 1)];
+            const int key0 = un.tok_begin + j * kKeys + 8 * lane;
+            issue = bi >= 0;   // an out-of-range id was reported by the scheduler; its keys stay unread
+            row = (bi * hkv + un.kvh) * bs + key0 % bs;
+          }
+          const uint32_t boxes = __popc(__ballot_sync(0xffffffffu, issue));
+          if (lane == 0) mbar_arrive_expect_tx(&slot_full[slot], boxes * kAtomBytes);
+          __syncwarp();
+          if (issue)
+            tma_load_3d(smem + GE::kOffRing + slot * kTileBytes + lane * kAtomBytes, is_k ? &tmap_k : &tmap_v,
+                        &slot_full[slot], 0, row, 0);
+          ++g_load;
+        }
+      } else {
+        // fp8 rows (128 B): per load 4 rows x 8 words of 16 codes; the next tile's
+        // words are in flight while the current tile is widened into shared memory
+        const int q = lane & 7, pn = q >> 2, c0 = (2 * q) & 7;   // word q: elements 16q..16q+15
+        auto fetch = [&](int i, uint4 (&w)[8]) {
+          const bool is_k = i < ntc;
+          const UnitHdr &un = is_k ? cur : prev;
+          const int j = is_k ? i : i - ntc;
+          const char *pool = is_k ? kpool : vpool;
+#pragma unroll
+          for (int r = 0; r < 2; ++r) {
+            int64_t row0;
+            const int nval = run_rows(un, is_k ? ib : ibp, j, r, row0);
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+              const int rr = 4 * k + (lane >> 3);
+              w[4 * r + k] = rr < nval ? ld_nc16(pool + (row0 + rr) * kRowBytes + q * 16) : make_uint4(0, 0, 0, 0);
+            }
+          }
+        };
+        const int n = ntc + ntp;
+        uint4 wc[8], wn[8];
+        if (n > 0) fetch(0, wc);
+        for (int i = 0; i < n && ok; ++i) {
+          if (i + 1 < n) fetch(i + 1, wn);
+          const int slot = acquire_slot();
+          if (!ok) break;
+          uint8_t *tile = smem + GE::kOffRing + slot * kTileBytes + pn * 1024;
+#pragma unroll
+          for (int r = 0; r < 2; ++r) {
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+              const int row = 32 * lw + 16 * r + 4 * k + (lane >> 3);
+              uint32_t o[8];
+              widen16<QT>(wc[4 * r + k], o);
+              uint8_t *dst = tile + (row >> 3) * kAtomBytes + (row & 7) * 128;
+              *reinterpret_cast<uint4 *>(dst + ((c0 ^ (row & 7)) << 4)) = make_uint4(o[0], o[1], o[2], o[3]);
+              *reinterpret_cast<uint4 *>(dst + (((c0 + 1) ^ (row & 7)) << 4)) = make_uint4(o[4], o[5], o[6], o[7]);
+            }
+          }
+          fence_async_smem();
+          mbar_arrive(&slot_full[slot]);
+          ++g_load;
+#pragma unroll
+          for (int k = 0; k < 8; ++k) wc[k] = wn[k];
+        }
+      }
+      if (!cur.valid) break;
+      prev = cur;
+    }
+    cp_async_wait_all();
+  } else if (warp == kSchedWarp) {
+    // ===================================================== scheduler
+    // Two units per claim (one atomic step of 2), published in order; the
+    // block id of run (lane & 7) of tile (lane >> 3) is read by lane `lane`.
+    const int bs = p.block_size;
+    const int total_units = __ldcg(&p.hdr->num_items) * hkv;
+    const int64_t cap = min((int64_t)p.max_blocks_per_seq * bs, (int64_t)p.max_partitions * p.partition_size);
+    bool ok = true;
+    for (int u = 0; ok; u += 2) {
+      for (int k = 0; k < 2 && ok; ++k)
+        if (u + k >= kInfo) ok = wait_all(&info_free[(u + k) % kInfo], (((u + k) / kInfo) - 1) & 1);
+      if (!ok) break;
+      int id0 = 0;
+      if (lane == 0) id0 = atomicAdd(&p.hdr->next_unit, 2);
+      id0 = __shfl_sync(0xffffffffu, id0, 0);
+      // lane k < 2 resolves unit id0 + k
+      const int id = id0 + (lane & 1);
+      const bool valid = lane < 2 && id < total_units;
+      int item = 0, L = 0;
+      if (valid) item = __ldg(p.items + id / hkv);
+      const int row = item >> 12, part = item & 4095;
+      if (valid) {
+        L = __ldg(p.seq_lens + row);
+        if (L < 0 || L > cap) L = L < 0 ? 0 : (int)cap;   // reported by the plan kernel
+      }
+      const int tok_begin = part * p.partition_size;
+      const int ntok = valid ? max(0, min(L, tok_begin + p.partition_size) - tok_begin) : 0;
+      const int nparts = max(1, (L + p.partition_size - 1) / p.partition_size);
+      bool any_invalid = false;
+#pragma unroll
+      for (int k = 0; k < 2; ++k) {
+        const int vk = __shfl_sync(0xffffffffu, (int)valid, k);
+        const int rk = __shfl_sync(0xffffffffu, row, k);
+        const int tb = __shfl_sync(0xffffffffu, tok_begin, k);
+        const int nk = __shfl_sync(0xffffffffu, ntok, k);
+        TcUnit *dst = &info[(u + k) % kInfo];
+        const int key0 = tb + (lane >> 3) * kKeys + 16 * (lane & 7);
+        int32_t blk = -1;
+        if (vk && key0 < tb + nk) {
+          const int32_t bi = __ldg(p.block_tables + (int64_t)rk * p.max_blocks_per_seq + key0 / bs);
+          if (bi < 0 || bi >= p.num_blocks) record_error(p.err, PA_ERR_DEVICE_CHECK);
+          else blk = bi;
+        }
+        dst->blk[lane] = blk;
+        if (lane == k) {
+          dst->valid = vk;
+          dst->row = rk;
+          dst->kvh = vk ? id % hkv : 0;
+          dst->part = part;
+          dst->tok_begin = tb;
+          dst->ntok = nk;
+          dst->nparts = nparts;
+          dst->pad = 0;
+        }
+        any_invalid |= !vk;
+      }
+      __syncwarp();
+      if (lane == 0) {
+        mbar_arrive(&info_full[u % kInfo]);
+        mbar_arrive(&info_full[(u + 1) % kInfo]);
+      }
+      if (any_invalid) break;   // the ids only grow: every later claim is past the end too
+    }
+  } else if (warp == kMergeWarp) {
+    // ===================================================== merge (last warp)
+    // out = sum_p 2^(m_p - M) acc_p / sum_p 2^(m_p - M) l_p over a split row's
+    // partitions p (m_p in log2 units, M their maximum), kept as a running
+    // maximum; lane l merges elements 4l..4l+3 of all G heads, the loads of a
+    // partition for every head in flight together.
+    for (int t = 0;; ++t) {
+      if (!wait_all(&job_full[t % kJobs], (t / kJobs) & 1)) break;
+      const volatile MergeJob *jv = &jobs[t % kJobs];
+      const int job_row = jv->row, job_kvh = jv->kvh, job_np = jv->nparts;
+      __syncwarp();
+      if (lane == 0) *jobs_taken = t + 1;   // the slot may be refilled
+      if (job_row < 0) break;
+      __threadfence();
+      const int64_t head0 = (int64_t)job_row * hq + (int64_t)job_kvh * G;
+      float m[G], l[G];
+      float4 acc[G];
+#pragma unroll
+      for (int h = 0; h < G; ++h) {
+        m[h] = kNegInf;
+        l[h] = 0.f;
+        acc[h] = make_float4(0.f, 0.f, 0.f, 0.f);
+      }
+      // two partitions per step: the loads of both are in flight together
+      for (int q0 = 0; q0 < job_np; q0 += 2) {
+        float2 ml[2][G];
+        float4 a[2][G];
+#pragma unroll
+        for (int k = 0; k < 2; ++k)
+#pragma unroll
+          for (int h = 0; h < G; ++h) {
+            const int q = min(q0 + k, job_np - 1);   // a lone last partition is read twice, merged once
+            const int64_t e = (head0 + h) * p.max_partitions + q;
+            ml[k][h] = __ldcg(&p.ws_ml[e]);
+            a[k][h] = __ldcg(reinterpret_cast<const float4 *>(p.ws_acc + e * kD) + lane);
+          }
+#pragma unroll
+        for (int k = 0; k < 2; ++k) {
+          if (q0 + k >= job_np) break;
+#pragma unroll
+          for (int h = 0; h < G; ++h) {
+            const float mn = fmaxf(m[h], ml[k][h].x);
+            const float so = fast_exp2(m[h] - mn), sn = fast_exp2(ml[k][h].x - mn);
+            m[h] = mn;
+            l[h] = l[h] * so + ml[k][h].y * sn;
+            acc[h] = make_float4(acc[h].x * so + a[k][h].x * sn, acc[h].y * so + a[k][h].y * sn,
+                                 acc[h].z * so + a[k][h].z * sn, acc[h].w * so + a[k][h].w * sn);
+          }
+        }
+      }
+#pragma unroll
+      for (int h = 0; h < G; ++h) {
+        const float inv = l[h] > 0.f ? p.out_mult / l[h] : 0.f;
+        const int64_t o0 = (head0 + h) * kD + 4 * lane;
+        store_out<QT>(p.out, o0, p.out_f32 != 0, acc[h].x * inv);
+        store_out<QT>(p.out, o0 + 1, p.out_f32 != 0, acc[h].y * inv);
+        store_out<QT>(p.out, o0 + 2, p.out_f32 != 0, acc[h].z * inv);
+        store_out<QT>(p.out, o0 + 3, p.out_f32 != 0, acc[h].w * inv);
+      }
+    }
+  } else {
+    // ===================================================== MMA issue
+    // The whole warp runs the schedule (descriptors stay warp-uniform); one
+    // elected lane issues the MMAs and their commits.
+    const bool leader = elect_one();
+    const uint32_t idesc_s = umma_idesc(kAB, kNS, false, false);
+    const uint32_t idesc_o = umma_idesc(kAB, kNO, false, true);
+    const uint32_t ring = smem_u32(smem + GE::kOffRing);
+    const uint32_t qbuf = smem_u32(smem + GE::kOffQ);
+    const uint32_t pbuf = smem_u32(smem + GE::kOffP);
+    uint32_t g_cons = 0;
+    bool ok = true, issued = false;
+    UnitHdr prev;
+    prev.valid = 0;
+    for (int u = 0; ok; ++u) {
+      const int ib = u % kInfo, b = u & 1;
+      ok = wait_all(&info_full[ib], (u / kInfo) & 1);
+      if (!ok) break;
+      const UnitHdr cur = read_unit(&info[ib]);
+      if (cur.valid) {
+        // S^T(u, j) = K_j . Q^T into buffer b (its previous reader: the softmax of u-2)
+        const int nt = num_tiles(cur);
+        if (u >= 2) {
+          ok = wait_all(&s_free[b], ((u >> 1) - 1) & 1);
+          if (!ok) break;
+        }
+        ok = wait_all(&q_full[b], (u >> 1) & 1);
+        if (!ok) break;
+        for (int j = 0; j < nt; ++j) {
+          const int slot = (int)(g_cons % S);
+          ok = wait_all(&slot_full[slot], (g_cons / S) & 1);
+          if (!ok) break;
+          fence_async_smem();   // tile and Q^T written through the generic proxy
+          tc_fence_after();
+          if (leader) {
+            const uint32_t kb = ring + slot * kTileBytes, qb = qbuf + b * kQBytes;
+#pragma unroll
+            for (int k = 0; k < kD / 16; ++k)
+              umma(col_s(b, j), umma_desc_sbo(kb + (k >> 2) * 1024 + (k & 3) * 32, 16, kAtomBytes),
+                   umma_desc(qb + (k >> 2) * (kNS * 128) + (k & 3) * 32, 16), idesc_s, k > 0 ? 1u : 0u);
+            umma_commit(&slot_free[slot]);
+          }
+          __syncwarp();
+          issued = true;
+          ++g_cons;
+        }
+        if (!ok) break;
+        if (leader) {
+          umma_commit(&s_full[b]);
+          umma_commit(&q_free[b]);
+        }
+        __syncwarp();
+      }
+      if (prev.valid) {
+        // O^T(u-1) = sum_j V_j^T . P_j^T (its previous reader: the epilogue of u-3)
+        const int bp = (u - 1) & 1, nt = num_tiles(prev);
+        ok = wait_all(&p_full[bp], ((u - 1) >> 1) & 1);
+        if (!ok) break;
+        if (u - 1 >= 2) {
+          ok = wait_all(&o_free[bp], (((u - 1) >> 1) - 1) & 1);
+          if (!ok) break;
+        }
+        for (int j = 0; j < nt; ++j) {
+          const int slot = (int)(g_cons % S);
+          ok = wait_all(&slot_full[slot], (g_cons / S) & 1);
+          if (!ok) break;
+          // keys past the end of the unit take part only up to the end of their
+          // 16-key group; their rows in that group may hold stale values (a whole
+          // atom is copied, and copies of later atoms are skipped), so they are
+          // zeroed: P is 0 there, and 0 * NaN would not be
+          const int nvalid = min(kKeys, prev.ntok - j * kKeys);
+          const int ngroups = (nvalid + 15) >> 4;
+          uint8_t *vt = smem + GE::kOffRing + slot * kTileBytes;
+          if (!kFp8 && (nvalid & 15)) {
+            for (int e = lane; e < (16 * ngroups - nvalid) * 16; e += 32) {
+              const int r = nvalid + (e >> 4), c = e & 15;   // row, 16-byte chunk of its 256 B
+              *reinterpret_cast<uint4 *>(vt + (r >> 3) * kAtomBytes + (c >> 3) * 1024 + (r & 7) * 128 + (c & 7) * 16) =
+                  make_uint4(0, 0, 0, 0);
+            }
+            __syncwarp();
+          }
+          fence_async_smem();   // zeroed rows, P^T (and fp8 tiles) written through the generic proxy
+          tc_fence_after();
+          if (leader) {
+            const uint32_t vb = ring + slot * kTileBytes, pb = pbuf + (bp * kMaxTiles + j) * GE::kPBytes;
+            for (int kk = 0; kk < ngroups; ++kk)
+              umma(col_o(bp), umma_desc_sbo(vb + kk * 2 * kAtomBytes, 1024, kAtomBytes),
+                   umma_desc(pb + (kk >> 2) * (kNO * 128) + (kk & 3) * 32, 16), idesc_o,
+                   (j > 0 || kk > 0) ? 1u : 0u);
+            umma_commit(&slot_free[slot]);
+          }
+          __syncwarp();
+          issued = true;
+          ++g_cons;
+        }
+        if (!ok) break;
+        if (leader) {
+          umma_commit(&o_full[bp]);
+          mbar_arrive(&info_free[(u - 1) % kInfo]);
+        }
+        __syncwarp();
+      }
+      if (!cur.valid) break;
+      prev = cur;
+    }
+    // every MMA issued above is complete before tensor memory is freed
+    if (issued) {
+      if (leader) umma_commit(fin);
+      __syncwarp();
+      mbar_wait(fin, 0, p.err);
+    }
+  }
+
+  // ===================================================== teardown
+  tc_fence_before();
+  __syncthreads();
+  if (warp == kMmaWarp) {
+    tc_fence_after();
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "n"(GE::kTmemCols));
+  }
+}
+
+// One CTA: list the (row, partition) items -- rows with the most partitions
+// first (a counting sort on the partition count; rows of equal count in any
+// order), each row's partitions together and in order -- and reset the
+// scheduling cursor and the split rows' completion counters.  Long rows are
+// then finished, and merged, while shorter ones still run; the single-
+// partition rows, which need no merge, come last and even out the CTAs'
+// finishing times.  An empty row lists one item of zero tokens.
+template <int kUnused>
+__global__ void __launch_bounds__(1024) decode_tc_plan_kernel(DecodeParams p) {
+  __shared__ int base[kMaxPartitions];   // per partition count (descending): items, then next free item
+  const int tid = threadIdx.x;
+  const int maxp = p.max_partitions;
+  for (int64_t i = tid; i < (int64_t)p.num_seqs * p.num_q_heads; i += blockDim.x) p.ws_count[i] = 0;
+  for (int i = tid; i < maxp; i += blockDim.x) base[i] = 0;
+  __syncthreads();
+  auto nparts_of = [&](int r, bool report) {
+    return max(1, (checked_len(p, r, report) + p.partition_size - 1) / p.partition_size);
+  };
+  for (int r = tid; r < p.num_seqs; r += blockDim.x) {
+    const int np = nparts_of(r, true);
+    atomicAdd(&base[maxp - np], np);
+  }
+  __syncthreads();
+  if (tid == 0) {   // exclusive scan (maxp entries; a small serial pass)
+    int run = 0;
+    for (int i = 0; i < maxp; ++i) {
+      const int c = base[i];
+      base[i] = run;
+      run += c;
+    }
+    p.hdr->num_items = run;
+    p.hdr->next_unit = 0;
+  }
+  __syncthreads();
+  for (int r = tid; r < p.num_seqs; r += blockDim.x) {
+    const int np = nparts_of(r, false);
+    const int at = atomicAdd(&base[maxp - np], np);
+    for (int q = 0; q < np; ++q) p.items[at + q] = (r << 12) | q;
+  }
+}
+
+// Host launcher: the plan kernel, then one persistent CTA per SM.
+template <typename KV, typename QT, int G>
+cudaError_t launch_decode_tc_one(const DecodeTcParams &p, const PoolMaps &m, cudaStream_t s) {
+  constexpr bool kSplit = std::is_same<QT, __nv_bfloat16>::value && !std::is_same<KV, uint8_t>::value;
+  constexpr int smem = dtc::TcGeo<G, kSplit>::kSmemBytes;
+  decode_tc_plan_kernel<0><<<1, 1024, 0, s>>>(p.d);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  if ((e = ensure_smem_limit<decode_tc_kernel<KV, QT, G>>(smem)) != cudaSuccess) return e;
+  int sms = 0;
+  if ((e = current_sm_count(&sms)) != cudaSuccess) return e;
+  decode_tc_kernel<KV, QT, G><<<sms, dtc::Roles<std::is_same<KV, uint8_t>::value>::kThreads, smem, s>>>(p, m.k, m.v);
+  return cudaGetLastError();
+}
+
+// m: tensor maps over the pools with 3D boxes {64, 8 rows, 2 panels} (16-bit caches; unused for fp8).
+template <typename KV, typename QT>
+cudaError_t launch_decode_tc(const DecodeTcParams &p, int gqa, const PoolMaps &m, cudaStream_t s) {
+  switch (gqa) {
+    case 4: return launch_decode_tc_one<KV, QT, 4>(p, m, s);
+    case 8: return launch_decode_tc_one<KV, QT, 8>(p, m, s);
+    case 16: return launch_decode_tc_one<KV, QT, 16>(p, m, s);
+    default: return cudaErrorInvalidValue;
+  }
+}
+
+}  // namespace pa

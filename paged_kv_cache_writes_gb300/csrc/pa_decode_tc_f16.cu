@@ -1,0 +1,8 @@
+// pa_decode_tc_f16.cu -- tensor-core decode instantiations for an f16 cache.
+#include "pa_decode_tc.cuh"
+
+namespace pa {
+cudaError_t launch_decode_tc_f16(const DecodeTcParams &p, int gqa, const PoolMaps &m, cudaStream_t s) {
+  return launch_decode_tc<__half, __half>(p, gqa, m, s);
+}
+}  // namespace pa

@@ -1,0 +1,13 @@
+// pa_decode_tc_fp8.cu -- tensor-core decode instantiations for an fp8-e4m3
+// cache, with bf16 or f16 queries (the codes are widened to the query type in
+// shared memory).
+#include "pa_decode_tc.cuh"
+
+namespace pa {
+cudaError_t launch_decode_tc_fp8_bf16q(const DecodeTcParams &p, int gqa, const PoolMaps &m, cudaStream_t s) {
+  return launch_decode_tc<uint8_t, __nv_bfloat16>(p, gqa, m, s);
+}
+cudaError_t launch_decode_tc_fp8_f16q(const DecodeTcParams &p, int gqa, const PoolMaps &m, cudaStream_t s) {
+  return launch_decode_tc<uint8_t, __half>(p, gqa, m, s);
+}
+}  // namespace pa

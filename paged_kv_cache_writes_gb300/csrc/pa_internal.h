@@ -106,6 +106,7 @@ struct PoolMaps {
 // The decode kernel reads 256-byte rows as one 3D box of two 128-byte panels.
 
 struct DecodeParams;     // pa_decode.cuh
+struct DecodeTcParams;   // pa_decode_tc.cuh
 struct PrefillTcParams;  // pa_prefill_tc.cuh
 
 // Launch the CUDA-core prefill-row kernel / the persistent decode for one (kv dtype, q dtype).
@@ -125,6 +126,15 @@ cudaError_t launch_decode_fp8_bf16q(const DecodeParams &p, int hpc, const PoolMa
                                     cudaStream_t s);
 cudaError_t launch_decode_fp8_f16q(const DecodeParams &p, int hpc, const PoolMaps &m, int head_dim,
                                    cudaStream_t s);
+
+// Tensor-core decode (head_dim 128; gqa = Hq / Hkv in {4, 8, 16}).
+constexpr bool decode_tc_supported(int head_dim, int gqa) {
+  return head_dim == 128 && (gqa == 4 || gqa == 8 || gqa == 16);
+}
+cudaError_t launch_decode_tc_bf16(const DecodeTcParams &p, int gqa, const PoolMaps &m, cudaStream_t s);
+cudaError_t launch_decode_tc_f16(const DecodeTcParams &p, int gqa, const PoolMaps &m, cudaStream_t s);
+cudaError_t launch_decode_tc_fp8_bf16q(const DecodeTcParams &p, int gqa, const PoolMaps &m, cudaStream_t s);
+cudaError_t launch_decode_tc_fp8_f16q(const DecodeTcParams &p, int gqa, const PoolMaps &m, cudaStream_t s);
 
 // Tensor-core chunked prefill (head_dim 128; gqa = Hq / Hkv in {1, 2, 4, 8, 16}).
 constexpr bool prefill_tc_supported(int head_dim, int gqa) {

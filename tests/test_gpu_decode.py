@@ -1,5 +1,10 @@
 """GPU parity of paged decode against the fp64 oracle, element by element.
 
+Two kernels serve pa_decode: the tensor-core one (head_dim 128 with 4, 8 or
+16 query heads per KV head, chosen by default) and the CUDA-core one (every
+other shape, or every shape once selected with pa_set_decode_kernel); both
+are checked here.
+
 Tolerance (max abs error): 2e-3 for f16/bf16 caches, 2e-2 for an fp8-e4m3
 cache (the oracle dequantises the same codes with the same scales).  Shapes
 span several tiles and partitions with ragged tails; the named workloads run
@@ -10,6 +15,7 @@ import pytest
 import torch
 
 import oracle
+import paged_kv_cache_writes_gb300 as pa
 import workloads as W
 from _gpu import TOL, max_err, oracle_pools, rounded_excess, run_gpu
 
@@ -43,6 +49,34 @@ def test_shapes_bf16(hq, hkv, d, bs):
 @pytest.mark.parametrize("hq,hkv,d,bs", [(32, 8, 128, 16), (64, 8, 128, 32), (8, 8, 64, 16), (16, 4, 64, 32)])
 def test_shapes_other_dtypes(kv, src, hq, hkv, d, bs):
     _check(W.decode_batch("s", EDGE_LENS, hq, hkv, d, bs, src, kv_dtype=kv, seed=hq + d + bs, partition_size=512))
+
+
+@pytest.mark.parametrize("kv,src", [("bf16", "bf16"), ("f16", "f16"), ("fp8", "bf16"), ("fp8", "f16")])
+@pytest.mark.parametrize("hq,hkv,bs", [(32, 2, 16), (64, 4, 32), (16, 1, 16)])
+def test_sixteen_heads_per_kv_head(kv, src, hq, hkv, bs):
+    _check(W.decode_batch("g16", EDGE_LENS, hq, hkv, 128, bs, src, kv_dtype=kv, seed=hq + hkv + bs,
+                          partition_size=512))
+
+
+@pytest.mark.parametrize("kv,src", [("bf16", "bf16"), ("f16", "f16"), ("fp8", "bf16")])
+@pytest.mark.parametrize("hq,hkv,bs", [(32, 8, 16), (64, 8, 32), (16, 2, 16), (32, 2, 32)])
+def test_cuda_core_kernel_on_tensor_core_shapes(kv, src, hq, hkv, bs):
+    """The shapes the tensor-core kernel takes by default, through the CUDA-core kernel."""
+    b = W.decode_batch("cc", EDGE_LENS, hq, hkv, 128, bs, src, kv_dtype=kv, seed=hq * 3 + hkv + bs,
+                       partition_size=512)
+    with pa.decode_kernel("cuda_cores"):
+        _check(b)
+
+
+def test_both_kernels_agree_on_the_llama70b_shape():
+    b = W.decode_batch("both", [1, 129, 512, 513, 1000, 2047, 4100, 8192], 64, 8, 128, 16, "bf16", seed=41)
+    tc = run_gpu(b).out.clone()
+    with pa.decode_kernel("cuda_cores"):
+        cc = run_gpu(b).out.clone()
+    kp, vp = oracle_pools(b)
+    ref = oracle.decode_batch(b, kp, vp)
+    assert max_err(tc, ref) <= TOL["bf16"] and max_err(cc, ref) <= TOL["bf16"]
+    assert (tc - cc).abs().max().item() <= 2 * TOL["bf16"]
 
 
 @pytest.mark.parametrize("ps", [0, 32, 96, 512, 2048])
@@ -125,16 +159,17 @@ def test_mixed_fp8_decode_part_sampled():
     _check(b, seq_ids=np.arange(0, b.num_seqs, 8))
 
 
-def test_bad_block_id_sets_error_without_fault():
-    import paged_kv_cache_writes_gb300 as pa
+@pytest.mark.parametrize("kernel", ["auto", "cuda_cores"])
+def test_bad_block_id_sets_error_without_fault(kernel):
     b = W.decode_batch("bad", [40, 70], 8, 2, 128, 16, "bf16", seed=35)
     from paged_kv_cache_writes_gb300.staging import DeviceBatch
     dev = DeviceBatch(b, "cuda")
     dev.run_setup()
     dev.write_step()
-    dev.block_tables[1, 2] = b.num_blocks + 5        # out of range
-    dev.decode()
-    assert pa.pa_get_device_error() == 4
-    dev.block_tables[1, 2] = -3
-    dev.decode()
-    assert pa.pa_get_device_error() == 4
+    with pa.decode_kernel(kernel):
+        dev.block_tables[1, 2] = b.num_blocks + 5        # out of range
+        dev.decode()
+        assert pa.pa_get_device_error() == 4
+        dev.block_tables[1, 2] = -3
+        dev.decode()
+        assert pa.pa_get_device_error() == 4
