@@ -163,12 +163,16 @@ def measure_prefill(dev_name: str, steps: int, warmup: int) -> dict:
     return res
 
 
+# the sources of the decode kernel the bench times (their hash dates the committed capture)
+DECODE_SOURCES = ("pa_decode_tc.cuh", "pa_tcgen05.cuh", "pa_decode.cuh", "pa_attention.cuh", "pa_common.cuh")
+
+
 def _profiled_traffic(kv_bytes: int):
     """DRAM bytes per decode launch, scaled from the committed ncu capture of the
     decode kernel -- or None if the decode sources changed since that capture."""
     import hashlib
     import re
-    path = os.path.join(ROOT, "profiles", "paged_decode_kernel__llama70b_decode.md")
+    path = os.path.join(ROOT, "profiles", "decode_tc_kernel__llama70b_decode.md")
     if not os.path.exists(path):
         return None
     text = open(path).read()
@@ -177,7 +181,7 @@ def _profiled_traffic(kv_bytes: int):
     if not (m1 and m2):
         return None
     h = hashlib.sha256()
-    for f in ("pa_decode.cuh", "pa_attention.cuh", "pa_common.cuh"):
+    for f in DECODE_SOURCES:
         with open(os.path.join(ROOT, "paged_kv_cache_writes_gb300", "csrc", f), "rb") as fh:
             h.update(fh.read())
     if h.hexdigest()[:16] != m2.group(1):
@@ -451,7 +455,7 @@ def run_ours(args):
         "write_ms": write_ms,
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
                      "traffic": _profiled_traffic(kv_bytes),
-                     "kernel": "paged_decode_kernel (pa_decode: plan + decode launches, timed together)",
+                     "kernel": "decode_tc_kernel (pa_decode: plan + decode launches, timed together)",
                      "peak_source": f"{peak_kind} hbm_gbs"},
         "e2e": {"value": kv_bytes * ws / (e2e_ms * 1e-3) / 1e9, "unit": UNIT, "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms},

@@ -89,13 +89,29 @@ PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
   return fn;
 }
 
+// One pool (256-byte rows) as a 4D tensor of 8-row atoms: dims {64 elements,
+// 8 rows (256 B apart), 2 panels (128 B apart), atoms (2048 B apart)}; one box
+// is a whole cache block of one KV head (block_size / 8 atoms), landing in
+// shared memory as [atom][panel][8 rows][128 B] with the 128-byte swizzle.
+bool encode_pool_map_atoms(CUtensorMap *map, const void *base, const pa_kv_cache &c) {
+  auto enc = tensor_map_encoder();
+  if (!enc || c.head_dim * dtype_bytes(c.kv_dtype) != 256) return false;
+  const CUtensorMapDataType dt = c.kv_dtype == PA_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
+  const cuuint64_t dims[4] = {64, 8, 2, (cuuint64_t)c.num_blocks * c.num_kv_heads * c.block_size / 8};
+  const cuuint64_t strides[3] = {256, 128, 2048};
+  const cuuint32_t box[4] = {64, 8, 2, (cuuint32_t)(c.block_size / 8)};
+  const cuuint32_t estr[4] = {1u, 1u, 1u, 1u};
+  return enc(map, dt, 4, const_cast<void *>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+             CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 // One pool as a 2D tensor [num_blocks*Hkv*bs rows][head_dim]; box = 16 rows x
 // one 128-byte (or 64-byte) panel, swizzled to match the kernels' reads.  With
 // `panels3d` and 256-byte rows the pool is viewed as [2 panels][rows][64] and
-// one box covers box_rows rows of both panels (same shared-memory layout as
-// two 2D boxes: the first panel's rows, then the second's).
-bool encode_pool_map(CUtensorMap *map, const void *base, const pa_kv_cache &c, bool panels3d = false,
-                     int box_rows = 16) {
+// one box covers 16 rows of both panels (same shared-memory layout as two
+// 2D boxes).
+bool encode_pool_map(CUtensorMap *map, const void *base, const pa_kv_cache &c, bool panels3d = false) {
   auto enc = tensor_map_encoder();
   if (!enc) return false;
   const int eb = dtype_bytes(c.kv_dtype);
@@ -114,7 +130,7 @@ bool encode_pool_map(CUtensorMap *map, const void *base, const pa_kv_cache &c, b
   if (panels3d && row_bytes == 2 * panel_bytes) {
     const cuuint64_t dims3[3] = {(cuuint64_t)(panel_bytes / eb), dims[1], 2};
     const cuuint64_t strides3[2] = {(cuuint64_t)row_bytes, (cuuint64_t)panel_bytes};
-    const cuuint32_t box3[3] = {(cuuint32_t)(panel_bytes / eb), (cuuint32_t)box_rows, 2u};
+    const cuuint32_t box3[3] = {(cuuint32_t)(panel_bytes / eb), 16u, 2u};
     const cuuint32_t estr3[3] = {1u, 1u, 1u};
     return enc(map, dt, 3, const_cast<void *>(base), dims3, strides3, box3, estr3,
                CU_TENSOR_MAP_INTERLEAVE_NONE, sw, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
@@ -291,7 +307,7 @@ pa_status pa_decode(const void *q, pa_dtype q_dtype, int32_t num_seqs, int32_t n
     tp.s_mult = p.q_mult;
     PoolMaps maps{};
     if (c.kv_dtype != PA_FP8_E4M3 &&
-        (!encode_pool_map(&maps.k, k_cache, c, true, 8) || !encode_pool_map(&maps.v, v_cache, c, true, 8)))
+        (!encode_pool_map_atoms(&maps.k, k_cache, c) || !encode_pool_map_atoms(&maps.v, v_cache, c)))
       return PA_ERR_CUDA;
     if (c.kv_dtype == PA_BF16) e = launch_decode_tc_bf16(tp, gqa, maps, s);
     else if (c.kv_dtype == PA_F16) e = launch_decode_tc_f16(tp, gqa, maps, s);

@@ -56,7 +56,7 @@
 //  * MMA warp (one elected lane issues): S^T of unit u, then O^T of unit
 //    u-1, whose softmax ran while the scores of u were computed;
 //  * scheduler warp: claims units two at a time and publishes each, with
-//    the block ids of its tiles, in a ring of eight descriptors, so the chain
+//    the block ids of its tiles, in a ring of four descriptors, so the chain
 //    of dependent reads behind a claim (cursor, work item, sequence length,
 //    block table) runs ahead of the loads instead of between them;
 //  * merge warp: merges split rows queued by the softmax warps.
@@ -88,11 +88,13 @@ constexpr int kKeys = 128;                // keys per tile (MMA M, tensor-memory
 constexpr int kMaxTiles = 4;              // tiles per unit: partitions hold <= 512 tokens
 // A K or V tile in shared memory: 16 atoms of 8 keys, atom a at a * 2048,
 // its first 64 elements (128-byte rows, 128-byte swizzle) at +0 and the last
-// 64 at +1024 -- the layout of one 3D bulk-tensor box {64, 8 rows, 2 panels}.
+// 64 at +1024 -- the layout of a 4D bulk-tensor box {64, 8 rows, 2 panels,
+// block_size / 8 atoms} over one cache block.
 constexpr int kTileBytes = kKeys * kD * 2;
 constexpr int kNS = 16;                   // S^T columns per tile (MMA N; heads padded to 16)
 constexpr int kQBytes = 2 * kNS * 128;    // Q^T operand: 2 panels x 16 rows x 128 B
-constexpr int kInfo = 8;                  // unit descriptors in flight
+constexpr int kInfo = 4;                  // unit descriptors in flight (bounds how far a CTA claims ahead)
+constexpr int kClaim = 2;                 // units per claim (a power of two)
 constexpr int kAtomBytes = 2048;          // 8 keys x 256 B: the two 128-byte panels of 8 rows
 
 // Warp roles: 0-3 softmax, then the loaders (one warp issuing bulk-tensor
@@ -495,6 +497,9 @@ __global__ void __launch_bounds__(dtc::Roles<std::is_same<KV, uint8_t>::value>::
         }
         tc_fence_before();
         mbar_arrive(&o_free[bp]);
+        // earlier split units first: the fence then waits only for stores one unit old
+        check_reported();
+        report_pending();
         const int64_t head0 = (int64_t)prev.row * hq + (int64_t)prev.kvh * G;
         const int d = tid;
         if (prev.nparts == 1) {
@@ -519,8 +524,6 @@ __global__ void __launch_bounds__(dtc::Roles<std::is_same<KV, uint8_t>::value>::
             p.ws_ml[(head0 + tid) * p.max_partitions + prev.part] = make_float2(mv, lv);
           }
         }
-        check_reported();
-        report_pending();
         if (prev.nparts > 1) {
           pend_row = prev.row;
           pend_kvh = prev.kvh;
@@ -591,7 +594,9 @@ __global__ void __launch_bounds__(dtc::Roles<std::is_same<KV, uint8_t>::value>::
       }
       // tiles in the MMA's order: K tiles of this unit, then V tiles of the previous one
       if constexpr (!kFp8) {
-        // one bulk-tensor box per atom of 8 keys holding keys of the unit; lane a issues atom a
+        // one bulk-tensor box per cache block holding keys of the unit (bs / 8
+        // atoms; tiles start on block boundaries); lane b issues block b
+        const int atoms = bs >> 3;
         for (int i = 0; i < ntc + ntp && ok; ++i) {
           const bool is_k = i < ntc;
           const UnitHdr &un = is_k ? cur : prev;
@@ -600,20 +605,19 @@ __global__ void __launch_bounds__(dtc::Roles<std::is_same<KV, uint8_t>::value>::
           if (!ok) break;
           const int nvalid = min(kKeys, un.ntok - j * kKeys);
           bool issue = false;
-          int32_t row = 0;
-          if (lane < (nvalid + 7) >> 3) {
+          int32_t atom = 0;
+          if (lane < (nvalid + bs - 1) / bs) {
             const int32_t bi =
-                reinterpret_cast<const volatile int32_t *>(info[is_k ? ib : ibp].blk)[8 * j + (lane >> 1)];
-            const int key0 = un.tok_begin + j * kKeys + 8 * lane;
+                reinterpret_cast<const volatile int32_t *>(info[is_k ? ib : ibp].blk)[8 * j + lane * (bs >> 4)];
             issue = bi >= 0;   // an out-of-range id was reported by the scheduler; its keys stay unread
-            row = (bi * hkv + un.kvh) * bs + key0 % bs;
+            atom = (bi * hkv + un.kvh) * atoms;
           }
           const uint32_t boxes = __popc(__ballot_sync(0xffffffffu, issue));
-          if (lane == 0) mbar_arrive_expect_tx(&slot_full[slot], boxes * kAtomBytes);
+          if (lane == 0) mbar_arrive_expect_tx(&slot_full[slot], boxes * atoms * kAtomBytes);
           __syncwarp();
           if (issue)
-            tma_load_3d(smem + GE::kOffRing + slot * kTileBytes + lane * kAtomBytes, is_k ? &tmap_k : &tmap_v,
-                        &slot_full[slot], 0, row, 0);
+            tma_load_4d(smem + GE::kOffRing + slot * kTileBytes + lane * atoms * kAtomBytes, is_k ? &tmap_k : &tmap_v,
+                        &slot_full[slot], 0, 0, 0, atom);
           ++g_load;
         }
       } else {
@@ -669,22 +673,22 @@ __global__ void __launch_bounds__(dtc::Roles<std::is_same<KV, uint8_t>::value>::
     cp_async_wait_all();
   } else if (warp == kSchedWarp) {
     // ===================================================== scheduler
-    // Two units per claim (one atomic step of 2), published in order; the
-    // block id of run (lane & 7) of tile (lane >> 3) is read by lane `lane`.
+    // kClaim units per claim (one atomic step), published in order; the block
+    // id of run (lane & 7) of tile (lane >> 3) is read by lane `lane`.
     const int bs = p.block_size;
     const int total_units = __ldcg(&p.hdr->num_items) * hkv;
     const int64_t cap = min((int64_t)p.max_blocks_per_seq * bs, (int64_t)p.max_partitions * p.partition_size);
     bool ok = true;
-    for (int u = 0; ok; u += 2) {
-      for (int k = 0; k < 2 && ok; ++k)
+    for (int u = 0; ok; u += kClaim) {
+      for (int k = 0; k < kClaim && ok; ++k)
         if (u + k >= kInfo) ok = wait_all(&info_free[(u + k) % kInfo], (((u + k) / kInfo) - 1) & 1);
       if (!ok) break;
       int id0 = 0;
-      if (lane == 0) id0 = atomicAdd(&p.hdr->next_unit, 2);
+      if (lane == 0) id0 = atomicAdd(&p.hdr->next_unit, kClaim);
       id0 = __shfl_sync(0xffffffffu, id0, 0);
-      // lane k < 2 resolves unit id0 + k
-      const int id = id0 + (lane & 1);
-      const bool valid = lane < 2 && id < total_units;
+      // lane k < kClaim resolves unit id0 + k
+      const int id = id0 + (lane & (kClaim - 1));
+      const bool valid = lane < kClaim && id < total_units;
       int item = 0, L = 0;
       if (valid) item = __ldg(p.items + id / hkv);
       const int row = item >> 12, part = item & 4095;
@@ -697,7 +701,7 @@ __global__ void __launch_bounds__(dtc::Roles<std::is_same<KV, uint8_t>::value>::
       const int nparts = max(1, (L + p.partition_size - 1) / p.partition_size);
       bool any_invalid = false;
 #pragma unroll
-      for (int k = 0; k < 2; ++k) {
+      for (int k = 0; k < kClaim; ++k) {
         const int vk = __shfl_sync(0xffffffffu, (int)valid, k);
         const int rk = __shfl_sync(0xffffffffu, row, k);
         const int tb = __shfl_sync(0xffffffffu, tok_begin, k);
@@ -724,10 +728,8 @@ __global__ void __launch_bounds__(dtc::Roles<std::is_same<KV, uint8_t>::value>::
         any_invalid |= !vk;
       }
       __syncwarp();
-      if (lane == 0) {
-        mbar_arrive(&info_full[u % kInfo]);
-        mbar_arrive(&info_full[(u + 1) % kInfo]);
-      }
+      if (lane == 0)
+        for (int k = 0; k < kClaim; ++k) mbar_arrive(&info_full[(u + k) % kInfo]);
       if (any_invalid) break;   // the ids only grow: every later claim is past the end too
     }
   } else if (warp == kMergeWarp) {
@@ -913,31 +915,34 @@ __global__ void __launch_bounds__(dtc::Roles<std::is_same<KV, uint8_t>::value>::
 }
 
 // One CTA: list the (row, partition) items -- rows with the most partitions
-// first (a counting sort on the partition count; rows of equal count in any
-// order), each row's partitions together and in order -- and reset the
-// scheduling cursor and the split rows' completion counters.  Long rows are
-// then finished, and merged, while shorter ones still run; the single-
-// partition rows, which need no merge, come last and even out the CTAs'
-// finishing times.  An empty row lists one item of zero tokens.
+// first, then the single-partition rows by their number of 128-key tiles
+// (a counting sort; rows of equal key in any order), each row's partitions
+// together and in order -- and reset the scheduling cursor and the split
+// rows' completion counters.  Long rows are then finished, and merged, while
+// shorter ones still run, and the smallest units come last, which evens out
+// the CTAs' finishing times.  An empty row lists one item of zero tokens.
 template <int kUnused>
 __global__ void __launch_bounds__(1024) decode_tc_plan_kernel(DecodeParams p) {
-  __shared__ int base[kMaxPartitions];   // per partition count (descending): items, then next free item
+  // sort key 0 .. maxp + 3: 3 + nparts for a split row, else its tiles (0 .. 4);
+  // base[maxp + 3 - key]: items of the key (descending), then its next free item
+  __shared__ int base[kMaxPartitions + 4];
   const int tid = threadIdx.x;
   const int maxp = p.max_partitions;
+  const int nkeys = maxp + 4;
   for (int64_t i = tid; i < (int64_t)p.num_seqs * p.num_q_heads; i += blockDim.x) p.ws_count[i] = 0;
-  for (int i = tid; i < maxp; i += blockDim.x) base[i] = 0;
+  for (int i = tid; i < nkeys; i += blockDim.x) base[i] = 0;
   __syncthreads();
-  auto nparts_of = [&](int r, bool report) {
-    return max(1, (checked_len(p, r, report) + p.partition_size - 1) / p.partition_size);
-  };
+  auto len_of = [&](int r, bool report) { return checked_len(p, r, report); };
+  auto nparts_of = [&](int L) { return max(1, (L + p.partition_size - 1) / p.partition_size); };
+  auto slot_of = [&](int L, int np) { return nkeys - 1 - (np > 1 ? 3 + np : (L + dtc::kKeys - 1) / dtc::kKeys); };
   for (int r = tid; r < p.num_seqs; r += blockDim.x) {
-    const int np = nparts_of(r, true);
-    atomicAdd(&base[maxp - np], np);
+    const int L = len_of(r, true), np = nparts_of(L);
+    atomicAdd(&base[slot_of(L, np)], np);
   }
   __syncthreads();
-  if (tid == 0) {   // exclusive scan (maxp entries; a small serial pass)
+  if (tid == 0) {   // exclusive scan (a small serial pass)
     int run = 0;
-    for (int i = 0; i < maxp; ++i) {
+    for (int i = 0; i < nkeys; ++i) {
       const int c = base[i];
       base[i] = run;
       run += c;
@@ -947,8 +952,8 @@ __global__ void __launch_bounds__(1024) decode_tc_plan_kernel(DecodeParams p) {
   }
   __syncthreads();
   for (int r = tid; r < p.num_seqs; r += blockDim.x) {
-    const int np = nparts_of(r, false);
-    const int at = atomicAdd(&base[maxp - np], np);
+    const int L = len_of(r, false), np = nparts_of(L);
+    const int at = atomicAdd(&base[slot_of(L, np)], np);
     for (int q = 0; q < np; ++q) p.items[at + q] = (r << 12) | q;
   }
 }
@@ -968,7 +973,8 @@ cudaError_t launch_decode_tc_one(const DecodeTcParams &p, const PoolMaps &m, cud
   return cudaGetLastError();
 }
 
-// m: tensor maps over the pools with 3D boxes {64, 8 rows, 2 panels} (16-bit caches; unused for fp8).
+// m: tensor maps over the pools viewed as [atoms of 8 rows][2 panels][8 rows][64], one box per cache
+// block (16-bit caches; unused for fp8).
 template <typename KV, typename QT>
 cudaError_t launch_decode_tc(const DecodeTcParams &p, int gqa, const PoolMaps &m, cudaStream_t s) {
   switch (gqa) {

@@ -213,5 +213,16 @@ __device__ __forceinline__ void widen16(uint4 w, uint32_t (&o)[8]) {
   }
 }
 
+// 4D tiled bulk-tensor load global -> shared, coordinates innermost first,
+// completion counted in bytes on `bar`.
+__device__ __forceinline__ void tma_load_4d(void *smem_dst, const CUtensorMap *map, uint64_t *bar, int32_t c0,
+                                            int32_t c1, int32_t c2, int32_t c3) {
+  asm volatile(
+      "cp.async.bulk.tensor.4d.shared::cta.global.tile.mbarrier::complete_tx::bytes "
+      "[%0], [%1, {%3, %4, %5, %6}], [%2];" ::"r"(smem_u32(smem_dst)),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(smem_u32(bar)), "r"(c0), "r"(c1), "r"(c2), "r"(c3)
+      : "memory");
+}
+
 }  // namespace tc
 }  // namespace pa
