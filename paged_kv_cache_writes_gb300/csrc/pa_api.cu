@@ -106,6 +106,20 @@ bool encode_pool_map_atoms(CUtensorMap *map, const void *base, const pa_kv_cache
              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// An fp8 pool (128-byte rows) as a 2D tensor [rows][128 codes]; one box is a
+// whole cache block of one KV head (block_size rows), 128-byte swizzle.
+bool encode_pool_map_fp8_blocks(CUtensorMap *map, const void *base, const pa_kv_cache &c) {
+  auto enc = tensor_map_encoder();
+  if (!enc || c.head_dim != 128 || c.kv_dtype != PA_FP8_E4M3) return false;
+  const cuuint64_t dims[2] = {128, (cuuint64_t)c.num_blocks * c.num_kv_heads * c.block_size};
+  const cuuint64_t strides[1] = {128};
+  const cuuint32_t box[2] = {128, (cuuint32_t)c.block_size};
+  const cuuint32_t estr[2] = {1u, 1u};
+  return enc(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void *>(base), dims, strides, box, estr,
+             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 // One pool as a 2D tensor [num_blocks*Hkv*bs rows][head_dim]; box = 16 rows x
 // one 128-byte (or 64-byte) panel, swizzled to match the kernels' reads.  With
 // `panels3d` and 256-byte rows the pool is viewed as [2 panels][rows][64] and
@@ -306,8 +320,9 @@ pa_status pa_decode(const void *q, pa_dtype q_dtype, int32_t num_seqs, int32_t n
     tp.v_cache = v_cache;
     tp.s_mult = p.q_mult;
     PoolMaps maps{};
-    if (c.kv_dtype != PA_FP8_E4M3 &&
-        (!encode_pool_map_atoms(&maps.k, k_cache, c) || !encode_pool_map_atoms(&maps.v, v_cache, c)))
+    const bool fp8_cache = c.kv_dtype == PA_FP8_E4M3;
+    if (fp8_cache ? (!encode_pool_map_fp8_blocks(&maps.k, k_cache, c) || !encode_pool_map_fp8_blocks(&maps.v, v_cache, c))
+                  : (!encode_pool_map_atoms(&maps.k, k_cache, c) || !encode_pool_map_atoms(&maps.v, v_cache, c)))
       return PA_ERR_CUDA;
     if (c.kv_dtype == PA_BF16) e = launch_decode_tc_bf16(tp, gqa, maps, s);
     else if (c.kv_dtype == PA_F16) e = launch_decode_tc_f16(tp, gqa, maps, s);

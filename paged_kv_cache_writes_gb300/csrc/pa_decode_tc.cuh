@@ -47,12 +47,12 @@
 // claimed from an atomic cursor by a persistent CTA per SM.  Roles:
 //  * warps 0-3, softmax and epilogue: thread i owns tensor-memory lane i (key
 //    i of a score tile, element d = i of an output row);
-//  * loaders (one warp for a 16-bit cache, four for fp8): stage Q (cp.async)
-//    and stream the unit's K tiles,
-//    then the previous unit's V tiles, through a ring of 32 KB tiles in the
-//    MMA's 128-byte-swizzled layout (16-byte cp.async with zero fill past the
-//    sequence end for 16-bit caches; register loads widened exactly to the
-//    query's type for fp8);
+//  * loader warp: stages Q (cp.async) and streams the unit's K tiles, then
+//    the previous unit's V tiles, with one bulk-tensor copy per cache block:
+//    a 16-bit cache straight into a ring of 32 KB tiles in the MMA's
+//    128-byte-swizzled layout, an fp8 cache into a ring of raw 16 KB tiles;
+//  * fp8 only, four widening warps: each staged tile is widened exactly to
+//    the query's 16-bit type into the MMA ring (rows past the end as zeros);
 //  * MMA warp (one elected lane issues): S^T of unit u, then O^T of unit
 //    u-1, whose softmax ran while the scores of u were computed;
 //  * scheduler warp: claims units two at a time and publishes each, with
@@ -97,14 +97,15 @@ constexpr int kInfo = 4;                  // unit descriptors in flight (bounds 
 constexpr int kClaim = 2;                 // units per claim (a power of two)
 constexpr int kAtomBytes = 2048;          // 8 keys x 256 B: the two 128-byte panels of 8 rows
 
-// Warp roles: 0-3 softmax, then the loaders (one warp issuing bulk-tensor
-// copies for a 16-bit cache; four widening fp8 codes), the MMA warp, the
+// Warp roles: 0-3 softmax, 4 the loader (bulk-tensor copies and Q), then for
+// an fp8 cache four warps widening the staged codes, the MMA warp, the
 // scheduler warp, the merge warp.
 template <bool kFp8>
 struct Roles {
-  static constexpr int kLoadWarps = kFp8 ? 4 : 1;
-  static constexpr int kLoadWarp0 = 4;
-  static constexpr int kMmaWarp = kLoadWarp0 + kLoadWarps;
+  static constexpr int kLoadWarp = 4;
+  static constexpr int kWidenWarp0 = 5;
+  static constexpr int kWidenWarps = kFp8 ? 4 : 0;
+  static constexpr int kMmaWarp = kWidenWarp0 + kWidenWarps;
   static constexpr int kSchedWarp = kMmaWarp + 1;
   static constexpr int kMergeWarp = kSchedWarp + 1;
   static constexpr int kThreads = (kMergeWarp + 1) * 32;
@@ -125,7 +126,10 @@ struct TcUnit {
   int32_t blk[kMaxTiles * 8];
 };
 
-template <int G, bool kSplit>
+constexpr int kStageSlots = 4;            // fp8: raw tiles staged by bulk copies
+constexpr int kStageBytes = kKeys * kD;   // 16 KB: 128 rows of 128 e4m3 codes
+
+template <int G, bool kSplit, bool kFp8>
 struct TcGeo {
   static_assert(G == 4 || G == 8 || G == 16, "4, 8 or 16 query heads per KV head");
   static constexpr int kPRows = kSplit ? 2 * G : G;         // P^T columns in use
@@ -133,7 +137,7 @@ struct TcGeo {
   static constexpr int kPBytes = 2 * kNO * 128;             // P^T of a tile: 2 panels (64 keys) x kNO rows
   static constexpr int kColO = 2 * kMaxTiles * kNS;         // tensor-memory column of O^T, buffer 0
   static constexpr int kTmemCols = 256;                     // 128 S^T + 2 * kNO O^T columns, rounded up
-  static constexpr int kNumBars = 2 * kMaxSlots + 8 * 2 + 2 * kInfo + kJobs + 1;
+  static constexpr int kNumBars = 2 * kMaxSlots + 8 * 2 + 2 * kInfo + kJobs + 1 + 2 * kStageSlots + 2;
   static constexpr int kOffQ = 0;                                        // [2] Q^T
   static constexpr int kOffP = kOffQ + 2 * kQBytes;                      // [2][4] P^T
   static constexpr int kOffRed = kOffP + 2 * kMaxTiles * kPBytes;        // float [2][4 warps][2][16]
@@ -141,11 +145,15 @@ struct TcGeo {
   static constexpr int kOffJobs = kOffInfo + kInfo * (int)sizeof(TcUnit);   // MergeJob [kJobs]
   static constexpr int kOffBar = kOffJobs + kJobs * (int)sizeof(MergeJob);
   static constexpr int kOffMisc = kOffBar + kNumBars * 8;
-  static constexpr int kOffRing = (kOffMisc + 64 + 1023) / 1024 * 1024;  // [kSlots] K/V tiles
+  static constexpr int kOffQraw = (kOffMisc + 64 + 15) / 16 * 16;        // fp8: [2] the G query rows as given
+  static constexpr int kOffStage = (kOffQraw + (kFp8 ? 2 * G * kD * 2 : 0) + 1023) / 1024 * 1024;  // fp8: raw tiles
+  static constexpr int kOffRing = kOffStage + (kFp8 ? kStageSlots * kStageBytes : 0);  // [kSlots] K/V tiles
   static constexpr int kSlots0 = (227 * 1024 - 1024 - kOffRing) / kTileBytes;
   static constexpr int kSlots = kSlots0 > kMaxSlots ? kMaxSlots : kSlots0;
   static constexpr int kSmemBytes = kOffRing + kSlots * kTileBytes + 1024;  // + alignment slack
   static_assert(kSlots >= 2 && kSmemBytes <= 227 * 1024, "shared memory");
+  static_assert(kOffQraw % 16 == 0 && kOffStage % 1024 == 0 && kOffRing % 1024 == 0 && kOffP % 1024 == 0,
+                "16-byte copies, 1024-byte swizzle atoms");
 };
 
 // N consecutive fp32 columns of this thread's tensor-memory lane (warp-collective).
@@ -232,12 +240,14 @@ __global__ void __launch_bounds__(dtc::Roles<std::is_same<KV, uint8_t>::value>::
   using namespace dtc;
   constexpr bool kFp8 = std::is_same<KV, uint8_t>::value;
   using RO = Roles<kFp8>;
-  constexpr int kLoadWarp0 = RO::kLoadWarp0, kLoadWarps = RO::kLoadWarps, kMmaWarp = RO::kMmaWarp;
+  constexpr int kLoadWarp = RO::kLoadWarp, kWidenWarp0 = RO::kWidenWarp0, kMmaWarp = RO::kMmaWarp;
   constexpr int kSchedWarp = RO::kSchedWarp, kMergeWarp = RO::kMergeWarp, kThreads = RO::kThreads;
-  constexpr int kLoaders = 32 * kLoadWarps;
-  constexpr bool kBf16 = std::is_same<QT, __nv_bfloat16>::value;
-  constexpr bool kSplit = kBf16 && !kFp8;   // bf16 cache: P as hi + lo
-  using GE = TcGeo<G, kSplit>;
+  constexpr int kWideners = 32 * RO::kWidenWarps;
+  // MMA operands: the cache's 16-bit type; an fp8 cache is widened to f16 (exact,
+  // one conversion per two codes) and the queries are converted to f16 too
+  constexpr bool kBf16 = std::is_same<QT, __nv_bfloat16>::value && !kFp8;
+  constexpr bool kSplit = kBf16;            // bf16 cache: P as hi + lo
+  using GE = TcGeo<G, kSplit, kFp8>;
   constexpr int S = GE::kSlots, kNO = GE::kNO;
   constexpr uint32_t kAB = kBf16 ? 1u : 0u;
   const DecodeParams &p = tp.d;
@@ -261,6 +271,9 @@ __global__ void __launch_bounds__(dtc::Roles<std::is_same<KV, uint8_t>::value>::
   uint64_t *info_free = info_full + kInfo;    // [kInfo] released by the MMA warp and the softmax warps
   uint64_t *job_full = info_free + kInfo;     // [kJobs] merge job queued
   uint64_t *fin = job_full + kJobs;           // every MMA of the CTA complete
+  uint64_t *stage_full = fin + 1;             // fp8 [kStageSlots] raw tile copied
+  uint64_t *stage_free = stage_full + kStageSlots;   // fp8 [kStageSlots] widened (every widening thread)
+  uint64_t *qraw_full = stage_free + kStageSlots;     // fp8 [2] query rows copied (loader lanes)
   MergeJob *jobs = reinterpret_cast<MergeJob *>(smem + GE::kOffJobs);
   TcUnit *info = reinterpret_cast<TcUnit *>(smem + GE::kOffInfo);
   float *red = reinterpret_cast<float *>(smem + GE::kOffRed);
@@ -277,11 +290,11 @@ __global__ void __launch_bounds__(dtc::Roles<std::is_same<KV, uint8_t>::value>::
     reinterpret_cast<uint4 *>(smem + GE::kOffQ)[i] = make_uint4(0, 0, 0, 0);
   if (tid == 0) {
     for (int s = 0; s < S; ++s) {
-      mbar_init(&slot_full[s], kFp8 ? kLoaders : 1);   // fp8: every loader thread; else one expect-tx arrival
+      mbar_init(&slot_full[s], kFp8 ? kWideners : 1);   // fp8: every widening thread; else one expect-tx arrival
       mbar_init(&slot_free[s], 1);
     }
     for (int b = 0; b < 2; ++b) {
-      mbar_init(&q_full[b], kLoaders);
+      mbar_init(&q_full[b], kFp8 ? kWideners : 32);   // fp8: the widening warps convert Q
       mbar_init(&q_free[b], 1);
       mbar_init(&s_full[b], 1);
       mbar_init(&s_free[b], 128);
@@ -296,15 +309,18 @@ __global__ void __launch_bounds__(dtc::Roles<std::is_same<KV, uint8_t>::value>::
     }
     for (int i = 0; i < kJobs; ++i) mbar_init(&job_full[i], 1);
     mbar_init(fin, 1);
+    for (int i = 0; i < kStageSlots; ++i) {
+      mbar_init(&stage_full[i], 1);
+      mbar_init(&stage_free[i], kWideners > 0 ? kWideners : 1);
+    }
+    for (int i = 0; i < 2; ++i) mbar_init(&qraw_full[i], 32);
     *abort_flag = 0;
     *job_ticket = 0;
     *softmax_done = 0;
     *jobs_taken = 0;
     fence_mbar_init();
-    if constexpr (!kFp8) {
-      prefetch_tensor_map(&tmap_k);
-      prefetch_tensor_map(&tmap_v);
-    }
+    prefetch_tensor_map(&tmap_k);
+    prefetch_tensor_map(&tmap_v);
   }
   if (warp == kMmaWarp) {
     asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(tmem_slot)),
@@ -325,7 +341,7 @@ __global__ void __launch_bounds__(dtc::Roles<std::is_same<KV, uint8_t>::value>::
   const int hkv = p.num_kv_heads;
   const int hq = p.num_q_heads;
 
-  if (warp < kLoadWarp0) {
+  if (warp < kLoadWarp) {
     // ===================================================== softmax and epilogue (warps 0-3)
     const uint32_t lane_base = (uint32_t)(warp * 32) << 16;
     const float c = tp.s_mult;
@@ -468,11 +484,7 @@ __global__ void __launch_bounds__(dtc::Roles<std::is_same<KV, uint8_t>::value>::
               *reinterpret_cast<uint16_t *>(pt + (G + h) * 128 + ((ck ^ ((G + h) & 7)) << 4)) =
                   (uint16_t)(__float_as_uint(lo) >> 16);
               l_part[h] += pv;
-            } else if constexpr (kBf16) {
-              const uint32_t r = bf16_round_bits(pv);
-              *reinterpret_cast<uint16_t *>(pt + h * 128 + ((ck ^ (h & 7)) << 4)) = (uint16_t)(r >> 16);
-              l_part[h] += __uint_as_float(r);   // the rounded p the MMA uses
-            } else {
+            } else {   // f16 operands (f16 cache, or an fp8 cache widened to f16)
               const __half hv = __float2half_rn(pv);
               *reinterpret_cast<__half *>(pt + h * 128 + ((ck ^ (h & 7)) << 4)) = hv;
               l_part[h] += __half2float(hv);
@@ -541,32 +553,17 @@ __global__ void __launch_bounds__(dtc::Roles<std::is_same<KV, uint8_t>::value>::
       report_pending();
       check_reported();
       // the last softmax warp to finish ends the merge queue (after every job of every warp)
-      if (lane == 0 && atomicAdd(softmax_done, 1) == kLoadWarp0 - 1) queue_job(-1, 0, 0);
+      if (lane == 0 && atomicAdd(softmax_done, 1) == 3) queue_job(-1, 0, 0);
     }
-  } else if (warp < kMmaWarp) {
-    // ===================================================== loaders
-    const int lt = tid - kLoadWarp0 * 32, lw = lt >> 5;
-    constexpr int kRowBytes = kFp8 ? kD : 2 * kD;
-    const char *kpool = static_cast<const char *>(tp.k_cache);
-    const char *vpool = static_cast<const char *>(tp.v_cache);
+  } else if (warp == kLoadWarp) {
+    // ===================================================== loader (one warp)
+    // Q with cp.async; every K and V tile with one bulk-tensor box per cache
+    // block holding keys of the unit (tiles start on block boundaries):
+    // 16-bit caches straight into the MMA's atom layout (bs / 8 atoms per box),
+    // fp8 caches raw into the staging ring (bs rows of 128 codes per box).
     const int bs = p.block_size;
     uint32_t g_load = 0;
     bool ok = true;
-
-    // first cache row of run r (of this warp's two) of tile j of the unit in
-    // descriptor slot ib, and how many of its 16 rows hold keys of the unit
-    auto run_rows = [&](const UnitHdr &un, int ib, int j, int r, int64_t &row0) -> int {
-      const int32_t bi = reinterpret_cast<const volatile int32_t *>(info[ib].blk)[8 * j + 2 * lw + r];
-      const int key0 = un.tok_begin + j * kKeys + 32 * lw + 16 * r;
-      row0 = ((int64_t)max(bi, 0) * hkv + un.kvh) * bs + (key0 % bs);
-      return bi < 0 ? 0 : min(16, un.tok_begin + un.ntok - key0);
-    };
-    auto acquire_slot = [&]() -> int {
-      const int slot = (int)(g_load % S);
-      if (g_load >= (uint32_t)S) ok = wait_all(&slot_free[slot], ((g_load / S) - 1) & 1);
-      return slot;
-    };
-
     UnitHdr prev;
     prev.valid = 0;
     for (int u = 0; ok; ++u) {
@@ -582,95 +579,140 @@ __global__ void __launch_bounds__(dtc::Roles<std::is_same<KV, uint8_t>::value>::
           if (!ok) break;
         }
 #pragma unroll
-        for (int e = lt; e < G * 16; e += kLoaders) {
+        for (int e = lane; e < G * 16; e += 32) {
           const int h = e >> 4, c16 = e & 15;
           const char *src = static_cast<const char *>(p.q) +
                             (((int64_t)cur.row * hq + (int64_t)cur.kvh * G + h) * kD) * 2 + c16 * 16;
-          cp_async16(smem + GE::kOffQ + b * kQBytes + (c16 >> 3) * (kNS * 128) + h * 128 +
-                         (((c16 & 7) ^ (h & 7)) << 4),
-                     src, 16u);
+          if constexpr (kFp8)   // as given, for the widening warps to convert
+            cp_async16(smem + GE::kOffQraw + b * (G * kD * 2) + e * 16, src, 16u);
+          else
+            cp_async16(smem + GE::kOffQ + b * kQBytes + (c16 >> 3) * (kNS * 128) + h * 128 +
+                           (((c16 & 7) ^ (h & 7)) << 4),
+                       src, 16u);
         }
-        cp_async_arrive_noinc(&q_full[b]);
+        cp_async_arrive_noinc(kFp8 ? &qraw_full[b] : &q_full[b]);
       }
       // tiles in the MMA's order: K tiles of this unit, then V tiles of the previous one
-      if constexpr (!kFp8) {
-        // one bulk-tensor box per cache block holding keys of the unit (bs / 8
-        // atoms; tiles start on block boundaries); lane b issues block b
-        const int atoms = bs >> 3;
-        for (int i = 0; i < ntc + ntp && ok; ++i) {
-          const bool is_k = i < ntc;
-          const UnitHdr &un = is_k ? cur : prev;
-          const int j = is_k ? i : i - ntc;
-          const int slot = acquire_slot();
-          if (!ok) break;
-          const int nvalid = min(kKeys, un.ntok - j * kKeys);
-          bool issue = false;
-          int32_t atom = 0;
-          if (lane < (nvalid + bs - 1) / bs) {
-            const int32_t bi =
-                reinterpret_cast<const volatile int32_t *>(info[is_k ? ib : ibp].blk)[8 * j + lane * (bs >> 4)];
-            issue = bi >= 0;   // an out-of-range id was reported by the scheduler; its keys stay unread
-            atom = (bi * hkv + un.kvh) * atoms;
-          }
-          const uint32_t boxes = __popc(__ballot_sync(0xffffffffu, issue));
-          if (lane == 0) mbar_arrive_expect_tx(&slot_full[slot], boxes * atoms * kAtomBytes);
+      for (int i = 0; i < ntc + ntp && ok; ++i) {
+        const bool is_k = i < ntc;
+        const UnitHdr &un = is_k ? cur : prev;
+        const int j = is_k ? i : i - ntc;
+        const uint32_t ring = kFp8 ? (uint32_t)kStageSlots : (uint32_t)S;
+        const int slot = (int)(g_load % ring);
+        uint64_t *free_bar = kFp8 ? &stage_free[slot] : &slot_free[slot];
+        uint64_t *full_bar = kFp8 ? &stage_full[slot] : &slot_full[slot];
+        if (g_load >= ring) ok = wait_all(free_bar, ((g_load / ring) - 1) & 1);
+        if (!ok) break;
+        const int nvalid = min(kKeys, un.ntok - j * kKeys);
+        bool issue = false;
+        int32_t bi = 0;
+        if (lane < (nvalid + bs - 1) / bs) {
+          bi = reinterpret_cast<const volatile int32_t *>(info[is_k ? ib : ibp].blk)[8 * j + lane * (bs >> 4)];
+          issue = bi >= 0;   // an out-of-range id was reported by the scheduler; its keys stay unread
+        }
+        const uint32_t boxes = __popc(__ballot_sync(0xffffffffu, issue));
+        const CUtensorMap *map = is_k ? &tmap_k : &tmap_v;
+        if constexpr (!kFp8) {
+          const int atoms = bs >> 3;
+          if (lane == 0) mbar_arrive_expect_tx(full_bar, boxes * atoms * kAtomBytes);
           __syncwarp();
           if (issue)
-            tma_load_4d(smem + GE::kOffRing + slot * kTileBytes + lane * atoms * kAtomBytes, is_k ? &tmap_k : &tmap_v,
-                        &slot_full[slot], 0, 0, 0, atom);
-          ++g_load;
+            tma_load_4d(smem + GE::kOffRing + slot * kTileBytes + lane * atoms * kAtomBytes, map, full_bar, 0, 0, 0,
+                        (bi * hkv + un.kvh) * atoms);
+        } else {
+          if (lane == 0) mbar_arrive_expect_tx(full_bar, boxes * bs * kD);
+          __syncwarp();
+          if (issue)
+            tma_load_2d(smem + GE::kOffStage + slot * kStageBytes + lane * bs * kD, map, full_bar, 0,
+                        (bi * hkv + un.kvh) * bs);
         }
-      } else {
-        // fp8 rows (128 B): per load 4 rows x 8 words of 16 codes; the next tile's
-        // words are in flight while the current tile is widened into shared memory
-        const int q = lane & 7, pn = q >> 2, c0 = (2 * q) & 7;   // word q: elements 16q..16q+15
-        auto fetch = [&](int i, uint4 (&w)[8]) {
-          const bool is_k = i < ntc;
-          const UnitHdr &un = is_k ? cur : prev;
-          const int j = is_k ? i : i - ntc;
-          const char *pool = is_k ? kpool : vpool;
-#pragma unroll
-          for (int r = 0; r < 2; ++r) {
-            int64_t row0;
-            const int nval = run_rows(un, is_k ? ib : ibp, j, r, row0);
-#pragma unroll
-            for (int k = 0; k < 4; ++k) {
-              const int rr = 4 * k + (lane >> 3);
-              w[4 * r + k] = rr < nval ? ld_nc16(pool + (row0 + rr) * kRowBytes + q * 16) : make_uint4(0, 0, 0, 0);
-            }
-          }
-        };
-        const int n = ntc + ntp;
-        uint4 wc[8], wn[8];
-        if (n > 0) fetch(0, wc);
-        for (int i = 0; i < n && ok; ++i) {
-          if (i + 1 < n) fetch(i + 1, wn);
-          const int slot = acquire_slot();
-          if (!ok) break;
-          uint8_t *tile = smem + GE::kOffRing + slot * kTileBytes + pn * 1024;
-#pragma unroll
-          for (int r = 0; r < 2; ++r) {
-#pragma unroll
-            for (int k = 0; k < 4; ++k) {
-              const int row = 32 * lw + 16 * r + 4 * k + (lane >> 3);
-              uint32_t o[8];
-              widen16<QT>(wc[4 * r + k], o);
-              uint8_t *dst = tile + (row >> 3) * kAtomBytes + (row & 7) * 128;
-              *reinterpret_cast<uint4 *>(dst + ((c0 ^ (row & 7)) << 4)) = make_uint4(o[0], o[1], o[2], o[3]);
-              *reinterpret_cast<uint4 *>(dst + (((c0 + 1) ^ (row & 7)) << 4)) = make_uint4(o[4], o[5], o[6], o[7]);
-            }
-          }
-          fence_async_smem();
-          mbar_arrive(&slot_full[slot]);
-          ++g_load;
-#pragma unroll
-          for (int k = 0; k < 8; ++k) wc[k] = wn[k];
-        }
+        ++g_load;
       }
       if (!cur.valid) break;
       prev = cur;
     }
     cp_async_wait_all();
+  } else if (warp < kMmaWarp) {
+    // ===================================================== fp8 widening (four warps)
+    // Per unit, the G query rows -> f16 Q^T.  Staged row r of a tile (128
+    // codes, 128-byte swizzle) -> row r of the f16 tile in the MMA's atom
+    // layout, exactly (widen16); rows past the end of the unit are written as
+    // zeros (P is 0 there, and 0 * NaN would not be).  A thread's eight staged
+    // words are read first, so their loads overlap.
+    const int wt = tid - kWidenWarp0 * 32;
+    uint32_t g = 0;
+    bool ok = true;
+    UnitHdr prev;
+    prev.valid = 0;
+    for (int u = 0; ok; ++u) {
+      const int ib = u % kInfo, b = u & 1;
+      ok = wait_all(&info_full[ib], (u / kInfo) & 1);
+      if (!ok) break;
+      const UnitHdr cur = read_unit(&info[ib]);
+      const int ntc = num_tiles(cur), ntp = num_tiles(prev);
+      if (cur.valid) {
+        // Q^T in f16: exact for |q| in [2^-17, 65504]; larger magnitudes saturate to 65504
+        if (u >= 2) ok = wait_all(&q_free[b], ((u >> 1) - 1) & 1);
+        if (ok) ok = wait_all(&qraw_full[b], (u >> 1) & 1);
+        if (!ok) break;
+        for (int e = wt; e < G * 16; e += kWideners) {
+          const int h = e >> 4, c16 = e & 15;
+          const uint4 w = *reinterpret_cast<const uint4 *>(smem + GE::kOffQraw + b * (G * kD * 2) + e * 16);
+          const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
+          uint32_t o[4];
+#pragma unroll
+          for (int k = 0; k < 4; ++k) {
+            float2 f = unpack2(ws[k], QT{});
+            f.x = fminf(fmaxf(f.x, -65504.f), 65504.f);
+            f.y = fminf(fmaxf(f.y, -65504.f), 65504.f);
+            o[k] = pack2(f.x, f.y, __half{});
+          }
+          *reinterpret_cast<uint4 *>(smem + GE::kOffQ + b * kQBytes + (c16 >> 3) * (kNS * 128) + h * 128 +
+                                     (((c16 & 7) ^ (h & 7)) << 4)) = make_uint4(o[0], o[1], o[2], o[3]);
+        }
+        fence_async_smem();
+        mbar_arrive(&q_full[b]);
+      }
+      for (int i = 0; i < ntc + ntp && ok; ++i) {
+        const bool is_k = i < ntc;
+        const UnitHdr &un = is_k ? cur : prev;
+        const int j = is_k ? i : i - ntc;
+        const int nvalid = min(kKeys, un.ntok - j * kKeys);
+        const int ss = (int)(g % kStageSlots), slot = (int)(g % S);
+        ok = wait_all(&stage_full[ss], (g / kStageSlots) & 1);
+        if (ok && g >= (uint32_t)S) ok = wait_all(&slot_free[slot], ((g / S) - 1) & 1);
+        if (!ok) break;
+        const uint8_t *st = smem + GE::kOffStage + ss * kStageBytes;
+        uint8_t *tile = smem + GE::kOffRing + slot * kTileBytes;
+        constexpr int kChunks = kStageBytes / 16 / 128;   // 16-code chunks per thread
+        uint4 raw[kChunks];
+#pragma unroll
+        for (int k = 0; k < kChunks; ++k) {
+          const int id = k * 128 + wt, r = id >> 3, c = id & 7;   // row, 16-code chunk
+          raw[k] = *reinterpret_cast<const uint4 *>(st + r * 128 + ((c ^ (r & 7)) << 4));
+        }
+#pragma unroll
+        for (int k = 0; k < kChunks; ++k) {
+          const int id = k * 128 + wt, r = id >> 3, c = id & 7;
+          uint32_t o[8];
+          widen16<__half>(raw[k], o);
+          if (r >= nvalid) {
+#pragma unroll
+            for (int i = 0; i < 8; ++i) o[i] = 0;
+          }
+          const int c0 = (2 * c) & 7;
+          uint8_t *dst = tile + (r >> 3) * kAtomBytes + (c >> 2) * 1024 + (r & 7) * 128;
+          *reinterpret_cast<uint4 *>(dst + ((c0 ^ (r & 7)) << 4)) = make_uint4(o[0], o[1], o[2], o[3]);
+          *reinterpret_cast<uint4 *>(dst + (((c0 + 1) ^ (r & 7)) << 4)) = make_uint4(o[4], o[5], o[6], o[7]);
+        }
+        fence_async_smem();
+        mbar_arrive(&slot_full[slot]);
+        mbar_arrive(&stage_free[ss]);
+        ++g;
+      }
+      if (!cur.valid) break;
+      prev = cur;
+    }
   } else if (warp == kSchedWarp) {
     // ===================================================== scheduler
     // kClaim units per claim (one atomic step), published in order; the block
@@ -962,7 +1004,7 @@ __global__ void __launch_bounds__(1024) decode_tc_plan_kernel(DecodeParams p) {
 template <typename KV, typename QT, int G>
 cudaError_t launch_decode_tc_one(const DecodeTcParams &p, const PoolMaps &m, cudaStream_t s) {
   constexpr bool kSplit = std::is_same<QT, __nv_bfloat16>::value && !std::is_same<KV, uint8_t>::value;
-  constexpr int smem = dtc::TcGeo<G, kSplit>::kSmemBytes;
+  constexpr int smem = dtc::TcGeo<G, kSplit, std::is_same<KV, uint8_t>::value>::kSmemBytes;
   decode_tc_plan_kernel<0><<<1, 1024, 0, s>>>(p.d);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
@@ -973,8 +1015,8 @@ cudaError_t launch_decode_tc_one(const DecodeTcParams &p, const PoolMaps &m, cud
   return cudaGetLastError();
 }
 
-// m: tensor maps over the pools viewed as [atoms of 8 rows][2 panels][8 rows][64], one box per cache
-// block (16-bit caches; unused for fp8).
+// m: tensor maps over the pools, one box per cache block of one KV head: 16-bit
+// caches viewed as [atoms of 8 rows][2 panels][8 rows][64], fp8 caches as [rows][128].
 template <typename KV, typename QT>
 cudaError_t launch_decode_tc(const DecodeTcParams &p, int gqa, const PoolMaps &m, cudaStream_t s) {
   switch (gqa) {
