@@ -185,6 +185,37 @@ PA_API pa_status pa_decode(const void *q, pa_dtype q_dtype, int32_t num_seqs,
                     pa_stream_t stream);
 
 /*
+ * pa_decode_write -- one decode step in one call: the cache write of the
+ * step's new tokens (pa_reshape_and_cache) fused with pa_decode.  Sequence i's
+ * new token, row i of k_new / v_new, is stored at slot_mapping[i] exactly as
+ * pa_reshape_and_cache stores it, and then every sequence attends exactly as
+ * pa_decode does, the new token included ([V07] "Architectural Blueprint 3:
+ * Chunked Prefill", decode phase: each step appends one token per sequence and
+ * reads the whole cache).  With the tensor-core decode the token is stored by
+ * the decode launch itself, just before the copy of the tile that holds it;
+ * otherwise the cache write is launched first, on the same stream.
+ *
+ *   k_new, v_new   device [num_seqs][num_kv_heads][head_dim] in q_dtype, token
+ *                  (row) stride token_stride elements (>= Hkv * head_dim, a
+ *                  multiple of 8), 16-byte aligned
+ *   slot_mapping   device int64 [num_seqs]: the slot of position seq_lens[i]-1
+ *                  of sequence i (its last token), or negative for a sequence
+ *                  with no new token this step.  Any other slot is a
+ *                  violation: PA_ERR_DEVICE_CHECK may be recorded and the token
+ *                  not stored.
+ *   all other arguments as for pa_decode.
+ */
+PA_API pa_status pa_decode_write(const void *q, pa_dtype q_dtype, int32_t num_seqs,
+                          int32_t num_q_heads, const void *k_new, const void *v_new,
+                          int64_t token_stride, const int64_t *slot_mapping,
+                          void *k_cache, void *v_cache, const pa_kv_cache *cache,
+                          const int32_t *block_tables, int32_t max_blocks_per_seq,
+                          const int32_t *seq_lens, int32_t max_seq_len, float scale,
+                          int32_t partition_size, void *workspace,
+                          size_t workspace_bytes, void *out, pa_dtype out_dtype,
+                          pa_stream_t stream);
+
+/*
  * pa_set_decode_kernel -- choose which of the library's two decode kernels
  * pa_decode and pa_decode_noalloc launch from now on (process-wide, any
  * thread, effective from the next call).  The pages describe one decode

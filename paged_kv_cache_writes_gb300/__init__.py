@@ -19,7 +19,7 @@ __all__ = [
     "PA_F16", "PA_BF16", "PA_FP8_E4M3", "PA_F32", "PaError", "PaKvCache", "lib", "kv_cache_desc",
     "pa_reshape_and_cache", "pa_copy_blocks", "pa_decode_workspace_bytes", "pa_decode",
     "pa_prefill_chunk", "pa_get_device_error", "pa_status_string", "pa_selftest_wait_timeout",
-    "BlockManager", "PaBmStats", "pa_set_decode_kernel", "decode_kernel", "DECODE_KERNELS",
+    "BlockManager", "PaBmStats", "pa_set_decode_kernel", "decode_kernel", "DECODE_KERNELS", "pa_decode_write",
 ]
 
 PA_F16, PA_BF16, PA_FP8_E4M3, PA_F32 = 0, 1, 2, 3
@@ -68,6 +68,8 @@ def lib() -> ctypes.CDLL:
         L.pa_decode_workspace_bytes.restype = SZ
         L.pa_decode.argtypes = [P, ctypes.c_int, I32, I32, P, P, ctypes.POINTER(PaKvCache), P, I32, P, I32, F,
                                 I32, P, SZ, P, ctypes.c_int, P]
+        L.pa_decode_write.argtypes = [P, ctypes.c_int, I32, I32, P, P, I64, P, P, P, ctypes.POINTER(PaKvCache), P,
+                                      I32, P, I32, F, I32, P, SZ, P, ctypes.c_int, P]
         L.pa_prefill_chunk.argtypes = [P, ctypes.c_int, P, P, I32, I32, I32, P, P, ctypes.POINTER(PaKvCache), P,
                                        I32, P, I32, F, P, ctypes.c_int, P]
         L.pa_get_device_error.argtypes = [P, ctypes.POINTER(I32)]
@@ -86,6 +88,7 @@ def lib() -> ctypes.CDLL:
         L.pa_bm_block_table.argtypes = [VP, I32, P, I32, ctypes.POINTER(I32), ctypes.POINTER(I32)]
         L.pa_bm_get_stats.argtypes = [VP, ctypes.POINTER(PaBmStats)]
         for name in ("pa_reshape_and_cache", "pa_copy_blocks", "pa_decode", "pa_prefill_chunk", "pa_set_decode_kernel",
+                     "pa_decode_write",
                      "pa_get_device_error", "pa_selftest_wait_timeout", "pa_bm_create", "pa_bm_new_sequence",
                      "pa_bm_fork", "pa_bm_append", "pa_bm_free", "pa_bm_block_table", "pa_bm_get_stats"):
             getattr(L, name).restype = ctypes.c_int
@@ -177,6 +180,27 @@ def pa_decode(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor, cac
                         ctypes.byref(cache), _dev(block_tables, "block_tables"), block_tables.shape[1],
                         _dev(seq_lens, "seq_lens"), int(max_seq_len), float(scale), int(partition_size), ws_ptr,
                         ws_bytes, _dev(out, "out"), _dtype_code(out.dtype), _stream(stream)), "pa_decode")
+
+
+def pa_decode_write(q: torch.Tensor, k_new: torch.Tensor, v_new: torch.Tensor, slot_mapping: torch.Tensor,
+                    k_cache: torch.Tensor, v_cache: torch.Tensor, cache: PaKvCache, block_tables: torch.Tensor,
+                    seq_lens: torch.Tensor, max_seq_len: int, scale: float, out: torch.Tensor,
+                    workspace: torch.Tensor | None = None, partition_size: int = 0, stream=None) -> None:
+    """One decode step: row i of k_new / v_new ([B, Hkv, D], q's dtype, unit inner strides) is written at
+    slot_mapping[i] (int64 [B]; the slot of position seq_lens[i]-1, or negative), then pa_decode."""
+    B, hq, _ = q.shape
+    if k_new.stride()[1:] != (k_new.shape[2], 1) or v_new.stride() != k_new.stride():
+        raise ValueError("k_new and v_new must be [B, Hkv, D] with unit inner strides and equal strides")
+    if slot_mapping.dtype != torch.int64:
+        raise TypeError("slot_mapping must be int64")
+    ws_ptr = _dev(workspace, "workspace")
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    _ok(lib().pa_decode_write(_dev(q, "q"), _dtype_code(q.dtype), B, hq, _dev(k_new, "k_new"), _dev(v_new, "v_new"),
+                              k_new.stride(0), _dev(slot_mapping, "slot_mapping"), _dev(k_cache, "k_cache"),
+                              _dev(v_cache, "v_cache"), ctypes.byref(cache), _dev(block_tables, "block_tables"),
+                              block_tables.shape[1], _dev(seq_lens, "seq_lens"), int(max_seq_len), float(scale),
+                              int(partition_size), ws_ptr, ws_bytes, _dev(out, "out"), _dtype_code(out.dtype),
+                              _stream(stream)), "pa_decode_write")
 
 
 def pa_prefill_chunk(q_chunk: torch.Tensor, cu_q_lens: torch.Tensor, q_start: torch.Tensor, max_q_len: int,

@@ -250,12 +250,23 @@ pa_status pa_set_decode_kernel(int32_t kernel) {
   return PA_OK;
 }
 
-pa_status pa_decode(const void *q, pa_dtype q_dtype, int32_t num_seqs, int32_t num_q_heads,
-                    const void *k_cache, const void *v_cache, const pa_kv_cache *cache,
-                    const int32_t *block_tables, int32_t max_blocks_per_seq,
-                    const int32_t *seq_lens, int32_t max_seq_len, float scale,
-                    int32_t partition_size, void *workspace, size_t workspace_bytes, void *out,
-                    pa_dtype out_dtype, pa_stream_t stream) {
+}  // extern "C"
+
+namespace pa {
+namespace {
+// The new tokens of a fused decode step (pa_decode_write).
+struct NewTokens {
+  const void *k, *v;
+  int64_t stride;
+  const int64_t *slots;
+};
+
+pa_status decode_impl(const void *q, pa_dtype q_dtype, int32_t num_seqs, int32_t num_q_heads,
+                      const void *k_cache, const void *v_cache, const pa_kv_cache *cache,
+                      const int32_t *block_tables, int32_t max_blocks_per_seq, const int32_t *seq_lens,
+                      int32_t max_seq_len, float scale, int32_t partition_size, void *workspace,
+                      size_t workspace_bytes, void *out, pa_dtype out_dtype, pa_stream_t stream,
+                      const NewTokens *nt) {
   pa_status st = check_cache(cache);
   if (st != PA_OK) return st;
   const pa_kv_cache &c = *cache;
@@ -319,6 +330,14 @@ pa_status pa_decode(const void *q, pa_dtype q_dtype, int32_t num_seqs, int32_t n
     tp.k_cache = k_cache;
     tp.v_cache = v_cache;
     tp.s_mult = p.q_mult;
+    tp.k_scale = c.k_scale;
+    tp.v_scale = c.v_scale;
+    if (nt) {
+      tp.k_new = nt->k;
+      tp.v_new = nt->v;
+      tp.new_stride = nt->stride;
+      tp.new_slots = nt->slots;
+    }
     PoolMaps maps{};
     const bool fp8_cache = c.kv_dtype == PA_FP8_E4M3;
     if (fp8_cache ? (!encode_pool_map_fp8_blocks(&maps.k, k_cache, c) || !encode_pool_map_fp8_blocks(&maps.v, v_cache, c))
@@ -330,6 +349,10 @@ pa_status pa_decode(const void *q, pa_dtype q_dtype, int32_t num_seqs, int32_t n
     else e = launch_decode_tc_fp8_f16q(tp, gqa, maps, s);
     return e == cudaSuccess ? PA_OK : PA_ERR_CUDA;
   }
+  if (nt &&   // CUDA-core decode: the cache write is its own launch, just before
+      launch_reshape_and_cache(nt->k, nt->v, q_dtype, num_seqs, nt->stride, nt->slots, const_cast<void *>(k_cache),
+                               const_cast<void *>(v_cache), c, p.err, s) != cudaSuccess)
+    return PA_ERR_CUDA;
   PoolMaps maps;
   if (!encode_pool_map(&maps.k, k_cache, c, true) || !encode_pool_map(&maps.v, v_cache, c, true))
     return PA_ERR_CUDA;
@@ -338,6 +361,40 @@ pa_status pa_decode(const void *q, pa_dtype q_dtype, int32_t num_seqs, int32_t n
   else if (q_dtype == PA_BF16) e = launch_decode_fp8_bf16q(p, hpc, maps, c.head_dim, s);
   else e = launch_decode_fp8_f16q(p, hpc, maps, c.head_dim, s);
   return e == cudaSuccess ? PA_OK : PA_ERR_CUDA;
+}
+}  // namespace
+}  // namespace pa
+
+extern "C" {
+
+pa_status pa_decode(const void *q, pa_dtype q_dtype, int32_t num_seqs, int32_t num_q_heads,
+                    const void *k_cache, const void *v_cache, const pa_kv_cache *cache,
+                    const int32_t *block_tables, int32_t max_blocks_per_seq,
+                    const int32_t *seq_lens, int32_t max_seq_len, float scale,
+                    int32_t partition_size, void *workspace, size_t workspace_bytes, void *out,
+                    pa_dtype out_dtype, pa_stream_t stream) {
+  return decode_impl(q, q_dtype, num_seqs, num_q_heads, k_cache, v_cache, cache, block_tables, max_blocks_per_seq,
+                     seq_lens, max_seq_len, scale, partition_size, workspace, workspace_bytes, out, out_dtype, stream,
+                     nullptr);
+}
+
+pa_status pa_decode_write(const void *q, pa_dtype q_dtype, int32_t num_seqs, int32_t num_q_heads,
+                          const void *k_new, const void *v_new, int64_t token_stride, const int64_t *slot_mapping,
+                          void *k_cache, void *v_cache, const pa_kv_cache *cache, const int32_t *block_tables,
+                          int32_t max_blocks_per_seq, const int32_t *seq_lens, int32_t max_seq_len, float scale,
+                          int32_t partition_size, void *workspace, size_t workspace_bytes, void *out,
+                          pa_dtype out_dtype, pa_stream_t stream) {
+  pa_status st = check_cache(cache);
+  if (st != PA_OK) return st;
+  if (num_seqs > 0) {
+    if (token_stride < (int64_t)cache->num_kv_heads * cache->head_dim || token_stride % 8) return PA_ERR_INVALID_ARG;
+    if (!k_new || !v_new || !slot_mapping || !aligned(k_new, 16) || !aligned(v_new, 16) || !aligned(slot_mapping, 8))
+      return PA_ERR_INVALID_ARG;
+  }
+  const NewTokens nt{k_new, v_new, token_stride, slot_mapping};
+  return decode_impl(q, q_dtype, num_seqs, num_q_heads, k_cache, v_cache, cache, block_tables, max_blocks_per_seq,
+                     seq_lens, max_seq_len, scale, partition_size, workspace, workspace_bytes, out, out_dtype, stream,
+                     &nt);
 }
 
 pa_status pa_prefill_chunk(const void *q_chunk, pa_dtype q_dtype, const int32_t *cu_q_lens,

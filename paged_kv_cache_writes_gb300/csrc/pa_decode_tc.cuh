@@ -79,6 +79,15 @@ struct DecodeTcParams {
   const void *k_cache;       // [num_blocks][Hkv][block_size][128]
   const void *v_cache;
   float s_mult;              // scale * log2(e) (* k_scale for an fp8 cache); any sign
+  // Fused cache write (pa_decode_write), or k_new == nullptr: row i's new token
+  // k_new/v_new[i] ([Hkv][128] in the query dtype, rows new_stride elements
+  // apart) goes to slot new_slots[i] (negative: none), which must be the slot of
+  // position seq_lens[i] - 1; fp8 caches store e4m3(fp32(x) / scale).
+  const void *k_new;
+  const void *v_new;
+  int64_t new_stride;
+  const int64_t *new_slots;
+  float k_scale, v_scale;
 };
 
 namespace dtc {
@@ -564,6 +573,44 @@ __global__ void __launch_bounds__(dtc::Roles<std::is_same<KV, uint8_t>::value>::
     const int bs = p.block_size;
     uint32_t g_load = 0;
     bool ok = true;
+    // Store the new token of unit un's row (K and V of its KV head) in its slot,
+    // the slot of the row's last position (else PA_ERR_DEVICE_CHECK and no
+    // store), then order the stores before the bulk copies that read them.
+    auto write_new = [&](const UnitHdr &un, int ibx) {
+      const int64_t slot = __ldg(tp.new_slots + un.row);
+      if (slot < 0) return;
+      const int pos = un.tok_begin + un.ntok - 1, rel = pos - un.tok_begin;
+      const int32_t bi = reinterpret_cast<const volatile int32_t *>(info[ibx].blk)[8 * (rel >> 7) + ((rel & 127) >> 4)];
+      if (bi < 0 || slot != (int64_t)bi * bs + pos % bs) {
+        if (lane == 0) record_error(p.err, PA_ERR_DEVICE_CHECK);
+        return;
+      }
+      const int64_t row = ((int64_t)bi * hkv + un.kvh) * bs + pos % bs;
+      const int side = lane >> 4, c = lane & 15;   // lanes 0-15: K, 16-31: V; 8 elements each
+      const uint4 x = __ldg(reinterpret_cast<const uint4 *>(
+          static_cast<const QT *>(side ? tp.v_new : tp.k_new) + (int64_t)un.row * tp.new_stride +
+          (int64_t)un.kvh * kD + c * 8));
+      if constexpr (!kFp8) {
+        *reinterpret_cast<uint4 *>(static_cast<QT *>(const_cast<void *>(side ? tp.v_cache : tp.k_cache)) + row * kD +
+                                   c * 8) = x;
+      } else {
+        const float sc = side ? tp.v_scale : tp.k_scale;
+        const uint32_t w[4] = {x.x, x.y, x.z, x.w};
+        uint32_t o[2];
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+          const float2 f = unpack2(w[k], QT{});
+          const uint32_t pair =
+              __nv_cvt_float2_to_fp8x2(make_float2(__fdiv_rn(f.x, sc), __fdiv_rn(f.y, sc)), __NV_SATFINITE, __NV_E4M3);
+          if (k & 1) o[k >> 1] |= pair << 16;
+          else o[k >> 1] = pair;
+        }
+        *reinterpret_cast<uint2 *>(static_cast<uint8_t *>(const_cast<void *>(side ? tp.v_cache : tp.k_cache)) +
+                                   row * kD + c * 8) = make_uint2(o[0], o[1]);
+      }
+      asm volatile("fence.proxy.async;" ::: "memory");   // generic stores -> the async proxy's copies
+      __syncwarp();
+    };
     UnitHdr prev;
     prev.valid = 0;
     for (int u = 0; ok; ++u) {
@@ -572,6 +619,9 @@ __global__ void __launch_bounds__(dtc::Roles<std::is_same<KV, uint8_t>::value>::
       if (!ok) break;
       const UnitHdr cur = read_unit(&info[ib]);
       const int ntc = num_tiles(cur), ntp = num_tiles(prev);
+      // fused write into an empty row: there is no last position to hold the token
+      if (tp.k_new != nullptr && cur.valid && cur.ntok == 0 && lane == 0 && __ldg(tp.new_slots + cur.row) >= 0)
+        record_error(p.err, PA_ERR_DEVICE_CHECK);
       if (cur.valid) {
         // Q^T rows: the G query heads of the KV head, 256 B each
         if (u >= 2) {
@@ -597,6 +647,9 @@ __global__ void __launch_bounds__(dtc::Roles<std::is_same<KV, uint8_t>::value>::
         const bool is_k = i < ntc;
         const UnitHdr &un = is_k ? cur : prev;
         const int j = is_k ? i : i - ntc;
+        // fused write: the row's new token, for this KV head, before the copy of
+        // its last tile (its V tile is copied later still)
+        if (tp.k_new != nullptr && is_k && j == ntc - 1 && un.part == un.nparts - 1) write_new(un, ib);
         const uint32_t ring = kFp8 ? (uint32_t)kStageSlots : (uint32_t)S;
         const int slot = (int)(g_load % ring);
         uint64_t *free_bar = kFp8 ? &stage_free[slot] : &slot_free[slot];

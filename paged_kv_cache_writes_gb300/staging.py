@@ -10,7 +10,7 @@ from __future__ import annotations
 import numpy as np
 import torch
 
-from . import (kv_cache_desc, pa_copy_blocks, pa_decode, pa_decode_workspace_bytes, pa_prefill_chunk,
+from . import (kv_cache_desc, pa_copy_blocks, pa_decode, pa_decode_workspace_bytes, pa_decode_write, pa_prefill_chunk,
                pa_reshape_and_cache)
 
 TORCH_DTYPES = {"f16": torch.float16, "bf16": torch.bfloat16, "fp8": torch.uint8}
@@ -100,6 +100,45 @@ class DeviceBatch:
         if b.num_seqs:
             pa_decode(self.q, self.k_cache, self.v_cache, self.desc, self.block_tables, self.seq_lens,
                       int(b.seq_lens.max()), b.scale, self.out, self.workspace, b.partition_size)
+        return self.out
+
+    def fused_step_tensors(self):
+        """Per-row new tokens for pa_decode_write: row i's step token is the one
+        stored at the slot of its last position (slot -1 and zeros for a row
+        without one).  Raises if the step writes anything else."""
+        b = self.b
+        if getattr(self, "_fused", None) is None:
+            if b.step_write is None:
+                raise ValueError("no step write")
+            sw = b.step_write
+            by_slot = {int(s): t for t, s in enumerate(sw.slots)}
+            k = np.zeros((b.num_seqs,) + sw.k.shape[1:], dtype=sw.k.dtype)
+            v = np.zeros_like(k)
+            slots = np.full(b.num_seqs, -1, dtype=np.int64)
+            used = 0
+            for i, L in enumerate(b.seq_lens):
+                if L <= 0:
+                    continue
+                s_last = int(b.block_tables[i][(L - 1) // b.block_size]) * b.block_size + (L - 1) % b.block_size
+                t = by_slot.get(s_last)
+                if t is None:
+                    continue
+                k[i], v[i], slots[i] = sw.k[t], sw.v[t], s_last
+                used += 1
+            if used != len(sw.slots):
+                raise ValueError("the step writes tokens other than the rows' last positions")
+            self._fused = (to_device(k, b.src_dtype, self.device), to_device(v, b.src_dtype, self.device),
+                           torch.from_numpy(slots).to(self.device))
+        return self._fused
+
+    def decode_write(self) -> torch.Tensor:
+        """The decode step as one call: the step's new tokens written, then attention (pa_decode_write)."""
+        b = self.b
+        k, v, slots = self.fused_step_tensors()
+        if b.num_seqs:
+            pa_decode_write(self.q, k, v, slots, self.k_cache, self.v_cache, self.desc, self.block_tables,
+                            self.seq_lens, int(b.seq_lens.max()), b.scale, self.out, self.workspace,
+                            b.partition_size)
         return self.out
 
     def prefill_chunk(self) -> torch.Tensor:
