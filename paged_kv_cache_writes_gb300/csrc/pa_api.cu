@@ -174,7 +174,9 @@ WorkspaceLayout decode_workspace_layout(int64_t rows, int64_t num_q_heads, int64
   const int64_t partials = max_partitions > 1 ? rows * num_q_heads * max_partitions : 0;
   w.ml_off = w.acc_off + round256((size_t)(partials * head_dim * 4));
   w.cnt_off = w.ml_off + round256((size_t)(partials * 8));
-  w.total = w.cnt_off + round256((size_t)(rows * num_q_heads * 4));
+  w.jobs_off = w.cnt_off + round256((size_t)(rows * num_q_heads * 4));
+  // merge list of the tensor-core decode (split rows only)
+  w.total = w.jobs_off + round256((size_t)(max_partitions > 1 ? rows * num_q_heads * 16 : 0));
   return w;
 }
 
@@ -332,6 +334,7 @@ pa_status decode_impl(const void *q, pa_dtype q_dtype, int32_t num_seqs, int32_t
     tp.s_mult = p.q_mult;
     tp.k_scale = c.k_scale;
     tp.v_scale = c.v_scale;
+    tp.jobs = reinterpret_cast<DecodeMergeJob *>(ws + w.jobs_off);
     if (nt) {
       tp.k_new = nt->k;
       tp.v_new = nt->v;

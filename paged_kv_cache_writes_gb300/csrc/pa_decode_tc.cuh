@@ -59,7 +59,8 @@
 //    the block ids of its tiles, in a ring of four descriptors, so the chain
 //    of dependent reads behind a claim (cursor, work item, sequence length,
 //    block table) runs ahead of the loads instead of between them;
-//  * merge warp: merges split rows queued by the softmax warps.
+//  * merge warp: merges split rows taken from a grid-wide list that the
+//    softmax warps append to, so the merging is shared by every CTA.
 //
 // Every mbarrier wait is bounded (PA_ERR_TIMEOUT, after which the CTA
 // abandons its work); tensor memory is freed only after every issued MMA has
@@ -74,8 +75,16 @@
 
 namespace pa {
 
+// A split row (sequence, KV head) whose partitions are all written, in the
+// workspace's merge list; ready is set (release) once the record is complete.
+struct DecodeMergeJob {
+  int32_t row, kvh, nparts, ready;
+};
+
 struct DecodeTcParams {
   DecodeParams d;            // shapes, plan and workspace (d.groups = 1: a unit serves all G heads)
+  DecodeMergeJob *jobs;      // merge list, one record per split (row, KV head); d.hdr->pad[0..2]:
+                             // records appended, records claimed, records in all
   const void *k_cache;       // [num_blocks][Hkv][block_size][128]
   const void *v_cache;
   float s_mult;              // scale * log2(e) (* k_scale for an fp8 cache); any sign
@@ -119,12 +128,7 @@ struct Roles {
   static constexpr int kMergeWarp = kSchedWarp + 1;
   static constexpr int kThreads = (kMergeWarp + 1) * 32;
 };
-constexpr int kJobs = 32;                 // merge jobs queued
 
-// A split row's (sequence, KV head) whose partitions are all written; row -1 ends the queue.
-struct MergeJob {
-  int32_t row, kvh, nparts, pad;
-};
 constexpr int kMaxSlots = 8;
 
 // A claimed unit as published by the scheduler warp: its place, and the
@@ -146,13 +150,12 @@ struct TcGeo {
   static constexpr int kPBytes = 2 * kNO * 128;             // P^T of a tile: 2 panels (64 keys) x kNO rows
   static constexpr int kColO = 2 * kMaxTiles * kNS;         // tensor-memory column of O^T, buffer 0
   static constexpr int kTmemCols = 256;                     // 128 S^T + 2 * kNO O^T columns, rounded up
-  static constexpr int kNumBars = 2 * kMaxSlots + 8 * 2 + 2 * kInfo + kJobs + 1 + 2 * kStageSlots + 2;
+  static constexpr int kNumBars = 2 * kMaxSlots + 8 * 2 + 2 * kInfo + 1 + 2 * kStageSlots + 2;
   static constexpr int kOffQ = 0;                                        // [2] Q^T
   static constexpr int kOffP = kOffQ + 2 * kQBytes;                      // [2][4] P^T
   static constexpr int kOffRed = kOffP + 2 * kMaxTiles * kPBytes;        // float [2][4 warps][2][16]
   static constexpr int kOffInfo = kOffRed + 2 * 4 * 2 * 16 * 4;          // TcUnit [kInfo] (16-byte aligned)
-  static constexpr int kOffJobs = kOffInfo + kInfo * (int)sizeof(TcUnit);   // MergeJob [kJobs]
-  static constexpr int kOffBar = kOffJobs + kJobs * (int)sizeof(MergeJob);
+  static constexpr int kOffBar = kOffInfo + kInfo * (int)sizeof(TcUnit);
   static constexpr int kOffMisc = kOffBar + kNumBars * 8;
   static constexpr int kOffQraw = (kOffMisc + 64 + 15) / 16 * 16;        // fp8: [2] the G query rows as given
   static constexpr int kOffStage = (kOffQraw + (kFp8 ? 2 * G * kD * 2 : 0) + 1023) / 1024 * 1024;  // fp8: raw tiles
@@ -278,19 +281,14 @@ __global__ void __launch_bounds__(dtc::Roles<std::is_same<KV, uint8_t>::value>::
   uint64_t *red_bar = o_free + 2;             // [2] per-warp maxima and sums exchanged (128)
   uint64_t *info_full = red_bar + 2;          // [kInfo] unit descriptor published
   uint64_t *info_free = info_full + kInfo;    // [kInfo] released by the MMA warp and the softmax warps
-  uint64_t *job_full = info_free + kInfo;     // [kJobs] merge job queued
-  uint64_t *fin = job_full + kJobs;           // every MMA of the CTA complete
+  uint64_t *fin = info_free + kInfo;          // every MMA of the CTA complete
   uint64_t *stage_full = fin + 1;             // fp8 [kStageSlots] raw tile copied
   uint64_t *stage_free = stage_full + kStageSlots;   // fp8 [kStageSlots] widened (every widening thread)
   uint64_t *qraw_full = stage_free + kStageSlots;     // fp8 [2] query rows copied (loader lanes)
-  MergeJob *jobs = reinterpret_cast<MergeJob *>(smem + GE::kOffJobs);
   TcUnit *info = reinterpret_cast<TcUnit *>(smem + GE::kOffInfo);
   float *red = reinterpret_cast<float *>(smem + GE::kOffRed);
   uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + GE::kOffMisc);
   volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + GE::kOffMisc + 8);
-  int *job_ticket = reinterpret_cast<int *>(smem + GE::kOffMisc + 16);      // next merge job's queue position
-  int *softmax_done = reinterpret_cast<int *>(smem + GE::kOffMisc + 20);    // softmax warps finished
-  volatile int *jobs_taken = reinterpret_cast<volatile int *>(smem + GE::kOffMisc + 24);  // read by the merge warp
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
 
@@ -316,7 +314,6 @@ __global__ void __launch_bounds__(dtc::Roles<std::is_same<KV, uint8_t>::value>::
       mbar_init(&info_full[i], 1);
       mbar_init(&info_free[i], 2);
     }
-    for (int i = 0; i < kJobs; ++i) mbar_init(&job_full[i], 1);
     mbar_init(fin, 1);
     for (int i = 0; i < kStageSlots; ++i) {
       mbar_init(&stage_full[i], 1);
@@ -324,9 +321,6 @@ __global__ void __launch_bounds__(dtc::Roles<std::is_same<KV, uint8_t>::value>::
     }
     for (int i = 0; i < 2; ++i) mbar_init(&qraw_full[i], 32);
     *abort_flag = 0;
-    *job_ticket = 0;
-    *softmax_done = 0;
-    *jobs_taken = 0;
     fence_mbar_init();
     prefetch_tensor_map(&tmap_k);
     prefetch_tensor_map(&tmap_v);
@@ -341,6 +335,9 @@ __global__ void __launch_bounds__(dtc::Roles<std::is_same<KV, uint8_t>::value>::
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
+  // launched as the plan kernel's programmatic dependent: everything above overlapped it;
+  // its work list, cursor and counters are complete and visible after this
+  asm volatile("griddepcontrol.wait;" ::: "memory");
   auto col_s = [&](int b, int j) { return tmem + (uint32_t)((b * kMaxTiles + j) * kNS); };
   auto col_o = [&](int b) { return tmem + (uint32_t)(GE::kColO + b * kNO); };
   auto wait_all = [&](uint64_t *bar, uint32_t parity) {
@@ -370,29 +367,17 @@ __global__ void __launch_bounds__(dtc::Roles<std::is_same<KV, uint8_t>::value>::
     // in one epilogue (pending), reported in the next (fence, then one count per
     // warp on the row's counter: by then the fence finds the writes done), and
     // the count returned is checked in the one after (reported); the warp that
-    // brings a row's count to 4 * nparts queues the row for the merge warp.
+    // brings a row's count to 4 * nparts appends it to the merge list.
     int pend_row = -1, pend_kvh = 0, pend_np = 0;
     int rep_row = -1, rep_kvh = 0, rep_np = 0, rep_old = 0;
-    // queue a merge job (one thread): its slot is free once the merge warp has
-    // read job t - kJobs (bounded wait)
+    // append a merge record (one thread); any CTA's merge warp may take it
     auto queue_job = [&](int row, int kvh, int np) {
-      const int t = atomicAdd(job_ticket, 1);
-      if (*jobs_taken <= t - kJobs) {
-        const uint64_t t0 = global_timer_ns();
-        while (*jobs_taken <= t - kJobs) {
-          if (*abort_flag) return;
-          if (global_timer_ns() - t0 > kWaitLimitNs) {
-            record_error(p.err, PA_ERR_TIMEOUT);
-            *abort_flag = 1;
-            return;
-          }
-        }
-      }
-      MergeJob *j = &jobs[t % kJobs];
+      const int t = atomicAdd(&p.hdr->pad[0], 1);
+      DecodeMergeJob *j = tp.jobs + t;
       j->row = row;
       j->kvh = kvh;
       j->nparts = np;
-      mbar_arrive(&job_full[t % kJobs]);
+      asm volatile("st.release.gpu.global.b32 [%0], %1;" ::"l"(&j->ready), "r"(1) : "memory");
     };
     auto check_reported = [&]() {
       if (rep_row >= 0) {
@@ -561,8 +546,6 @@ __global__ void __launch_bounds__(dtc::Roles<std::is_same<KV, uint8_t>::value>::
       check_reported();
       report_pending();
       check_reported();
-      // the last softmax warp to finish ends the merge queue (after every job of every warp)
-      if (lane == 0 && atomicAdd(softmax_done, 1) == 3) queue_job(-1, 0, 0);
     }
   } else if (warp == kLoadWarp) {
     // ===================================================== loader (one warp)
@@ -832,14 +815,40 @@ __global__ void __launch_bounds__(dtc::Roles<std::is_same<KV, uint8_t>::value>::
     // out = sum_p 2^(m_p - M) acc_p / sum_p 2^(m_p - M) l_p over a split row's
     // partitions p (m_p in log2 units, M their maximum), kept as a running
     // maximum; lane l merges elements 4l..4l+3 of all G heads, the loads of a
-    // partition for every head in flight together.
-    for (int t = 0;; ++t) {
-      if (!wait_all(&job_full[t % kJobs], (t / kJobs) & 1)) break;
-      const volatile MergeJob *jv = &jobs[t % kJobs];
-      const int job_row = jv->row, job_kvh = jv->kvh, job_np = jv->nparts;
-      __syncwarp();
-      if (lane == 0) *jobs_taken = t + 1;   // the slot may be refilled
-      if (job_row < 0) break;
+    // partition for every head in flight together.  Records are taken from the
+    // grid-wide merge list in the order they were appended, so every CTA's
+    // merge warp shares the merging; taking record t waits (bounded) for it.
+    const int total_jobs = __ldcg(&p.hdr->pad[2]);
+    for (;;) {
+      int t = 0;
+      if (lane == 0) t = atomicAdd(&p.hdr->pad[1], 1);
+      t = __shfl_sync(0xffffffffu, t, 0);
+      if (t >= total_jobs) break;
+      int ready = 0;
+      if (lane == 0) {
+        const uint64_t t0 = global_timer_ns();
+        for (;;) {
+          asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(ready) : "l"(&tp.jobs[t].ready) : "memory");
+          if (ready || *abort_flag) break;
+          if (global_timer_ns() - t0 > kWaitLimitNs) {
+            record_error(p.err, PA_ERR_TIMEOUT);
+            *abort_flag = 1;
+            break;
+          }
+          __nanosleep(256);
+        }
+      }
+      int job_row = 0, job_kvh = 0, job_np = 0;
+      if (lane == 0 && ready) {   // read by the lane that acquired the record, then broadcast
+        const volatile DecodeMergeJob *jv = tp.jobs + t;
+        job_row = jv->row;
+        job_kvh = jv->kvh;
+        job_np = jv->nparts;
+      }
+      if (!__shfl_sync(0xffffffffu, ready, 0)) break;
+      job_row = __shfl_sync(0xffffffffu, job_row, 0);
+      job_kvh = __shfl_sync(0xffffffffu, job_kvh, 0);
+      job_np = __shfl_sync(0xffffffffu, job_np, 0);
       __threadfence();
       const int64_t head0 = (int64_t)job_row * hq + (int64_t)job_kvh * G;
       float m[G], l[G];
@@ -1009,7 +1018,8 @@ __global__ void __launch_bounds__(dtc::Roles<std::is_same<KV, uint8_t>::value>::
   }
 }
 
-// One CTA: list the (row, partition) items -- rows with the most partitions
+// One CTA: count the split rows' merges and clear the merge list, and list
+// the (row, partition) items -- rows with the most partitions
 // first, then the single-partition rows by their number of 128-key tiles
 // (a counting sort; rows of equal key in any order), each row's partitions
 // together and in order -- and reset the scheduling cursor and the split
@@ -1017,15 +1027,21 @@ __global__ void __launch_bounds__(dtc::Roles<std::is_same<KV, uint8_t>::value>::
 // shorter ones still run, and the smallest units come last, which evens out
 // the CTAs' finishing times.  An empty row lists one item of zero tokens.
 template <int kUnused>
-__global__ void __launch_bounds__(1024) decode_tc_plan_kernel(DecodeParams p) {
+__global__ void __launch_bounds__(1024) decode_tc_plan_kernel(DecodeParams p, DecodeMergeJob *jobs) {
+  // the decode grid may launch now: it sets itself up, then waits for this grid
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   // sort key 0 .. maxp + 3: 3 + nparts for a split row, else its tiles (0 .. 4);
   // base[maxp + 3 - key]: items of the key (descending), then its next free item
   __shared__ int base[kMaxPartitions + 4];
   const int tid = threadIdx.x;
   const int maxp = p.max_partitions;
   const int nkeys = maxp + 4;
+  __shared__ int split_rows;
   for (int64_t i = tid; i < (int64_t)p.num_seqs * p.num_q_heads; i += blockDim.x) p.ws_count[i] = 0;
+  if (p.max_partitions > 1)   // the merge list exists only when a row can be split
+    for (int64_t i = tid; i < (int64_t)p.num_seqs * p.num_kv_heads; i += blockDim.x) jobs[i].ready = 0;
   for (int i = tid; i < nkeys; i += blockDim.x) base[i] = 0;
+  if (tid == 0) split_rows = 0;
   __syncthreads();
   auto len_of = [&](int r, bool report) { return checked_len(p, r, report); };
   auto nparts_of = [&](int L) { return max(1, (L + p.partition_size - 1) / p.partition_size); };
@@ -1033,6 +1049,7 @@ __global__ void __launch_bounds__(1024) decode_tc_plan_kernel(DecodeParams p) {
   for (int r = tid; r < p.num_seqs; r += blockDim.x) {
     const int L = len_of(r, true), np = nparts_of(L);
     atomicAdd(&base[slot_of(L, np)], np);
+    if (np > 1) atomicAdd(&split_rows, 1);
   }
   __syncthreads();
   if (tid == 0) {   // exclusive scan (a small serial pass)
@@ -1044,6 +1061,9 @@ __global__ void __launch_bounds__(1024) decode_tc_plan_kernel(DecodeParams p) {
     }
     p.hdr->num_items = run;
     p.hdr->next_unit = 0;
+    p.hdr->pad[0] = 0;                              // merge records appended
+    p.hdr->pad[1] = 0;                              // merge records taken
+    p.hdr->pad[2] = split_rows * p.num_kv_heads;    // one per split (row, KV head)
   }
   __syncthreads();
   for (int r = tid; r < p.num_seqs; r += blockDim.x) {
@@ -1053,19 +1073,30 @@ __global__ void __launch_bounds__(1024) decode_tc_plan_kernel(DecodeParams p) {
   }
 }
 
-// Host launcher: the plan kernel, then one persistent CTA per SM.
+// Host launcher: the plan kernel, then one persistent CTA per SM launched as its
+// programmatic dependent.
 template <typename KV, typename QT, int G>
 cudaError_t launch_decode_tc_one(const DecodeTcParams &p, const PoolMaps &m, cudaStream_t s) {
   constexpr bool kSplit = std::is_same<QT, __nv_bfloat16>::value && !std::is_same<KV, uint8_t>::value;
   constexpr int smem = dtc::TcGeo<G, kSplit, std::is_same<KV, uint8_t>::value>::kSmemBytes;
-  decode_tc_plan_kernel<0><<<1, 1024, 0, s>>>(p.d);
+  decode_tc_plan_kernel<0><<<1, 1024, 0, s>>>(p.d, p.jobs);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   if ((e = ensure_smem_limit<decode_tc_kernel<KV, QT, G>>(smem)) != cudaSuccess) return e;
   int sms = 0;
   if ((e = current_sm_count(&sms)) != cudaSuccess) return e;
-  decode_tc_kernel<KV, QT, G><<<sms, dtc::Roles<std::is_same<KV, uint8_t>::value>::kThreads, smem, s>>>(p, m.k, m.v);
-  return cudaGetLastError();
+  // programmatic dependent launch: the decode grid's set-up overlaps the plan kernel
+  cudaLaunchConfig_t cfg{};
+  cfg.gridDim = dim3((unsigned)sms);
+  cfg.blockDim = dim3(dtc::Roles<std::is_same<KV, uint8_t>::value>::kThreads);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, decode_tc_kernel<KV, QT, G>, p, m.k, m.v);
 }
 
 // m: tensor maps over the pools, one box per cache block of one KV head: 16-bit

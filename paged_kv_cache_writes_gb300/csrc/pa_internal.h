@@ -85,7 +85,7 @@ struct AttnParams {
 
 // Decode workspace: header | item list | split-KV partials (acc, max/sum) | counters.
 struct WorkspaceLayout {
-  size_t hdr_off, items_off, acc_off, ml_off, cnt_off, total;
+  size_t hdr_off, items_off, acc_off, ml_off, cnt_off, jobs_off, total;
 };
 WorkspaceLayout decode_workspace_layout(int64_t rows, int64_t num_q_heads, int64_t head_dim,
                                         int64_t max_partitions);

@@ -145,7 +145,8 @@ def test_workspace_size(lib):
     items = 256 * parts * 4
     acc = 256 * 64 * parts * 128 * 4
     ml = 256 * 64 * parts * 8
-    assert n == hdr + items + acc + ml + cnt                                  # all multiples of 256
+    jobs = 256 * 64 * 16                                                      # merge list (split rows)
+    assert n == hdr + items + acc + ml + cnt + jobs                           # all multiples of 256
     assert pa.pa_decode_workspace_bytes(256, 64, 8, 128, 8192, 2048) == n     # partitions above 512 act as 512
     assert pa.pa_decode_workspace_bytes(4, 30, 8, 128, 8192, 0) == 0         # invalid -> 0
     assert pa.pa_decode_workspace_bytes(4, 32, 8, 128, 8192, 48) == 0
