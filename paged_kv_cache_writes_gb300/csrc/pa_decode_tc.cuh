@@ -835,7 +835,7 @@ __global__ void __launch_bounds__(dtc::Roles<std::is_same<KV, uint8_t>::value>::
             *abort_flag = 1;
             break;
           }
-          __nanosleep(256);
+          __nanosleep(2000);
         }
       }
       int job_row = 0, job_kvh = 0, job_np = 0;
