@@ -64,13 +64,13 @@ def _load():
         lib.or_e4m3_to_double.restype = ctypes.c_double
         lib.or_e4m3_encode.argtypes = [ctypes.c_float]
         lib.or_e4m3_encode.restype = ctypes.c_uint8
-        lib.or_reshape_and_cache.argtypes = [P, P, I, I64, I64, P, P, P, I64, I, I, I, I, F, F]
+        lib.or_reshape_and_cache.argtypes = [P, P, I, I64, I64, P, P, P, I64, I, I, I, I, P, P]
         lib.or_reshape_and_cache.restype = I
         lib.or_copy_blocks.argtypes = [P, P, I64, I64, P, I64]
         lib.or_copy_blocks.restype = I
-        lib.or_decode.argtypes = [P, I, I, I, P, P, I64, I, I, I, I, F, F, P, I, P, F, P, I, P]
+        lib.or_decode.argtypes = [P, I, I, I, P, P, I64, I, I, I, I, P, P, P, I, P, F, P, I, P]
         lib.or_decode.restype = I
-        lib.or_prefill.argtypes = [P, I, P, P, I, I, P, P, I64, I, I, I, I, F, F, P, I, F, P]
+        lib.or_prefill.argtypes = [P, I, P, P, I, I, P, P, I64, I, I, I, I, P, P, P, I, F, P]
         lib.or_prefill.restype = I
         lib.or_max_threads.restype = I
         lib.or_set_threads.argtypes = [I]
@@ -120,12 +120,22 @@ def e4m3_encode(x: np.ndarray) -> np.ndarray:
     return np.array([lib.or_e4m3_encode(float(v)) for v in flat], dtype=np.uint8).reshape(np.shape(x))
 
 
+def _scales(x, hkv: int) -> np.ndarray:
+    """fp8 scales as one fp32 value per KV head: a per-tensor scale is the same for every head."""
+    a = np.asarray(x, dtype=np.float32).reshape(-1)
+    if a.size == 1:
+        a = np.full(hkv, a[0], dtype=np.float32)
+    assert a.shape == (hkv,), "one scale, or one per KV head"
+    return np.ascontiguousarray(a)
+
+
 # -------------------------------------------------------------- cache write
 def reshape_and_cache(k: np.ndarray, v: np.ndarray, in_dtype: int, slot_mapping: np.ndarray,
                       k_cache: np.ndarray, v_cache: np.ndarray, kv_dtype: int,
-                      k_scale: float = 1.0, v_scale: float = 1.0) -> None:
+                      k_scale=1.0, v_scale=1.0) -> None:
     """Write tokens into the pools in place.  k, v: [T, Hkv, d] bits (token
-    stride = Hkv*d); pools: [NB, Hkv, bs, d] bits; slot_mapping int64 [T]."""
+    stride = Hkv*d); pools: [NB, Hkv, bs, d] bits; slot_mapping int64 [T];
+    k_scale / v_scale: one fp8 scale, or one per KV head."""
     lib = _load()
     T, hkv, d = k.shape
     nb, hkv2, bs, d2 = k_cache.shape
@@ -133,9 +143,10 @@ def reshape_and_cache(k: np.ndarray, v: np.ndarray, in_dtype: int, slot_mapping:
     assert k.dtype == np.uint16 and k_cache.dtype == _bits_dtype(kv_dtype)
     slots = np.ascontiguousarray(slot_mapping, dtype=np.int64)
     assert slots.shape == (T,)
+    ks, vs = _scales(k_scale, hkv), _scales(v_scale, hkv)
     _check(lib.or_reshape_and_cache(_ptr(k), _ptr(v), in_dtype, T, hkv * d, _ptr(slots),
                                     _ptr(k_cache), _ptr(v_cache), nb, bs, hkv, d, kv_dtype,
-                                    float(k_scale), float(v_scale)), "reshape_and_cache")
+                                    _ptr(ks), _ptr(vs)), "reshape_and_cache")
 
 
 def copy_blocks(k_cache: np.ndarray, v_cache: np.ndarray, pairs: np.ndarray) -> None:
@@ -151,7 +162,7 @@ def copy_blocks(k_cache: np.ndarray, v_cache: np.ndarray, pairs: np.ndarray) -> 
 # ---------------------------------------------------------------- attention
 def decode(q: np.ndarray, q_dtype: int, k_cache: np.ndarray, v_cache: np.ndarray, kv_dtype: int,
            block_tables: np.ndarray, seq_lens: np.ndarray, scale: float,
-           k_scale: float = 1.0, v_scale: float = 1.0, seq_ids=None) -> np.ndarray:
+           k_scale=1.0, v_scale=1.0, seq_ids=None) -> np.ndarray:
     """Paged decode in fp64.  q: [B, Hq, d] bits.  Returns float64 [B, Hq, d];
     with ``seq_ids`` only those sequences are evaluated (other rows are NaN)."""
     lib = _load()
@@ -162,15 +173,16 @@ def decode(q: np.ndarray, q_dtype: int, k_cache: np.ndarray, v_cache: np.ndarray
     sl = np.ascontiguousarray(seq_lens, dtype=np.int32)
     out = np.full((B, hq, d), np.nan)
     ids = None if seq_ids is None else np.ascontiguousarray(seq_ids, dtype=np.int32)
+    ks, vs = _scales(k_scale, hkv), _scales(v_scale, hkv)
     _check(lib.or_decode(_ptr(q), q_dtype, B, hq, _ptr(k_cache), _ptr(v_cache), nb, bs, hkv, d,
-                         kv_dtype, float(k_scale), float(v_scale), _ptr(bt), bt.shape[1], _ptr(sl),
+                         kv_dtype, _ptr(ks), _ptr(vs), _ptr(bt), bt.shape[1], _ptr(sl),
                          float(scale), _ptr(ids), 0 if ids is None else len(ids), _ptr(out)), "decode")
     return out
 
 
 def prefill(q: np.ndarray, q_dtype: int, cu_q_lens: np.ndarray, q_start: np.ndarray,
             k_cache: np.ndarray, v_cache: np.ndarray, kv_dtype: int, block_tables: np.ndarray,
-            scale: float, k_scale: float = 1.0, v_scale: float = 1.0) -> np.ndarray:
+            scale: float, k_scale=1.0, v_scale=1.0) -> np.ndarray:
     """Chunked prefill in fp64.  q: [total_q, Hq, d] bits.  Returns float64."""
     lib = _load()
     total, hq, d = q.shape
@@ -181,8 +193,9 @@ def prefill(q: np.ndarray, q_dtype: int, cu_q_lens: np.ndarray, q_start: np.ndar
     bt = np.ascontiguousarray(block_tables, dtype=np.int32)
     assert cu[-1] == total and len(cu) == len(qs) + 1
     out = np.full((total, hq, d), np.nan)
+    ks, vs = _scales(k_scale, hkv), _scales(v_scale, hkv)
     _check(lib.or_prefill(_ptr(q), q_dtype, _ptr(cu), _ptr(qs), len(qs), hq, _ptr(k_cache),
-                          _ptr(v_cache), nb, bs, hkv, d, kv_dtype, float(k_scale), float(v_scale),
+                          _ptr(v_cache), nb, bs, hkv, d, kv_dtype, _ptr(ks), _ptr(vs),
                           _ptr(bt), bt.shape[1], float(scale), _ptr(out)), "prefill")
     return out
 

@@ -156,13 +156,15 @@ static double elem(const void *base, int64_t idx, int dtype, float scale)
  * (the address arithmetic of PagedKVCacheManager.allocate_slot in "Inside
  * vLLM Architecture", section "The Block Table Mapping Subsystem").  A cache
  * of the input dtype receives the bits unchanged; an fp8 cache receives
- * e4m3(fp32(x) / scale) with an IEEE fp32 division. */
+ * e4m3(fp32(x) / scale) with an IEEE fp32 division, scale = k_scales[h]
+ * (resp. v_scales[h]) for KV head h: one value per head, or the same value
+ * for every head when the cache has one scale per tensor. */
 int or_reshape_and_cache(const void *k, const void *v, int in_dtype,
                          int64_t num_tokens, int64_t token_stride,
                          const int64_t *slot_mapping, void *k_cache,
                          void *v_cache, int64_t num_blocks, int block_size,
                          int num_kv_heads, int head_dim, int kv_dtype,
-                         float k_scale, float v_scale)
+                         const float *k_scales, const float *v_scales)
 {
     int64_t t;
     if (in_dtype != OR_F16 && in_dtype != OR_BF16)
@@ -181,9 +183,9 @@ int or_reshape_and_cache(const void *k, const void *v, int in_dtype,
         for (side = 0; side < 2; ++side) {
             const uint16_t *src = (const uint16_t *)(side ? v : k);
             void *dst = side ? v_cache : k_cache;
-            float sc = side ? v_scale : k_scale;
             for (h = 0; h < num_kv_heads; ++h)
                 for (e = 0; e < head_dim; ++e) {
+                    float sc = side ? v_scales[h] : k_scales[h];
                     int64_t si = t * token_stride + (int64_t)h * head_dim + e;
                     int64_t di = ((blk * num_kv_heads + h) * block_size + off) *
                                      head_dim + e;
@@ -278,7 +280,7 @@ static void attend(const double *qrow, const double *K, const double *V,
 int or_decode(const void *q, int q_dtype, int num_seqs, int num_q_heads,
               const void *k_cache, const void *v_cache, int64_t num_blocks,
               int block_size, int num_kv_heads, int head_dim, int kv_dtype,
-              float k_scale, float v_scale, const int32_t *block_tables,
+              const float *k_scales, const float *v_scales, const int32_t *block_tables,
               int max_blocks_per_seq, const int32_t *seq_lens, float scale,
               const int32_t *seq_ids, int num_ids, double *out)
 {
@@ -306,11 +308,11 @@ int or_decode(const void *q, int q_dtype, int num_seqs, int num_q_heads,
         if (!K || !V || !s || !qrow) {
 #pragma omp atomic write
             err = OR_ERR_NOMEM;
-        } else if (gather(k_cache, kv_dtype, k_scale, num_blocks, block_size,
+        } else if (gather(k_cache, kv_dtype, k_scales[g], num_blocks, block_size,
                           num_kv_heads, head_dim,
                           block_tables + (int64_t)i * max_blocks_per_seq, g, L,
                           K) ||
-                   gather(v_cache, kv_dtype, v_scale, num_blocks, block_size,
+                   gather(v_cache, kv_dtype, v_scales[g], num_blocks, block_size,
                           num_kv_heads, head_dim,
                           block_tables + (int64_t)i * max_blocks_per_seq, g, L,
                           V)) {
@@ -342,7 +344,7 @@ int or_prefill(const void *q, int q_dtype, const int32_t *cu_q_lens,
                const int32_t *q_start, int num_chunks, int num_q_heads,
                const void *k_cache, const void *v_cache, int64_t num_blocks,
                int block_size, int num_kv_heads, int head_dim, int kv_dtype,
-               float k_scale, float v_scale, const int32_t *block_tables,
+               const float *k_scales, const float *v_scales, const int32_t *block_tables,
                int max_blocks_per_seq, float scale, double *out)
 {
     int G, err = OR_OK;
@@ -369,11 +371,11 @@ int or_prefill(const void *q, int q_dtype, const int32_t *cu_q_lens,
         if (!K || !V || !s || !qrow) {
 #pragma omp atomic write
             err = OR_ERR_NOMEM;
-        } else if (gather(k_cache, kv_dtype, k_scale, num_blocks, block_size,
+        } else if (gather(k_cache, kv_dtype, k_scales[g], num_blocks, block_size,
                           num_kv_heads, head_dim,
                           block_tables + (int64_t)c * max_blocks_per_seq, g,
                           ctx, K) ||
-                   gather(v_cache, kv_dtype, v_scale, num_blocks, block_size,
+                   gather(v_cache, kv_dtype, v_scales[g], num_blocks, block_size,
                           num_kv_heads, head_dim,
                           block_tables + (int64_t)c * max_blocks_per_seq, g,
                           ctx, V)) {

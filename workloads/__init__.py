@@ -131,8 +131,8 @@ class PagedBatch:
     setup: list = field(default_factory=list)   # WriteOp / CopyOp run before the step
     step_write: WriteOp | None = None           # new tokens written inside the step
     prefill: PrefillPart | None = None
-    k_scale: float = 1.0
-    v_scale: float = 1.0
+    k_scale: float | np.ndarray = 1.0   # fp8: one scale, or fp32 [Hkv] (one per KV head)
+    v_scale: float | np.ndarray = 1.0
     partition_size: int = 0  # 0 = let the library choose
     blocks_unshared: int = 0  # physical blocks the same batch needs without sharing
 
@@ -202,7 +202,7 @@ def _tables(rows: list, pad: int) -> np.ndarray:
 def decode_batch(name: str, lens, num_q_heads: int, num_kv_heads: int, head_dim: int, block_size: int,
                  src_dtype: str, kv_dtype: str | None = None, seed: int = 0, layout_seed: int | None = None,
                  num_blocks: int | None = None, partition_size: int = 0,
-                 scale: float | None = None) -> PagedBatch:
+                 scale: float | None = None, fp8_scales: str = "tensor") -> PagedBatch:
     """A decode batch: sequence i has ``lens[i]`` tokens, the last of which is
     the new token written inside the step; the others are existing context.
 
@@ -231,7 +231,7 @@ def decode_batch(name: str, lens, num_q_heads: int, num_kv_heads: int, head_dim:
     is_new[(starts + lens - 1)[lens > 0]] = True
     ctx = WriteOp(k_all[~is_new], v_all[~is_new], slots[~is_new])
     new = WriteOp(k_all[is_new], v_all[is_new], slots[is_new])
-    ks, vs = _fp8_scales([k_all], [v_all], src_dtype) if kv_dtype == "fp8" else (1.0, 1.0)
+    ks, vs = _fp8_scales([k_all], [v_all], src_dtype, fp8_scales == "head") if kv_dtype == "fp8" else (1.0, 1.0)
     return PagedBatch(name=name, num_q_heads=num_q_heads, num_kv_heads=num_kv_heads, head_dim=head_dim,
                       block_size=bs, src_dtype=src_dtype, kv_dtype=kv_dtype, num_blocks=nb, pad_block=pool.pad,
                       block_tables=bt, seq_lens=lens.astype(np.int32), q=q,
@@ -250,12 +250,18 @@ def _amax(bits: np.ndarray, src_dtype: str) -> np.float32:
     return bits_to_f32(np.array([m], np.uint16), src_dtype)[0]
 
 
-def _fp8_scales(k_parts, v_parts, src_dtype: str):
-    """Per-tensor scales amax(|x|) / 448 in fp32 (448 = largest E4M3 magnitude),
-    the amax taken over every token of the tensor (given as a list of parts)."""
+def _fp8_scales(k_parts, v_parts, src_dtype: str, per_head: bool = False):
+    """Scales amax(|x|) / 448 in fp32 (448 = largest E4M3 magnitude), the amax
+    taken over every token of the tensor (given as a list of [..., Hkv, d]
+    parts): one per tensor, or with ``per_head`` one per KV head (fp32 array)."""
     def one(parts):
         amax = max(_amax(p, src_dtype) for p in parts)
         return float(np.float32(amax) / np.float32(448.0)) if amax > 0 else 1.0
+    def heads(parts):
+        hkv = parts[0].shape[-2]
+        return np.array([one([p[..., h, :] for p in parts]) for h in range(hkv)], dtype=np.float32)
+    if per_head:
+        return heads(k_parts), heads(v_parts)
     return one(k_parts), one(v_parts)
 
 
@@ -377,7 +383,8 @@ def mixed_prefill_batch(name: str = "chunked-prefill mixed batch, fp8 KV", chunk
 
 
 def prefill_batch(name: str, chunks, num_q_heads: int, num_kv_heads: int, head_dim: int, block_size: int,
-                  src_dtype: str = "bf16", kv_dtype: str | None = None, seed: int = 0) -> PagedBatch:
+                  src_dtype: str = "bf16", kv_dtype: str | None = None, seed: int = 0,
+                  fp8_scales: str = "tensor") -> PagedBatch:
     """Prefill-only batch: ``chunks`` is a list of (q_start, chunk_len).  The
     context 0..q_start-1 is written in setup, the chunk's own K/V in the step."""
     kv_dtype = kv_dtype or src_dtype
@@ -403,7 +410,7 @@ def prefill_batch(name: str, chunks, num_q_heads: int, num_kv_heads: int, head_d
     ctx = WriteOp(np.concatenate(ks), np.concatenate(vs), np.concatenate(sc))
     new = WriteOp(np.concatenate(kn), np.concatenate(vn), np.concatenate(sn))
     if kv_dtype == "fp8":
-        k_scale, v_scale = _fp8_scales([ctx.k, new.k], [ctx.v, new.v], src_dtype)
+        k_scale, v_scale = _fp8_scales([ctx.k, new.k], [ctx.v, new.v], src_dtype, fp8_scales == "head")
     else:
         k_scale, v_scale = 1.0, 1.0
     cu = np.concatenate([[0], np.cumsum([c for _, c in chunks])]).astype(np.int32)
