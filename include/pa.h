@@ -83,6 +83,14 @@ typedef struct {
      * Ignored for f16/bf16 pools.  Must be finite and > 0 for fp8. */
     float k_scale;
     float v_scale;
+    /* fp8 only, optional: device fp32 [num_kv_heads], one scale per KV head
+     * (4-byte aligned, each finite and > 0, not checked on the device).  When
+     * set, KV head h's codes mean c * k_head_scales[h] (resp. v_head_scales[h])
+     * in every call and k_scale / v_scale are not used.  NULL: the per-pool
+     * scale.  Must be NULL for f16/bf16 pools.  (Per-head scales are this
+     * library's extension of the pages' per-tensor fp8 cache.) */
+    const float *k_head_scales;
+    const float *v_head_scales;
 } pa_kv_cache;
 
 /*

@@ -40,7 +40,8 @@ class PaKvCache(ctypes.Structure):
     """Mirror of ``pa_kv_cache``."""
     _fields_ = [("num_blocks", ctypes.c_int64), ("block_size", ctypes.c_int32),
                 ("num_kv_heads", ctypes.c_int32), ("head_dim", ctypes.c_int32),
-                ("kv_dtype", ctypes.c_int), ("k_scale", ctypes.c_float), ("v_scale", ctypes.c_float)]
+                ("kv_dtype", ctypes.c_int), ("k_scale", ctypes.c_float), ("v_scale", ctypes.c_float),
+                ("k_head_scales", ctypes.c_void_p), ("v_head_scales", ctypes.c_void_p)]
 
 
 class PaBmStats(ctypes.Structure):
@@ -129,10 +130,17 @@ def _ok(status: int, where: str) -> None:
         raise PaError(status, where)
 
 
-def kv_cache_desc(k_cache: torch.Tensor, k_scale: float = 1.0, v_scale: float = 1.0) -> PaKvCache:
-    """Descriptor of a pool tensor shaped [num_blocks, num_kv_heads, block_size, head_dim]."""
+def kv_cache_desc(k_cache: torch.Tensor, k_scale: float = 1.0, v_scale: float = 1.0,
+                  k_head_scales: torch.Tensor | None = None, v_head_scales: torch.Tensor | None = None) -> PaKvCache:
+    """Descriptor of a pool tensor shaped [num_blocks, num_kv_heads, block_size, head_dim].
+    fp8 per-head scales: float32 device tensors [num_kv_heads] (kept alive by the caller)."""
     nb, hkv, bs, d = k_cache.shape
-    return PaKvCache(nb, bs, hkv, d, _dtype_code(k_cache.dtype), float(k_scale), float(v_scale))
+    for t in (k_head_scales, v_head_scales):
+        if t is not None and (t.dtype != torch.float32 or tuple(t.shape) != (hkv,) or not t.is_contiguous()):
+            raise ValueError("per-head scales must be contiguous float32 [num_kv_heads]")
+    return PaKvCache(nb, bs, hkv, d, _dtype_code(k_cache.dtype), float(k_scale), float(v_scale),
+                     None if k_head_scales is None else k_head_scales.data_ptr(),
+                     None if v_head_scales is None else v_head_scales.data_ptr())
 
 
 def pa_reshape_and_cache(k: torch.Tensor, v: torch.Tensor, slot_mapping: torch.Tensor, k_cache: torch.Tensor,

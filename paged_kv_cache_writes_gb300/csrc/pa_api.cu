@@ -54,6 +54,11 @@ pa_status check_cache(const pa_kv_cache *c) {
       !(std::isfinite(c->k_scale) && c->k_scale > 0.f && std::isfinite(c->v_scale) &&
         c->v_scale > 0.f))
     return PA_ERR_INVALID_ARG;
+  // per-head scales: both or neither, fp8 only
+  if ((c->k_head_scales == nullptr) != (c->v_head_scales == nullptr)) return PA_ERR_INVALID_ARG;
+  if (c->k_head_scales && (c->kv_dtype != PA_FP8_E4M3 || !aligned(c->k_head_scales, 4) ||
+                           !aligned(c->v_head_scales, 4)))
+    return PA_ERR_INVALID_ARG;
   // tile rows of the 2D pool view are addressed with int32 TMA coordinates
   if ((double)c->num_blocks * c->num_kv_heads * c->block_size >= 2147483648.0)
     return PA_ERR_UNSUPPORTED;
@@ -312,8 +317,10 @@ pa_status decode_impl(const void *q, pa_dtype q_dtype, int32_t num_seqs, int32_t
   p.partition_size = ps;
   p.max_partitions = parts;
   const bool fp8 = c.kv_dtype == PA_FP8_E4M3;
-  p.q_mult = scale * 1.4426950408889634f * (fp8 ? c.k_scale : 1.f);
-  p.out_mult = fp8 ? c.v_scale : 1.f;
+  p.q_mult = scale * 1.4426950408889634f * (fp8 && !c.k_head_scales ? c.k_scale : 1.f);
+  p.out_mult = fp8 && !c.v_head_scales ? c.v_scale : 1.f;
+  p.k_hs = c.k_head_scales;
+  p.v_hs = c.v_head_scales;
   char *ws = static_cast<char *>(workspace);
   p.hdr = reinterpret_cast<DecodeHeader *>(ws + w.hdr_off);
   p.items = reinterpret_cast<int32_t *>(ws + w.items_off);
@@ -445,8 +452,10 @@ pa_status pa_prefill_chunk(const void *q_chunk, pa_dtype q_dtype, const int32_t 
     t.num_kv_heads = c.num_kv_heads;
     t.block_size = c.block_size;
     t.num_blocks = c.num_blocks;
-    t.s_mult = scale * 1.4426950408889634f * (fp8 ? c.k_scale : 1.f);
-    t.out_mult = fp8 ? c.v_scale : 1.f;
+    t.s_mult = scale * 1.4426950408889634f * (fp8 && !c.k_head_scales ? c.k_scale : 1.f);
+    t.out_mult = fp8 && !c.v_head_scales ? c.v_scale : 1.f;
+    t.k_hs = c.k_head_scales;
+    t.v_hs = c.v_head_scales;
     t.err = device_error_word();
     if (!t.err) return PA_ERR_CUDA;
     cudaError_t e;
@@ -474,8 +483,10 @@ pa_status pa_prefill_chunk(const void *q_chunk, pa_dtype q_dtype, const int32_t 
   p.num_blocks = c.num_blocks;
   p.partition_size = std::max(32, (max_seq_len + 31) / 32 * 32);  // one partition per row
   p.max_partitions = 1;
-  p.q_mult = scale * 1.4426950408889634f * (fp8 ? c.k_scale : 1.f);
-  p.out_mult = fp8 ? c.v_scale : 1.f;
+  p.q_mult = scale * 1.4426950408889634f * (fp8 && !c.k_head_scales ? c.k_scale : 1.f);
+  p.out_mult = fp8 && !c.v_head_scales ? c.v_scale : 1.f;
+  p.k_hs = c.k_head_scales;
+  p.v_hs = c.v_head_scales;
   p.out_f32 = out_dtype == PA_F32;
   p.err = device_error_word();
   PoolMaps maps;

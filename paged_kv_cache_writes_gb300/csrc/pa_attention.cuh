@@ -194,7 +194,8 @@ __global__ void __launch_bounds__(Geo<KV, D>::kThreads)
     const QT *qrow = static_cast<const QT *>(p.q) + ((int64_t)row * p.num_q_heads + h0) * D;
     for (int e = tid; e < HPC * D; e += blockDim.x) {
       const int h = e / D, d = e % D;
-      q_s[((d >> 1) * HPC + h) * 2 + (d & 1)] = Elem<QT>::to_f32(qrow[e]) * p.q_mult;
+      q_s[((d >> 1) * HPC + h) * 2 + (d & 1)] =
+          Elem<QT>::to_f32(qrow[e]) * (p.k_hs ? p.q_mult * __ldg(p.k_hs + kvh) : p.q_mult);
     }
   }
   __syncthreads();
@@ -432,7 +433,8 @@ __global__ void __launch_bounds__(Geo<KV, D>::kThreads)
       l += wt * mg_l[w * HPC + h];
     }
     if (!split) {
-      store_out<QT>(p.out, out_row + e, out_f32, l > 0.f ? a / l * p.out_mult : 0.f);
+      store_out<QT>(p.out, out_row + e, out_f32,
+                    l > 0.f ? a / l * (p.v_hs ? p.out_mult * __ldg(p.v_hs + kvh) : p.out_mult) : 0.f);
     } else {
       const int64_t slot = (ws_head + h) * p.max_partitions + part;
       p.ws_acc[slot * D + d] = a;
@@ -465,7 +467,8 @@ __global__ void __launch_bounds__(Geo<KV, D>::kThreads)
       a += wt * __ldcg(&p.ws_acc[(base + q) * D + d]);
       l += wt * ml.y;
     }
-    store_out<QT>(p.out, out_row + e, out_f32, l > 0.f ? a / l * p.out_mult : 0.f);
+    store_out<QT>(p.out, out_row + e, out_f32,
+                  l > 0.f ? a / l * (p.v_hs ? p.out_mult * __ldg(p.v_hs + kvh) : p.out_mult) : 0.f);
   }
 }
 

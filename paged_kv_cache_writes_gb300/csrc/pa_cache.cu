@@ -23,7 +23,7 @@ __global__ void __launch_bounds__(256) reshape_and_cache_kernel(
     const In *__restrict__ k, const In *__restrict__ v, int64_t num_tokens, int64_t token_stride,
     const int64_t *__restrict__ slot_mapping, void *__restrict__ k_cache, void *__restrict__ v_cache,
     int64_t num_slots, int32_t block_size, int32_t num_kv_heads, int32_t head_dim, float k_scale,
-    float v_scale, int32_t *err) {
+    float v_scale, const float *__restrict__ k_hs, const float *__restrict__ v_hs, int32_t *err) {
   const int32_t vec_per_head = head_dim >> 3;
   const int64_t per_token = 2ll * num_kv_heads * vec_per_head;
   const int64_t total = num_tokens * per_token;
@@ -49,7 +49,7 @@ __global__ void __launch_bounds__(256) reshape_and_cache_kernel(
       In *dst = static_cast<In *>(side ? v_cache : k_cache) + dst_elem;
       *reinterpret_cast<uint4 *>(dst) = x;
     } else {
-      const float s = side ? v_scale : k_scale;
+      const float s = k_hs ? __ldg((side ? v_hs : k_hs) + h) : side ? v_scale : k_scale;   // per head, or per pool
       const uint32_t w[4] = {x.x, x.y, x.z, x.w};
       uint32_t out[2];
 #pragma unroll
@@ -98,7 +98,7 @@ cudaError_t launch_reshape_and_cache(const void *k, const void *v, pa_dtype in_d
   reshape_and_cache_kernel<T, F><<<grid, threads, 0, stream>>>(                              \
       static_cast<const T *>(k), static_cast<const T *>(v), num_tokens, token_stride,        \
       slot_mapping, k_cache, v_cache, num_slots, c.block_size, c.num_kv_heads, c.head_dim,   \
-      c.k_scale, c.v_scale, err)
+      c.k_scale, c.v_scale, c.k_head_scales, c.v_head_scales, err)
   if (in_dtype == PA_BF16) {
     if (fp8) PA_RAC(__nv_bfloat16, true);
     else PA_RAC(__nv_bfloat16, false);

@@ -92,6 +92,8 @@ struct DecodeParams {
   int32_t kv_rows;           // num_kv_heads * block_size: rows of one block in the 2D pool view
   float q_mult;
   float out_mult;
+  const float *k_hs;         // fp8, optional: [Hkv] per-head scales multiplying q_mult / out_mult
+  const float *v_hs;
   DecodeHeader *hdr;
   int32_t *items;            // (row << 12) | partition
   float *ws_acc;             // [rows][Hq][max_partitions][D]
@@ -374,6 +376,7 @@ __global__ void __launch_bounds__(DecGeo<KV, D, HPC>::kNW * 32, 1)
     ok = __all_sync(0xffffffffu, mbar_wait(qbar, qphase, p.err));
     if (!ok) break;
     qphase ^= 1;
+    const float qm = p.k_hs ? p.q_mult * __ldg(p.k_hs + U0.kvh) : p.q_mult;
     for (int e8 = lane * 8; e8 < HPC * D; e8 += 256) {
       const uint4 w = *reinterpret_cast<const uint4 *>(q_raw + e8);
       const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
@@ -381,8 +384,7 @@ __global__ void __launch_bounds__(DecGeo<KV, D, HPC>::kNW * 32, 1)
 #pragma unroll
       for (int i = 0; i < 4; ++i) {
         const float2 f = unpack2(ws[i], QT{});
-        *reinterpret_cast<float2 *>(q_s + q_index<D, HPC>(d0 + 2 * i, h)) =
-            make_float2(f.x * p.q_mult, f.y * p.q_mult);
+        *reinterpret_cast<float2 *>(q_s + q_index<D, HPC>(d0 + 2 * i, h)) = make_float2(f.x * qm, f.y * qm);
       }
     }
     __syncwarp();
@@ -618,7 +620,8 @@ __global__ void __launch_bounds__(DecGeo<KV, D, HPC>::kNW * 32, 1)
       if (ts == 0) {
 #pragma unroll
         for (int h = 0; h < HPC; ++h) {
-          const float inv = l_all[h] > 0.f ? p.out_mult / l_all[h] : 0.f;
+          const float om = p.v_hs ? p.out_mult * __ldg(p.v_hs + U0.kvh) : p.out_mult;
+          const float inv = l_all[h] > 0.f ? om / l_all[h] : 0.f;
 #pragma unroll
           for (int i = 0; i < 4; ++i) {
             const int64_t idx = (head0 + h) * D + dc * 8 + 2 * i;
@@ -694,7 +697,8 @@ __global__ void __launch_bounds__(DecGeo<KV, D, HPC>::kNW * 32, 1)
           }
 #pragma unroll
           for (int off = 16; off > 0; off >>= 1) l += __shfl_xor_sync(0xffffffffu, l, off);
-          const float inv = l > 0.f ? p.out_mult / l : 0.f;
+          const float om = p.v_hs ? p.out_mult * __ldg(p.v_hs + U0.kvh) : p.out_mult;
+          const float inv = l > 0.f ? om / l : 0.f;
 #pragma unroll
           for (int e = 0; e < EPL; ++e)
             store_out<QT>(p.out, (head0 + h) * D + lane * EPL + e, p.out_f32 != 0, a[e] * inv);

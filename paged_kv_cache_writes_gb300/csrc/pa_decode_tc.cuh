@@ -350,7 +350,7 @@ __global__ void __launch_bounds__(dtc::Roles<std::is_same<KV, uint8_t>::value>::
   if (warp < kLoadWarp) {
     // ===================================================== softmax and epilogue (warps 0-3)
     const uint32_t lane_base = (uint32_t)(warp * 32) << 16;
-    const float c = tp.s_mult;
+    const float c0 = tp.s_mult;
     constexpr int kLog = G == 4 ? 2 : G == 8 ? 3 : 4;
     const int my_head = lane >> (5 - kLog);
     const bool red_writer = (lane & ((1 << (5 - kLog)) - 1)) == 0;
@@ -407,6 +407,7 @@ __global__ void __launch_bounds__(dtc::Roles<std::is_same<KV, uint8_t>::value>::
       if (!ok) break;
       const UnitHdr cur = read_unit(&info[ib]);
       const int nt = num_tiles(cur);
+      const float c = p.k_hs && cur.valid ? c0 * __ldg(p.k_hs + cur.kvh) : c0;
       // scores of this unit in log2 units, t = s * scale * log2(e); masked keys -inf
       float t[kMaxTiles][G];
       float mloc[G];
@@ -512,7 +513,8 @@ __global__ void __launch_bounds__(dtc::Roles<std::is_same<KV, uint8_t>::value>::
 #pragma unroll
           for (int h = 0; h < G; ++h) {
             const float val = kSplit ? o[h] + o[G + h] : o[h];
-            const float inv = l_prev[h] > 0.f ? p.out_mult / l_prev[h] : 0.f;
+            const float om = p.v_hs ? p.out_mult * __ldg(p.v_hs + prev.kvh) : p.out_mult;
+            const float inv = l_prev[h] > 0.f ? om / l_prev[h] : 0.f;
             store_out<QT>(p.out, (head0 + h) * kD + d, p.out_f32 != 0, val * inv);
           }
         } else {
@@ -577,7 +579,7 @@ __global__ void __launch_bounds__(dtc::Roles<std::is_same<KV, uint8_t>::value>::
         *reinterpret_cast<uint4 *>(static_cast<QT *>(const_cast<void *>(side ? tp.v_cache : tp.k_cache)) + row * kD +
                                    c * 8) = x;
       } else {
-        const float sc = side ? tp.v_scale : tp.k_scale;
+        const float sc = p.k_hs ? __ldg((side ? p.v_hs : p.k_hs) + un.kvh) : side ? tp.v_scale : tp.k_scale;
         const uint32_t w[4] = {x.x, x.y, x.z, x.w};
         uint32_t o[2];
 #pragma unroll
@@ -888,7 +890,8 @@ __global__ void __launch_bounds__(dtc::Roles<std::is_same<KV, uint8_t>::value>::
       }
 #pragma unroll
       for (int h = 0; h < G; ++h) {
-        const float inv = l[h] > 0.f ? p.out_mult / l[h] : 0.f;
+        const float om = p.v_hs ? p.out_mult * __ldg(p.v_hs + job_kvh) : p.out_mult;
+        const float inv = l[h] > 0.f ? om / l[h] : 0.f;
         const int64_t o0 = (head0 + h) * kD + 4 * lane;
         store_out<QT>(p.out, o0, p.out_f32 != 0, acc[h].x * inv);
         store_out<QT>(p.out, o0 + 1, p.out_f32 != 0, acc[h].y * inv);

@@ -75,6 +75,8 @@ struct AttnParams {
   int32_t max_partitions;     // grid.z
   float q_mult;               // softmax scale * log2(e) (* k_scale for fp8)
   float out_mult;             // v_scale for fp8, else 1
+  const float *k_hs;          // fp8, optional: [Hkv] per-head scales multiplying q_mult / out_mult
+  const float *v_hs;
   int32_t out_f32;            // 1: out is fp32; 0: out has the query dtype
   // split-KV workspace (null when max_partitions == 1)
   float *ws_acc;              // [rows][Hq][max_partitions][D]

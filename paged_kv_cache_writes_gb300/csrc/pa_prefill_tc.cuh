@@ -78,6 +78,8 @@ struct PrefillTcParams {
   int64_t num_blocks;
   float s_mult;                // scale * log2(e) (* k_scale for fp8); a negative value flips q's sign
   float out_mult;              // v_scale for fp8, else 1
+  const float *k_hs;           // fp8, optional: [Hkv] per-head scales multiplying s_mult / out_mult
+  const float *v_hs;
   int32_t *err;
 };
 
@@ -217,7 +219,7 @@ __global__ void __launch_bounds__(tc::Roles<kQTiles>::kThreads, 1) prefill_tc_ke
     const int lim = row_ok ? min(seq_eff, max(0, qs + r0 + rl + 1)) : 0;
     const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
     // scores are scaled by |s_mult| in the exponent; a negative scale flips q's sign instead
-    const float cmul = fabsf(p.s_mult);
+    const float cmul = fabsf(p.s_mult) * (p.k_hs ? __ldg(p.k_hs + g) : 1.f);
     const uint32_t qflip = p.s_mult < 0.f ? 0x80008000u : 0u;
     {  // stage row m of Q (16-bit, 128-byte-swizzled K-major, 2 panels per tile)
       const QT *src = static_cast<const QT *>(p.q) + ((int64_t)(cu0 + r0 + rl) * p.num_q_heads + head) * kD;
@@ -349,7 +351,7 @@ __global__ void __launch_bounds__(tc::Roles<kQTiles>::kThreads, 1) prefill_tc_ke
     if (ok && nkt > 0) ok = wait_all(&o_done[t], (nkt - 1) & 1);
     if (ok) {
       tc_fence_after();
-      const float inv = l > 0.f ? p.out_mult / l : 0.f;
+      const float inv = l > 0.f ? p.out_mult * (p.v_hs ? __ldg(p.v_hs + g) : 1.f) / l : 0.f;
       const int64_t obase = ((int64_t)(cu0 + r0 + rl) * p.num_q_heads + head) * kD;
 #pragma unroll 1
       for (int c0 = 0; c0 < kD; c0 += 32) {

@@ -48,7 +48,13 @@ class DeviceBatch:
             nan = np.uint16(NAN_BITS[b.kv_dtype]).view(np.int16).item()
             self.k_cache = torch.full(shape, nan, dtype=torch.int16, device=dev).view(TORCH_DTYPES[b.kv_dtype])
         self.v_cache = self.k_cache.clone()
-        self.desc = kv_cache_desc(self.k_cache, b.k_scale, b.v_scale)
+        if np.ndim(b.k_scale) == 0:
+            self.head_scales = None
+            self.desc = kv_cache_desc(self.k_cache, b.k_scale, b.v_scale)
+        else:   # one fp8 scale per KV head
+            self.head_scales = (torch.from_numpy(np.ascontiguousarray(b.k_scale, dtype=np.float32)).to(dev),
+                                torch.from_numpy(np.ascontiguousarray(b.v_scale, dtype=np.float32)).to(dev))
+            self.desc = kv_cache_desc(self.k_cache, 1.0, 1.0, *self.head_scales)
         self.setup_ops = []
         for op in b.setup:
             if hasattr(op, "pairs"):

@@ -150,3 +150,15 @@ def test_workspace_size(lib):
     assert pa.pa_decode_workspace_bytes(256, 64, 8, 128, 8192, 2048) == n     # partitions above 512 act as 512
     assert pa.pa_decode_workspace_bytes(4, 30, 8, 128, 8192, 0) == 0         # invalid -> 0
     assert pa.pa_decode_workspace_bytes(4, 32, 8, 128, 8192, 48) == 0
+
+
+def test_per_head_scale_validation(lib):
+    import paged_kv_cache_writes_gb300 as pa
+    f = lib.pa_reshape_and_cache
+    # per-head scales with a 16-bit cache, or only one of the two arrays, or misaligned
+    for d in (_desc(k_head_scales=FAKE, v_head_scales=FAKE),
+              _desc(kv_dtype=pa.PA_FP8_E4M3, k_head_scales=FAKE),
+              _desc(kv_dtype=pa.PA_FP8_E4M3, k_head_scales=FAKE + 2, v_head_scales=FAKE)):
+        assert f(FAKE, FAKE, 1, 4, 1024, FAKE, FAKE, FAKE, ctypes.byref(d), None) == 1
+    ok = _desc(kv_dtype=pa.PA_FP8_E4M3, k_head_scales=FAKE, v_head_scales=FAKE)
+    assert f(FAKE, FAKE, 1, 0, 1024, FAKE, FAKE, FAKE, ctypes.byref(ok), None) == 0      # valid, no tokens
