@@ -132,7 +132,11 @@ def measure_other_decodes(dev_name: str, steps: int, warmup: int) -> dict:
     cases = (("llama8b", W.cfg_llama8b), ("shared_prefix", W.cfg_shared_prefix),
              ("mixed_fp8_decodes", W.cfg_mixed_fp8),
              ("llama8b_fp8_cache", lambda: W.cfg_llama8b(kv_dtype="fp8")),
-             ("llama70b_fp8_cache", lambda: W.cfg_llama70b(kv_dtype="fp8")))
+             ("llama70b_fp8_cache", lambda: W.cfg_llama70b(kv_dtype="fp8")),
+             ("llama70b_fp8_cache_head_scales",
+              lambda: W.decode_batch("Llama-3-70B-shaped decode layer, fp8 KV with per-head scales",
+                                     W.lognormal_lens(np.random.default_rng(102), 256), 64, 8, 128, 32, "bf16",
+                                     kv_dtype="fp8", seed=2, partition_size=512, fp8_scales="head")))
     for key, fn in cases:
         b = fn()
         db = DeviceBatch(b, dev_name)
