@@ -449,34 +449,58 @@ def run_ours(args):
         torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
         ms = float(t.item())
 
-    # end to end through the public API with host buffers (pinned), copies inside the timed region
+    # end to end through the public API with host buffers (pinned), copies inside the timed region:
+    # every step copies its inputs (q, the new tokens' K/V and slots, tables, lengths) from pinned host
+    # memory and reads its output back.  Two device buffer sets and separate copy streams let step i+1's
+    # inputs and step i-1's output move while step i computes (the copy engines run beside the kernels).
     k_new, v_new, slots_new = db.fused_step_tensors()
-    host = {k: v.cpu().pin_memory() for k, v in (("q", db.q), ("bt", db.block_tables), ("sl", db.seq_lens),
-                                                 ("k", k_new), ("v", v_new), ("s", slots_new))}
-    out_h = torch.empty(db.out.shape, dtype=db.out.dtype, pin_memory=True)
+    srcs = {"q": db.q, "bt": db.block_tables, "sl": db.seq_lens, "k": k_new, "v": v_new, "s": slots_new}
+    host = {k: v.cpu().pin_memory() for k, v in srcs.items()}
+    out_h = [torch.empty(db.out.shape, dtype=db.out.dtype, pin_memory=True) for _ in range(2)]
     h2d = sum(t.numel() * t.element_size() for t in host.values())
-    d2h = out_h.numel() * out_h.element_size()
+    d2h = out_h[0].numel() * out_h[0].element_size()
+    bufs = [{k: torch.empty_like(v) for k, v in srcs.items()} for _ in range(2)]
+    for bset in bufs:
+        bset["out"] = torch.empty_like(db.out)
+    s_in, s_out = torch.cuda.Stream(), torch.cuda.Stream()
+    ev_in = [torch.cuda.Event() for _ in range(2)]
+    ev_done = [torch.cuda.Event() for _ in range(2)]
+    ev_read = [torch.cuda.Event() for _ in range(2)]
+    for i in range(2):   # the buffers start free
+        ev_done[i].record(stream)
+        ev_read[i].record(stream)
 
-    def e2e_step():
-        db.q.copy_(host["q"], non_blocking=True)
-        db.block_tables.copy_(host["bt"], non_blocking=True)
-        db.seq_lens.copy_(host["sl"], non_blocking=True)
-        k_new.copy_(host["k"], non_blocking=True)
-        v_new.copy_(host["v"], non_blocking=True)
-        slots_new.copy_(host["s"], non_blocking=True)
-        db.decode_write()
-        out_h.copy_(db.out, non_blocking=True)
+    def e2e_step(i):
+        bset = bufs[i % 2]
+        with torch.cuda.stream(s_in):
+            s_in.wait_event(ev_done[i % 2])            # the step that last used this set has computed
+            for k in ("q", "bt", "sl", "k", "v", "s"):
+                bset[k].copy_(host[k], non_blocking=True)
+            ev_in[i % 2].record(s_in)
+        stream.wait_event(ev_in[i % 2])
+        stream.wait_event(ev_read[i % 2])              # its output has been read back
+        pa.pa_decode_write(bset["q"], bset["k"], bset["v"], bset["s"], db.k_cache, db.v_cache, db.desc,
+                           bset["bt"], bset["sl"], int(b.seq_lens.max()), b.scale, bset["out"], db.workspace,
+                           b.partition_size, stream=stream)
+        ev_done[i % 2].record(stream)
+        with torch.cuda.stream(s_out):
+            s_out.wait_event(ev_done[i % 2])
+            out_h[i % 2].copy_(bset["out"], non_blocking=True)
+            ev_read[i % 2].record(s_out)
 
-    for _ in range(args.warmup):
-        e2e_step()
+    for i in range(args.warmup):
+        e2e_step(i)
     torch.cuda.synchronize()
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     e0.record(stream)
-    for _ in range(args.steps):
-        e2e_step()
+    s_in.wait_event(e0)
+    for i in range(args.steps):
+        e2e_step(i)
+    stream.wait_stream(s_out)                          # the last output is back on the host
     e1.record(stream)
     torch.cuda.synchronize()
     e2e_ms = e0.elapsed_time(e1) / args.steps
+    assert torch.equal(out_h[(args.steps - 1) % 2].view(torch.int32), bufs[(args.steps - 1) % 2]["out"].cpu().view(torch.int32))
     if ws > 1:
         t = torch.tensor([e2e_ms], device=dev_name)
         torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
@@ -503,11 +527,30 @@ def run_ours(args):
                      "kernel": "decode_tc_kernel (pa_decode_write: plan + decode launches, timed together)",
                      "peak_source": f"{peak_kind} hbm_gbs"},
         "e2e": {"value": kv_bytes * ws / (e2e_ms * 1e-3) / 1e9, "unit": UNIT, "h2d_bytes_per_step": h2d,
-                "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms},
+                "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms,
+                "note": "pa_decode_write per step; inputs copied from pinned host memory and the output read "
+                        "back every step, on copy streams overlapping the neighbouring steps' compute"},
         "gpu_launches": 2 * args.steps,  # per step: decode plan, decode (the cache write is inside)
         "clocks": clocks.summary(),
     }
     if ws == 1:
+        # the same step through the CUDA-core decode kernel (selectable; the default uses the tensor cores)
+        with pa.decode_kernel("cuda_cores"):
+            for _ in range(args.warmup):
+                db.decode_write()
+            c0, c1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            n_cc = max(5, args.steps // 5)
+            c0.record(stream)
+            for _ in range(n_cc):
+                db.decode_write()
+            c1.record(stream)
+            torch.cuda.synchronize()
+        cc_ms = c0.elapsed_time(c1) / n_cc
+        assert pa.pa_get_device_error() == 0
+        line["decode_cuda_cores"] = {
+            "kernel": "paged_decode_kernel (pa_set_decode_kernel(PA_DECODE_KERNEL_CUDA_CORES))",
+            "ms": cc_ms, "achieved": dec_bytes / (cc_ms * 1e-3) / 1e9, "unit": "GB/s",
+            "frac": dec_bytes / (cc_ms * 1e-3) / 1e9 / peak}
         del db
         torch.cuda.empty_cache()
         line["prefill"] = measure_prefill(dev_name, max(5, args.steps // 5), args.warmup)
