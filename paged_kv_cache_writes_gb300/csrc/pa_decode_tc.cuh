@@ -36,6 +36,15 @@
 // G..2G-1 hold the lo part p - hi, so one MMA per 16 keys accumulates both
 // and the epilogue adds the two halves of O^T.
 //
+// fp8 caches: the e4m3 codes are the MMA operands as stored (kind::f8f6f4,
+// 32 keys or elements per MMA), so a tile goes from the bulk copy to the
+// MMAs untouched.  The other operand is then e4m3 too, as two terms: the
+// query rows scaled by a power of two 2^e per unit (|q| 2^e in [128, 256)
+// at the unit's largest element) and 256 p are each written as hi + lo / 16
+// (hi in rows 0..G-1 of Q^T / P^T, lo in rows G..2G-1), which holds every
+// value to 2^-8 of itself; the softmax and the epilogue add the two column
+// halves of S^T and O^T and undo the scales.
+//
 // Softmax per unit (no online rescale): all tiles of a unit (<= 4 x 128
 // keys) are scored first, the exact maximum per head over the unit comes from
 // a warp reduction and one exchange between the four softmax warps (an
@@ -47,16 +56,16 @@
 // claimed from an atomic cursor by a persistent CTA per SM.  Roles:
 //  * warps 0-3, softmax and epilogue: thread i owns tensor-memory lane i (key
 //    i of a score tile, element d = i of an output row);
-//  * loader warp: stages Q (cp.async) and streams the unit's K tiles, then
-//    the previous unit's V tiles, with one bulk-tensor copy per cache block:
-//    a 16-bit cache straight into a ring of 32 KB tiles in the MMA's
-//    128-byte-swizzled layout, an fp8 cache into a ring of raw 16 KB tiles;
-//  * fp8 only, four widening warps: each staged tile is widened exactly to
-//    the query's 16-bit type into the MMA ring (rows past the end as zeros);
+//  * loader warp: stages Q^T (cp.async; fp8: converted to its two e4m3
+//    terms) and streams the unit's K tiles, then the previous unit's V
+//    tiles, with one bulk-tensor copy per cache block straight into a ring
+//    of tiles in the MMA's 128-byte-swizzled layout (32 KB for a 16-bit
+//    cache, 16 KB for fp8);
 //  * MMA warp (one elected lane issues): S^T of unit u, then O^T of unit
 //    u-1, whose softmax ran while the scores of u were computed;
 //  * scheduler warp: claims units two at a time and publishes each, with
-//    the block ids of its tiles, in a ring of four descriptors, so the chain
+//    the block ids of its tiles (and, fp8, the scale of its query rows), in
+//    a ring of four descriptors, so the chain
 //    of dependent reads behind a claim (cursor, work item, sequence length,
 //    block table) runs ahead of the loads instead of between them;
 //  * merge warp: merges split rows taken from a grid-wide list that the
@@ -104,68 +113,67 @@ namespace dtc {
 constexpr int kD = 128;                   // head_dim
 constexpr int kKeys = 128;                // keys per tile (MMA M, tensor-memory lanes)
 constexpr int kMaxTiles = 4;              // tiles per unit: partitions hold <= 512 tokens
-// A K or V tile in shared memory: 16 atoms of 8 keys, atom a at a * 2048,
-// its first 64 elements (128-byte rows, 128-byte swizzle) at +0 and the last
-// 64 at +1024 -- the layout of a 4D bulk-tensor box {64, 8 rows, 2 panels,
-// block_size / 8 atoms} over one cache block.
-constexpr int kTileBytes = kKeys * kD * 2;
-constexpr int kNS = 16;                   // S^T columns per tile (MMA N; heads padded to 16)
-constexpr int kQBytes = 2 * kNS * 128;    // Q^T operand: 2 panels x 16 rows x 128 B
 constexpr int kInfo = 4;                  // unit descriptors in flight (bounds how far a CTA claims ahead)
 constexpr int kClaim = 2;                 // units per claim (a power of two)
+// A 16-bit K or V tile in shared memory: 16 atoms of 8 keys, atom a at
+// a * 2048, its first 64 elements (128-byte rows, 128-byte swizzle) at +0 and
+// the last 64 at +1024 -- the layout of a 4D bulk-tensor box {64, 8 rows,
+// 2 panels, block_size / 8 atoms} over one cache block.
 constexpr int kAtomBytes = 2048;          // 8 keys x 256 B: the two 128-byte panels of 8 rows
 
-// Warp roles: 0-3 softmax, 4 the loader (bulk-tensor copies and Q), then for
-// an fp8 cache four warps widening the staged codes, the MMA warp, the
-// scheduler warp, the merge warp.
-template <bool kFp8>
+// Warp roles: 0-3 softmax, 4 the loader (bulk-tensor copies and Q), 5 the
+// MMA warp, 6 the scheduler, 7 the merge warp.
 struct Roles {
   static constexpr int kLoadWarp = 4;
-  static constexpr int kWidenWarp0 = 5;
-  static constexpr int kWidenWarps = kFp8 ? 4 : 0;
-  static constexpr int kMmaWarp = kWidenWarp0 + kWidenWarps;
-  static constexpr int kSchedWarp = kMmaWarp + 1;
-  static constexpr int kMergeWarp = kSchedWarp + 1;
+  static constexpr int kMmaWarp = 5;
+  static constexpr int kSchedWarp = 6;
+  static constexpr int kMergeWarp = 7;
   static constexpr int kThreads = (kMergeWarp + 1) * 32;
 };
 
-constexpr int kMaxSlots = 8;
+constexpr int kMaxSlots = 12;
 
 // A claimed unit as published by the scheduler warp: its place, and the
 // block id of each 16-key run of its tiles (run r of tile j at blk[8*j + r];
-// -1 past the end of the unit).
+// -1 past the end of the unit).  qscale: fp8 caches, the bits of the power
+// of two its query rows are multiplied by before their e4m3 split.
 struct TcUnit {
-  int32_t valid, row, kvh, part, tok_begin, ntok, nparts, pad;
+  int32_t valid, row, kvh, part, tok_begin, ntok, nparts, qscale;
   int32_t blk[kMaxTiles * 8];
 };
 
-constexpr int kStageSlots = 4;            // fp8: raw tiles staged by bulk copies
-constexpr int kStageBytes = kKeys * kD;   // 16 KB: 128 rows of 128 e4m3 codes
-
+// Shared-memory and tensor-memory geometry.  16-bit caches: K/V tiles of
+// 32 KB (two 128-byte panels per 8-key atom), Q^T of 16 rows (the heads,
+// padded) and P^T of kNO rows, each in two 64-element panels.  fp8 caches:
+// tiles of 16 KB (128 rows of 128 codes, the layout a 2D bulk-tensor box
+// with 128-byte swizzle writes), Q^T and P^T of one 128-element panel
+// holding the hi terms in rows 0..G-1 and the lo terms in rows G..2G-1.
 template <int G, bool kSplit, bool kFp8>
 struct TcGeo {
   static_assert(G == 4 || G == 8 || G == 16, "4, 8 or 16 query heads per KV head");
-  static constexpr int kPRows = kSplit ? 2 * G : G;         // P^T columns in use
-  static constexpr int kNO = kPRows <= 16 ? 16 : 32;        // O^T columns (MMA N)
-  static constexpr int kPBytes = 2 * kNO * 128;             // P^T of a tile: 2 panels (64 keys) x kNO rows
-  static constexpr int kColO = 2 * kMaxTiles * kNS;         // tensor-memory column of O^T, buffer 0
-  static constexpr int kTmemCols = 256;                     // 128 S^T + 2 * kNO O^T columns, rounded up
-  static constexpr int kNumBars = 2 * kMaxSlots + 8 * 2 + 2 * kInfo + 1 + 2 * kStageSlots + 2;
+  static constexpr int kPRows = (kSplit || kFp8) ? 2 * G : G;       // P^T rows in use
+  static constexpr int kNO = kPRows <= 16 ? 16 : 32;                // O^T columns (MMA N)
+  static constexpr int kNS = kFp8 ? kNO : 16;                       // S^T columns per tile (MMA N)
+  static constexpr int kSCols = kFp8 ? 2 * G : G;                   // S^T columns in use
+  static constexpr int kQBytes = kFp8 ? kNS * 128 : 2 * kNS * 128;  // Q^T of a unit
+  static constexpr int kPBytes = kFp8 ? kNO * 128 : 2 * kNO * 128;  // P^T of a tile
+  static constexpr int kSlotBytes = kFp8 ? kKeys * kD : kKeys * kD * 2;   // one K or V tile
+  static constexpr int kColO = 2 * kMaxTiles * kNS;                 // tensor-memory column of O^T, buffer 0
+  static constexpr int kTmemCols = kColO + 2 * kNO <= 256 ? 256 : 512;
+  static constexpr int kNumBars = 2 * kMaxSlots + 8 * 2 + 2 * kInfo + 1;
   static constexpr int kOffQ = 0;                                        // [2] Q^T
   static constexpr int kOffP = kOffQ + 2 * kQBytes;                      // [2][4] P^T
   static constexpr int kOffRed = kOffP + 2 * kMaxTiles * kPBytes;        // float [2][4 warps][2][16]
   static constexpr int kOffInfo = kOffRed + 2 * 4 * 2 * 16 * 4;          // TcUnit [kInfo] (16-byte aligned)
   static constexpr int kOffBar = kOffInfo + kInfo * (int)sizeof(TcUnit);
   static constexpr int kOffMisc = kOffBar + kNumBars * 8;
-  static constexpr int kOffQraw = (kOffMisc + 64 + 15) / 16 * 16;        // fp8: [2] the G query rows as given
-  static constexpr int kOffStage = (kOffQraw + (kFp8 ? 2 * G * kD * 2 : 0) + 1023) / 1024 * 1024;  // fp8: raw tiles
-  static constexpr int kOffRing = kOffStage + (kFp8 ? kStageSlots * kStageBytes : 0);  // [kSlots] K/V tiles
-  static constexpr int kSlots0 = (227 * 1024 - 1024 - kOffRing) / kTileBytes;
+  static constexpr int kOffRing = (kOffMisc + 64 + 1023) / 1024 * 1024;  // [kSlots] K/V tiles
+  static constexpr int kSlots0 = (227 * 1024 - 1024 - kOffRing) / kSlotBytes;
   static constexpr int kSlots = kSlots0 > kMaxSlots ? kMaxSlots : kSlots0;
-  static constexpr int kSmemBytes = kOffRing + kSlots * kTileBytes + 1024;  // + alignment slack
+  static constexpr int kSmemBytes = kOffRing + kSlots * kSlotBytes + 1024;  // + alignment slack
   static_assert(kSlots >= 2 && kSmemBytes <= 227 * 1024, "shared memory");
-  static_assert(kOffQraw % 16 == 0 && kOffStage % 1024 == 0 && kOffRing % 1024 == 0 && kOffP % 1024 == 0,
-                "16-byte copies, 1024-byte swizzle atoms");
+  static_assert(kOffRing % 1024 == 0 && kOffP % 1024 == 0 && kQBytes % 1024 == 0 && kPBytes % 1024 == 0,
+                "1024-byte swizzle atoms");
 };
 
 // N consecutive fp32 columns of this thread's tensor-memory lane (warp-collective).
@@ -224,7 +232,7 @@ __device__ __forceinline__ float warp_reduce_heads(float (&v)[G], int lane) {
 
 // The descriptor's header, copied to registers (the block ids stay in shared memory).
 struct UnitHdr {
-  int32_t valid, row, kvh, part, tok_begin, ntok, nparts, pad;
+  int32_t valid, row, kvh, part, tok_begin, ntok, nparts, qscale;
 };
 __device__ __forceinline__ UnitHdr read_unit(const TcUnit *u) {
   const volatile int32_t *s = reinterpret_cast<const volatile int32_t *>(u);
@@ -236,32 +244,58 @@ __device__ __forceinline__ UnitHdr read_unit(const TcUnit *u) {
   r.tok_begin = s[4];
   r.ntok = s[5];
   r.nparts = s[6];
-  r.pad = 0;
+  r.qscale = s[7];
   return r;
 }
 
 __device__ __forceinline__ int num_tiles(const UnitHdr &u) { return u.valid ? (u.ntok + kKeys - 1) / kKeys : 0; }
 
+// Largest |x| of the 8 query elements in a 16-byte word (NaN ignored).
+__device__ __forceinline__ float absmax8(uint4 w, __nv_bfloat16) {
+  const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
+  float m = 0.f;
+#pragma unroll
+  for (int i = 0; i < 4; ++i) m = fmaxf(m, fmaxf(__uint_as_float((ws[i] << 16) & 0x7fffffffu),
+                                                 __uint_as_float(ws[i] & 0x7fff0000u)));
+  return m;
+}
+__device__ __forceinline__ float absmax8(uint4 w, __half) {
+  const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
+  float m = 0.f;
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const float2 f = __half22float2(*reinterpret_cast<const __half2 *>(&ws[i]));
+    m = fmaxf(m, fmaxf(fabsf(f.x), fabsf(f.y)));
+  }
+  return m;
+}
+
+// The power of two 2^e with amax * 2^e in [128, 256) (e clamped to +-100;
+// 1 for amax = 0), as fp32 bits.
+__device__ __forceinline__ int32_t query_scale_bits(float amax) {
+  const int eb = (int)((__float_as_uint(amax) >> 23) & 0xff);
+  const int e = amax > 0.f ? max(-100, min(100, 134 - eb)) : 0;
+  return (e + 127) << 23;
+}
+
 }  // namespace dtc
 
 template <typename KV, typename QT, int G>
-__global__ void __launch_bounds__(dtc::Roles<std::is_same<KV, uint8_t>::value>::kThreads, 1)
+__global__ void __launch_bounds__(dtc::Roles::kThreads, 1)
     decode_tc_kernel(const DecodeTcParams tp, const __grid_constant__ CUtensorMap tmap_k,
                      const __grid_constant__ CUtensorMap tmap_v) {
   using namespace tc;
   using namespace dtc;
   constexpr bool kFp8 = std::is_same<KV, uint8_t>::value;
-  using RO = Roles<kFp8>;
-  constexpr int kLoadWarp = RO::kLoadWarp, kWidenWarp0 = RO::kWidenWarp0, kMmaWarp = RO::kMmaWarp;
-  constexpr int kSchedWarp = RO::kSchedWarp, kMergeWarp = RO::kMergeWarp, kThreads = RO::kThreads;
-  constexpr int kWideners = 32 * RO::kWidenWarps;
-  // MMA operands: the cache's 16-bit type; an fp8 cache is widened to f16 (exact,
-  // one conversion per two codes) and the queries are converted to f16 too
+  constexpr int kLoadWarp = Roles::kLoadWarp, kMmaWarp = Roles::kMmaWarp;
+  constexpr int kSchedWarp = Roles::kSchedWarp, kMergeWarp = Roles::kMergeWarp, kThreads = Roles::kThreads;
+  // MMA operands: the cache's type (bf16 / f16 with a 16-bit cache, the queries
+  // in the same type; e4m3 with an fp8 cache, the queries and P as two e4m3 terms)
   constexpr bool kBf16 = std::is_same<QT, __nv_bfloat16>::value && !kFp8;
   constexpr bool kSplit = kBf16;            // bf16 cache: P as hi + lo
   using GE = TcGeo<G, kSplit, kFp8>;
-  constexpr int S = GE::kSlots, kNO = GE::kNO;
-  constexpr uint32_t kAB = kBf16 ? 1u : 0u;
+  constexpr int S = GE::kSlots, kNO = GE::kNO, kNS = GE::kNS;
+  constexpr uint32_t kAB = kBf16 ? 1u : 0u;   // instruction-descriptor format: bf16 1, f16 0, e4m3 0
   const DecodeParams &p = tp.d;
   const float kNegInf = -__int_as_float(0x7f800000);
 
@@ -282,9 +316,6 @@ __global__ void __launch_bounds__(dtc::Roles<std::is_same<KV, uint8_t>::value>::
   uint64_t *info_full = red_bar + 2;          // [kInfo] unit descriptor published
   uint64_t *info_free = info_full + kInfo;    // [kInfo] released by the MMA warp and the softmax warps
   uint64_t *fin = info_free + kInfo;          // every MMA of the CTA complete
-  uint64_t *stage_full = fin + 1;             // fp8 [kStageSlots] raw tile copied
-  uint64_t *stage_free = stage_full + kStageSlots;   // fp8 [kStageSlots] widened (every widening thread)
-  uint64_t *qraw_full = stage_free + kStageSlots;     // fp8 [2] query rows copied (loader lanes)
   TcUnit *info = reinterpret_cast<TcUnit *>(smem + GE::kOffInfo);
   float *red = reinterpret_cast<float *>(smem + GE::kOffRed);
   uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + GE::kOffMisc);
@@ -297,11 +328,11 @@ __global__ void __launch_bounds__(dtc::Roles<std::is_same<KV, uint8_t>::value>::
     reinterpret_cast<uint4 *>(smem + GE::kOffQ)[i] = make_uint4(0, 0, 0, 0);
   if (tid == 0) {
     for (int s = 0; s < S; ++s) {
-      mbar_init(&slot_full[s], kFp8 ? kWideners : 1);   // fp8: every widening thread; else one expect-tx arrival
+      mbar_init(&slot_full[s], 1);   // one expect-tx arrival
       mbar_init(&slot_free[s], 1);
     }
     for (int b = 0; b < 2; ++b) {
-      mbar_init(&q_full[b], kFp8 ? kWideners : 32);   // fp8: the widening warps convert Q
+      mbar_init(&q_full[b], 32);     // every loader lane
       mbar_init(&q_free[b], 1);
       mbar_init(&s_full[b], 1);
       mbar_init(&s_free[b], 128);
@@ -315,11 +346,6 @@ __global__ void __launch_bounds__(dtc::Roles<std::is_same<KV, uint8_t>::value>::
       mbar_init(&info_free[i], 2);
     }
     mbar_init(fin, 1);
-    for (int i = 0; i < kStageSlots; ++i) {
-      mbar_init(&stage_full[i], 1);
-      mbar_init(&stage_free[i], kWideners > 0 ? kWideners : 1);
-    }
-    for (int i = 0; i < 2; ++i) mbar_init(&qraw_full[i], 32);
     *abort_flag = 0;
     fence_mbar_init();
     prefetch_tensor_map(&tmap_k);
@@ -407,7 +433,8 @@ __global__ void __launch_bounds__(dtc::Roles<std::is_same<KV, uint8_t>::value>::
       if (!ok) break;
       const UnitHdr cur = read_unit(&info[ib]);
       const int nt = num_tiles(cur);
-      const float c = p.k_hs && cur.valid ? c0 * __ldg(p.k_hs + cur.kvh) : c0;
+      float c = p.k_hs && cur.valid ? c0 * __ldg(p.k_hs + cur.kvh) : c0;
+      if constexpr (kFp8) c *= __frcp_rn(__int_as_float(cur.valid ? cur.qscale : 127 << 23));   // exact: 2^-e
       // scores of this unit in log2 units, t = s * scale * log2(e); masked keys -inf
       float t[kMaxTiles][G];
       float mloc[G];
@@ -420,12 +447,13 @@ __global__ void __launch_bounds__(dtc::Roles<std::is_same<KV, uint8_t>::value>::
 #pragma unroll
         for (int j = 0; j < kMaxTiles; ++j) {
           if (j < nt) {
-            float raw[G];
-            tmem_ld_cols<G>(col_s(b, j) + lane_base, raw);
+            float raw[GE::kSCols];
+            tmem_ld_cols<GE::kSCols>(col_s(b, j) + lane_base, raw);
             const bool kv = j * kKeys + tid < cur.ntok;
 #pragma unroll
             for (int h = 0; h < G; ++h) {
-              t[j][h] = kv ? raw[h] * c : kNegInf;
+              const float sv = kFp8 ? fmaf(raw[G + h], 0.0625f, raw[h]) : raw[h];   // fp8: hi + lo / 16
+              t[j][h] = kv ? sv * c : kNegInf;
               mloc[h] = fmaxf(mloc[h], t[j][h]);
             }
           } else {
@@ -458,7 +486,34 @@ __global__ void __launch_bounds__(dtc::Roles<std::is_same<KV, uint8_t>::value>::
       }
       // P^T of this unit (its buffer's previous reader, P.V of unit u-2, finished
       // before the epilogue of u-2, which ran in the previous iteration)
-      if (cur.valid) {
+      if (cur.valid && kFp8) {
+        // 256 p = hi + lo / 16 in e4m3, key tid's byte of rows h and G + h
+#pragma unroll
+        for (int h = 0; h < G; ++h) l_part[h] = 0.f;
+        uint8_t *pb = smem + GE::kOffP + b * kMaxTiles * GE::kPBytes + (tid & 15);
+#pragma unroll
+        for (int j = 0; j < kMaxTiles; ++j) {
+          if (j >= nt) break;
+          uint8_t *pt = pb + j * GE::kPBytes;
+#pragma unroll
+          for (int h = 0; h < G; h += 2) {
+            const float msub0 = m_cur[h] == kNegInf ? 0.f : m_cur[h];
+            const float msub1 = m_cur[h + 1] == kNegInf ? 0.f : m_cur[h + 1];
+            const float p0 = fast_exp2(t[j][h] - msub0), p1 = fast_exp2(t[j][h + 1] - msub1);
+            uint32_t hi, lo;
+            split2_e4m3(make_float2(p0 * 256.f, p1 * 256.f), hi, lo);
+            auto put = [&](int row, uint32_t code) { pt[row * 128 + (((tid >> 4) ^ (row & 7)) << 4)] = (uint8_t)code; };
+            put(h, hi);
+            put(h + 1, hi >> 8);
+            put(G + h, lo);
+            put(G + h + 1, lo >> 8);
+            l_part[h] += p0;
+            l_part[h + 1] += p1;
+          }
+        }
+        fence_async_smem();
+        mbar_arrive(&p_full[b]);
+      } else if (cur.valid) {
 #pragma unroll
         for (int h = 0; h < G; ++h) l_part[h] = 0.f;
         uint8_t *pb = smem + GE::kOffP + b * kMaxTiles * GE::kPBytes + (tid >> 6) * (kNO * 128) + (tid & 7) * 2;
@@ -479,7 +534,7 @@ __global__ void __launch_bounds__(dtc::Roles<std::is_same<KV, uint8_t>::value>::
               *reinterpret_cast<uint16_t *>(pt + (G + h) * 128 + ((ck ^ ((G + h) & 7)) << 4)) =
                   (uint16_t)(__float_as_uint(lo) >> 16);
               l_part[h] += pv;
-            } else {   // f16 operands (f16 cache, or an fp8 cache widened to f16)
+            } else {   // f16 operands
               const __half hv = __float2half_rn(pv);
               *reinterpret_cast<__half *>(pt + h * 128 + ((ck ^ (h & 7)) << 4)) = hv;
               l_part[h] += __half2float(hv);
@@ -509,10 +564,14 @@ __global__ void __launch_bounds__(dtc::Roles<std::is_same<KV, uint8_t>::value>::
         report_pending();
         const int64_t head0 = (int64_t)prev.row * hq + (int64_t)prev.kvh * G;
         const int d = tid;
+        // the two column halves of O^T: bf16 p = hi + lo; fp8 256 p = hi + lo / 16
+        auto o_val = [&](int h) {
+          return kSplit ? o[h] + o[G + h] : kFp8 ? fmaf(o[G + h], 0.0625f, o[h]) * (1.f / 256.f) : o[h];
+        };
         if (prev.nparts == 1) {
 #pragma unroll
           for (int h = 0; h < G; ++h) {
-            const float val = kSplit ? o[h] + o[G + h] : o[h];
+            const float val = o_val(h);
             const float om = p.v_hs ? p.out_mult * __ldg(p.v_hs + prev.kvh) : p.out_mult;
             const float inv = l_prev[h] > 0.f ? om / l_prev[h] : 0.f;
             store_out<QT>(p.out, (head0 + h) * kD + d, p.out_f32 != 0, val * inv);
@@ -520,7 +579,7 @@ __global__ void __launch_bounds__(dtc::Roles<std::is_same<KV, uint8_t>::value>::
         } else {
 #pragma unroll
           for (int h = 0; h < G; ++h)
-            p.ws_acc[((head0 + h) * p.max_partitions + prev.part) * kD + d] = kSplit ? o[h] + o[G + h] : o[h];
+            p.ws_acc[((head0 + h) * p.max_partitions + prev.part) * kD + d] = o_val(h);
           if (tid < G) {
             float mv = m_prev[0], lv = l_prev[0];
 #pragma unroll
@@ -551,10 +610,11 @@ __global__ void __launch_bounds__(dtc::Roles<std::is_same<KV, uint8_t>::value>::
     }
   } else if (warp == kLoadWarp) {
     // ===================================================== loader (one warp)
-    // Q with cp.async; every K and V tile with one bulk-tensor box per cache
-    // block holding keys of the unit (tiles start on block boundaries):
-    // 16-bit caches straight into the MMA's atom layout (bs / 8 atoms per box),
-    // fp8 caches raw into the staging ring (bs rows of 128 codes per box).
+    // Q^T with cp.async (fp8: loaded, scaled and split into two e4m3 terms);
+    // every K and V tile with one bulk-tensor box per cache block holding keys
+    // of the unit (tiles start on block boundaries), straight into the ring in
+    // the MMA's layout: 16-bit caches bs / 8 atoms per box, fp8 bs rows of 128
+    // codes per box.
     const int bs = p.block_size;
     uint32_t g_load = 0;
     bool ok = true;
@@ -613,19 +673,42 @@ __global__ void __launch_bounds__(dtc::Roles<std::is_same<KV, uint8_t>::value>::
           ok = wait_all(&q_free[b], ((u >> 1) - 1) & 1);
           if (!ok) break;
         }
+        if constexpr (kFp8) {
+          // q 2^e = hi + lo / 16: elements d .. d+7 of head h are bytes d .. d+7 of rows h and G + h
+          const float qs = __int_as_float(cur.qscale);
+          uint8_t *qb = smem + GE::kOffQ + b * GE::kQBytes;
 #pragma unroll
-        for (int e = lane; e < G * 16; e += 32) {
-          const int h = e >> 4, c16 = e & 15;
-          const char *src = static_cast<const char *>(p.q) +
-                            (((int64_t)cur.row * hq + (int64_t)cur.kvh * G + h) * kD) * 2 + c16 * 16;
-          if constexpr (kFp8)   // as given, for the widening warps to convert
-            cp_async16(smem + GE::kOffQraw + b * (G * kD * 2) + e * 16, src, 16u);
-          else
-            cp_async16(smem + GE::kOffQ + b * kQBytes + (c16 >> 3) * (kNS * 128) + h * 128 +
+          for (int e = lane; e < G * 16; e += 32) {
+            const int h = e >> 4, c16 = e & 15;
+            const uint4 w = ld_nc16(static_cast<const char *>(p.q) +
+                                    (((int64_t)cur.row * hq + (int64_t)cur.kvh * G + h) * kD) * 2 + c16 * 16);
+            const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
+            uint32_t hi[4], lo[4];
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+              const float2 f = unpack2(ws[k], QT{});
+              split2_e4m3(make_float2(f.x * qs, f.y * qs), hi[k], lo[k]);
+            }
+            const int hr = h, lr = G + h, half = (c16 & 1) * 8;
+            *reinterpret_cast<uint2 *>(qb + hr * 128 + ((((c16 >> 1) ^ (hr & 7))) << 4) + half) =
+                make_uint2(hi[0] | (hi[1] << 16), hi[2] | (hi[3] << 16));
+            *reinterpret_cast<uint2 *>(qb + lr * 128 + ((((c16 >> 1) ^ (lr & 7))) << 4) + half) =
+                make_uint2(lo[0] | (lo[1] << 16), lo[2] | (lo[3] << 16));
+          }
+          fence_async_smem();
+          mbar_arrive(&q_full[b]);
+        } else {
+#pragma unroll
+          for (int e = lane; e < G * 16; e += 32) {
+            const int h = e >> 4, c16 = e & 15;
+            const char *src = static_cast<const char *>(p.q) +
+                              (((int64_t)cur.row * hq + (int64_t)cur.kvh * G + h) * kD) * 2 + c16 * 16;
+            cp_async16(smem + GE::kOffQ + b * GE::kQBytes + (c16 >> 3) * (kNS * 128) + h * 128 +
                            (((c16 & 7) ^ (h & 7)) << 4),
                        src, 16u);
+          }
+          cp_async_arrive_noinc(&q_full[b]);
         }
-        cp_async_arrive_noinc(kFp8 ? &qraw_full[b] : &q_full[b]);
       }
       // tiles in the MMA's order: K tiles of this unit, then V tiles of the previous one
       for (int i = 0; i < ntc + ntp && ok; ++i) {
@@ -635,11 +718,10 @@ __global__ void __launch_bounds__(dtc::Roles<std::is_same<KV, uint8_t>::value>::
         // fused write: the row's new token, for this KV head, before the copy of
         // its last tile (its V tile is copied later still)
         if (tp.k_new != nullptr && is_k && j == ntc - 1 && un.part == un.nparts - 1) write_new(un, ib);
-        const uint32_t ring = kFp8 ? (uint32_t)kStageSlots : (uint32_t)S;
-        const int slot = (int)(g_load % ring);
-        uint64_t *free_bar = kFp8 ? &stage_free[slot] : &slot_free[slot];
-        uint64_t *full_bar = kFp8 ? &stage_full[slot] : &slot_full[slot];
-        if (g_load >= ring) ok = wait_all(free_bar, ((g_load / ring) - 1) & 1);
+        const int slot = (int)(g_load % S);
+        uint64_t *free_bar = &slot_free[slot];
+        uint64_t *full_bar = &slot_full[slot];
+        if (g_load >= (uint32_t)S) ok = wait_all(free_bar, ((g_load / S) - 1) & 1);
         if (!ok) break;
         const int nvalid = min(kKeys, un.ntok - j * kKeys);
         bool issue = false;
@@ -655,13 +737,13 @@ __global__ void __launch_bounds__(dtc::Roles<std::is_same<KV, uint8_t>::value>::
           if (lane == 0) mbar_arrive_expect_tx(full_bar, boxes * atoms * kAtomBytes);
           __syncwarp();
           if (issue)
-            tma_load_4d(smem + GE::kOffRing + slot * kTileBytes + lane * atoms * kAtomBytes, map, full_bar, 0, 0, 0,
-                        (bi * hkv + un.kvh) * atoms);
+            tma_load_4d(smem + GE::kOffRing + slot * GE::kSlotBytes + lane * atoms * kAtomBytes, map, full_bar, 0, 0,
+                        0, (bi * hkv + un.kvh) * atoms);
         } else {
           if (lane == 0) mbar_arrive_expect_tx(full_bar, boxes * bs * kD);
           __syncwarp();
           if (issue)
-            tma_load_2d(smem + GE::kOffStage + slot * kStageBytes + lane * bs * kD, map, full_bar, 0,
+            tma_load_2d(smem + GE::kOffRing + slot * GE::kSlotBytes + lane * bs * kD, map, full_bar, 0,
                         (bi * hkv + un.kvh) * bs);
         }
         ++g_load;
@@ -670,91 +752,11 @@ __global__ void __launch_bounds__(dtc::Roles<std::is_same<KV, uint8_t>::value>::
       prev = cur;
     }
     cp_async_wait_all();
-  } else if (warp < kMmaWarp) {
-    // ===================================================== fp8 widening (four warps)
-    // Per unit, the G query rows -> f16 Q^T.  Staged row r of a tile (128
-    // codes, 128-byte swizzle) -> row r of the f16 tile in the MMA's atom
-    // layout, exactly (widen16); rows past the end of the unit are written as
-    // zeros (P is 0 there, and 0 * NaN would not be).  A thread's eight staged
-    // words are read first, so their loads overlap.
-    const int wt = tid - kWidenWarp0 * 32;
-    uint32_t g = 0;
-    bool ok = true;
-    UnitHdr prev;
-    prev.valid = 0;
-    for (int u = 0; ok; ++u) {
-      const int ib = u % kInfo, b = u & 1;
-      ok = wait_all(&info_full[ib], (u / kInfo) & 1);
-      if (!ok) break;
-      const UnitHdr cur = read_unit(&info[ib]);
-      const int ntc = num_tiles(cur), ntp = num_tiles(prev);
-      if (cur.valid) {
-        // Q^T in f16: exact for |q| in [2^-17, 65504]; larger magnitudes saturate to 65504
-        if (u >= 2) ok = wait_all(&q_free[b], ((u >> 1) - 1) & 1);
-        if (ok) ok = wait_all(&qraw_full[b], (u >> 1) & 1);
-        if (!ok) break;
-        for (int e = wt; e < G * 16; e += kWideners) {
-          const int h = e >> 4, c16 = e & 15;
-          const uint4 w = *reinterpret_cast<const uint4 *>(smem + GE::kOffQraw + b * (G * kD * 2) + e * 16);
-          const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
-          uint32_t o[4];
-#pragma unroll
-          for (int k = 0; k < 4; ++k) {
-            float2 f = unpack2(ws[k], QT{});
-            f.x = fminf(fmaxf(f.x, -65504.f), 65504.f);
-            f.y = fminf(fmaxf(f.y, -65504.f), 65504.f);
-            o[k] = pack2(f.x, f.y, __half{});
-          }
-          *reinterpret_cast<uint4 *>(smem + GE::kOffQ + b * kQBytes + (c16 >> 3) * (kNS * 128) + h * 128 +
-                                     (((c16 & 7) ^ (h & 7)) << 4)) = make_uint4(o[0], o[1], o[2], o[3]);
-        }
-        fence_async_smem();
-        mbar_arrive(&q_full[b]);
-      }
-      for (int i = 0; i < ntc + ntp && ok; ++i) {
-        const bool is_k = i < ntc;
-        const UnitHdr &un = is_k ? cur : prev;
-        const int j = is_k ? i : i - ntc;
-        const int nvalid = min(kKeys, un.ntok - j * kKeys);
-        const int ss = (int)(g % kStageSlots), slot = (int)(g % S);
-        ok = wait_all(&stage_full[ss], (g / kStageSlots) & 1);
-        if (ok && g >= (uint32_t)S) ok = wait_all(&slot_free[slot], ((g / S) - 1) & 1);
-        if (!ok) break;
-        const uint8_t *st = smem + GE::kOffStage + ss * kStageBytes;
-        uint8_t *tile = smem + GE::kOffRing + slot * kTileBytes;
-        constexpr int kChunks = kStageBytes / 16 / 128;   // 16-code chunks per thread
-        uint4 raw[kChunks];
-#pragma unroll
-        for (int k = 0; k < kChunks; ++k) {
-          const int id = k * 128 + wt, r = id >> 3, c = id & 7;   // row, 16-code chunk
-          raw[k] = *reinterpret_cast<const uint4 *>(st + r * 128 + ((c ^ (r & 7)) << 4));
-        }
-#pragma unroll
-        for (int k = 0; k < kChunks; ++k) {
-          const int id = k * 128 + wt, r = id >> 3, c = id & 7;
-          uint32_t o[8];
-          widen16<__half>(raw[k], o);
-          if (r >= nvalid) {
-#pragma unroll
-            for (int i = 0; i < 8; ++i) o[i] = 0;
-          }
-          const int c0 = (2 * c) & 7;
-          uint8_t *dst = tile + (r >> 3) * kAtomBytes + (c >> 2) * 1024 + (r & 7) * 128;
-          *reinterpret_cast<uint4 *>(dst + ((c0 ^ (r & 7)) << 4)) = make_uint4(o[0], o[1], o[2], o[3]);
-          *reinterpret_cast<uint4 *>(dst + (((c0 + 1) ^ (r & 7)) << 4)) = make_uint4(o[4], o[5], o[6], o[7]);
-        }
-        fence_async_smem();
-        mbar_arrive(&slot_full[slot]);
-        mbar_arrive(&stage_free[ss]);
-        ++g;
-      }
-      if (!cur.valid) break;
-      prev = cur;
-    }
   } else if (warp == kSchedWarp) {
     // ===================================================== scheduler
     // kClaim units per claim (one atomic step), published in order; the block
-    // id of run (lane & 7) of tile (lane >> 3) is read by lane `lane`.
+    // id of run (lane & 7) of tile (lane >> 3) is read by lane `lane`.  fp8:
+    // the unit's query scale from the largest |q| of its G query rows.
     const int bs = p.block_size;
     const int total_units = __ldcg(&p.hdr->num_items) * hkv;
     const int64_t cap = min((int64_t)p.max_blocks_per_seq * bs, (int64_t)p.max_partitions * p.partition_size);
@@ -786,6 +788,19 @@ __global__ void __launch_bounds__(dtc::Roles<std::is_same<KV, uint8_t>::value>::
         const int rk = __shfl_sync(0xffffffffu, row, k);
         const int tb = __shfl_sync(0xffffffffu, tok_begin, k);
         const int nk = __shfl_sync(0xffffffffu, ntok, k);
+        int32_t qscale = 0;
+        if constexpr (kFp8) {
+          float amax = 0.f;
+          if (vk) {
+            const int kvk = __shfl_sync(0xffffffffu, id % hkv, k);
+            const char *q0 = static_cast<const char *>(p.q) + ((int64_t)rk * hq + (int64_t)kvk * G) * kD * 2;
+#pragma unroll
+            for (int e = lane; e < G * 16; e += 32) amax = fmaxf(amax, absmax8(ld_nc16(q0 + e * 16), QT{}));
+#pragma unroll
+            for (int m = 16; m > 0; m >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, m));
+          }
+          qscale = query_scale_bits(amax);
+        }
         TcUnit *dst = &info[(u + k) % kInfo];
         const int key0 = tb + (lane >> 3) * kKeys + 16 * (lane & 7);
         int32_t blk = -1;
@@ -803,7 +818,7 @@ __global__ void __launch_bounds__(dtc::Roles<std::is_same<KV, uint8_t>::value>::
           dst->tok_begin = tb;
           dst->ntok = nk;
           dst->nparts = nparts;
-          dst->pad = 0;
+          dst->qscale = qscale;
         }
         any_invalid |= !vk;
       }
@@ -906,6 +921,11 @@ __global__ void __launch_bounds__(dtc::Roles<std::is_same<KV, uint8_t>::value>::
     const bool leader = elect_one();
     const uint32_t idesc_s = umma_idesc(kAB, kNS, false, false);
     const uint32_t idesc_o = umma_idesc(kAB, kNO, false, true);
+    // one MMA: kind::f8f6f4 for an fp8 cache, else kind::f16
+    auto mma = [&](uint32_t d, uint64_t a, uint64_t bdesc, uint32_t idesc, uint32_t acc) {
+      if constexpr (kFp8) umma_f8(d, a, bdesc, idesc, acc);
+      else umma(d, a, bdesc, idesc, acc);
+    };
     const uint32_t ring = smem_u32(smem + GE::kOffRing);
     const uint32_t qbuf = smem_u32(smem + GE::kOffQ);
     const uint32_t pbuf = smem_u32(smem + GE::kOffP);
@@ -934,11 +954,18 @@ __global__ void __launch_bounds__(dtc::Roles<std::is_same<KV, uint8_t>::value>::
           fence_async_smem();   // tile and Q^T written through the generic proxy
           tc_fence_after();
           if (leader) {
-            const uint32_t kb = ring + slot * kTileBytes, qb = qbuf + b * kQBytes;
+            const uint32_t kb = ring + slot * GE::kSlotBytes, qb = qbuf + b * GE::kQBytes;
+            if constexpr (kFp8) {
+              // 32 elements (32 B of each 128-byte row) per MMA; 8-row groups 1024 B apart
 #pragma unroll
-            for (int k = 0; k < kD / 16; ++k)
-              umma(col_s(b, j), umma_desc_sbo(kb + (k >> 2) * 1024 + (k & 3) * 32, 16, kAtomBytes),
-                   umma_desc(qb + (k >> 2) * (kNS * 128) + (k & 3) * 32, 16), idesc_s, k > 0 ? 1u : 0u);
+              for (int k = 0; k < kD / 32; ++k)
+                mma(col_s(b, j), umma_desc(kb + k * 32, 16), umma_desc(qb + k * 32, 16), idesc_s, k > 0 ? 1u : 0u);
+            } else {
+#pragma unroll
+              for (int k = 0; k < kD / 16; ++k)
+                mma(col_s(b, j), umma_desc_sbo(kb + (k >> 2) * 1024 + (k & 3) * 32, 16, kAtomBytes),
+                    umma_desc(qb + (k >> 2) * (kNS * 128) + (k & 3) * 32, 16), idesc_s, k > 0 ? 1u : 0u);
+            }
             umma_commit(&slot_free[slot]);
           }
           __syncwarp();
@@ -966,28 +993,42 @@ __global__ void __launch_bounds__(dtc::Roles<std::is_same<KV, uint8_t>::value>::
           ok = wait_all(&slot_full[slot], (g_cons / S) & 1);
           if (!ok) break;
           // keys past the end of the unit take part only up to the end of their
-          // 16-key group; their rows in that group may hold stale values (a whole
-          // atom is copied, and copies of later atoms are skipped), so they are
-          // zeroed: P is 0 there, and 0 * NaN would not be
+          // key group (16 keys per MMA, 32 with fp8); their rows in that group may
+          // hold stale values (a whole atom or cache block is copied, and copies
+          // of later ones are skipped), so they are zeroed: P is 0 there, and
+          // 0 * NaN would not be
+          constexpr int kGroup = kFp8 ? 32 : 16;
           const int nvalid = min(kKeys, prev.ntok - j * kKeys);
-          const int ngroups = (nvalid + 15) >> 4;
-          uint8_t *vt = smem + GE::kOffRing + slot * kTileBytes;
-          if (!kFp8 && (nvalid & 15)) {
-            for (int e = lane; e < (16 * ngroups - nvalid) * 16; e += 32) {
-              const int r = nvalid + (e >> 4), c = e & 15;   // row, 16-byte chunk of its 256 B
-              *reinterpret_cast<uint4 *>(vt + (r >> 3) * kAtomBytes + (c >> 3) * 1024 + (r & 7) * 128 + (c & 7) * 16) =
-                  make_uint4(0, 0, 0, 0);
+          const int ngroups = (nvalid + kGroup - 1) / kGroup;
+          uint8_t *vt = smem + GE::kOffRing + slot * GE::kSlotBytes;
+          if (nvalid % kGroup) {
+            if constexpr (kFp8) {
+              for (int e = lane; e < (kGroup * ngroups - nvalid) * 8; e += 32)   // rows of 128 B
+                *reinterpret_cast<uint4 *>(vt + (nvalid + (e >> 3)) * 128 + (e & 7) * 16) = make_uint4(0, 0, 0, 0);
+            } else {
+              for (int e = lane; e < (kGroup * ngroups - nvalid) * 16; e += 32) {
+                const int r = nvalid + (e >> 4), c = e & 15;   // row, 16-byte chunk of its 256 B
+                *reinterpret_cast<uint4 *>(vt + (r >> 3) * kAtomBytes + (c >> 3) * 1024 + (r & 7) * 128 +
+                                           (c & 7) * 16) = make_uint4(0, 0, 0, 0);
+              }
             }
             __syncwarp();
           }
-          fence_async_smem();   // zeroed rows, P^T (and fp8 tiles) written through the generic proxy
+          fence_async_smem();   // zeroed rows and P^T written through the generic proxy
           tc_fence_after();
           if (leader) {
-            const uint32_t vb = ring + slot * kTileBytes, pb = pbuf + (bp * kMaxTiles + j) * GE::kPBytes;
-            for (int kk = 0; kk < ngroups; ++kk)
-              umma(col_o(bp), umma_desc_sbo(vb + kk * 2 * kAtomBytes, 1024, kAtomBytes),
-                   umma_desc(pb + (kk >> 2) * (kNO * 128) + (kk & 3) * 32, 16), idesc_o,
-                   (j > 0 || kk > 0) ? 1u : 0u);
+            const uint32_t vb = ring + slot * GE::kSlotBytes, pb = pbuf + (bp * kMaxTiles + j) * GE::kPBytes;
+            if constexpr (kFp8) {
+              // V^T: one 128-element MN panel, 8-key groups 1024 B apart, 32 keys per MMA
+              for (int kk = 0; kk < ngroups; ++kk)
+                mma(col_o(bp), umma_desc_sbo(vb + kk * 4096, 1024, 1024), umma_desc(pb + kk * 32, 16), idesc_o,
+                    (j > 0 || kk > 0) ? 1u : 0u);
+            } else {
+              for (int kk = 0; kk < ngroups; ++kk)
+                mma(col_o(bp), umma_desc_sbo(vb + kk * 2 * kAtomBytes, 1024, kAtomBytes),
+                    umma_desc(pb + (kk >> 2) * (kNO * 128) + (kk & 3) * 32, 16), idesc_o,
+                    (j > 0 || kk > 0) ? 1u : 0u);
+            }
             umma_commit(&slot_free[slot]);
           }
           __syncwarp();
@@ -1091,7 +1132,7 @@ cudaError_t launch_decode_tc_one(const DecodeTcParams &p, const PoolMaps &m, cud
   // programmatic dependent launch: the decode grid's set-up overlaps the plan kernel
   cudaLaunchConfig_t cfg{};
   cfg.gridDim = dim3((unsigned)sms);
-  cfg.blockDim = dim3(dtc::Roles<std::is_same<KV, uint8_t>::value>::kThreads);
+  cfg.blockDim = dim3(dtc::Roles::kThreads);
   cfg.dynamicSmemBytes = smem;
   cfg.stream = s;
   cudaLaunchAttribute attr[1];
@@ -1103,7 +1144,8 @@ cudaError_t launch_decode_tc_one(const DecodeTcParams &p, const PoolMaps &m, cud
 }
 
 // m: tensor maps over the pools, one box per cache block of one KV head: 16-bit
-// caches viewed as [atoms of 8 rows][2 panels][8 rows][64], fp8 caches as [rows][128].
+// caches viewed as [atoms of 8 rows][2 panels][8 rows][64], fp8 caches as [rows][128]
+// (128-byte swizzle).
 template <typename KV, typename QT>
 cudaError_t launch_decode_tc(const DecodeTcParams &p, int gqa, const PoolMaps &m, cudaStream_t s) {
   switch (gqa) {

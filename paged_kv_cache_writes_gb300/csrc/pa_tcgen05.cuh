@@ -2,8 +2,9 @@
 // (sm_103a) shared by the tensor-core attention kernels: UMMA shared-memory
 // and instruction descriptors, tcgen05.mma / commit / ld / st, the fences
 // between the generic and async proxies, elected-lane issue, bounded waits
-// that honour a CTA-wide abort flag, 16-byte cp.async with zero-fill, and
-// the exact e4m3 -> 16-bit widening used to feed fp8 caches to kind::f16.
+// that honour a CTA-wide abort flag, 16-byte cp.async with zero-fill, the
+// exact e4m3 -> 16-bit widening used to feed fp8 caches to kind::f16, and
+// the two-term e4m3 split of fp32 operands for kind::f8f6f4.
 #pragma once
 
 #include <type_traits>
@@ -40,6 +41,27 @@ __device__ __forceinline__ void umma(uint32_t tmem_d, uint64_t a, uint64_t b, ui
       "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(tmem_d),
       "l"(a), "l"(b), "r"(idesc), "r"(acc)
       : "memory");
+}
+
+// The same with 8-bit operands (kind::f8f6f4; an instruction descriptor whose
+// A and B formats are 0 selects e4m3 x e4m3), K = 32 per instruction.
+__device__ __forceinline__ void umma_f8(uint32_t tmem_d, uint64_t a, uint64_t b, uint32_t idesc, uint32_t acc) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], %1, %2, %3, p;\n\t}" ::"r"(tmem_d),
+      "l"(a), "l"(b), "r"(idesc), "r"(acc)
+      : "memory");
+}
+
+// x -> two e4m3 codes with x = hi + lo / 16 + err: hi = e4m3(x), lo =
+// e4m3(16 (x - hi)) (round to nearest even; x - hi is exact in fp32).  For
+// |x| <= 256, |err| <= 2^-8 |x| + 2^-14 (hi is within 2^-4 |x| of x, lo
+// within 2^-4 of its argument or half of e4m3's subnormal step 2^-9), and
+// nothing saturates.  Two values at a time: bytes (x0, x1) of each 16-bit result.
+__device__ __forceinline__ void split2_e4m3(float2 x, uint32_t &hi, uint32_t &lo) {
+  hi = __nv_cvt_float2_to_fp8x2(x, __NV_SATFINITE, __NV_E4M3);
+  const float2 h = unpack2_e4m3(hi);
+  lo = __nv_cvt_float2_to_fp8x2(make_float2((x.x - h.x) * 16.f, (x.y - h.y) * 16.f), __NV_SATFINITE, __NV_E4M3);
 }
 
 // Arrive once on `bar` when every tcgen05 operation this thread issued so far is complete.
