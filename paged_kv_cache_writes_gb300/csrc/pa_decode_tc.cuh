@@ -56,18 +56,20 @@
 // claimed from an atomic cursor by a persistent CTA per SM.  Roles:
 //  * warps 0-3, softmax and epilogue: thread i owns tensor-memory lane i (key
 //    i of a score tile, element d = i of an output row);
-//  * loader warp: stages Q^T (cp.async; fp8: converted to its two e4m3
-//    terms) and streams the unit's K tiles, then the previous unit's V
-//    tiles, with one bulk-tensor copy per cache block straight into a ring
-//    of tiles in the MMA's 128-byte-swizzled layout (32 KB for a 16-bit
-//    cache, 16 KB for fp8);
+//  * loader warp: stages Q^T (16-bit caches, cp.async) and streams the
+//    unit's K tiles, then the previous unit's V tiles, with one bulk-tensor
+//    copy per cache block straight into a ring of tiles in the MMA's
+//    128-byte-swizzled layout (32 KB for a 16-bit cache, 16 KB for fp8);
 //  * MMA warp (one elected lane issues): S^T of unit u, then O^T of unit
 //    u-1, whose softmax ran while the scores of u were computed;
 //  * scheduler warp: claims units two at a time and publishes each, with
-//    the block ids of its tiles (and, fp8, the scale of its query rows), in
-//    a ring of four descriptors, so the chain
+//    the block ids of its tiles, in a ring of four descriptors, so the chain
 //    of dependent reads behind a claim (cursor, work item, sequence length,
-//    block table) runs ahead of the loads instead of between them;
+//    block table) runs ahead of the loads instead of between them.  It also
+//    stores a fused step's new token (pa_decode_write) before publishing the
+//    unit that reads it, and with an fp8 cache writes the unit's Q^T (the
+//    query rows' scale and two e4m3 terms) beside the descriptor, so that no
+//    dependent global read stalls the loader;
 //  * merge warp: merges split rows taken from a grid-wide list that the
 //    softmax warps append to, so the merging is shared by every CTA.
 //
@@ -156,13 +158,16 @@ struct TcGeo {
   static constexpr int kNS = kFp8 ? kNO : 16;                       // S^T columns per tile (MMA N)
   static constexpr int kSCols = kFp8 ? 2 * G : G;                   // S^T columns in use
   static constexpr int kQBytes = kFp8 ? kNS * 128 : 2 * kNS * 128;  // Q^T of a unit
+  // Q^T buffers: fp8, one per unit descriptor (written by the scheduler warp
+  // with the descriptor); 16-bit, two (copied by the loader per unit parity)
+  static constexpr int kQBufs = kFp8 ? kInfo : 2;
   static constexpr int kPBytes = kFp8 ? kNO * 128 : 2 * kNO * 128;  // P^T of a tile
   static constexpr int kSlotBytes = kFp8 ? kKeys * kD : kKeys * kD * 2;   // one K or V tile
   static constexpr int kColO = 2 * kMaxTiles * kNS;                 // tensor-memory column of O^T, buffer 0
   static constexpr int kTmemCols = kColO + 2 * kNO <= 256 ? 256 : 512;
   static constexpr int kNumBars = 2 * kMaxSlots + 8 * 2 + 2 * kInfo + 1;
-  static constexpr int kOffQ = 0;                                        // [2] Q^T
-  static constexpr int kOffP = kOffQ + 2 * kQBytes;                      // [2][4] P^T
+  static constexpr int kOffQ = 0;                                        // [kQBufs] Q^T
+  static constexpr int kOffP = kOffQ + kQBufs * kQBytes;                 // [2][4] P^T
   static constexpr int kOffRed = kOffP + 2 * kMaxTiles * kPBytes;        // float [2][4 warps][2][16]
   static constexpr int kOffInfo = kOffRed + 2 * 4 * 2 * 16 * 4;          // TcUnit [kInfo] (16-byte aligned)
   static constexpr int kOffBar = kOffInfo + kInfo * (int)sizeof(TcUnit);
@@ -313,7 +318,7 @@ __global__ void __launch_bounds__(dtc::Roles::kThreads, 1)
   uint64_t *o_full = p_full + 2;              // [2] O^T complete
   uint64_t *o_free = o_full + 2;              // [2] O^T read by every softmax thread (128)
   uint64_t *red_bar = o_free + 2;             // [2] per-warp maxima and sums exchanged (128)
-  uint64_t *info_full = red_bar + 2;          // [kInfo] unit descriptor published
+  uint64_t *info_full = red_bar + 2;          // [kInfo] unit descriptor published (32 scheduler lanes)
   uint64_t *info_free = info_full + kInfo;    // [kInfo] released by the MMA warp and the softmax warps
   uint64_t *fin = info_free + kInfo;          // every MMA of the CTA complete
   TcUnit *info = reinterpret_cast<TcUnit *>(smem + GE::kOffInfo);
@@ -342,7 +347,7 @@ __global__ void __launch_bounds__(dtc::Roles::kThreads, 1)
       mbar_init(&red_bar[b], 128);
     }
     for (int i = 0; i < kInfo; ++i) {
-      mbar_init(&info_full[i], 1);
+      mbar_init(&info_full[i], 32);   // every scheduler lane, after its own stores
       mbar_init(&info_free[i], 2);
     }
     mbar_init(fin, 1);
@@ -390,10 +395,11 @@ __global__ void __launch_bounds__(dtc::Roles::kThreads, 1)
     prev.valid = 0;
     bool ok = true;
     // Completion of split units, per warp.  A unit's partial results are written
-    // in one epilogue (pending), reported in the next (fence, then one count per
-    // warp on the row's counter: by then the fence finds the writes done), and
-    // the count returned is checked in the one after (reported); the warp that
-    // brings a row's count to 4 * nparts appends it to the merge list.
+    // in one epilogue (pending), reported in the next (one count per warp on the
+    // row's counter, an acquire-release atomic: it publishes the warp's results
+    // and, for the last count, acquires everyone else's), and the count returned
+    // is checked in the one after (reported); the warp that brings a row's count
+    // to 4 * nparts appends it to the merge list.
     int pend_row = -1, pend_kvh = 0, pend_np = 0;
     int rep_row = -1, rep_kvh = 0, rep_np = 0, rep_old = 0;
     // append a merge record (one thread); any CTA's merge warp may take it
@@ -408,19 +414,16 @@ __global__ void __launch_bounds__(dtc::Roles::kThreads, 1)
     auto check_reported = [&]() {
       if (rep_row >= 0) {
         const int last = __shfl_sync(0xffffffffu, rep_old, 0) == 4 * rep_np - 1;
-        if (last && lane == 0) {
-          __threadfence();   // the other partitions' results, observed through the counter
-          queue_job(rep_row, rep_kvh, rep_np);
-        }
+        // lane 0's count acquired the other partitions' results; the record's release passes them on
+        if (last && lane == 0) queue_job(rep_row, rep_kvh, rep_np);
         rep_row = -1;
       }
     };
     auto report_pending = [&]() {
       if (pend_row >= 0) {
-        __threadfence();
-        __syncwarp();
+        __syncwarp();   // the warp's stores of the unit's results precede lane 0's release
         if (lane == 0)
-          rep_old = atomicAdd(p.ws_count + (int64_t)pend_row * hq + (int64_t)pend_kvh * G, 1);
+          rep_old = atom_add_acq_rel_gpu(p.ws_count + (int64_t)pend_row * hq + (int64_t)pend_kvh * G, 1);
         rep_row = pend_row;
         rep_kvh = pend_kvh;
         rep_np = pend_np;
@@ -610,52 +613,13 @@ __global__ void __launch_bounds__(dtc::Roles::kThreads, 1)
     }
   } else if (warp == kLoadWarp) {
     // ===================================================== loader (one warp)
-    // Q^T with cp.async (fp8: loaded, scaled and split into two e4m3 terms);
-    // every K and V tile with one bulk-tensor box per cache block holding keys
-    // of the unit (tiles start on block boundaries), straight into the ring in
-    // the MMA's layout: 16-bit caches bs / 8 atoms per box, fp8 bs rows of 128
-    // codes per box.
+    // Q^T with cp.async (16-bit caches); every K and V tile with one
+    // bulk-tensor box per cache block holding keys of the unit (tiles start on
+    // block boundaries), straight into the ring in the MMA's layout: 16-bit
+    // caches bs / 8 atoms per box, fp8 bs rows of 128 codes per box.
     const int bs = p.block_size;
     uint32_t g_load = 0;
     bool ok = true;
-    // Store the new token of unit un's row (K and V of its KV head) in its slot,
-    // the slot of the row's last position (else PA_ERR_DEVICE_CHECK and no
-    // store), then order the stores before the bulk copies that read them.
-    auto write_new = [&](const UnitHdr &un, int ibx) {
-      const int64_t slot = __ldg(tp.new_slots + un.row);
-      if (slot < 0) return;
-      const int pos = un.tok_begin + un.ntok - 1, rel = pos - un.tok_begin;
-      const int32_t bi = reinterpret_cast<const volatile int32_t *>(info[ibx].blk)[8 * (rel >> 7) + ((rel & 127) >> 4)];
-      if (bi < 0 || slot != (int64_t)bi * bs + pos % bs) {
-        if (lane == 0) record_error(p.err, PA_ERR_DEVICE_CHECK);
-        return;
-      }
-      const int64_t row = ((int64_t)bi * hkv + un.kvh) * bs + pos % bs;
-      const int side = lane >> 4, c = lane & 15;   // lanes 0-15: K, 16-31: V; 8 elements each
-      const uint4 x = __ldg(reinterpret_cast<const uint4 *>(
-          static_cast<const QT *>(side ? tp.v_new : tp.k_new) + (int64_t)un.row * tp.new_stride +
-          (int64_t)un.kvh * kD + c * 8));
-      if constexpr (!kFp8) {
-        *reinterpret_cast<uint4 *>(static_cast<QT *>(const_cast<void *>(side ? tp.v_cache : tp.k_cache)) + row * kD +
-                                   c * 8) = x;
-      } else {
-        const float sc = p.k_hs ? __ldg((side ? p.v_hs : p.k_hs) + un.kvh) : side ? tp.v_scale : tp.k_scale;
-        const uint32_t w[4] = {x.x, x.y, x.z, x.w};
-        uint32_t o[2];
-#pragma unroll
-        for (int k = 0; k < 4; ++k) {
-          const float2 f = unpack2(w[k], QT{});
-          const uint32_t pair =
-              __nv_cvt_float2_to_fp8x2(make_float2(__fdiv_rn(f.x, sc), __fdiv_rn(f.y, sc)), __NV_SATFINITE, __NV_E4M3);
-          if (k & 1) o[k >> 1] |= pair << 16;
-          else o[k >> 1] = pair;
-        }
-        *reinterpret_cast<uint2 *>(static_cast<uint8_t *>(const_cast<void *>(side ? tp.v_cache : tp.k_cache)) +
-                                   row * kD + c * 8) = make_uint2(o[0], o[1]);
-      }
-      asm volatile("fence.proxy.async;" ::: "memory");   // generic stores -> the async proxy's copies
-      __syncwarp();
-    };
     UnitHdr prev;
     prev.valid = 0;
     for (int u = 0; ok; ++u) {
@@ -664,60 +628,28 @@ __global__ void __launch_bounds__(dtc::Roles::kThreads, 1)
       if (!ok) break;
       const UnitHdr cur = read_unit(&info[ib]);
       const int ntc = num_tiles(cur), ntp = num_tiles(prev);
-      // fused write into an empty row: there is no last position to hold the token
-      if (tp.k_new != nullptr && cur.valid && cur.ntok == 0 && lane == 0 && __ldg(tp.new_slots + cur.row) >= 0)
-        record_error(p.err, PA_ERR_DEVICE_CHECK);
-      if (cur.valid) {
+      if (!kFp8 && cur.valid) {
         // Q^T rows: the G query heads of the KV head, 256 B each
         if (u >= 2) {
           ok = wait_all(&q_free[b], ((u >> 1) - 1) & 1);
           if (!ok) break;
         }
-        if constexpr (kFp8) {
-          // q 2^e = hi + lo / 16: elements d .. d+7 of head h are bytes d .. d+7 of rows h and G + h
-          const float qs = __int_as_float(cur.qscale);
-          uint8_t *qb = smem + GE::kOffQ + b * GE::kQBytes;
 #pragma unroll
-          for (int e = lane; e < G * 16; e += 32) {
-            const int h = e >> 4, c16 = e & 15;
-            const uint4 w = ld_nc16(static_cast<const char *>(p.q) +
-                                    (((int64_t)cur.row * hq + (int64_t)cur.kvh * G + h) * kD) * 2 + c16 * 16);
-            const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
-            uint32_t hi[4], lo[4];
-#pragma unroll
-            for (int k = 0; k < 4; ++k) {
-              const float2 f = unpack2(ws[k], QT{});
-              split2_e4m3(make_float2(f.x * qs, f.y * qs), hi[k], lo[k]);
-            }
-            const int hr = h, lr = G + h, half = (c16 & 1) * 8;
-            *reinterpret_cast<uint2 *>(qb + hr * 128 + ((((c16 >> 1) ^ (hr & 7))) << 4) + half) =
-                make_uint2(hi[0] | (hi[1] << 16), hi[2] | (hi[3] << 16));
-            *reinterpret_cast<uint2 *>(qb + lr * 128 + ((((c16 >> 1) ^ (lr & 7))) << 4) + half) =
-                make_uint2(lo[0] | (lo[1] << 16), lo[2] | (lo[3] << 16));
-          }
-          fence_async_smem();
-          mbar_arrive(&q_full[b]);
-        } else {
-#pragma unroll
-          for (int e = lane; e < G * 16; e += 32) {
-            const int h = e >> 4, c16 = e & 15;
-            const char *src = static_cast<const char *>(p.q) +
-                              (((int64_t)cur.row * hq + (int64_t)cur.kvh * G + h) * kD) * 2 + c16 * 16;
-            cp_async16(smem + GE::kOffQ + b * GE::kQBytes + (c16 >> 3) * (kNS * 128) + h * 128 +
-                           (((c16 & 7) ^ (h & 7)) << 4),
-                       src, 16u);
-          }
-          cp_async_arrive_noinc(&q_full[b]);
+        for (int e = lane; e < G * 16; e += 32) {
+          const int h = e >> 4, c16 = e & 15;
+          const char *src = static_cast<const char *>(p.q) +
+                            (((int64_t)cur.row * hq + (int64_t)cur.kvh * G + h) * kD) * 2 + c16 * 16;
+          cp_async16(smem + GE::kOffQ + b * GE::kQBytes + (c16 >> 3) * (kNS * 128) + h * 128 +
+                         (((c16 & 7) ^ (h & 7)) << 4),
+                     src, 16u);
         }
+        cp_async_arrive_noinc(&q_full[b]);
       }
       // tiles in the MMA's order: K tiles of this unit, then V tiles of the previous one
       for (int i = 0; i < ntc + ntp && ok; ++i) {
         const bool is_k = i < ntc;
         const UnitHdr &un = is_k ? cur : prev;
         const int j = is_k ? i : i - ntc;
-        // fused write: the row's new token, for this KV head, before the copy of
-        // its last tile (its V tile is copied later still)
-        if (tp.k_new != nullptr && is_k && j == ntc - 1 && un.part == un.nparts - 1) write_new(un, ib);
         const int slot = (int)(g_load % S);
         uint64_t *free_bar = &slot_free[slot];
         uint64_t *full_bar = &slot_full[slot];
@@ -761,6 +693,32 @@ __global__ void __launch_bounds__(dtc::Roles::kThreads, 1)
     const int total_units = __ldcg(&p.hdr->num_items) * hkv;
     const int64_t cap = min((int64_t)p.max_blocks_per_seq * bs, (int64_t)p.max_partitions * p.partition_size);
     bool ok = true;
+    // Store a new token's 16 bytes x (lanes 0-15: K, 16-31: V; elements 8c ..
+    // 8c+7; fp8: e4m3(fp32(x) / sc) with an IEEE division, as the cache-write
+    // kernel) at cache row crow = (block * Hkv + kvh) * bs + offset, then order
+    // the generic stores before the bulk copies that read them (issued by the
+    // loader after it acquires the unit's descriptor).
+    auto store_new = [&](uint4 x, float sc, int64_t crow) {
+      const int side = lane >> 4, c = lane & 15;
+      if constexpr (!kFp8) {
+        *reinterpret_cast<uint4 *>(static_cast<QT *>(const_cast<void *>(side ? tp.v_cache : tp.k_cache)) + crow * kD +
+                                   c * 8) = x;
+      } else {
+        const uint32_t w[4] = {x.x, x.y, x.z, x.w};
+        uint32_t o[2];
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+          const float2 f = unpack2(w[k], QT{});
+          const uint32_t pair =
+              __nv_cvt_float2_to_fp8x2(make_float2(__fdiv_rn(f.x, sc), __fdiv_rn(f.y, sc)), __NV_SATFINITE, __NV_E4M3);
+          if (k & 1) o[k >> 1] |= pair << 16;
+          else o[k >> 1] = pair;
+        }
+        *reinterpret_cast<uint2 *>(static_cast<uint8_t *>(const_cast<void *>(side ? tp.v_cache : tp.k_cache)) +
+                                   crow * kD + c * 8) = make_uint2(o[0], o[1]);
+      }
+      asm volatile("fence.proxy.async.global;" ::: "memory");   // generic stores -> the async proxy's copies
+    };
     for (int u = 0; ok; u += kClaim) {
       for (int k = 0; k < kClaim && ok; ++k)
         if (u + k >= kInfo) ok = wait_all(&info_free[(u + k) % kInfo], (((u + k) / kInfo) - 1) & 1);
@@ -788,18 +746,59 @@ __global__ void __launch_bounds__(dtc::Roles::kThreads, 1)
         const int rk = __shfl_sync(0xffffffffu, row, k);
         const int tb = __shfl_sync(0xffffffffu, tok_begin, k);
         const int nk = __shfl_sync(0xffffffffu, ntok, k);
+        const int kvk = __shfl_sync(0xffffffffu, id % hkv, k);
+        const int pk = __shfl_sync(0xffffffffu, part, k);
+        const int npk = __shfl_sync(0xffffffffu, nparts, k);
+        // fused step: the row's new token goes with its last partition; its loads
+        // are in flight with the block-table reads below
+        const bool wr = tp.k_new != nullptr && vk && pk == npk - 1;
+        int64_t new_slot = -1;
+        uint4 new_x = make_uint4(0, 0, 0, 0);
+        float new_sc = 1.f;
+        if (wr) {
+          const int side = lane >> 4;
+          new_slot = __ldg(tp.new_slots + rk);
+          new_x = __ldg(reinterpret_cast<const uint4 *>(static_cast<const QT *>(side ? tp.v_new : tp.k_new) +
+                                                        (int64_t)rk * tp.new_stride + (int64_t)kvk * kD +
+                                                        (lane & 15) * 8));
+          if (kFp8) new_sc = p.k_hs ? __ldg((side ? p.v_hs : p.k_hs) + kvk) : side ? tp.v_scale : tp.k_scale;
+        }
         int32_t qscale = 0;
         if constexpr (kFp8) {
+          // Q^T of the unit, in the buffer of its descriptor (free: the descriptor's
+          // last reader released it): q 2^e = hi + lo / 16; elements d .. d+7 of
+          // head h are bytes d .. d+7 of rows h and G + h
+          uint4 qw[G / 2];
           float amax = 0.f;
-          if (vk) {
-            const int kvk = __shfl_sync(0xffffffffu, id % hkv, k);
-            const char *q0 = static_cast<const char *>(p.q) + ((int64_t)rk * hq + (int64_t)kvk * G) * kD * 2;
+          const char *q0 = static_cast<const char *>(p.q) + ((int64_t)rk * hq + (int64_t)kvk * G) * kD * 2;
 #pragma unroll
-            for (int e = lane; e < G * 16; e += 32) amax = fmaxf(amax, absmax8(ld_nc16(q0 + e * 16), QT{}));
-#pragma unroll
-            for (int m = 16; m > 0; m >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, m));
+          for (int i = 0; i < G / 2; ++i) {
+            qw[i] = vk ? ld_nc16(q0 + (lane + 32 * i) * 16) : make_uint4(0, 0, 0, 0);
+            amax = fmaxf(amax, absmax8(qw[i], QT{}));
           }
+#pragma unroll
+          for (int m = 16; m > 0; m >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, m));
           qscale = query_scale_bits(amax);
+          if (vk) {
+            const float qs = __int_as_float(qscale);
+            uint8_t *qb = smem + GE::kOffQ + ((u + k) % kInfo) * GE::kQBytes;
+#pragma unroll
+            for (int i = 0; i < G / 2; ++i) {
+              const int e = lane + 32 * i, h = e >> 4, c16 = e & 15, lr = G + h, half = (c16 & 1) * 8;
+              const uint32_t ws[4] = {qw[i].x, qw[i].y, qw[i].z, qw[i].w};
+              uint32_t hi[4], lo[4];
+#pragma unroll
+              for (int c = 0; c < 4; ++c) {
+                const float2 f = unpack2(ws[c], QT{});
+                split2_e4m3(make_float2(f.x * qs, f.y * qs), hi[c], lo[c]);
+              }
+              *reinterpret_cast<uint2 *>(qb + h * 128 + (((c16 >> 1) ^ (h & 7)) << 4) + half) =
+                  make_uint2(hi[0] | (hi[1] << 16), hi[2] | (hi[3] << 16));
+              *reinterpret_cast<uint2 *>(qb + lr * 128 + (((c16 >> 1) ^ (lr & 7)) << 4) + half) =
+                  make_uint2(lo[0] | (lo[1] << 16), lo[2] | (lo[3] << 16));
+            }
+            fence_async_smem();   // generic stores -> the MMAs' reads (after the descriptor's release)
+          }
         }
         TcUnit *dst = &info[(u + k) % kInfo];
         const int key0 = tb + (lane >> 3) * kKeys + 16 * (lane & 7);
@@ -810,10 +809,22 @@ __global__ void __launch_bounds__(dtc::Roles::kThreads, 1)
           else blk = bi;
         }
         dst->blk[lane] = blk;
+        // fused step: the row's new token, for this KV head, stored before the
+        // unit that reads it (the row's last partition) is published
+        if (wr && new_slot >= 0) {
+          const int pos = tb + nk - 1;
+          const int32_t bi = __shfl_sync(0xffffffffu, blk, max(nk - 1, 0) >> 4);
+          if (nk == 0 || bi < 0 || new_slot != (int64_t)bi * bs + pos % bs) {
+            // an empty row has no last position to hold the token; else the slot must be its
+            if (lane == 0) record_error(p.err, PA_ERR_DEVICE_CHECK);
+          } else {
+            store_new(new_x, new_sc, ((int64_t)bi * hkv + kvk) * bs + pos % bs);
+          }
+        }
         if (lane == k) {
           dst->valid = vk;
           dst->row = rk;
-          dst->kvh = vk ? id % hkv : 0;
+          dst->kvh = vk ? kvk : 0;
           dst->part = part;
           dst->tok_begin = tb;
           dst->ntok = nk;
@@ -823,8 +834,7 @@ __global__ void __launch_bounds__(dtc::Roles::kThreads, 1)
         any_invalid |= !vk;
       }
       __syncwarp();
-      if (lane == 0)
-        for (int k = 0; k < kClaim; ++k) mbar_arrive(&info_full[(u + k) % kInfo]);
+      for (int k = 0; k < kClaim; ++k) mbar_arrive(&info_full[(u + k) % kInfo]);
       if (any_invalid) break;   // the ids only grow: every later claim is past the end too
     }
   } else if (warp == kMergeWarp) {
@@ -945,8 +955,10 @@ __global__ void __launch_bounds__(dtc::Roles::kThreads, 1)
           ok = wait_all(&s_free[b], ((u >> 1) - 1) & 1);
           if (!ok) break;
         }
-        ok = wait_all(&q_full[b], (u >> 1) & 1);
-        if (!ok) break;
+        if constexpr (!kFp8) {   // fp8: Q^T was written with the descriptor
+          ok = wait_all(&q_full[b], (u >> 1) & 1);
+          if (!ok) break;
+        }
         for (int j = 0; j < nt; ++j) {
           const int slot = (int)(g_cons % S);
           ok = wait_all(&slot_full[slot], (g_cons / S) & 1);
@@ -954,7 +966,7 @@ __global__ void __launch_bounds__(dtc::Roles::kThreads, 1)
           fence_async_smem();   // tile and Q^T written through the generic proxy
           tc_fence_after();
           if (leader) {
-            const uint32_t kb = ring + slot * GE::kSlotBytes, qb = qbuf + b * GE::kQBytes;
+            const uint32_t kb = ring + slot * GE::kSlotBytes, qb = qbuf + (kFp8 ? ib : b) * GE::kQBytes;
             if constexpr (kFp8) {
               // 32 elements (32 B of each 128-byte row) per MMA; 8-row groups 1024 B apart
 #pragma unroll
@@ -975,7 +987,7 @@ __global__ void __launch_bounds__(dtc::Roles::kThreads, 1)
         if (!ok) break;
         if (leader) {
           umma_commit(&s_full[b]);
-          umma_commit(&q_free[b]);
+          if constexpr (!kFp8) umma_commit(&q_free[b]);
         }
         __syncwarp();
       }
