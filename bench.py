@@ -165,6 +165,45 @@ def measure_other_decodes(dev_name: str, steps: int, warmup: int) -> dict:
     return res
 
 
+def measure_mixed_step(dev_name: str, steps: int, warmup: int) -> dict:
+    """The chunked-prefill mixed batch (one 512-row chunk + 128 decodes, fp8 KV): its attention as two
+    calls (pa_prefill_chunk, then pa_decode) against one pa_mixed_step (prefill tiles and decode CTAs in
+    one grid), each timed with CUDA events over the same number of back-to-back steps."""
+    import torch
+    import workloads as W
+    import paged_kv_cache_writes_gb300 as pa
+    from paged_kv_cache_writes_gb300.staging import DeviceBatch
+    b = W.cfg_mixed_fp8()
+    db = DeviceBatch(b, dev_name)
+    db.run_setup()
+    db.write_step()
+
+    def two():
+        db.prefill_chunk()
+        db.decode()
+
+    res = {"workload": "chunked-prefill mixed batch, fp8 KV: 512-token chunk at 4096 + 128 decodes "
+                       "(256..8192 tokens), GQA 32/8, head_dim 128, block 16",
+           "kv_bytes_decode": b.decode_kv_bytes(), "useful_tflop_prefill": _causal_flops(b) / 1e12}
+    s = torch.cuda.current_stream()
+    for key, fn in (("two_calls", two), ("one_launch", db.mixed_attention)):
+        for _ in range(warmup):
+            fn()
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(s)
+        for _ in range(steps):
+            fn()
+        e1.record(s)
+        torch.cuda.synchronize()
+        assert pa.pa_get_device_error() == 0
+        res[key + "_ms"] = e0.elapsed_time(e1) / steps
+    res["speedup"] = res["two_calls_ms"] / res["one_launch_ms"]
+    del db
+    torch.cuda.empty_cache()
+    return res
+
+
 def measure_prefill(dev_name: str, steps: int, warmup: int) -> dict:
     import torch
     import workloads as W
@@ -555,6 +594,7 @@ def run_ours(args):
         torch.cuda.empty_cache()
         line["prefill"] = measure_prefill(dev_name, max(5, args.steps // 5), args.warmup)
         line["other_decodes"] = measure_other_decodes(dev_name, max(5, args.steps // 5), args.warmup)
+        line["mixed_step"] = measure_mixed_step(dev_name, max(5, args.steps // 5), args.warmup)
         line["block_manager"] = measure_block_manager()
     if not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_oracle_rate(b, args.cpu_seconds)

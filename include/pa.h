@@ -309,6 +309,69 @@ PA_API pa_status pa_prefill_chunk(const void *q_chunk, pa_dtype q_dtype,
                            pa_dtype out_dtype, pa_stream_t stream);
 
 /*
+ * pa_mixed_step -- one layer's chunked-prefill batch and decode batch in one
+ * call ([V07] "Architectural Blueprint 3: Chunked Prefill": prompt chunks are
+ * batched with decoding sequences; [HT] "5. Chunked Prefill & Latency SLA
+ * Management").  The results are exactly those of pa_prefill_chunk on the
+ * prefill part and of pa_decode_write (pa_decode when decode->k_new is null)
+ * on the decode part, with the shared arguments below.  Where both parts run
+ * on the tensor cores (head_dim 128, 4 or 8 query heads per KV head, the
+ * default decode kernel) they share one launch after the decode's plan
+ * kernel: the prefill chunks' tiles and the decode's persistent CTAs form one
+ * grid, so the tensor-bound and the bandwidth-bound work run side by side.
+ * Otherwise the decode and then the prefill are launched on the stream, as the
+ * two calls would launch them.
+ *
+ * The parts must not meet in the cache: the prefill chunks' own K/V must
+ * already be stored (as for pa_prefill_chunk), and no prefill chunk may read
+ * a block that a decode row's new token is written into.
+ *
+ *   decode   the decode part; num_seqs 0 for none.  Fields as the arguments
+ *            of pa_decode_write of the same names; k_new, v_new and
+ *            slot_mapping all null for no new tokens.
+ *   prefill  the prefill part; num_chunks 0 for none.  Fields as the
+ *            arguments of pa_prefill_chunk of the same names.
+ *   q_dtype, num_q_heads, k_cache, v_cache, cache, scale, out_dtype, stream:
+ *            shared by both parts, as for those calls.
+ * Errors: as those calls return them; nothing is launched when an argument
+ * of either part is invalid.
+ */
+typedef struct {
+  const void *q;                /* [num_seqs][num_q_heads][head_dim] */
+  int32_t num_seqs;
+  const int32_t *block_tables;  /* [num_seqs][max_blocks_per_seq] */
+  int32_t max_blocks_per_seq;
+  const int32_t *seq_lens;      /* [num_seqs] */
+  int32_t max_seq_len;
+  int32_t partition_size;
+  const void *k_new;            /* [num_seqs][num_kv_heads][head_dim], or null */
+  const void *v_new;
+  int64_t token_stride;
+  const int64_t *slot_mapping;  /* [num_seqs], or null */
+  void *workspace;              /* >= pa_decode_workspace_bytes(...) */
+  size_t workspace_bytes;
+  void *out;                    /* [num_seqs][num_q_heads][head_dim] */
+} pa_decode_part;
+
+typedef struct {
+  const void *q_chunk;          /* [total_q][num_q_heads][head_dim] */
+  const int32_t *cu_q_lens;     /* [num_chunks + 1] */
+  const int32_t *q_start;       /* [num_chunks] */
+  int32_t num_chunks;
+  int32_t max_q_len;
+  const int32_t *block_tables;  /* [num_chunks][max_blocks_per_seq] */
+  int32_t max_blocks_per_seq;
+  const int32_t *seq_lens;      /* [num_chunks] */
+  int32_t max_seq_len;
+  void *out;                    /* [total_q][num_q_heads][head_dim] */
+} pa_prefill_part;
+
+PA_API pa_status pa_mixed_step(const pa_decode_part *decode, const pa_prefill_part *prefill,
+                        pa_dtype q_dtype, int32_t num_q_heads, void *k_cache,
+                        void *v_cache, const pa_kv_cache *cache, float scale,
+                        pa_dtype out_dtype, pa_stream_t stream);
+
+/*
  * pa_get_device_error -- read and clear the current device's error word.
  * Synchronises `stream`, then stores into *code the first device-side status
  * recorded since the last clear (PA_OK if none): PA_ERR_DEVICE_CHECK for

@@ -20,6 +20,7 @@ __all__ = [
     "pa_reshape_and_cache", "pa_copy_blocks", "pa_decode_workspace_bytes", "pa_decode",
     "pa_prefill_chunk", "pa_get_device_error", "pa_status_string", "pa_selftest_wait_timeout",
     "BlockManager", "PaBmStats", "pa_set_decode_kernel", "decode_kernel", "DECODE_KERNELS", "pa_decode_write",
+    "pa_mixed_step", "PaDecodePart", "PaPrefillPart",
 ]
 
 PA_F16, PA_BF16, PA_FP8_E4M3, PA_F32 = 0, 1, 2, 3
@@ -42,6 +43,23 @@ class PaKvCache(ctypes.Structure):
                 ("num_kv_heads", ctypes.c_int32), ("head_dim", ctypes.c_int32),
                 ("kv_dtype", ctypes.c_int), ("k_scale", ctypes.c_float), ("v_scale", ctypes.c_float),
                 ("k_head_scales", ctypes.c_void_p), ("v_head_scales", ctypes.c_void_p)]
+
+
+class PaDecodePart(ctypes.Structure):
+    """Mirror of ``pa_decode_part``."""
+    _fields_ = [("q", ctypes.c_void_p), ("num_seqs", ctypes.c_int32), ("block_tables", ctypes.c_void_p),
+                ("max_blocks_per_seq", ctypes.c_int32), ("seq_lens", ctypes.c_void_p),
+                ("max_seq_len", ctypes.c_int32), ("partition_size", ctypes.c_int32), ("k_new", ctypes.c_void_p),
+                ("v_new", ctypes.c_void_p), ("token_stride", ctypes.c_int64), ("slot_mapping", ctypes.c_void_p),
+                ("workspace", ctypes.c_void_p), ("workspace_bytes", ctypes.c_size_t), ("out", ctypes.c_void_p)]
+
+
+class PaPrefillPart(ctypes.Structure):
+    """Mirror of ``pa_prefill_part``."""
+    _fields_ = [("q_chunk", ctypes.c_void_p), ("cu_q_lens", ctypes.c_void_p), ("q_start", ctypes.c_void_p),
+                ("num_chunks", ctypes.c_int32), ("max_q_len", ctypes.c_int32), ("block_tables", ctypes.c_void_p),
+                ("max_blocks_per_seq", ctypes.c_int32), ("seq_lens", ctypes.c_void_p),
+                ("max_seq_len", ctypes.c_int32), ("out", ctypes.c_void_p)]
 
 
 class PaBmStats(ctypes.Structure):
@@ -73,6 +91,8 @@ def lib() -> ctypes.CDLL:
                                       I32, P, I32, F, I32, P, SZ, P, ctypes.c_int, P]
         L.pa_prefill_chunk.argtypes = [P, ctypes.c_int, P, P, I32, I32, I32, P, P, ctypes.POINTER(PaKvCache), P,
                                        I32, P, I32, F, P, ctypes.c_int, P]
+        L.pa_mixed_step.argtypes = [ctypes.POINTER(PaDecodePart), ctypes.POINTER(PaPrefillPart), ctypes.c_int, I32,
+                                    P, P, ctypes.POINTER(PaKvCache), F, ctypes.c_int, P]
         L.pa_get_device_error.argtypes = [P, ctypes.POINTER(I32)]
         L.pa_set_decode_kernel.argtypes = [I32]
         L.pa_selftest_wait_timeout.argtypes = [P]
@@ -89,7 +109,7 @@ def lib() -> ctypes.CDLL:
         L.pa_bm_block_table.argtypes = [VP, I32, P, I32, ctypes.POINTER(I32), ctypes.POINTER(I32)]
         L.pa_bm_get_stats.argtypes = [VP, ctypes.POINTER(PaBmStats)]
         for name in ("pa_reshape_and_cache", "pa_copy_blocks", "pa_decode", "pa_prefill_chunk", "pa_set_decode_kernel",
-                     "pa_decode_write",
+                     "pa_decode_write", "pa_mixed_step",
                      "pa_get_device_error", "pa_selftest_wait_timeout", "pa_bm_create", "pa_bm_new_sequence",
                      "pa_bm_fork", "pa_bm_append", "pa_bm_free", "pa_bm_block_table", "pa_bm_get_stats"):
             getattr(L, name).restype = ctypes.c_int
@@ -223,6 +243,37 @@ def pa_prefill_chunk(q_chunk: torch.Tensor, cu_q_lens: torch.Tensor, q_start: to
                                int(max_seq_len), float(scale), _dev(out, "out"), _dtype_code(out.dtype),
                                _stream(stream)),
         "pa_prefill_chunk")
+
+
+def pa_mixed_step(q: torch.Tensor, block_tables: torch.Tensor, seq_lens: torch.Tensor, max_seq_len: int,
+                  out: torch.Tensor, q_chunk: torch.Tensor, cu_q_lens: torch.Tensor, q_start: torch.Tensor,
+                  max_q_len: int, chunk_block_tables: torch.Tensor, chunk_seq_lens: torch.Tensor,
+                  chunk_max_seq_len: int, chunk_out: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor,
+                  cache: PaKvCache, scale: float, workspace: torch.Tensor | None = None, partition_size: int = 0,
+                  k_new: torch.Tensor | None = None, v_new: torch.Tensor | None = None,
+                  slot_mapping: torch.Tensor | None = None, stream=None) -> None:
+    """One layer's decode batch (q ... out, with optional new tokens k_new / v_new / slot_mapping as for
+    pa_decode_write) and chunked-prefill batch (q_chunk ... chunk_out, as for pa_prefill_chunk) in one call."""
+    if (k_new is None) != (v_new is None) or (k_new is None) != (slot_mapping is None):
+        raise ValueError("k_new, v_new and slot_mapping go together")
+    if slot_mapping is not None and slot_mapping.dtype != torch.int64:
+        raise TypeError("slot_mapping must be int64")
+    d = PaDecodePart(q=_dev(q, "q"), num_seqs=q.shape[0], block_tables=_dev(block_tables, "block_tables"),
+                     max_blocks_per_seq=block_tables.shape[1], seq_lens=_dev(seq_lens, "seq_lens"),
+                     max_seq_len=int(max_seq_len), partition_size=int(partition_size),
+                     k_new=_dev(k_new, "k_new"), v_new=_dev(v_new, "v_new"),
+                     token_stride=0 if k_new is None else k_new.stride(0),
+                     slot_mapping=_dev(slot_mapping, "slot_mapping"), workspace=_dev(workspace, "workspace"),
+                     workspace_bytes=0 if workspace is None else workspace.numel() * workspace.element_size(),
+                     out=_dev(out, "out"))
+    pf = PaPrefillPart(q_chunk=_dev(q_chunk, "q_chunk"), cu_q_lens=_dev(cu_q_lens, "cu_q_lens"),
+                       q_start=_dev(q_start, "q_start"), num_chunks=q_start.shape[0], max_q_len=int(max_q_len),
+                       block_tables=_dev(chunk_block_tables, "chunk_block_tables"),
+                       max_blocks_per_seq=chunk_block_tables.shape[1], seq_lens=_dev(chunk_seq_lens, "chunk_seq_lens"),
+                       max_seq_len=int(chunk_max_seq_len), out=_dev(chunk_out, "chunk_out"))
+    _ok(lib().pa_mixed_step(ctypes.byref(d), ctypes.byref(pf), _dtype_code(q.dtype), q.shape[1],
+                            _dev(k_cache, "k_cache"), _dev(v_cache, "v_cache"), ctypes.byref(cache), float(scale),
+                            _dtype_code(out.dtype), _stream(stream)), "pa_mixed_step")
 
 
 def pa_get_device_error(stream=None) -> int:

@@ -268,12 +268,19 @@ struct NewTokens {
   const int64_t *slots;
 };
 
+// The prefill part of a one-launch mixed step (pa_mixed_step): the prefill
+// kernel's parameters as pa_prefill_chunk would pass them.
+struct MixedPrefill {
+  PrefillTcParams t;
+  int num_chunks;
+};
+
 pa_status decode_impl(const void *q, pa_dtype q_dtype, int32_t num_seqs, int32_t num_q_heads,
                       const void *k_cache, const void *v_cache, const pa_kv_cache *cache,
                       const int32_t *block_tables, int32_t max_blocks_per_seq, const int32_t *seq_lens,
                       int32_t max_seq_len, float scale, int32_t partition_size, void *workspace,
                       size_t workspace_bytes, void *out, pa_dtype out_dtype, pa_stream_t stream,
-                      const NewTokens *nt) {
+                      const NewTokens *nt, const MixedPrefill *mix = nullptr) {
   pa_status st = check_cache(cache);
   if (st != PA_OK) return st;
   const pa_kv_cache &c = *cache;
@@ -353,12 +360,22 @@ pa_status decode_impl(const void *q, pa_dtype q_dtype, int32_t num_seqs, int32_t
     if (fp8_cache ? (!encode_pool_map_fp8_blocks(&maps.k, k_cache, c) || !encode_pool_map_fp8_blocks(&maps.v, v_cache, c))
                   : (!encode_pool_map_atoms(&maps.k, k_cache, c) || !encode_pool_map_atoms(&maps.v, v_cache, c)))
       return PA_ERR_CUDA;
+    if (mix) {   // the prefill tiles join the decode's grid (pa_mixed_tc.cuh)
+      PrefillTcParams pt = mix->t;
+      pt.err = p.err;
+      if (c.kv_dtype == PA_BF16) e = launch_mixed_tc_bf16(tp, maps, pt, mix->num_chunks, gqa, s);
+      else if (c.kv_dtype == PA_F16) e = launch_mixed_tc_f16(tp, maps, pt, mix->num_chunks, gqa, s);
+      else if (q_dtype == PA_BF16) e = launch_mixed_tc_fp8_bf16q(tp, maps, pt, mix->num_chunks, gqa, s);
+      else e = launch_mixed_tc_fp8_f16q(tp, maps, pt, mix->num_chunks, gqa, s);
+      return e == cudaSuccess ? PA_OK : PA_ERR_CUDA;
+    }
     if (c.kv_dtype == PA_BF16) e = launch_decode_tc_bf16(tp, gqa, maps, s);
     else if (c.kv_dtype == PA_F16) e = launch_decode_tc_f16(tp, gqa, maps, s);
     else if (q_dtype == PA_BF16) e = launch_decode_tc_fp8_bf16q(tp, gqa, maps, s);
     else e = launch_decode_tc_fp8_f16q(tp, gqa, maps, s);
     return e == cudaSuccess ? PA_OK : PA_ERR_CUDA;
   }
+  if (mix) return PA_ERR_INVALID_ARG;   // the caller asks for one launch only where both parts use tensor cores
   if (nt &&   // CUDA-core decode: the cache write is its own launch, just before
       launch_reshape_and_cache(nt->k, nt->v, q_dtype, num_seqs, nt->stride, nt->slots, const_cast<void *>(k_cache),
                                const_cast<void *>(v_cache), c, p.err, s) != cudaSuccess)
@@ -407,13 +424,20 @@ pa_status pa_decode_write(const void *q, pa_dtype q_dtype, int32_t num_seqs, int
                      &nt);
 }
 
-pa_status pa_prefill_chunk(const void *q_chunk, pa_dtype q_dtype, const int32_t *cu_q_lens,
-                           const int32_t *q_start, int32_t num_chunks, int32_t max_q_len,
-                           int32_t num_q_heads, const void *k_cache, const void *v_cache,
-                           const pa_kv_cache *cache, const int32_t *block_tables,
-                           int32_t max_blocks_per_seq, const int32_t *seq_lens,
-                           int32_t max_seq_len, float scale, void *out, pa_dtype out_dtype,
-                           pa_stream_t stream) {
+}  // extern "C"
+
+namespace pa {
+namespace {
+// pa_prefill_chunk's argument checks.  PA_OK with *empty set: nothing to do;
+// otherwise *tc tells whether the tensor-core kernel applies, and then t holds
+// its parameters.
+pa_status prefill_prepare(const void *q_chunk, pa_dtype q_dtype, const int32_t *cu_q_lens, const int32_t *q_start,
+                          int32_t num_chunks, int32_t max_q_len, int32_t num_q_heads, const void *k_cache,
+                          const void *v_cache, const pa_kv_cache *cache, const int32_t *block_tables,
+                          int32_t max_blocks_per_seq, const int32_t *seq_lens, int32_t max_seq_len, float scale,
+                          void *out, pa_dtype out_dtype, bool *empty, bool *tc, PrefillTcParams *tp) {
+  *empty = false;
+  *tc = false;
   pa_status st = check_cache(cache);
   if (st != PA_OK) return st;
   const pa_kv_cache &c = *cache;
@@ -422,7 +446,10 @@ pa_status pa_prefill_chunk(const void *q_chunk, pa_dtype q_dtype, const int32_t 
     return PA_ERR_INVALID_ARG;
   if ((st = check_q_dtype(q_dtype, c)) != PA_OK) return st;
   if (out_dtype != q_dtype && out_dtype != PA_F32) return PA_ERR_UNSUPPORTED;
-  if (num_chunks == 0 || max_q_len == 0) return PA_OK;
+  if (num_chunks == 0 || max_q_len == 0) {
+    *empty = true;
+    return PA_OK;
+  }
   if (!q_chunk || !out || !cu_q_lens || !q_start || !block_tables || !seq_lens ||
       !aligned(q_chunk, 16) || !aligned(out, 16) || !aligned(cu_q_lens, 4) ||
       !aligned(q_start, 4) || !aligned(block_tables, 4) || !aligned(seq_lens, 4))
@@ -432,11 +459,11 @@ pa_status pa_prefill_chunk(const void *q_chunk, pa_dtype q_dtype, const int32_t 
   if (rows > 2147483647ll || num_q_heads > 65535) return PA_ERR_UNSUPPORTED;
   const bool fp8 = c.kv_dtype == PA_FP8_E4M3;
   const int gqa = num_q_heads / c.num_kv_heads;
-  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-
   if (prefill_tc_supported(c.head_dim, gqa)) {
-    // tensor-core tiles: 128 GQA-packed rows x 64-key tiles (pa_prefill_tc.cuh)
-    PrefillTcParams t{};
+    // tensor-core tiles: 128 GQA-packed rows x 128-key tiles (pa_prefill_tc.cuh)
+    *tc = true;
+    PrefillTcParams &t = *tp;
+    t = PrefillTcParams{};
     t.q = q_chunk;
     t.k_cache = k_cache;
     t.v_cache = v_cache;
@@ -456,6 +483,34 @@ pa_status pa_prefill_chunk(const void *q_chunk, pa_dtype q_dtype, const int32_t 
     t.out_mult = fp8 && !c.v_head_scales ? c.v_scale : 1.f;
     t.k_hs = c.k_head_scales;
     t.v_hs = c.v_head_scales;
+  }
+  return PA_OK;   // t.err is set by the caller, after every check
+}
+}  // namespace
+}  // namespace pa
+
+extern "C" {
+
+pa_status pa_prefill_chunk(const void *q_chunk, pa_dtype q_dtype, const int32_t *cu_q_lens,
+                           const int32_t *q_start, int32_t num_chunks, int32_t max_q_len,
+                           int32_t num_q_heads, const void *k_cache, const void *v_cache,
+                           const pa_kv_cache *cache, const int32_t *block_tables,
+                           int32_t max_blocks_per_seq, const int32_t *seq_lens,
+                           int32_t max_seq_len, float scale, void *out, pa_dtype out_dtype,
+                           pa_stream_t stream) {
+  bool empty = false, use_tc = false;
+  PrefillTcParams t{};
+  pa_status st = prefill_prepare(q_chunk, q_dtype, cu_q_lens, q_start, num_chunks, max_q_len, num_q_heads, k_cache,
+                                 v_cache, cache, block_tables, max_blocks_per_seq, seq_lens, max_seq_len, scale, out,
+                                 out_dtype, &empty, &use_tc, &t);
+  if (st != PA_OK || empty) return st;
+  const pa_kv_cache &c = *cache;
+  const int64_t rows = (int64_t)num_chunks * max_q_len;
+  const bool fp8 = c.kv_dtype == PA_FP8_E4M3;
+  const int gqa = num_q_heads / c.num_kv_heads;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+
+  if (use_tc) {
     t.err = device_error_word();
     if (!t.err) return PA_ERR_CUDA;
     cudaError_t e;
@@ -495,6 +550,44 @@ pa_status pa_prefill_chunk(const void *q_chunk, pa_dtype q_dtype, const int32_t 
   return dispatch_attention(q_dtype, c, p, maps, (int)rows, s) == cudaSuccess
              ? PA_OK
              : PA_ERR_CUDA;
+}
+
+pa_status pa_mixed_step(const pa_decode_part *d, const pa_prefill_part *pf, pa_dtype q_dtype, int32_t num_q_heads,
+                        void *k_cache, void *v_cache, const pa_kv_cache *cache, float scale, pa_dtype out_dtype,
+                        pa_stream_t stream) {
+  if (!d || !pf) return PA_ERR_INVALID_ARG;
+  pa_status st = check_cache(cache);
+  if (st != PA_OK) return st;
+  // every argument of the prefill part, checked as pa_prefill_chunk checks them
+  bool p_empty = false, p_tc = false;
+  MixedPrefill mp{};
+  st = prefill_prepare(pf->q_chunk, q_dtype, pf->cu_q_lens, pf->q_start, pf->num_chunks, pf->max_q_len, num_q_heads,
+                       k_cache, v_cache, cache, pf->block_tables, pf->max_blocks_per_seq, pf->seq_lens,
+                       pf->max_seq_len, scale, pf->out, out_dtype, &p_empty, &p_tc, &mp.t);
+  if (st != PA_OK) return st;
+  mp.num_chunks = pf->num_chunks;
+  // the decode part's new tokens, checked as pa_decode_write checks them
+  if (d->num_seqs < 0) return PA_ERR_INVALID_ARG;
+  const bool has_new = d->k_new || d->v_new || d->slot_mapping;
+  if (has_new && d->num_seqs > 0) {
+    if (d->token_stride < (int64_t)cache->num_kv_heads * cache->head_dim || d->token_stride % 8)
+      return PA_ERR_INVALID_ARG;
+    if (!d->k_new || !d->v_new || !d->slot_mapping || !aligned(d->k_new, 16) || !aligned(d->v_new, 16) ||
+        !aligned(d->slot_mapping, 8))
+      return PA_ERR_INVALID_ARG;
+  }
+  const NewTokens nt{d->k_new, d->v_new, d->token_stride, d->slot_mapping};
+  const int gqa = num_q_heads / cache->num_kv_heads;   // num_q_heads checked above
+  const bool one_launch = !p_empty && p_tc && d->num_seqs > 0 && mixed_tc_supported(cache->head_dim, gqa) &&
+                          decode_tc_supported(cache->head_dim, gqa) &&
+                          g_decode_kernel.load(std::memory_order_relaxed) == PA_DECODE_KERNEL_AUTO;
+  st = decode_impl(d->q, q_dtype, d->num_seqs, num_q_heads, k_cache, v_cache, cache, d->block_tables,
+                   d->max_blocks_per_seq, d->seq_lens, d->max_seq_len, scale, d->partition_size, d->workspace,
+                   d->workspace_bytes, d->out, out_dtype, stream, has_new ? &nt : nullptr, one_launch ? &mp : nullptr);
+  if (st != PA_OK || one_launch || p_empty) return st;
+  return pa_prefill_chunk(pf->q_chunk, q_dtype, pf->cu_q_lens, pf->q_start, pf->num_chunks, pf->max_q_len,
+                          num_q_heads, k_cache, v_cache, cache, pf->block_tables, pf->max_blocks_per_seq,
+                          pf->seq_lens, pf->max_seq_len, scale, pf->out, out_dtype, stream);
 }
 
 pa_status pa_selftest_wait_timeout(pa_stream_t stream) {

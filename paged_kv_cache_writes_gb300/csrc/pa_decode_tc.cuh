@@ -38,12 +38,14 @@
 //
 // fp8 caches: the e4m3 codes are the MMA operands as stored (kind::f8f6f4,
 // 32 keys or elements per MMA), so a tile goes from the bulk copy to the
-// MMAs untouched.  The other operand is then e4m3 too, as two terms: the
-// query rows scaled by a power of two 2^e per unit (|q| 2^e in [128, 256)
-// at the unit's largest element) and 256 p are each written as hi + lo / 16
-// (hi in rows 0..G-1 of Q^T / P^T, lo in rows G..2G-1), which holds every
-// value to 2^-8 of itself; the softmax and the epilogue add the two column
-// halves of S^T and O^T and undo the scales.
+// MMAs untouched.  The other operand is then e4m3 too, as a sum of terms:
+// 256 p is written as hi + lo / 16 (hi in rows 0..G-1 of P^T, lo in rows
+// G..2G-1), which holds it to 2^-8 of itself; the query rows, scaled by a
+// power of two 2^e per unit (|q| 2^e in [128, 256) at the unit's largest
+// element), likewise as hi + lo / 16 for bf16 queries (exact: 8 significant
+// bits) and as hi + mid / 16 + lo / 256 in rows 0..3G-1 for f16 queries (11
+// bits, held to 2^-12).  The softmax and the epilogue add the column groups
+// of S^T and O^T and undo the scales.
 //
 // Softmax per unit (no online rescale): all tiles of a unit (<= 4 x 128
 // keys) are scored first, the exact maximum per head over the unit comes from
@@ -144,19 +146,28 @@ struct TcUnit {
   int32_t blk[kMaxTiles * 8];
 };
 
+// e4m3 terms per query value with an fp8 cache: two hold a bf16 value's 8
+// significant bits, three an f16 value's 11; 1 (no split) for 16-bit caches.
+template <typename KV, typename QT>
+struct QTerms {
+  static constexpr int value = !std::is_same<KV, uint8_t>::value ? 1 : std::is_same<QT, __half>::value ? 3 : 2;
+};
+
 // Shared-memory and tensor-memory geometry.  16-bit caches: K/V tiles of
 // 32 KB (two 128-byte panels per 8-key atom), Q^T of 16 rows (the heads,
 // padded) and P^T of kNO rows, each in two 64-element panels.  fp8 caches:
 // tiles of 16 KB (128 rows of 128 codes, the layout a 2D bulk-tensor box
 // with 128-byte swizzle writes), Q^T and P^T of one 128-element panel
-// holding the hi terms in rows 0..G-1 and the lo terms in rows G..2G-1.
-template <int G, bool kSplit, bool kFp8>
+// holding the hi terms in rows 0..G-1, the lo terms in rows G..2G-1 (and
+// with three query terms, the last in rows 2G..3G-1 of Q^T).
+template <int G, bool kSplit, bool kFp8, int kQTerms = 1>
 struct TcGeo {
   static_assert(G == 4 || G == 8 || G == 16, "4, 8 or 16 query heads per KV head");
   static constexpr int kPRows = (kSplit || kFp8) ? 2 * G : G;       // P^T rows in use
   static constexpr int kNO = kPRows <= 16 ? 16 : 32;                // O^T columns (MMA N)
-  static constexpr int kNS = kFp8 ? kNO : 16;                       // S^T columns per tile (MMA N)
-  static constexpr int kSCols = kFp8 ? 2 * G : G;                   // S^T columns in use
+  static constexpr int kQRows = kQTerms * G;                        // Q^T rows in use
+  static constexpr int kNS = kQRows <= 16 ? 16 : (kQRows + 15) / 16 * 16;   // S^T columns per tile (MMA N)
+  static constexpr int kSCols = kFp8 ? kNS : G;                     // S^T columns read per tile
   static constexpr int kQBytes = kFp8 ? kNS * 128 : 2 * kNS * 128;  // Q^T of a unit
   // Q^T buffers: fp8, one per unit descriptor (written by the scheduler warp
   // with the descriptor); 16-bit, two (copied by the loader per unit parity)
@@ -203,9 +214,17 @@ __device__ __forceinline__ void tmem_ld_cols(uint32_t taddr, float (&v)[N]) {
     for (int i = 0; i < 8; ++i) v[i] = __uint_as_float(r[i]);
   } else if constexpr (N == 16) {
     tc::tmem_ld16(taddr, v);
-  } else {
-    static_assert(N == 32, "4, 8, 16 or 32 columns");
+  } else if constexpr (N == 32) {
     tc::tmem_ld32(taddr, v);
+  } else {
+    static_assert(N == 48, "4, 8, 16, 32 or 48 columns");
+    float a[32], b[16];
+    tc::tmem_ld32(taddr, a);
+    tc::tmem_ld16(taddr + 32, b);
+#pragma unroll
+    for (int i = 0; i < 32; ++i) v[i] = a[i];
+#pragma unroll
+    for (int i = 0; i < 16; ++i) v[32 + i] = b[i];
   }
 }
 
@@ -285,10 +304,12 @@ __device__ __forceinline__ int32_t query_scale_bits(float amax) {
 
 }  // namespace dtc
 
+// The decode CTA, for decode_tc_kernel and for the decode CTAs of the mixed
+// kernel (pa_mixed_tc.cuh).  Warps past the eight roles (a wider mixed block)
+// only take part in the two CTA-wide barriers.
 template <typename KV, typename QT, int G>
-__global__ void __launch_bounds__(dtc::Roles::kThreads, 1)
-    decode_tc_kernel(const DecodeTcParams tp, const __grid_constant__ CUtensorMap tmap_k,
-                     const __grid_constant__ CUtensorMap tmap_v) {
+__device__ __forceinline__ void decode_tc_body(const DecodeTcParams &tp, const CUtensorMap *tmap_k,
+                                               const CUtensorMap *tmap_v) {
   using namespace tc;
   using namespace dtc;
   constexpr bool kFp8 = std::is_same<KV, uint8_t>::value;
@@ -298,7 +319,8 @@ __global__ void __launch_bounds__(dtc::Roles::kThreads, 1)
   // in the same type; e4m3 with an fp8 cache, the queries and P as two e4m3 terms)
   constexpr bool kBf16 = std::is_same<QT, __nv_bfloat16>::value && !kFp8;
   constexpr bool kSplit = kBf16;            // bf16 cache: P as hi + lo
-  using GE = TcGeo<G, kSplit, kFp8>;
+  constexpr int kQTerms = QTerms<KV, QT>::value;
+  using GE = TcGeo<G, kSplit, kFp8, kQTerms>;
   constexpr int S = GE::kSlots, kNO = GE::kNO, kNS = GE::kNS;
   constexpr uint32_t kAB = kBf16 ? 1u : 0u;   // instruction-descriptor format: bf16 1, f16 0, e4m3 0
   const DecodeParams &p = tp.d;
@@ -329,7 +351,7 @@ __global__ void __launch_bounds__(dtc::Roles::kThreads, 1)
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
 
   // Q^T and P^T buffers start zeroed: their padding rows are never written
-  for (int i = tid; i < (GE::kOffRed - GE::kOffQ) / 16; i += kThreads)
+  for (int i = tid; i < (GE::kOffRed - GE::kOffQ) / 16; i += kThreads)   // (threads past kThreads repeat zeros)
     reinterpret_cast<uint4 *>(smem + GE::kOffQ)[i] = make_uint4(0, 0, 0, 0);
   if (tid == 0) {
     for (int s = 0; s < S; ++s) {
@@ -353,8 +375,8 @@ __global__ void __launch_bounds__(dtc::Roles::kThreads, 1)
     mbar_init(fin, 1);
     *abort_flag = 0;
     fence_mbar_init();
-    prefetch_tensor_map(&tmap_k);
-    prefetch_tensor_map(&tmap_v);
+    prefetch_tensor_map(tmap_k);
+    prefetch_tensor_map(tmap_v);
   }
   if (warp == kMmaWarp) {
     asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(tmem_slot)),
@@ -455,7 +477,10 @@ __global__ void __launch_bounds__(dtc::Roles::kThreads, 1)
             const bool kv = j * kKeys + tid < cur.ntok;
 #pragma unroll
             for (int h = 0; h < G; ++h) {
-              const float sv = kFp8 ? fmaf(raw[G + h], 0.0625f, raw[h]) : raw[h];   // fp8: hi + lo / 16
+              // fp8: hi + lo / 16, or hi + (mid + lo / 16) / 16
+              const float sv = kQTerms == 3   ? fmaf(fmaf(raw[2 * G + h], 0.0625f, raw[G + h]), 0.0625f, raw[h])
+                               : kQTerms == 2 ? fmaf(raw[G + h], 0.0625f, raw[h])
+                                              : raw[h];
               t[j][h] = kv ? sv * c : kNegInf;
               mloc[h] = fmaxf(mloc[h], t[j][h]);
             }
@@ -663,7 +688,7 @@ __global__ void __launch_bounds__(dtc::Roles::kThreads, 1)
           issue = bi >= 0;   // an out-of-range id was reported by the scheduler; its keys stay unread
         }
         const uint32_t boxes = __popc(__ballot_sync(0xffffffffu, issue));
-        const CUtensorMap *map = is_k ? &tmap_k : &tmap_v;
+        const CUtensorMap *map = is_k ? tmap_k : tmap_v;
         if constexpr (!kFp8) {
           const int atoms = bs >> 3;
           if (lane == 0) mbar_arrive_expect_tx(full_bar, boxes * atoms * kAtomBytes);
@@ -786,16 +811,22 @@ __global__ void __launch_bounds__(dtc::Roles::kThreads, 1)
             for (int i = 0; i < G / 2; ++i) {
               const int e = lane + 32 * i, h = e >> 4, c16 = e & 15, lr = G + h, half = (c16 & 1) * 8;
               const uint32_t ws[4] = {qw[i].x, qw[i].y, qw[i].z, qw[i].w};
-              uint32_t hi[4], lo[4];
+              uint32_t hi[4], lo[4], lo2[4];
 #pragma unroll
               for (int c = 0; c < 4; ++c) {
                 const float2 f = unpack2(ws[c], QT{});
-                split2_e4m3(make_float2(f.x * qs, f.y * qs), hi[c], lo[c]);
+                if constexpr (kQTerms == 3) split3_e4m3(make_float2(f.x * qs, f.y * qs), hi[c], lo[c], lo2[c]);
+                else split2_e4m3(make_float2(f.x * qs, f.y * qs), hi[c], lo[c]);
               }
               *reinterpret_cast<uint2 *>(qb + h * 128 + (((c16 >> 1) ^ (h & 7)) << 4) + half) =
                   make_uint2(hi[0] | (hi[1] << 16), hi[2] | (hi[3] << 16));
               *reinterpret_cast<uint2 *>(qb + lr * 128 + (((c16 >> 1) ^ (lr & 7)) << 4) + half) =
                   make_uint2(lo[0] | (lo[1] << 16), lo[2] | (lo[3] << 16));
+              if constexpr (kQTerms == 3) {
+                const int r3 = 2 * G + h;
+                *reinterpret_cast<uint2 *>(qb + r3 * 128 + (((c16 >> 1) ^ (r3 & 7)) << 4) + half) =
+                    make_uint2(lo2[0] | (lo2[1] << 16), lo2[2] | (lo2[3] << 16));
+              }
             }
             fence_async_smem();   // generic stores -> the MMAs' reads (after the descriptor's release)
           }
@@ -924,7 +955,7 @@ __global__ void __launch_bounds__(dtc::Roles::kThreads, 1)
         store_out<QT>(p.out, o0 + 3, p.out_f32 != 0, acc[h].w * inv);
       }
     }
-  } else {
+  } else if (warp == kMmaWarp) {
     // ===================================================== MMA issue
     // The whole warp runs the schedule (descriptors stay warp-uniform); one
     // elected lane issues the MMAs and their commits.
@@ -1074,6 +1105,13 @@ __global__ void __launch_bounds__(dtc::Roles::kThreads, 1)
   }
 }
 
+template <typename KV, typename QT, int G>
+__global__ void __launch_bounds__(dtc::Roles::kThreads, 1)
+    decode_tc_kernel(const DecodeTcParams tp, const __grid_constant__ CUtensorMap tmap_k,
+                     const __grid_constant__ CUtensorMap tmap_v) {
+  decode_tc_body<KV, QT, G>(tp, &tmap_k, &tmap_v);
+}
+
 // One CTA: count the split rows' merges and clear the merge list, and list
 // the (row, partition) items -- rows with the most partitions
 // first, then the single-partition rows by their number of 128-key tiles
@@ -1134,7 +1172,8 @@ __global__ void __launch_bounds__(1024) decode_tc_plan_kernel(DecodeParams p, De
 template <typename KV, typename QT, int G>
 cudaError_t launch_decode_tc_one(const DecodeTcParams &p, const PoolMaps &m, cudaStream_t s) {
   constexpr bool kSplit = std::is_same<QT, __nv_bfloat16>::value && !std::is_same<KV, uint8_t>::value;
-  constexpr int smem = dtc::TcGeo<G, kSplit, std::is_same<KV, uint8_t>::value>::kSmemBytes;
+  constexpr int smem =
+      dtc::TcGeo<G, kSplit, std::is_same<KV, uint8_t>::value, dtc::QTerms<KV, QT>::value>::kSmemBytes;
   decode_tc_plan_kernel<0><<<1, 1024, 0, s>>>(p.d, p.jobs);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;

@@ -1,6 +1,5 @@
 // pa_decode_tc_fp8.cu -- tensor-core decode instantiations for an fp8-e4m3
-// cache, with bf16 or f16 queries (the codes are widened to the query type in
-// shared memory).
+// cache, with bf16 or f16 queries (the codes enter kind::f8f6f4 MMAs as stored).
 #include "pa_decode_tc.cuh"
 
 namespace pa {

@@ -138,6 +138,18 @@ cudaError_t launch_decode_tc_f16(const DecodeTcParams &p, int gqa, const PoolMap
 cudaError_t launch_decode_tc_fp8_bf16q(const DecodeTcParams &p, int gqa, const PoolMaps &m, cudaStream_t s);
 cudaError_t launch_decode_tc_fp8_f16q(const DecodeTcParams &p, int gqa, const PoolMaps &m, cudaStream_t s);
 
+// One launch for a prefill chunk batch and a decode batch (pa_mixed_tc.cuh):
+// both on the tensor cores, head_dim 128, 4 or 8 query heads per KV head.
+constexpr bool mixed_tc_supported(int head_dim, int gqa) { return head_dim == 128 && (gqa == 4 || gqa == 8); }
+cudaError_t launch_mixed_tc_bf16(const DecodeTcParams &d, const PoolMaps &m, const PrefillTcParams &p, int num_chunks,
+                                 int gqa, cudaStream_t s);
+cudaError_t launch_mixed_tc_f16(const DecodeTcParams &d, const PoolMaps &m, const PrefillTcParams &p, int num_chunks,
+                                int gqa, cudaStream_t s);
+cudaError_t launch_mixed_tc_fp8_bf16q(const DecodeTcParams &d, const PoolMaps &m, const PrefillTcParams &p,
+                                      int num_chunks, int gqa, cudaStream_t s);
+cudaError_t launch_mixed_tc_fp8_f16q(const DecodeTcParams &d, const PoolMaps &m, const PrefillTcParams &p,
+                                     int num_chunks, int gqa, cudaStream_t s);
+
 // Tensor-core chunked prefill (head_dim 128; gqa = Hq / Hkv in {1, 2, 4, 8, 16}).
 constexpr bool prefill_tc_supported(int head_dim, int gqa) {
   return head_dim == 128 && (gqa == 1 || gqa == 2 || gqa == 4 || gqa == 8 || gqa == 16);

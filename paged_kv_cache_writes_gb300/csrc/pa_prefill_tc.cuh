@@ -124,8 +124,10 @@ struct Layout {
 
 }  // namespace tc
 
+// The prefill CTA (chunk x row block bx, KV head by), for prefill_tc_kernel and
+// for the prefill CTAs of the mixed kernel (pa_mixed_tc.cuh).
 template <typename KV, typename QT, int G, int kQTiles>
-__global__ void __launch_bounds__(tc::Roles<kQTiles>::kThreads, 1) prefill_tc_kernel(const PrefillTcParams p) {
+__device__ __forceinline__ void prefill_tc_body(const PrefillTcParams &p, int bx, int by) {
   using namespace tc;
   using L = Layout<kQTiles>;
   using R = Roles<kQTiles>;
@@ -157,8 +159,8 @@ __global__ void __launch_bounds__(tc::Roles<kQTiles>::kThreads, 1) prefill_tc_ke
   volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + L::kOffMisc + 8);
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int c = blockIdx.x / p.row_blocks, rb = blockIdx.x % p.row_blocks;
-  const int g = blockIdx.y;
+  const int c = bx / p.row_blocks, rb = bx % p.row_blocks;
+  const int g = by;
   const int cu0 = __ldg(p.cu_q_lens + c), nrows = __ldg(p.cu_q_lens + c + 1) - cu0;
   const int qs = __ldg(p.q_start + c);
   if (tid == 0 && g == 0 && rb == 0) {
@@ -596,6 +598,11 @@ __global__ void __launch_bounds__(tc::Roles<kQTiles>::kThreads, 1) prefill_tc_ke
     tc_fence_after();
     asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "n"(kTmemCols));
   }
+}
+
+template <typename KV, typename QT, int G, int kQTiles>
+__global__ void __launch_bounds__(tc::Roles<kQTiles>::kThreads, 1) prefill_tc_kernel(const PrefillTcParams p) {
+  prefill_tc_body<KV, QT, G, kQTiles>(p, blockIdx.x, blockIdx.y);
 }
 
 // Host launcher: grid (chunks x row blocks, KV heads), one CTA per SM.  Two Q

@@ -64,6 +64,16 @@ __device__ __forceinline__ void split2_e4m3(float2 x, uint32_t &hi, uint32_t &lo
   lo = __nv_cvt_float2_to_fp8x2(make_float2((x.x - h.x) * 16.f, (x.y - h.y) * 16.f), __NV_SATFINITE, __NV_E4M3);
 }
 
+// x -> three e4m3 codes with x = hi + mid / 16 + lo / 256 + err: the two-term
+// split of x, then of 16 (x - hi) - mid.  Holds |x| <= 256 to 2^-12 |x| + 2^-18,
+// so every f16 value's 11 significant bits survive.  Bytes (x0, x1) of each result.
+__device__ __forceinline__ void split3_e4m3(float2 x, uint32_t &hi, uint32_t &mid, uint32_t &lo) {
+  hi = __nv_cvt_float2_to_fp8x2(x, __NV_SATFINITE, __NV_E4M3);
+  const float2 h = unpack2_e4m3(hi);
+  const float2 r = make_float2((x.x - h.x) * 16.f, (x.y - h.y) * 16.f);
+  split2_e4m3(r, mid, lo);
+}
+
 // Arrive once on `bar` when every tcgen05 operation this thread issued so far is complete.
 __device__ __forceinline__ void umma_commit(uint64_t *bar) {
   asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(

@@ -10,8 +10,8 @@ from __future__ import annotations
 import numpy as np
 import torch
 
-from . import (kv_cache_desc, pa_copy_blocks, pa_decode, pa_decode_workspace_bytes, pa_decode_write, pa_prefill_chunk,
-               pa_reshape_and_cache)
+from . import (kv_cache_desc, pa_copy_blocks, pa_decode, pa_decode_workspace_bytes, pa_decode_write, pa_mixed_step,
+               pa_prefill_chunk, pa_reshape_and_cache)
 
 TORCH_DTYPES = {"f16": torch.float16, "bf16": torch.bfloat16, "fp8": torch.uint8}
 NAN_BITS = {"f16": 0x7E00, "bf16": 0x7FC0, "fp8": 0x7F}
@@ -108,10 +108,11 @@ class DeviceBatch:
                       int(b.seq_lens.max()), b.scale, self.out, self.workspace, b.partition_size)
         return self.out
 
-    def fused_step_tensors(self):
+    def fused_step_tensors(self, allow_others: bool = False):
         """Per-row new tokens for pa_decode_write: row i's step token is the one
         stored at the slot of its last position (slot -1 and zeros for a row
-        without one).  Raises if the step writes anything else."""
+        without one).  Raises if the step writes anything else, unless
+        allow_others (the other tokens are then in self._others)."""
         b = self.b
         if getattr(self, "_fused", None) is None:
             if b.step_write is None:
@@ -121,7 +122,7 @@ class DeviceBatch:
             k = np.zeros((b.num_seqs,) + sw.k.shape[1:], dtype=sw.k.dtype)
             v = np.zeros_like(k)
             slots = np.full(b.num_seqs, -1, dtype=np.int64)
-            used = 0
+            used = np.zeros(len(sw.slots), dtype=bool)
             for i, L in enumerate(b.seq_lens):
                 if L <= 0:
                     continue
@@ -130,9 +131,12 @@ class DeviceBatch:
                 if t is None:
                     continue
                 k[i], v[i], slots[i] = sw.k[t], sw.v[t], s_last
-                used += 1
-            if used != len(sw.slots):
-                raise ValueError("the step writes tokens other than the rows' last positions")
+                used[t] = True
+            self._others = None
+            if not used.all():
+                if not allow_others:
+                    raise ValueError("the step writes tokens other than the rows' last positions")
+                self._others = self._write_tensors(type(sw)(sw.k[~used], sw.v[~used], sw.slots[~used]))
             self._fused = (to_device(k, b.src_dtype, self.device), to_device(v, b.src_dtype, self.device),
                            torch.from_numpy(slots).to(self.device))
         return self._fused
@@ -152,6 +156,32 @@ class DeviceBatch:
         pa_prefill_chunk(p["q"], p["cu_q_lens"], p["q_start"], p["max_q_len"], self.k_cache, self.v_cache, self.desc,
                          p["block_tables"], p["seq_lens"], p["max_seq_len"], self.b.scale, p["out"])
         return p["out"]
+
+    def mixed_step(self, fused: bool = False) -> None:
+        """The prefill part and the decode part in one pa_mixed_step call.  fused: the
+        chunk's own tokens are written first and the decode rows' new tokens by the
+        call itself; else every new token is written first (write_step)."""
+        b, p = self.b, self.prefill
+        new = {}
+        if fused:
+            k, v, slots = self.fused_step_tensors(allow_others=True)
+            if self._others is not None:
+                pa_reshape_and_cache(*self._others, self.k_cache, self.v_cache, self.desc)
+            new = dict(k_new=k, v_new=v, slot_mapping=slots)
+        else:
+            self.write_step()
+        pa_mixed_step(self.q, self.block_tables, self.seq_lens, int(b.seq_lens.max()) if b.num_seqs else 0, self.out,
+                      p["q"], p["cu_q_lens"], p["q_start"], p["max_q_len"], p["block_tables"], p["seq_lens"],
+                      p["max_seq_len"], p["out"], self.k_cache, self.v_cache, self.desc, b.scale, self.workspace,
+                      b.partition_size, **new)
+
+    def mixed_attention(self) -> None:
+        """pa_mixed_step without new tokens: the attention of both parts only."""
+        b, p = self.b, self.prefill
+        pa_mixed_step(self.q, self.block_tables, self.seq_lens, int(b.seq_lens.max()) if b.num_seqs else 0, self.out,
+                      p["q"], p["cu_q_lens"], p["q_start"], p["max_q_len"], p["block_tables"], p["seq_lens"],
+                      p["max_seq_len"], p["out"], self.k_cache, self.v_cache, self.desc, b.scale, self.workspace,
+                      b.partition_size)
 
     def step_all(self) -> None:
         """One pass of the hot path: write the new tokens, then attend."""

@@ -162,3 +162,39 @@ def test_per_head_scale_validation(lib):
         assert f(FAKE, FAKE, 1, 4, 1024, FAKE, FAKE, FAKE, ctypes.byref(d), None) == 1
     ok = _desc(kv_dtype=pa.PA_FP8_E4M3, k_head_scales=FAKE, v_head_scales=FAKE)
     assert f(FAKE, FAKE, 1, 0, 1024, FAKE, FAKE, FAKE, ctypes.byref(ok), None) == 0      # valid, no tokens
+
+
+def test_mixed_step_validation(lib):
+    """pa_mixed_step checks both parts before it launches anything."""
+    import paged_kv_cache_writes_gb300 as pa
+    d = _desc()
+
+    def parts(**kw):
+        dp = dict(q=FAKE, num_seqs=4, block_tables=FAKE, max_blocks_per_seq=8, seq_lens=FAKE, max_seq_len=100,
+                  partition_size=0, k_new=None, v_new=None, token_stride=0, slot_mapping=None, workspace=None,
+                  workspace_bytes=0, out=FAKE)
+        pp = dict(q_chunk=FAKE, cu_q_lens=FAKE, q_start=FAKE, num_chunks=1, max_q_len=64, block_tables=FAKE,
+                  max_blocks_per_seq=8, seq_lens=FAKE, max_seq_len=128, out=FAKE)
+        for k, v in kw.items():
+            (dp if k.startswith("d_") else pp)[k[2:]] = v
+        return pa.PaDecodePart(**dp), pa.PaPrefillPart(**pp)
+
+    def call(q_dtype=1, hq=32, odt=1, **kw):
+        dp, pp = parts(**kw)
+        return lib.pa_mixed_step(ctypes.byref(dp), ctypes.byref(pp), q_dtype, hq, FAKE, FAKE, ctypes.byref(d), 0.1,
+                                 odt, None)
+
+    dp, pp = parts()
+    assert lib.pa_mixed_step(None, ctypes.byref(pp), 1, 32, FAKE, FAKE, ctypes.byref(d), 0.1, 1, None) == 1
+    assert lib.pa_mixed_step(ctypes.byref(dp), None, 1, 32, FAKE, FAKE, ctypes.byref(d), 0.1, 1, None) == 1
+    assert lib.pa_mixed_step(ctypes.byref(dp), ctypes.byref(pp), 1, 32, FAKE, FAKE, None, 0.1, 1, None) == 1
+    assert call(d_num_seqs=0, p_num_chunks=0) == 0           # nothing to do
+    assert call(p_num_chunks=-1) == 1                        # prefill part invalid
+    assert call(p_cu_q_lens=None) == 1
+    assert call(hq=31) == 1                                  # Hq % Hkv
+    assert call(q_dtype=0) == 2                              # f16 q, bf16 cache
+    assert call(odt=2) == 2                                  # fp8 output
+    assert call(d_num_seqs=-1) == 1                          # decode part invalid
+    assert call(d_k_new=FAKE) == 1                           # new tokens: all three or none
+    assert call(d_k_new=FAKE, d_v_new=FAKE, d_slot_mapping=FAKE, d_token_stride=7) == 1
+    assert call(d_workspace=None) == 1                       # decode workspace missing
