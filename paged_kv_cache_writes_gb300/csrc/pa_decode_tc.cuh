@@ -42,10 +42,11 @@
 // 256 p is written as hi + lo / 16 (hi in rows 0..G-1 of P^T, lo in rows
 // G..2G-1), which holds it to 2^-8 of itself; the query rows, scaled by a
 // power of two 2^e per unit (|q| 2^e in [128, 256) at the unit's largest
-// element), likewise as hi + lo / 16 for bf16 queries (exact: 8 significant
-// bits) and as hi + mid / 16 + lo / 256 in rows 0..3G-1 for f16 queries (11
-// bits, held to 2^-12).  The softmax and the epilogue add the column groups
-// of S^T and O^T and undo the scales.
+// element), likewise as hi + lo / 16 for bf16 queries and as hi + mid / 16 +
+// lo / 256 in rows 0..3G-1 for f16 queries: either holds every query element
+// within 2^-13 of the unit's largest exactly (8 or 11 significant bits).  The
+// softmax and the epilogue add the column groups of S^T and O^T and undo the
+// scales.
 //
 // Softmax per unit (no online rescale): all tiles of a unit (<= 4 x 128
 // keys) are scored first, the exact maximum per head over the unit comes from

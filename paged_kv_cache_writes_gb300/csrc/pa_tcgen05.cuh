@@ -65,8 +65,10 @@ __device__ __forceinline__ void split2_e4m3(float2 x, uint32_t &hi, uint32_t &lo
 }
 
 // x -> three e4m3 codes with x = hi + mid / 16 + lo / 256 + err: the two-term
-// split of x, then of 16 (x - hi) - mid.  Holds |x| <= 256 to 2^-12 |x| + 2^-18,
-// so every f16 value's 11 significant bits survive.  Bytes (x0, x1) of each result.
+// split of 16 (x - hi) after hi.  Every f16 value with 2^-7 <= |x| <= 256 is
+// held exactly (its 11 significant bits fit in three terms), any smaller one
+// to 2^-18.  (Two terms hold every bf16 value with |x| >= 2^-6 exactly.)
+// Bytes (x0, x1) of each result.
 __device__ __forceinline__ void split3_e4m3(float2 x, uint32_t &hi, uint32_t &mid, uint32_t &lo) {
   hi = __nv_cvt_float2_to_fp8x2(x, __NV_SATFINITE, __NV_E4M3);
   const float2 h = unpack2_e4m3(hi);
