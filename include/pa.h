@@ -200,8 +200,8 @@ PA_API pa_status pa_decode(const void *q, pa_dtype q_dtype, int32_t num_seqs,
  * pa_decode does, the new token included ([V07] "Architectural Blueprint 3:
  * Chunked Prefill", decode phase: each step appends one token per sequence and
  * reads the whole cache).  With the tensor-core decode the token is stored by
- * the decode launch itself, just before the copy of the tile that holds it;
- * otherwise the cache write is launched first, on the same stream.
+ * the decode launch itself, before the work unit that reads it starts copying
+ * its tiles; otherwise the cache write is launched first, on the same stream.
  *
  *   k_new, v_new   device [num_seqs][num_kv_heads][head_dim] in q_dtype, token
  *                  (row) stride token_stride elements (>= Hkv * head_dim, a
