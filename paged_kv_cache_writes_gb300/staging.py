@@ -162,6 +162,8 @@ class DeviceBatch:
         chunk's own tokens are written first and the decode rows' new tokens by the
         call itself; else every new token is written first (write_step)."""
         b, p = self.b, self.prefill
+        if p is None:
+            raise ValueError("the batch has no prefill part")
         new = {}
         if fused:
             k, v, slots = self.fused_step_tensors(allow_others=True)
@@ -178,6 +180,8 @@ class DeviceBatch:
     def mixed_attention(self) -> None:
         """pa_mixed_step without new tokens: the attention of both parts only."""
         b, p = self.b, self.prefill
+        if p is None:
+            raise ValueError("the batch has no prefill part")
         pa_mixed_step(self.q, self.block_tables, self.seq_lens, int(b.seq_lens.max()) if b.num_seqs else 0, self.out,
                       p["q"], p["cu_q_lens"], p["q_start"], p["max_q_len"], p["block_tables"], p["seq_lens"],
                       p["max_seq_len"], p["out"], self.k_cache, self.v_cache, self.desc, b.scale, self.workspace,
