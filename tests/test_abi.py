@@ -28,7 +28,8 @@ def declared_functions():
 def test_header_declares_the_boundary():
     names = declared_functions()
     for want in ("pa_reshape_and_cache", "pa_decode", "pa_prefill_chunk", "pa_copy_blocks",
-                 "pa_decode_workspace_bytes", "pa_get_device_error", "pa_status_string"):
+                 "pa_decode_workspace_bytes", "pa_get_device_error", "pa_status_string", "pa_decode_write",
+                 "pa_mixed_step"):
         assert want in names
 
 
