@@ -2,17 +2,22 @@
 
 One step = one pass of the whole path over the Llama-3-70B-shaped decode
 batch (256 sequences, 64 query / 8 KV heads, head_dim 128, 32-token blocks,
-bf16, log-normal context lengths, split-KV partitions of 512 tokens):
-write the 256 new tokens' K/V into their slots (pa_reshape_and_cache), then
-paged decode over every sequence (pa_decode).  The metric is decode KV
-bandwidth: algorithmic K+V bytes read per step / step time, plus decode
-tokens/s per layer.
+bf16, log-normal context lengths, split-KV partitions of 512 tokens): one
+pa_decode_write call, which stores the 256 new tokens' K/V in their slots and
+runs paged decode over every sequence (plan + decode launches).  The metric
+is decode KV bandwidth: algorithmic K+V bytes read per step / step time, plus
+decode tokens/s per layer.  Under torchrun every rank runs its own replica
+(weak scaling); the step time is the slowest rank's.
 
 Prints one JSON line.  ``--impl reference`` times the fp64 CPU oracle instead
 (bounded samples of the same workload on the host cores).
 
 ``other_decodes`` is pa_decode alone on the 8B-shaped, shared-prefix and
-mixed fp8 decode workloads (K+V bytes / time).  The line also carries
+mixed fp8 decode workloads and on fp8 caches (K+V bytes / time);
+``decode_cuda_cores`` the step through the CUDA-core decode kernel;
+``mixed_step`` the chunked-prefill mixed batch as two calls and as one
+pa_mixed_step launch; ``block_manager`` the host block manager's numbers;
+``e2e`` the step with host buffers.  The line also carries
 ``prefill``: the tensor-core chunked-prefill kernel
 timed on its own (CUDA events, inputs resident), as useful causal TFLOP/s
 (4 * head_dim * Hq * sum over query rows of the keys each row attends to)
@@ -347,6 +352,23 @@ def _dist():
     return ws, rank, local
 
 
+def _max_over_ranks(x: float, device) -> float:
+    """The largest x over the ranks of the process group (x itself without one)."""
+    import torch
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return x
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def _job_rate(units_per_rank: float, ms: float, world_size: int) -> float:
+    """Whole-job rate of a weak-scaling run: every rank processes units_per_rank
+    units (its own replica of the workload) and ms is the slowest rank's time."""
+    return units_per_rank * world_size / (ms * 1e-3)
+
+
 def _time_oracle(b, kp, vp, ids) -> float:
     import oracle
     t0 = time.perf_counter()
@@ -483,10 +505,7 @@ def run_ours(args):
     def pct(q):
         return dec_all[min(len(dec_all) - 1, int(q * (len(dec_all) - 1) + 0.5))]
     assert pa.pa_get_device_error() == 0
-    if ws > 1:
-        t = torch.tensor([ms], device=dev_name)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        ms = float(t.item())
+    ms = _max_over_ranks(ms, dev_name)
 
     # end to end through the public API with host buffers (pinned), copies inside the timed region:
     # every step copies its inputs (q, the new tokens' K/V and slots, tables, lengths) from pinned host
@@ -540,10 +559,7 @@ def run_ours(args):
     torch.cuda.synchronize()
     e2e_ms = e0.elapsed_time(e1) / args.steps
     assert torch.equal(out_h[(args.steps - 1) % 2].view(torch.int32), bufs[(args.steps - 1) % 2]["out"].cpu().view(torch.int32))
-    if ws > 1:
-        t = torch.tensor([e2e_ms], device=dev_name)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        e2e_ms = float(t.item())
+    e2e_ms = _max_over_ranks(e2e_ms, dev_name)
 
     if rank != 0:
         if ws > 1:
@@ -551,13 +567,13 @@ def run_ours(args):
         return
     peak, peak_kind = _peaks()
     achieved = dec_bytes / (dec_ms * 1e-3) / 1e9
-    value = kv_bytes * ws / (ms * 1e-3) / 1e9
+    value = _job_rate(kv_bytes, ms, ws) / 1e9
     line = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": ws, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": ms, "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
         "data": "synthetic (seeded N(0,1) K/V/q rounded to bf16, seeded shuffled block tables)",
         "config": _config(b, {"parallelism": f"replicas x{ws}" if ws > 1 else "single GPU"}),
-        "tokens_per_s_per_layer": b.num_seqs * ws / (ms * 1e-3),
+        "tokens_per_s_per_layer": _job_rate(b.num_seqs, ms, ws),
         "decode_ms": dec_ms,
         "decode_ms_p10_p50_p90": [pct(0.1), pct(0.5), pct(0.9)],
         "step": "one pa_decode_write call: the new tokens' cache write fused into the decode launch",
@@ -565,7 +581,7 @@ def run_ours(args):
                      "traffic": _profiled_traffic(kv_bytes),
                      "kernel": "decode_tc_kernel (pa_decode_write: plan + decode launches, timed together)",
                      "peak_source": f"{peak_kind} hbm_gbs"},
-        "e2e": {"value": kv_bytes * ws / (e2e_ms * 1e-3) / 1e9, "unit": UNIT, "h2d_bytes_per_step": h2d,
+        "e2e": {"value": _job_rate(kv_bytes, e2e_ms, ws) / 1e9, "unit": UNIT, "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms,
                 "note": "pa_decode_write per step; inputs copied from pinned host memory and the output read "
                         "back every step, on copy streams overlapping the neighbouring steps' compute"},
