@@ -88,7 +88,7 @@ def test_copy_blocks_bad_id_sets_error():
 def test_config_pools_bit_exact(name):
     """Every write and copy of each named workload (setup and step) lands
     bit-exactly where the oracle puts it."""
-    b = W.CONFIGS[name]()
+    b = W.NAMED_WORKLOADS[name]()
     dev = run_gpu(b, step=False)
     dev.write_step()
     torch.cuda.synchronize()

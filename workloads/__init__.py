@@ -25,7 +25,7 @@ a spare physical block that is never written (all NaN).
 
 The five named workloads follow the configurations these tests and the
 benchmark are quoted on (Llama-3-8B / 70B shaped GQA layers, shared-prefix
-sampling, chunked prefill with an fp8 KV cache); see ``CONFIGS``.
+sampling, chunked prefill with an fp8 KV cache); see ``NAMED_WORKLOADS``.
 """
 from __future__ import annotations
 
@@ -467,7 +467,7 @@ def cfg_mixed_fp8(seed: int = 4, num_decode: int = 128) -> PagedBatch:
     return mixed_prefill_batch(num_decode=num_decode, seed=seed)
 
 
-CONFIGS = {
+NAMED_WORKLOADS = {
     "tiny": cfg_tiny,
     "llama8b": cfg_llama8b,
     "llama70b": cfg_llama70b,
