@@ -339,7 +339,11 @@ int or_decode(const void *q, int q_dtype, int num_seqs, int num_q_heads,
 /* Chunked prefill: chunk c owns query rows cu_q_lens[c] .. cu_q_lens[c+1]-1;
  * row r of the chunk sits at absolute position q_start[c] + r and attends to
  * positions 0 .. q_start[c] + r (inclusive) of sequence c through
- * block_tables[c]. */
+ * block_tables[c].  The work is shared among threads by (chunk, KV head,
+ * block of OR_PREFILL_ROWS rows); each job gathers the keys its last row
+ * sees and evaluates its rows exactly as above, so the split changes no
+ * result. */
+#define OR_PREFILL_ROWS 64
 int or_prefill(const void *q, int q_dtype, const int32_t *cu_q_lens,
                const int32_t *q_start, int num_chunks, int num_q_heads,
                const void *k_cache, const void *v_cache, int64_t num_blocks,
@@ -347,23 +351,34 @@ int or_prefill(const void *q, int q_dtype, const int32_t *cu_q_lens,
                const float *k_scales, const float *v_scales, const int32_t *block_tables,
                int max_blocks_per_seq, float scale, double *out)
 {
-    int G, err = OR_OK;
-    int64_t job;
+    int G, c, err = OR_OK;
+    int64_t job, nrb = 1;
     if (num_q_heads % num_kv_heads)
         return OR_ERR_ARG;
     G = num_q_heads / num_kv_heads;
+    for (c = 0; c < num_chunks; ++c) {
+        int64_t len = cu_q_lens[c + 1] - cu_q_lens[c];
+        int64_t rb = (len + OR_PREFILL_ROWS - 1) / OR_PREFILL_ROWS;
+        if (rb > nrb)
+            nrb = rb;
+    }
 #pragma omp parallel for schedule(dynamic, 1)
-    for (job = 0; job < (int64_t)num_chunks * num_kv_heads; ++job) {
-        int c = (int)(job / num_kv_heads), g = (int)(job % num_kv_heads), j, e;
+    for (job = 0; job < (int64_t)num_chunks * num_kv_heads * nrb; ++job) {
+        int c = (int)(job / ((int64_t)num_kv_heads * nrb));
+        int g = (int)((job / nrb) % num_kv_heads), j, e;
         int64_t r, len = cu_q_lens[c + 1] - cu_q_lens[c];
-        int64_t ctx = (int64_t)q_start[c] + len;
+        int64_t r0 = (job % nrb) * OR_PREFILL_ROWS;
+        int64_t r1 = r0 + OR_PREFILL_ROWS < len ? r0 + OR_PREFILL_ROWS : len;
+        int64_t ctx = (int64_t)q_start[c] + r1;
         double *K, *V, *s, *qrow;
         if (len < 0 || q_start[c] < 0 ||
-            ctx > (int64_t)max_blocks_per_seq * block_size) {
+            (int64_t)q_start[c] + len > (int64_t)max_blocks_per_seq * block_size) {
 #pragma omp atomic write
             err = OR_ERR_RANGE;
             continue;
         }
+        if (r0 >= len)
+            continue;
         K = (double *)malloc(sizeof(double) * (size_t)(ctx * head_dim + 1));
         V = (double *)malloc(sizeof(double) * (size_t)(ctx * head_dim + 1));
         s = (double *)malloc(sizeof(double) * (size_t)(ctx + 1));
@@ -382,7 +397,7 @@ int or_prefill(const void *q, int q_dtype, const int32_t *cu_q_lens,
 #pragma omp atomic write
             err = OR_ERR_RANGE;
         } else {
-            for (r = 0; r < len; ++r)
+            for (r = r0; r < r1; ++r)
                 for (j = 0; j < G; ++j) {
                     int h = g * G + j;
                     int64_t row = ((int64_t)cu_q_lens[c] + r) * num_q_heads + h;
