@@ -1,13 +1,12 @@
 """GPU parity of chunked-prefill attention against the fp64 oracle.
 
 Row r of a chunk at absolute position q_start + r attends causally to
-positions 0 .. q_start + r of its sequence.  Small batches are compared on
-every row; the 512-row chunks (mixed fp8 workload, long bf16/f16 chunks) are
-compared on sampled rows, each of which the oracle computes as a decode with
-seq_len = q_start + r + 1 (the pinned identity "last row of a chunk = decode").
+positions 0 .. q_start + r of its sequence.  Every batch is compared on every
+row, head and element, including the chunk of the chunked-prefill mixed batch
+and each prefill batch the benchmark times.
 
 head_dim 128 with a GQA group of 1, 2, 4, 8 or 16 runs on the tensor-core
-kernel (128 GQA-packed rows per CTA, 64-key tiles); head_dim 64 and other
+kernel (128 GQA-packed rows per Q tile, 128-key tiles); head_dim 64 and other
 groups run on the CUDA-core row kernel.  Both are covered here."""
 import numpy as np
 import pytest
@@ -39,22 +38,23 @@ def test_prefill_query_dtype_output():
     assert rounded_excess(dev.prefill["out"], ref, "bf16", TOL["bf16"]) <= 0
 
 
-def test_mixed_fp8_prefill_sampled_rows():
+def test_mixed_fp8_prefill_full():
+    # the chunk of the chunked-prefill mixed batch (512 rows at 4096, fp8 KV), every row, and its decode part
     b = W.cfg_mixed_fp8()
     dev = run_gpu(b)
     kp, vp = oracle_pools(b)
-    p = b.prefill
-    rows = np.unique(np.concatenate([np.arange(0, 512, 37), [0, 1, 255, 510, 511]]))
-    qs = int(p.q_start[0])
-    ref = oracle.decode(p.q[rows], oracle.BF16, kp, vp, oracle.FP8_E4M3,
-                        np.repeat(p.block_tables, len(rows), axis=0), (qs + rows + 1).astype(np.int32),
-                        b.scale, b.k_scale, b.v_scale)
-    got = dev.prefill["out"][torch.as_tensor(rows, device="cuda")]
-    assert max_err(got, ref) <= TOL["fp8"]
-    # decode part of the same step
-    sample = np.arange(0, b.num_seqs, 16)
-    dref = oracle.decode_batch(b, kp, vp, seq_ids=sample)[sample]
-    assert max_err(dev.out[torch.as_tensor(sample, device="cuda")], dref) <= TOL["fp8"]
+    assert max_err(dev.prefill["out"], oracle.prefill_batch(b, kp, vp)) <= TOL["fp8"]
+    assert max_err(dev.out, oracle.decode_batch(b, kp, vp)) <= TOL["fp8"]
+
+
+@pytest.mark.parametrize("key", sorted(W.PREFILL_WORKLOADS))
+def test_benchmarked_prefill_batches_full(key):
+    # each prefill batch the benchmark times, at its full size, every row
+    b = W.PREFILL_WORKLOADS[key][1]()
+    dev = run_gpu(b)
+    kp, vp = oracle_pools(b)
+    err = max_err(dev.prefill["out"], oracle.prefill_batch(b, kp, vp))
+    assert err <= TOL[b.kv_dtype], err
 
 
 def test_prefill_seq_len_mismatch_sets_error():
@@ -103,20 +103,12 @@ def test_prefill_tensor_core_query_dtype_output(src, kv):
 
 
 @pytest.mark.parametrize("src,hq", [("bf16", 64), ("f16", 32)])
-def test_prefill_long_chunk_sampled_rows(src, hq):
-    # a 512-row chunk over 4096 tokens of context, Llama-shaped GQA (8 KV heads)
+def test_prefill_long_chunk_full(src, hq):
+    # a 512-row chunk over 4096 tokens of context, Llama-shaped GQA (8 KV heads), every row
     b = W.prefill_batch("p", [(4096, 512)], hq, 8, 128, 16, src, seed=23)
     dev = run_gpu(b)
     kp, vp = oracle_pools(b)
-    p = b.prefill
-    rows = np.unique(np.concatenate([np.arange(0, 512, 29), [0, 1, 127, 128, 511]]))
-    qs = int(p.q_start[0])
-    ref = oracle.decode(p.q[rows], {"bf16": oracle.BF16, "f16": oracle.F16}[src], kp, vp,
-                        {"bf16": oracle.BF16, "f16": oracle.F16}[src],
-                        np.repeat(p.block_tables, len(rows), axis=0), (qs + rows + 1).astype(np.int32),
-                        b.scale, 1.0, 1.0)
-    got = dev.prefill["out"][torch.as_tensor(rows, device="cuda")]
-    assert max_err(got, ref) <= TOL[src]
+    assert max_err(dev.prefill["out"], oracle.prefill_batch(b, kp, vp)) <= TOL[src]
 
 
 @pytest.mark.parametrize("kv", ["bf16", "fp8"])

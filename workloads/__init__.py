@@ -441,22 +441,32 @@ def cfg_tiny(seed: int = 0) -> PagedBatch:
                         num_blocks=64, scale=float(np.float32(0.125)))
 
 
-def cfg_llama8b(seed: int = 1, batch: int = 64, kv_dtype: str = "bf16") -> PagedBatch:
+def _fp8_name(kv_dtype: str, fp8_scales: str) -> str:
+    if kv_dtype != "fp8":
+        return ""
+    return ", fp8 KV with per-head scales" if fp8_scales == "head" else ", fp8 KV"
+
+
+def cfg_llama8b(seed: int = 1, batch: int = 64, kv_dtype: str = "bf16", fp8_scales: str = "tensor") -> PagedBatch:
     """Llama-3-8B-shaped decode layer: 32/8 heads, head_dim 128, block 16,
     bf16, lengths uniform 512..4096, 20k-block pool.  kv_dtype "fp8" stores
-    the same values as e4m3 codes with per-tensor scales."""
+    the same values as e4m3 codes with per-tensor scales (fp8_scales "head":
+    one scale per KV head)."""
     lens = np.random.default_rng(seed + 100).integers(512, 4097, size=batch)
-    name = "Llama-3-8B-shaped decode layer" + (", fp8 KV" if kv_dtype == "fp8" else "")
-    return decode_batch(name, lens, 32, 8, 128, 16, "bf16", kv_dtype=kv_dtype, seed=seed, num_blocks=20000)
+    name = "Llama-3-8B-shaped decode layer" + _fp8_name(kv_dtype, fp8_scales)
+    return decode_batch(name, lens, 32, 8, 128, 16, "bf16", kv_dtype=kv_dtype, seed=seed, num_blocks=20000,
+                        fp8_scales=fp8_scales)
 
 
-def cfg_llama70b(seed: int = 2, batch: int = 256, kv_dtype: str = "bf16") -> PagedBatch:
+def cfg_llama70b(seed: int = 2, batch: int = 256, kv_dtype: str = "bf16", fp8_scales: str = "tensor") -> PagedBatch:
     """Llama-3-70B-shaped decode layer: 64/8 heads, head_dim 128, block 32,
     bf16, log-normal lengths (median 1000, cap 8192), split-KV 512.  kv_dtype
-    "fp8" stores the same values as e4m3 codes with per-tensor scales."""
+    "fp8" stores the same values as e4m3 codes with per-tensor scales
+    (fp8_scales "head": one scale per KV head)."""
     lens = lognormal_lens(np.random.default_rng(seed + 100), batch)
-    name = "Llama-3-70B-shaped decode layer" + (", fp8 KV" if kv_dtype == "fp8" else "")
-    return decode_batch(name, lens, 64, 8, 128, 32, "bf16", kv_dtype=kv_dtype, seed=seed, partition_size=512)
+    name = "Llama-3-70B-shaped decode layer" + _fp8_name(kv_dtype, fp8_scales)
+    return decode_batch(name, lens, 64, 8, 128, 32, "bf16", kv_dtype=kv_dtype, seed=seed, partition_size=512,
+                        fp8_scales=fp8_scales)
 
 
 def cfg_shared_prefix(seed: int = 3, num_prompts: int = 32) -> PagedBatch:
@@ -465,6 +475,22 @@ def cfg_shared_prefix(seed: int = 3, num_prompts: int = 32) -> PagedBatch:
 
 def cfg_mixed_fp8(seed: int = 4, num_decode: int = 128) -> PagedBatch:
     return mixed_prefill_batch(num_decode=num_decode, seed=seed)
+
+
+# Prefill-only batches the benchmark times (and the tests compare in full):
+# (description, builder).  Chunk sizes follow the pages' 512-token chunks and
+# the 256 / 2048-token variants; one batch fills every SM with two-tile CTAs.
+PREFILL_WORKLOADS = {
+    "bf16_8x2048": ("8 chunks x 2048 tokens at position 2048, GQA 32/8, head_dim 128, block 16, bf16 KV",
+                    lambda: prefill_batch("prefill 8x2048", [(2048, 2048)] * 8, 32, 8, 128, 16, "bf16", seed=3)),
+    "bf16_chunk2048": ("one 2048-token chunk at position 4096, GQA 32/8, head_dim 128, block 16, bf16 KV",
+                       lambda: prefill_batch("prefill chunk 2048", [(4096, 2048)], 32, 8, 128, 16, "bf16", seed=5)),
+    "bf16_mha_4x1024": ("4 chunks x 1024 tokens at position 1024, MHA 32/32, head_dim 128, block 16, bf16 KV",
+                        lambda: prefill_batch("prefill MHA 4x1024", [(1024, 1024)] * 4, 32, 32, 128, 16, "bf16",
+                                              seed=6)),
+    "bf16_16x256": ("16 chunks x 256 tokens at position 1024, GQA 32/8, head_dim 128, block 16, bf16 KV",
+                    lambda: prefill_batch("prefill 16x256", [(1024, 256)] * 16, 32, 8, 128, 16, "bf16", seed=7)),
+}
 
 
 NAMED_WORKLOADS = {
