@@ -4,6 +4,8 @@
 // decode workspace (work list, split-KV partials, arrival counters) lives in a
 // fixed static device array instead of caller memory; everything else is the
 // ordinary pa_decode path, called unchanged with that array as its workspace.
+#include <cuda.h>
+
 #include <mutex>
 
 #include "pa_common.cuh"
@@ -15,23 +17,65 @@ namespace {
 static __device__ __align__(256) unsigned char g_noalloc_scratch[PA_NOALLOC_SCRATCH_BYTES];
 
 constexpr int kMaxDevices = 64;
+
+// The array's device address per device, with the id of the context it was
+// looked up in: a device reset creates a new context (new id), in which the
+// array may sit elsewhere, so the address is looked up again.
+struct DeviceScratch {
+  unsigned long long ctx_id;
+  void *ptr;
+};
 std::mutex g_scratch_mu;
-void *g_scratch_ptr[kMaxDevices] = {};
+DeviceScratch g_scratch[kMaxDevices] = {};
+
+typedef CUresult (*CtxGetCurrentFn)(CUcontext *);
+typedef CUresult (*CtxGetIdFn)(CUcontext, unsigned long long *);
+
+// Id of the context current on this thread (0: none yet).
+pa_status current_context_id(unsigned long long *id) {
+  static CtxGetCurrentFn get_current = nullptr;
+  static CtxGetIdFn get_id = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void *p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &p, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      get_current = reinterpret_cast<CtxGetCurrentFn>(p);
+    p = nullptr;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetId", &p, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      get_id = reinterpret_cast<CtxGetIdFn>(p);
+  });
+  if (!get_current || !get_id) return PA_ERR_CUDA;
+  CUcontext ctx = nullptr;
+  if (get_current(&ctx) != CUDA_SUCCESS) return PA_ERR_CUDA;
+  *id = 0;
+  if (ctx != nullptr && get_id(ctx, id) != CUDA_SUCCESS) return PA_ERR_CUDA;
+  return PA_OK;
+}
 
 // Device address of the scratch array on the current device.  The array's
-// name is only a host-side handle; the runtime resolves it per device.
+// name is only a host-side handle; the runtime resolves it per device (and
+// per context: the look-up is repeated after a device reset).
 pa_status scratch_on_current_device(void **out) {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return PA_ERR_CUDA;
   if (dev < 0 || dev >= kMaxDevices) return PA_ERR_UNSUPPORTED;
+  unsigned long long id = 0;
+  pa_status st = current_context_id(&id);
+  if (st != PA_OK) return st;
   std::lock_guard<std::mutex> lock(g_scratch_mu);
-  if (g_scratch_ptr[dev] == nullptr) {
+  DeviceScratch &s = g_scratch[dev];
+  if (id == 0 || s.ptr == nullptr || s.ctx_id != id) {
     void *ptr = nullptr;
-    if (cudaGetSymbolAddress(&ptr, g_noalloc_scratch) != cudaSuccess || ptr == nullptr)
-      return PA_ERR_CUDA;
-    g_scratch_ptr[dev] = ptr;
+    // also binds the device's primary context to this thread if none was
+    if (cudaGetSymbolAddress(&ptr, g_noalloc_scratch) != cudaSuccess || ptr == nullptr) return PA_ERR_CUDA;
+    if ((st = current_context_id(&id)) != PA_OK) return st;
+    s.ptr = ptr;
+    s.ctx_id = id;
   }
-  *out = g_scratch_ptr[dev];
+  *out = s.ptr;
   return PA_OK;
 }
 

@@ -5,20 +5,19 @@ device memory belongs to another framework) get a decode that uses a fixed
 scratch array inside the library instead of a caller-provided workspace.
 These tests call it through the C ABI and compare it with pa_decode on the
 same inputs, twice in a row (the scratch keeps the previous call's contents,
-which must not leak into the next result).  The file is named so that pytest
-collects it last.
+which must not leak into the next result).  Both decode kernels run the same
+units in the same order whatever memory holds their workspace, so the
+results must equal pa_decode's bit for bit.  The file is named so that
+pytest collects it last.
 """
 import ctypes
 
-import numpy as np
 import pytest
 import torch
 
 import workloads as W
 
 pytestmark = pytest.mark.gpu
-
-TOL = 2e-3  # fp32 outputs of a bf16 cache, as in the other decode parity tests
 
 
 def _noalloc_fn():
@@ -36,33 +35,57 @@ def _noalloc_fn():
 def _call(f, dev, out, max_seq_len=None):
     import paged_kv_cache_writes_gb300 as pa
     b = dev.b
-    return f(dev.q.data_ptr(), pa.PA_BF16, b.num_seqs, b.num_q_heads, dev.k_cache.data_ptr(),
+    q_code = {"bf16": pa.PA_BF16, "f16": pa.PA_F16}[b.src_dtype]
+    return f(dev.q.data_ptr(), q_code, b.num_seqs, b.num_q_heads, dev.k_cache.data_ptr(),
              dev.v_cache.data_ptr(), ctypes.byref(dev.desc), dev.block_tables.data_ptr(),
              dev.block_tables.shape[1], dev.seq_lens.data_ptr(),
              int(b.seq_lens.max()) if max_seq_len is None else max_seq_len, b.scale, b.partition_size,
              out.data_ptr(), pa.PA_F32, torch.cuda.current_stream().cuda_stream)
 
 
-def test_noalloc_matches_pa_decode_on_two_calls():
+@pytest.mark.parametrize("kernel", ["auto", "cuda_cores"])
+@pytest.mark.parametrize("kv", ["bf16", "fp8"])
+def test_noalloc_equals_pa_decode_on_two_calls(kernel, kv):
     import paged_kv_cache_writes_gb300 as pa
     from paged_kv_cache_writes_gb300.staging import DeviceBatch
     f = _noalloc_fn()
     # split-KV rows (several partitions), a short row, an empty row
-    b = W.decode_batch("noalloc", [3000, 700, 17, 0, 2049, 1], 32, 8, 128, 16, "bf16", seed=41,
+    b = W.decode_batch("noalloc", [3000, 700, 17, 0, 2049, 1], 32, 8, 128, 16, "bf16", kv_dtype=kv, seed=41,
                        partition_size=256)
     dev = DeviceBatch(b, "cuda")
     dev.run_setup()
     dev.write_step()
-    ref = dev.decode().clone()          # the existing entry point, caller-owned workspace
-    torch.cuda.synchronize()
-    assert pa.pa_get_device_error() == 0
-    for _ in range(2):
-        out = torch.full_like(ref, float("nan"))
-        assert _call(f, dev, out) == 0
+    with pa.decode_kernel(kernel):
+        ref = dev.decode().clone()          # the existing entry point, caller-owned workspace
         torch.cuda.synchronize()
         assert pa.pa_get_device_error() == 0
-        assert torch.isfinite(out).all()
-        assert float((out - ref).abs().max()) <= TOL
+        for _ in range(2):
+            out = torch.full_like(ref, float("nan"))
+            assert _call(f, dev, out) == 0
+            torch.cuda.synchronize()
+            assert pa.pa_get_device_error() == 0
+            assert torch.equal(out.view(torch.int32), ref.view(torch.int32))
+
+
+def test_noalloc_makes_no_allocation():
+    import paged_kv_cache_writes_gb300 as pa
+    from paged_kv_cache_writes_gb300.staging import DeviceBatch
+    f = _noalloc_fn()
+    b = W.decode_batch("noalloc-mem", [1500, 40, 900], 32, 8, 128, 16, "bf16", seed=43, partition_size=256)
+    dev = DeviceBatch(b, "cuda")
+    dev.run_setup()
+    dev.write_step()
+    out = torch.empty_like(dev.out)
+    assert _call(f, dev, out) == 0      # first call on the device: set-up (and lazy module loading)
+    torch.cuda.synchronize()
+    allocs = torch.cuda.memory_stats().get("allocation.all.allocated", 0)
+    free0, _ = torch.cuda.mem_get_info()
+    for _ in range(3):
+        assert _call(f, dev, out) == 0
+    torch.cuda.synchronize()
+    assert pa.pa_get_device_error() == 0
+    assert torch.cuda.memory_stats().get("allocation.all.allocated", 0) == allocs
+    assert torch.cuda.mem_get_info()[0] == free0
 
 
 def test_noalloc_rejects_problems_larger_than_its_scratch():
