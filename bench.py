@@ -44,6 +44,7 @@ sys.path.insert(0, ROOT)
 METRIC = "paged-attn decode KV GB/s and tokens/s/layer on 1 GB300; % of HBM roofline"
 UNIT = "GB/s"
 WORKLOAD = "Llama-3-70B-shaped decode layer"
+NOMINAL_HBM_GBPS = 7900.0     # GB300 HBM3e, vendor figure (context; the roofline uses the measured copy rate)
 
 
 def _peaks():
@@ -74,19 +75,10 @@ def _causal_flops(b) -> float:
     return 4.0 * b.head_dim * b.num_q_heads * keys
 
 
-PREFILL_WORKLOADS = {
-    # the chunk of the chunked-prefill mixed batch (fp8 KV, bf16 q): one 512-row chunk over 4096 tokens
-    "mixed_fp8_chunk": ("chunked-prefill mixed batch, fp8 KV: 512-token chunk at position 4096, GQA 32/8, "
-                        "head_dim 128, block 16"),
-    # enough rows to give every SM a CTA: 8 chunks of 2048 tokens over 2048 tokens of context, bf16 KV
-    "bf16_8x2048": "8 chunks x 2048 tokens at position 2048, GQA 32/8, head_dim 128, block 16, bf16 KV",
-    # chunk-size and shape variants: one 2048-token chunk at position 4096 (GQA 32/8), and an MHA layer
-    # (32 KV heads) with 4 chunks of 1024 tokens at position 1024
-    "bf16_chunk2048": "one 2048-token chunk at position 4096, GQA 32/8, head_dim 128, block 16, bf16 KV",
-    "bf16_mha_4x1024": "4 chunks x 1024 tokens at position 1024, MHA 32/32, head_dim 128, block 16, bf16 KV",
-    # the smallest chunk size the pages name: 16 chunks of 256 tokens at position 1024
-    "bf16_16x256": "16 chunks x 256 tokens at position 1024, GQA 32/8, head_dim 128, block 16, bf16 KV",
-}
+# the chunk of the chunked-prefill mixed batch (fp8 KV, bf16 q: one 512-row chunk over 4096 tokens), then the
+# prefill-only batches of workloads.PREFILL_WORKLOADS (2048 / 256-token chunks, MHA, every SM busy)
+MIXED_CHUNK_DESC = ("chunked-prefill mixed batch, fp8 KV: 512-token chunk at position 4096, GQA 32/8, "
+                    "head_dim 128, block 16")
 
 
 def measure_block_manager() -> dict:
@@ -138,10 +130,7 @@ def measure_other_decodes(dev_name: str, steps: int, warmup: int) -> dict:
              ("mixed_fp8_decodes", W.cfg_mixed_fp8),
              ("llama8b_fp8_cache", lambda: W.cfg_llama8b(kv_dtype="fp8")),
              ("llama70b_fp8_cache", lambda: W.cfg_llama70b(kv_dtype="fp8")),
-             ("llama70b_fp8_cache_head_scales",
-              lambda: W.decode_batch("Llama-3-70B-shaped decode layer, fp8 KV with per-head scales",
-                                     W.lognormal_lens(np.random.default_rng(102), 256), 64, 8, 128, 32, "bf16",
-                                     kv_dtype="fp8", seed=2, partition_size=512, fp8_scales="head")))
+             ("llama70b_fp8_cache_head_scales", lambda: W.cfg_llama70b(kv_dtype="fp8", fp8_scales="head")))
     for key, fn in cases:
         b = fn()
         db = DeviceBatch(b, dev_name)
@@ -160,14 +149,33 @@ def measure_other_decodes(dev_name: str, steps: int, warmup: int) -> dict:
         assert pa.pa_get_device_error() == 0
         ms = e0.elapsed_time(e1) / steps
         gbs = b.decode_kv_bytes() / (ms * 1e-3) / 1e9
-        res[key] = {"workload": b.name, "kv_dtype": b.kv_dtype, "num_seqs": b.num_seqs,
-                    "heads": f"{b.num_q_heads}/{b.num_kv_heads}", "kv_bytes": b.decode_kv_bytes(), "ms": ms,
-                    "GBps": gbs, "frac_of_hbm": gbs / peak, "peak_source": kind,
-                    "note": "shared prefix blocks are read once per branch (counted per branch)"
-                    if key == "shared_prefix" else None}
+        r = {"workload": b.name, "kv_dtype": b.kv_dtype, "num_seqs": b.num_seqs,
+             "heads": f"{b.num_q_heads}/{b.num_kv_heads}", "kv_bytes": b.decode_kv_bytes(), "ms": ms,
+             "GBps": gbs, "frac_of_hbm": gbs / peak, "peak_source": kind, "note": None}
+        if key == "shared_prefix":
+            # logical bytes count each shared prefix block once per branch that reads it; the unique
+            # bytes count each physical block once (a floor for the DRAM traffic, re-reads may hit L2)
+            uniq = unique_kv_bytes(b)
+            r.pop("frac_of_hbm")
+            r.update({"GBps_logical": r.pop("GBps"), "frac_of_hbm_logical": gbs / peak, "kv_bytes_unique": uniq,
+                      "GBps_unique": uniq / (ms * 1e-3) / 1e9, "frac_of_hbm_unique": uniq / (ms * 1e-3) / 1e9 / peak,
+                      "note": "kv_bytes counts the shared prefix once per branch (logical); kv_bytes_unique "
+                              "counts each physical block once"})
+        res[key] = r
         del db
         torch.cuda.empty_cache()
     return res
+
+
+def unique_kv_bytes(b) -> int:
+    """K+V bytes of the physical blocks a decode pass reads, each block once (the most tokens of it
+    that any sequence reads), for batches whose sequences share blocks."""
+    used = {}
+    for i, L in enumerate(b.seq_lens.astype(np.int64)):
+        for j in range(int(-(-L // b.block_size))):
+            blk = int(b.block_tables[i, j])
+            used[blk] = max(used.get(blk, 0), int(min(b.block_size, L - j * b.block_size)))
+    return sum(used.values()) * 2 * b.num_kv_heads * b.head_dim * b.kv_elem_bytes
 
 
 def measure_mixed_step(dev_name: str, steps: int, warmup: int) -> dict:
@@ -216,17 +224,10 @@ def measure_prefill(dev_name: str, steps: int, warmup: int) -> dict:
     from paged_kv_cache_writes_gb300.staging import DeviceBatch
     peak, kind = _tensor_peak()
     res = {}
-    for key, desc in PREFILL_WORKLOADS.items():
-        if key == "mixed_fp8_chunk":
-            b = W.cfg_mixed_fp8()
-        elif key == "bf16_8x2048":
-            b = W.prefill_batch("prefill 8x2048", [(2048, 2048)] * 8, 32, 8, 128, 16, "bf16", seed=3)
-        elif key == "bf16_chunk2048":
-            b = W.prefill_batch("prefill chunk 2048", [(4096, 2048)], 32, 8, 128, 16, "bf16", seed=5)
-        elif key == "bf16_16x256":
-            b = W.prefill_batch("prefill 16x256", [(1024, 256)] * 16, 32, 8, 128, 16, "bf16", seed=7)
-        else:
-            b = W.prefill_batch("prefill MHA 4x1024", [(1024, 1024)] * 4, 32, 32, 128, 16, "bf16", seed=6)
+    cases = [("mixed_fp8_chunk", MIXED_CHUNK_DESC, W.cfg_mixed_fp8)]
+    cases += [(k, d, f) for k, (d, f) in W.PREFILL_WORKLOADS.items()]
+    for key, desc, make in cases:
+        b = make()
         db = DeviceBatch(b, dev_name)
         db.run_setup()
         db.write_step()
@@ -256,26 +257,36 @@ def measure_prefill(dev_name: str, steps: int, warmup: int) -> dict:
 DECODE_SOURCES = ("pa_decode_tc.cuh", "pa_tcgen05.cuh", "pa_decode.cuh", "pa_attention.cuh", "pa_common.cuh")
 
 
-def _profiled_traffic(kv_bytes: int):
-    """DRAM bytes per decode launch, scaled from the committed ncu capture of the
-    decode kernel -- or None if the decode sources changed since that capture."""
+def _sources_hash(names) -> str:
     import hashlib
+    h = hashlib.sha256()
+    for f in names:
+        with open(os.path.join(ROOT, "paged_kv_cache_writes_gb300", "csrc", f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def _profile_figures(profile: str, sources) -> dict | None:
+    """The ``name: number`` lines of a committed ncu summary under profiles/, or None when the
+    summary is missing or the kernel's sources changed since it was captured (source_sha256_16)."""
     import re
-    path = os.path.join(ROOT, "profiles", "decode_tc_kernel__llama70b_decode.md")
+    path = os.path.join(ROOT, "profiles", profile)
     if not os.path.exists(path):
         return None
     text = open(path).read()
-    m1 = re.search(r"traffic_per_kv_byte:\s*([0-9.]+)", text)
-    m2 = re.search(r"source_sha256_16:\s*([0-9a-f]{16})", text)
-    if not (m1 and m2):
+    m = re.search(r"^source_sha256_16:\s*([0-9a-f]{16})\s*$", text, re.M)
+    if not m or m.group(1) != _sources_hash(sources):
         return None
-    h = hashlib.sha256()
-    for f in DECODE_SOURCES:
-        with open(os.path.join(ROOT, "paged_kv_cache_writes_gb300", "csrc", f), "rb") as fh:
-            h.update(fh.read())
-    if h.hexdigest()[:16] != m2.group(1):
+    return {k: float(v) for k, v in re.findall(r"^([a-z][a-z0-9_]*):\s*([0-9.eE+-]+)\s*$", text, re.M)}
+
+
+def _profiled_traffic(kv_bytes: int):
+    """DRAM bytes per decode launch, scaled from the committed ncu capture of the
+    decode kernel -- or None if the decode sources changed since that capture."""
+    f = _profile_figures("decode_tc_kernel__llama70b_decode.md", DECODE_SOURCES)
+    if not f or "traffic_per_kv_byte" not in f:
         return None
-    return float(m1.group(1)) * kv_bytes
+    return f["traffic_per_kv_byte"] * kv_bytes
 
 
 def _config(b, extra=None):
@@ -291,8 +302,51 @@ def _config(b, extra=None):
     return cfg
 
 
+_NVML_REASONS = {0x8: "hw_slowdown", 0x40: "hw_thermal_slowdown", 0x20: "sw_thermal_slowdown", 0x4: "sw_power_cap"}
+
+
+class _Nvml:
+    """Read-only NVML queries through ctypes (SM clock, its maximum, clock-event reasons)."""
+
+    def __init__(self, cuda_index: int):
+        import ctypes
+        self.c = ctypes
+        self.lib = ctypes.CDLL("libnvidia-ml.so.1")
+        if self.lib.nvmlInit_v2() != 0:
+            raise OSError("nvmlInit failed")
+        self.h = ctypes.c_void_p()
+        bus = None
+        try:
+            import torch
+            pr = torch.cuda.get_device_properties(cuda_index)
+            bus = "%08x:%02x:%02x.0" % (pr.pci_domain_id, pr.pci_bus_id, pr.pci_device_id)
+        except Exception:
+            bus = None
+        ok = bus is not None and self.lib.nvmlDeviceGetHandleByPciBusId_v2(bus.encode(), ctypes.byref(self.h)) == 0
+        if not ok and self.lib.nvmlDeviceGetHandleByIndex_v2(cuda_index, ctypes.byref(self.h)) != 0:
+            raise OSError("no NVML handle")
+        try:
+            self.reasons_fn = self.lib.nvmlDeviceGetCurrentClocksEventReasons
+        except AttributeError:
+            self.reasons_fn = self.lib.nvmlDeviceGetCurrentClocksThrottleReasons
+
+    def sm_mhz(self) -> int:
+        v = self.c.c_uint()
+        return v.value if self.lib.nvmlDeviceGetClockInfo(self.h, 1, self.c.byref(v)) == 0 else -1
+
+    def sm_max_mhz(self) -> int:
+        v = self.c.c_uint()
+        return v.value if self.lib.nvmlDeviceGetMaxClockInfo(self.h, 1, self.c.byref(v)) == 0 else -1
+
+    def reasons(self) -> int:
+        v = self.c.c_ulonglong()
+        return v.value if self.reasons_fn(self.h, self.c.byref(v)) == 0 else 0
+
+
 class ClockSampler:
-    """nvidia-smi samples of SM clock and throttle reasons during the timed region."""
+    """SM clock and throttle reasons sampled during the timed region: NVML read in a
+    thread of this process every ~0.5 ms (the timed region can be a few ms long),
+    and nvidia-smi every 200 ms when NVML cannot be loaded."""
     Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
          "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
          "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
@@ -300,9 +354,20 @@ class ClockSampler:
     def __init__(self, index: int):
         self.index = index
         self.proc = None
+        self.nvml = None
         self.lines = []
+        self.samples = []       # (sm MHz, reason bits)
+        self.stop = threading.Event()
 
     def __enter__(self):
+        try:
+            self.nvml = _Nvml(self.index)
+            self.max_mhz = self.nvml.sm_max_mhz()
+            self.thread = threading.Thread(target=self._poll, daemon=True)
+            self.thread.start()
+            return self
+        except (OSError, AttributeError):
+            self.nvml = None
         try:
             self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.index), "--query-gpu=" + self.Q,
                                           "--format=csv,noheader,nounits", "-lms", "200"],
@@ -314,11 +379,19 @@ class ClockSampler:
         time.sleep(0.3)
         return self
 
+    def _poll(self):
+        while not self.stop.is_set():
+            self.samples.append((self.nvml.sm_mhz(), self.nvml.reasons()))
+            time.sleep(0.0005)
+
     def _read(self):
         for ln in self.proc.stdout:
             self.lines.append(ln.strip())
 
     def __exit__(self, *a):
+        self.stop.set()
+        if self.nvml is not None:
+            self.thread.join(timeout=5)
         if self.proc is not None:
             self.proc.terminate()
             try:
@@ -327,6 +400,11 @@ class ClockSampler:
                 self.proc.kill()
 
     def summary(self):
+        if self.nvml is not None:
+            sm = [m for m, _ in self.samples if m > 0]
+            reasons = sorted({n for _, r in self.samples for bit, n in _NVML_REASONS.items() if r & bit})
+            return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": self.max_mhz,
+                    "reasons": reasons, "samples": len(sm), "source": "NVML, every ~0.5 ms"}
         sm, mx, reasons = [], None, set()
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
         for ln in self.lines:
@@ -342,7 +420,34 @@ class ClockSampler:
                 if v.lower().startswith("active"):
                     reasons.add(n)
         return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": mx,
-                "reasons": sorted(reasons), "samples": len(sm)}
+                "reasons": sorted(reasons), "samples": len(sm), "source": "nvidia-smi, every 200 ms"}
+
+
+def measure_stream_copy(dev_name: str) -> dict:
+    """Device-to-device copy of 2 GiB (torch copy_, bytes read + written), best of 10 with CUDA events:
+    the HBM figure of this run, beside the measured peak and the nominal one."""
+    import torch
+    n = 1 << 30
+    a = torch.empty(n, dtype=torch.bfloat16, device=dev_name).fill_(1.0)
+    bb = torch.empty_like(a)
+    for _ in range(3):
+        bb.copy_(a)
+    torch.cuda.synchronize()
+    best = None
+    for _ in range(10):
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        bb.copy_(a)
+        e1.record()
+        torch.cuda.synchronize()
+        t = e0.elapsed_time(e1)
+        best = t if best is None else min(best, t)
+    del a, bb
+    torch.cuda.empty_cache()
+    peak, kind = _peaks()
+    return {"GBps": 2 * 2 * n / (best * 1e-3) / 1e9, "how": "torch copy_ of 1 Gi bf16 elements (read + write bytes), "
+            "best of 10, CUDA events", "measured_peak_GBps": peak, "measured_peak_source": kind,
+            "nominal_hbm3e_GBps": NOMINAL_HBM_GBPS}
 
 
 def _dist():
@@ -588,6 +693,10 @@ def run_ours(args):
         "gpu_launches": 2 * args.steps,  # per step: decode plan, decode (the cache write is inside)
         "clocks": clocks.summary(),
     }
+    prof = _profile_figures("decode_tc_kernel__llama70b_decode.md", DECODE_SOURCES)
+    if prof:
+        # pipe figures of the committed ncu capture of this kernel (same sources)
+        line["roofline"]["ncu"] = {k: v for k, v in prof.items() if k != "traffic_per_kv_byte"}
     if ws == 1:
         # the same step through the CUDA-core decode kernel (selectable; the default uses the tensor cores)
         with pa.decode_kernel("cuda_cores"):
@@ -612,6 +721,7 @@ def run_ours(args):
         line["other_decodes"] = measure_other_decodes(dev_name, max(5, args.steps // 5), args.warmup)
         line["mixed_step"] = measure_mixed_step(dev_name, max(5, args.steps // 5), args.warmup)
         line["block_manager"] = measure_block_manager()
+        line["stream_copy"] = measure_stream_copy(dev_name)
     if not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_oracle_rate(b, args.cpu_seconds)
     print(json.dumps(line))
@@ -619,10 +729,65 @@ def run_ours(args):
         torch.distributed.destroy_process_group()
 
 
+def run_case(args):
+    """--case NAME: W warm-up and K timed calls of one kernel on one workload, for ncu captures.
+    decode_bf16 / decode_fp8 / decode_fp8_head: pa_decode on the Llama-3-70B-shaped batch (--batch
+    sequences); decode_write: pa_decode_write on it; prefill:<key>: pa_prefill_chunk on the mixed
+    batch's chunk (mixed_fp8_chunk) or a batch of workloads.PREFILL_WORKLOADS; mixed: pa_mixed_step
+    on the chunked-prefill mixed batch; mixed_two: its pa_prefill_chunk + pa_decode."""
+    import torch
+    import workloads as W
+    from paged_kv_cache_writes_gb300 import build_lib
+    build_lib.build()
+    import paged_kv_cache_writes_gb300 as pa
+    from paged_kv_cache_writes_gb300.staging import DeviceBatch
+    torch.cuda.set_device(0)
+    c = args.case
+    if c.startswith("decode"):
+        kv = "fp8" if "fp8" in c else "bf16"
+        b = W.cfg_llama70b(batch=args.batch, kv_dtype=kv, fp8_scales="head" if c.endswith("_head") else "tensor")
+    elif c.startswith("prefill:"):
+        key = c.split(":", 1)[1]
+        b = W.cfg_mixed_fp8() if key == "mixed_fp8_chunk" else W.PREFILL_WORKLOADS[key][1]()
+    elif c in ("mixed", "mixed_two"):
+        b = W.cfg_mixed_fp8()
+    else:
+        raise SystemExit(f"unknown case {c}")
+    db = DeviceBatch(b, "cuda:0")
+    db.run_setup()
+    if c != "decode_write":
+        db.write_step()
+
+    def two():
+        db.prefill_chunk()
+        db.decode()
+    fn = {"decode_write": db.decode_write, "mixed": db.mixed_attention, "mixed_two": two}.get(
+        c, db.prefill_chunk if c.startswith("prefill:") else db.decode)
+    for _ in range(args.warmup):
+        fn()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(args.steps):
+        fn()
+    e1.record()
+    torch.cuda.synchronize()
+    assert pa.pa_get_device_error() == 0
+    ms = e0.elapsed_time(e1) / args.steps
+    out = {"case": c, "workload": b.name, "ms": ms, "steps": args.steps, "warmup": args.warmup}
+    if c.startswith("decode"):
+        out["kv_bytes"] = b.decode_kv_bytes()
+        out["GBps"] = b.decode_kv_bytes() / (ms * 1e-3) / 1e9
+    elif c.startswith("prefill:"):
+        out["useful_tflop"] = _causal_flops(b) / 1e12
+        out["TFLOPs"] = _causal_flops(b) / (ms * 1e-3) / 1e12
+    print(json.dumps(out))
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--steps", type=int, default=200)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-cpu-baseline", action="store_true")
@@ -631,9 +796,15 @@ def main():
                     help="sequences in the decode batch (256 = the named workload; smaller only for profiling)")
     ap.add_argument("--prefill-only", action="store_true",
                     help="time only the tensor-core prefill kernel (profiling)")
+    ap.add_argument("--case", default=None,
+                    help="time one kernel alone (profiling): decode_bf16, decode_fp8, decode_fp8_head, "
+                         "decode_write, prefill:<key>, mixed, mixed_two")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
+    if args.case:
+        run_case(args)
+        return
     if args.prefill_only:
         import torch
         from paged_kv_cache_writes_gb300 import build_lib
