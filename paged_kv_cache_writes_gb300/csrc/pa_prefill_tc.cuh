@@ -30,8 +30,9 @@
 //    each inside one block of the block table) of every K and V tile into a
 //    ring of kStages tiles, 512 contiguous bytes per warp instruction.
 //    16-bit caches: 16-byte cp.async straight into the 128-byte-swizzled MMA
-//    layout; fp8 caches: register loads a quarter tile ahead, widened
-//    exactly to the query's 16-bit type on the way to shared memory.  Rows past the end of the sequence are
+//    layout; fp8 caches: register loads a whole tile ahead (half a tile with
+//    two Q tiles per CTA), widened exactly to f16 on the way to shared
+//    memory.  Rows past the end of the sequence are
 //    zero-filled so a zero probability never meets a stale (possibly NaN)
 //    value in the MMA.
 //  * last warp, MMA (one elected lane issues): for each Q tile t in turn,
@@ -39,12 +40,19 @@
 //    K_{j+1}^T into the same buffer once that P.V has completed; with two Q
 //    tiles, one tile's MMAs run while the other tile's softmax works.
 //
-// Precision.  Q, K and V are exact in the MMA (fp8 codes widen exactly to
-// bf16/f16); accumulation is fp32.  P must be 16-bit in the MMA: with a bf16
-// cache P is split into hi + lo bf16 parts (two P.V MMAs) that sum to P
-// within 2^-15 relative; with f16 or fp8 caches P is rounded once and the
-// softmax denominator sums the rounded P, so the output remains a convex
-// combination of V rows.
+// Precision.  K and V are exact in the MMA; accumulation is fp32.  With a
+// 16-bit cache the MMAs take the cache's type and Q is exact.  With an fp8
+// cache they take f16 operands: the codes widen to f16 exactly (one
+// conversion per pair, where bf16 would take three), and bf16 query rows are
+// each multiplied by a power of two 2^e that puts the row's largest element
+// in [2^14, 2^15) and rounded to f16, exact for every element above 2^-28 of
+// that largest one (bf16 has 8 significant bits, f16 11); the scores are
+// multiplied back by 2^-e in the softmax.  P must be 16-bit in the MMA: with
+// a bf16 cache P is split into hi + lo bf16 parts (two P.V MMAs) that sum to
+// P within 2^-15 relative; otherwise P is rounded once to f16 (by integer
+// operations: to nearest even above 2^-14, within one subnormal step below)
+// and the softmax denominator sums the rounded P, so the output remains a
+// convex combination of V rows.
 //
 // Every mbarrier wait is bounded (PA_ERR_TIMEOUT, then the CTA abandons its
 // work); before tensor memory is freed the CTA waits for its outstanding MMAs
@@ -138,8 +146,8 @@ __device__ __forceinline__ void prefill_tc_body(const PrefillTcParams &p, int bx
   constexpr bool kBf16 = std::is_same<QT, __nv_bfloat16>::value;
   constexpr bool kSplit = kBf16 && !kFp8;   // bf16 cache: P as hi + lo
   constexpr int BR = kQTiles * kM / G;      // token rows per CTA
-  constexpr uint32_t kAB = kBf16 ? 1u : 0u;
-  constexpr int kChunks = kN / 32;          // 32-key chunks of a score tile
+  constexpr bool kF16Ops = kFp8 || !kBf16;   // f16 MMA operands (f16 cache, or any fp8 cache)
+  constexpr uint32_t kAB = kF16Ops ? 0u : 1u;
   const float kNegInf = -__int_as_float(0x7f800000);
 
   extern __shared__ uint8_t smem_raw[];
@@ -221,17 +229,50 @@ __device__ __forceinline__ void prefill_tc_body(const PrefillTcParams &p, int bx
     const int lim = row_ok ? min(seq_eff, max(0, qs + r0 + rl + 1)) : 0;
     const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
     // scores are scaled by |s_mult| in the exponent; a negative scale flips q's sign instead
-    const float cmul = fabsf(p.s_mult) * (p.k_hs ? __ldg(p.k_hs + g) : 1.f);
+    float cmul = fabsf(p.s_mult) * (p.k_hs ? __ldg(p.k_hs + g) : 1.f);
     const uint32_t qflip = p.s_mult < 0.f ? 0x80008000u : 0u;
     {  // stage row m of Q (16-bit, 128-byte-swizzled K-major, 2 panels per tile)
       const QT *src = static_cast<const QT *>(p.q) + ((int64_t)(cu0 + r0 + rl) * p.num_q_heads + head) * kD;
       const int mr = m % kM;
       uint8_t *qt = smem + L::kOffQ + t * kQBytes;
+      if constexpr (kFp8 && kBf16) {
+        // f16 operands: the row times 2^e (its largest element in [2^14, 2^15)), rounded to f16;
+        // the scores are multiplied back by 2^-e
+        uint4 v[16];
+        float amax = 0.f;
 #pragma unroll
-      for (int ch = 0; ch < 16; ++ch) {
-        uint4 v = row_ok ? __ldg(reinterpret_cast<const uint4 *>(src) + ch) : make_uint4(0, 0, 0, 0);
-        v.x ^= qflip; v.y ^= qflip; v.z ^= qflip; v.w ^= qflip;
-        *reinterpret_cast<uint4 *>(qt + (ch >> 3) * (kM * 128) + mr * 128 + (((ch & 7) ^ (mr & 7)) << 4)) = v;
+        for (int ch = 0; ch < 16; ++ch) {
+          v[ch] = row_ok ? __ldg(reinterpret_cast<const uint4 *>(src) + ch) : make_uint4(0, 0, 0, 0);
+          const uint32_t ws[4] = {v[ch].x, v[ch].y, v[ch].z, v[ch].w};
+#pragma unroll
+          for (int i = 0; i < 4; ++i)
+            amax = fmaxf(amax, fmaxf(__uint_as_float((ws[i] << 16) & 0x7fffffffu),
+                                     __uint_as_float(ws[i] & 0x7fff0000u)));   // NaN ignored
+        }
+        const int eb = max(1, (int)((__float_as_uint(amax) >> 23) & 0xff));
+        const int e = amax > 0.f ? max(-126, min(126, 141 - eb)) : 0;
+        const float sc = __uint_as_float((uint32_t)(e + 127) << 23);
+        cmul *= __uint_as_float((uint32_t)(127 - e) << 23);
+#pragma unroll
+        for (int ch = 0; ch < 16; ++ch) {
+          const uint32_t ws[4] = {v[ch].x, v[ch].y, v[ch].z, v[ch].w};
+          uint32_t o[4];
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            const float2 f = unpack2(ws[i], __nv_bfloat16{});
+            const __half2 h = __floats2half2_rn(f.x * sc, f.y * sc);
+            o[i] = *reinterpret_cast<const uint32_t *>(&h) ^ qflip;
+          }
+          *reinterpret_cast<uint4 *>(qt + (ch >> 3) * (kM * 128) + mr * 128 + (((ch & 7) ^ (mr & 7)) << 4)) =
+              make_uint4(o[0], o[1], o[2], o[3]);
+        }
+      } else {
+#pragma unroll
+        for (int ch = 0; ch < 16; ++ch) {
+          uint4 v = row_ok ? __ldg(reinterpret_cast<const uint4 *>(src) + ch) : make_uint4(0, 0, 0, 0);
+          v.x ^= qflip; v.y ^= qflip; v.z ^= qflip; v.w ^= qflip;
+          *reinterpret_cast<uint4 *>(qt + (ch >> 3) * (kM * 128) + mr * 128 + (((ch & 7) ^ (mr & 7)) << 4)) = v;
+        }
       }
     }
     fence_async_smem();
@@ -240,6 +281,9 @@ __device__ __forceinline__ void prefill_tc_body(const PrefillTcParams &p, int bx
     float m_ref = kNegInf;                     // reference maximum, log2 units
     float2 lacc[4] = {{0.f, 0.f}, {0.f, 0.f}, {0.f, 0.f}, {0.f, 0.f}};   // partial row sums
     const float2 ones = make_float2(1.f, 1.f);
+    const float2 zero2 = make_float2(0.f, 0.f);
+    const float2 k2m112 = make_float2(__uint_as_float(15u << 23), __uint_as_float(15u << 23));     // 2^-112
+    const float2 k2p112 = make_float2(__uint_as_float(239u << 23), __uint_as_float(239u << 23));   // 2^112
     bool ok = true;
     auto wait_all = [&](uint64_t *bar, uint32_t parity) {
       return __all_sync(0xffffffffu, wait_or_abort(bar, parity, p.err, abort_flag));
@@ -259,7 +303,7 @@ __device__ __forceinline__ void prefill_tc_body(const PrefillTcParams &p, int bx
 #pragma unroll
       for (int i = 0; i < 8; ++i) mx[i] = kNegInf;
 #pragma unroll
-      for (int ck = 0; ck < kChunks; ++ck) {
+      for (int ck = 0; ck < kN / 32; ++ck) {
         float sv[32];
         tmem_ld32(sb + 32 * ck, sv);
         if (!full_tile) {
@@ -302,7 +346,7 @@ __device__ __forceinline__ void prefill_tc_body(const PrefillTcParams &p, int bx
       const float msub = m_ref == kNegInf ? 0.f : m_ref;
       const float2 cc = make_float2(cmul, cmul), nm = make_float2(-msub, -msub);
 #pragma unroll 1
-      for (int ck = 0; ck < kChunks; ++ck) {
+      for (int ck = 0; ck < kN / 32; ++ck) {
 #pragma unroll
         for (int hh = 0; hh < 2; ++hh) {   // keys 32ck + 16hh .. +15
           float sv[16];
@@ -326,15 +370,20 @@ __device__ __forceinline__ void prefill_tc_body(const PrefillTcParams &p, int bx
                                       make_float2(-1.f, -1.f), pk);
               wl[k] = pack_hi_halves(__float_as_uint(lo.x), __float_as_uint(lo.y));
               lacc[k & 3] = ffma2(pk, ones, lacc[k & 3]);
-            } else if constexpr (kBf16) {
-              // integer rounding keeps the conversion off the transcendental pipe
-              const uint32_t h0 = bf16_round_bits(pk.x), h1 = bf16_round_bits(pk.y);
-              w[k] = pack_hi_halves(h0, h1);
-              lacc[k & 3] = ffma2(make_float2(__uint_as_float(h0), __uint_as_float(h1)), ones,
-                                  lacc[k & 3]);   // the rounded P that the MMA will use
             } else {
-              w[k] = pack2(pk.x, pk.y, QT{});
-              lacc[k & 3] = ffma2(unpack2(w[k], QT{}), ones, lacc[k & 3]);   // the rounded P the MMA uses
+              // f16 P rounded by integer operations (conversion instructions share
+              // the exponentials' pipe): p 2^-112 (p <= 2^8) carries the f16
+              // pattern, normal or subnormal, in bits 13..28 of its fp32 pattern.
+              // To nearest even for p >= 2^-14; below, within one f16 subnormal
+              // step (the product is rounded first).  The denominator sums the
+              // rounded P.
+              const float2 sv2 = ffma2(pk, k2m112, zero2);
+              uint32_t u0 = __float_as_uint(sv2.x), u1 = __float_as_uint(sv2.y);
+              u0 += 0xfffu + ((u0 >> 13) & 1u);
+              u1 += 0xfffu + ((u1 >> 13) & 1u);
+              w[k] = (u0 >> 13) | ((u1 << 3) & 0xffff0000u);
+              lacc[k & 3] = ffma2(make_float2(__uint_as_float(u0 & 0xffffe000u), __uint_as_float(u1 & 0xffffe000u)),
+                                  k2p112, lacc[k & 3]);
             }
           }
           // P of these 16 keys goes over their own 16 score columns (read just
@@ -450,8 +499,11 @@ __device__ __forceinline__ void prefill_tc_body(const PrefillTcParams &p, int bx
       }
     } else {
       // fp8 rows (128 B): per instruction 4 rows x 8 words of 16 codes.  A tile
-      // is four quarters (K run 0, K run 1, V run 0, V run 1); the next quarter
-      // is in flight while the current one is widened into shared memory.
+      // is four quarters (K run 0, K run 1, V run 0, V run 1).  The loads run
+      // kPf quarters ahead of the widening into shared memory: a whole tile
+      // (32 KB of codes per CTA) with one Q tile per CTA, half a tile with two
+      // (whose threads have fewer registers each).
+      constexpr int kPf = kQTiles == 1 ? 4 : 2;
       const int q = lane & 7, pn = q >> 2, c0 = (2 * q) & 7;
       auto load = [&](int j, int qi, uint4 (&w)[4]) {
         int64_t row0;
@@ -463,33 +515,35 @@ __device__ __forceinline__ void prefill_tc_body(const PrefillTcParams &p, int bx
           w[i] = rr < nval ? ld_nc16(pool + (row0 + rr) * kRowBytes + q * 16) : make_uint4(0, 0, 0, 0);
         }
       };
-      uint4 cur[4], nxt[4];
-      if (nkt > 0) load(0, 0, cur);
+      uint4 buf[kPf][4];   // quarter g of the load order in buf[g % kPf]
+#pragma unroll
+      for (int g = 0; g < kPf; ++g)
+        if (g / 4 < nkt) load(g / 4, g % 4, buf[g]);
       for (int j = 0; j < nkt && ok; ++j) {
         const int s = j % kStages;
         const uint32_t ph_prev = ((j / kStages) - 1) & 1;
 #pragma unroll
         for (int qi = 0; qi < 4; ++qi) {
           const int which = qi >> 1, r = qi & 1;
-          if (qi < 3) load(j, qi + 1, nxt);
-          else if (j + 1 < nkt) load(j + 1, 0, nxt);
           if (r == 0 && j >= kStages && !wait_slot(which ? &v_free[s] : &k_free[s], ph_prev)) break;
           uint8_t *tile = smem + (which ? L::kOffV : L::kOffK) + s * kTileBytes + pn * kTilePanel;
+          uint4 (&cur)[4] = buf[qi % kPf];
 #pragma unroll
           for (int i = 0; i < 4; ++i) {
             const int row = 32 * lw + 16 * r + 4 * i + (lane >> 3);
             uint32_t o[8];
-            widen16<QT>(cur[i], o);
+            widen16<__half>(cur[i], o);   // the MMAs take f16 operands with an fp8 cache
             uint8_t *dst = tile + row * 128;
             *reinterpret_cast<uint4 *>(dst + ((c0 ^ (row & 7)) << 4)) = make_uint4(o[0], o[1], o[2], o[3]);
             *reinterpret_cast<uint4 *>(dst + (((c0 + 1) ^ (row & 7)) << 4)) = make_uint4(o[4], o[5], o[6], o[7]);
           }
+          // refill the buffer with the quarter kPf ahead in the load order
+          const int g = 4 * j + qi + kPf;
+          if (g / 4 < nkt) load(g / 4, g % 4, cur);
           if (r == 1) {
             fence_async_smem();
             mbar_arrive(which ? &v_full[s] : &k_full[s]);
           }
-#pragma unroll
-          for (int i = 0; i < 4; ++i) cur[i] = nxt[i];
         }
       }
     }
