@@ -120,6 +120,7 @@ constexpr int kKeys = 128;                // keys per tile (MMA M, tensor-memory
 constexpr int kMaxTiles = 4;              // tiles per unit: partitions hold <= 512 tokens
 constexpr int kInfo = 4;                  // unit descriptors in flight (bounds how far a CTA claims ahead)
 constexpr int kClaim = 2;                 // units per claim (a power of two)
+constexpr int kRep = 8;                   // split units handed from the softmax warps to the merge warp
 // A 16-bit K or V tile in shared memory: 16 atoms of 8 keys, atom a at
 // a * 2048, its first 64 elements (128-byte rows, 128-byte swizzle) at +0 and
 // the last 64 at +1024 -- the layout of a 4D bulk-tensor box {64, 8 rows,
@@ -177,18 +178,21 @@ struct TcGeo {
   static constexpr int kSlotBytes = kFp8 ? kKeys * kD : kKeys * kD * 2;   // one K or V tile
   static constexpr int kColO = 2 * kMaxTiles * kNS;                 // tensor-memory column of O^T, buffer 0
   static constexpr int kTmemCols = kColO + 2 * kNO <= 256 ? 256 : 512;
-  static constexpr int kNumBars = 2 * kMaxSlots + 8 * 2 + 2 * kInfo + 1;
+  static constexpr int kNumBars = 2 * kMaxSlots + 8 * 2 + 2 * kInfo + 1 + 2 * kRep;
   static constexpr int kOffQ = 0;                                        // [kQBufs] Q^T
   static constexpr int kOffP = kOffQ + kQBufs * kQBytes;                 // [2][4] P^T
   static constexpr int kOffRed = kOffP + 2 * kMaxTiles * kPBytes;        // float [2][4 warps][2][16]
   static constexpr int kOffInfo = kOffRed + 2 * 4 * 2 * 16 * 4;          // TcUnit [kInfo] (16-byte aligned)
   static constexpr int kOffBar = kOffInfo + kInfo * (int)sizeof(TcUnit);
   static constexpr int kOffMisc = kOffBar + kNumBars * 8;
-  static constexpr int kOffRing = (kOffMisc + 64 + 1023) / 1024 * 1024;  // [kSlots] K/V tiles
+  static constexpr int kOffRep = (kOffMisc + 16 + 15) / 16 * 16;         // int4 [kRep] reports (16-byte aligned)
+  static constexpr int kOffRing = (kOffRep + kRep * 16 + 1023) / 1024 * 1024;  // [kSlots] K/V tiles
   static constexpr int kSlots0 = (227 * 1024 - 1024 - kOffRing) / kSlotBytes;
   static constexpr int kSlots = kSlots0 > kMaxSlots ? kMaxSlots : kSlots0;
   static constexpr int kSmemBytes = kOffRing + kSlots * kSlotBytes + 1024;  // + alignment slack
   static_assert(kSlots >= 2 && kSmemBytes <= 227 * 1024, "shared memory");
+  static_assert(kOffRep % 16 == 0 && kOffInfo % 16 == 0 && kOffBar % 8 == 0 && kOffMisc % 8 == 0,
+                "aligned reports, descriptors and barriers");
   static_assert(kOffRing % 1024 == 0 && kOffP % 1024 == 0 && kQBytes % 1024 == 0 && kPBytes % 1024 == 0,
                 "1024-byte swizzle atoms");
 };
@@ -344,10 +348,15 @@ __device__ __forceinline__ void decode_tc_body(const DecodeTcParams &tp, const C
   uint64_t *info_full = red_bar + 2;          // [kInfo] unit descriptor published (32 scheduler lanes)
   uint64_t *info_free = info_full + kInfo;    // [kInfo] released by the MMA warp and the softmax warps
   uint64_t *fin = info_free + kInfo;          // every MMA of the CTA complete
+  uint64_t *rep_full = fin + 1;               // [kRep] a split unit's partials stored (one arrival per softmax warp)
+  uint64_t *rep_free = rep_full + kRep;       // [kRep] its report taken by the merge warp
   TcUnit *info = reinterpret_cast<TcUnit *>(smem + GE::kOffInfo);
   float *red = reinterpret_cast<float *>(smem + GE::kOffRed);
   uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + GE::kOffMisc);
   volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + GE::kOffMisc + 8);
+  // [kRep] reports {row, KV head, partitions (-1: the softmax warps are done), 0}; ordered
+  // by the report barriers
+  int4 *reports = reinterpret_cast<int4 *>(smem + GE::kOffRep);
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
 
@@ -374,6 +383,10 @@ __device__ __forceinline__ void decode_tc_body(const DecodeTcParams &tp, const C
       mbar_init(&info_free[i], 2);
     }
     mbar_init(fin, 1);
+    for (int i = 0; i < kRep; ++i) {
+      mbar_init(&rep_full[i], 4);   // lane 0 of each softmax warp, after the warp's stores
+      mbar_init(&rep_free[i], 1);
+    }
     *abort_flag = 0;
     fence_mbar_init();
     prefetch_tensor_map(tmap_k);
@@ -417,41 +430,19 @@ __device__ __forceinline__ void decode_tc_body(const DecodeTcParams &tp, const C
     UnitHdr prev;
     prev.valid = 0;
     bool ok = true;
-    // Completion of split units, per warp.  A unit's partial results are written
-    // in one epilogue (pending), reported in the next (one count per warp on the
-    // row's counter, an acquire-release atomic: it publishes the warp's results
-    // and, for the last count, acquires everyone else's), and the count returned
-    // is checked in the one after (reported); the warp that brings a row's count
-    // to 4 * nparts appends it to the merge list.
-    int pend_row = -1, pend_kvh = 0, pend_np = 0;
-    int rep_row = -1, rep_kvh = 0, rep_np = 0, rep_old = 0;
-    // append a merge record (one thread); any CTA's merge warp may take it
-    auto queue_job = [&](int row, int kvh, int np) {
-      const int t = atomicAdd(&p.hdr->pad[0], 1);
-      DecodeMergeJob *j = tp.jobs + t;
-      j->row = row;
-      j->kvh = kvh;
-      j->nparts = np;
-      asm volatile("st.release.gpu.global.b32 [%0], %1;" ::"l"(&j->ready), "r"(1) : "memory");
-    };
-    auto check_reported = [&]() {
-      if (rep_row >= 0) {
-        const int last = __shfl_sync(0xffffffffu, rep_old, 0) == 4 * rep_np - 1;
-        // lane 0's count acquired the other partitions' results; the record's release passes them on
-        if (last && lane == 0) queue_job(rep_row, rep_kvh, rep_np);
-        rep_row = -1;
-      }
-    };
-    auto report_pending = [&]() {
-      if (pend_row >= 0) {
-        __syncwarp();   // the warp's stores of the unit's results precede lane 0's release
-        if (lane == 0)
-          rep_old = atom_add_acq_rel_gpu(p.ws_count + (int64_t)pend_row * hq + (int64_t)pend_kvh * G, 1);
-        rep_row = pend_row;
-        rep_kvh = pend_kvh;
-        rep_np = pend_np;
-        pend_row = -1;
-      }
+    // A split unit's partial results, once stored by every softmax warp, are
+    // handed to the CTA's merge warp through a ring of reports (each warp arrives
+    // after its stores); the merge warp publishes them to the rest of the GPU,
+    // so that the release and its wait stay off the softmax warps' path.
+    int n_rep = 0;
+    auto hand_over = [&](int row, int kvh, int np) {   // np -1: no more reports
+      const int rs = n_rep % kRep;
+      if (n_rep >= kRep && !wait_all(&rep_free[rs], ((n_rep / kRep) - 1) & 1)) return false;
+      if (tid == 0) reports[rs] = make_int4(row, kvh, np, 0);
+      __syncwarp();   // the warp's stores precede lane 0's arrival
+      if (lane == 0) mbar_arrive(&rep_full[rs]);
+      ++n_rep;
+      return true;
     };
     for (int u = 0; ok; ++u) {
       const int ib = u % kInfo, b = u & 1;
@@ -588,9 +579,6 @@ __device__ __forceinline__ void decode_tc_body(const DecodeTcParams &tp, const C
         }
         tc_fence_before();
         mbar_arrive(&o_free[bp]);
-        // earlier split units first: the fence then waits only for stores one unit old
-        check_reported();
-        report_pending();
         const int64_t head0 = (int64_t)prev.row * hq + (int64_t)prev.kvh * G;
         const int d = tid;
         // the two column halves of O^T: bf16 p = hi + lo; fp8 256 p = hi + lo / 16
@@ -620,10 +608,9 @@ __device__ __forceinline__ void decode_tc_body(const DecodeTcParams &tp, const C
             p.ws_ml[(head0 + tid) * p.max_partitions + prev.part] = make_float2(mv, lv);
           }
         }
-        if (prev.nparts > 1) {
-          pend_row = prev.row;
-          pend_kvh = prev.kvh;
-          pend_np = prev.nparts;
+        if (prev.nparts > 1 && !hand_over(prev.row, prev.kvh, prev.nparts)) {
+          ok = false;
+          break;
         }
         if (tid == 0) mbar_arrive(&info_free[(u - 1) % kInfo]);
       }
@@ -632,11 +619,7 @@ __device__ __forceinline__ void decode_tc_body(const DecodeTcParams &tp, const C
 #pragma unroll
       for (int h = 0; h < G; ++h) m_prev[h] = m_cur[h];
     }
-    if (ok) {
-      check_reported();
-      report_pending();
-      check_reported();
-    }
+    if (ok) hand_over(0, 0, -1);
   } else if (warp == kLoadWarp) {
     // ===================================================== loader (one warp)
     // Q^T with cp.async (16-bit caches); every K and V tile with one
@@ -871,43 +854,94 @@ __device__ __forceinline__ void decode_tc_body(const DecodeTcParams &tp, const C
     }
   } else if (warp == kMergeWarp) {
     // ===================================================== merge (last warp)
-    // out = sum_p 2^(m_p - M) acc_p / sum_p 2^(m_p - M) l_p over a split row's
-    // partitions p (m_p in log2 units, M their maximum), kept as a running
-    // maximum; lane l merges elements 4l..4l+3 of all G heads, the loads of a
-    // partition for every head in flight together.  Records are taken from the
-    // grid-wide merge list in the order they were appended, so every CTA's
-    // merge warp shares the merging; taking record t waits (bounded) for it.
+    // Two duties, polled in turn so that neither waits on the other:
+    //  * the CTA's split units (reports from its softmax warps, in order): one
+    //    release count per unit on its row's counter publishes the partials; the
+    //    count that completes a row acquires every partition's results (fence)
+    //    and appends the row to the grid-wide merge list (record, then a release
+    //    flag);
+    //  * the merge list: out = sum_p 2^(m_p - M) acc_p / sum_p 2^(m_p - M) l_p
+    //    over a split row's partitions p (m_p in log2 units, M their maximum),
+    //    kept as a running maximum; lane l merges elements 4l..4l+3 of all G
+    //    heads, the loads of a partition for every head in flight together.
+    //    Records are claimed in the order they were appended, so every CTA's
+    //    merge warp shares the merging.
+    // Waiting without progress on either is bounded (PA_ERR_TIMEOUT).
     const int total_jobs = __ldcg(&p.hdr->pad[2]);
+    int nrep = 0, t = -1;
+    bool local_done = false, list_done = false;
+    uint64_t t_idle = global_timer_ns();
     for (;;) {
-      int t = 0;
-      if (lane == 0) t = atomicAdd(&p.hdr->pad[1], 1);
-      t = __shfl_sync(0xffffffffu, t, 0);
-      if (t >= total_jobs) break;
-      int ready = 0;
-      if (lane == 0) {
-        const uint64_t t0 = global_timer_ns();
-        for (;;) {
-          asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(ready) : "l"(&tp.jobs[t].ready) : "memory");
-          if (ready || *abort_flag) break;
-          if (global_timer_ns() - t0 > kWaitLimitNs) {
-            record_error(p.err, PA_ERR_TIMEOUT);
-            *abort_flag = 1;
-            break;
+      if (*abort_flag) break;
+      if (local_done && list_done && t < 0) break;
+      bool progress = false;
+      if (!local_done) {
+        const int rs = nrep % kRep;
+        int got = 0;
+        if (lane == 0) got = mbar_try_wait(&rep_full[rs], (nrep / kRep) & 1) ? 1 : 0;
+        if (__shfl_sync(0xffffffffu, got, 0)) {
+          if (lane == 0) {
+            const int4 r = reports[rs];
+            if (r.z < 0) {
+              got = 2;
+            } else {
+              int old;
+              asm volatile("atom.release.gpu.global.add.s32 %0, [%1], 1;"
+                           : "=r"(old)
+                           : "l"(p.ws_count + (int64_t)r.x * hq + (int64_t)r.y * G)
+                           : "memory");
+              if (old == r.z - 1) {
+                asm volatile("fence.acq_rel.gpu;" ::: "memory");
+                const int jt = atomicAdd(&p.hdr->pad[0], 1);
+                DecodeMergeJob *j = tp.jobs + jt;
+                j->row = r.x;
+                j->kvh = r.y;
+                j->nparts = r.z;
+                asm volatile("st.release.gpu.global.b32 [%0], %1;" ::"l"(&j->ready), "r"(1) : "memory");
+              }
+              mbar_arrive(&rep_free[rs]);
+            }
           }
-          __nanosleep(2000);
+          if (__shfl_sync(0xffffffffu, got, 0) == 2) local_done = true;
+          ++nrep;
+          progress = true;
         }
       }
+      if (t < 0 && !list_done) {
+        if (lane == 0) t = atomicAdd(&p.hdr->pad[1], 1);
+        t = __shfl_sync(0xffffffffu, t, 0);
+        if (t >= total_jobs) {
+          list_done = true;
+          t = -1;
+        }
+      }
+      int ready = 0;
+      if (t >= 0 && lane == 0)
+        asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(ready) : "l"(&tp.jobs[t].ready) : "memory");
+      if (!__shfl_sync(0xffffffffu, ready, 0)) {
+        if (progress) {
+          t_idle = global_timer_ns();
+        } else if (global_timer_ns() - t_idle > kWaitLimitNs) {
+          if (lane == 0) record_error(p.err, PA_ERR_TIMEOUT);
+          *abort_flag = 1;
+          break;
+        } else {
+          __nanosleep(500);
+        }
+        continue;
+      }
       int job_row = 0, job_kvh = 0, job_np = 0;
-      if (lane == 0 && ready) {   // read by the lane that acquired the record, then broadcast
+      if (lane == 0) {   // read by the lane that acquired the record, then broadcast
         const volatile DecodeMergeJob *jv = tp.jobs + t;
         job_row = jv->row;
         job_kvh = jv->kvh;
         job_np = jv->nparts;
       }
-      if (!__shfl_sync(0xffffffffu, ready, 0)) break;
       job_row = __shfl_sync(0xffffffffu, job_row, 0);
       job_kvh = __shfl_sync(0xffffffffu, job_kvh, 0);
       job_np = __shfl_sync(0xffffffffu, job_np, 0);
+      t = -1;
+      t_idle = global_timer_ns();
       __threadfence();
       const int64_t head0 = (int64_t)job_row * hq + (int64_t)job_kvh * G;
       float m[G], l[G];
