@@ -414,6 +414,100 @@ __device__ __forceinline__ void decode_tc_body(const DecodeTcParams &tp, const C
   const int hkv = p.num_kv_heads;
   const int hq = p.num_q_heads;
 
+  // Merge the split row of record t of the grid-wide merge list (its ready flag
+  // acquired by lane 0): out = sum_p 2^(m_p - M) acc_p / sum_p 2^(m_p - M) l_p
+  // over the row's partitions p (m_p in log2 units, M their maximum), kept as a
+  // running maximum; lane l merges elements 4l..4l+3 of all G heads, the loads
+  // of two partitions for every head in flight together.
+  auto merge_job = [&](int t) {
+    int job_row = 0, job_kvh = 0, job_np = 0;
+    if (lane == 0) {   // read by the lane that acquired the record, then broadcast
+      const volatile DecodeMergeJob *jv = tp.jobs + t;
+      job_row = jv->row;
+      job_kvh = jv->kvh;
+      job_np = jv->nparts;
+    }
+    job_row = __shfl_sync(0xffffffffu, job_row, 0);
+    job_kvh = __shfl_sync(0xffffffffu, job_kvh, 0);
+    job_np = __shfl_sync(0xffffffffu, job_np, 0);
+    __syncwarp();   // lane 0's acquire of the record orders every lane's reads of the partials
+    const int64_t head0 = (int64_t)job_row * hq + (int64_t)job_kvh * G;
+    float m[G], l[G];
+    float4 acc[G];
+#pragma unroll
+    for (int h = 0; h < G; ++h) {
+      m[h] = kNegInf;
+      l[h] = 0.f;
+      acc[h] = make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+    // two partitions per step: the loads of both are in flight together
+    for (int q0 = 0; q0 < job_np; q0 += 2) {
+      float2 ml[2][G];
+      float4 a[2][G];
+#pragma unroll
+      for (int k = 0; k < 2; ++k)
+#pragma unroll
+        for (int h = 0; h < G; ++h) {
+          const int q = min(q0 + k, job_np - 1);   // a lone last partition is read twice, merged once
+          const int64_t e = (head0 + h) * p.max_partitions + q;
+          ml[k][h] = __ldcg(&p.ws_ml[e]);
+          a[k][h] = __ldcg(reinterpret_cast<const float4 *>(p.ws_acc + e * kD) + lane);
+        }
+#pragma unroll
+      for (int k = 0; k < 2; ++k) {
+        if (q0 + k >= job_np) break;
+#pragma unroll
+        for (int h = 0; h < G; ++h) {
+          const float mn = fmaxf(m[h], ml[k][h].x);
+          const float so = fast_exp2(m[h] - mn), sn = fast_exp2(ml[k][h].x - mn);
+          m[h] = mn;
+          l[h] = l[h] * so + ml[k][h].y * sn;
+          acc[h] = make_float4(acc[h].x * so + a[k][h].x * sn, acc[h].y * so + a[k][h].y * sn,
+                               acc[h].z * so + a[k][h].z * sn, acc[h].w * so + a[k][h].w * sn);
+        }
+      }
+    }
+#pragma unroll
+    for (int h = 0; h < G; ++h) {
+      const float om = p.v_hs ? p.out_mult * __ldg(p.v_hs + job_kvh) : p.out_mult;
+      const float inv = l[h] > 0.f ? om / l[h] : 0.f;
+      const int64_t o0 = (head0 + h) * kD + 4 * lane;
+      store_out<QT>(p.out, o0, p.out_f32 != 0, acc[h].x * inv);
+      store_out<QT>(p.out, o0 + 1, p.out_f32 != 0, acc[h].y * inv);
+      store_out<QT>(p.out, o0 + 2, p.out_f32 != 0, acc[h].z * inv);
+      store_out<QT>(p.out, o0 + 3, p.out_f32 != 0, acc[h].w * inv);
+    }
+  };
+  // Claim records of the merge list and merge them until every one is claimed:
+  // the warps that have finished their own role help drain the list at the end
+  // of the kernel.  Waiting for a claimed record is bounded (PA_ERR_TIMEOUT).
+  auto drain = [&]() {
+    const int total_jobs = __ldcg(&p.hdr->pad[2]);
+    for (;;) {
+      if (*abort_flag) return;
+      int t = 0;
+      if (lane == 0) t = atomicAdd(&p.hdr->pad[1], 1);
+      t = __shfl_sync(0xffffffffu, t, 0);
+      if (t >= total_jobs) return;
+      int ready = 0;
+      if (lane == 0) {
+        const uint64_t t0 = global_timer_ns();
+        for (;;) {
+          asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(ready) : "l"(&tp.jobs[t].ready) : "memory");
+          if (ready || *abort_flag) break;
+          if (global_timer_ns() - t0 > kWaitLimitNs) {
+            record_error(p.err, PA_ERR_TIMEOUT);
+            *abort_flag = 1;
+            break;
+          }
+          __nanosleep(500);
+        }
+      }
+      if (!__shfl_sync(0xffffffffu, ready, 0)) return;
+      merge_job(t);
+    }
+  };
+
   if (warp < kLoadWarp) {
     // ===================================================== softmax and epilogue (warps 0-3)
     const uint32_t lane_base = (uint32_t)(warp * 32) << 16;
@@ -619,7 +713,10 @@ __device__ __forceinline__ void decode_tc_body(const DecodeTcParams &tp, const C
 #pragma unroll
       for (int h = 0; h < G; ++h) m_prev[h] = m_cur[h];
     }
-    if (ok) hand_over(0, 0, -1);
+    if (ok) {
+      hand_over(0, 0, -1);
+      drain();
+    }
   } else if (warp == kLoadWarp) {
     // ===================================================== loader (one warp)
     // Q^T with cp.async (16-bit caches); every K and V tile with one
@@ -693,6 +790,7 @@ __device__ __forceinline__ void decode_tc_body(const DecodeTcParams &tp, const C
       prev = cur;
     }
     cp_async_wait_all();
+    if (ok) drain();
   } else if (warp == kSchedWarp) {
     // ===================================================== scheduler
     // kClaim units per claim (one atomic step), published in order; the block
@@ -852,6 +950,7 @@ __device__ __forceinline__ void decode_tc_body(const DecodeTcParams &tp, const C
       for (int k = 0; k < kClaim; ++k) mbar_arrive(&info_full[(u + k) % kInfo]);
       if (any_invalid) break;   // the ids only grow: every later claim is past the end too
     }
+    if (ok) drain();
   } else if (warp == kMergeWarp) {
     // ===================================================== merge (last warp)
     // Two duties, polled in turn so that neither waits on the other:
@@ -860,12 +959,8 @@ __device__ __forceinline__ void decode_tc_body(const DecodeTcParams &tp, const C
     //    count that completes a row acquires every partition's results (fence)
     //    and appends the row to the grid-wide merge list (record, then a release
     //    flag);
-    //  * the merge list: out = sum_p 2^(m_p - M) acc_p / sum_p 2^(m_p - M) l_p
-    //    over a split row's partitions p (m_p in log2 units, M their maximum),
-    //    kept as a running maximum; lane l merges elements 4l..4l+3 of all G
-    //    heads, the loads of a partition for every head in flight together.
-    //    Records are claimed in the order they were appended, so every CTA's
-    //    merge warp shares the merging.
+    //  * records of the merge list, claimed in the order they were appended and
+    //    merged (merge_job), so every CTA's merge warp shares the merging.
     // Waiting without progress on either is bounded (PA_ERR_TIMEOUT).
     const int total_jobs = __ldcg(&p.hdr->pad[2]);
     int nrep = 0, t = -1;
@@ -930,65 +1025,9 @@ __device__ __forceinline__ void decode_tc_body(const DecodeTcParams &tp, const C
         }
         continue;
       }
-      int job_row = 0, job_kvh = 0, job_np = 0;
-      if (lane == 0) {   // read by the lane that acquired the record, then broadcast
-        const volatile DecodeMergeJob *jv = tp.jobs + t;
-        job_row = jv->row;
-        job_kvh = jv->kvh;
-        job_np = jv->nparts;
-      }
-      job_row = __shfl_sync(0xffffffffu, job_row, 0);
-      job_kvh = __shfl_sync(0xffffffffu, job_kvh, 0);
-      job_np = __shfl_sync(0xffffffffu, job_np, 0);
+      merge_job(t);
       t = -1;
       t_idle = global_timer_ns();
-      __threadfence();
-      const int64_t head0 = (int64_t)job_row * hq + (int64_t)job_kvh * G;
-      float m[G], l[G];
-      float4 acc[G];
-#pragma unroll
-      for (int h = 0; h < G; ++h) {
-        m[h] = kNegInf;
-        l[h] = 0.f;
-        acc[h] = make_float4(0.f, 0.f, 0.f, 0.f);
-      }
-      // two partitions per step: the loads of both are in flight together
-      for (int q0 = 0; q0 < job_np; q0 += 2) {
-        float2 ml[2][G];
-        float4 a[2][G];
-#pragma unroll
-        for (int k = 0; k < 2; ++k)
-#pragma unroll
-          for (int h = 0; h < G; ++h) {
-            const int q = min(q0 + k, job_np - 1);   // a lone last partition is read twice, merged once
-            const int64_t e = (head0 + h) * p.max_partitions + q;
-            ml[k][h] = __ldcg(&p.ws_ml[e]);
-            a[k][h] = __ldcg(reinterpret_cast<const float4 *>(p.ws_acc + e * kD) + lane);
-          }
-#pragma unroll
-        for (int k = 0; k < 2; ++k) {
-          if (q0 + k >= job_np) break;
-#pragma unroll
-          for (int h = 0; h < G; ++h) {
-            const float mn = fmaxf(m[h], ml[k][h].x);
-            const float so = fast_exp2(m[h] - mn), sn = fast_exp2(ml[k][h].x - mn);
-            m[h] = mn;
-            l[h] = l[h] * so + ml[k][h].y * sn;
-            acc[h] = make_float4(acc[h].x * so + a[k][h].x * sn, acc[h].y * so + a[k][h].y * sn,
-                                 acc[h].z * so + a[k][h].z * sn, acc[h].w * so + a[k][h].w * sn);
-          }
-        }
-      }
-#pragma unroll
-      for (int h = 0; h < G; ++h) {
-        const float om = p.v_hs ? p.out_mult * __ldg(p.v_hs + job_kvh) : p.out_mult;
-        const float inv = l[h] > 0.f ? om / l[h] : 0.f;
-        const int64_t o0 = (head0 + h) * kD + 4 * lane;
-        store_out<QT>(p.out, o0, p.out_f32 != 0, acc[h].x * inv);
-        store_out<QT>(p.out, o0 + 1, p.out_f32 != 0, acc[h].y * inv);
-        store_out<QT>(p.out, o0 + 2, p.out_f32 != 0, acc[h].z * inv);
-        store_out<QT>(p.out, o0 + 3, p.out_f32 != 0, acc[h].w * inv);
-      }
     }
   } else if (warp == kMmaWarp) {
     // ===================================================== MMA issue
@@ -1129,6 +1168,7 @@ __device__ __forceinline__ void decode_tc_body(const DecodeTcParams &tp, const C
       __syncwarp();
       mbar_wait(fin, 0, p.err);
     }
+    if (ok) drain();
   }
 
   // ===================================================== teardown
