@@ -98,9 +98,23 @@ PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
 // 8 rows (256 B apart), 2 panels (128 B apart), atoms (2048 B apart)}; one box
 // is a whole cache block of one KV head (block_size / 8 atoms), landing in
 // shared memory as [atom][panel][8 rows][128 B] with the 128-byte swizzle.
+// A pool of 128-byte rows (16-bit, head_dim 64) is the 3D tensor {64
+// elements, 8 rows, atoms (1024 B apart)}, landing as [atom][8 rows][128 B].
 bool encode_pool_map_atoms(CUtensorMap *map, const void *base, const pa_kv_cache &c) {
   auto enc = tensor_map_encoder();
-  if (!enc || c.head_dim * dtype_bytes(c.kv_dtype) != 256) return false;
+  if (!enc) return false;
+  if (c.kv_dtype != PA_FP8_E4M3 && c.head_dim == 64) {
+    const CUtensorMapDataType dt =
+        c.kv_dtype == PA_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
+    const cuuint64_t dims[3] = {64, 8, (cuuint64_t)c.num_blocks * c.num_kv_heads * c.block_size / 8};
+    const cuuint64_t strides[2] = {128, 1024};
+    const cuuint32_t box[3] = {64, 8, (cuuint32_t)(c.block_size / 8)};
+    const cuuint32_t estr[3] = {1u, 1u, 1u};
+    return enc(map, dt, 3, const_cast<void *>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+               CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+  }
+  if (c.head_dim * dtype_bytes(c.kv_dtype) != 256) return false;
   const CUtensorMapDataType dt = c.kv_dtype == PA_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
   const cuuint64_t dims[4] = {64, 8, 2, (cuuint64_t)c.num_blocks * c.num_kv_heads * c.block_size / 8};
   const cuuint64_t strides[3] = {256, 128, 2048};
@@ -302,7 +316,7 @@ pa_status decode_impl(const void *q, pa_dtype q_dtype, int32_t num_seqs, int32_t
   const int parts = (int)parts64;
   const int gqa = num_q_heads / c.num_kv_heads;
   const bool use_tc = g_decode_kernel.load(std::memory_order_relaxed) == PA_DECODE_KERNEL_AUTO &&
-                      decode_tc_supported(c.head_dim, gqa);
+                      decode_tc_supported(c.head_dim, gqa, c.kv_dtype);
   const int hpc = use_tc ? gqa : heads_per_cta(gqa);   // query heads per work unit
   if ((double)num_seqs * parts * num_q_heads / hpc >= 2147483647.0) return PA_ERR_UNSUPPORTED;
   const WorkspaceLayout w = decode_workspace_layout(num_seqs, num_q_heads, c.head_dim, parts);
@@ -369,10 +383,10 @@ pa_status decode_impl(const void *q, pa_dtype q_dtype, int32_t num_seqs, int32_t
       else e = launch_mixed_tc_fp8_f16q(tp, maps, pt, mix->num_chunks, gqa, s);
       return e == cudaSuccess ? PA_OK : PA_ERR_CUDA;
     }
-    if (c.kv_dtype == PA_BF16) e = launch_decode_tc_bf16(tp, gqa, maps, s);
-    else if (c.kv_dtype == PA_F16) e = launch_decode_tc_f16(tp, gqa, maps, s);
-    else if (q_dtype == PA_BF16) e = launch_decode_tc_fp8_bf16q(tp, gqa, maps, s);
-    else e = launch_decode_tc_fp8_f16q(tp, gqa, maps, s);
+    if (c.kv_dtype == PA_BF16) e = launch_decode_tc_bf16(tp, gqa, c.head_dim, maps, s);
+    else if (c.kv_dtype == PA_F16) e = launch_decode_tc_f16(tp, gqa, c.head_dim, maps, s);
+    else if (q_dtype == PA_BF16) e = launch_decode_tc_fp8_bf16q(tp, gqa, c.head_dim, maps, s);
+    else e = launch_decode_tc_fp8_f16q(tp, gqa, c.head_dim, maps, s);
     return e == cudaSuccess ? PA_OK : PA_ERR_CUDA;
   }
   if (mix) return PA_ERR_INVALID_ARG;   // the caller asks for one launch only where both parts use tensor cores
@@ -579,7 +593,7 @@ pa_status pa_mixed_step(const pa_decode_part *d, const pa_prefill_part *pf, pa_d
   const NewTokens nt{d->k_new, d->v_new, d->token_stride, d->slot_mapping};
   const int gqa = num_q_heads / cache->num_kv_heads;   // num_q_heads checked above
   const bool one_launch = !p_empty && p_tc && d->num_seqs > 0 && mixed_tc_supported(cache->head_dim, gqa) &&
-                          decode_tc_supported(cache->head_dim, gqa) &&
+                          decode_tc_supported(cache->head_dim, gqa, cache->kv_dtype) &&
                           g_decode_kernel.load(std::memory_order_relaxed) == PA_DECODE_KERNEL_AUTO;
   st = decode_impl(d->q, q_dtype, d->num_seqs, num_q_heads, k_cache, v_cache, cache, d->block_tables,
                    d->max_blocks_per_seq, d->seq_lens, d->max_seq_len, scale, d->partition_size, d->workspace,

@@ -1,6 +1,7 @@
 // pa_decode_tc.cuh -- paged decode for grouped-query attention on the
 // 5th-generation tensor cores (tcgen05.mma, accumulators in tensor memory),
-// head_dim 128, G = 4, 8 or 16 query heads per KV head.
+// G = 4, 8 or 16 query heads per KV head with head_dim 128 (any cache dtype),
+// G = 4 or 8 with head_dim 64 (16-bit caches).
 //
 // What it computes: the same as the CUDA-core decode (pa_decode.cuh).  For
 // each sequence and query head h,
@@ -30,7 +31,10 @@
 //   S^T (128 keys x 16)  = K_tile (128 x 128, K-major) . Q^T (K-major: the q rows)
 //   O^T (128 d x N_O)   += V_tile^T (MN-major view of the tile as stored) . P^T
 // S^T lands in tensor memory with lane = key, column = head; O^T with lane =
-// head element d, column = head.  Q rows G..15 are zero.  P^T is staged in
+// head element d, column = head.  Q rows G..15 are zero.  With head_dim 64 a
+// row is one 128-byte panel; O^T keeps M = 128 with both 64-element halves of
+// its A operand read from that one panel, so lanes 64..127 repeat lanes 0..63
+// and are ignored.  P^T is staged in
 // shared memory (K-major, lane = key writes its column): columns 0..G-1 hold
 // p (its bf16 hi part for a bf16 cache) and, for a bf16 cache, columns
 // G..2G-1 hold the lo part p - hi, so one MMA per 16 keys accumulates both
@@ -162,20 +166,23 @@ struct QTerms {
 // with 128-byte swizzle writes), Q^T and P^T of one 128-element panel
 // holding the hi terms in rows 0..G-1, the lo terms in rows G..2G-1 (and
 // with three query terms, the last in rows 2G..3G-1 of Q^T).
-template <int G, bool kSplit, bool kFp8, int kQTerms = 1>
+template <int G, bool kSplit, bool kFp8, int kQTerms = 1, int D = 128>
 struct TcGeo {
   static_assert(G == 4 || G == 8 || G == 16, "4, 8 or 16 query heads per KV head");
+  static_assert(D == 128 || (D == 64 && !kFp8), "head_dim 128, or 64 with a 16-bit cache");
+  static constexpr int kPanels = D / 64;                            // 128-byte panels of a 16-bit row
+  static constexpr int kAtom = 8 * 2 * D;                           // 8 keys of a 16-bit tile (all panels)
   static constexpr int kPRows = (kSplit || kFp8) ? 2 * G : G;       // P^T rows in use
   static constexpr int kNO = kPRows <= 16 ? 16 : 32;                // O^T columns (MMA N)
   static constexpr int kQRows = kQTerms * G;                        // Q^T rows in use
   static constexpr int kNS = kQRows <= 16 ? 16 : (kQRows + 15) / 16 * 16;   // S^T columns per tile (MMA N)
   static constexpr int kSCols = kFp8 ? kNS : G;                     // S^T columns read per tile
-  static constexpr int kQBytes = kFp8 ? kNS * 128 : 2 * kNS * 128;  // Q^T of a unit
+  static constexpr int kQBytes = kFp8 ? kNS * 128 : kPanels * kNS * 128;  // Q^T of a unit
   // Q^T buffers: fp8, one per unit descriptor (written by the scheduler warp
   // with the descriptor); 16-bit, two (copied by the loader per unit parity)
   static constexpr int kQBufs = kFp8 ? kInfo : 2;
   static constexpr int kPBytes = kFp8 ? kNO * 128 : 2 * kNO * 128;  // P^T of a tile
-  static constexpr int kSlotBytes = kFp8 ? kKeys * kD : kKeys * kD * 2;   // one K or V tile
+  static constexpr int kSlotBytes = kFp8 ? kKeys * D : kKeys * D * 2;     // one K or V tile
   static constexpr int kColO = 2 * kMaxTiles * kNS;                 // tensor-memory column of O^T, buffer 0
   static constexpr int kTmemCols = kColO + 2 * kNO <= 256 ? 256 : 512;
   static constexpr int kNumBars = 2 * kMaxSlots + 8 * 2 + 2 * kInfo + 1 + 2 * kRep;
@@ -312,11 +319,12 @@ __device__ __forceinline__ int32_t query_scale_bits(float amax) {
 // The decode CTA, for decode_tc_kernel and for the decode CTAs of the mixed
 // kernel (pa_mixed_tc.cuh).  Warps past the eight roles (a wider mixed block)
 // only take part in the two CTA-wide barriers.
-template <typename KV, typename QT, int G>
+template <typename KV, typename QT, int G, int D = 128>
 __device__ __forceinline__ void decode_tc_body(const DecodeTcParams &tp, const CUtensorMap *tmap_k,
                                                const CUtensorMap *tmap_v) {
   using namespace tc;
   using namespace dtc;
+  constexpr int kD = D;                       // head_dim (hides dtc::kD)
   constexpr bool kFp8 = std::is_same<KV, uint8_t>::value;
   constexpr int kLoadWarp = Roles::kLoadWarp, kMmaWarp = Roles::kMmaWarp;
   constexpr int kSchedWarp = Roles::kSchedWarp, kMergeWarp = Roles::kMergeWarp, kThreads = Roles::kThreads;
@@ -325,7 +333,9 @@ __device__ __forceinline__ void decode_tc_body(const DecodeTcParams &tp, const C
   constexpr bool kBf16 = std::is_same<QT, __nv_bfloat16>::value && !kFp8;
   constexpr bool kSplit = kBf16;            // bf16 cache: P as hi + lo
   constexpr int kQTerms = QTerms<KV, QT>::value;
-  using GE = TcGeo<G, kSplit, kFp8, kQTerms>;
+  using GE = TcGeo<G, kSplit, kFp8, kQTerms, D>;
+  constexpr int kAtomB = GE::kAtom;           // bytes of 8 keys of a 16-bit tile
+  constexpr int kRowChunks = kD * 2 / 16;     // 16-byte chunks of a 16-bit row
   constexpr int S = GE::kSlots, kNO = GE::kNO, kNS = GE::kNS;
   constexpr uint32_t kAB = kBf16 ? 1u : 0u;   // instruction-descriptor format: bf16 1, f16 0, e4m3 0
   const DecodeParams &p = tp.d;
@@ -451,7 +461,8 @@ __device__ __forceinline__ void decode_tc_body(const DecodeTcParams &tp, const C
           const int q = min(q0 + k, job_np - 1);   // a lone last partition is read twice, merged once
           const int64_t e = (head0 + h) * p.max_partitions + q;
           ml[k][h] = __ldcg(&p.ws_ml[e]);
-          a[k][h] = __ldcg(reinterpret_cast<const float4 *>(p.ws_acc + e * kD) + lane);
+          a[k][h] = 4 * lane < kD ? __ldcg(reinterpret_cast<const float4 *>(p.ws_acc + e * kD) + lane)
+                                  : make_float4(0.f, 0.f, 0.f, 0.f);
         }
 #pragma unroll
       for (int k = 0; k < 2; ++k) {
@@ -472,6 +483,7 @@ __device__ __forceinline__ void decode_tc_body(const DecodeTcParams &tp, const C
       const float om = p.v_hs ? p.out_mult * __ldg(p.v_hs + job_kvh) : p.out_mult;
       const float inv = l[h] > 0.f ? om / l[h] : 0.f;
       const int64_t o0 = (head0 + h) * kD + 4 * lane;
+      if (4 * lane >= kD) continue;   // head_dim 64: lanes 0..15
       store_out<QT>(p.out, o0, p.out_f32 != 0, acc[h].x * inv);
       store_out<QT>(p.out, o0 + 1, p.out_f32 != 0, acc[h].y * inv);
       store_out<QT>(p.out, o0 + 2, p.out_f32 != 0, acc[h].z * inv);
@@ -674,7 +686,7 @@ __device__ __forceinline__ void decode_tc_body(const DecodeTcParams &tp, const C
         tc_fence_before();
         mbar_arrive(&o_free[bp]);
         const int64_t head0 = (int64_t)prev.row * hq + (int64_t)prev.kvh * G;
-        const int d = tid;
+        const int d = tid;            // with head_dim 64, lanes 64..127 repeat 0..63: not stored
         // the two column halves of O^T: bf16 p = hi + lo; fp8 256 p = hi + lo / 16
         auto o_val = [&](int h) {
           return kSplit ? o[h] + o[G + h] : kFp8 ? fmaf(o[G + h], 0.0625f, o[h]) * (1.f / 256.f) : o[h];
@@ -685,12 +697,12 @@ __device__ __forceinline__ void decode_tc_body(const DecodeTcParams &tp, const C
             const float val = o_val(h);
             const float om = p.v_hs ? p.out_mult * __ldg(p.v_hs + prev.kvh) : p.out_mult;
             const float inv = l_prev[h] > 0.f ? om / l_prev[h] : 0.f;
-            store_out<QT>(p.out, (head0 + h) * kD + d, p.out_f32 != 0, val * inv);
+            if (d < kD) store_out<QT>(p.out, (head0 + h) * kD + d, p.out_f32 != 0, val * inv);
           }
         } else {
 #pragma unroll
           for (int h = 0; h < G; ++h)
-            p.ws_acc[((head0 + h) * p.max_partitions + prev.part) * kD + d] = o_val(h);
+            if (d < kD) p.ws_acc[((head0 + h) * p.max_partitions + prev.part) * kD + d] = o_val(h);
           if (tid < G) {
             float mv = m_prev[0], lv = l_prev[0];
 #pragma unroll
@@ -721,11 +733,53 @@ __device__ __forceinline__ void decode_tc_body(const DecodeTcParams &tp, const C
     // ===================================================== loader (one warp)
     // Q^T with cp.async (16-bit caches); every K and V tile with one
     // bulk-tensor box per cache block holding keys of the unit (tiles start on
-    // block boundaries), straight into the ring in the MMA's layout: 16-bit
+    // block boundaries), straight into a ring slot in the MMA's layout: 16-bit
     // caches bs / 8 atoms per box, fp8 bs rows of 128 codes per box.
     const int bs = p.block_size;
-    uint32_t g_load = 0;
     bool ok = true;
+    auto issue_tile = [&](const UnitHdr &un, int info_idx, int j, bool is_k, int slot) {
+      uint64_t *full_bar = &slot_full[slot];
+      const int nvalid = min(kKeys, un.ntok - j * kKeys);
+      bool issue = false;
+      int32_t bi = 0;
+      if (lane < (nvalid + bs - 1) / bs) {
+        bi = reinterpret_cast<const volatile int32_t *>(info[info_idx].blk)[8 * j + lane * (bs >> 4)];
+        issue = bi >= 0;   // an out-of-range id was reported by the scheduler; its keys stay unread
+      }
+      const uint32_t boxes = __popc(__ballot_sync(0xffffffffu, issue));
+      const CUtensorMap *map = is_k ? tmap_k : tmap_v;
+      if constexpr (!kFp8) {
+        const int atoms = bs >> 3;
+        if (lane == 0) mbar_arrive_expect_tx(full_bar, boxes * atoms * kAtomB);
+        __syncwarp();
+        if (issue) {
+          uint8_t *dst = smem + GE::kOffRing + slot * GE::kSlotBytes + lane * atoms * kAtomB;
+          if constexpr (kD == 128) tma_load_4d(dst, map, full_bar, 0, 0, 0, (bi * hkv + un.kvh) * atoms);
+          else tma_load_3d(dst, map, full_bar, 0, 0, (bi * hkv + un.kvh) * atoms);
+        }
+      } else {
+        if (lane == 0) mbar_arrive_expect_tx(full_bar, boxes * bs * kD);
+        __syncwarp();
+        if (issue)
+          tma_load_2d(smem + GE::kOffRing + slot * GE::kSlotBytes + lane * bs * kD, map, full_bar, 0,
+                      (bi * hkv + un.kvh) * bs);
+      }
+    };
+    // Q^T rows of a unit (16-bit caches): the G query heads of the KV head, 2 * kD bytes each
+    auto load_q = [&](const UnitHdr &cur, int b) {
+#pragma unroll
+      for (int e = lane; e < G * kRowChunks; e += 32) {
+        const int h = e / kRowChunks, c16 = e % kRowChunks;
+        const char *src = static_cast<const char *>(p.q) +
+                          (((int64_t)cur.row * hq + (int64_t)cur.kvh * G + h) * kD) * 2 + c16 * 16;
+        cp_async16(smem + GE::kOffQ + b * GE::kQBytes + (c16 >> 3) * (kNS * 128) + h * 128 +
+                       (((c16 & 7) ^ (h & 7)) << 4),
+                   src, 16u);
+      }
+      cp_async_arrive_noinc(&q_full[b]);
+    };
+    // one ring, tiles in the MMAs' order: K tiles of unit u, then V tiles of unit u-1
+    uint32_t g_load = 0;
     UnitHdr prev;
     prev.valid = 0;
     for (int u = 0; ok; ++u) {
@@ -735,55 +789,18 @@ __device__ __forceinline__ void decode_tc_body(const DecodeTcParams &tp, const C
       const UnitHdr cur = read_unit(&info[ib]);
       const int ntc = num_tiles(cur), ntp = num_tiles(prev);
       if (!kFp8 && cur.valid) {
-        // Q^T rows: the G query heads of the KV head, 256 B each
         if (u >= 2) {
           ok = wait_all(&q_free[b], ((u >> 1) - 1) & 1);
           if (!ok) break;
         }
-#pragma unroll
-        for (int e = lane; e < G * 16; e += 32) {
-          const int h = e >> 4, c16 = e & 15;
-          const char *src = static_cast<const char *>(p.q) +
-                            (((int64_t)cur.row * hq + (int64_t)cur.kvh * G + h) * kD) * 2 + c16 * 16;
-          cp_async16(smem + GE::kOffQ + b * GE::kQBytes + (c16 >> 3) * (kNS * 128) + h * 128 +
-                         (((c16 & 7) ^ (h & 7)) << 4),
-                     src, 16u);
-        }
-        cp_async_arrive_noinc(&q_full[b]);
+        load_q(cur, b);
       }
-      // tiles in the MMA's order: K tiles of this unit, then V tiles of the previous one
       for (int i = 0; i < ntc + ntp && ok; ++i) {
         const bool is_k = i < ntc;
-        const UnitHdr &un = is_k ? cur : prev;
-        const int j = is_k ? i : i - ntc;
         const int slot = (int)(g_load % S);
-        uint64_t *free_bar = &slot_free[slot];
-        uint64_t *full_bar = &slot_full[slot];
-        if (g_load >= (uint32_t)S) ok = wait_all(free_bar, ((g_load / S) - 1) & 1);
+        if (g_load >= (uint32_t)S) ok = wait_all(&slot_free[slot], ((g_load / S) - 1) & 1);
         if (!ok) break;
-        const int nvalid = min(kKeys, un.ntok - j * kKeys);
-        bool issue = false;
-        int32_t bi = 0;
-        if (lane < (nvalid + bs - 1) / bs) {
-          bi = reinterpret_cast<const volatile int32_t *>(info[is_k ? ib : ibp].blk)[8 * j + lane * (bs >> 4)];
-          issue = bi >= 0;   // an out-of-range id was reported by the scheduler; its keys stay unread
-        }
-        const uint32_t boxes = __popc(__ballot_sync(0xffffffffu, issue));
-        const CUtensorMap *map = is_k ? tmap_k : tmap_v;
-        if constexpr (!kFp8) {
-          const int atoms = bs >> 3;
-          if (lane == 0) mbar_arrive_expect_tx(full_bar, boxes * atoms * kAtomBytes);
-          __syncwarp();
-          if (issue)
-            tma_load_4d(smem + GE::kOffRing + slot * GE::kSlotBytes + lane * atoms * kAtomBytes, map, full_bar, 0, 0,
-                        0, (bi * hkv + un.kvh) * atoms);
-        } else {
-          if (lane == 0) mbar_arrive_expect_tx(full_bar, boxes * bs * kD);
-          __syncwarp();
-          if (issue)
-            tma_load_2d(smem + GE::kOffRing + slot * GE::kSlotBytes + lane * bs * kD, map, full_bar, 0,
-                        (bi * hkv + un.kvh) * bs);
-        }
+        issue_tile(is_k ? cur : prev, is_k ? ib : ibp, is_k ? i : i - ntc, is_k, slot);
         ++g_load;
       }
       if (!cur.valid) break;
@@ -808,8 +825,9 @@ __device__ __forceinline__ void decode_tc_body(const DecodeTcParams &tp, const C
     auto store_new = [&](uint4 x, float sc, int64_t crow) {
       const int side = lane >> 4, c = lane & 15;
       if constexpr (!kFp8) {
-        *reinterpret_cast<uint4 *>(static_cast<QT *>(const_cast<void *>(side ? tp.v_cache : tp.k_cache)) + crow * kD +
-                                   c * 8) = x;
+        if (c < kD / 8)   // head_dim 64: 8 chunks per row
+          *reinterpret_cast<uint4 *>(static_cast<QT *>(const_cast<void *>(side ? tp.v_cache : tp.k_cache)) +
+                                     crow * kD + c * 8) = x;
       } else {
         const uint32_t w[4] = {x.x, x.y, x.z, x.w};
         uint32_t o[2];
@@ -865,9 +883,10 @@ __device__ __forceinline__ void decode_tc_body(const DecodeTcParams &tp, const C
         if (wr) {
           const int side = lane >> 4;
           new_slot = __ldg(tp.new_slots + rk);
-          new_x = __ldg(reinterpret_cast<const uint4 *>(static_cast<const QT *>(side ? tp.v_new : tp.k_new) +
-                                                        (int64_t)rk * tp.new_stride + (int64_t)kvk * kD +
-                                                        (lane & 15) * 8));
+          if ((lane & 15) < kD / 8)
+            new_x = __ldg(reinterpret_cast<const uint4 *>(static_cast<const QT *>(side ? tp.v_new : tp.k_new) +
+                                                          (int64_t)rk * tp.new_stride + (int64_t)kvk * kD +
+                                                          (lane & 15) * 8));
           if (kFp8) new_sc = p.k_hs ? __ldg((side ? p.v_hs : p.k_hs) + kvk) : side ? tp.v_scale : tp.k_scale;
         }
         int32_t qscale = 0;
@@ -1044,7 +1063,7 @@ __device__ __forceinline__ void decode_tc_body(const DecodeTcParams &tp, const C
     const uint32_t ring = smem_u32(smem + GE::kOffRing);
     const uint32_t qbuf = smem_u32(smem + GE::kOffQ);
     const uint32_t pbuf = smem_u32(smem + GE::kOffP);
-    uint32_t g_cons = 0;
+    uint32_t g_cons = 0;   // tiles consumed, in the ring's order
     bool ok = true, issued = false;
     UnitHdr prev;
     prev.valid = 0;
@@ -1080,7 +1099,7 @@ __device__ __forceinline__ void decode_tc_body(const DecodeTcParams &tp, const C
             } else {
 #pragma unroll
               for (int k = 0; k < kD / 16; ++k)
-                mma(col_s(b, j), umma_desc_sbo(kb + (k >> 2) * 1024 + (k & 3) * 32, 16, kAtomBytes),
+                mma(col_s(b, j), umma_desc_sbo(kb + (k >> 2) * 1024 + (k & 3) * 32, 16, kAtomB),
                     umma_desc(qb + (k >> 2) * (kNS * 128) + (k & 3) * 32, 16), idesc_s, k > 0 ? 1u : 0u);
             }
             umma_commit(&slot_free[slot]);
@@ -1123,9 +1142,9 @@ __device__ __forceinline__ void decode_tc_body(const DecodeTcParams &tp, const C
               for (int e = lane; e < (kGroup * ngroups - nvalid) * 8; e += 32)   // rows of 128 B
                 *reinterpret_cast<uint4 *>(vt + (nvalid + (e >> 3)) * 128 + (e & 7) * 16) = make_uint4(0, 0, 0, 0);
             } else {
-              for (int e = lane; e < (kGroup * ngroups - nvalid) * 16; e += 32) {
-                const int r = nvalid + (e >> 4), c = e & 15;   // row, 16-byte chunk of its 256 B
-                *reinterpret_cast<uint4 *>(vt + (r >> 3) * kAtomBytes + (c >> 3) * 1024 + (r & 7) * 128 +
+              for (int e = lane; e < (kGroup * ngroups - nvalid) * kRowChunks; e += 32) {
+                const int r = nvalid + e / kRowChunks, c = e % kRowChunks;   // row, 16-byte chunk of it
+                *reinterpret_cast<uint4 *>(vt + (r >> 3) * kAtomB + (c >> 3) * 1024 + (r & 7) * 128 +
                                            (c & 7) * 16) = make_uint4(0, 0, 0, 0);
               }
             }
@@ -1141,8 +1160,10 @@ __device__ __forceinline__ void decode_tc_body(const DecodeTcParams &tp, const C
                 mma(col_o(bp), umma_desc_sbo(vb + kk * 4096, 1024, 1024), umma_desc(pb + kk * 32, 16), idesc_o,
                     (j > 0 || kk > 0) ? 1u : 0u);
             } else {
+              // M = 128 elements of V^T in two 64-element halves (LBO apart): panels 0 and 1,
+              // or panel 0 twice with head_dim 64 (lanes 64..127 of O^T then repeat 0..63)
               for (int kk = 0; kk < ngroups; ++kk)
-                mma(col_o(bp), umma_desc_sbo(vb + kk * 2 * kAtomBytes, 1024, kAtomBytes),
+                mma(col_o(bp), umma_desc_sbo(vb + kk * 2 * kAtomB, kD == 128 ? 1024 : 0, kAtomB),
                     umma_desc(pb + (kk >> 2) * (kNO * 128) + (kk & 3) * 32, 16), idesc_o,
                     (j > 0 || kk > 0) ? 1u : 0u);
             }
@@ -1180,11 +1201,11 @@ __device__ __forceinline__ void decode_tc_body(const DecodeTcParams &tp, const C
   }
 }
 
-template <typename KV, typename QT, int G>
+template <typename KV, typename QT, int G, int D>
 __global__ void __launch_bounds__(dtc::Roles::kThreads, 1)
     decode_tc_kernel(const DecodeTcParams tp, const __grid_constant__ CUtensorMap tmap_k,
                      const __grid_constant__ CUtensorMap tmap_v) {
-  decode_tc_body<KV, QT, G>(tp, &tmap_k, &tmap_v);
+  decode_tc_body<KV, QT, G, D>(tp, &tmap_k, &tmap_v);
 }
 
 // One CTA: count the split rows' merges and clear the merge list, and list
@@ -1244,15 +1265,15 @@ __global__ void __launch_bounds__(1024) decode_tc_plan_kernel(DecodeParams p, De
 
 // Host launcher: the plan kernel, then one persistent CTA per SM launched as its
 // programmatic dependent.
-template <typename KV, typename QT, int G>
+template <typename KV, typename QT, int G, int D>
 cudaError_t launch_decode_tc_one(const DecodeTcParams &p, const PoolMaps &m, cudaStream_t s) {
   constexpr bool kSplit = std::is_same<QT, __nv_bfloat16>::value && !std::is_same<KV, uint8_t>::value;
   constexpr int smem =
-      dtc::TcGeo<G, kSplit, std::is_same<KV, uint8_t>::value, dtc::QTerms<KV, QT>::value>::kSmemBytes;
+      dtc::TcGeo<G, kSplit, std::is_same<KV, uint8_t>::value, dtc::QTerms<KV, QT>::value, D>::kSmemBytes;
   decode_tc_plan_kernel<0><<<1, 1024, 0, s>>>(p.d, p.jobs);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
-  if ((e = ensure_smem_limit<decode_tc_kernel<KV, QT, G>>(smem)) != cudaSuccess) return e;
+  if ((e = ensure_smem_limit<decode_tc_kernel<KV, QT, G, D>>(smem)) != cudaSuccess) return e;
   int sms = 0;
   if ((e = current_sm_count(&sms)) != cudaSuccess) return e;
   // programmatic dependent launch: the decode grid's set-up overlaps the plan kernel
@@ -1266,18 +1287,23 @@ cudaError_t launch_decode_tc_one(const DecodeTcParams &p, const PoolMaps &m, cud
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, decode_tc_kernel<KV, QT, G>, p, m.k, m.v);
+  return cudaLaunchKernelEx(&cfg, decode_tc_kernel<KV, QT, G, D>, p, m.k, m.v);
 }
 
 // m: tensor maps over the pools, one box per cache block of one KV head: 16-bit
-// caches viewed as [atoms of 8 rows][2 panels][8 rows][64], fp8 caches as [rows][128]
+// caches viewed as [atoms of 8 rows][2 panels][8 rows][64] (head_dim 128) or
+// [atoms of 8 rows][8 rows][64] (head_dim 64), fp8 caches as [rows][128]
 // (128-byte swizzle).
 template <typename KV, typename QT>
-cudaError_t launch_decode_tc(const DecodeTcParams &p, int gqa, const PoolMaps &m, cudaStream_t s) {
+cudaError_t launch_decode_tc(const DecodeTcParams &p, int gqa, int head_dim, const PoolMaps &m, cudaStream_t s) {
+  if constexpr (!std::is_same<KV, uint8_t>::value) {
+    if (head_dim == 64) return gqa == 8 ? launch_decode_tc_one<KV, QT, 8, 64>(p, m, s) : cudaErrorInvalidValue;
+  }
+  if (head_dim != 128) return cudaErrorInvalidValue;
   switch (gqa) {
-    case 4: return launch_decode_tc_one<KV, QT, 4>(p, m, s);
-    case 8: return launch_decode_tc_one<KV, QT, 8>(p, m, s);
-    case 16: return launch_decode_tc_one<KV, QT, 16>(p, m, s);
+    case 4: return launch_decode_tc_one<KV, QT, 4, 128>(p, m, s);
+    case 8: return launch_decode_tc_one<KV, QT, 8, 128>(p, m, s);
+    case 16: return launch_decode_tc_one<KV, QT, 16, 128>(p, m, s);
     default: return cudaErrorInvalidValue;
   }
 }

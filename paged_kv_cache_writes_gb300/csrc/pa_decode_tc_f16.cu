@@ -2,7 +2,8 @@
 #include "pa_decode_tc.cuh"
 
 namespace pa {
-cudaError_t launch_decode_tc_f16(const DecodeTcParams &p, int gqa, const PoolMaps &m, cudaStream_t s) {
-  return launch_decode_tc<__half, __half>(p, gqa, m, s);
+cudaError_t launch_decode_tc_f16(const DecodeTcParams &p, int gqa, int head_dim, const PoolMaps &m,
+                                 cudaStream_t s) {
+  return launch_decode_tc<__half, __half>(p, gqa, head_dim, m, s);
 }
 }  // namespace pa

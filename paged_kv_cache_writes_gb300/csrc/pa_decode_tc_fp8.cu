@@ -3,10 +3,12 @@
 #include "pa_decode_tc.cuh"
 
 namespace pa {
-cudaError_t launch_decode_tc_fp8_bf16q(const DecodeTcParams &p, int gqa, const PoolMaps &m, cudaStream_t s) {
-  return launch_decode_tc<uint8_t, __nv_bfloat16>(p, gqa, m, s);
+cudaError_t launch_decode_tc_fp8_bf16q(const DecodeTcParams &p, int gqa, int head_dim, const PoolMaps &m,
+                                       cudaStream_t s) {
+  return launch_decode_tc<uint8_t, __nv_bfloat16>(p, gqa, head_dim, m, s);
 }
-cudaError_t launch_decode_tc_fp8_f16q(const DecodeTcParams &p, int gqa, const PoolMaps &m, cudaStream_t s) {
-  return launch_decode_tc<uint8_t, __half>(p, gqa, m, s);
+cudaError_t launch_decode_tc_fp8_f16q(const DecodeTcParams &p, int gqa, int head_dim, const PoolMaps &m,
+                                      cudaStream_t s) {
+  return launch_decode_tc<uint8_t, __half>(p, gqa, head_dim, m, s);
 }
 }  // namespace pa

@@ -1,9 +1,9 @@
 """GPU parity of paged decode against the fp64 oracle, element by element.
 
-Two kernels serve pa_decode: the tensor-core one (head_dim 128 with 4, 8 or
-16 query heads per KV head, chosen by default) and the CUDA-core one (every
-other shape, or every shape once selected with pa_set_decode_kernel); both
-are checked here.
+Two kernels serve pa_decode: the tensor-core one (chosen by default for
+head_dim 128 with 4, 8 or 16 query heads per KV head, and for head_dim 64
+with a 16-bit cache and 8) and the CUDA-core one (every other shape, or
+every shape once selected with pa_set_decode_kernel); both are checked here.
 
 Tolerance (max abs error): 2e-3 for f16/bf16 caches, 2e-2 for an fp8-e4m3
 cache (the oracle dequantises the same codes with the same scales).  Shapes
@@ -121,6 +121,20 @@ def test_workspace_contents_ignored_and_reusable():
         dev.decode()
         torch.cuda.synchronize()
         assert torch.equal(dev.out.view(torch.int32), first.view(torch.int32))
+
+
+@pytest.mark.parametrize("kv", ["bf16", "f16"])
+@pytest.mark.parametrize("hq,hkv", [(64, 8), (128, 16)])
+def test_head_dim_64_batch_both_kernels(kv, hq, hkv):
+    # a bandwidth-sized head_dim-64 batch (128 sequences of 512..4096 tokens): the tensor-core
+    # kernel against the oracle in full, and against the CUDA-core kernel
+    lens = np.random.default_rng(101).integers(512, 4097, size=128)
+    b = W.decode_batch("d64", lens, hq, hkv, 64, 16, kv, seed=5, partition_size=512)
+    tc, _ = _check(b)
+    tc_out = tc.out.clone()
+    with pa.decode_kernel("cuda_cores"):
+        cc, _ = _check(b)
+    assert (tc_out - cc.out).abs().max().item() <= 2 * TOL[kv]
 
 
 def test_llama8b_full():

@@ -43,6 +43,14 @@ def test_fused_step_matches_write_then_decode(kernel, kv, src, hq, hkv, bs):
     _fused(b, kernel)
 
 
+@pytest.mark.parametrize("kernel", ["auto", "cuda_cores"])
+@pytest.mark.parametrize("kv", ["bf16", "f16"])
+@pytest.mark.parametrize("hq,hkv,bs", [(32, 8, 16), (16, 2, 32)])
+def test_fused_step_head_dim_64(kernel, kv, hq, hkv, bs):
+    b = W.decode_batch("fused d64", LENS, hq, hkv, 64, bs, kv, seed=hq + hkv + bs + 64, partition_size=512)
+    _fused(b, kernel)
+
+
 @pytest.mark.parametrize("ps", [32, 96, 0])
 def test_fused_step_partition_sizes(ps):
     b = W.decode_batch("fused ps", [1, 40, 700, 2049, 3000], 16, 2, 128, 16, "bf16", seed=51, partition_size=ps)
