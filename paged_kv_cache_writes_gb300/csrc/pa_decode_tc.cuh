@@ -76,7 +76,7 @@
 //  * MMA warp (one elected lane issues): S^T of unit u, then O^T of unit
 //    u-1, whose softmax ran while the scores of u were computed;
 //  * scheduler warp: claims units two at a time and publishes each, with
-//    the block ids of its tiles, in a ring of four descriptors, so the chain
+//    the block ids of its tiles, in a ring of six descriptors, so the chain
 //    of dependent reads behind a claim (cursor, work item, sequence length,
 //    block table) runs ahead of the loads instead of between them.  It also
 //    stores a fused step's new token (pa_decode_write) before publishing the
@@ -128,7 +128,7 @@ namespace dtc {
 constexpr int kD = 128;                   // head_dim
 constexpr int kKeys = 128;                // keys per tile (MMA M, tensor-memory lanes)
 constexpr int kMaxTiles = 4;              // tiles per unit: partitions hold <= 512 tokens
-constexpr int kInfo = 4;                  // unit descriptors in flight (bounds how far a CTA claims ahead)
+constexpr int kInfo = 6;                  // unit descriptors in flight (bounds how far a CTA claims ahead)
 constexpr int kClaim = 2;                 // units per claim (a power of two)
 constexpr int kRep = 8;                   // split units handed from the softmax warps to the merge warp
 // A 16-bit K or V tile in shared memory: 16 atoms of 8 keys, atom a at
