@@ -63,16 +63,16 @@
 // claimed from an atomic cursor by a persistent CTA per SM.  Roles:
 //  * warps 0-3, softmax and epilogue: thread i owns tensor-memory lane i (key
 //    i of a score tile, element d = i of an output row);
-//  * two loader warps: one stages Q^T (16-bit caches, cp.async) and the
-//    unit's K tiles, the other the previous unit's V tiles, each tile with
-//    one bulk-tensor copy per cache block straight into a ring of tiles in
-//    the MMA's 128-byte-swizzled layout (32 KB for a 16-bit cache, 16 KB for
-//    fp8), at its place in the ring's order (K tiles of unit u, then V tiles
-//    of unit u-1).  One warp issuing the copies of 4 KB blocks one after
-//    another streamed at most ~21 bytes per SM clock; two warps reach the
-//    memory's rate.  With 16 query heads per KV head one warp loads both
-//    (a ninth warp would cap the softmax threads' registers below their
-//    needs);
+//  * loader warps (NL of them): the ring's tiles, in the MMAs' order (K
+//    tiles of unit u, then V tiles of unit u-1), go to the loaders in turn by
+//    ring position; each tile is one bulk-tensor copy per cache block
+//    straight into its slot in the MMA's 128-byte-swizzled layout (32 KB for
+//    a 16-bit cache, 16 KB for fp8).  Loader 0 also stages Q^T (16-bit
+//    caches, cp.async).  One warp issuing the copies of 4 KB blocks one
+//    after another streamed at most ~21 bytes per SM clock, so the decode
+//    launch has four loaders (two in the mixed launch, whose block has nine
+//    warps; one with 16 query heads per KV head, whose softmax needs more
+//    registers than nine or more warps leave);
 //  * MMA warp (one elected lane issues): S^T of unit u, then O^T of unit
 //    u-1, whose softmax ran while the scores of u were computed;
 //  * scheduler warp: claims units two at a time and publishes each, with
@@ -140,16 +140,16 @@ constexpr int kAtomBytes = 2048;          // 8 keys x 256 B: the two 128-byte pa
 // Warp roles: 0-3 softmax, 4 the loader (bulk-tensor copies and Q), 5 the
 // MMA warp, 6 the scheduler, 7 the merge warp.
 struct Roles {
-  static constexpr int kLoadWarp = 4;    // Q^T and K tiles (and V tiles without a V loader)
+  static constexpr int kLoadWarp = 4;    // loader 0 (also stages Q^T)
   static constexpr int kMmaWarp = 5;
   static constexpr int kSchedWarp = 6;
   static constexpr int kMergeWarp = 7;
-  static constexpr int kLoadVWarp = 8;   // V tiles
-  static constexpr int kThreads = (kLoadVWarp + 1) * 32;
-  // nine warps leave 168 registers per thread (three warps on one of the SM's
-  // four register files), too few for the softmax of 16 heads
-  static constexpr bool two_loaders(int g) { return g <= 8; }
-  static constexpr int threads(int g) { return two_loaders(g) ? kThreads : kLoadVWarp * 32; }
+  static constexpr int kLoadWarp1 = 8;   // loaders 1 .. NL-1
+  // Loader warps of the decode launch: nine to twelve warps leave 168
+  // registers per thread (three warps on one of the SM's four register
+  // files), too few for the softmax of 16 heads, which keeps one loader.
+  static constexpr int loaders(int g) { return g <= 8 ? 4 : 1; }
+  static constexpr int threads_for(int nl) { return (nl > 1 ? kLoadWarp1 + nl - 1 : kLoadWarp1) * 32; }
 };
 
 constexpr int kMaxSlots = 12;
@@ -330,7 +330,7 @@ __device__ __forceinline__ int32_t query_scale_bits(float amax) {
 // The decode CTA, for decode_tc_kernel and for the decode CTAs of the mixed
 // kernel (pa_mixed_tc.cuh).  Warps past the eight roles (a wider mixed block)
 // only take part in the two CTA-wide barriers.
-template <typename KV, typename QT, int G, int D = 128>
+template <typename KV, typename QT, int G, int D = 128, int NL = 1>
 __device__ __forceinline__ void decode_tc_body(const DecodeTcParams &tp, const CUtensorMap *tmap_k,
                                                const CUtensorMap *tmap_v) {
   using namespace tc;
@@ -339,8 +339,7 @@ __device__ __forceinline__ void decode_tc_body(const DecodeTcParams &tp, const C
   constexpr bool kFp8 = std::is_same<KV, uint8_t>::value;
   constexpr int kLoadWarp = Roles::kLoadWarp, kMmaWarp = Roles::kMmaWarp;
   constexpr int kSchedWarp = Roles::kSchedWarp, kMergeWarp = Roles::kMergeWarp;
-  constexpr int kThreads = Roles::threads(G), kLoadVWarp = Roles::kLoadVWarp;
-  constexpr bool kTwoLoaders = Roles::two_loaders(G);
+  constexpr int kThreads = Roles::threads_for(NL), kLoadWarp1 = Roles::kLoadWarp1;
   // MMA operands: the cache's type (bf16 / f16 with a 16-bit cache, the queries
   // in the same type; e4m3 with an fp8 cache, the queries and P as two e4m3 terms)
   constexpr bool kBf16 = std::is_same<QT, __nv_bfloat16>::value && !kFp8;
@@ -742,7 +741,7 @@ __device__ __forceinline__ void decode_tc_body(const DecodeTcParams &tp, const C
       hand_over(0, 0, -1);
       drain();
     }
-  } else if (warp == kLoadWarp || warp == kLoadVWarp) {
+  } else if (warp == kLoadWarp || (warp >= kLoadWarp1 && warp < kLoadWarp1 + NL - 1)) {
     // ===================================================== loaders (two warps)
     // Q^T with cp.async (16-bit caches); every K and V tile with one
     // bulk-tensor box per cache block holding keys of the unit (tiles start on
@@ -751,7 +750,7 @@ __device__ __forceinline__ void decode_tc_body(const DecodeTcParams &tp, const C
     // warp and the V warp walk the same units and ring positions, each
     // filling its own tiles' slots.
     const int bs = p.block_size;
-    const bool k_side = warp == kLoadWarp;
+    const int ldr = warp == kLoadWarp ? 0 : warp - kLoadWarp1 + 1;   // this warp's share: positions = ldr mod NL
     bool ok = true;
     auto issue_tile = [&](const UnitHdr &un, int info_idx, int j, bool is_k, int slot) {
       uint64_t *full_bar = &slot_full[slot];
@@ -804,15 +803,14 @@ __device__ __forceinline__ void decode_tc_body(const DecodeTcParams &tp, const C
       if (!ok) break;
       const UnitHdr cur = read_unit(&info[ib]);
       const int ntc = num_tiles(cur), ntp = num_tiles(prev);
-      if (k_side && !kFp8 && cur.valid) {
+      if (ldr == 0 && !kFp8 && cur.valid) {
         if (u >= 2) {
           ok = wait_all(&q_free[b], ((u >> 1) - 1) & 1);
           if (!ok) break;
         }
         load_q(cur, b);
       }
-      const int i0 = kTwoLoaders && !k_side ? ntc : 0, i1 = kTwoLoaders && k_side ? ntc : ntc + ntp;
-      for (int i = i0; i < i1 && ok; ++i) {
+      for (int i = (int)((uint32_t)(ldr + NL) - g_pos % NL) % NL; i < ntc + ntp && ok; i += NL) {
         const bool is_k = i < ntc;
         const uint32_t g = g_pos + (uint32_t)i;
         const int slot = (int)(g % S);
@@ -1220,10 +1218,10 @@ __device__ __forceinline__ void decode_tc_body(const DecodeTcParams &tp, const C
 }
 
 template <typename KV, typename QT, int G, int D>
-__global__ void __launch_bounds__(dtc::Roles::threads(G), 1)
+__global__ void __launch_bounds__(dtc::Roles::threads_for(dtc::Roles::loaders(G)), 1)
     decode_tc_kernel(const DecodeTcParams tp, const __grid_constant__ CUtensorMap tmap_k,
                      const __grid_constant__ CUtensorMap tmap_v) {
-  decode_tc_body<KV, QT, G, D>(tp, &tmap_k, &tmap_v);
+  decode_tc_body<KV, QT, G, D, dtc::Roles::loaders(G)>(tp, &tmap_k, &tmap_v);
 }
 
 // One CTA: count the split rows' merges and clear the merge list, and list
@@ -1297,7 +1295,7 @@ cudaError_t launch_decode_tc_one(const DecodeTcParams &p, const PoolMaps &m, cud
   // programmatic dependent launch: the decode grid's set-up overlaps the plan kernel
   cudaLaunchConfig_t cfg{};
   cfg.gridDim = dim3((unsigned)sms);
-  cfg.blockDim = dim3(dtc::Roles::threads(G));
+  cfg.blockDim = dim3(dtc::Roles::threads_for(dtc::Roles::loaders(G)));
   cfg.dynamicSmemBytes = smem;
   cfg.stream = s;
   cudaLaunchAttribute attr[1];

@@ -18,7 +18,7 @@
 // plan kernel (programmatic launch); the prefill CTAs do not.
 //
 // One CTA per SM (either body uses most of shared memory); the block is the
-// prefill CTA's 288 threads, which is also the decode body's nine warps.
+// prefill CTA's 288 threads: the decode body's nine warps, with two loaders.
 #pragma once
 
 #include "pa_decode_tc.cuh"
@@ -31,10 +31,10 @@ __global__ void __launch_bounds__(tc::Roles<1>::kThreads, 1)
     mixed_tc_kernel(const DecodeTcParams tp, const __grid_constant__ CUtensorMap tmap_k,
                     const __grid_constant__ CUtensorMap tmap_v, const PrefillTcParams pp, int prefill_ctas,
                     int prefill_x) {
-  static_assert(tc::Roles<1>::kThreads == dtc::Roles::threads(G), "the decode roles fill the block");
+  static_assert(tc::Roles<1>::kThreads == dtc::Roles::threads_for(2), "two decode loaders fill the block");
   const int b = blockIdx.x;   // block-uniform: every barrier of a body is reached by its whole block
   if (b < prefill_ctas) prefill_tc_body<KV, QT, G, 1>(pp, b % prefill_x, b / prefill_x);
-  else decode_tc_body<KV, QT, G>(tp, &tmap_k, &tmap_v);
+  else decode_tc_body<KV, QT, G, 128, 2>(tp, &tmap_k, &tmap_v);
 }
 
 // Host launcher: the decode's plan kernel, then the mixed grid as its
