@@ -181,7 +181,9 @@ def unique_kv_bytes(b) -> int:
 def measure_mixed_step(dev_name: str, steps: int, warmup: int) -> dict:
     """The chunked-prefill mixed batch (one 512-row chunk + 128 decodes, fp8 KV): its attention as two
     calls (pa_prefill_chunk, then pa_decode) against one pa_mixed_step (prefill tiles and decode CTAs in
-    one grid), each timed with CUDA events over the same number of back-to-back steps."""
+    one grid), and each part alone, each timed with CUDA events over the same number of back-to-back
+    steps.  vs_longer_part: the one launch's time over the longer part's alone (1.0 would be a perfect
+    overlap of the shorter part)."""
     import torch
     import workloads as W
     import paged_kv_cache_writes_gb300 as pa
@@ -199,7 +201,8 @@ def measure_mixed_step(dev_name: str, steps: int, warmup: int) -> dict:
                        "(256..8192 tokens), GQA 32/8, head_dim 128, block 16",
            "kv_bytes_decode": b.decode_kv_bytes(), "useful_tflop_prefill": _causal_flops(b) / 1e12}
     s = torch.cuda.current_stream()
-    for key, fn in (("two_calls", two), ("one_launch", db.mixed_attention)):
+    for key, fn in (("two_calls", two), ("one_launch", db.mixed_attention), ("prefill_alone", db.prefill_chunk),
+                    ("decode_alone", db.decode)):
         for _ in range(warmup):
             fn()
         torch.cuda.synchronize()
@@ -212,6 +215,7 @@ def measure_mixed_step(dev_name: str, steps: int, warmup: int) -> dict:
         assert pa.pa_get_device_error() == 0
         res[key + "_ms"] = e0.elapsed_time(e1) / steps
     res["speedup"] = res["two_calls_ms"] / res["one_launch_ms"]
+    res["vs_longer_part"] = res["one_launch_ms"] / max(res["prefill_alone_ms"], res["decode_alone_ms"])
     del db
     torch.cuda.empty_cache()
     return res

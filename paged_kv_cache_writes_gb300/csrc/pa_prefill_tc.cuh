@@ -49,10 +49,9 @@
 // that largest one (bf16 has 8 significant bits, f16 11); the scores are
 // multiplied back by 2^-e in the softmax.  P must be 16-bit in the MMA: with
 // a bf16 cache P is split into hi + lo bf16 parts (two P.V MMAs) that sum to
-// P within 2^-15 relative; otherwise P is rounded once to f16 (by integer
-// operations: to nearest even above 2^-14, within one subnormal step below)
-// and the softmax denominator sums the rounded P, so the output remains a
-// convex combination of V rows.
+// P within 2^-15 relative; otherwise P is rounded once to f16 (to nearest
+// even) and the softmax denominator sums the rounded P, so the output
+// remains a convex combination of V rows.
 //
 // Every mbarrier wait is bounded (PA_ERR_TIMEOUT, then the CTA abandons its
 // work); before tensor memory is freed the CTA waits for its outstanding MMAs
@@ -92,6 +91,22 @@ struct PrefillTcParams {
 };
 
 namespace tc {
+
+// p0, p1 -> one f16x2 word (p0 in the low half), each rounded to nearest
+// even by the conversion pipe; the two rounded values, widened exactly, are
+// added to acc on the FMA pipe (mixed-precision fma with f16 sources).  The
+// integer pipe, which the masks, maxima and addressing keep busy, is left
+// alone.
+__device__ __forceinline__ uint32_t f16x2_rn_add(float p0, float p1, float2 &acc) {
+  uint32_t w;
+  asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(w) : "f"(p1), "f"(p0));
+  unsigned short lo, hi;
+  asm("mov.b32 {%0, %1}, %2;" : "=h"(lo), "=h"(hi) : "r"(w));
+  const unsigned short one = 0x3c00;   // f16 1.0
+  asm("fma.rn.f32.f16 %0, %1, %2, %0;" : "+f"(acc.x) : "h"(lo), "h"(one));
+  asm("fma.rn.f32.f16 %0, %1, %2, %0;" : "+f"(acc.y) : "h"(hi), "h"(one));
+  return w;
+}
 
 constexpr int kD = 128;         // head_dim
 constexpr int kM = 128;         // packed query rows per Q tile (MMA M, tensor-memory lanes)
@@ -281,9 +296,6 @@ __device__ __forceinline__ void prefill_tc_body(const PrefillTcParams &p, int bx
     float m_ref = kNegInf;                     // reference maximum, log2 units
     float2 lacc[4] = {{0.f, 0.f}, {0.f, 0.f}, {0.f, 0.f}, {0.f, 0.f}};   // partial row sums
     const float2 ones = make_float2(1.f, 1.f);
-    const float2 zero2 = make_float2(0.f, 0.f);
-    const float2 k2m112 = make_float2(__uint_as_float(15u << 23), __uint_as_float(15u << 23));     // 2^-112
-    const float2 k2p112 = make_float2(__uint_as_float(239u << 23), __uint_as_float(239u << 23));   // 2^112
     bool ok = true;
     auto wait_all = [&](uint64_t *bar, uint32_t parity) {
       return __all_sync(0xffffffffu, wait_or_abort(bar, parity, p.err, abort_flag));
@@ -371,19 +383,8 @@ __device__ __forceinline__ void prefill_tc_body(const PrefillTcParams &p, int bx
               wl[k] = pack_hi_halves(__float_as_uint(lo.x), __float_as_uint(lo.y));
               lacc[k & 3] = ffma2(pk, ones, lacc[k & 3]);
             } else {
-              // f16 P rounded by integer operations (conversion instructions share
-              // the exponentials' pipe): p 2^-112 (p <= 2^8) carries the f16
-              // pattern, normal or subnormal, in bits 13..28 of its fp32 pattern.
-              // To nearest even for p >= 2^-14; below, within one f16 subnormal
-              // step (the product is rounded first).  The denominator sums the
-              // rounded P.
-              const float2 sv2 = ffma2(pk, k2m112, zero2);
-              uint32_t u0 = __float_as_uint(sv2.x), u1 = __float_as_uint(sv2.y);
-              u0 += 0xfffu + ((u0 >> 13) & 1u);
-              u1 += 0xfffu + ((u1 >> 13) & 1u);
-              w[k] = (u0 >> 13) | ((u1 << 3) & 0xffff0000u);
-              lacc[k & 3] = ffma2(make_float2(__uint_as_float(u0 & 0xffffe000u), __uint_as_float(u1 & 0xffffe000u)),
-                                  k2p112, lacc[k & 3]);
+              // f16 P (p <= 2^8), rounded to nearest even; the denominator sums the rounded P
+              w[k] = f16x2_rn_add(pk.x, pk.y, lacc[k & 3]);
             }
           }
           // P of these 16 keys goes over their own 16 score columns (read just
