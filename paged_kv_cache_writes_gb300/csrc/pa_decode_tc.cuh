@@ -1079,6 +1079,14 @@ __device__ __forceinline__ void decode_tc_body(const DecodeTcParams &tp, const C
     const uint32_t ring = smem_u32(smem + GE::kOffRing);
     const uint32_t qbuf = smem_u32(smem + GE::kOffQ);
     const uint32_t pbuf = smem_u32(smem + GE::kOffP);
+    // Operand descriptors: built once; a tile, buffer or k step adds its byte
+    // offset / 16 to the start-address field (every address stays below 256 KB,
+    // so the 14-bit field never carries).  One thread issues every MMA, and each
+    // instruction on its path delays the next issue.
+    auto dofs = [](uint32_t bytes) { return (uint64_t)(bytes >> 4); };
+    const uint64_t kdesc0 = kFp8 ? umma_desc(ring, 16) : umma_desc_sbo(ring, 16, kAtomB);
+    const uint64_t vdesc0 = kFp8 ? umma_desc_sbo(ring, 1024, 1024) : umma_desc_sbo(ring, kD == 128 ? 1024 : 0, kAtomB);
+    const uint64_t qdesc0 = umma_desc(qbuf, 16), pdesc0 = umma_desc(pbuf, 16);
     uint32_t g_cons = 0;   // tiles consumed, in the ring's order
     bool ok = true, issued = false;
     UnitHdr prev;
@@ -1106,17 +1114,17 @@ __device__ __forceinline__ void decode_tc_body(const DecodeTcParams &tp, const C
           fence_async_smem();   // tile and Q^T written through the generic proxy
           tc_fence_after();
           if (leader) {
-            const uint32_t kb = ring + slot * GE::kSlotBytes, qb = qbuf + (kFp8 ? ib : b) * GE::kQBytes;
+            const uint64_t kd = kdesc0 + dofs(slot * GE::kSlotBytes), qd = qdesc0 + dofs((kFp8 ? ib : b) * GE::kQBytes);
+            const uint32_t dcol = col_s(b, j);
             if constexpr (kFp8) {
               // 32 elements (32 B of each 128-byte row) per MMA; 8-row groups 1024 B apart
 #pragma unroll
-              for (int k = 0; k < kD / 32; ++k)
-                mma(col_s(b, j), umma_desc(kb + k * 32, 16), umma_desc(qb + k * 32, 16), idesc_s, k > 0 ? 1u : 0u);
+              for (int k = 0; k < kD / 32; ++k) mma(dcol, kd + dofs(k * 32), qd + dofs(k * 32), idesc_s, k > 0 ? 1u : 0u);
             } else {
 #pragma unroll
               for (int k = 0; k < kD / 16; ++k)
-                mma(col_s(b, j), umma_desc_sbo(kb + (k >> 2) * 1024 + (k & 3) * 32, 16, kAtomB),
-                    umma_desc(qb + (k >> 2) * (kNS * 128) + (k & 3) * 32, 16), idesc_s, k > 0 ? 1u : 0u);
+                mma(dcol, kd + dofs((k >> 2) * 1024 + (k & 3) * 32), qd + dofs((k >> 2) * (kNS * 128) + (k & 3) * 32),
+                    idesc_s, k > 0 ? 1u : 0u);
             }
             umma_commit(&slot_free[slot]);
           }
@@ -1169,19 +1177,22 @@ __device__ __forceinline__ void decode_tc_body(const DecodeTcParams &tp, const C
           fence_async_smem();   // zeroed rows and P^T written through the generic proxy
           tc_fence_after();
           if (leader) {
-            const uint32_t vb = ring + slot * GE::kSlotBytes, pb = pbuf + (bp * kMaxTiles + j) * GE::kPBytes;
+            const uint64_t vd = vdesc0 + dofs(slot * GE::kSlotBytes), pd = pdesc0 + dofs((bp * kMaxTiles + j) * GE::kPBytes);
+            const uint32_t dcol = col_o(bp), acc0 = j > 0 ? 1u : 0u;
+            // unrolled over a whole tile's key groups, the tail's predicated off
             if constexpr (kFp8) {
               // V^T: one 128-element MN panel, 8-key groups 1024 B apart, 32 keys per MMA
-              for (int kk = 0; kk < ngroups; ++kk)
-                mma(col_o(bp), umma_desc_sbo(vb + kk * 4096, 1024, 1024), umma_desc(pb + kk * 32, 16), idesc_o,
-                    (j > 0 || kk > 0) ? 1u : 0u);
+#pragma unroll
+              for (int kk = 0; kk < kKeys / 32; ++kk)
+                if (kk < ngroups) mma(dcol, vd + dofs(kk * 4096), pd + dofs(kk * 32), idesc_o, kk > 0 ? 1u : acc0);
             } else {
               // M = 128 elements of V^T in two 64-element halves (LBO apart): panels 0 and 1,
               // or panel 0 twice with head_dim 64 (lanes 64..127 of O^T then repeat 0..63)
-              for (int kk = 0; kk < ngroups; ++kk)
-                mma(col_o(bp), umma_desc_sbo(vb + kk * 2 * kAtomB, kD == 128 ? 1024 : 0, kAtomB),
-                    umma_desc(pb + (kk >> 2) * (kNO * 128) + (kk & 3) * 32, 16), idesc_o,
-                    (j > 0 || kk > 0) ? 1u : 0u);
+#pragma unroll
+              for (int kk = 0; kk < kKeys / 16; ++kk)
+                if (kk < ngroups)
+                  mma(dcol, vd + dofs(kk * 2 * kAtomB), pd + dofs((kk >> 2) * (kNO * 128) + (kk & 3) * 32), idesc_o,
+                      kk > 0 ? 1u : acc0);
             }
             umma_commit(&slot_free[slot]);
           }
