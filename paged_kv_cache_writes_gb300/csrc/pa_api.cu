@@ -527,11 +527,15 @@ pa_status pa_prefill_chunk(const void *q_chunk, pa_dtype q_dtype, const int32_t 
   if (use_tc) {
     t.err = device_error_word();
     if (!t.err) return PA_ERR_CUDA;
+    // fp8: the loaders copy whole cache blocks with bulk-tensor boxes
+    PoolMaps maps{};
+    if (fp8 && (!encode_pool_map_fp8_blocks(&maps.k, k_cache, c) || !encode_pool_map_fp8_blocks(&maps.v, v_cache, c)))
+      return PA_ERR_CUDA;
     cudaError_t e;
-    if (c.kv_dtype == PA_BF16) e = launch_prefill_tc_bf16(t, gqa, num_chunks, s);
-    else if (c.kv_dtype == PA_F16) e = launch_prefill_tc_f16(t, gqa, num_chunks, s);
-    else if (q_dtype == PA_BF16) e = launch_prefill_tc_fp8_bf16q(t, gqa, num_chunks, s);
-    else e = launch_prefill_tc_fp8_f16q(t, gqa, num_chunks, s);
+    if (c.kv_dtype == PA_BF16) e = launch_prefill_tc_bf16(t, maps, gqa, num_chunks, s);
+    else if (c.kv_dtype == PA_F16) e = launch_prefill_tc_f16(t, maps, gqa, num_chunks, s);
+    else if (q_dtype == PA_BF16) e = launch_prefill_tc_fp8_bf16q(t, maps, gqa, num_chunks, s);
+    else e = launch_prefill_tc_fp8_f16q(t, maps, gqa, num_chunks, s);
     return e == cudaSuccess ? PA_OK : PA_ERR_CUDA;
   }
 

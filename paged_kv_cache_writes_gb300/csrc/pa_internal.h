@@ -159,13 +159,13 @@ cudaError_t launch_mixed_tc_fp8_f16q(const DecodeTcParams &d, const PoolMaps &m,
 constexpr bool prefill_tc_supported(int head_dim, int gqa) {
   return head_dim == 128 && (gqa == 1 || gqa == 2 || gqa == 4 || gqa == 8 || gqa == 16);
 }
-cudaError_t launch_prefill_tc_bf16(const PrefillTcParams &p, int gqa, int num_chunks,
+cudaError_t launch_prefill_tc_bf16(const PrefillTcParams &p, const PoolMaps &m, int gqa, int num_chunks,
                                    cudaStream_t s);
-cudaError_t launch_prefill_tc_f16(const PrefillTcParams &p, int gqa, int num_chunks,
+cudaError_t launch_prefill_tc_f16(const PrefillTcParams &p, const PoolMaps &m, int gqa, int num_chunks,
                                   cudaStream_t s);
-cudaError_t launch_prefill_tc_fp8_bf16q(const PrefillTcParams &p, int gqa, int num_chunks,
+cudaError_t launch_prefill_tc_fp8_bf16q(const PrefillTcParams &p, const PoolMaps &m, int gqa, int num_chunks,
                                         cudaStream_t s);
-cudaError_t launch_prefill_tc_fp8_f16q(const PrefillTcParams &p, int gqa, int num_chunks,
+cudaError_t launch_prefill_tc_fp8_f16q(const PrefillTcParams &p, const PoolMaps &m, int gqa, int num_chunks,
                                        cudaStream_t s);
 
 }  // namespace pa

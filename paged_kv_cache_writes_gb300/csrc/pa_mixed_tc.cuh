@@ -33,7 +33,7 @@ __global__ void __launch_bounds__(tc::Roles<1>::kThreads, 1)
                     int prefill_x) {
   static_assert(tc::Roles<1>::kThreads == dtc::Roles::threads_for(2), "two decode loaders fill the block");
   const int b = blockIdx.x;   // block-uniform: every barrier of a body is reached by its whole block
-  if (b < prefill_ctas) prefill_tc_body<KV, QT, G, 1>(pp, b % prefill_x, b / prefill_x);
+  if (b < prefill_ctas) prefill_tc_body<KV, QT, G, 1>(pp, b % prefill_x, b / prefill_x, &tmap_k, &tmap_v);
   else decode_tc_body<KV, QT, G, 128, 2>(tp, &tmap_k, &tmap_v);
 }
 
@@ -45,7 +45,7 @@ cudaError_t launch_mixed_tc_one(const DecodeTcParams &tp, const PoolMaps &m, con
   constexpr bool kFp8 = std::is_same<KV, uint8_t>::value;
   constexpr bool kSplit = std::is_same<QT, __nv_bfloat16>::value && !kFp8;
   constexpr int smem_d = dtc::TcGeo<G, kSplit, kFp8, dtc::QTerms<KV, QT>::value>::kSmemBytes;
-  constexpr int smem_p = tc::Layout<1>::kSmemBytes;
+  constexpr int smem_p = tc::Layout<1, kFp8>::kSmemBytes;
   constexpr int smem = smem_d > smem_p ? smem_d : smem_p;
   constexpr int BR = tc::kM / G;   // token rows per prefill CTA
   PrefillTcParams pp = pp0;

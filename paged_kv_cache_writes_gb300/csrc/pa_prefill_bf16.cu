@@ -4,8 +4,8 @@
 #include "pa_prefill_tc.cuh"
 
 namespace pa {
-cudaError_t launch_prefill_tc_bf16(const PrefillTcParams &p, int gqa, int num_chunks,
+cudaError_t launch_prefill_tc_bf16(const PrefillTcParams &p, const PoolMaps &m, int gqa, int num_chunks,
                                    cudaStream_t s) {
-  return launch_prefill_tc<__nv_bfloat16, __nv_bfloat16>(p, gqa, num_chunks, s);
+  return launch_prefill_tc<__nv_bfloat16, __nv_bfloat16>(p, m, gqa, num_chunks, s);
 }
 }  // namespace pa

@@ -3,8 +3,8 @@
 #include "pa_prefill_tc.cuh"
 
 namespace pa {
-cudaError_t launch_prefill_tc_f16(const PrefillTcParams &p, int gqa, int num_chunks,
+cudaError_t launch_prefill_tc_f16(const PrefillTcParams &p, const PoolMaps &m, int gqa, int num_chunks,
                                   cudaStream_t s) {
-  return launch_prefill_tc<__half, __half>(p, gqa, num_chunks, s);
+  return launch_prefill_tc<__half, __half>(p, m, gqa, num_chunks, s);
 }
 }  // namespace pa

@@ -4,12 +4,12 @@
 #include "pa_prefill_tc.cuh"
 
 namespace pa {
-cudaError_t launch_prefill_tc_fp8_bf16q(const PrefillTcParams &p, int gqa, int num_chunks,
+cudaError_t launch_prefill_tc_fp8_bf16q(const PrefillTcParams &p, const PoolMaps &m, int gqa, int num_chunks,
                                         cudaStream_t s) {
-  return launch_prefill_tc<uint8_t, __nv_bfloat16>(p, gqa, num_chunks, s);
+  return launch_prefill_tc<uint8_t, __nv_bfloat16>(p, m, gqa, num_chunks, s);
 }
-cudaError_t launch_prefill_tc_fp8_f16q(const PrefillTcParams &p, int gqa, int num_chunks,
+cudaError_t launch_prefill_tc_fp8_f16q(const PrefillTcParams &p, const PoolMaps &m, int gqa, int num_chunks,
                                        cudaStream_t s) {
-  return launch_prefill_tc<uint8_t, __half>(p, gqa, num_chunks, s);
+  return launch_prefill_tc<uint8_t, __half>(p, m, gqa, num_chunks, s);
 }
 }  // namespace pa

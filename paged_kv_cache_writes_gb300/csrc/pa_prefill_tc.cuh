@@ -30,9 +30,12 @@
 //    each inside one block of the block table) of every K and V tile into a
 //    ring of kStages tiles, 512 contiguous bytes per warp instruction.
 //    16-bit caches: 16-byte cp.async straight into the 128-byte-swizzled MMA
-//    layout; fp8 caches: register loads a whole tile ahead (half a tile with
-//    two Q tiles per CTA), widened exactly to f16 on the way to shared
-//    memory.  Rows past the end of the sequence are
+//    layout; fp8 caches, one Q tile per CTA: each warp brings its rows'
+//    cache blocks (one bulk-tensor box per block) into a ring of code tiles
+//    two tiles ahead, then widens them exactly to f16 from shared memory
+//    into the MMA layout; with two Q tiles (no shared memory to spare):
+//    register loads half a tile ahead, widened on the way to shared memory.
+//    Rows past the end of the sequence are
 //    zero-filled so a zero probability never meets a stale (possibly NaN)
 //    value in the MMA.
 //  * last warp, MMA (one elected lane issues): for each Q tile t in turn,
@@ -131,18 +134,25 @@ constexpr int kQBytes = kM * kD * 2;        // one Q tile: 2 panels x [128 rows 
 constexpr int kTileBytes = kN * kD * 2;     // 2 panels x [128 rows x 128 B]
 constexpr int kTilePanel = kN * 128;        // 16 KB
 constexpr int kLoaders = 128;               // threads of the load warps
-constexpr int kNumBars = 4 * kStages + 3 * 4 + 2;
+constexpr int kCodeTile = kN * kD;          // fp8 codes of one K or V tile (128 rows x 128 B)
+constexpr int kMaxCodeStages = 2;
+constexpr int kNumBars = 4 * kStages + 3 * 4 + 2 + 4 * kMaxCodeStages;
 
 // Shared-memory map, bytes from a 1024-aligned base (128-byte swizzle atoms).
-template <int QT>
+// fp8 caches with one Q tile: kCStages tiles of codes (K then V) after the
+// 16-bit K/V stages.
+template <int QT, bool kFp8 = false>
 struct Layout {
+  static constexpr int kCStages = (kFp8 && QT == 1) ? kMaxCodeStages : 0;
   static constexpr int kOffQ = 0;
   static constexpr int kOffK = kOffQ + QT * kQBytes;
   static constexpr int kOffV = kOffK + kStages * kTileBytes;
-  static constexpr int kOffBar = kOffV + kStages * kTileBytes;
+  static constexpr int kOffCode = kOffV + kStages * kTileBytes;
+  static constexpr int kOffBar = kOffCode + kCStages * 2 * kCodeTile;
   static constexpr int kOffMisc = kOffBar + kNumBars * 8;
   static constexpr int kSmemBytes = kOffMisc + 64 + 1024;  // + alignment slack
   static_assert(kSmemBytes <= 227 * 1024, "shared memory");
+  static_assert(kOffCode % 1024 == 0 && kCodeTile % 1024 == 0, "1024-byte swizzle atoms for the code boxes");
 };
 
 }  // namespace tc
@@ -150,9 +160,10 @@ struct Layout {
 // The prefill CTA (chunk x row block bx, KV head by), for prefill_tc_kernel and
 // for the prefill CTAs of the mixed kernel (pa_mixed_tc.cuh).
 template <typename KV, typename QT, int G, int kQTiles>
-__device__ __forceinline__ void prefill_tc_body(const PrefillTcParams &p, int bx, int by) {
+__device__ __forceinline__ void prefill_tc_body(const PrefillTcParams &p, int bx, int by, const CUtensorMap *tmap_k,
+                                                const CUtensorMap *tmap_v) {
   using namespace tc;
-  using L = Layout<kQTiles>;
+  using L = Layout<kQTiles, std::is_same<KV, uint8_t>::value>;
   using R = Roles<kQTiles>;
   constexpr int kSoftmax = R::kSoftmax, kLoadWarp0 = R::kLoadWarp0, kMmaWarp = R::kMmaWarp;
   constexpr int kTmemCols = R::kTmemCols;
@@ -178,6 +189,7 @@ __device__ __forceinline__ void prefill_tc_body(const PrefillTcParams &p, int bx
   uint64_t *o_done = p_full + 4;                 // [tile] P.V of key tile j complete (phase j)
   uint64_t *q_ready = o_done + 4;                // Q staged (every softmax thread)
   uint64_t *fin = q_ready + 1;                   // every MMA of the CTA complete
+  uint64_t *code_full = fin + 1;                 // [load warp][code stage] the warp's fp8 boxes landed
   uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + L::kOffMisc);
   volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + L::kOffMisc + 8);
 
@@ -217,6 +229,7 @@ __device__ __forceinline__ void prefill_tc_body(const PrefillTcParams &p, int bx
     }
     mbar_init(q_ready, kSoftmax);
     mbar_init(fin, 1);
+    for (int i = 0; i < 4 * kMaxCodeStages; ++i) mbar_init(&code_full[i], 1);   // one expect-tx arrival
     *abort_flag = 0;
     fence_mbar_init();
   }
@@ -498,13 +511,79 @@ __device__ __forceinline__ void prefill_tc_body(const PrefillTcParams &p, int bx
           cp_async_arrive_noinc(which ? &v_full[s] : &k_full[s]);
         }
       }
+    } else if constexpr (L::kCStages > 0) {
+      // fp8, one Q tile: warp lw's rows of tile j are one or two whole cache
+      // blocks (block_size 32 or 16) of K and of V; it copies them with one
+      // bulk-tensor box each into code stage j % kCS (128-byte swizzle, as in
+      // the pool map) kCS tiles ahead, then widens them to f16 into the K/V
+      // stage.  Each warp waits only for its own boxes.
+      constexpr int kCS = L::kCStages;
+      const int q = lane & 7, pn = q >> 2, c0 = (2 * q) & 7;
+      const int bs = p.block_size;
+      uint64_t *cbar = code_full + lw * kCS;
+      int issued = 0;      // tiles whose boxes this warp has issued
+      uint32_t nvs = 0;    // byte 2 * stage + run: rows of that run holding keys (the block-id window only moves forward)
+      auto issue_codes = [&](int j) {
+        const int cs = j % kCS;
+        int64_t row0;
+        const uint32_t n0 = (uint32_t)rows_of(j, 0, row0), n1 = (uint32_t)rows_of(j, 1, row0);
+        nvs = (nvs & ~(0xffffu << (16 * cs))) | ((n0 | (n1 << 8)) << (16 * cs));
+        const int32_t b0 = block_of(j, 0), b1 = bs == 16 ? block_of(j, 1) : -1;
+        const uint32_t n = (b0 >= 0 ? 1u : 0u) + (b1 >= 0 ? 1u : 0u);
+        if (lane == 0) mbar_arrive_expect_tx(&cbar[cs], n * 2u * (uint32_t)(bs * kD));
+        __syncwarp();
+        if (lane < 4) {   // lane = 2 * which + run
+          const int which = lane >> 1, r = lane & 1;
+          const int32_t blk = r ? b1 : b0;
+          if (blk >= 0)
+            tma_load_2d(smem + L::kOffCode + cs * 2 * kCodeTile + which * kCodeTile + (32 * lw + 16 * r) * 128,
+                        which ? tmap_v : tmap_k, &cbar[cs], 0, (int32_t)(((int64_t)blk * p.num_kv_heads + g) * bs));
+        }
+        ++issued;
+      };
+      for (int j = 0; j < kCS && j < nkt; ++j) issue_codes(j);
+      for (int j = 0; j < nkt && ok; ++j) {
+        const int s = j % kStages, cs = j % kCS;
+        const uint32_t ph_prev = ((j / kStages) - 1) & 1;
+        if (!wait_slot(&cbar[cs], (j / kCS) & 1)) break;
+        const uint8_t *cst = smem + L::kOffCode + cs * 2 * kCodeTile;
+#pragma unroll
+        for (int qi = 0; qi < 4; ++qi) {
+          const int which = qi >> 1, r = qi & 1;
+          if (r == 0 && j >= kStages && !wait_slot(which ? &v_free[s] : &k_free[s], ph_prev)) break;
+          const int nval = (int)((nvs >> (16 * cs + 8 * r)) & 0xffu);   // rows past the sequence end: zeros
+          uint8_t *tile = smem + (which ? L::kOffV : L::kOffK) + s * kTileBytes + pn * kTilePanel;
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            const int rr = 4 * i + (lane >> 3), row = 32 * lw + 16 * r + rr;
+            const uint4 cw = rr < nval ? *reinterpret_cast<const uint4 *>(cst + which * kCodeTile + row * 128 +
+                                                                            ((q ^ (row & 7)) << 4))
+                                       : make_uint4(0, 0, 0, 0);
+            uint32_t o[8];
+            widen16<__half>(cw, o);   // the MMAs take f16 operands with an fp8 cache
+            uint8_t *dst = tile + row * 128;
+            *reinterpret_cast<uint4 *>(dst + ((c0 ^ (row & 7)) << 4)) = make_uint4(o[0], o[1], o[2], o[3]);
+            *reinterpret_cast<uint4 *>(dst + (((c0 + 1) ^ (row & 7)) << 4)) = make_uint4(o[4], o[5], o[6], o[7]);
+          }
+          if (r == 1) {
+            fence_async_smem();
+            mbar_arrive(which ? &v_full[s] : &k_full[s]);
+          }
+        }
+        if (!ok) break;
+        // code stage cs is read: its next boxes (generic reads before the async-proxy writes)
+        fence_async_smem();
+        if (j + kCS < nkt) issue_codes(j + kCS);
+      }
+      // no box of this warp in flight at exit (bounded waits)
+      for (int jj = max(0, issued - kCS); jj < issued; ++jj)
+        wait_or_abort(&cbar[jj % kCS], (jj / kCS) & 1, p.err, abort_flag);
     } else {
-      // fp8 rows (128 B): per instruction 4 rows x 8 words of 16 codes.  A tile
-      // is four quarters (K run 0, K run 1, V run 0, V run 1).  The loads run
-      // kPf quarters ahead of the widening into shared memory: a whole tile
-      // (32 KB of codes per CTA) with one Q tile per CTA, half a tile with two
-      // (whose threads have fewer registers each).
-      constexpr int kPf = kQTiles == 1 ? 4 : 2;
+      // fp8 rows (128 B), two Q tiles: per instruction 4 rows x 8 words of 16
+      // codes.  A tile is four quarters (K run 0, K run 1, V run 0, V run 1).
+      // The loads run kPf quarters (half a tile) ahead of the widening into
+      // shared memory.
+      constexpr int kPf = 2;
       const int q = lane & 7, pn = q >> 2, c0 = (2 * q) & 7;
       auto load = [&](int j, int qi, uint4 (&w)[4]) {
         int64_t row0;
@@ -656,16 +735,18 @@ __device__ __forceinline__ void prefill_tc_body(const PrefillTcParams &p, int bx
 }
 
 template <typename KV, typename QT, int G, int kQTiles>
-__global__ void __launch_bounds__(tc::Roles<kQTiles>::kThreads, 1) prefill_tc_kernel(const PrefillTcParams p) {
-  prefill_tc_body<KV, QT, G, kQTiles>(p, blockIdx.x, blockIdx.y);
+__global__ void __launch_bounds__(tc::Roles<kQTiles>::kThreads, 1)
+    prefill_tc_kernel(const PrefillTcParams p, const __grid_constant__ CUtensorMap tmap_k,
+                      const __grid_constant__ CUtensorMap tmap_v) {
+  prefill_tc_body<KV, QT, G, kQTiles>(p, blockIdx.x, blockIdx.y, &tmap_k, &tmap_v);
 }
 
 // Host launcher: grid (chunks x row blocks, KV heads), one CTA per SM.  Two Q
 // tiles per CTA share every K/V tile, unless that leaves SMs idle (few rows):
 // then one Q tile per CTA doubles the grid.
 template <typename KV, typename QT, int G, int kQTiles>
-cudaError_t launch_prefill_tc_tiles(const PrefillTcParams &p0, int num_chunks, cudaStream_t s) {
-  constexpr int smem = tc::Layout<kQTiles>::kSmemBytes;
+cudaError_t launch_prefill_tc_tiles(const PrefillTcParams &p0, const PoolMaps &m, int num_chunks, cudaStream_t s) {
+  constexpr int smem = tc::Layout<kQTiles, std::is_same<KV, uint8_t>::value>::kSmemBytes;
   constexpr int BR = kQTiles * tc::kM / G;
   PrefillTcParams p = p0;
   p.row_blocks = (p.max_q_len + BR - 1) / BR;
@@ -675,27 +756,30 @@ cudaError_t launch_prefill_tc_tiles(const PrefillTcParams &p0, int num_chunks, c
   const int64_t gx = (int64_t)num_chunks * p.row_blocks;
   if (gx > 2147483647ll || p.num_kv_heads > 65535) return cudaErrorInvalidValue;
   dim3 grid((unsigned)gx, (unsigned)p.num_kv_heads);
-  kern<<<grid, tc::Roles<kQTiles>::kThreads, smem, s>>>(p);
+  kern<<<grid, tc::Roles<kQTiles>::kThreads, smem, s>>>(p, m.k, m.v);
   return cudaGetLastError();
 }
 
 template <typename KV, typename QT, int G>
-cudaError_t launch_prefill_tc_one(const PrefillTcParams &p, int num_chunks, int num_sms, cudaStream_t s) {
+cudaError_t launch_prefill_tc_one(const PrefillTcParams &p, const PoolMaps &m, int num_chunks, int num_sms,
+                                  cudaStream_t s) {
   const int64_t two = (int64_t)num_chunks * ((p.max_q_len + 2 * tc::kM / G - 1) / (2 * tc::kM / G)) * p.num_kv_heads;
-  if (two >= num_sms) return launch_prefill_tc_tiles<KV, QT, G, 2>(p, num_chunks, s);
-  return launch_prefill_tc_tiles<KV, QT, G, 1>(p, num_chunks, s);
+  if (two >= num_sms) return launch_prefill_tc_tiles<KV, QT, G, 2>(p, m, num_chunks, s);
+  return launch_prefill_tc_tiles<KV, QT, G, 1>(p, m, num_chunks, s);
 }
 
+// m: with an fp8 cache, each pool as [rows][128 codes] with one cache block per
+// box (encode_pool_map_fp8_blocks); unused with a 16-bit cache.
 template <typename KV, typename QT>
-cudaError_t launch_prefill_tc(const PrefillTcParams &p, int gqa, int num_chunks, cudaStream_t s) {
+cudaError_t launch_prefill_tc(const PrefillTcParams &p, const PoolMaps &m, int gqa, int num_chunks, cudaStream_t s) {
   int num_sms = 0;
   if (current_sm_count(&num_sms) != cudaSuccess) return cudaErrorUnknown;
   switch (gqa) {
-    case 1: return launch_prefill_tc_one<KV, QT, 1>(p, num_chunks, num_sms, s);
-    case 2: return launch_prefill_tc_one<KV, QT, 2>(p, num_chunks, num_sms, s);
-    case 4: return launch_prefill_tc_one<KV, QT, 4>(p, num_chunks, num_sms, s);
-    case 8: return launch_prefill_tc_one<KV, QT, 8>(p, num_chunks, num_sms, s);
-    case 16: return launch_prefill_tc_one<KV, QT, 16>(p, num_chunks, num_sms, s);
+    case 1: return launch_prefill_tc_one<KV, QT, 1>(p, m, num_chunks, num_sms, s);
+    case 2: return launch_prefill_tc_one<KV, QT, 2>(p, m, num_chunks, num_sms, s);
+    case 4: return launch_prefill_tc_one<KV, QT, 4>(p, m, num_chunks, num_sms, s);
+    case 8: return launch_prefill_tc_one<KV, QT, 8>(p, m, num_chunks, num_sms, s);
+    case 16: return launch_prefill_tc_one<KV, QT, 16>(p, m, num_chunks, num_sms, s);
     default: return cudaErrorInvalidValue;
   }
 }
