@@ -346,6 +346,9 @@ __device__ __forceinline__ void decode_tc_body(const DecodeTcParams &tp, const C
   constexpr bool kSplit = kBf16;            // bf16 cache: P as hi + lo
   constexpr int kQTerms = QTerms<KV, QT>::value;
   using GE = TcGeo<G, kSplit, kFp8, kQTerms, D>;
+  // The MMA warp consumes the ring in order, so a loader's wait for the consumption of
+  // position g - S is never two phases behind while it has NL <= S positions in hand.
+  static_assert(GE::kSlots >= NL, "at least as many ring slots as loaders (parity waits stay within one phase)");
   constexpr int kAtomB = GE::kAtom;           // bytes of 8 keys of a 16-bit tile
   constexpr int kRowChunks = kD * 2 / 16;     // 16-byte chunks of a 16-bit row
   constexpr int S = GE::kSlots, kNO = GE::kNO, kNS = GE::kNS;
@@ -368,7 +371,7 @@ __device__ __forceinline__ void decode_tc_body(const DecodeTcParams &tp, const C
   uint64_t *o_free = o_full + 2;              // [2] O^T read by every softmax thread (128)
   uint64_t *red_bar = o_free + 2;             // [2] per-warp maxima and sums exchanged (128)
   uint64_t *info_full = red_bar + 2;          // [kInfo] unit descriptor published (32 scheduler lanes)
-  uint64_t *info_free = info_full + kInfo;    // [kInfo] released by the MMA warp and the softmax warps
+  uint64_t *info_free = info_full + kInfo;    // [kInfo] released by the MMA warp, the softmax warps and every loader
   uint64_t *fin = info_free + kInfo;          // every MMA of the CTA complete
   uint64_t *rep_full = fin + 1;               // [kRep] a split unit's partials stored (one arrival per softmax warp)
   uint64_t *rep_free = rep_full + kRep;       // [kRep] its report taken by the merge warp
@@ -402,7 +405,7 @@ __device__ __forceinline__ void decode_tc_body(const DecodeTcParams &tp, const C
     }
     for (int i = 0; i < kInfo; ++i) {
       mbar_init(&info_full[i], 32);   // every scheduler lane, after its own stores
-      mbar_init(&info_free[i], 2);
+      mbar_init(&info_free[i], 2 + NL);   // O^T issued, epilogue done, each loader past the unit
     }
     mbar_init(fin, 1);
     for (int i = 0; i < kRep; ++i) {
@@ -818,6 +821,12 @@ __device__ __forceinline__ void decode_tc_body(const DecodeTcParams &tp, const C
         if (!ok) break;
         issue_tile(is_k ? cur : prev, is_k ? ib : ibp, is_k ? i : i - ntc, is_k, slot);
       }
+      if (!ok) break;
+      // this loader is done with unit u-1's descriptor (its V tiles' block ids): a loader
+      // may own no tile of several units in a row, and the descriptor must not be
+      // reused before it has passed them
+      __syncwarp();
+      if (u >= 1 && lane == 0) mbar_arrive(&info_free[ibp]);
       g_pos += (uint32_t)(ntc + ntp);
       if (!cur.valid) break;
       prev = cur;
