@@ -1112,16 +1112,16 @@ __device__ __forceinline__ void decode_tc_body(const DecodeTcParams &tp, const C
           ok = wait_all(&s_free[b], ((u >> 1) - 1) & 1);
           if (!ok) break;
         }
-        if constexpr (!kFp8) {   // fp8: Q^T was written with the descriptor
+        if constexpr (!kFp8) {   // fp8: Q^T was written (and fenced) with the descriptor
           ok = wait_all(&q_full[b], (u >> 1) & 1);
           if (!ok) break;
+          fence_async_smem();   // Q^T staged by cp.async (generic proxy) -> the MMAs' reads
         }
         for (int j = 0; j < nt; ++j) {
           const int slot = (int)(g_cons % S);
           ok = wait_all(&slot_full[slot], (g_cons / S) & 1);
           if (!ok) break;
-          fence_async_smem();   // tile and Q^T written through the generic proxy
-          tc_fence_after();
+          tc_fence_after();   // the tile came by bulk copy (async proxy): no proxy fence
           if (leader) {
             const uint64_t kd = kdesc0 + dofs(slot * GE::kSlotBytes), qd = qdesc0 + dofs((kFp8 ? ib : b) * GE::kQBytes);
             const uint32_t dcol = col_s(b, j);
@@ -1181,9 +1181,10 @@ __device__ __forceinline__ void decode_tc_body(const DecodeTcParams &tp, const C
                                            (c & 7) * 16) = make_uint4(0, 0, 0, 0);
               }
             }
+            fence_async_smem();   // the zeroed rows (generic proxy) -> the MMAs' reads
             __syncwarp();
           }
-          fence_async_smem();   // zeroed rows and P^T written through the generic proxy
+          // P^T was fenced by the softmax warps before p_full; the tile came by bulk copy
           tc_fence_after();
           if (leader) {
             const uint64_t vd = vdesc0 + dofs(slot * GE::kSlotBytes), pd = pdesc0 + dofs((bp * kMaxTiles + j) * GE::kPBytes);
