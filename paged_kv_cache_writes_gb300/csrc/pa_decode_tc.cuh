@@ -100,10 +100,17 @@
 namespace pa {
 
 // A split row (sequence, KV head) whose partitions are all written, in the
-// workspace's merge list; ready is set (release) once the record is complete.
+// workspace's merge list: one 64-bit word, row << 32 | kvh << 13 | nparts,
+// stored with release once the partials are published and read with one
+// acquire load (nparts >= 2, so a published word is never 0; the plan kernel
+// zeroes the list).  The merge needs no second round trip for the record.
 struct DecodeMergeJob {
-  int32_t row, kvh, nparts, ready;
+  uint64_t word;
+  uint64_t unused;   // 16-byte records
 };
+__device__ __forceinline__ uint64_t merge_word(int row, int kvh, int nparts) {
+  return ((uint64_t)(uint32_t)row << 32) | ((uint64_t)(uint32_t)kvh << 13) | (uint64_t)(uint32_t)nparts;
+}
 
 struct DecodeTcParams {
   DecodeParams d;            // shapes, plan and workspace (d.groups = 1: a unit serves all G heads)
@@ -444,17 +451,10 @@ __device__ __forceinline__ void decode_tc_body(const DecodeTcParams &tp, const C
   // over the row's partitions p (m_p in log2 units, M their maximum), kept as a
   // running maximum; lane l merges elements 4l..4l+3 of all G heads, the loads
   // of two partitions for every head in flight together.
-  auto merge_job = [&](int t) {
-    int job_row = 0, job_kvh = 0, job_np = 0;
-    if (lane == 0) {   // read by the lane that acquired the record, then broadcast
-      const volatile DecodeMergeJob *jv = tp.jobs + t;
-      job_row = jv->row;
-      job_kvh = jv->kvh;
-      job_np = jv->nparts;
-    }
-    job_row = __shfl_sync(0xffffffffu, job_row, 0);
-    job_kvh = __shfl_sync(0xffffffffu, job_kvh, 0);
-    job_np = __shfl_sync(0xffffffffu, job_np, 0);
+  auto merge_job = [&](uint64_t word) {   // the record as lane 0 acquired it
+    word = ((uint64_t)__shfl_sync(0xffffffffu, (uint32_t)(word >> 32), 0) << 32) |
+           __shfl_sync(0xffffffffu, (uint32_t)word, 0);
+    const int job_row = (int)(word >> 32), job_kvh = (int)((word >> 13) & 0x7ffffu), job_np = (int)(word & 0x1fffu);
     __syncwarp();   // lane 0's acquire of the record orders every lane's reads of the partials
     const int64_t head0 = (int64_t)job_row * hq + (int64_t)job_kvh * G;
     float m[G], l[G];
@@ -516,12 +516,12 @@ __device__ __forceinline__ void decode_tc_body(const DecodeTcParams &tp, const C
       if (lane == 0) t = atomicAdd(&p.hdr->pad[1], 1);
       t = __shfl_sync(0xffffffffu, t, 0);
       if (t >= total_jobs) return;
-      int ready = 0;
+      uint64_t word = 0;
       if (lane == 0) {
         const uint64_t t0 = global_timer_ns();
         for (;;) {
-          asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(ready) : "l"(&tp.jobs[t].ready) : "memory");
-          if (ready || *abort_flag) break;
+          asm volatile("ld.acquire.gpu.global.b64 %0, [%1];" : "=l"(word) : "l"(&tp.jobs[t].word) : "memory");
+          if (word || *abort_flag) break;
           if (global_timer_ns() - t0 > kWaitLimitNs) {
             record_error(p.err, PA_ERR_TIMEOUT);
             *abort_flag = 1;
@@ -530,8 +530,8 @@ __device__ __forceinline__ void decode_tc_body(const DecodeTcParams &tp, const C
           __nanosleep(500);
         }
       }
-      if (!__shfl_sync(0xffffffffu, ready, 0)) return;
-      merge_job(t);
+      if (!__shfl_sync(0xffffffffu, word != 0, 0)) return;
+      merge_job(word);
     }
   };
 
@@ -1032,11 +1032,8 @@ __device__ __forceinline__ void decode_tc_body(const DecodeTcParams &tp, const C
               if (old == r.z - 1) {
                 asm volatile("fence.acq_rel.gpu;" ::: "memory");
                 const int jt = atomicAdd(&p.hdr->pad[0], 1);
-                DecodeMergeJob *j = tp.jobs + jt;
-                j->row = r.x;
-                j->kvh = r.y;
-                j->nparts = r.z;
-                asm volatile("st.release.gpu.global.b32 [%0], %1;" ::"l"(&j->ready), "r"(1) : "memory");
+                asm volatile("st.release.gpu.global.b64 [%0], %1;" ::"l"(&tp.jobs[jt].word), "l"(merge_word(r.x, r.y, r.z))
+                             : "memory");
               }
               mbar_arrive(&rep_free[rs]);
             }
@@ -1054,10 +1051,10 @@ __device__ __forceinline__ void decode_tc_body(const DecodeTcParams &tp, const C
           t = -1;
         }
       }
-      int ready = 0;
+      uint64_t word = 0;
       if (t >= 0 && lane == 0)
-        asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(ready) : "l"(&tp.jobs[t].ready) : "memory");
-      if (!__shfl_sync(0xffffffffu, ready, 0)) {
+        asm volatile("ld.acquire.gpu.global.b64 %0, [%1];" : "=l"(word) : "l"(&tp.jobs[t].word) : "memory");
+      if (!__shfl_sync(0xffffffffu, word != 0, 0)) {
         if (progress) {
           t_idle = global_timer_ns();
         } else if (global_timer_ns() - t_idle > kWaitLimitNs) {
@@ -1069,7 +1066,7 @@ __device__ __forceinline__ void decode_tc_body(const DecodeTcParams &tp, const C
         }
         continue;
       }
-      merge_job(t);
+      merge_job(word);
       t = -1;
       t_idle = global_timer_ns();
     }
@@ -1266,7 +1263,7 @@ __global__ void __launch_bounds__(1024) decode_tc_plan_kernel(DecodeParams p, De
   __shared__ int split_rows;
   for (int64_t i = tid; i < (int64_t)p.num_seqs * p.num_q_heads; i += blockDim.x) p.ws_count[i] = 0;
   if (p.max_partitions > 1)   // the merge list exists only when a row can be split
-    for (int64_t i = tid; i < (int64_t)p.num_seqs * p.num_kv_heads; i += blockDim.x) jobs[i].ready = 0;
+    for (int64_t i = tid; i < (int64_t)p.num_seqs * p.num_kv_heads; i += blockDim.x) jobs[i].word = 0;
   for (int i = tid; i < nkeys; i += blockDim.x) base[i] = 0;
   if (tid == 0) split_rows = 0;
   __syncthreads();
