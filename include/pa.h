@@ -258,11 +258,10 @@ PA_API pa_status pa_set_decode_kernel(int32_t kernel);
  * that array until the process exits.
  *
  *  - The first call on a device, with that device current, looks up the
- *    array's device address (cudaGetSymbolAddress); make that first call
- *    before any stream capture on that device.  The address is kept per
- *    device together with the id of the context it belongs to; after a
- *    cudaDeviceReset the next call sees a new context and looks the address
- *    up again (so that call, too, should come before any stream capture).
+ *    array's device address (cudaGetSymbolAddress, a runtime call that
+ *    allocates nothing).  The address is kept per device together with the
+ *    id of the context it belongs to; after a cudaDeviceReset the next call
+ *    sees a new context and looks the address up again.
  *  - A problem whose workspace (pa_decode_workspace_bytes) exceeds the array
  *    returns PA_ERR_UNSUPPORTED before anything is launched.
  *  - Every call on a device shares the one array.  Its contents are rebuilt
