@@ -52,7 +52,7 @@
 // that largest one (bf16 has 8 significant bits, f16 11); the scores are
 // multiplied back by 2^-e in the softmax.  P must be 16-bit in the MMA: with
 // a bf16 cache P is split into hi + lo bf16 parts (two P.V MMAs) that sum to
-// P within 2^-15 relative; otherwise P is rounded once to f16 (to nearest
+// P within 2^-16 relative; otherwise P is rounded once to f16 (to nearest
 // even) and the softmax denominator sums the rounded P, so the output
 // remains a convex combination of V rows.
 //
@@ -387,13 +387,16 @@ __device__ __forceinline__ void prefill_tc_body(const PrefillTcParams &p, int bx
               if (i0 + 1 >= nvis) pk.y = 0.f;
             }
             if constexpr (kSplit) {
-              // bf16 cache: hi = p truncated to bf16, lo = p - hi (exact in fp32) truncated to
-              // bf16; hi + lo is within 2^-15 of p, and the denominator sums p itself
-              const uint32_t h0 = __float_as_uint(pk.x) & 0xffff0000u, h1 = __float_as_uint(pk.y) & 0xffff0000u;
-              w[k] = pack_hi_halves(h0, h1);
-              const float2 lo = ffma2(make_float2(__uint_as_float(h0), __uint_as_float(h1)),
+              // bf16 cache: hi = p rounded to bf16, lo = p - hi (exact in fp32) rounded to
+              // bf16, both by the conversion pipe; hi + lo is within 2^-16 of p, and the
+              // denominator sums p itself
+              uint32_t hw, lw2;
+              asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(hw) : "f"(pk.y), "f"(pk.x));
+              w[k] = hw;
+              const float2 lo = ffma2(make_float2(__uint_as_float(hw << 16), __uint_as_float(hw & 0xffff0000u)),
                                       make_float2(-1.f, -1.f), pk);
-              wl[k] = pack_hi_halves(__float_as_uint(lo.x), __float_as_uint(lo.y));
+              asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(lw2) : "f"(lo.y), "f"(lo.x));
+              wl[k] = lw2;
               lacc[k & 3] = ffma2(pk, ones, lacc[k & 3]);
             } else {
               // f16 P (p <= 2^8), rounded to nearest even; the denominator sums the rounded P
