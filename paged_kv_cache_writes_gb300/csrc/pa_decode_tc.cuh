@@ -151,12 +151,18 @@ struct Roles {
   static constexpr int kMmaWarp = 5;
   static constexpr int kSchedWarp = 6;
   static constexpr int kMergeWarp = 7;
-  static constexpr int kLoadWarp1 = 8;   // loaders 1 .. NL-1
-  // Loader warps of the decode launch: nine to twelve warps leave 168
-  // registers per thread (three warps on one of the SM's four register
-  // files), too few for the softmax of 16 heads, which keeps one loader.
+  static constexpr int kLoadWarp1 = 8;   // loaders 1 .. NL-1, then (kSepMerge) the merging warp
+  // Loader warps of the decode launch, and whether a separate warp merges the
+  // split rows (the merge warp then only counts its CTA's reports): nine to
+  // twelve warps leave 168 registers per thread (three warps on one of the
+  // SM's four register files), too few for the softmax of 16 heads, which
+  // keeps one loader and one merge warp.
   static constexpr int loaders(int g) { return g <= 8 ? 4 : 1; }
-  static constexpr int threads_for(int nl) { return (nl > 1 ? kLoadWarp1 + nl - 1 : kLoadWarp1) * 32; }
+  static constexpr bool sep_merge(int g) { return g <= 8; }
+  static constexpr int merge2_warp(int nl) { return kLoadWarp1 + nl - 1; }
+  static constexpr int threads_for(int nl, bool sep = false) {
+    return (kLoadWarp1 + (nl > 1 ? nl - 1 : 0) + (sep ? 1 : 0)) * 32;
+  }
 };
 
 constexpr int kMaxSlots = 12;
@@ -337,7 +343,7 @@ __device__ __forceinline__ int32_t query_scale_bits(float amax) {
 // The decode CTA, for decode_tc_kernel and for the decode CTAs of the mixed
 // kernel (pa_mixed_tc.cuh).  Warps past the eight roles (a wider mixed block)
 // only take part in the two CTA-wide barriers.
-template <typename KV, typename QT, int G, int D = 128, int NL = 1>
+template <typename KV, typename QT, int G, int D = 128, int NL = 1, bool kSepMerge = false>
 __device__ __forceinline__ void decode_tc_body(const DecodeTcParams &tp, const CUtensorMap *tmap_k,
                                                const CUtensorMap *tmap_v) {
   using namespace tc;
@@ -346,7 +352,8 @@ __device__ __forceinline__ void decode_tc_body(const DecodeTcParams &tp, const C
   constexpr bool kFp8 = std::is_same<KV, uint8_t>::value;
   constexpr int kLoadWarp = Roles::kLoadWarp, kMmaWarp = Roles::kMmaWarp;
   constexpr int kSchedWarp = Roles::kSchedWarp, kMergeWarp = Roles::kMergeWarp;
-  constexpr int kThreads = Roles::threads_for(NL), kLoadWarp1 = Roles::kLoadWarp1;
+  constexpr int kThreads = Roles::threads_for(NL, kSepMerge), kLoadWarp1 = Roles::kLoadWarp1;
+  constexpr int kMerge2Warp = Roles::merge2_warp(NL);   // with kSepMerge: merges only
   // MMA operands: the cache's type (bf16 / f16 with a 16-bit cache, the queries
   // in the same type; e4m3 with an fp8 cache, the queries and P as two e4m3 terms)
   constexpr bool kBf16 = std::is_same<QT, __nv_bfloat16>::value && !kFp8;
@@ -1006,9 +1013,12 @@ __device__ __forceinline__ void decode_tc_body(const DecodeTcParams &tp, const C
     //  * records of the merge list, claimed in the order they were appended and
     //    merged (merge_job), so every CTA's merge warp shares the merging.
     // Waiting without progress on either is bounded (PA_ERR_TIMEOUT).
+    // With kSepMerge another warp merges from the start, and this one only
+    // counts: a merge (one or more dependent L2 round trips, several µs under
+    // the decode's memory load) no longer delays the appends behind it.
     const int total_jobs = __ldcg(&p.hdr->pad[2]);
     int nrep = 0, t = -1;
-    bool local_done = false, list_done = false;
+    bool local_done = false, list_done = kSepMerge;
     uint64_t t_idle = global_timer_ns();
     for (;;) {
       if (*abort_flag) break;
@@ -1070,6 +1080,10 @@ __device__ __forceinline__ void decode_tc_body(const DecodeTcParams &tp, const C
       t = -1;
       t_idle = global_timer_ns();
     }
+    if constexpr (kSepMerge) drain();
+  } else if (kSepMerge && warp == kMerge2Warp) {
+    // ===================================================== merging (kSepMerge)
+    drain();
   } else if (warp == kMmaWarp) {
     // ===================================================== MMA issue
     // The whole warp runs the schedule (descriptors stay warp-uniform); one
@@ -1236,10 +1250,10 @@ __device__ __forceinline__ void decode_tc_body(const DecodeTcParams &tp, const C
 }
 
 template <typename KV, typename QT, int G, int D>
-__global__ void __launch_bounds__(dtc::Roles::threads_for(dtc::Roles::loaders(G)), 1)
+__global__ void __launch_bounds__(dtc::Roles::threads_for(dtc::Roles::loaders(G), dtc::Roles::sep_merge(G)), 1)
     decode_tc_kernel(const DecodeTcParams tp, const __grid_constant__ CUtensorMap tmap_k,
                      const __grid_constant__ CUtensorMap tmap_v) {
-  decode_tc_body<KV, QT, G, D, dtc::Roles::loaders(G)>(tp, &tmap_k, &tmap_v);
+  decode_tc_body<KV, QT, G, D, dtc::Roles::loaders(G), dtc::Roles::sep_merge(G)>(tp, &tmap_k, &tmap_v);
 }
 
 // One CTA: count the split rows' merges and clear the merge list, and list
@@ -1313,7 +1327,7 @@ cudaError_t launch_decode_tc_one(const DecodeTcParams &p, const PoolMaps &m, cud
   // programmatic dependent launch: the decode grid's set-up overlaps the plan kernel
   cudaLaunchConfig_t cfg{};
   cfg.gridDim = dim3((unsigned)sms);
-  cfg.blockDim = dim3(dtc::Roles::threads_for(dtc::Roles::loaders(G)));
+  cfg.blockDim = dim3(dtc::Roles::threads_for(dtc::Roles::loaders(G), dtc::Roles::sep_merge(G)));
   cfg.dynamicSmemBytes = smem;
   cfg.stream = s;
   cudaLaunchAttribute attr[1];
