@@ -70,9 +70,8 @@
 //    a 16-bit cache, 16 KB for fp8).  Loader 0 also stages Q^T (16-bit
 //    caches, cp.async).  One warp issuing the copies of 4 KB blocks one
 //    after another streamed at most ~21 bytes per SM clock, so the decode
-//    launch has four loaders (two in the mixed launch, whose block has nine
-//    warps; one with 16 query heads per KV head, whose softmax needs more
-//    registers than nine or more warps leave);
+//    and mixed launches have four loaders (one with 16 query heads per KV
+//    head, whose softmax needs more registers than nine or more warps leave);
 //  * MMA warp (one elected lane issues): S^T of unit u, then O^T of unit
 //    u-1, whose softmax ran while the scores of u were computed;
 //  * scheduler warp: claims units two at a time and publishes each, with

@@ -18,7 +18,8 @@
 // plan kernel (programmatic launch); the prefill CTAs do not.
 //
 // One CTA per SM (either body uses most of shared memory); the block is the
-// prefill CTA's 288 threads: the decode body's nine warps, with two loaders.
+// decode body's twelve warps (four loaders, a merging warp), of which a
+// prefill CTA uses the first nine.
 #pragma once
 
 #include "pa_decode_tc.cuh"
@@ -26,15 +27,19 @@
 
 namespace pa {
 
+// The block is the decode body's twelve warps (four loaders, a merging warp);
+// a prefill CTA's body uses its first nine and the rest have no role.
+constexpr int kMixedThreads = dtc::Roles::threads_for(4, true);
+
 template <typename KV, typename QT, int G>
-__global__ void __launch_bounds__(tc::Roles<1>::kThreads, 1)
+__global__ void __launch_bounds__(kMixedThreads, 1)
     mixed_tc_kernel(const DecodeTcParams tp, const __grid_constant__ CUtensorMap tmap_k,
                     const __grid_constant__ CUtensorMap tmap_v, const PrefillTcParams pp, int prefill_ctas,
                     int prefill_x) {
-  static_assert(tc::Roles<1>::kThreads == dtc::Roles::threads_for(2), "two decode loaders fill the block");
+  static_assert(kMixedThreads >= tc::Roles<1>::kThreads, "the prefill roles fit in the block");
   const int b = blockIdx.x;   // block-uniform: every barrier of a body is reached by its whole block
   if (b < prefill_ctas) prefill_tc_body<KV, QT, G, 1>(pp, b % prefill_x, b / prefill_x, &tmap_k, &tmap_v);
-  else decode_tc_body<KV, QT, G, 128, 2>(tp, &tmap_k, &tmap_v);
+  else decode_tc_body<KV, QT, G, 128, 4, true>(tp, &tmap_k, &tmap_v);
 }
 
 // Host launcher: the decode's plan kernel, then the mixed grid as its
@@ -61,7 +66,7 @@ cudaError_t launch_mixed_tc_one(const DecodeTcParams &tp, const PoolMaps &m, con
   if ((e = ensure_smem_limit<mixed_tc_kernel<KV, QT, G>>(smem)) != cudaSuccess) return e;
   cudaLaunchConfig_t cfg{};
   cfg.gridDim = dim3((unsigned)(pctas + sms));
-  cfg.blockDim = dim3(tc::Roles<1>::kThreads);
+  cfg.blockDim = dim3(kMixedThreads);
   cfg.dynamicSmemBytes = smem;
   cfg.stream = s;
   cudaLaunchAttribute attr[1];

@@ -638,8 +638,9 @@ __device__ __forceinline__ void prefill_tc_body(const PrefillTcParams &p, int bx
       }
     }
     if constexpr (!kFp8) cp_async_wait_all();
-  } else {
-    // ===================================================== MMA issue (last warp)
+  } else if (warp == kMmaWarp) {
+    // ===================================================== MMA issue (warp kMmaWarp; warps
+    // past it, in a larger block such as the mixed launch's, have no role)
     // The whole warp runs the schedule (so descriptors stay warp-uniform); one
     // elected lane issues the MMAs and their commits.  Per key tile j and Q
     // tile t: O_t += P_t(j) V_j, then -- once that P.V is complete, because
