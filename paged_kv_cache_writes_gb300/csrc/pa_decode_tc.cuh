@@ -533,7 +533,7 @@ __device__ __forceinline__ void decode_tc_body(const DecodeTcParams &tp, const C
             *abort_flag = 1;
             break;
           }
-          __nanosleep(500);
+          __nanosleep(128);   // a short poll: the record's merge is on the kernel's tail
         }
       }
       if (!__shfl_sync(0xffffffffu, word != 0, 0)) return;
