@@ -443,6 +443,8 @@ __device__ __forceinline__ void decode_tc_body(const DecodeTcParams &tp, const C
   // launched as the plan kernel's programmatic dependent: everything above overlapped it;
   // its work list, cursor and counters are complete and visible after this
   asm volatile("griddepcontrol.wait;" ::: "memory");
+  // the next step's plan kernel may launch (it waits for this grid before it starts its work)
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   auto col_s = [&](int b, int j) { return tmem + (uint32_t)((b * kMaxTiles + j) * kNS); };
   auto col_o = [&](int b) { return tmem + (uint32_t)(GE::kColO + b * kNO); };
   auto wait_all = [&](uint64_t *bar, uint32_t parity) {
@@ -1269,6 +1271,10 @@ __global__ void __launch_bounds__(dtc::Roles::threads_for(dtc::Roles::loaders(G)
 // the CTAs' finishing times.  An empty row lists one item of zero tokens.
 template <int kUnused>
 __global__ void __launch_bounds__(1024) decode_tc_plan_kernel(DecodeParams p, DecodeMergeJob *jobs) {
+  // launched as a programmatic dependent of what precedes it on the stream
+  // (the previous step's decode among others): its launch overlaps that grid's
+  // end, and nothing of the workspace is touched before that grid is complete
+  asm volatile("griddepcontrol.wait;" ::: "memory");
   // the decode grid may launch now: it sets itself up, then waits for this grid
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   // sort key 0 .. maxp + 3: 3 + nparts for a split row, else its tiles (0 .. 4);
@@ -1316,13 +1322,29 @@ __global__ void __launch_bounds__(1024) decode_tc_plan_kernel(DecodeParams p, De
 
 // Host launcher: the plan kernel, then one persistent CTA per SM launched as its
 // programmatic dependent.
+// The plan kernel, launched as a programmatic dependent of the stream's
+// previous work (it waits for that work before touching anything).
+template <int kUnused = 0>
+cudaError_t launch_decode_tc_plan(const DecodeParams &d, DecodeMergeJob *jobs, cudaStream_t s) {
+  cudaLaunchConfig_t cfg{};
+  cfg.gridDim = dim3(1);
+  cfg.blockDim = dim3(1024);
+  cfg.dynamicSmemBytes = 0;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, decode_tc_plan_kernel<0>, d, jobs);
+}
+
 template <typename KV, typename QT, int G, int D>
 cudaError_t launch_decode_tc_one(const DecodeTcParams &p, const PoolMaps &m, cudaStream_t s) {
   constexpr bool kSplit = std::is_same<QT, __nv_bfloat16>::value && !std::is_same<KV, uint8_t>::value;
   constexpr int smem =
       dtc::TcGeo<G, kSplit, std::is_same<KV, uint8_t>::value, dtc::QTerms<KV, QT>::value, D>::kSmemBytes;
-  decode_tc_plan_kernel<0><<<1, 1024, 0, s>>>(p.d, p.jobs);
-  cudaError_t e = cudaGetLastError();
+  cudaError_t e = launch_decode_tc_plan(p.d, p.jobs, s);
   if (e != cudaSuccess) return e;
   if ((e = ensure_smem_limit<decode_tc_kernel<KV, QT, G, D>>(smem)) != cudaSuccess) return e;
   int sms = 0;

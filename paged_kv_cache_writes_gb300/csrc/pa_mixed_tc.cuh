@@ -61,8 +61,7 @@ cudaError_t launch_mixed_tc_one(const DecodeTcParams &tp, const PoolMaps &m, con
   cudaError_t e = current_sm_count(&sms);
   if (e != cudaSuccess) return e;
   if (pctas + sms > 2147483647ll) return cudaErrorInvalidValue;
-  decode_tc_plan_kernel<0><<<1, 1024, 0, s>>>(tp.d, tp.jobs);
-  if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  if ((e = launch_decode_tc_plan(tp.d, tp.jobs, s)) != cudaSuccess) return e;
   if ((e = ensure_smem_limit<mixed_tc_kernel<KV, QT, G>>(smem)) != cudaSuccess) return e;
   cudaLaunchConfig_t cfg{};
   cfg.gridDim = dim3((unsigned)(pctas + sms));
