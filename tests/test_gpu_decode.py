@@ -123,6 +123,35 @@ def test_workspace_contents_ignored_and_reusable():
         assert torch.equal(dev.out.view(torch.int32), first.view(torch.int32))
 
 
+@pytest.mark.parametrize("kv", ["bf16", "fp8"])
+def test_back_to_back_calls_share_one_workspace(kv):
+    """Calls on one stream, with no synchronisation between them, may share a
+    workspace: each call's plan kernel waits for the stream's previous decode
+    before rebuilding the work list (it is launched as a programmatic
+    dependent, so it starts while that decode finishes).  Two different
+    batches, alternated three times, each checked against the oracle."""
+    a = W.decode_batch("bb-a", [3000, 100, 2500, 0, 17, 4100, 777], 64, 8, 128, 32, "bf16", kv_dtype=kv, seed=61,
+                       partition_size=512)
+    c = W.decode_batch("bb-c", [64, 5000, 1, 2049, 900], 64, 8, 128, 32, "bf16", kv_dtype=kv, seed=62,
+                       partition_size=512)
+    da, dc = run_gpu(a), run_gpu(c)
+    shared = torch.zeros(max(da.workspace.numel(), dc.workspace.numel()), dtype=da.workspace.dtype,
+                         device=da.workspace.device)
+    da.workspace = shared[: da.workspace.numel()]
+    dc.workspace = shared[: dc.workspace.numel()]
+    for d in (da, dc):
+        d.out.fill_(float("nan"))
+    for _ in range(3):
+        da.decode()
+        dc.decode()
+    torch.cuda.synchronize()
+    assert pa.pa_get_device_error() == 0
+    for b, d in ((a, da), (c, dc)):
+        kp, vp = oracle_pools(b)
+        ref = oracle.decode_batch(b, kp, vp)
+        assert max_err(d.out, ref) <= TOL[kv]
+
+
 @pytest.mark.parametrize("kv", ["bf16", "f16"])
 @pytest.mark.parametrize("hq,hkv", [(64, 8), (128, 16)])
 def test_head_dim_64_batch_both_kernels(kv, hq, hkv):
