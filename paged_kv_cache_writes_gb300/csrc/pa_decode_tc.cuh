@@ -1370,7 +1370,13 @@ cudaError_t launch_decode_tc_one(const DecodeTcParams &p, const PoolMaps &m, cud
 template <typename KV, typename QT>
 cudaError_t launch_decode_tc(const DecodeTcParams &p, int gqa, int head_dim, const PoolMaps &m, cudaStream_t s) {
   if constexpr (!std::is_same<KV, uint8_t>::value) {
-    if (head_dim == 64) return gqa == 8 ? launch_decode_tc_one<KV, QT, 8, 64>(p, m, s) : cudaErrorInvalidValue;
+    if (head_dim == 64) {
+      switch (gqa) {
+        case 4: return launch_decode_tc_one<KV, QT, 4, 64>(p, m, s);
+        case 8: return launch_decode_tc_one<KV, QT, 8, 64>(p, m, s);
+        default: return cudaErrorInvalidValue;
+      }
+    }
   }
   if (head_dim != 128) return cudaErrorInvalidValue;
   switch (gqa) {

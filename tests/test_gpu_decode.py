@@ -2,7 +2,7 @@
 
 Two kernels serve pa_decode: the tensor-core one (chosen by default for
 head_dim 128 with 4, 8 or 16 query heads per KV head, and for head_dim 64
-with a 16-bit cache and 8) and the CUDA-core one (every other shape, or
+with a 16-bit cache and 4 or 8) and the CUDA-core one (every other shape, or
 every shape once selected with pa_set_decode_kernel); both are checked here.
 
 Tolerance (max abs error): 2e-3 for f16/bf16 caches, 2e-2 for an fp8-e4m3
@@ -153,7 +153,7 @@ def test_back_to_back_calls_share_one_workspace(kv):
 
 
 @pytest.mark.parametrize("kv", ["bf16", "f16"])
-@pytest.mark.parametrize("hq,hkv", [(64, 8), (128, 16)])
+@pytest.mark.parametrize("hq,hkv", [(32, 8), (64, 8), (128, 16)])
 def test_head_dim_64_batch_both_kernels(kv, hq, hkv):
     # a bandwidth-sized head_dim-64 batch (128 sequences of 512..4096 tokens): the tensor-core
     # kernel against the oracle in full, and against the CUDA-core kernel
