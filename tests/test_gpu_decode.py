@@ -166,6 +166,12 @@ def test_head_dim_64_batch_both_kernels(kv, hq, hkv):
     assert (tc_out - cc.out).abs().max().item() <= 2 * TOL[kv]
 
 
+@pytest.mark.parametrize("hq", [32, 64])
+def test_head_dim_64_layer_full(hq):
+    # the benchmark's head_dim-64 decode layers (256 sequences): every row and element
+    _check(W.cfg_d64(num_q_heads=hq))
+
+
 def test_llama8b_full():
     _check(W.cfg_llama8b())
 

@@ -469,6 +469,16 @@ def cfg_llama70b(seed: int = 2, batch: int = 256, kv_dtype: str = "bf16", fp8_sc
                         fp8_scales=fp8_scales)
 
 
+def cfg_d64(seed: int = 6, batch: int = 256, num_q_heads: int = 32, kv_dtype: str = "bf16") -> PagedBatch:
+    """head_dim-64 decode layer: num_q_heads/8 heads (32/8: 4 query heads per KV
+    head, 64/8: 8), block 16, bf16, lengths uniform 512..4096, split-KV 512,
+    40k-block pool."""
+    lens = np.random.default_rng(seed + 100).integers(512, 4097, size=batch)
+    name = f"head_dim-64 decode layer, {num_q_heads}/8 heads" + _fp8_name(kv_dtype, "tensor")
+    return decode_batch(name, lens, num_q_heads, 8, 64, 16, "bf16", kv_dtype=kv_dtype, seed=seed, num_blocks=40000,
+                        partition_size=512)
+
+
 def cfg_shared_prefix(seed: int = 3, num_prompts: int = 32) -> PagedBatch:
     return shared_prefix_batch(num_prompts=num_prompts, seed=seed)
 
