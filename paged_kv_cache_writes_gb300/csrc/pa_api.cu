@@ -125,18 +125,20 @@ bool encode_pool_map_atoms(CUtensorMap *map, const void *base, const pa_kv_cache
              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-// An fp8 pool (128-byte rows) as a 2D tensor [rows][128 codes]; one box is a
-// whole cache block of one KV head (block_size rows), 128-byte swizzle.
+// An fp8 pool as a 2D tensor [rows][head_dim codes]; one box is a whole
+// cache block of one KV head (block_size rows), with the 128-byte swizzle
+// (head_dim 128) or the 64-byte one (head_dim 64).
 bool encode_pool_map_fp8_blocks(CUtensorMap *map, const void *base, const pa_kv_cache &c) {
   auto enc = tensor_map_encoder();
-  if (!enc || c.head_dim != 128 || c.kv_dtype != PA_FP8_E4M3) return false;
-  const cuuint64_t dims[2] = {128, (cuuint64_t)c.num_blocks * c.num_kv_heads * c.block_size};
-  const cuuint64_t strides[1] = {128};
-  const cuuint32_t box[2] = {128, (cuuint32_t)c.block_size};
+  if (!enc || (c.head_dim != 128 && c.head_dim != 64) || c.kv_dtype != PA_FP8_E4M3) return false;
+  const cuuint64_t d = (cuuint64_t)c.head_dim;
+  const cuuint64_t dims[2] = {d, (cuuint64_t)c.num_blocks * c.num_kv_heads * c.block_size};
+  const cuuint64_t strides[1] = {d};
+  const cuuint32_t box[2] = {(cuuint32_t)d, (cuuint32_t)c.block_size};
   const cuuint32_t estr[2] = {1u, 1u};
   return enc(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void *>(base), dims, strides, box, estr,
-             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+             CU_TENSOR_MAP_INTERLEAVE_NONE, d == 128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B,
+             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
 // One pool as a 2D tensor [num_blocks*Hkv*bs rows][head_dim]; box = 16 rows x

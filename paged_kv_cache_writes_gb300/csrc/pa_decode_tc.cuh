@@ -185,14 +185,16 @@ struct QTerms {
 // Shared-memory and tensor-memory geometry.  16-bit caches: K/V tiles of
 // 32 KB (two 128-byte panels per 8-key atom), Q^T of 16 rows (the heads,
 // padded) and P^T of kNO rows, each in two 64-element panels.  fp8 caches:
-// tiles of 16 KB (128 rows of 128 codes, the layout a 2D bulk-tensor box
-// with 128-byte swizzle writes), Q^T and P^T of one 128-element panel
-// holding the hi terms in rows 0..G-1, the lo terms in rows G..2G-1 (and
-// with three query terms, the last in rows 2G..3G-1 of Q^T).
+// tiles of 128 rows of head_dim codes (16 KB with the 128-byte swizzle, or 8
+// KB of 64-byte rows with the 64-byte swizzle for head_dim 64: the layouts a
+// 2D bulk-tensor box writes), Q^T of head_dim-byte rows in the same swizzle
+// and P^T of one 128-key panel, holding the hi terms in rows 0..G-1, the lo
+// terms in rows G..2G-1 (and with three query terms, the last in rows
+// 2G..3G-1 of Q^T).
 template <int G, bool kSplit, bool kFp8, int kQTerms = 1, int D = 128>
 struct TcGeo {
   static_assert(G == 4 || G == 8 || G == 16, "4, 8 or 16 query heads per KV head");
-  static_assert(D == 128 || (D == 64 && !kFp8), "head_dim 128, or 64 with a 16-bit cache");
+  static_assert(D == 128 || D == 64, "head_dim 128 or 64");
   static constexpr int kPanels = D / 64;                            // 128-byte panels of a 16-bit row
   static constexpr int kAtom = 8 * 2 * D;                           // 8 keys of a 16-bit tile (all panels)
   static constexpr int kPRows = (kSplit || kFp8) ? 2 * G : G;       // P^T rows in use
@@ -200,7 +202,7 @@ struct TcGeo {
   static constexpr int kQRows = kQTerms * G;                        // Q^T rows in use
   static constexpr int kNS = kQRows <= 16 ? 16 : (kQRows + 15) / 16 * 16;   // S^T columns per tile (MMA N)
   static constexpr int kSCols = kFp8 ? kNS : G;                     // S^T columns read per tile
-  static constexpr int kQBytes = kFp8 ? kNS * 128 : kPanels * kNS * 128;  // Q^T of a unit
+  static constexpr int kQBytes = kFp8 ? kNS * D : kPanels * kNS * 128;    // Q^T of a unit
   // Q^T buffers: fp8, one per unit descriptor (written by the scheduler warp
   // with the descriptor); 16-bit, two (copied by the loader per unit parity)
   static constexpr int kQBufs = kFp8 ? kInfo : 2;
@@ -863,7 +865,7 @@ __device__ __forceinline__ void decode_tc_body(const DecodeTcParams &tp, const C
         if (c < kD / 8)   // head_dim 64: 8 chunks per row
           *reinterpret_cast<uint4 *>(static_cast<QT *>(const_cast<void *>(side ? tp.v_cache : tp.k_cache)) +
                                      crow * kD + c * 8) = x;
-      } else {
+      } else if (c < kD / 8) {   // head_dim 64: 8 chunks per row
         const uint32_t w[4] = {x.x, x.y, x.z, x.w};
         uint32_t o[2];
 #pragma unroll
@@ -930,12 +932,19 @@ __device__ __forceinline__ void decode_tc_body(const DecodeTcParams &tp, const C
         if constexpr (kFp8) {
           // Q^T of the unit, in the buffer of its descriptor (free: the descriptor's
           // last reader released it): q 2^e = hi + lo / 16; elements d .. d+7 of
-          // head h are bytes d .. d+7 of rows h and G + h
-          uint4 qw[G / 2];
+          // head h are bytes d .. d+7 of rows h and G + h (rows of kD bytes,
+          // 16-byte chunk c of row r at chunk c ^ (r & 7) with kD 128, or
+          // c ^ ((r >> 1) & 3) with kD 64: the 128- and 64-byte swizzles)
+          constexpr int kQIt = G * kD / 256;   // 16-byte query chunks per lane
+          constexpr int kCPH = kD / 8;         // chunks per head
+          auto qoff = [](int r, int c16) {
+            return kD == 128 ? r * 128 + (((c16 >> 1) ^ (r & 7)) << 4) : r * 64 + (((c16 >> 1) ^ ((r >> 1) & 3)) << 4);
+          };
+          uint4 qw[kQIt];
           float amax = 0.f;
           const char *q0 = static_cast<const char *>(p.q) + ((int64_t)rk * hq + (int64_t)kvk * G) * kD * 2;
 #pragma unroll
-          for (int i = 0; i < G / 2; ++i) {
+          for (int i = 0; i < kQIt; ++i) {
             qw[i] = vk ? ld_nc16(q0 + (lane + 32 * i) * 16) : make_uint4(0, 0, 0, 0);
             amax = fmaxf(amax, absmax8(qw[i], QT{}));
           }
@@ -946,8 +955,8 @@ __device__ __forceinline__ void decode_tc_body(const DecodeTcParams &tp, const C
             const float qs = __int_as_float(qscale);
             uint8_t *qb = smem + GE::kOffQ + ((u + k) % kInfo) * GE::kQBytes;
 #pragma unroll
-            for (int i = 0; i < G / 2; ++i) {
-              const int e = lane + 32 * i, h = e >> 4, c16 = e & 15, lr = G + h, half = (c16 & 1) * 8;
+            for (int i = 0; i < kQIt; ++i) {
+              const int e = lane + 32 * i, h = e / kCPH, c16 = e % kCPH, lr = G + h, half = (c16 & 1) * 8;
               const uint32_t ws[4] = {qw[i].x, qw[i].y, qw[i].z, qw[i].w};
               uint32_t hi[4], lo[4], lo2[4];
 #pragma unroll
@@ -956,13 +965,11 @@ __device__ __forceinline__ void decode_tc_body(const DecodeTcParams &tp, const C
                 if constexpr (kQTerms == 3) split3_e4m3(make_float2(f.x * qs, f.y * qs), hi[c], lo[c], lo2[c]);
                 else split2_e4m3(make_float2(f.x * qs, f.y * qs), hi[c], lo[c]);
               }
-              *reinterpret_cast<uint2 *>(qb + h * 128 + (((c16 >> 1) ^ (h & 7)) << 4) + half) =
-                  make_uint2(hi[0] | (hi[1] << 16), hi[2] | (hi[3] << 16));
-              *reinterpret_cast<uint2 *>(qb + lr * 128 + (((c16 >> 1) ^ (lr & 7)) << 4) + half) =
-                  make_uint2(lo[0] | (lo[1] << 16), lo[2] | (lo[3] << 16));
+              *reinterpret_cast<uint2 *>(qb + qoff(h, c16) + half) = make_uint2(hi[0] | (hi[1] << 16), hi[2] | (hi[3] << 16));
+              *reinterpret_cast<uint2 *>(qb + qoff(lr, c16) + half) = make_uint2(lo[0] | (lo[1] << 16), lo[2] | (lo[3] << 16));
               if constexpr (kQTerms == 3) {
                 const int r3 = 2 * G + h;
-                *reinterpret_cast<uint2 *>(qb + r3 * 128 + (((c16 >> 1) ^ (r3 & 7)) << 4) + half) =
+                *reinterpret_cast<uint2 *>(qb + qoff(r3, c16) + half) =
                     make_uint2(lo2[0] | (lo2[1] << 16), lo2[2] | (lo2[3] << 16));
               }
             }
@@ -1109,9 +1116,14 @@ __device__ __forceinline__ void decode_tc_body(const DecodeTcParams &tp, const C
     // so the 14-bit field never carries).  One thread issues every MMA, and each
     // instruction on its path delays the next issue.
     auto dofs = [](uint32_t bytes) { return (uint64_t)(bytes >> 4); };
-    const uint64_t kdesc0 = kFp8 ? umma_desc(ring, 16) : umma_desc_sbo(ring, 16, kAtomB);
-    const uint64_t vdesc0 = kFp8 ? umma_desc_sbo(ring, 1024, 1024) : umma_desc_sbo(ring, kD == 128 ? 1024 : 0, kAtomB);
-    const uint64_t qdesc0 = umma_desc(qbuf, 16), pdesc0 = umma_desc(pbuf, 16);
+    // fp8 with head_dim 64: K, V and Q^T in 64-byte rows (64-byte swizzle, 8-row groups 512 B
+    // apart); V^T's second 64-element half of M repeats the first (LBO 0), as with 16-bit V
+    constexpr bool kSw64 = kFp8 && kD == 64;
+    const uint64_t kdesc0 = kSw64 ? umma_desc_sw64(ring, 16, 512) : kFp8 ? umma_desc(ring, 16) : umma_desc_sbo(ring, 16, kAtomB);
+    const uint64_t vdesc0 = kSw64  ? umma_desc_sw64(ring, 0, 512)
+                            : kFp8 ? umma_desc_sbo(ring, 1024, 1024)
+                                   : umma_desc_sbo(ring, kD == 128 ? 1024 : 0, kAtomB);
+    const uint64_t qdesc0 = kSw64 ? umma_desc_sw64(qbuf, 16, 512) : umma_desc(qbuf, 16), pdesc0 = umma_desc(pbuf, 16);
     uint32_t g_cons = 0;   // tiles consumed, in the ring's order
     bool ok = true, issued = false;
     UnitHdr prev;
@@ -1142,7 +1154,7 @@ __device__ __forceinline__ void decode_tc_body(const DecodeTcParams &tp, const C
             const uint64_t kd = kdesc0 + dofs(slot * GE::kSlotBytes), qd = qdesc0 + dofs((kFp8 ? ib : b) * GE::kQBytes);
             const uint32_t dcol = col_s(b, j);
             if constexpr (kFp8) {
-              // 32 elements (32 B of each 128-byte row) per MMA; 8-row groups 1024 B apart
+              // 32 elements (32 B of each kD-byte row) per MMA
 #pragma unroll
               for (int k = 0; k < kD / 32; ++k) mma(dcol, kd + dofs(k * 32), qd + dofs(k * 32), idesc_s, k > 0 ? 1u : 0u);
             } else {
@@ -1188,8 +1200,9 @@ __device__ __forceinline__ void decode_tc_body(const DecodeTcParams &tp, const C
           uint8_t *vt = smem + GE::kOffRing + slot * GE::kSlotBytes;
           if (nvalid % kGroup) {
             if constexpr (kFp8) {
-              for (int e = lane; e < (kGroup * ngroups - nvalid) * 8; e += 32)   // rows of 128 B
-                *reinterpret_cast<uint4 *>(vt + (nvalid + (e >> 3)) * 128 + (e & 7) * 16) = make_uint4(0, 0, 0, 0);
+              constexpr int kRowC = kD / 16;   // 16-byte chunks of a kD-byte row
+              for (int e = lane; e < (kGroup * ngroups - nvalid) * kRowC; e += 32)
+                *reinterpret_cast<uint4 *>(vt + (nvalid + e / kRowC) * kD + (e % kRowC) * 16) = make_uint4(0, 0, 0, 0);
             } else {
               for (int e = lane; e < (kGroup * ngroups - nvalid) * kRowChunks; e += 32) {
                 const int r = nvalid + e / kRowChunks, c = e % kRowChunks;   // row, 16-byte chunk of it
@@ -1207,10 +1220,10 @@ __device__ __forceinline__ void decode_tc_body(const DecodeTcParams &tp, const C
             const uint32_t dcol = col_o(bp), acc0 = j > 0 ? 1u : 0u;
             // unrolled over a whole tile's key groups, the tail's predicated off
             if constexpr (kFp8) {
-              // V^T: one 128-element MN panel, 8-key groups 1024 B apart, 32 keys per MMA
+              // V^T: one kD-element MN panel, 8-key groups 8 kD bytes apart, 32 keys per MMA
 #pragma unroll
               for (int kk = 0; kk < kKeys / 32; ++kk)
-                if (kk < ngroups) mma(dcol, vd + dofs(kk * 4096), pd + dofs(kk * 32), idesc_o, kk > 0 ? 1u : acc0);
+                if (kk < ngroups) mma(dcol, vd + dofs(kk * 32 * kD), pd + dofs(kk * 32), idesc_o, kk > 0 ? 1u : acc0);
             } else {
               // M = 128 elements of V^T in two 64-element halves (LBO apart): panels 0 and 1,
               // or panel 0 twice with head_dim 64 (lanes 64..127 of O^T then repeat 0..63)
@@ -1369,13 +1382,11 @@ cudaError_t launch_decode_tc_one(const DecodeTcParams &p, const PoolMaps &m, cud
 // (128-byte swizzle).
 template <typename KV, typename QT>
 cudaError_t launch_decode_tc(const DecodeTcParams &p, int gqa, int head_dim, const PoolMaps &m, cudaStream_t s) {
-  if constexpr (!std::is_same<KV, uint8_t>::value) {
-    if (head_dim == 64) {
-      switch (gqa) {
-        case 4: return launch_decode_tc_one<KV, QT, 4, 64>(p, m, s);
-        case 8: return launch_decode_tc_one<KV, QT, 8, 64>(p, m, s);
-        default: return cudaErrorInvalidValue;
-      }
+  if (head_dim == 64) {
+    switch (gqa) {
+      case 4: return launch_decode_tc_one<KV, QT, 4, 64>(p, m, s);
+      case 8: return launch_decode_tc_one<KV, QT, 8, 64>(p, m, s);
+      default: return cudaErrorInvalidValue;
     }
   }
   if (head_dim != 128) return cudaErrorInvalidValue;

@@ -130,10 +130,9 @@ cudaError_t launch_decode_fp8_f16q(const DecodeParams &p, int hpc, const PoolMap
                                    cudaStream_t s);
 
 // Tensor-core decode: head_dim 128 with gqa = Hq / Hkv in {4, 8, 16}, or head_dim 64
-// with a 16-bit cache and gqa in {4, 8}.
-constexpr bool decode_tc_supported(int head_dim, int gqa, pa_dtype kv) {
-  return (head_dim == 128 && (gqa == 4 || gqa == 8 || gqa == 16)) ||
-         (head_dim == 64 && kv != PA_FP8_E4M3 && (gqa == 4 || gqa == 8));
+// with gqa in {4, 8}.
+constexpr bool decode_tc_supported(int head_dim, int gqa, pa_dtype) {
+  return (head_dim == 128 && (gqa == 4 || gqa == 8 || gqa == 16)) || (head_dim == 64 && (gqa == 4 || gqa == 8));
 }
 cudaError_t launch_decode_tc_bf16(const DecodeTcParams &p, int gqa, int head_dim, const PoolMaps &m, cudaStream_t s);
 cudaError_t launch_decode_tc_f16(const DecodeTcParams &p, int gqa, int head_dim, const PoolMaps &m, cudaStream_t s);

@@ -28,6 +28,13 @@ __device__ __forceinline__ uint64_t umma_desc_sbo(uint32_t saddr, uint32_t lbo, 
          ((uint64_t)((sbo >> 4) & 0x3FFF) << 32) | ((uint64_t)1 << 46) | ((uint64_t)2 << 61);
 }
 
+// UMMA shared-memory descriptor with the 64-byte swizzle (8 rows x 64 B per
+// 512-byte atom), for operands whose rows are 64 bytes: fp8 with head_dim 64.
+__device__ __forceinline__ uint64_t umma_desc_sw64(uint32_t saddr, uint32_t lbo, uint32_t sbo) {
+  return (uint64_t)((saddr & 0x3FFFF) >> 4) | ((uint64_t)((lbo >> 4) & 0x3FFF) << 16) |
+         ((uint64_t)((sbo >> 4) & 0x3FFF) << 32) | ((uint64_t)1 << 46) | ((uint64_t)4 << 61);
+}
+
 // Instruction descriptor, kind::f16: fp32 accumulator, A and B of the same
 // 16-bit type (1 = bf16, 0 = f16), each K-major or MN-major (transposed), M = 128.
 __device__ __forceinline__ uint32_t umma_idesc(uint32_t ab_fmt, uint32_t n, bool b_mn_major, bool a_mn_major = false) {

@@ -2,7 +2,7 @@
 
 Two kernels serve pa_decode: the tensor-core one (chosen by default for
 head_dim 128 with 4, 8 or 16 query heads per KV head, and for head_dim 64
-with a 16-bit cache and 4 or 8) and the CUDA-core one (every other shape, or
+with 4 or 8) and the CUDA-core one (every other shape, or
 every shape once selected with pa_set_decode_kernel); both are checked here.
 
 Tolerance (max abs error): 2e-3 for f16/bf16 caches, 2e-2 for an fp8-e4m3
@@ -45,7 +45,8 @@ def test_shapes_bf16(hq, hkv, d, bs):
 
 
 @pytest.mark.parametrize("kv,src", [("f16", "f16"), ("fp8", "bf16"), ("fp8", "f16")])
-@pytest.mark.parametrize("hq,hkv,d,bs", [(32, 8, 128, 16), (64, 8, 128, 32), (8, 8, 64, 16), (16, 4, 64, 32)])
+@pytest.mark.parametrize("hq,hkv,d,bs", [(32, 8, 128, 16), (64, 8, 128, 32), (8, 8, 64, 16), (16, 4, 64, 32),
+                                         (64, 8, 64, 16)])
 def test_shapes_other_dtypes(kv, src, hq, hkv, d, bs):
     _check(W.decode_batch("s", EDGE_LENS, hq, hkv, d, bs, src, kv_dtype=kv, seed=hq + d + bs, partition_size=512))
 
@@ -164,6 +165,19 @@ def test_head_dim_64_batch_both_kernels(kv, hq, hkv):
     with pa.decode_kernel("cuda_cores"):
         cc, _ = _check(b)
     assert (tc_out - cc.out).abs().max().item() <= 2 * TOL[kv]
+
+
+@pytest.mark.parametrize("q", ["bf16", "f16"])
+@pytest.mark.parametrize("hq,hkv", [(32, 8), (64, 8), (128, 16)])
+def test_head_dim_64_fp8_batch_both_kernels(q, hq, hkv):
+    # the same batch with an e4m3 cache (64-byte rows, 64-byte swizzle on the tensor-core path)
+    lens = np.random.default_rng(102).integers(512, 4097, size=128)
+    b = W.decode_batch("d64 fp8", lens, hq, hkv, 64, 16, q, kv_dtype="fp8", seed=6, partition_size=512)
+    tc, _ = _check(b)
+    tc_out = tc.out.clone()
+    with pa.decode_kernel("cuda_cores"):
+        cc, _ = _check(b)
+    assert (tc_out - cc.out).abs().max().item() <= 2 * TOL["fp8"]
 
 
 @pytest.mark.parametrize("hq", [32, 64])

@@ -51,6 +51,16 @@ def test_fused_step_head_dim_64(kernel, kv, hq, hkv, bs):
     _fused(b, kernel)
 
 
+@pytest.mark.parametrize("kernel", ["auto", "cuda_cores"])
+@pytest.mark.parametrize("q", ["bf16", "f16"])
+@pytest.mark.parametrize("hq,hkv,bs", [(32, 8, 16), (64, 8, 32)])
+def test_fused_step_head_dim_64_fp8(kernel, q, hq, hkv, bs):
+    # 64-byte cache rows: the new token's eight 8-code chunks per row, and no store past the row
+    b = W.decode_batch("fused d64 fp8", LENS, hq, hkv, 64, bs, q, kv_dtype="fp8", seed=hq + hkv + bs + 65,
+                       partition_size=512)
+    _fused(b, kernel)
+
+
 @pytest.mark.parametrize("ps", [32, 96, 0])
 def test_fused_step_partition_sizes(ps):
     b = W.decode_batch("fused ps", [1, 40, 700, 2049, 3000], 16, 2, 128, 16, "bf16", seed=51, partition_size=ps)
