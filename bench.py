@@ -769,18 +769,20 @@ def run_case(args):
         db.decode()
     fn = {"decode_write": db.decode_write, "mixed": db.mixed_attention, "mixed_two": two}.get(
         c, db.prefill_chunk if c.startswith("prefill:") else db.decode)
-    for _ in range(args.warmup):
-        fn()
-    torch.cuda.synchronize()
-    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    e0.record()
-    for _ in range(args.steps):
-        fn()
-    e1.record()
-    torch.cuda.synchronize()
+    with pa.decode_kernel(args.decode_kernel):
+        for _ in range(args.warmup):
+            fn()
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        for _ in range(args.steps):
+            fn()
+        e1.record()
+        torch.cuda.synchronize()
     assert pa.pa_get_device_error() == 0
     ms = e0.elapsed_time(e1) / args.steps
-    out = {"case": c, "workload": b.name, "ms": ms, "steps": args.steps, "warmup": args.warmup}
+    out = {"case": c, "workload": b.name, "ms": ms, "steps": args.steps, "warmup": args.warmup,
+           "decode_kernel": args.decode_kernel}
     if c.startswith("decode"):
         out["kv_bytes"] = b.decode_kv_bytes()
         out["GBps"] = b.decode_kv_bytes() / (ms * 1e-3) / 1e9
@@ -805,6 +807,8 @@ def main():
     ap.add_argument("--case", default=None,
                     help="time one kernel alone (profiling): decode_bf16, decode_fp8, decode_fp8_head, "
                          "decode_write, prefill:<key>, mixed, mixed_two")
+    ap.add_argument("--decode-kernel", choices=["auto", "cuda_cores"], default="auto",
+                    help="with --case: the decode kernel pa_set_decode_kernel selects")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
