@@ -132,7 +132,8 @@ def measure_other_decodes(dev_name: str, steps: int, warmup: int) -> dict:
              ("llama70b_fp8_cache", lambda: W.cfg_llama70b(kv_dtype="fp8")),
              ("llama70b_fp8_cache_head_scales", lambda: W.cfg_llama70b(kv_dtype="fp8", fp8_scales="head")),
              ("head_dim64_32_8", W.cfg_d64), ("head_dim64_64_8", lambda: W.cfg_d64(num_q_heads=64)),
-             ("head_dim64_64_8_fp8_cache", lambda: W.cfg_d64(num_q_heads=64, kv_dtype="fp8")))
+             ("head_dim64_64_8_fp8_cache", lambda: W.cfg_d64(num_q_heads=64, kv_dtype="fp8")),
+             ("gqa3_24_8", lambda: W.cfg_gqa(24)), ("gqa5_40_8", lambda: W.cfg_gqa(40)))
     for key, fn in cases:
         b = fn()
         db = DeviceBatch(b, dev_name)

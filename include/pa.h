@@ -230,9 +230,10 @@ PA_API pa_status pa_decode_write(const void *q, pa_dtype q_dtype, int32_t num_se
  * kernel on CUDA cores; the choice is this library's own.  Both compute the
  * result defined above, in fp32, within the decode tolerance of each other.
  *   PA_DECODE_KERNEL_AUTO (default): the tensor-core kernel where it applies
- *     (head_dim 128 with 4, 8 or 16 query heads per KV head, or head_dim 64
- *     with 4 or 8, any cache dtype: the Q.K^T and P.V of a KV head's query
- *     group run as MMAs),
+ *     (head_dim 128 with 1 to 16 query heads per KV head, or head_dim 64
+ *     with 1 to 8, any cache dtype, except one query head per KV head with
+ *     a 16-bit cache: the Q.K^T and P.V of a KV head's query group run as
+ *     MMAs, the group padded to 4, 8 or 16 rows),
  *     the CUDA-core kernel for every other shape;
  *   PA_DECODE_KERNEL_CUDA_CORES: the CUDA-core kernel for every shape.
  * Returns PA_ERR_INVALID_ARG for any other value (the setting is unchanged).

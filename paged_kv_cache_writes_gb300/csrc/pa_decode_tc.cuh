@@ -455,6 +455,9 @@ __device__ __forceinline__ void decode_tc_body(const DecodeTcParams &tp, const C
 
   const int hkv = p.num_kv_heads;
   const int hq = p.num_q_heads;
+  // query heads per KV head (1..G): a unit's rows gr..G-1 are padding, with q = 0 (finite
+  // scores and softmax), never read from or written to global memory
+  const int gr = hq / hkv;
 
   // Merge the split row of record t of the grid-wide merge list (its ready flag
   // acquired by lane 0): out = sum_p 2^(m_p - M) acc_p / sum_p 2^(m_p - M) l_p
@@ -466,7 +469,7 @@ __device__ __forceinline__ void decode_tc_body(const DecodeTcParams &tp, const C
            __shfl_sync(0xffffffffu, (uint32_t)word, 0);
     const int job_row = (int)(word >> 32), job_kvh = (int)((word >> 13) & 0x7ffffu), job_np = (int)(word & 0x1fffu);
     __syncwarp();   // lane 0's acquire of the record orders every lane's reads of the partials
-    const int64_t head0 = (int64_t)job_row * hq + (int64_t)job_kvh * G;
+    const int64_t head0 = (int64_t)job_row * hq + (int64_t)job_kvh * gr;
     float m[G], l[G];
     float4 acc[G];
 #pragma unroll
@@ -484,7 +487,7 @@ __device__ __forceinline__ void decode_tc_body(const DecodeTcParams &tp, const C
 #pragma unroll
         for (int h = 0; h < G; ++h) {
           const int q = min(q0 + k, job_np - 1);   // a lone last partition is read twice, merged once
-          const int64_t e = (head0 + h) * p.max_partitions + q;
+          const int64_t e = (head0 + min(h, gr - 1)) * p.max_partitions + q;   // padding rows: a real head, unused
           ml[k][h] = __ldcg(&p.ws_ml[e]);
           a[k][h] = 4 * lane < kD ? __ldcg(reinterpret_cast<const float4 *>(p.ws_acc + e * kD) + lane)
                                   : make_float4(0.f, 0.f, 0.f, 0.f);
@@ -508,7 +511,7 @@ __device__ __forceinline__ void decode_tc_body(const DecodeTcParams &tp, const C
       const float om = p.v_hs ? p.out_mult * __ldg(p.v_hs + job_kvh) : p.out_mult;
       const float inv = l[h] > 0.f ? om / l[h] : 0.f;
       const int64_t o0 = (head0 + h) * kD + 4 * lane;
-      if (4 * lane >= kD) continue;   // head_dim 64: lanes 0..15
+      if (4 * lane >= kD || h >= gr) continue;   // head_dim 64: lanes 0..15; padding rows
       store_out<QT>(p.out, o0, p.out_f32 != 0, acc[h].x * inv);
       store_out<QT>(p.out, o0 + 1, p.out_f32 != 0, acc[h].y * inv);
       store_out<QT>(p.out, o0 + 2, p.out_f32 != 0, acc[h].z * inv);
@@ -710,7 +713,7 @@ __device__ __forceinline__ void decode_tc_body(const DecodeTcParams &tp, const C
         }
         tc_fence_before();
         mbar_arrive(&o_free[bp]);
-        const int64_t head0 = (int64_t)prev.row * hq + (int64_t)prev.kvh * G;
+        const int64_t head0 = (int64_t)prev.row * hq + (int64_t)prev.kvh * gr;
         const int d = tid;            // with head_dim 64, lanes 64..127 repeat 0..63: not stored
         // the two column halves of O^T: bf16 p = hi + lo; fp8 256 p = hi + lo / 16
         auto o_val = [&](int h) {
@@ -722,13 +725,13 @@ __device__ __forceinline__ void decode_tc_body(const DecodeTcParams &tp, const C
             const float val = o_val(h);
             const float om = p.v_hs ? p.out_mult * __ldg(p.v_hs + prev.kvh) : p.out_mult;
             const float inv = l_prev[h] > 0.f ? om / l_prev[h] : 0.f;
-            if (d < kD) store_out<QT>(p.out, (head0 + h) * kD + d, p.out_f32 != 0, val * inv);
+            if (d < kD && h < gr) store_out<QT>(p.out, (head0 + h) * kD + d, p.out_f32 != 0, val * inv);
           }
         } else {
 #pragma unroll
           for (int h = 0; h < G; ++h)
-            if (d < kD) p.ws_acc[((head0 + h) * p.max_partitions + prev.part) * kD + d] = o_val(h);
-          if (tid < G) {
+            if (d < kD && h < gr) p.ws_acc[((head0 + h) * p.max_partitions + prev.part) * kD + d] = o_val(h);
+          if (tid < gr) {
             float mv = m_prev[0], lv = l_prev[0];
 #pragma unroll
             for (int h = 1; h < G; ++h)
@@ -798,11 +801,12 @@ __device__ __forceinline__ void decode_tc_body(const DecodeTcParams &tp, const C
 #pragma unroll
       for (int e = lane; e < G * kRowChunks; e += 32) {
         const int h = e / kRowChunks, c16 = e % kRowChunks;
+        const bool real = h < gr;   // padding rows are zero-filled (nothing read)
         const char *src = static_cast<const char *>(p.q) +
-                          (((int64_t)cur.row * hq + (int64_t)cur.kvh * G + h) * kD) * 2 + c16 * 16;
+                          (real ? (((int64_t)cur.row * hq + (int64_t)cur.kvh * gr + h) * kD) * 2 + c16 * 16 : 0);
         cp_async16(smem + GE::kOffQ + b * GE::kQBytes + (c16 >> 3) * (kNS * 128) + h * 128 +
                        (((c16 & 7) ^ (h & 7)) << 4),
-                   src, 16u);
+                   src, real ? 16u : 0u);
       }
       cp_async_arrive_noinc(&q_full[b]);
     };
@@ -942,10 +946,11 @@ __device__ __forceinline__ void decode_tc_body(const DecodeTcParams &tp, const C
           };
           uint4 qw[kQIt];
           float amax = 0.f;
-          const char *q0 = static_cast<const char *>(p.q) + ((int64_t)rk * hq + (int64_t)kvk * G) * kD * 2;
+          const char *q0 = static_cast<const char *>(p.q) + ((int64_t)rk * hq + (int64_t)kvk * gr) * kD * 2;
 #pragma unroll
           for (int i = 0; i < kQIt; ++i) {
-            qw[i] = vk ? ld_nc16(q0 + (lane + 32 * i) * 16) : make_uint4(0, 0, 0, 0);
+            const bool real = (lane + 32 * i) / kCPH < gr;   // padding rows: zeros
+            qw[i] = vk && real ? ld_nc16(q0 + (lane + 32 * i) * 16) : make_uint4(0, 0, 0, 0);
             amax = fmaxf(amax, absmax8(qw[i], QT{}));
           }
 #pragma unroll
@@ -1049,7 +1054,7 @@ __device__ __forceinline__ void decode_tc_body(const DecodeTcParams &tp, const C
               int old;
               asm volatile("atom.release.gpu.global.add.s32 %0, [%1], 1;"
                            : "=r"(old)
-                           : "l"(p.ws_count + (int64_t)r.x * hq + (int64_t)r.y * G)
+                           : "l"(p.ws_count + (int64_t)r.x * hq + (int64_t)r.y * gr)
                            : "memory");
               if (old == r.z - 1) {
                 asm volatile("fence.acq_rel.gpu;" ::: "memory");
@@ -1382,20 +1387,18 @@ cudaError_t launch_decode_tc_one(const DecodeTcParams &p, const PoolMaps &m, cud
 // (128-byte swizzle).
 template <typename KV, typename QT>
 cudaError_t launch_decode_tc(const DecodeTcParams &p, int gqa, int head_dim, const PoolMaps &m, cudaStream_t s) {
+  // a group of gqa query heads runs in the kernel for the next of 4, 8 or 16 rows
+  if (gqa < 1) return cudaErrorInvalidValue;
   if (head_dim == 64) {
-    switch (gqa) {
-      case 4: return launch_decode_tc_one<KV, QT, 4, 64>(p, m, s);
-      case 8: return launch_decode_tc_one<KV, QT, 8, 64>(p, m, s);
-      default: return cudaErrorInvalidValue;
-    }
+    if (gqa <= 4) return launch_decode_tc_one<KV, QT, 4, 64>(p, m, s);
+    if (gqa <= 8) return launch_decode_tc_one<KV, QT, 8, 64>(p, m, s);
+    return cudaErrorInvalidValue;
   }
   if (head_dim != 128) return cudaErrorInvalidValue;
-  switch (gqa) {
-    case 4: return launch_decode_tc_one<KV, QT, 4, 128>(p, m, s);
-    case 8: return launch_decode_tc_one<KV, QT, 8, 128>(p, m, s);
-    case 16: return launch_decode_tc_one<KV, QT, 16, 128>(p, m, s);
-    default: return cudaErrorInvalidValue;
-  }
+  if (gqa <= 4) return launch_decode_tc_one<KV, QT, 4, 128>(p, m, s);
+  if (gqa <= 8) return launch_decode_tc_one<KV, QT, 8, 128>(p, m, s);
+  if (gqa <= 16) return launch_decode_tc_one<KV, QT, 16, 128>(p, m, s);
+  return cudaErrorInvalidValue;
 }
 
 }  // namespace pa

@@ -1,9 +1,10 @@
 """GPU parity of paged decode against the fp64 oracle, element by element.
 
 Two kernels serve pa_decode: the tensor-core one (chosen by default for
-head_dim 128 with 4, 8 or 16 query heads per KV head, and for head_dim 64
-with 4 or 8) and the CUDA-core one (every other shape, or
-every shape once selected with pa_set_decode_kernel); both are checked here.
+head_dim 128 with 1..16 query heads per KV head and head_dim 64 with 1..8,
+a group running padded to 4, 8 or 16 rows; one head per KV head only with
+an fp8 cache) and the CUDA-core one (every other shape, or every shape once
+selected with pa_set_decode_kernel); both are checked here.
 
 Tolerance (max abs error): 2e-3 for f16/bf16 caches, 2e-2 for an fp8-e4m3
 cache (the oracle dequantises the same codes with the same scales).  Shapes
@@ -38,7 +39,8 @@ def test_tiny_config():
     _check(W.cfg_tiny())
 
 
-@pytest.mark.parametrize("hq,hkv", [(4, 4), (8, 2), (16, 2), (32, 8), (64, 8), (12, 4), (6, 2), (5, 5)])
+@pytest.mark.parametrize("hq,hkv", [(4, 4), (8, 2), (16, 2), (32, 8), (64, 8), (12, 4), (6, 2), (5, 5), (40, 8),
+                                    (96, 8), (16, 8)])
 @pytest.mark.parametrize("d,bs", [(128, 16), (64, 32), (128, 32), (64, 16)])
 def test_shapes_bf16(hq, hkv, d, bs):
     _check(W.decode_batch("s", EDGE_LENS, hq, hkv, d, bs, "bf16", seed=hq * 7 + d + bs, partition_size=512))
@@ -46,7 +48,7 @@ def test_shapes_bf16(hq, hkv, d, bs):
 
 @pytest.mark.parametrize("kv,src", [("f16", "f16"), ("fp8", "bf16"), ("fp8", "f16")])
 @pytest.mark.parametrize("hq,hkv,d,bs", [(32, 8, 128, 16), (64, 8, 128, 32), (8, 8, 64, 16), (16, 4, 64, 32),
-                                         (64, 8, 64, 16)])
+                                         (64, 8, 64, 16), (24, 8, 128, 16), (40, 8, 128, 32), (8, 8, 128, 16)])
 def test_shapes_other_dtypes(kv, src, hq, hkv, d, bs):
     _check(W.decode_batch("s", EDGE_LENS, hq, hkv, d, bs, src, kv_dtype=kv, seed=hq + d + bs, partition_size=512))
 
@@ -178,6 +180,12 @@ def test_head_dim_64_fp8_batch_both_kernels(q, hq, hkv):
     with pa.decode_kernel("cuda_cores"):
         cc, _ = _check(b)
     assert (tc_out - cc.out).abs().max().item() <= 2 * TOL["fp8"]
+
+
+@pytest.mark.parametrize("hq", [24, 40])
+def test_gqa_layer_full(hq):
+    # the benchmark's decode layers with 3 and 5 query heads per KV head: every row and element
+    _check(W.cfg_gqa(hq))
 
 
 @pytest.mark.parametrize("hq", [32, 64])

@@ -479,6 +479,15 @@ def cfg_d64(seed: int = 6, batch: int = 256, num_q_heads: int = 32, kv_dtype: st
                         partition_size=512)
 
 
+def cfg_gqa(num_q_heads: int, seed: int = 7, batch: int = 128) -> PagedBatch:
+    """Decode layer with num_q_heads/8 heads (groups such as 3 or 5 query heads
+    per KV head), head_dim 128, block 16, bf16, lengths uniform 512..4096,
+    split-KV 512, 40k-block pool."""
+    lens = np.random.default_rng(seed + 100).integers(512, 4097, size=batch)
+    return decode_batch(f"GQA decode layer, {num_q_heads}/8 heads", lens, num_q_heads, 8, 128, 16, "bf16", seed=seed,
+                        num_blocks=40000, partition_size=512)
+
+
 def cfg_shared_prefix(seed: int = 3, num_prompts: int = 32) -> PagedBatch:
     return shared_prefix_batch(num_prompts=num_prompts, seed=seed)
 
