@@ -344,7 +344,7 @@ __device__ __forceinline__ int32_t query_scale_bits(float amax) {
 // The decode CTA, for decode_tc_kernel and for the decode CTAs of the mixed
 // kernel (pa_mixed_tc.cuh).  Warps past the eight roles (a wider mixed block)
 // only take part in the two CTA-wide barriers.
-template <typename KV, typename QT, int G, int D = 128, int NL = 1, bool kSepMerge = false>
+template <typename KV, typename QT, int G, int D = 128, int NL = 1, bool kSepMerge = false, bool kPadRows = false>
 __device__ __forceinline__ void decode_tc_body(const DecodeTcParams &tp, const CUtensorMap *tmap_k,
                                                const CUtensorMap *tmap_v) {
   using namespace tc;
@@ -455,9 +455,9 @@ __device__ __forceinline__ void decode_tc_body(const DecodeTcParams &tp, const C
 
   const int hkv = p.num_kv_heads;
   const int hq = p.num_q_heads;
-  // query heads per KV head (1..G): a unit's rows gr..G-1 are padding, with q = 0 (finite
-  // scores and softmax), never read from or written to global memory
-  const int gr = hq / hkv;
+  // query heads per KV head: G, or with kPadRows 1..G, a unit's rows gr..G-1 then being
+  // padding, with q = 0 (finite scores and softmax), never read from or written to global memory
+  const int gr = kPadRows ? hq / hkv : G;
 
   // Merge the split row of record t of the grid-wide merge list (its ready flag
   // acquired by lane 0): out = sum_p 2^(m_p - M) acc_p / sum_p 2^(m_p - M) l_p
@@ -801,7 +801,7 @@ __device__ __forceinline__ void decode_tc_body(const DecodeTcParams &tp, const C
 #pragma unroll
       for (int e = lane; e < G * kRowChunks; e += 32) {
         const int h = e / kRowChunks, c16 = e % kRowChunks;
-        const bool real = h < gr;   // padding rows are zero-filled (nothing read)
+        const bool real = !kPadRows || h < gr;   // padding rows are zero-filled (nothing read)
         const char *src = static_cast<const char *>(p.q) +
                           (real ? (((int64_t)cur.row * hq + (int64_t)cur.kvh * gr + h) * kD) * 2 + c16 * 16 : 0);
         cp_async16(smem + GE::kOffQ + b * GE::kQBytes + (c16 >> 3) * (kNS * 128) + h * 128 +
@@ -949,7 +949,7 @@ __device__ __forceinline__ void decode_tc_body(const DecodeTcParams &tp, const C
           const char *q0 = static_cast<const char *>(p.q) + ((int64_t)rk * hq + (int64_t)kvk * gr) * kD * 2;
 #pragma unroll
           for (int i = 0; i < kQIt; ++i) {
-            const bool real = (lane + 32 * i) / kCPH < gr;   // padding rows: zeros
+            const bool real = !kPadRows || (lane + 32 * i) / kCPH < gr;   // padding rows: zeros
             qw[i] = vk && real ? ld_nc16(q0 + (lane + 32 * i) * 16) : make_uint4(0, 0, 0, 0);
             amax = fmaxf(amax, absmax8(qw[i], QT{}));
           }
@@ -1272,11 +1272,11 @@ __device__ __forceinline__ void decode_tc_body(const DecodeTcParams &tp, const C
   }
 }
 
-template <typename KV, typename QT, int G, int D>
+template <typename KV, typename QT, int G, int D, bool kPadRows>
 __global__ void __launch_bounds__(dtc::Roles::threads_for(dtc::Roles::loaders(G), dtc::Roles::sep_merge(G)), 1)
     decode_tc_kernel(const DecodeTcParams tp, const __grid_constant__ CUtensorMap tmap_k,
                      const __grid_constant__ CUtensorMap tmap_v) {
-  decode_tc_body<KV, QT, G, D, dtc::Roles::loaders(G), dtc::Roles::sep_merge(G)>(tp, &tmap_k, &tmap_v);
+  decode_tc_body<KV, QT, G, D, dtc::Roles::loaders(G), dtc::Roles::sep_merge(G), kPadRows>(tp, &tmap_k, &tmap_v);
 }
 
 // One CTA: count the split rows' merges and clear the merge list, and list
@@ -1357,14 +1357,14 @@ cudaError_t launch_decode_tc_plan(const DecodeParams &d, DecodeMergeJob *jobs, c
   return cudaLaunchKernelEx(&cfg, decode_tc_plan_kernel<0>, d, jobs);
 }
 
-template <typename KV, typename QT, int G, int D>
+template <typename KV, typename QT, int G, int D, bool kPadRows>
 cudaError_t launch_decode_tc_one(const DecodeTcParams &p, const PoolMaps &m, cudaStream_t s) {
   constexpr bool kSplit = std::is_same<QT, __nv_bfloat16>::value && !std::is_same<KV, uint8_t>::value;
   constexpr int smem =
       dtc::TcGeo<G, kSplit, std::is_same<KV, uint8_t>::value, dtc::QTerms<KV, QT>::value, D>::kSmemBytes;
   cudaError_t e = launch_decode_tc_plan(p.d, p.jobs, s);
   if (e != cudaSuccess) return e;
-  if ((e = ensure_smem_limit<decode_tc_kernel<KV, QT, G, D>>(smem)) != cudaSuccess) return e;
+  if ((e = ensure_smem_limit<decode_tc_kernel<KV, QT, G, D, kPadRows>>(smem)) != cudaSuccess) return e;
   int sms = 0;
   if ((e = current_sm_count(&sms)) != cudaSuccess) return e;
   // programmatic dependent launch: the decode grid's set-up overlaps the plan kernel
@@ -1378,26 +1378,29 @@ cudaError_t launch_decode_tc_one(const DecodeTcParams &p, const PoolMaps &m, cud
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, decode_tc_kernel<KV, QT, G, D>, p, m.k, m.v);
+  return cudaLaunchKernelEx(&cfg, decode_tc_kernel<KV, QT, G, D, kPadRows>, p, m.k, m.v);
 }
 
 // m: tensor maps over the pools, one box per cache block of one KV head: 16-bit
 // caches viewed as [atoms of 8 rows][2 panels][8 rows][64] (head_dim 128) or
 // [atoms of 8 rows][8 rows][64] (head_dim 64), fp8 caches as [rows][128]
 // (128-byte swizzle).
-template <typename KV, typename QT>
+// kPadRows false: gqa is exactly 4, 8 or 16 (head_dim 64: 4 or 8), every head index compile-time;
+// true: any other group of 1..16 (1..8), run in the kernel for the next of those sizes.
+template <typename KV, typename QT, bool kPadRows>
 cudaError_t launch_decode_tc(const DecodeTcParams &p, int gqa, int head_dim, const PoolMaps &m, cudaStream_t s) {
   // a group of gqa query heads runs in the kernel for the next of 4, 8 or 16 rows
   if (gqa < 1) return cudaErrorInvalidValue;
+  if (decode_tc_exact_group(head_dim, gqa) == kPadRows) return cudaErrorInvalidValue;
   if (head_dim == 64) {
-    if (gqa <= 4) return launch_decode_tc_one<KV, QT, 4, 64>(p, m, s);
-    if (gqa <= 8) return launch_decode_tc_one<KV, QT, 8, 64>(p, m, s);
+    if (gqa <= 4) return launch_decode_tc_one<KV, QT, 4, 64, kPadRows>(p, m, s);
+    if (gqa <= 8) return launch_decode_tc_one<KV, QT, 8, 64, kPadRows>(p, m, s);
     return cudaErrorInvalidValue;
   }
   if (head_dim != 128) return cudaErrorInvalidValue;
-  if (gqa <= 4) return launch_decode_tc_one<KV, QT, 4, 128>(p, m, s);
-  if (gqa <= 8) return launch_decode_tc_one<KV, QT, 8, 128>(p, m, s);
-  if (gqa <= 16) return launch_decode_tc_one<KV, QT, 16, 128>(p, m, s);
+  if (gqa <= 4) return launch_decode_tc_one<KV, QT, 4, 128, kPadRows>(p, m, s);
+  if (gqa <= 8) return launch_decode_tc_one<KV, QT, 8, 128, kPadRows>(p, m, s);
+  if (gqa <= 16) return launch_decode_tc_one<KV, QT, 16, 128, kPadRows>(p, m, s);
   return cudaErrorInvalidValue;
 }
 

@@ -4,6 +4,7 @@
 namespace pa {
 cudaError_t launch_decode_tc_f16(const DecodeTcParams &p, int gqa, int head_dim, const PoolMaps &m,
                                  cudaStream_t s) {
-  return launch_decode_tc<__half, __half>(p, gqa, head_dim, m, s);
+  if (!decode_tc_exact_group(head_dim, gqa)) return launch_decode_tc_pad_f16(p, gqa, head_dim, m, s);
+  return launch_decode_tc<__half, __half, false>(p, gqa, head_dim, m, s);
 }
 }  // namespace pa

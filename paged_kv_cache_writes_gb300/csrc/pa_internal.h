@@ -133,11 +133,24 @@ cudaError_t launch_decode_fp8_f16q(const DecodeParams &p, int hpc, const PoolMap
 // gqa in 1..8 (a group runs padded to 4, 8 or 16 query rows); one query head per KV
 // head with a 16-bit cache stays on the CUDA-core kernel, measured faster there
 // (128 sequences: 0.191 against 0.198 ms with head_dim 128, 0.115 against 0.137 with 64).
+// A group the tensor-core decode runs without padding rows.
+constexpr bool decode_tc_exact_group(int head_dim, int gqa) {
+  return gqa == 4 || gqa == 8 || (gqa == 16 && head_dim == 128);
+}
 constexpr bool decode_tc_supported(int head_dim, int gqa, pa_dtype kv) {
   return ((head_dim == 128 && gqa >= 1 && gqa <= 16) || (head_dim == 64 && gqa >= 1 && gqa <= 8)) &&
          (gqa >= 2 || kv == PA_FP8_E4M3);
 }
+// exact groups here; the other groups by the _pad launchers (their own translation units)
 cudaError_t launch_decode_tc_bf16(const DecodeTcParams &p, int gqa, int head_dim, const PoolMaps &m, cudaStream_t s);
+cudaError_t launch_decode_tc_pad_bf16(const DecodeTcParams &p, int gqa, int head_dim, const PoolMaps &m,
+                                      cudaStream_t s);
+cudaError_t launch_decode_tc_pad_f16(const DecodeTcParams &p, int gqa, int head_dim, const PoolMaps &m,
+                                     cudaStream_t s);
+cudaError_t launch_decode_tc_pad_fp8_bf16q(const DecodeTcParams &p, int gqa, int head_dim, const PoolMaps &m,
+                                           cudaStream_t s);
+cudaError_t launch_decode_tc_pad_fp8_f16q(const DecodeTcParams &p, int gqa, int head_dim, const PoolMaps &m,
+                                          cudaStream_t s);
 cudaError_t launch_decode_tc_f16(const DecodeTcParams &p, int gqa, int head_dim, const PoolMaps &m, cudaStream_t s);
 cudaError_t launch_decode_tc_fp8_bf16q(const DecodeTcParams &p, int gqa, int head_dim, const PoolMaps &m,
                                        cudaStream_t s);
