@@ -53,6 +53,13 @@ def test_shapes_other_dtypes(kv, src, hq, hkv, d, bs):
     _check(W.decode_batch("s", EDGE_LENS, hq, hkv, d, bs, src, kv_dtype=kv, seed=hq + d + bs, partition_size=512))
 
 
+@pytest.mark.parametrize("kv,src", [("f16", "f16"), ("fp8", "bf16"), ("fp8", "f16")])
+@pytest.mark.parametrize("hq,hkv,d", [(24, 2, 128), (13, 1, 128), (10, 2, 64), (14, 2, 64)])
+def test_padded_groups_other_dtypes(kv, src, hq, hkv, d):
+    # groups of 12, 13, 5 and 7 query heads per KV head: run padded to 16 or 8 rows
+    _check(W.decode_batch("pad", EDGE_LENS, hq, hkv, d, 16, src, kv_dtype=kv, seed=hq + hkv + d, partition_size=512))
+
+
 @pytest.mark.parametrize("kv,src", [("bf16", "bf16"), ("f16", "f16"), ("fp8", "bf16"), ("fp8", "f16")])
 @pytest.mark.parametrize("hq,hkv,bs", [(32, 2, 16), (64, 4, 32), (16, 1, 16)])
 def test_sixteen_heads_per_kv_head(kv, src, hq, hkv, bs):
