@@ -1,7 +1,7 @@
 // pa_decode_tc.cuh -- paged decode for grouped-query attention on the
 // 5th-generation tensor cores (tcgen05.mma, accumulators in tensor memory),
-// G = 4, 8 or 16 query heads per KV head with head_dim 128 (any cache dtype),
-// G = 4 or 8 with head_dim 64 (16-bit caches).
+// G = 4, 8 or 16 query rows per KV head (other groups padded), head_dim 128
+// with G up to 16 or head_dim 64 with G up to 8, any cache dtype.
 //
 // What it computes: the same as the CUDA-core decode (pa_decode.cuh).  For
 // each sequence and query head h,
